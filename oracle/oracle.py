@@ -1,0 +1,224 @@
+"""ctypes wrapper around the C oracle (``qgemv_oracle.c``) plus an independent
+numpy dequantizer used as its brute-force pin.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  Parity for the choices
+of byte layout, rounding and Q8_1 storage precision is unpinned by the pages:
+they name the formats without defining them; the readings are listed in the
+C file's header.
+
+Shapes and byte layouts:
+  canonical Q4_0 weights: uint8 [N, K/32, 18]   = {fp16 d, qs[16]}
+  canonical Q6_K weights: uint8 [N, K/256, 210] = {ql[128], qh[64], sc[16], fp16 d}
+  Q8_1 activations:       uint8 [M, K/32, 36]   = {fp16 d, fp16 s, int8 q[32]}
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qgemv_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_qgemv.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with the system C compiler; returns the .so path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["cc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            L = ctypes.c_int64
+            lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+            lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_f64.restype = ctypes.c_double
+            lib.oracle_quantize_q8_1.argtypes = [P, L, I, I, P]
+            for name in ("oracle_dequant_q4_0", "oracle_dequant_q6_k", "oracle_dequant_q8_1"):
+                getattr(lib, name).argtypes = [P, I, I, P]
+            for name in ("oracle_block_dots_q4_0", "oracle_block_dots_q6_k"):
+                getattr(lib, name).argtypes = [P, P, I, I, I, P]
+            for name in ("oracle_qgemv_q4_0", "oracle_qgemv_q6_k"):
+                getattr(lib, name).argtypes = [P, P, I, I, I, P, P, I]
+            lib.oracle_top1_f64.argtypes = [P, L, I, I, P]
+            lib.oracle_top1_f32.argtypes = [P, L, I, I, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+# --------------------------------------------------------------------------
+# scalar helpers
+# --------------------------------------------------------------------------
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    """binary16 bits of each fp32 value (IEEE round to nearest even)."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float32).ravel()
+    out = np.array([lib.oracle_f32_to_f16(float(v)) for v in a], dtype=np.uint16)
+    return out.reshape(np.shape(x))
+
+
+def f16_bits_to_f64(h) -> np.ndarray:
+    lib = _load()
+    a = np.asarray(h, dtype=np.uint16).ravel()
+    out = np.array([lib.oracle_f16_to_f64(int(v)) for v in a], dtype=np.float64)
+    return out.reshape(np.shape(h))
+
+
+# --------------------------------------------------------------------------
+# the path's steps
+# --------------------------------------------------------------------------
+
+def quantize_q8_1(x: np.ndarray, K: int | None = None) -> np.ndarray:
+    """fp32 x [M, >=K] -> Q8_1 uint8 [M, K/32, 36]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    M, ldx = x.shape
+    K = ldx if K is None else K
+    assert K % 32 == 0 and K <= ldx
+    out = np.zeros((M, K // 32, 36), dtype=np.uint8)
+    _load().oracle_quantize_q8_1(_ptr(x), ldx, M, K, _ptr(out))
+    return out
+
+
+def qgemv_q4_0(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
+    """canonical Q4_0 w [N, K/32, 18], Q8_1 xq [M, K/32, 36] -> (y, S) fp64 [M, N].
+
+    y[m, n] = sum_b d_w * d_a * I_b (I_b exact integer block dots), and
+    S[m, n] = sum_b |d_w * d_a * I_b| (the scale of the fp32 rounding error).
+    """
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    N, nb = w.shape[0], w.shape[1]
+    M = xq.shape[0]
+    assert xq.shape[1] == nb and w.shape[2] == 18
+    y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_qgemv_q4_0(_ptr(w), _ptr(xq), M, nb * 32, N, _ptr(y), _ptr(S),
+                              nthreads or default_threads())
+    return y, S
+
+
+def qgemv_q6_k(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
+    """canonical Q6_K w [N, K/256, 210], Q8_1 xq [M, K/32, 36] -> (y, S) fp64 [M, N]."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    N, ns = w.shape[0], w.shape[1]
+    M = xq.shape[0]
+    assert xq.shape[1] == ns * 8 and w.shape[2] == 210
+    y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_qgemv_q6_k(_ptr(w), _ptr(xq), M, ns * 256, N, _ptr(y), _ptr(S),
+                              nthreads or default_threads())
+    return y, S
+
+
+def block_dots_q4_0(w: np.ndarray, xq: np.ndarray) -> np.ndarray:
+    """Exact integer block dots I[m, n, b] = sum_i (q_w - 8) * q_a."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    N, nb = w.shape[0], w.shape[1]
+    M = xq.shape[0]
+    out = np.zeros((M, N, nb), dtype=np.int32)
+    _load().oracle_block_dots_q4_0(_ptr(w), _ptr(xq), M, nb * 32, N, _ptr(out))
+    return out
+
+
+def block_dots_q6_k(w: np.ndarray, xq: np.ndarray) -> np.ndarray:
+    """Exact integer block dots J[m, n, b] = sum_subblocks sc * sum_i (q - 32) * q_a."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    N, ns = w.shape[0], w.shape[1]
+    M = xq.shape[0]
+    out = np.zeros((M, N, ns * 8), dtype=np.int32)
+    _load().oracle_block_dots_q6_k(_ptr(w), _ptr(xq), M, ns * 256, N, _ptr(out))
+    return out
+
+
+def top1(y: np.ndarray) -> np.ndarray:
+    """Lowest index attaining each row's maximum (NaN never wins; all-NaN -> 0)."""
+    y = np.ascontiguousarray(y)
+    M, N = y.shape
+    ids = np.zeros(M, dtype=np.int32)
+    if y.dtype == np.float64:
+        _load().oracle_top1_f64(_ptr(y), N, M, N, _ptr(ids))
+    elif y.dtype == np.float32:
+        _load().oracle_top1_f32(_ptr(y), N, M, N, _ptr(ids))
+    else:
+        raise TypeError(y.dtype)
+    return ids
+
+
+def lmhead_q6_k_top1(w: np.ndarray, x: np.ndarray, nthreads: int | None = None):
+    """Fused LM-head top-1, step by step: quantize the rows of x to Q8_1, project
+    them through the Q6_K weight, take the lowest-ID argmax of each row.
+    Returns (ids, y, S) so that callers can judge near-ties."""
+    xq = quantize_q8_1(x)
+    y, S = qgemv_q6_k(w, xq, nthreads)
+    return top1(y), y, S
+
+
+# --------------------------------------------------------------------------
+# independent numpy dequantization (the brute-force pin for the C decoder)
+# --------------------------------------------------------------------------
+
+def _f16(bits: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(bits).view(np.float16).astype(np.float64)
+
+
+def dequant_q4_0_np(w: np.ndarray) -> np.ndarray:
+    """[N, K/32, 18] -> fp64 [N, K]: d * (q - 8), low nibbles first."""
+    N, nb, _ = w.shape
+    d = _f16(w[:, :, 0:2].copy()).reshape(N, nb, 1)
+    qs = w[:, :, 2:18].astype(np.int64)
+    q = np.concatenate([qs & 0x0F, qs >> 4], axis=2)
+    return (d * (q - 8)).reshape(N, nb * 32)
+
+
+def dequant_q6_k_np(w: np.ndarray) -> np.ndarray:
+    """[N, K/256, 210] -> fp64 [N, K]: d * sc * (q - 32)."""
+    N, ns, _ = w.shape
+    ql = w[:, :, 0:128].astype(np.int64)
+    qh = w[:, :, 128:192].astype(np.int64)
+    sc = w[:, :, 192:208].view(np.int8).astype(np.float64)
+    d = _f16(w[:, :, 208:210].copy()).reshape(N, ns, 1)
+    lo = np.stack([ql & 0x0F, ql >> 4], axis=3).reshape(N, ns, 256)
+    hi = np.stack([(qh >> s) & 3 for s in (0, 2, 4, 6)], axis=3).reshape(N, ns, 256)
+    q = lo | (hi << 4)
+    scale = np.repeat(sc, 16, axis=2)
+    return (d * scale * (q - 32)).reshape(N, ns * 256)
+
+
+def dequant_q8_1_np(xq: np.ndarray) -> np.ndarray:
+    """[M, K/32, 36] -> fp64 [M, K]: d * q (the stored fp16 d)."""
+    M, nb, _ = xq.shape
+    d = _f16(xq[:, :, 0:2].copy()).reshape(M, nb, 1)
+    q = xq[:, :, 4:36].view(np.int8).astype(np.float64)
+    return (d * q).reshape(M, nb * 32)

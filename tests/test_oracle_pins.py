@@ -1,0 +1,298 @@
+"""Pins for the CPU oracle: each test checks it against something other than
+itself (IEEE binary16 via numpy, hand-worked blocks, an independent numpy
+dequantizer, algebraic invariants, the pages' byte count, planted ties)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from block_quantized_gemv_quantize_gb300 import synth
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "single_blocks.json")))
+
+
+def _q4_0_block(d: float, codes) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.uint8)
+    blk = np.zeros(18, dtype=np.uint8)
+    blk[0:2] = np.array([d], dtype=np.float16).view(np.uint8)
+    blk[2:18] = (codes[:16] & 0x0F) | ((codes[16:] & 0x0F) << 4)
+    return blk
+
+
+def _q6_k_superblock(d: float, sc, codes) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.int64)
+    sb = np.zeros(210, dtype=np.uint8)
+    for i in range(256):
+        sb[i >> 1] |= (codes[i] & 0x0F) << (4 * (i & 1))
+        sb[128 + (i >> 2)] |= ((codes[i] >> 4) & 3) << (2 * (i & 3))
+    sb[192:208] = np.asarray(sc, dtype=np.int8).view(np.uint8)
+    sb[208:210] = np.array([d], dtype=np.float16).view(np.uint8)
+    return sb
+
+
+# ---------------------------------------------------------------- binary16
+
+def test_f32_to_f16_matches_ieee_rne():
+    g = np.random.default_rng(1)
+    vals = np.concatenate([
+        g.standard_normal(3000).astype(np.float32) * np.float32(10.0) ** g.integers(-9, 6, 3000).astype(np.float32),
+        np.array([0.0, -0.0, 65504.0, 65519.0, 65520.0, 1e6, -1e6, 2.0 ** -14, 2.0 ** -24, 2.0 ** -25,
+                  3 * 2.0 ** -26, 2.0 ** -26, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 6.1e-5, 5.96e-8,
+                  np.inf, -np.inf], dtype=np.float32),
+    ])
+    mine = oracle.f32_to_f16_bits(vals)
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    assert np.array_equal(mine, ref)
+
+
+def test_f16_decode_exact():
+    bits = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
+    bits = bits[(bits & 0x7C00) != 0x7C00]  # finite only
+    mine = oracle.f16_bits_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    assert np.array_equal(mine, ref)
+
+
+# ---------------------------------------------------------------- Q8_1
+
+def test_q8_1_hand_block():
+    g = GOLDEN["q8_1_all_ones"]
+    xq = oracle.quantize_q8_1(np.ones((1, 32), dtype=np.float32))
+    d16 = int(xq[0, 0, 0]) | (int(xq[0, 0, 1]) << 8)
+    s16 = int(xq[0, 0, 2]) | (int(xq[0, 0, 3]) << 8)
+    assert d16 == int(g["d16_bits"], 16)
+    assert s16 == int(g["s16_bits"], 16)
+    assert np.all(xq[0, 0, 4:].view(np.int8) == g["q"])
+
+
+def test_q8_1_rounds_half_away_from_zero():
+    # amax = 127 makes d = 1 exactly, so x/d is x itself: the ties are exact.
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, 0] = 127.0
+    x[0, 1:7] = [2.5, -2.5, 0.5, -0.5, 3.5, 126.5]
+    xq = oracle.quantize_q8_1(x)
+    q = xq[0, 0, 4:].view(np.int8)
+    assert q[:7].tolist() == [127, 3, -3, 1, -1, 4, 127]
+
+
+def test_q8_1_divides_by_fp32_scale_not_fp16():
+    # amax = 1: fp32 d = 1/127, its fp16 rounding is 1032/131072.  x = 0.05118
+    # gives 6 with the fp32 d and 7 with the fp16 one.
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, 0] = 1.0
+    x[0, 1] = np.float32(0.05118)
+    q = oracle.quantize_q8_1(x)[0, 0, 4:].view(np.int8)
+    d32 = np.float32(1.0) / np.float32(127.0)
+    assert q[1] == int(np.floor(x[0, 1] / d32 + np.float32(0.5)))
+    assert q[1] == 6
+
+
+def test_q8_1_properties():
+    x = synth.activations(4, 512, seed=7, outlier_frac=0.02)
+    xq = oracle.quantize_q8_1(x)
+    q = xq[:, :, 4:].view(np.int8).astype(np.int64)
+    xb = x.reshape(4, 16, 32)
+    amax = np.abs(xb).max(axis=2)
+    # the largest |x| of each block maps to +-127, and |q| <= 127
+    arg = np.abs(xb).argmax(axis=2)
+    assert np.all(np.abs(np.take_along_axis(q, arg[..., None], 2)) == 127)
+    assert np.all(np.abs(q) <= 127)
+    # q = round(x / d) with the fp32 d = amax/127: |x/d - q| <= 1/2
+    d32 = (amax / np.float32(127.0)).astype(np.float32)
+    r = xb / d32[..., None]
+    assert np.all(np.abs(r - q) <= 0.5)
+    # stored fp16 d is the RNE rounding of d; s is fp16(d * sum q)
+    d16 = xq[:, :, 0:2].copy().view(np.float16)[..., 0]
+    assert np.array_equal(d16, d32.astype(np.float16))
+    s16 = xq[:, :, 2:4].copy().view(np.float16)[..., 0]
+    assert np.array_equal(s16, (d32 * q.sum(axis=2).astype(np.float32)).astype(np.float16))
+    # sign symmetry
+    xq_neg = oracle.quantize_q8_1(-x)
+    assert np.array_equal(xq_neg[:, :, 4:].view(np.int8), -xq[:, :, 4:].view(np.int8))
+    assert np.array_equal(xq_neg[:, :, 0:2], xq[:, :, 0:2])
+
+
+def test_q8_1_zero_block_and_power_of_two_scaling():
+    x = synth.activations(2, 256, seed=3)
+    x[1, 64:96] = 0.0
+    xq = oracle.quantize_q8_1(x)
+    assert np.all(xq[1, 2] == 0)
+    for k in (-3, 4):
+        xs = (x * np.float32(2.0 ** k)).astype(np.float32)
+        xqs = oracle.quantize_q8_1(xs)
+        assert np.array_equal(xqs[:, :, 4:], xq[:, :, 4:])
+        d = xq[:, :, 0:2].copy().view(np.float16).astype(np.float64)
+        ds = xqs[:, :, 0:2].copy().view(np.float16).astype(np.float64)
+        nz = d != 0
+        assert np.array_equal(ds[nz], d[nz] * 2.0 ** k)
+
+
+# ---------------------------------------------------------------- hand blocks
+
+def test_q4_0_hand_block():
+    g = GOLDEN["q4_0_block_times_ones"]
+    w = _q4_0_block(1.0, [9] * 32).reshape(1, 1, 18)
+    xq = oracle.quantize_q8_1(np.ones((1, 32), dtype=np.float32))
+    assert oracle.block_dots_q4_0(w, xq)[0, 0, 0] == g["I"]
+    y, S = oracle.qgemv_q4_0(w, xq)
+    assert y[0, 0] == g["y"]
+    assert S[0, 0] == g["y"]
+
+
+def test_q6_k_hand_superblock():
+    g = GOLDEN["q6_k_superblock_times_ones"]
+    w = _q6_k_superblock(2.0 ** -10, [1] * 16, [33] * 256).reshape(1, 1, 210)
+    xq = oracle.quantize_q8_1(np.ones((1, 256), dtype=np.float32))
+    assert np.all(oracle.block_dots_q6_k(w, xq) == g["J_per_block"])
+    y, _ = oracle.qgemv_q6_k(w, xq)
+    assert y[0, 0] == g["y"]
+
+
+def test_q6_k_codes_subscales_and_offsets_hand():
+    # distinct codes and subscales: the dot against a one-hot activation reads
+    # back exactly one weight value d * sc * (q - 32)
+    g = np.random.default_rng(5)
+    codes = g.integers(0, 64, 256)
+    sc = g.integers(-64, 64, 16)
+    w = _q6_k_superblock(2.0 ** -8, sc, codes).reshape(1, 1, 210)
+    for i in (0, 1, 15, 16, 17, 31, 100, 129, 255):
+        x = np.zeros((1, 256), dtype=np.float32)
+        x[0, i] = 1.0
+        xq = oracle.quantize_q8_1(x)
+        y, _ = oracle.qgemv_q6_k(w, xq)
+        expect = 2.0 ** -8 * sc[i >> 4] * (codes[i] - 32) * 127 * (1032 / 131072)
+        assert y[0, 0] == expect, i
+
+
+def test_q4_0_codes_one_hot():
+    g = np.random.default_rng(6)
+    codes = g.integers(0, 16, 32)
+    w = _q4_0_block(0.5, codes).reshape(1, 1, 18)
+    for i in range(32):
+        x = np.zeros((1, 32), dtype=np.float32)
+        x[0, i] = -1.0
+        y, _ = oracle.qgemv_q4_0(w, oracle.quantize_q8_1(x))
+        assert y[0, 0] == 0.5 * (codes[i] - 8) * -127 * (1032 / 131072), i
+
+
+# ---------------------------------------------------------------- brute force
+
+@pytest.mark.parametrize("M", [1, 2, 3])
+@pytest.mark.parametrize("K", [32, 64, 256, 512])
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 33])
+def test_q4_0_int_dots_match_fp64_dequant_matmul(M, K, N):
+    w = synth.q4_0_weights(N, K, seed=100 + K + N)
+    xq = oracle.quantize_q8_1(synth.activations(M, K, seed=200 + M))
+    y, S = oracle.qgemv_q4_0(w, xq)
+    ref = oracle.dequant_q8_1_np(xq) @ oracle.dequant_q4_0_np(w).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * np.maximum(S, 1e-300))
+
+
+@pytest.mark.parametrize("M", [1, 2, 3])
+@pytest.mark.parametrize("K", [256, 512])
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 33])
+def test_q6_k_int_dots_match_fp64_dequant_matmul(M, K, N):
+    w = synth.q6_k_weights(N, K, seed=300 + K + N)
+    xq = oracle.quantize_q8_1(synth.activations(M, K, seed=400 + M))
+    y, S = oracle.qgemv_q6_k(w, xq)
+    ref = oracle.dequant_q8_1_np(xq) @ oracle.dequant_q6_k_np(w).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * np.maximum(S, 1e-300))
+
+
+def test_c_and_numpy_dequantizers_agree():
+    w4 = synth.q4_0_weights(5, 256, seed=1)
+    w6 = synth.q6_k_weights(5, 512, seed=2)
+    out4 = np.zeros((5, 256))
+    out6 = np.zeros((5, 512))
+    lib = oracle.oracle._load()
+    lib.oracle_dequant_q4_0(w4.ctypes.data, 5, 256, out4.ctypes.data)
+    lib.oracle_dequant_q6_k(w6.ctypes.data, 5, 512, out6.ctypes.data)
+    assert np.array_equal(out4, oracle.dequant_q4_0_np(w4))
+    assert np.array_equal(out6, oracle.dequant_q6_k_np(w6))
+
+
+def test_block_dots_sum_to_output():
+    w = synth.q4_0_weights(9, 512, seed=4)
+    xq = oracle.quantize_q8_1(synth.activations(2, 512, seed=5))
+    I = oracle.block_dots_q4_0(w, xq).astype(np.float64)
+    dw = w[:, :, 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    da = xq[:, :, 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    y = (I * dw[None, :, :] * da[:, None, :]).sum(axis=2)
+    ref, _ = oracle.qgemv_q4_0(w, xq)
+    assert np.allclose(y, ref, rtol=1e-13, atol=0)
+
+
+def test_threads_do_not_change_results():
+    w = synth.q6_k_weights(37, 512, seed=8)
+    xq = oracle.quantize_q8_1(synth.activations(3, 512, seed=9))
+    y1, s1 = oracle.qgemv_q6_k(w, xq, nthreads=1)
+    y4, s4 = oracle.qgemv_q6_k(w, xq, nthreads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(s1, s4)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_invariants_zero_row_permutation_scaling():
+    K, N = 512, 40
+    w = synth.q4_0_weights(N, K, seed=11)
+    x = synth.activations(3, K, seed=12)
+    x[1] = 0.0
+    xq = oracle.quantize_q8_1(x)
+    y, _ = oracle.qgemv_q4_0(w, xq)
+    assert np.all(y[1] == 0.0)
+    perm = np.random.default_rng(0).permutation(N)
+    yp, _ = oracle.qgemv_q4_0(w[perm], xq)
+    assert np.array_equal(yp, y[:, perm])
+    ys, _ = oracle.qgemv_q4_0(w, oracle.quantize_q8_1(x * np.float32(4.0)))
+    assert np.array_equal(ys, 4.0 * y)
+
+
+# ---------------------------------------------------------------- byte counts
+
+def test_pages_expanded_pack_byte_count():
+    g = GOLDEN["q6_k_expanded_pack_bytes"]
+    ns = g["K"] // 256
+    # expanded: 256 int8 quants + 16 int8 subscales + one fp16 scale per superblock
+    assert g["N"] * ns * (256 + 16 + 2) == g["expanded_bytes"]
+    # canonical 6-bit superblock
+    assert synth.Q6_K_BYTES == 256 * 6 // 8 + 16 + 2
+    assert g["N"] * ns * synth.Q6_K_BYTES == g["canonical_bytes"]
+    assert synth.Q4_0_BYTES == 32 * 4 // 8 + 2
+
+
+# ---------------------------------------------------------------- top-1
+
+def test_top1_ties_and_specials():
+    y = np.zeros((6, 300))
+    y[1, [1, 256]] = 5.0
+    y[2, [255, 256]] = 5.0
+    y[3, [0, 299]] = 5.0
+    y[4, :] = np.nan
+    y[5, 10] = -0.0
+    y[5, :] = -1.0
+    y[5, 7] = 0.0
+    y[5, 3] = -0.0
+    assert oracle.top1(y).tolist() == [0, 1, 255, 0, 0, 3]
+    z = np.full((2, 10), -np.inf)
+    z[0, 4] = np.inf
+    z[0, 6] = np.inf
+    z[1, 2] = np.nan
+    assert oracle.top1(z).tolist() == [4, 0]
+    assert oracle.top1(y.astype(np.float32)).tolist() == [0, 1, 255, 0, 0, 3]
+
+
+def test_top1_all_zero_weights_give_token_0():
+    w = np.zeros((64, 1, 210), dtype=np.uint8)
+    ids, y, _ = oracle.lmhead_q6_k_top1(w, synth.activations(5, 256, seed=1))
+    assert np.all(y == 0.0) and ids.tolist() == [0] * 5
+
+
+def test_top1_matches_brute_force_argmax():
+    w = synth.q6_k_weights(300, 512, seed=21)
+    x = synth.activations(4, 512, seed=22)
+    ids, y, _ = oracle.lmhead_q6_k_top1(w, x)
+    ref = oracle.dequant_q8_1_np(oracle.quantize_q8_1(x)) @ oracle.dequant_q6_k_np(w).T
+    assert ids.tolist() == np.argmax(ref, axis=1).tolist()
