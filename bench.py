@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Benchmark of the width-6 speculative-verifier hot path on one GB300.
+
+One step = one pass of every hot-path call over one batch of synthetic input
+(weights resident in HBM, seeded synthetic data shaped like the pages'
+workloads):
+  1. quantize_q8_1   x [6, 5120] -> Q8_1          (shared by gate and up)
+  2. qgemv_q4_0      gate  M=6 K=5120  N=17408
+  3. qgemv_q4_0      up    M=6 K=5120  N=17408    (same Q8_1 activation)
+  4. quantize_q8_1   h [6, 17408]
+  5. qgemv_q4_0      down  M=6 K=17408 N=5120
+  6. lmhead_q6_k_top1  draft rows 1..5 of [6, 5120] against the Q6_K
+                     [5120, 248320] LM-head -> 5 token ids, no logits
+  7. quantize_q8_1   target hidden [6, 5120]
+  8. qgemv_q6_k      target LM-head M=6 N=248320 (logits)
+  9. argmax_f32_rows the 6 target rows -> 6 token ids
+About 2.2 GB of weights stream from HBM per step, far more than L2 (129 MB),
+so no call finds its weights in L2.
+
+value = effective GB/s: bytes of quantized weights plus activations read by
+the calls / step time.  Per-kernel figures (CUDA events on the launching
+stream) give the M=6 MMVQ GB/s, the fused LM-head microseconds and the
+roofline of the dominant kernel.  `--impl reference` times the CPU oracle on a
+bounded sample of the same step instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective weight GB/s (% of GB300 HBM peak) for M=6 MMVQ; µs per fused LM-head top-1"
+UNIT = "GB/s"
+K_H, N_FF, N_V = 5120, 17408, 248320
+M_T = 6
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD = ("width-6 verifier step: Q4_0 gate/up M=6 K=5120 N=17408 (shared Q8_1), Q4_0 down M=6 K=17408 N=5120, "
+            "fused Q6_K draft LM-head top-1 rows 1..5 K=5120 N=248320, target Q6_K LM-head M=6 N=248320 + argmax")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded oracle sample length")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- inputs
+
+
+def make_inputs(seed_base: int = 0):
+    from block_quantized_gemv_quantize_gb300 import synth
+
+    c1 = synth.WORKLOADS["verifier_gate_up"]
+    c2 = synth.WORKLOADS["verifier_down"]
+    c3 = synth.WORKLOADS["lmhead_q6_k"]
+    return dict(
+        w_gate=synth.q4_0_weights(N_FF, K_H, seed=c1["seed"]),
+        w_up=synth.q4_0_weights(N_FF, K_H, seed=c1["seed"] + 10),
+        w_down=synth.q4_0_weights(K_H, N_FF, seed=c2["seed"]),
+        w_vocab=synth.q6_k_weights(N_V, K_H, seed=c3["seed"]),
+        x=synth.activations(M_T, K_H, seed=c1["seed"] + 100, outlier_frac=0.01),
+        h=synth.activations(M_T, N_FF, seed=c2["seed"] + 100, outlier_frac=0.01),
+        x_draft=synth.activations(6, K_H, seed=c3["seed"] + 100),
+        x_target=synth.activations(M_T, K_H, seed=c3["seed"] + 200),
+    )
+
+
+def step_bytes():
+    """Algorithmic bytes read per call (quantized weights + activations)."""
+    from block_quantized_gemv_quantize_gb300 import ops
+
+    q4 = ops.q4_0_pack_bytes(N_FF, K_H)
+    q6 = ops.q6_k_pack_bytes(N_V, K_H)
+    return {
+        "quantize_x": M_T * K_H * 4,
+        "gate": q4 + ops.q8_1_bytes(M_T, K_H),
+        "up": q4 + ops.q8_1_bytes(M_T, K_H),
+        "quantize_h": M_T * N_FF * 4,
+        "down": ops.q4_0_pack_bytes(K_H, N_FF) + ops.q8_1_bytes(M_T, N_FF),
+        "lmhead_top1": q6 + 5 * K_H * 4,
+        "quantize_t": M_T * K_H * 4,
+        "target_head": q6 + ops.q8_1_bytes(M_T, K_H),
+        "argmax": M_T * N_V * 4,
+    }
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- native arm
+
+
+def run_native(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from block_quantized_gemv_quantize_gb300 import build
+
+    build.build()
+    from block_quantized_gemv_quantize_gb300 import ops
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = make_inputs()
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    w = {}
+    for name, fmt, n, k in (("w_gate", "q4_0", N_FF, K_H), ("w_up", "q4_0", N_FF, K_H), ("w_down", "q4_0", K_H, N_FF),
+                            ("w_vocab", "q6_k", N_V, K_H)):
+        canon = up(inp[name])
+        w[name] = (ops.qpack_q4_0 if fmt == "q4_0" else ops.qpack_q6_k)(canon, n, k)
+        del canon
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # resident activations, outputs and Q8_1 buffers
+    x, h, xd, xt = up(inp["x"]), up(inp["h"]), up(inp["x_draft"]), up(inp["x_target"])
+    xq1 = torch.empty(ops.q8_1_bytes(M_T, K_H), dtype=torch.uint8, device=dev)
+    xq2 = torch.empty(ops.q8_1_bytes(M_T, N_FF), dtype=torch.uint8, device=dev)
+    xq3 = torch.empty(ops.q8_1_bytes(M_T, K_H), dtype=torch.uint8, device=dev)
+    y_gate = torch.empty((M_T, N_FF), device=dev)
+    y_up = torch.empty((M_T, N_FF), device=dev)
+    y_down = torch.empty((M_T, K_H), device=dev)
+    logits = torch.empty((M_T, N_V), device=dev)
+    ids_d = torch.empty(5, dtype=torch.int32, device=dev)
+    ids_t = torch.empty(M_T, dtype=torch.int32, device=dev)
+    ws1 = torch.zeros(ops.lmhead_q6_k_top1_workspace_bytes(5, K_H, N_V), dtype=torch.uint8, device=dev)
+    ws2 = torch.zeros(ops.argmax_f32_rows_workspace_bytes(M_T, N_V), dtype=torch.uint8, device=dev)
+    xd_rows = xd[1:6]
+
+    names = ["quantize_x", "gate", "up", "quantize_h", "down", "lmhead_top1", "quantize_t", "target_head", "argmax"]
+    calls = [
+        lambda: ops.quantize_q8_1(x, out=xq1),
+        lambda: ops.qgemv_q4_0(w["w_gate"], xq1, M_T, K_H, N_FF, y=y_gate),
+        lambda: ops.qgemv_q4_0(w["w_up"], xq1, M_T, K_H, N_FF, y=y_up),
+        lambda: ops.quantize_q8_1(h, out=xq2),
+        lambda: ops.qgemv_q4_0(w["w_down"], xq2, M_T, N_FF, K_H, y=y_down),
+        lambda: ops.lmhead_q6_k_top1(w["w_vocab"], xd_rows, K_H, N_V, ids=ids_d, ws=ws1),
+        lambda: ops.quantize_q8_1(xt, out=xq3),
+        lambda: ops.qgemv_q6_k(w["w_vocab"], xq3, M_T, K_H, N_V, y=logits),
+        lambda: ops.argmax_f32_rows(logits, ids=ids_t, ws=ws2),
+    ]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        for i, c in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            c()
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-call events, clocks sampled meanwhile
+    per = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            step(per[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    call_ms = {n: statistics.mean(per[s][i][0].elapsed_time(per[s][i][1]) for s in range(args.steps))
+               for i, n in enumerate(names)}
+
+    nbytes = step_bytes()
+    step_total = sum(nbytes.values())
+    value = world * step_total / (ms_per_step * 1e-3) / 1e9
+
+    # e2e: the same step through the public API with host buffers: per step the
+    # activations are copied in from pinned host memory and the results
+    # (both id vectors and the MLP output) are copied back.
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory() for k in ("x", "h", "x_draft", "x_target")}
+    dev_in = {"x": x, "h": h, "x_draft": xd, "x_target": xt}
+    host_out = {"ids_d": torch.empty(5, dtype=torch.int32).pin_memory(),
+                "ids_t": torch.empty(M_T, dtype=torch.int32).pin_memory(),
+                "y_down": torch.empty((M_T, K_H)).pin_memory()}
+    dev_out = {"ids_d": ids_d, "ids_t": ids_t, "y_down": y_down}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        step()
+        for k, t in host_out.items():
+            t.copy_(dev_out[k], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * step_total / (e2e_ms * 1e-3) / 1e9
+
+    # fused vs unfused LM-head on identical inputs (rows 1..5), interleaved A/B
+    y5 = torch.empty((5, N_V), device=dev)
+    xq5 = torch.empty(ops.q8_1_bytes(5, K_H), dtype=torch.uint8, device=dev)
+    ids_u = torch.empty(5, dtype=torch.int32, device=dev)
+
+    def fused():
+        ops.lmhead_q6_k_top1(w["w_vocab"], xd_rows, K_H, N_V, ids=ids_d, ws=ws1)
+
+    def unfused():
+        ops.quantize_q8_1(xd_rows, out=xq5)
+        ops.qgemv_q6_k(w["w_vocab"], xq5, 5, K_H, N_V, y=y5)
+        ops.argmax_f32_rows(y5, ids=ids_u, ws=ws2)
+
+    ab = {"fused": [], "unfused": []}
+    for _ in range(5):
+        for name, fn in (("fused", fused), ("unfused", unfused)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(10):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ab[name].append(a.elapsed_time(b) * 1e3 / 10)
+    same_ids = ids_d.cpu().tolist() == ids_u.cpu().tolist()
+
+    peak, peak_kind = peaks()
+    dominant = max(("lmhead_top1", "target_head", "gate", "up", "down"), key=lambda n: call_ms[n])
+    achieved = nbytes[dominant] / (call_ms[dominant] * 1e-3) / 1e9
+    traffic = load_traffic(dominant)
+    mmvq_names = ("gate", "up", "down")
+    mmvq_gbs = sum(nbytes[n] for n in mmvq_names) / (sum(call_ms[n] for n in mmvq_names) * 1e-3) / 1e9
+
+    result = None
+    if rank == 0:
+        clocks = clk.summary()
+        run_native.inputs = inp
+        result = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int8 x int4/int6 -> int32 block dots, fp32 accumulate",
+            "data": "synthetic (seeded; Q4_0/Q6_K/Q8_1 shapes and distributions of the pages' workloads)",
+            "config": {"workload": WORKLOAD, "bytes_per_step": step_total,
+                       "l2": "inputs larger than L2: ~2.2 GB of weights streamed per step, no flush needed",
+                       "replicas": world},
+            "mmvq_m6_q4_0": {"gbs": round(mmvq_gbs, 1), "frac_of_hbm_peak": round(mmvq_gbs / peak, 4),
+                             "us": {n: round(call_ms[n] * 1e3, 2) for n in mmvq_names}},
+            "lmhead_top1_us": round(call_ms["lmhead_top1"] * 1e3, 2),
+            "fused_vs_unfused_us": {"fused": round(statistics.median(ab["fused"]), 2),
+                                    "unfused": round(statistics.median(ab["unfused"]), 2),
+                                    "same_ids": same_ids},
+            "per_call_us": {n: round(call_ms[n] * 1e3, 2) for n in names},
+            "per_call_gbs": {n: round(nbytes[n] / (call_ms[n] * 1e-3) / 1e9, 1) for n in names},
+            "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "algorithmic_bytes": nbytes[dominant]},
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": len(calls) * args.steps,
+            "clocks": clocks,
+        }
+    return result
+
+
+def _source_digest() -> str:
+    csrc = os.path.join(ROOT, "block_quantized_gemv_quantize_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernels changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("source_digest") != _source_digest():
+        return None
+    return d.get("per_launch_dram_bytes", {}).get(kernel)
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample_step(inp, frac: float, nthreads: int):
+    """One step of the oracle over the first `frac` of every weight's rows;
+    returns (seconds, algorithmic bytes of the sample)."""
+    import oracle
+
+    def rows(a):
+        return a[: max(1, int(round(a.shape[0] * frac)))]
+
+    t = time.perf_counter()
+    nbytes = 0
+    xq1 = oracle.quantize_q8_1(inp["x"])
+    for name in ("w_gate", "w_up"):
+        wr = rows(inp[name])
+        oracle.qgemv_q4_0(wr, xq1, nthreads)
+        nbytes += wr.nbytes + xq1.nbytes
+    xq2 = oracle.quantize_q8_1(inp["h"])
+    wr = rows(inp["w_down"])
+    oracle.qgemv_q4_0(wr, xq2, nthreads)
+    nbytes += wr.nbytes + xq2.nbytes
+    wv = rows(inp["w_vocab"])
+    y5, _ = oracle.qgemv_q6_k(wv, oracle.quantize_q8_1(inp["x_draft"][1:6]), nthreads)
+    oracle.top1(y5)
+    nbytes += wv.nbytes + 5 * K_H * 4
+    yt, _ = oracle.qgemv_q6_k(wv, oracle.quantize_q8_1(inp["x_target"]), nthreads)
+    oracle.top1(yt)
+    nbytes += wv.nbytes + xq1.nbytes + yt.size * 4
+    nbytes += (inp["x"].nbytes + inp["h"].nbytes + inp["x_target"].nbytes)
+    return time.perf_counter() - t, nbytes
+
+
+def calibrate_fraction(inp, seconds: float, nthreads: int) -> float:
+    dt, _ = oracle_sample_step(inp, 0.002, nthreads)
+    return min(1.0, max(0.0005, 0.002 * seconds / max(dt, 1e-3)))
+
+
+def cpu_baseline(inp, seconds: float):
+    import oracle
+
+    n = oracle.default_threads()
+    frac = calibrate_fraction(inp, seconds, n)
+    dt, nb = oracle_sample_step(inp, frac, n)
+    return {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"first {frac:.4%} of the rows of every weight in one step ({dt:.1f} s, {nb / 1e6:.1f} MB)"}
+
+
+def run_reference(args):
+    import oracle
+
+    inp = make_inputs()
+    n = oracle.default_threads()
+    per_step_s = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    frac = calibrate_fraction(inp, per_step_s, n)
+    for _ in range(args.warmup):
+        oracle_sample_step(inp, frac, n)
+    times, nb = [], 0
+    for _ in range(args.steps):
+        dt, nb = oracle_sample_step(inp, frac, n)
+        times.append(dt)
+    total = sum(times)
+    value = nb * args.steps / total / 1e9
+    sample = f"first {frac:.4%} of the rows of every weight per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32 block dots, fp64 accumulate (CPU oracle)",
+        "data": "synthetic (seeded; same inputs as the native arm)",
+        "config": {"workload": WORKLOAD, "sampled": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    result = run_native(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(run_native.inputs, args.cpu_seconds)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+"""Thin ctypes binding of libqgemv.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes torch
+tensors (device memory) plus sizes, passes raw pointers and the current CUDA
+stream, and raises ``QgemvError`` on a non-zero status.  All computation runs
+in the library's CUDA kernels; there is no other code path.  If the shared
+library is missing, importing this module raises: build it first
+(``python -m block_quantized_gemv_quantize_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_S = ctypes.c_size_t
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "qgemv_status_string": (ctypes.c_char_p, [_I]),
+    "q8_1_bytes": (_S, [_I, _I]),
+    "q4_0_pack_bytes": (_S, [_I, _I]),
+    "q6_k_pack_bytes": (_S, [_I, _I]),
+    "lmhead_q6_k_top1_workspace_bytes": (_S, [_I, _I, _I]),
+    "argmax_f32_rows_workspace_bytes": (_S, [_I, _I]),
+    "quantize_q8_1": (_I, [_P, _L, _P, _I, _I, _P]),
+    "qpack_q4_0": (_I, [_P, _P, _I, _I, _P]),
+    "qpack_q6_k": (_I, [_P, _P, _I, _I, _P]),
+    "qgemv_q4_0": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
+    "qgemv_q6_k": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
+    "lmhead_q6_k_top1": (_I, [_P, _P, _L, _P, _P, _S, _I, _I, _I, _P]),
+    "argmax_f32_rows": (_I, [_P, _L, _P, _P, _S, _I, _I, _P]),
+    "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+}
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, name: str, status: int):
+        super().__init__(f"{name} failed with status {status}: {status_string(status)}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build the CUDA library first "
+                          f"(python -m block_quantized_gemv_quantize_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+LIB_PATH = _build.LIB
+
+
+def status_string(status: int) -> str:
+    return LIB.qgemv_status_string(status).decode()
+
+
+def _check(name: str, status: int) -> None:
+    if status != 0:
+        raise QgemvError(name, status)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _dev(t: torch.Tensor, what: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    return t.data_ptr()
+
+
+# ---------------------------------------------------------------- sizes
+
+def q8_1_bytes(M: int, K: int) -> int:
+    return LIB.q8_1_bytes(M, K)
+
+
+def q4_0_pack_bytes(N: int, K: int) -> int:
+    return LIB.q4_0_pack_bytes(N, K)
+
+
+def q6_k_pack_bytes(N: int, K: int) -> int:
+    return LIB.q6_k_pack_bytes(N, K)
+
+
+def lmhead_q6_k_top1_workspace_bytes(M: int, K: int, N: int) -> int:
+    return LIB.lmhead_q6_k_top1_workspace_bytes(M, K, N)
+
+
+def argmax_f32_rows_workspace_bytes(M: int, N: int) -> int:
+    return LIB.argmax_f32_rows_workspace_bytes(M, N)
+
+
+# ---------------------------------------------------------------- workspaces
+
+_ws_lock = threading.Lock()
+_ws_cache: dict[tuple, torch.Tensor] = {}
+
+
+def workspace(device: torch.device, nbytes: int, key: str = "top1") -> torch.Tensor:
+    """A zero-filled device workspace, one per (device, stream, key); the
+    kernels leave it zero-filled after every call."""
+    device = torch.device(device)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    k = (device.index, stream, key)
+    with _ws_lock:
+        ws = _ws_cache.get(k)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[k] = ws
+    return ws
+
+
+# ---------------------------------------------------------------- the calls
+
+def quantize_q8_1(x: torch.Tensor, K: int | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32 x [M, ldx] (row stride = x.stride(0)) -> Q8_1 uint8 [M, K/32*36]."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    if out is None:
+        out = torch.empty((M, q8_1_bytes(1, K)), dtype=torch.uint8, device=x.device)
+    _check("quantize_q8_1", LIB.quantize_q8_1(_dev(x, "x"), x.stride(0), _dev(out, "xq"), M, K, _stream(x)))
+    return out
+
+
+def qpack_q4_0(w_canon: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(q4_0_pack_bytes(N, K), dtype=torch.uint8, device=w_canon.device)
+    _check("qpack_q4_0", LIB.qpack_q4_0(_dev(w_canon, "w_canon"), _dev(out, "w_pack"), N, K, _stream(w_canon)))
+    return out
+
+
+def qpack_q6_k(w_canon: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(q6_k_pack_bytes(N, K), dtype=torch.uint8, device=w_canon.device)
+    _check("qpack_q6_k", LIB.qpack_q6_k(_dev(w_canon, "w_canon"), _dev(out, "w_pack"), N, K, _stream(w_canon)))
+    return out
+
+
+def _gemv(name: str, w_pack, xq, M, K, N, y):
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    assert y.dtype == torch.float32 and y.stride(1) == 1
+    fn = getattr(LIB, name)
+    _check(name, fn(_dev(w_pack, "w_pack"), _dev(xq, "xq"), _dev(y, "y"), y.stride(0), M, K, N, _stream(xq)))
+    return y
+
+
+def qgemv_q4_0(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
+               y: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp32 = Q4_0 weight (packed) x Q8_1 activation."""
+    return _gemv("qgemv_q4_0", w_pack, xq, M, K, N, y)
+
+
+def qgemv_q6_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
+               y: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp32 = Q6_K weight (packed) x Q8_1 activation."""
+    return _gemv("qgemv_q6_k", w_pack, xq, M, K, N, y)
+
+
+def lmhead_q6_k_top1(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, ids: torch.Tensor | None = None,
+                     ws: torch.Tensor | None = None) -> torch.Tensor:
+    """Greedy token id of each row of fp32 x [M, >=K] (row stride x.stride(0))."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    if ids is None:
+        ids = torch.empty(M, dtype=torch.int32, device=x.device)
+    nb = lmhead_q6_k_top1_workspace_bytes(M, K, N)
+    if ws is None:
+        ws = workspace(x.device, nb)
+    _check("lmhead_q6_k_top1", LIB.lmhead_q6_k_top1(_dev(w_pack, "w_pack"), _dev(x, "x"), x.stride(0),
+                                                    _dev(ids, "ids"), _dev(ws, "workspace"), ws.numel(),
+                                                    M, K, N, _stream(x)))
+    return ids
+
+
+def argmax_f32_rows(y: torch.Tensor, N: int | None = None, ids: torch.Tensor | None = None,
+                    ws: torch.Tensor | None = None) -> torch.Tensor:
+    assert y.dtype == torch.float32 and y.dim() == 2 and y.stride(1) == 1
+    M = y.shape[0]
+    N = y.shape[1] if N is None else N
+    if ids is None:
+        ids = torch.empty(M, dtype=torch.int32, device=y.device)
+    if ws is None:
+        ws = workspace(y.device, argmax_f32_rows_workspace_bytes(M, N), key="argmax")
+    _check("argmax_f32_rows", LIB.argmax_f32_rows(_dev(y, "y"), y.stride(0), _dev(ids, "ids"),
+                                                  _dev(ws, "workspace"), ws.numel(), M, N, _stream(y)))
+    return ids
+
+
+def qgemv_block_dots_q4_0(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int) -> torch.Tensor:
+    out = torch.empty((M, N, K // 32), dtype=torch.int32, device=xq.device)
+    _check("qgemv_block_dots_q4_0", LIB.qgemv_block_dots_q4_0(_dev(w_pack, "w_pack"), _dev(xq, "xq"),
+                                                              out.data_ptr(), M, K, N, _stream(xq)))
+    return out
+
+
+def qgemv_block_dots_q6_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int) -> torch.Tensor:
+    out = torch.empty((M, N, K // 32), dtype=torch.int32, device=xq.device)
+    _check("qgemv_block_dots_q6_k", LIB.qgemv_block_dots_q6_k(_dev(w_pack, "w_pack"), _dev(xq, "xq"),
+                                                              out.data_ptr(), M, K, N, _stream(xq)))
+    return out

@@ -1,0 +1,159 @@
+// C ABI entry points: host-side validation, then one enqueue on the caller's
+// stream.  Nothing here allocates or synchronizes.  Fail closed: every
+// precondition is checked before any work is enqueued ("Q6_K M=6 fused DFlash
+// top-1 production record", Exactness and safety contracts: non-matching
+// inputs never reach the fused kernel).
+#include "../../include/qgemv.h"
+#include "launch.cuh"
+
+using namespace qgemv;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int check_mk(int M, int K, int kmult)
+{
+    if (M < 1 || K < kmult) return QGEMV_INVALID_ARG;
+    if (M > QGEMV_MAX_M) return QGEMV_UNSUPPORTED_SHAPE;
+    if (K % kmult != 0) return QGEMV_UNSUPPORTED_SHAPE;
+    return QGEMV_OK;
+}
+
+int check_gemv(const void* w, const void* xq, const void* y, int64_t ldy, int M, int K, int N, int kmult)
+{
+    if (!w || !xq || !y) return QGEMV_INVALID_ARG;
+    int st = check_mk(M, K, kmult);
+    if (st) return st;
+    if (N < 1 || ldy < N) return QGEMV_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(xq) || !aligned16(y)) return QGEMV_MISALIGNED;
+    return QGEMV_OK;
+}
+
+size_t top1_ws_bytes() { return sizeof(Top1Workspace); }
+
+}  // namespace
+
+extern "C" {
+
+const char* qgemv_status_string(int status)
+{
+    switch (status) {
+    case QGEMV_OK: return "ok";
+    case QGEMV_INVALID_ARG: return "invalid argument (null pointer, or M/K/N/leading dimension out of range)";
+    case QGEMV_UNSUPPORTED_SHAPE: return "unsupported shape (M > 17, or K not a multiple of the block size)";
+    case QGEMV_MISALIGNED: return "a device pointer is not 16-byte aligned";
+    case QGEMV_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case QGEMV_CUDA_ERROR: return "CUDA error (launch or device query failed)";
+    default: return "unknown status";
+    }
+}
+
+size_t q8_1_bytes(int M, int K) { return (M < 0 || K < 0) ? 0 : (size_t)M * (size_t)(K / QK) * Q8_1_BYTES; }
+size_t q4_0_pack_bytes(int N, int K) { return (N < 0 || K < 0) ? 0 : (size_t)N * (size_t)(K / QK) * Q4_0_BYTES; }
+size_t q6_k_pack_bytes(int N, int K) { return (N < 0 || K < 0) ? 0 : (size_t)N * (size_t)(K / QK_K) * Q6_K_BYTES; }
+size_t lmhead_q6_k_top1_workspace_bytes(int, int, int) { return top1_ws_bytes(); }
+size_t argmax_f32_rows_workspace_bytes(int, int) { return top1_ws_bytes(); }
+
+int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* stream)
+{
+    if (!x || !xq) return QGEMV_INVALID_ARG;
+    int st = check_mk(M, K, QK);
+    if (st) return st;
+    if (ldx < K) return QGEMV_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq)) return QGEMV_MISALIGNED;
+    return launch_quantize_q8_1(x, ldx, xq, M, K, as_stream(stream));
+}
+
+int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
+{
+    if (!w_canon || !w_pack || N < 1 || K < QK) return QGEMV_INVALID_ARG;
+    if (K % QK) return QGEMV_UNSUPPORTED_SHAPE;
+    if (!aligned16(w_canon) || !aligned16(w_pack)) return QGEMV_MISALIGNED;
+    return launch_qpack_q4_0(w_canon, w_pack, N, K, as_stream(stream));
+}
+
+int qpack_q6_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
+{
+    if (!w_canon || !w_pack || N < 1 || K < QK_K) return QGEMV_INVALID_ARG;
+    if (K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
+    if (!aligned16(w_canon) || !aligned16(w_pack)) return QGEMV_MISALIGNED;
+    return launch_qpack_q6_k(w_canon, w_pack, N, K, as_stream(stream));
+}
+
+int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
+{
+    int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK);
+    if (st) return st;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.y = y;
+    a.ldy = ldy;
+    a.K = K;
+    a.N = N;
+    return launch_mmvq_q4_0(a, M, as_stream(stream));
+}
+
+int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
+{
+    int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK_K);
+    if (st) return st;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.y = y;
+    a.ldy = ldy;
+    a.K = K;
+    a.N = N;
+    return launch_mmvq_q6_k(a, M, as_stream(stream));
+}
+
+int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* ids, void* workspace,
+                     size_t ws_bytes, int M, int K, int N, void* stream)
+{
+    if (!w_pack || !x || !ids || !workspace) return QGEMV_INVALID_ARG;
+    int st = check_mk(M, K, QK_K);
+    if (st) return st;
+    if (N < 1 || ldx < K) return QGEMV_INVALID_ARG;
+    if (ws_bytes < top1_ws_bytes()) return QGEMV_WORKSPACE_TOO_SMALL;
+    if (!aligned16(w_pack) || !aligned16(x) || !aligned16(ids) || !aligned16(workspace)) return QGEMV_MISALIGNED;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.x = x;
+    a.ldx = ldx;
+    a.K = K;
+    a.N = N;
+    a.ws = static_cast<Top1Workspace*>(workspace);
+    a.ids = ids;
+    return launch_lmhead_q6_k(a, M, as_stream(stream));
+}
+
+int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, size_t ws_bytes, int M, int N,
+                    void* stream)
+{
+    if (!y || !ids || !workspace) return QGEMV_INVALID_ARG;
+    if (M < 1 || N < 1 || ldy < N) return QGEMV_INVALID_ARG;
+    if (M > QGEMV_MAX_M) return QGEMV_UNSUPPORTED_SHAPE;
+    if (ws_bytes < top1_ws_bytes()) return QGEMV_WORKSPACE_TOO_SMALL;
+    if (!aligned16(y) || !aligned16(ids) || !aligned16(workspace)) return QGEMV_MISALIGNED;
+    return launch_argmax_rows(y, ldy, ids, static_cast<Top1Workspace*>(workspace), M, N, as_stream(stream));
+}
+
+int qgemv_block_dots_q4_0(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream)
+{
+    int st = check_gemv(w_pack, xq, out, N, M, K, N, QK);
+    if (st) return st;
+    return launch_block_dots(FMT_Q4_0, w_pack, xq, out, M, K, N, as_stream(stream));
+}
+
+int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream)
+{
+    int st = check_gemv(w_pack, xq, out, N, M, K, N, QK_K);
+    if (st) return st;
+    return launch_block_dots(FMT_Q6_K, w_pack, xq, out, M, K, N, as_stream(stream));
+}
+
+}  // extern "C"

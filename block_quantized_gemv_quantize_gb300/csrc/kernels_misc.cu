@@ -1,0 +1,262 @@
+// Q8_1 activation quantizer, weight repackers, row argmax (the unfused
+// control path) and the integer block-dot debug kernel.
+#include "launch.cuh"
+
+namespace qgemv {
+
+DeviceInfo device_info()
+{
+    static DeviceInfo cache[64];
+    static bool have[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DeviceInfo{0, 0};
+    if (!have[dev]) {
+        DeviceInfo d{0, 0};
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DeviceInfo{0, 0};
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return DeviceInfo{0, 0};
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    return cache[dev];
+}
+
+// ---------------------------------------------------------------------------
+// quantize_q8_1: one warp per 32-value block ("Qwen3.6 27B B70 follow-up: Q8
+// activation cache", Q8_1 activation cache prototype: the activation is
+// quantized once and the Q8_1 copy is reused by sibling matmuls).
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
+                                                            uint8_t* __restrict__ xq, int M, int NB)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nblk = (int64_t)M * NB;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < nblk; i += stride) {
+        const int m = (int)(i / NB), b = (int)(i - (int64_t)m * NB);
+        const float xv = x[(int64_t)m * ldx + (int64_t)b * QK + lane];
+        const Q81Lane r = q8_1_quantize_lane(xv);
+        const int S = warp_sum_i32(r.q);
+        uint8_t* blk = xq + i * Q8_1_BYTES;
+        blk[4 + lane] = (uint8_t)(int8_t)r.q;
+        if (lane == 0) {
+            const __half d16 = __float2half_rn(r.d);
+            const __half s16 = __float2half_rn(__fmul_rn(r.d, (float)S));
+            reinterpret_cast<uint32_t*>(blk)[0] =
+                (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(s16) << 16);
+        }
+    }
+}
+
+int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cudaStream_t s)
+{
+    const DeviceInfo di = device_info();
+    if (di.sms <= 0) return QGEMV_CUDA_ERROR;
+    const int NB = K / QK;
+    const int64_t nblk = (int64_t)M * NB;
+    int64_t grid = (nblk + 7) / 8;
+    if (grid > (int64_t)di.sms * 8) grid = (int64_t)di.sms * 8;
+    quantize_q8_1_kernel<<<(int)grid, 256, 0, s>>>(x, ldx, static_cast<uint8_t*>(xq), M, NB);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+// ---------------------------------------------------------------------------
+// Repackers: canonical blocks -> coalesced streams.  Pure bit moves; fp16
+// scales are copied as raw bits ("Qwen3.6 27B Q4_0 DFlash/SYCL closure",
+// Transfer, rule 7: converting fp16 storage objects numerically once produced
+// an all-zero kernel).
+// ---------------------------------------------------------------------------
+
+__global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int64_t nblocks)
+{
+    uint4* nib = reinterpret_cast<uint4*>(pack);
+    uint16_t* dst_d = reinterpret_cast<uint16_t*>(pack + nblocks * 16);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(canon + i * Q4_0_BYTES);  // 2-byte aligned
+        uint32_t q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] = (uint32_t)src[1 + 2 * k] | ((uint32_t)src[2 + 2 * k] << 16);
+        nib[i] = make_uint4(q[0], q[1], q[2], q[3]);
+        dst_d[i] = src[0];
+    }
+}
+
+__global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int64_t nblocks)
+{
+    uint4* ql = reinterpret_cast<uint4*>(pack);
+    uint2* qh = reinterpret_cast<uint2*>(pack + nblocks * 16);
+    uint16_t* sc = reinterpret_cast<uint16_t*>(pack + nblocks * 24);
+    uint16_t* dd = reinterpret_cast<uint16_t*>(pack + nblocks * 26);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t sbi = i >> 3;
+        const int bb = (int)(i & 7);
+        const uint8_t* sb = canon + sbi * Q6_K_BYTES;
+        // canonical sequential packing: low4(q_v) = nibble (v & 1) of ql[v >> 1],
+        // high2(q_v) = bits 2 (v & 3) of qh[v >> 2]; this block's values are
+        // v = 32 bb .. 32 bb + 31.
+        uint8_t q[32];
+#pragma unroll
+        for (int v = 0; v < 32; ++v) {
+            const int g = 32 * bb + v;
+            const int lo = (sb[g >> 1] >> (4 * (g & 1))) & 0x0F;
+            const int hi = (sb[128 + (g >> 2)] >> (2 * (g & 3))) & 0x03;
+            q[v] = (uint8_t)(lo | (hi << 4));
+        }
+        uint32_t wl[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const uint32_t byte = (uint32_t)(q[t] & 0x0F) | ((uint32_t)(q[t + 16] & 0x0F) << 4);
+            wl[t >> 2] |= byte << (8 * (t & 3));
+        }
+        uint32_t wh[2] = {0, 0};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            uint32_t byte = 0;
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) byte |= (uint32_t)(q[t + 8 * s2] >> 4) << (2 * s2);
+            wh[t >> 2] |= byte << (8 * (t & 3));
+        }
+        ql[i] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        qh[i] = make_uint2(wh[0], wh[1]);
+        sc[i] = (uint16_t)sb[192 + 2 * bb] | ((uint16_t)sb[192 + 2 * bb + 1] << 8);
+        if (bb == 0) dd[sbi] = (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
+    }
+}
+
+static int grid_for(int64_t n, int threads, int sms)
+{
+    int64_t g = (n + threads - 1) / threads;
+    const int64_t cap = (int64_t)sms * 16;
+    return (int)(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+int launch_qpack_q4_0(const void* canon, void* pack, int N, int K, cudaStream_t s)
+{
+    const DeviceInfo di = device_info();
+    if (di.sms <= 0) return QGEMV_CUDA_ERROR;
+    const int64_t nblocks = (int64_t)N * (K / QK);
+    qpack_q4_0_kernel<<<grid_for(nblocks, 256, di.sms), 256, 0, s>>>(static_cast<const uint8_t*>(canon),
+                                                                     static_cast<uint8_t*>(pack), nblocks);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+int launch_qpack_q6_k(const void* canon, void* pack, int N, int K, cudaStream_t s)
+{
+    const DeviceInfo di = device_info();
+    if (di.sms <= 0) return QGEMV_CUDA_ERROR;
+    const int64_t nblocks = (int64_t)N * (K / QK);
+    qpack_q6_k_kernel<<<grid_for(nblocks, 256, di.sms), 256, 0, s>>>(static_cast<const uint8_t*>(canon),
+                                                                     static_cast<uint8_t*>(pack), nblocks);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+// ---------------------------------------------------------------------------
+// argmax_f32_rows: the separate argmax of the unfused LM-head path ("Q6_K M=6
+// fused DFlash top-1 production record", Why this was slow), with the same
+// lowest-ID tie contract as the fused reducer (Exactness and safety
+// contracts, item 3).  Cross-CTA reduction: 64-bit atomicMax on the
+// order-preserving key, then the last CTA to finish writes the ids and resets
+// the workspace.
+// ---------------------------------------------------------------------------
+
+constexpr int ARGMAX_THREADS = 256;
+
+__global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float* __restrict__ y, int64_t ldy,
+                                                                     int32_t* __restrict__ ids, Top1Workspace* ws,
+                                                                     int M, int N)
+{
+    __shared__ unsigned long long s_red[ARGMAX_THREADS / 32];
+    __shared__ int s_last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int m = 0; m < M; ++m) {
+        const float* row = y + (int64_t)m * ldy;
+        unsigned long long k = 0ull;
+        for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < N; n += stride) {
+            const unsigned long long kn = top1_key(__ldg(row + n), (int)n);
+            k = kn > k ? kn : k;
+        }
+        k = warp_max_u64(k);
+        if (lane == 0) s_red[warp] = k;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned long long b = 0ull;
+            for (int w = 0; w < ARGMAX_THREADS / 32; ++w) b = s_red[w] > b ? s_red[w] : b;
+            atomicMax(&ws->keys[m], b);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(&ws->done, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        if (threadIdx.x < M) ids[threadIdx.x] = top1_key_to_id(atomicExch(&ws->keys[threadIdx.x], 0ull));
+        if (threadIdx.x == 0) atomicExch(&ws->done, 0u);
+    }
+}
+
+int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int M, int N, cudaStream_t s)
+{
+    const DeviceInfo di = device_info();
+    if (di.sms <= 0) return QGEMV_CUDA_ERROR;
+    int grid = (int)(((int64_t)N + ARGMAX_THREADS * 4 - 1) / (ARGMAX_THREADS * 4));
+    if (grid > di.sms * 2) grid = di.sms * 2;
+    if (grid < 1) grid = 1;
+    argmax_rows_kernel<<<grid, ARGMAX_THREADS, 0, s>>>(y, ldy, ids, ws, M, N);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+// ---------------------------------------------------------------------------
+// Integer block dots, for checking them bit for bit: out[m][n][b] is the
+// exact int32 dot of weight block (n, b) with activation block (m, b), made by
+// the same staging, unpacking and dot routines as the MMVQ kernels.
+// ---------------------------------------------------------------------------
+
+template <int FMT>
+__global__ void block_dots_kernel(const void* __restrict__ w_pack, const uint8_t* __restrict__ xq,
+                                  int32_t* __restrict__ out, int M, int NB, int N)
+{
+    const int64_t total = (int64_t)M * N * NB;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int b = (int)(i % NB);
+        const int64_t mn = i / NB;
+        const int n = (int)(mn % N), m = (int)(mn / N);
+        uint4 lo, hi;
+        uint2 meta;
+        act_from_q8_1<FMT>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES, lo, hi, meta);
+        uint32_t w[8];
+        const int64_t wi = (int64_t)n * NB + b;
+        if (FMT == FMT_Q4_0) {
+            const PackQ40 pk = pack_q4_0(w_pack, N, NB);
+            q4_0_unpack(pk.nib[wi], w);
+            out[i] = q4_0_dot(w, lo, hi, (int)meta.y);
+        } else {
+            const PackQ6K pk = pack_q6_k(w_pack, N, NB);
+            q6_k_unpack(pk.ql[wi], pk.qh[wi], w);
+            out[i] = q6_k_dot(w, lo, hi, meta.y, pk.sc[wi]);
+        }
+    }
+}
+
+int launch_block_dots(int fmt, const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, cudaStream_t s)
+{
+    const DeviceInfo di = device_info();
+    if (di.sms <= 0) return QGEMV_CUDA_ERROR;
+    const int NB = K / QK;
+    const int64_t total = (int64_t)M * N * NB;
+    const int grid = grid_for(total, 256, di.sms);
+    if (fmt == FMT_Q4_0)
+        block_dots_kernel<FMT_Q4_0><<<grid, 256, 0, s>>>(w_pack, static_cast<const uint8_t*>(xq), out, M, NB, N);
+    else
+        block_dots_kernel<FMT_Q6_K><<<grid, 256, 0, s>>>(w_pack, static_cast<const uint8_t*>(xq), out, M, NB, N);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+}  // namespace qgemv

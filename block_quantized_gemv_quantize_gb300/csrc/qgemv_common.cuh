@@ -1,0 +1,324 @@
+// Shared device-side definitions of the GB300 small-M block-quantized GEMV
+// library: packed weight layouts, the Q8_1 block, the shared-memory
+// activation tile, integer block dots and the top-1 key.
+//
+// The pages ("Qwen3.6 27B Q4_0 DFlash/SYCL closure", "Q6_K M=6 fused DFlash
+// top-1 production record", "Qwen3.6 27B B70 follow-up: Q8 activation cache")
+// name Q4_0, Q6_K and Q8_1 but do not define their bytes; the definitions used
+// are the llama.cpp-family ones:
+//   Q8_1  per 32 activations: fp16 d, fp16 s = d * sum(q), int8 q[32]   (36 B)
+//   Q4_0  per 32 weights:     fp16 d, 4-bit q, value d * (q - 8)         (18 B)
+//   Q6_K  per 256 weights:    fp16 d, int8 sc[16], 6-bit q,
+//                             value d * sc[i / 16] * (q - 32)           (210 B)
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qgemv {
+
+constexpr int QK = 32;              // values per Q8_1 / Q4_0 block
+constexpr int QK_K = 256;           // values per Q6_K superblock
+constexpr int Q8_1_BYTES = 36;
+constexpr int Q4_0_BYTES = 18;
+constexpr int Q6_K_BYTES = 210;
+constexpr int MAX_M = 17;
+
+// ---------------------------------------------------------------------------
+// Packed weight layouts (same total bytes as the canonical blocks).
+//
+// Q4_0 pack, for N rows of K/32 blocks (NB = K/32), two streams:
+//   nib[N*NB]  16 B each: the canonical qs[16] bytes of block (n, b) unchanged
+//              (value i < 16 = low nibble of byte i, value i + 16 = high nibble)
+//   d  [N*NB]  fp16 bits of the block scale, copied raw
+// stream offsets: nib at 0, d at N*NB*16.
+//
+// Q6_K pack, per 32-value block (n, b), four streams:
+//   ql[N*NB]   16 B: byte t = low4(q[t]) | low4(q[t + 16]) << 4
+//   qh[N*NB]    8 B: byte t, bits 2s..2s+1 = high2(q[t + 8 s]), s = 0..3
+//   sc[N*NB]    2 B: the two int8 subscales of the block's 16-value halves
+//   d [N*NSB]  fp16 bits of the superblock scale (NSB = K/256), copied raw
+// stream offsets: ql at 0, qh at N*NB*16, sc at N*NB*24, d at N*NB*26.
+// With these layouts, 32 consecutive blocks of one row are 512 contiguous bytes
+// of nib / ql, so a warp whose lanes take consecutive blocks issues fully
+// coalesced 16-byte loads.
+// ---------------------------------------------------------------------------
+
+struct PackQ40 {
+    const uint4* nib;
+    const __half* d;
+};
+
+struct PackQ6K {
+    const uint4* ql;
+    const uint2* qh;
+    const uint16_t* sc;
+    const __half* d;
+};
+
+__host__ __device__ inline PackQ40 pack_q4_0(const void* base, int64_t N, int NB)
+{
+    const char* p = static_cast<const char*>(base);
+    PackQ40 r;
+    r.nib = reinterpret_cast<const uint4*>(p);
+    r.d = reinterpret_cast<const __half*>(p + N * NB * 16);
+    return r;
+}
+
+__host__ __device__ inline PackQ6K pack_q6_k(const void* base, int64_t N, int NB)
+{
+    const char* p = static_cast<const char*>(base);
+    PackQ6K r;
+    r.ql = reinterpret_cast<const uint4*>(p);
+    r.qh = reinterpret_cast<const uint2*>(p + N * NB * 16);
+    r.sc = reinterpret_cast<const uint16_t*>(p + N * NB * 24);
+    r.d = reinterpret_cast<const __half*>(p + N * NB * 26);
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Loads
+// ---------------------------------------------------------------------------
+
+// Streaming read-only 16-byte load: weights are read exactly once, so keep
+// them out of L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const uint2* p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p)
+{
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// ---------------------------------------------------------------------------
+// Q8_1 quantization of one 32-value block by one warp: lane i holds x_i.
+// d = max|x| / 127 (IEEE fp32 divide), q_i = round(x_i / d) with round half
+// away from zero; an all-zero block gives d = 0 and q = 0.  The stored scale is
+// the fp16 rounding (nearest even) of d; x is divided by the fp32 d.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_max_f32(float v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_i32(int v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sum over the 16 lanes of this lane's half-warp.
+__device__ __forceinline__ int halfwarp_sum_i32(int v)
+{
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+struct Q81Lane {
+    int q;      // this lane's code
+    float d;    // fp32 scale of the block (before fp16 rounding)
+};
+
+__device__ __forceinline__ Q81Lane q8_1_quantize_lane(float x)
+{
+    float amax = warp_max_f32(fabsf(x));
+    Q81Lane r;
+    r.d = __fdiv_rn(amax, 127.0f);
+    int q = 0;
+    if (amax != 0.0f) {
+        q = (int)roundf(__fdiv_rn(x, r.d));
+        q = max(-127, min(127, q));
+    }
+    r.q = q;
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory activation tile (one CTA, a chunk of KC blocks, M rows).
+//   aq  [M][2][KC] uint4 : q bytes 0..15 (h = 0) and 16..31 (h = 1) of block b
+//   am  [M][KC]    uint2 : x = fp32 bits of the block's fp16 scale d_a
+//                          y = Q4_0: -8 * sum(q[0..31])
+//                              Q6_K: sum(q[0..15]) | sum(q[16..31]) << 16 (int16 pair)
+// The integer sums fold the weight offsets (q_w - 8, q_w - 32) into the dot
+// products exactly: sum (q_w - c) q_a = sum q_w q_a - c * sum q_a.
+// Lanes of a warp read consecutive blocks, so the 16-byte reads are
+// bank-conflict free.
+// ---------------------------------------------------------------------------
+
+constexpr int ACT_BYTES_PER_BLOCK = 2 * 16 + 8;  // per (row, block)
+
+enum WeightFormat { FMT_Q4_0 = 0, FMT_Q6_K = 1 };
+
+template <int FMT>
+__device__ __forceinline__ uint32_t act_meta_sums(const uint32_t (&q)[8])
+{
+    int s0 = 0, s1 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s0 = __dp4a((int)q[i], 0x01010101, s0);
+#pragma unroll
+    for (int i = 4; i < 8; ++i) s1 = __dp4a((int)q[i], 0x01010101, s1);
+    if (FMT == FMT_Q4_0) return (uint32_t)(-8 * (s0 + s1));
+    return ((uint32_t)s0 & 0xFFFFu) | ((uint32_t)s1 << 16);
+}
+
+// Read one canonical Q8_1 block from global memory (4-byte aligned) into the
+// tile representation.
+template <int FMT>
+__device__ __forceinline__ void act_from_q8_1(const uint8_t* blk, uint4& lo, uint4& hi, uint2& meta)
+{
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(blk);
+    uint32_t q[8];
+    uint32_t ds = w[0];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = w[1 + i];
+    lo = make_uint4(q[0], q[1], q[2], q[3]);
+    hi = make_uint4(q[4], q[5], q[6], q[7]);
+    float d = __half2float(__ushort_as_half((unsigned short)(ds & 0xFFFFu)));
+    meta.x = __float_as_uint(d);
+    meta.y = act_meta_sums<FMT>(q);
+}
+
+// ---------------------------------------------------------------------------
+// Integer block dots.  All sums are exact in int32.
+// ---------------------------------------------------------------------------
+
+// Q4_0: the 8 words of codes (value order matching the activation words):
+// word i < 4 = low nibbles of nib word i, word i + 4 = high nibbles.
+__device__ __forceinline__ void q4_0_unpack(const uint4 nib, uint32_t (&w)[8])
+{
+    const uint32_t m = 0x0F0F0F0Fu;
+    w[0] = nib.x & m;
+    w[1] = nib.y & m;
+    w[2] = nib.z & m;
+    w[3] = nib.w & m;
+    w[4] = (nib.x >> 4) & m;
+    w[5] = (nib.y >> 4) & m;
+    w[6] = (nib.z >> 4) & m;
+    w[7] = (nib.w >> 4) & m;
+}
+
+// I = sum_i (q_w - 8) * q_a, starting from init = -8 * sum(q_a) + bias.
+__device__ __forceinline__ int q4_0_dot(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, int init)
+{
+    int s = init;
+    s = __dp4a((int)w[0], (int)lo.x, s);
+    s = __dp4a((int)w[1], (int)lo.y, s);
+    s = __dp4a((int)w[2], (int)lo.z, s);
+    s = __dp4a((int)w[3], (int)lo.w, s);
+    s = __dp4a((int)w[4], (int)hi.x, s);
+    s = __dp4a((int)w[5], (int)hi.y, s);
+    s = __dp4a((int)w[6], (int)hi.z, s);
+    s = __dp4a((int)w[7], (int)hi.w, s);
+    return s;
+}
+
+// Q6_K: the 8 words of 6-bit codes of one packed 32-value block, value order
+// 4i .. 4i+3 in word i.
+__device__ __forceinline__ void q6_k_unpack(const uint4 ql, const uint2 qh, uint32_t (&w)[8])
+{
+    const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x30303030u;
+    w[0] = (ql.x & m4) | ((qh.x << 4) & m2);
+    w[1] = (ql.y & m4) | ((qh.y << 4) & m2);
+    w[2] = (ql.z & m4) | ((qh.x << 2) & m2);
+    w[3] = (ql.w & m4) | ((qh.y << 2) & m2);
+    w[4] = ((ql.x >> 4) & m4) | (qh.x & m2);
+    w[5] = ((ql.y >> 4) & m4) | (qh.y & m2);
+    w[6] = ((ql.z >> 4) & m4) | ((qh.x >> 2) & m2);
+    w[7] = ((ql.w >> 4) & m4) | ((qh.y >> 2) & m2);
+}
+
+// J = sc0 * sum_{i<16} (q - 32) q_a + sc1 * sum_{i>=16} (q - 32) q_a.
+// sums = sum(q_a[0..15]) | sum(q_a[16..31]) << 16; sc2 = the two int8 subscales.
+__device__ __forceinline__ int q6_k_dot(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, uint32_t sums,
+                                        uint32_t sc2)
+{
+    int g0 = -32 * (int)(int16_t)(sums & 0xFFFFu);
+    int g1 = -32 * (int)(int16_t)(sums >> 16);
+    g0 = __dp4a((int)w[0], (int)lo.x, g0);
+    g0 = __dp4a((int)w[1], (int)lo.y, g0);
+    g0 = __dp4a((int)w[2], (int)lo.z, g0);
+    g0 = __dp4a((int)w[3], (int)lo.w, g0);
+    g1 = __dp4a((int)w[4], (int)hi.x, g1);
+    g1 = __dp4a((int)w[5], (int)hi.y, g1);
+    g1 = __dp4a((int)w[6], (int)hi.z, g1);
+    g1 = __dp4a((int)w[7], (int)hi.w, g1);
+    int sc0 = (int)(int8_t)(sc2 & 0xFFu);
+    int sc1 = (int)(int8_t)(sc2 >> 8);
+    return sc0 * g0 + sc1 * g1;
+}
+
+// Exact int -> float for |i| < 2^22 without a conversion instruction: the
+// integer is added to the bit pattern of 1.5 * 2^23, whose unit in the last
+// place is 1.  Used by the Q4_0 path, where |I| <= 32 * 8 * 127.
+constexpr int MAGIC_I2F_BITS = 0x4B400000;
+constexpr float MAGIC_I2F = 12582912.0f;
+
+// ---------------------------------------------------------------------------
+// Top-1 key: orders (value, index) pairs so that a 64-bit max picks the
+// largest value and, among exactly equal values, the lowest index.  -0 and +0
+// are the same value; NaN maps to 0 and so never wins; when every value of a
+// row is NaN the result is index 0.  ("Q6_K M=6 fused DFlash top-1 production
+// record", Exactness and safety contracts, item 3: lowest-token-ID
+// finite-tie contract shared by the fused reducer and the generic argmax.)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long top1_key(float v, int n)
+{
+    if (v != v) return 0ull;
+    uint32_t u = (v == 0.0f) ? 0u : __float_as_uint(v);
+    uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
+}
+
+__host__ __device__ inline int top1_key_to_id(unsigned long long k)
+{
+    return k == 0ull ? 0 : (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        unsigned long long t = __shfl_xor_sync(0xffffffffu, v, o);
+        v = t > v ? t : v;
+    }
+    return v;
+}
+
+// Cross-CTA top-1 workspace: M 64-bit keys, then a CTA completion counter.
+// Every call leaves it zeroed again (the last CTA resets it).
+struct Top1Workspace {
+    unsigned long long keys[MAX_M];
+    unsigned int done;
+    unsigned int pad;
+};
+
+}  // namespace qgemv

@@ -1,0 +1,173 @@
+/*
+ * qgemv.h - C ABI of the GB300 small-M block-quantized GEMV library.
+ *
+ * Computes, for M = 1..17 activation rows (a width-6 speculative verifier uses
+ * 6; the fused draft head uses rows 1..5), llama.cpp-family block-quantized
+ * matrix-vector products against activations quantized on the fly to Q8_1,
+ * and a fused LM-head that reduces each row to its greedy token id without
+ * writing logits.  The pages this follows:
+ *   [closure]  "Qwen3.6 27B Q4_0 DFlash/SYCL closure"
+ *   [record]   "Q6_K M=6 fused DFlash top-1 production record"
+ *   [q8cache]  "Qwen3.6 27B B70 follow-up: Q8 activation cache..."
+ *
+ * Block formats (named on the pages, defined here as in llama.cpp):
+ *   Q8_1  32 activations: fp16 d, fp16 s = d * sum(q), int8 q[32]      36 B
+ *         d = max|x| / 127 (fp32), q = round(x / d) half away from zero,
+ *         all-zero block -> d = s = 0, q = 0.
+ *   Q4_0  32 weights: fp16 d, uint8 qs[16]; value i < 16 is the low nibble
+ *         of qs[i], value i + 16 the high nibble; w = d * (q - 8)      18 B
+ *   Q6_K  256 weights: uint8 ql[128], uint8 qh[64], int8 sc[16], fp16 d;
+ *         low 4 bits of value i = nibble (i & 1) of ql[i >> 1], high 2 bits
+ *         = bits 2 (i & 3) of qh[i >> 2]; w = d * sc[i >> 4] * (q - 32) 210 B
+ * All multi-byte fields are little endian.
+ *
+ * Conventions for every call:
+ *   - Pointers named w_*, x, xq, y, ids, workspace are DEVICE pointers and
+ *     must be 16-byte aligned; the caller allocates and owns all of them.
+ *     The library allocates no memory and never synchronizes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream); all work is enqueued on it, in order.
+ *   - Arguments are validated on the host before anything is enqueued; on
+ *     error nothing is enqueued and a negative status is returned.  Device
+ *     faults surface at the caller's next synchronization.
+ *   - Matrices are row-major: a weight is N rows of K values (K contiguous,
+ *     the ggml [K, N] tensor); activations are M rows of K values with row
+ *     stride ldx (in elements); outputs y are M rows of N values with row
+ *     stride ldy, i.e. y[m * ldy + n] (the ggml [N, M] output).
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define QGEMV_OK 0
+#define QGEMV_INVALID_ARG (-1)        /* null pointer, M/K/N/ld out of range  */
+#define QGEMV_UNSUPPORTED_SHAPE (-2)  /* M > 17, K not a multiple of the block */
+#define QGEMV_MISALIGNED (-3)         /* a pointer is not 16-byte aligned      */
+#define QGEMV_WORKSPACE_TOO_SMALL (-4)
+#define QGEMV_CUDA_ERROR (-5)         /* a CUDA call or launch failed          */
+
+#define QGEMV_MAX_M 17
+
+/* Human-readable text for a status code (static storage). */
+const char* qgemv_status_string(int status);
+
+/* ---- sizes (host-only, no CUDA call) ---------------------------------- */
+
+/* Bytes of the Q8_1 activation for M rows of K values: M * (K/32) * 36. */
+size_t q8_1_bytes(int M, int K);
+/* Bytes of a packed Q4_0 weight of N rows of K values: N * (K/32) * 18
+ * (the canonical size; the pack only reorders bytes). */
+size_t q4_0_pack_bytes(int N, int K);
+/* Bytes of a packed Q6_K weight: N * (K/256) * 210 (the canonical size). */
+size_t q6_k_pack_bytes(int N, int K);
+/* Workspace bytes of lmhead_q6_k_top1 and argmax_f32_rows (a few hundred). */
+size_t lmhead_q6_k_top1_workspace_bytes(int M, int K, int N);
+size_t argmax_f32_rows_workspace_bytes(int M, int N);
+
+/* ---- A1: activation quantizer ----------------------------------------- */
+
+/* quantize_q8_1 - quantize M rows of K fp32 activations to Q8_1 blocks.
+ * [q8cache] "Q8_1 activation cache prototype": the activation is quantized
+ * once and the same Q8_1 copy feeds sibling matmuls (gate and up).
+ *   x   fp32 [M][ldx] device, ldx >= K      (read)
+ *   xq  uint8 [M][K/32][36] device           (written; q8_1_bytes(M, K))
+ *   1 <= M <= 17, K % 32 == 0, K >= 32.
+ * The output is caller-owned and may be passed to any number of qgemv_*
+ * calls. */
+int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* stream);
+
+/* ---- A2: weight repackers (offline) ------------------------------------ */
+
+/* qpack_q4_0 - reorder canonical Q4_0 blocks into the kernel's coalesced
+ * streams (a nibble stream of 16-byte blocks, then the fp16 scales; raw
+ * bits, same total size).  [closure] "What materially worked" item 3
+ * (offline-packed projections) and "Transfer" rule 7 (copy fp16 storage
+ * bits, never convert them).
+ *   w_canon  uint8 [N][K/32][18] device   (read)
+ *   w_pack   q4_0_pack_bytes(N, K) device (written; must not alias w_canon)
+ *   N >= 1, K % 32 == 0. */
+int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream);
+
+/* qpack_q6_k - reorder canonical Q6_K superblocks into four streams (low
+ * nibbles, high bit pairs, subscales, fp16 scales; raw bits, same size).
+ * [record] "Why this was slow" (the Q6_K output tensor is packed once).
+ *   w_canon  uint8 [N][K/256][210] device (read)
+ *   w_pack   q6_k_pack_bytes(N, K) device (written; must not alias w_canon)
+ *   N >= 1, K % 256 == 0. */
+int qpack_q6_k(const void* w_canon, void* w_pack, int N, int K, void* stream);
+
+/* ---- A3 / A4: small-M MMVQ ---------------------------------------------- */
+
+/* qgemv_q4_0 - y[m][n] = sum_b d_w[n,b] * d_a[m,b] * sum_i (q_w - 8) q_a,
+ * integer block dots exact, fp32 accumulation.  Each weight byte is read
+ * from HBM once and reused for all M rows.  [closure] "What materially
+ * worked" item 2 (direct Q4_0 MMVQ for rows 1..17 removed repeated
+ * full-weight reads).
+ *   w_pack  packed Q4_0 (qpack_q4_0) of N rows of K values (read)
+ *   xq      Q8_1 [M][K/32] from quantize_q8_1 (read)
+ *   y       fp32, y[m * ldy + n] for n < N (written), ldy >= N
+ *   1 <= M <= 17, K % 32 == 0, N >= 1. */
+int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
+
+/* qgemv_q6_k - y[m][n] = sum_b d6[n] * d_a[m,b] * sum_{half j of b} sc_j *
+ * sum_i (q - 32) q_a.  [record] "Why this was slow" (the MMVQ part of the
+ * fused head: each weight slice reused across all rows).
+ *   w_pack  packed Q6_K (qpack_q6_k); xq, y, ldy as qgemv_q4_0;
+ *   1 <= M <= 17, K % 256 == 0, N >= 1. */
+int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
+
+/* ---- A5: fused LM-head top-1 -------------------------------------------- */
+
+/* lmhead_q6_k_top1 - for each of M fp32 rows of x: quantize to Q8_1, project
+ * through the Q6_K weight, and write the greedy token id (lowest id among
+ * exactly equal maxima; -0 == +0; NaN never wins; a row of all NaN gives 0)
+ * to ids[m].  No logits are written.  [record] "Outcome" and "Why this was
+ * slow" (rows 1..5 only, reduced to five ids on device) and "Exactness and
+ * safety contracts" item 3 (lowest-token-ID finite-tie contract).
+ *   w_pack     packed Q6_K of N rows of K values (read)
+ *   x          fp32 [M][ldx], ldx >= K (read); pass row 1 of a [6][K] block
+ *              with M = 5 for the rows-1..5 view
+ *   ids        int32 [M] (written)
+ *   workspace  lmhead_q6_k_top1_workspace_bytes(M, K, N) bytes, zero-filled
+ *              before its first use; every call leaves it zero-filled again.
+ *              Calls that share a workspace must not overlap in time.
+ *   1 <= M <= 17, K % 256 == 0, N >= 1. */
+int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* ids, void* workspace,
+                     size_t ws_bytes, int M, int K, int N, void* stream);
+
+/* ---- A6: row argmax (the unfused control) -------------------------------- */
+
+/* argmax_f32_rows - ids[m] = lowest n attaining max_n y[m * ldy + n], with the
+ * same tie contract as lmhead_q6_k_top1.  [record] "Why this was slow" (the
+ * separate argmax of the unfused path) and "Exactness and safety contracts"
+ * item 3.
+ *   y          fp32 [M][ldy] (read), ldy >= N
+ *   ids        int32 [M] (written)
+ *   workspace  argmax_f32_rows_workspace_bytes(M, N), same contract as above
+ *   1 <= M <= 17, N >= 1. */
+int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, size_t ws_bytes, int M, int N,
+                    void* stream);
+
+/* ---- checking aid --------------------------------------------------------- */
+
+/* qgemv_block_dots_q4_0 / _q6_k - out[(m * N + n) * (K/32) + b] = the exact
+ * int32 dot of weight block (n, b) with activation block (m, b), computed by
+ * the same unpack and dot routines the MMVQ kernels use (Q4_0: sum (q-8) q_a;
+ * Q6_K: sum over the two halves of sc * sum (q-32) q_a).  For checking the
+ * integer part bit for bit; not a fast path.
+ *   out  int32 [M][N][K/32] device (written). */
+int qgemv_block_dots_q4_0(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream);
+int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

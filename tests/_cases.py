@@ -1,0 +1,118 @@
+"""Test helpers: the documented pack layouts undone on the CPU, the parity
+gates, and the adversarial top-1 inputs.  Test code only."""
+from __future__ import annotations
+
+import numpy as np
+
+# ---------------------------------------------------------------- pack layouts (inverse, numpy)
+
+
+def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Packed Q4_0 bytes -> canonical [N, K/32, 18]: a 16-byte nibble stream
+    followed by a stream of fp16 scales."""
+    nb = K // 32
+    nib = pack[: N * nb * 16].reshape(N, nb, 16)
+    d = pack[N * nb * 16: N * nb * 18].reshape(N, nb, 2)
+    return np.concatenate([d, nib], axis=2)
+
+
+def unpack_q6_k(pack: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Packed Q6_K bytes -> canonical [N, K/256, 210].
+
+    Per 32-value block: ql byte t = low4(q[t]) | low4(q[t+16]) << 4;
+    qh byte t, bits 2s = high2(q[t + 8 s]); sc = the block's two subscales;
+    then one fp16 scale per superblock."""
+    nb, ns = K // 32, K // 256
+    nblk = N * nb
+    ql = pack[: nblk * 16].reshape(nblk, 16).astype(np.int64)
+    qh = pack[nblk * 16: nblk * 24].reshape(nblk, 8).astype(np.int64)
+    sc = pack[nblk * 24: nblk * 26].reshape(N, ns, 16)
+    d = pack[nblk * 26: nblk * 26 + N * ns * 2].reshape(N, ns, 2)
+    q = np.zeros((nblk, 32), dtype=np.int64)
+    q[:, 0:16] = ql & 0x0F
+    q[:, 16:32] = ql >> 4
+    for s in range(4):
+        q[:, 8 * s: 8 * s + 8] |= ((qh >> (2 * s)) & 3) << 4
+    q = q.reshape(N, ns, 256)
+    canon = np.zeros((N, ns, 210), dtype=np.uint8)
+    lo = (q & 0x0F).reshape(N, ns, 128, 2)
+    canon[:, :, 0:128] = (lo[..., 0] | (lo[..., 1] << 4)).astype(np.uint8)
+    hi = (q >> 4).reshape(N, ns, 64, 4)
+    canon[:, :, 128:192] = (hi[..., 0] | (hi[..., 1] << 2) | (hi[..., 2] << 4) | (hi[..., 3] << 6)).astype(np.uint8)
+    canon[:, :, 192:208] = sc
+    canon[:, :, 208:210] = d
+    return canon
+
+
+def q6_k_from_codes(codes: np.ndarray, sc: np.ndarray, d16_bits: np.ndarray) -> np.ndarray:
+    """Canonical Q6_K bytes from codes [N, K] (0..63), subscales [N, K/16]
+    (int8) and fp16 scale bits [N, K/256]."""
+    N, K = codes.shape
+    ns = K // 256
+    q = codes.reshape(N, ns, 256).astype(np.int64)
+    out = np.zeros((N, ns, 210), dtype=np.uint8)
+    lo = (q & 0x0F).reshape(N, ns, 128, 2)
+    out[:, :, 0:128] = (lo[..., 0] | (lo[..., 1] << 4)).astype(np.uint8)
+    hi = (q >> 4).reshape(N, ns, 64, 4)
+    out[:, :, 128:192] = (hi[..., 0] | (hi[..., 1] << 2) | (hi[..., 2] << 4) | (hi[..., 3] << 6)).astype(np.uint8)
+    out[:, :, 192:208] = sc.reshape(N, ns, 16).astype(np.int8).view(np.uint8)
+    out[:, :, 208:210] = np.asarray(d16_bits, dtype=np.uint16).reshape(N, ns, 1).view(np.uint8)
+    return out
+
+
+# ---------------------------------------------------------------- gates
+
+REL_TOL = 1e-5   # fp32 outputs: |err| <= 1e-5 * max(|y_oracle|, S)
+TOP1_TOL = 1e-4  # top-1: exact where the oracle gap exceeds 1e-4 * |top1|
+
+
+def check_close(y: np.ndarray, y_ref: np.ndarray, S: np.ndarray, rel: float = REL_TOL) -> dict:
+    """Parity gate for fp32 outputs against the fp64 oracle.  The error of an
+    fp32 accumulation scales with S = sum_b |d_w d_a I_b|, so the gate is
+    |err| <= rel * max(|y_ref|, S); the literal per-output relative error is
+    reported too."""
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - y_ref)
+    bound = rel * np.maximum(np.abs(y_ref), S)
+    bad = err > bound
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lit = np.where(y_ref != 0, err / np.abs(y_ref), np.where(err == 0, 0.0, np.inf))
+    return dict(ok=not bad.any(), n_bad=int(bad.sum()), max_err_over_S=float((err / np.maximum(S, 1e-300)).max()),
+                max_literal_rel=float(lit.max()), n_literal_over=int((err > rel * np.abs(y_ref)).sum()),
+                n=int(y.size))
+
+
+def check_top1(ids, y_ref: np.ndarray, tol: float = TOP1_TOL) -> list[str]:
+    """Rule: the id must equal the oracle's where the oracle's top-2 gap exceeds
+    tol * |top1|; otherwise any id whose oracle value is within tol * |top1| of
+    the maximum is accepted.  Returns a list of violations."""
+    ids = np.asarray(ids)
+    errs = []
+    for m in range(y_ref.shape[0]):
+        row = y_ref[m]
+        order = np.argsort(-row, kind="stable")
+        top1 = row[order[0]]
+        top2 = row[order[1]] if row.size > 1 else -np.inf
+        best = int(np.flatnonzero(row == top1)[0])
+        if top1 - top2 > tol * abs(top1):
+            if int(ids[m]) != best:
+                errs.append(f"row {m}: id {int(ids[m])} != oracle {best} (gap {top1 - top2:.3g})")
+        else:
+            if not (0 <= int(ids[m]) < row.size) or row[int(ids[m])] < top1 - tol * abs(top1):
+                errs.append(f"row {m}: id {int(ids[m])} not within tolerance of the max")
+    return errs
+
+
+# ---------------------------------------------------------------- adversarial top-1
+
+
+def winner_q6_k_row(x_rows: np.ndarray) -> np.ndarray:
+    """A Q6_K row that scores far above random rows for every row of x: the
+    sign pattern of v = sum_m x_m / |x_m| at the largest codes, subscales and
+    scale the workload's distributions allow (q in {1, 63}, sc = 63, d = 1e-3)."""
+    K = x_rows.shape[1]
+    v = (x_rows / np.linalg.norm(x_rows, axis=1, keepdims=True)).sum(axis=0)
+    codes = np.where(v >= 0, 63, 1).reshape(1, K)
+    sc = np.full((1, K // 16), 63, dtype=np.int8)
+    d = np.array([[1e-3] * (K // 256)], dtype=np.float32).astype(np.float16).view(np.uint16)
+    return q6_k_from_codes(codes, sc, d)[0]

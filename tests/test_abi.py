@@ -1,0 +1,87 @@
+"""The C-ABI library loads and exports every symbol include/qgemv.h declares;
+host-only calls (sizes, status strings, argument validation that rejects
+before any CUDA call) behave as documented.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_quantized_gemv_quantize_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+\**([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("quantize_q8_1", "qgemv_q4_0", "qgemv_q6_k", "lmhead_q6_k_top1", "qpack_q4_0", "qpack_q6_k",
+                     "argmax_f32_rows", "q8_1_bytes", "q4_0_pack_bytes", "q6_k_pack_bytes",
+                     "lmhead_q6_k_top1_workspace_bytes", "qgemv_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_cover_the_header():
+    from block_quantized_gemv_quantize_gb300 import _lib
+
+    assert set(declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_sizes(lib):
+    lib.q8_1_bytes.restype = ctypes.c_size_t
+    lib.q4_0_pack_bytes.restype = ctypes.c_size_t
+    lib.q6_k_pack_bytes.restype = ctypes.c_size_t
+    assert lib.q8_1_bytes(6, 5120) == 6 * 160 * 36 == 34560
+    assert lib.q8_1_bytes(6, 17408) == 117504
+    assert lib.q8_1_bytes(5, 5120) == 28800
+    assert lib.q4_0_pack_bytes(17408, 5120) == 50135040
+    assert lib.q4_0_pack_bytes(5120, 17408) == 50135040
+    assert lib.q4_0_pack_bytes(248320, 5120) == 715161600
+    assert lib.q6_k_pack_bytes(248320, 5120) == 1042944000
+    assert lib.q6_k_pack_bytes(5120, 5120) == 21504000
+
+
+def test_status_strings(lib):
+    lib.qgemv_status_string.restype = ctypes.c_char_p
+    for s in (0, -1, -2, -3, -4, -5):
+        assert lib.qgemv_status_string(s).decode() != "unknown status"
+    assert lib.qgemv_status_string(7).decode() == "unknown status"
+
+
+def test_validation_rejects_before_any_cuda_call(lib):
+    P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.qgemv_q4_0.argtypes = [P, P, P, L, I, I, I, P]
+    lib.quantize_q8_1.argtypes = [P, L, P, I, I, P]
+    lib.lmhead_q6_k_top1.argtypes = [P, P, L, P, P, ctypes.c_size_t, I, I, I, P]
+    fake = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+    odd = 0x10008
+    assert lib.qgemv_q4_0(None, fake, fake, 10, 6, 64, 10, None) == -1
+    assert lib.qgemv_q4_0(fake, fake, fake, 10, 0, 64, 10, None) == -1
+    assert lib.qgemv_q4_0(fake, fake, fake, 10, 18, 64, 10, None) == -2
+    assert lib.qgemv_q4_0(fake, fake, fake, 10, 6, 48, 10, None) == -2
+    assert lib.qgemv_q4_0(fake, fake, fake, 9, 6, 64, 10, None) == -1
+    assert lib.qgemv_q4_0(fake, fake, fake, 10, 6, 64, 0, None) == -1
+    assert lib.qgemv_q4_0(odd, fake, fake, 10, 6, 64, 10, None) == -3
+    assert lib.quantize_q8_1(fake, 31, fake, 1, 32, None) == -1
+    assert lib.quantize_q8_1(fake, 32, odd, 1, 32, None) == -3
+    assert lib.lmhead_q6_k_top1(fake, fake, 512, fake, fake, 8, 5, 512, 100, None) == -4
+    assert lib.lmhead_q6_k_top1(fake, fake, 512, fake, fake, 4096, 5, 320, 100, None) == -2

@@ -1,0 +1,186 @@
+"""Parity at the full workload sizes the benchmark times (same launch
+configuration: the library picks it from M, K, N), against the CPU oracle.
+
+  * width-6 verifier MMVQ, Q4_0: gate/up M=6 K=5120 N=17408, down M=6 K=17408
+    N=5120 (1% outlier channels x20) -- every output checked;
+  * fused Q6_K LM-head top-1, K=5120 N=248320, rows 1..5 of a [6, 5120] block
+    -- ids against the full oracle, and against the unfused path;
+  * M sweep {1,2,4,6,9,12,17} for Q4_0 and Q6_K at K=5120, N in {5120, 17408,
+    248320} -- sampled rows (first 64, last 64 and 1024 random rows);
+  * adversarial top-1 at K=5120 N=248320 M=5: all-zero weights, planted exact
+    ties at (1,256), (255,256), (0,248319), a planted near tie.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+import oracle  # noqa: E402
+from block_quantized_gemv_quantize_gb300 import synth  # noqa: E402
+
+from . import _cases as C  # noqa: E402
+
+DEV = "cuda:0"
+K_H, N_V = 5120, 248320
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_quantized_gemv_quantize_gb300 import build
+
+    build.build()
+    from block_quantized_gemv_quantize_gb300 import ops as o
+
+    return o
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _np(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["verifier_gate_up", "verifier_down"])
+def test_verifier_mmvq_full(ops, name):
+    c = synth.WORKLOADS[name]
+    M, K, N = c["M"], c["K"], c["N"]
+    w = synth.q4_0_weights(N, K, seed=c["seed"])
+    x = synth.activations(M, K, seed=c["seed"] + 100, outlier_frac=c["outlier_frac"])
+    xq_ref = oracle.quantize_q8_1(x)
+    y_ref, S = oracle.qgemv_q4_0(w, xq_ref)
+    xq = ops.quantize_q8_1(_t(x))
+    assert np.array_equal(_np(xq).reshape(xq_ref.shape), xq_ref)
+    y = _np(ops.qgemv_q4_0(ops.qpack_q4_0(_t(w), N, K), xq, M, K, N))
+    r = C.check_close(y, y_ref, S)
+    print(name, r)
+    assert r["ok"], r
+
+
+@pytest.fixture(scope="module")
+def vocab(ops):
+    c = synth.WORKLOADS["lmhead_q6_k"]
+    w = synth.q6_k_weights(N_V, K_H, seed=c["seed"])
+    x6 = synth.activations(6, K_H, seed=c["seed"] + 100)
+    wd = _t(w)
+    wp = ops.qpack_q6_k(wd, N_V, K_H)
+    torch.cuda.synchronize()
+    y_ref, S = oracle.qgemv_q6_k(w, oracle.quantize_q8_1(x6[1:6]))
+    return dict(w=w, x6=x6, wd=wd, wp=wp, y_ref=y_ref, S=S)
+
+
+def test_lmhead_top1_full(ops, vocab):
+    x6d = _t(vocab["x6"])
+    ids = _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V))
+    assert C.check_top1(ids, vocab["y_ref"]) == []
+    # unfused: full logits, then argmax; same ids, and the logits pass the gate
+    y = ops.qgemv_q6_k(vocab["wp"], ops.quantize_q8_1(x6d[1:6]), 5, K_H, N_V)
+    assert _np(ops.argmax_f32_rows(y)).tolist() == ids.tolist()
+    r = C.check_close(_np(y), vocab["y_ref"], vocab["S"])
+    print("lmhead logits", r)
+    assert r["ok"], r
+    # repeatable (workspace reset, order-independent reduction)
+    assert _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V)).tolist() == ids.tolist()
+
+
+def _sample_rows(N, seed=0):
+    g = np.random.default_rng(seed)
+    return np.unique(np.concatenate([np.arange(min(64, N)), np.arange(max(0, N - 64), N),
+                                     g.choice(N, size=min(1024, N), replace=False)]))
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q6_k"])
+@pytest.mark.parametrize("N", [5120, 17408, 248320])
+def test_m_sweep_sampled(ops, fmt, N):
+    K = K_H
+    w = synth.q4_0_weights(N, K, seed=N + 1) if fmt == "q4_0" else synth.q6_k_weights(N, K, seed=N + 2)
+    wp = ops.qpack_q4_0(_t(w), N, K) if fmt == "q4_0" else ops.qpack_q6_k(_t(w), N, K)
+    rows = _sample_rows(N)
+    for M in (1, 2, 4, 6, 9, 12, 17):
+        x = synth.activations(M, K, seed=1000 + M, outlier_frac=0.01)
+        xq_ref = oracle.quantize_q8_1(x)
+        xq = ops.quantize_q8_1(_t(x))
+        y = _np((ops.qgemv_q4_0 if fmt == "q4_0" else ops.qgemv_q6_k)(wp, xq, M, K, N))
+        f = oracle.qgemv_q4_0 if fmt == "q4_0" else oracle.qgemv_q6_k
+        y_ref, S = f(w[rows], xq_ref)
+        r = C.check_close(y[:, rows], y_ref, S)
+        assert r["ok"], (M, r)
+    del wp
+    torch.cuda.empty_cache()
+
+
+def _set_rows(ops, vocab, rows, data):
+    """Overwrite canonical rows on the device and re-pack the whole weight."""
+    for r, d in zip(rows, data):
+        vocab["wd"][r] = _t(d)
+    ops.qpack_q6_k(vocab["wd"], N_V, K_H, out=vocab["wp"])
+
+
+def test_adversarial_all_zero_weights(ops):
+    w = torch.zeros((N_V, K_H // 256, 210), dtype=torch.uint8, device=DEV)
+    wp = ops.qpack_q6_k(w, N_V, K_H)
+    x = _t(synth.activations(6, K_H, seed=5))
+    assert _np(ops.lmhead_q6_k_top1(wp, x[1:6], K_H, N_V)).tolist() == [0] * 5
+    y = ops.qgemv_q6_k(wp, ops.quantize_q8_1(x[1:6]), 5, K_H, N_V)
+    assert _np(ops.argmax_f32_rows(y)).tolist() == [0] * 5
+
+
+@pytest.mark.parametrize("pair", [(1, 256), (255, 256), (0, 248319)])
+def test_adversarial_planted_ties(ops, vocab, pair):
+    x5 = vocab["x6"][1:6]
+    win = C.winner_q6_k_row(x5)
+    yw, _ = oracle.qgemv_q6_k(win.reshape(1, -1, 210), oracle.quantize_q8_1(x5))
+    others = np.delete(vocab["y_ref"], list(pair), axis=1).max(axis=1)
+    assert np.all(yw[:, 0] - others > C.TOP1_TOL * np.abs(yw[:, 0]))  # a clear winner for every row
+    saved = [vocab["w"][p].copy() for p in pair]
+    try:
+        _set_rows(ops, vocab, pair, [win, win])
+        x6d = _t(vocab["x6"])
+        ids = _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V))
+        assert ids.tolist() == [min(pair)] * 5
+        y = ops.qgemv_q6_k(vocab["wp"], ops.quantize_q8_1(x6d[1:6]), 5, K_H, N_V)
+        assert _np(ops.argmax_f32_rows(y)).tolist() == [min(pair)] * 5
+    finally:
+        _set_rows(ops, vocab, pair, saved)
+
+
+def test_adversarial_near_tie(ops, vocab):
+    x5 = vocab["x6"][1:6]
+    xq = oracle.quantize_q8_1(x5)
+    win = C.winner_q6_k_row(x5)
+    # change one code by one step at the channel with the smallest nonzero
+    # activation magnitude over the five rows
+    qa = np.abs(xq[:, :, 4:].view(np.int8).astype(np.int64).reshape(5, -1)).max(axis=0)
+    i = int(np.argmin(np.where(qa > 0, qa, 1 << 20)))
+    codes = np.zeros(K_H, dtype=np.int64)
+    wf = win.reshape(-1)
+    for j in range(K_H):  # decode the winner's codes (sequential packing)
+        sb, t = divmod(j, 256)
+        lo = (int(wf[sb * 210 + (t >> 1)]) >> (4 * (t & 1))) & 0xF
+        hi = (int(wf[sb * 210 + 128 + (t >> 2)]) >> (2 * (t & 3))) & 3
+        codes[j] = lo | (hi << 4)
+    codes[i] += -1 if codes[i] == 63 else 1
+    sc = np.full((1, K_H // 16), 63, dtype=np.int8)
+    d = np.array([[1e-3] * (K_H // 256)], dtype=np.float32).astype(np.float16).view(np.uint16)
+    near = C.q6_k_from_codes(codes.reshape(1, -1), sc, d)[0]
+    pair = (1000, 2000)
+    saved = [vocab["w"][p].copy() for p in pair]
+    try:
+        _set_rows(ops, vocab, pair, [near, win])
+        y_ref = vocab["y_ref"].copy()
+        yp, _ = oracle.qgemv_q6_k(np.stack([near, win]), xq)
+        y_ref[:, list(pair)] = yp
+        gap = np.abs(yp[:, 0] - yp[:, 1]) / np.abs(yp[:, 1])
+        print("planted relative gaps", gap)
+        x6d = _t(vocab["x6"])
+        ids = _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V))
+        assert C.check_top1(ids, y_ref) == []
+        assert set(ids.tolist()) <= set(pair)
+        assert _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V)).tolist() == ids.tolist()
+    finally:
+        _set_rows(ops, vocab, pair, saved)
