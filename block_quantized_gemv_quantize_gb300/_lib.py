@@ -39,6 +39,7 @@ SIGNATURES = {
     "argmax_f32_rows": (_I, [_P, _L, _P, _P, _S, _I, _I, _P]),
     "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
 }
 
 
@@ -216,3 +217,10 @@ def qgemv_block_dots_q6_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int
     _check("qgemv_block_dots_q6_k", LIB.qgemv_block_dots_q6_k(_dev(w_pack, "w_pack"), _dev(xq, "xq"),
                                                               out.data_ptr(), M, K, N, _stream(xq)))
     return out
+
+
+def qgemv_take_wait_timeouts() -> int:
+    """Warps that gave up waiting for a weight copy since the last call (synchronous)."""
+    c = ctypes.c_uint(0)
+    _check("qgemv_take_wait_timeouts", LIB.qgemv_take_wait_timeouts(ctypes.byref(c)))
+    return c.value

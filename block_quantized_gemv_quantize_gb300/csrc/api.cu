@@ -52,8 +52,8 @@ const char* qgemv_status_string(int status)
 }
 
 size_t q8_1_bytes(int M, int K) { return (M < 0 || K < 0) ? 0 : (size_t)M * (size_t)(K / QK) * Q8_1_BYTES; }
-size_t q4_0_pack_bytes(int N, int K) { return (N < 0 || K < 0) ? 0 : (size_t)N * (size_t)(K / QK) * Q4_0_BYTES; }
-size_t q6_k_pack_bytes(int N, int K) { return (N < 0 || K < 0) ? 0 : (size_t)N * (size_t)(K / QK_K) * Q6_K_BYTES; }
+size_t q4_0_pack_bytes(int N, int K) { return (N < 1 || K < QK) ? 0 : (size_t)q4_0_pack_size(N, K); }
+size_t q6_k_pack_bytes(int N, int K) { return (N < 1 || K < QK_K) ? 0 : (size_t)q6_k_pack_size(N, K); }
 size_t lmhead_q6_k_top1_workspace_bytes(int, int, int) { return top1_ws_bytes(); }
 size_t argmax_f32_rows_workspace_bytes(int, int) { return top1_ws_bytes(); }
 
@@ -154,6 +154,13 @@ int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int 
     int st = check_gemv(w_pack, xq, out, N, M, K, N, QK_K);
     if (st) return st;
     return launch_block_dots(FMT_Q6_K, w_pack, xq, out, M, K, N, as_stream(stream));
+}
+
+int qgemv_take_wait_timeouts(unsigned int* count)
+{
+    if (!count) return QGEMV_INVALID_ARG;
+    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead();
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
 }  // extern "C"

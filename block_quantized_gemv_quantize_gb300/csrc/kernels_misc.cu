@@ -22,7 +22,7 @@ DeviceInfo device_info()
 }
 
 // ---------------------------------------------------------------------------
-// quantize_q8_1: one warp per 32-value block ("Qwen3.6 27B B70 follow-up: Q8
+// quantize_q8_1: one thread per 32-value block ("Qwen3.6 27B B70 follow-up: Q8
 // activation cache", Q8_1 activation cache prototype: the activation is
 // quantized once and the Q8_1 copy is reused by sibling matmuls).
 // ---------------------------------------------------------------------------
@@ -30,22 +30,18 @@ DeviceInfo device_info()
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
                                                             uint8_t* __restrict__ xq, int M, int NB)
 {
-    const int lane = threadIdx.x & 31;
     const int64_t nblk = (int64_t)M * NB;
-    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < nblk; i += stride) {
+    const bool vec4 = ((reinterpret_cast<uintptr_t>(x) | ((uintptr_t)ldx * 4)) & 15u) == 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
         const int m = (int)(i / NB), b = (int)(i - (int64_t)m * NB);
-        const float xv = x[(int64_t)m * ldx + (int64_t)b * QK + lane];
-        const Q81Lane r = q8_1_quantize_lane(xv);
-        const int S = warp_sum_i32(r.q);
-        uint8_t* blk = xq + i * Q8_1_BYTES;
-        blk[4 + lane] = (uint8_t)(int8_t)r.q;
-        if (lane == 0) {
-            const __half d16 = __float2half_rn(r.d);
-            const __half s16 = __float2half_rn(__fmul_rn(r.d, (float)S));
-            reinterpret_cast<uint32_t*>(blk)[0] =
-                (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(s16) << 16);
-        }
+        Q81Block qb;
+        q8_1_quantize_block(x + (int64_t)m * ldx + (int64_t)b * QK, vec4, qb);
+        const __half d16 = __float2half_rn(qb.d);
+        const __half s16 = __float2half_rn(__fmul_rn(qb.d, (float)(qb.s_lo + qb.s_hi)));
+        uint32_t* o = reinterpret_cast<uint32_t*>(xq + i * Q8_1_BYTES);  // 4-byte aligned
+        o[0] = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(s16) << 16);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) o[1 + w] = qb.q[w];
     }
 }
 
@@ -55,9 +51,9 @@ int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cu
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     const int NB = K / QK;
     const int64_t nblk = (int64_t)M * NB;
-    int64_t grid = (nblk + 7) / 8;
+    int64_t grid = (nblk + 63) / 64;
     if (grid > (int64_t)di.sms * 8) grid = (int64_t)di.sms * 8;
-    quantize_q8_1_kernel<<<(int)grid, 256, 0, s>>>(x, ldx, static_cast<uint8_t*>(xq), M, NB);
+    quantize_q8_1_kernel<<<(int)grid, 64, 0, s>>>(x, ldx, static_cast<uint8_t*>(xq), M, NB);
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -68,41 +64,49 @@ int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cu
 // an all-zero kernel).
 // ---------------------------------------------------------------------------
 
-__global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int64_t nblocks)
+__global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
 {
-    uint4* nib = reinterpret_cast<uint4*>(pack);
-    uint16_t* dst_d = reinterpret_cast<uint16_t*>(pack + nblocks * 16);
+    const Geom g = geom_q4_0(K);
+    const int64_t nblocks = (int64_t)N * g.NB;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
          i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / g.NB;
+        const int b = (int)(i - n * g.NB);
         const uint16_t* src = reinterpret_cast<const uint16_t*>(canon + i * Q4_0_BYTES);  // 2-byte aligned
         uint32_t q[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) q[k] = (uint32_t)src[1 + 2 * k] | ((uint32_t)src[2 + 2 * k] << 16);
-        nib[i] = make_uint4(q[0], q[1], q[2], q[3]);
-        dst_d[i] = src[0];
+        const BlockAddr ad = block_addr(pack, g, n, b);
+        uint8_t* tile = const_cast<uint8_t*>(ad.tile);
+        reinterpret_cast<uint4*>(tile)[ad.j] = make_uint4(q[0], q[1], q[2], q[3]);
+        reinterpret_cast<uint16_t*>(tile + ad.nb * 16)[ad.j] = src[0];
+        if (ad.j == 0) {  // zero the tile's pad bytes (present only when nb % 8 != 0)
+            for (int p = ad.nb * 18; p < q4_0_tile_bytes(ad.nb); ++p) tile[p] = 0;
+        }
     }
 }
 
-__global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int64_t nblocks)
+__global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
 {
-    uint4* ql = reinterpret_cast<uint4*>(pack);
-    uint2* qh = reinterpret_cast<uint2*>(pack + nblocks * 16);
-    uint16_t* sc = reinterpret_cast<uint16_t*>(pack + nblocks * 24);
-    uint16_t* dd = reinterpret_cast<uint16_t*>(pack + nblocks * 26);
+    const Geom g = geom_q6_k(K);
+    const int64_t nblocks = (int64_t)N * g.NB;
+    uint16_t* dd = reinterpret_cast<uint16_t*>(pack + (int64_t)N * g.row);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t sbi = i >> 3;
-        const int bb = (int)(i & 7);
+        const int64_t n = i / g.NB;
+        const int b = (int)(i - n * g.NB);
+        const int64_t sbi = i >> 3;  // superblock index (n * NSB + b / 8)
+        const int bb = b & 7;
         const uint8_t* sb = canon + sbi * Q6_K_BYTES;
         // canonical sequential packing: low4(q_v) = nibble (v & 1) of ql[v >> 1],
         // high2(q_v) = bits 2 (v & 3) of qh[v >> 2]; this block's values are
-        // v = 32 bb .. 32 bb + 31.
+        // v = 32 bb .. 32 bb + 31 of the superblock.
         uint8_t q[32];
 #pragma unroll
         for (int v = 0; v < 32; ++v) {
-            const int g = 32 * bb + v;
-            const int lo = (sb[g >> 1] >> (4 * (g & 1))) & 0x0F;
-            const int hi = (sb[128 + (g >> 2)] >> (2 * (g & 3))) & 0x03;
+            const int gv = 32 * bb + v;
+            const int lo = (sb[gv >> 1] >> (4 * (gv & 1))) & 0x0F;
+            const int hi = (sb[128 + (gv >> 2)] >> (2 * (gv & 3))) & 0x03;
             q[v] = (uint8_t)(lo | (hi << 4));
         }
         uint32_t wl[4] = {0, 0, 0, 0};
@@ -119,9 +123,12 @@ __global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
             for (int s2 = 0; s2 < 4; ++s2) byte |= (uint32_t)(q[t + 8 * s2] >> 4) << (2 * s2);
             wh[t >> 2] |= byte << (8 * (t & 3));
         }
-        ql[i] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        qh[i] = make_uint2(wh[0], wh[1]);
-        sc[i] = (uint16_t)sb[192 + 2 * bb] | ((uint16_t)sb[192 + 2 * bb + 1] << 8);
+        const BlockAddr ad = block_addr(pack, g, n, b);
+        uint8_t* tile = const_cast<uint8_t*>(ad.tile);
+        reinterpret_cast<uint4*>(tile)[ad.j] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        reinterpret_cast<uint2*>(tile + ad.nb * 16)[ad.j] = make_uint2(wh[0], wh[1]);
+        reinterpret_cast<uint16_t*>(tile + ad.nb * 24)[ad.j] =
+            (uint16_t)sb[192 + 2 * bb] | ((uint16_t)sb[192 + 2 * bb + 1] << 8);
         if (bb == 0) dd[sbi] = (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
     }
 }
@@ -139,7 +146,7 @@ int launch_qpack_q4_0(const void* canon, void* pack, int N, int K, cudaStream_t 
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     const int64_t nblocks = (int64_t)N * (K / QK);
     qpack_q4_0_kernel<<<grid_for(nblocks, 256, di.sms), 256, 0, s>>>(static_cast<const uint8_t*>(canon),
-                                                                     static_cast<uint8_t*>(pack), nblocks);
+                                                                     static_cast<uint8_t*>(pack), N, K);
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -149,7 +156,7 @@ int launch_qpack_q6_k(const void* canon, void* pack, int N, int K, cudaStream_t 
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     const int64_t nblocks = (int64_t)N * (K / QK);
     qpack_q6_k_kernel<<<grid_for(nblocks, 256, di.sms), 256, 0, s>>>(static_cast<const uint8_t*>(canon),
-                                                                     static_cast<uint8_t*>(pack), nblocks);
+                                                                     static_cast<uint8_t*>(pack), N, K);
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -164,31 +171,68 @@ int launch_qpack_q6_k(const void* canon, void* pack, int N, int K, cudaStream_t 
 
 constexpr int ARGMAX_THREADS = 256;
 
+template <int M>
 __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float* __restrict__ y, int64_t ldy,
                                                                      int32_t* __restrict__ ids, Top1Workspace* ws,
-                                                                     int M, int N)
+                                                                     int N)
 {
-    __shared__ unsigned long long s_red[ARGMAX_THREADS / 32];
+    __shared__ unsigned long long s_red[ARGMAX_THREADS / 32][M];
     __shared__ int s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int m = 0; m < M; ++m) {
-        const float* row = y + (int64_t)m * ldy;
-        unsigned long long k = 0ull;
-        for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < N; n += stride) {
-            const unsigned long long kn = top1_key(__ldg(row + n), (int)n);
-            k = kn > k ? kn : k;
+    unsigned long long k[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) k[m] = 0ull;
+    const bool vec4 = ((reinterpret_cast<uintptr_t>(y) | ((uintptr_t)ldy * 4)) & 15u) == 0;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (vec4) {
+        const int64_t n4 = N / 4;
+        for (int64_t q = tid; q < n4; q += nthreads) {
+            float4 v[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) v[m] = __ldg(reinterpret_cast<const float4*>(y + (int64_t)m * ldy) + q);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const int n = (int)(4 * q);
+                unsigned long long c;
+                c = top1_key(v[m].x, n);
+                k[m] = c > k[m] ? c : k[m];
+                c = top1_key(v[m].y, n + 1);
+                k[m] = c > k[m] ? c : k[m];
+                c = top1_key(v[m].z, n + 2);
+                k[m] = c > k[m] ? c : k[m];
+                c = top1_key(v[m].w, n + 3);
+                k[m] = c > k[m] ? c : k[m];
+            }
         }
-        k = warp_max_u64(k);
-        if (lane == 0) s_red[warp] = k;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            unsigned long long b = 0ull;
-            for (int w = 0; w < ARGMAX_THREADS / 32; ++w) b = s_red[w] > b ? s_red[w] : b;
-            atomicMax(&ws->keys[m], b);
+        for (int64_t n = 4 * n4 + tid; n < N; n += nthreads) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const unsigned long long c = top1_key(__ldg(y + (int64_t)m * ldy + n), (int)n);
+                k[m] = c > k[m] ? c : k[m];
+            }
         }
-        __syncthreads();
+    } else {
+        for (int64_t n = tid; n < N; n += nthreads) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const unsigned long long c = top1_key(__ldg(y + (int64_t)m * ldy + n), (int)n);
+                k[m] = c > k[m] ? c : k[m];
+            }
+        }
     }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const unsigned long long w = warp_max_u64(k[m]);
+        if (lane == 0) s_red[warp][m] = w;
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+        unsigned long long b = 0ull;
+        for (int w = 0; w < ARGMAX_THREADS / 32; ++w) b = s_red[w][threadIdx.x] > b ? s_red[w][threadIdx.x] : b;
+        atomicMax(&ws->keys[threadIdx.x], b);
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         s_last = atomicAdd(&ws->done, 1u) == gridDim.x - 1;
@@ -201,6 +245,13 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float
     }
 }
 
+template <int M>
+static void launch_argmax_m(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int N, int grid,
+                            cudaStream_t s)
+{
+    argmax_rows_kernel<M><<<grid, ARGMAX_THREADS, 0, s>>>(y, ldy, ids, ws, N);
+}
+
 int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int M, int N, cudaStream_t s)
 {
     const DeviceInfo di = device_info();
@@ -208,7 +259,16 @@ int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace*
     int grid = (int)(((int64_t)N + ARGMAX_THREADS * 4 - 1) / (ARGMAX_THREADS * 4));
     if (grid > di.sms * 2) grid = di.sms * 2;
     if (grid < 1) grid = 1;
-    argmax_rows_kernel<<<grid, ARGMAX_THREADS, 0, s>>>(y, ldy, ids, ws, M, N);
+    switch (M) {
+#define QGEMV_ARGMAX_CASE(m) \
+    case m: launch_argmax_m<m>(y, ldy, ids, ws, N, grid, s); break;
+    QGEMV_ARGMAX_CASE(1) QGEMV_ARGMAX_CASE(2) QGEMV_ARGMAX_CASE(3) QGEMV_ARGMAX_CASE(4) QGEMV_ARGMAX_CASE(5)
+    QGEMV_ARGMAX_CASE(6) QGEMV_ARGMAX_CASE(7) QGEMV_ARGMAX_CASE(8) QGEMV_ARGMAX_CASE(9) QGEMV_ARGMAX_CASE(10)
+    QGEMV_ARGMAX_CASE(11) QGEMV_ARGMAX_CASE(12) QGEMV_ARGMAX_CASE(13) QGEMV_ARGMAX_CASE(14)
+    QGEMV_ARGMAX_CASE(15) QGEMV_ARGMAX_CASE(16) QGEMV_ARGMAX_CASE(17)
+#undef QGEMV_ARGMAX_CASE
+    default: return QGEMV_UNSUPPORTED_SHAPE;
+    }
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -232,15 +292,15 @@ __global__ void block_dots_kernel(const void* __restrict__ w_pack, const uint8_t
         uint2 meta;
         act_from_q8_1<FMT>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES, lo, hi, meta);
         uint32_t w[8];
-        const int64_t wi = (int64_t)n * NB + b;
         if (FMT == FMT_Q4_0) {
-            const PackQ40 pk = pack_q4_0(w_pack, N, NB);
-            q4_0_unpack(pk.nib[wi], w);
+            const BlockAddr ad = block_addr(w_pack, geom_q4_0(NB * QK), n, b);
+            q4_0_unpack(reinterpret_cast<const uint4*>(ad.tile)[ad.j], w);
             out[i] = q4_0_dot(w, lo, hi, (int)meta.y);
         } else {
-            const PackQ6K pk = pack_q6_k(w_pack, N, NB);
-            q6_k_unpack(pk.ql[wi], pk.qh[wi], w);
-            out[i] = q6_k_dot(w, lo, hi, meta.y, pk.sc[wi]);
+            const BlockAddr ad = block_addr(w_pack, geom_q6_k(NB * QK), n, b);
+            q6_k_unpack(reinterpret_cast<const uint4*>(ad.tile)[ad.j],
+                        reinterpret_cast<const uint2*>(ad.tile + ad.nb * 16)[ad.j], w);
+            out[i] = q6_k_dot(w, lo, hi, meta.y, reinterpret_cast<const uint16_t*>(ad.tile + ad.nb * 24)[ad.j]);
         }
     }
 }

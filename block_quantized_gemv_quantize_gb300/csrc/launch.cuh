@@ -17,6 +17,10 @@ struct DeviceInfo {
 // Per-device properties, queried once per device.
 DeviceInfo device_info();
 
+// Counts warps that gave up waiting for a weight copy (one per translation
+// unit that instantiates the ring kernel).
+static __device__ unsigned int g_wait_timeouts;
+
 // Largest multiple-of-32 block chunk of activation that fits in shared memory
 // next to `extra` bytes (all of K when it fits).
 inline int mmvq_chunk_blocks(const DeviceInfo& di, int M, int NB, size_t extra)
@@ -29,37 +33,100 @@ inline int mmvq_chunk_blocks(const DeviceInfo& di, int M, int NB, size_t extra)
     return kc < 32 ? 32 : (int)kc;
 }
 
+constexpr int MAX_RING_STAGES = 8;
+
+// Launch configuration of one MMVQ call.
+struct MmvqPlan {
+    bool ring;
+    int grid, warps, stages, KC;
+    size_t smem;
+};
+
+template <int FMT, int M, bool TOP1>
+MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N)
+{
+    constexpr int R = RowsPerWarp<M>::value;
+    const Geom g = fmt_geom<FMT>(K);
+    const int n_rg = (N + R - 1) / R;
+    MmvqPlan p{};
+    p.grid = n_rg < di.sms ? n_rg : di.sms;
+    const int per_cta = (n_rg + p.grid - 1) / p.grid;
+    p.warps = per_cta < MMVQ_MAX_WARPS ? per_cta : MMVQ_MAX_WARPS;
+    const size_t act = (size_t)M * g.NB * ACT_BYTES_PER_BLOCK;
+    const size_t extra = TOP1 ? top1_scratch_bytes(p.warps) : 0;
+    const size_t stage = (size_t)R * g.full_tile;
+    const size_t fixed = act + extra + 128;
+    long long s = fixed < (size_t)di.smem_optin ? (long long)(((size_t)di.smem_optin - fixed) / (p.warps * (stage + 8))) : 0;
+    if (s > MAX_RING_STAGES) s = MAX_RING_STAGES;
+    if (s >= 2) {
+        p.ring = true;
+        p.stages = (int)s;
+        p.KC = g.NB;
+        p.smem = (size_t)p.warps * p.stages * (stage + 8) + act + extra;
+        return p;
+    }
+    p.ring = false;
+    p.warps = MMVQ_MAX_WARPS;
+    const int n_items = (n_rg + p.warps - 1) / p.warps;
+    p.grid = n_items < di.sms ? n_items : di.sms;
+    const size_t ex = TOP1 ? top1_scratch_bytes(p.warps) : 0;
+    p.KC = mmvq_chunk_blocks(di, M, g.NB, ex);
+    p.stages = 0;
+    p.smem = (size_t)M * p.KC * ACT_BYTES_PER_BLOCK + ex;
+    return p;
+}
+
 template <int FMT, int M, bool TOP1>
 int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
 {
     const DeviceInfo di = device_info();
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
-    const int NB = a.K / QK;
-    const size_t extra = mmvq_smem_bytes<M, TOP1>(0);
-    a.KC = mmvq_chunk_blocks(di, M, NB, extra);
-    const size_t smem = mmvq_smem_bytes<M, TOP1>(a.KC);
-    if (smem > (size_t)di.smem_optin) return QGEMV_UNSUPPORTED_SHAPE;
-    auto kern = mmvq_kernel<FMT, M, TOP1>;
-    // Opt in to the device's full shared memory once per device.
-    static bool opted[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QGEMV_CUDA_ERROR;
-    if (!opted[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
-            return QGEMV_CUDA_ERROR;
-        opted[dev] = true;
+    const MmvqPlan p = mmvq_plan<FMT, M, TOP1>(di, a.K, a.N);
+    if (p.smem > (size_t)di.smem_optin) return QGEMV_UNSUPPORTED_SHAPE;
+    a.KC = p.KC;
+    a.stages = p.stages;
+    // Opt in to the device's full shared memory once per device and kernel.
+    static bool opted_ring[64], opted_lock[64];
+    static unsigned int* timeouts[64];
+    if (p.ring) {
+        auto kern = mmvq_ring_kernel<FMT, M, TOP1>;
+        if (!opted_ring[dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
+                return QGEMV_CUDA_ERROR;
+            if (cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) != cudaSuccess)
+                return QGEMV_CUDA_ERROR;
+            opted_ring[dev] = true;
+        }
+        kern<<<p.grid, p.warps * 32, p.smem, s>>>(a, timeouts[dev]);
+    } else {
+        auto kern = mmvq_lockstep_kernel<FMT, M, TOP1>;
+        if (!opted_lock[dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
+                return QGEMV_CUDA_ERROR;
+            opted_lock[dev] = true;
+        }
+        kern<<<p.grid, p.warps * 32, p.smem, s>>>(a);
     }
-    constexpr int R = RowsPerWarp<M>::value;
-    const int n_rg = (a.N + R - 1) / R;
-    const int n_items = (n_rg + MMVQ_WARPS - 1) / MMVQ_WARPS;
-    const int grid = n_items < di.sms ? n_items : di.sms;
-    kern<<<grid, MMVQ_THREADS, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+// Reads and clears this translation unit's timeout counter (synchronous).
+inline unsigned int take_wait_timeouts_tu()
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
+    return v;
 }
 
 int launch_mmvq_q4_0(const MmvqArgs& a, int M, cudaStream_t s);
 int launch_mmvq_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
+unsigned int take_wait_timeouts_q4_0();
+unsigned int take_wait_timeouts_q6_k();
+unsigned int take_wait_timeouts_lmhead();
 
 int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cudaStream_t s);
 int launch_qpack_q4_0(const void* canon, void* pack, int N, int K, cudaStream_t s);

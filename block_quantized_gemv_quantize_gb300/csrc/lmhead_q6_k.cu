@@ -1,4 +1,4 @@
-// Instantiations of the fused Q6_K LM-head top-1 kernel for M = 1..17.
+// Instantiations of the fused Q6_K LM-head top-1 kernels for M = 1..17.
 #include "launch.cuh"
 
 namespace qgemv {
@@ -26,5 +26,7 @@ int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s)
     default: return QGEMV_UNSUPPORTED_SHAPE;
     }
 }
+
+unsigned int take_wait_timeouts_lmhead() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

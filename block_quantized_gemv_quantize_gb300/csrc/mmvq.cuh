@@ -8,27 +8,30 @@
 // "Q6_K M=6 fused DFlash top-1 production record", Why this was slow: the
 // five-row kernel reuses each weight slice across all rows).
 //
-// Work decomposition (GB300, 152 SMs, one 512-thread CTA per SM):
-//   * a warp owns a group of R consecutive weight rows and walks the whole K
-//     dimension; lane l takes blocks b = l, l + 32, ... so that the 32 lanes
-//     read 512 contiguous bytes of the packed nibble stream per row and load;
-//   * each lane keeps R x M fp32 partial sums, reusing one activation block
-//     (read from shared memory) for R rows and each weight block for M rows;
-//   * a transpose-reduction sums the R x M partials over the 32 lanes with the
-//     same butterfly tree for every output, so an output's value does not
-//     depend on where its row sits (duplicated rows give identical floats);
-//   * the activation tile (Q8_1 codes, fp16 scale, integer sums) is staged in
-//     shared memory once per CTA; when it does not fit, K is processed in
-//     chunks of a multiple of 32 blocks (same lane-to-block map, same order).
-// Weights are streamed with L1-bypassing 16-byte loads and read exactly once.
+// Work decomposition (GB300: 152 SMs, one CTA of up to 16 warps per SM):
+//   * the N rows are split into groups of R rows; each CTA takes a contiguous,
+//     balanced range of groups and its warps take the groups in turn;
+//   * a warp walks its groups' (row, 32-block chunk) tiles in order and keeps
+//     them streaming through a private ring of shared-memory stages filled by
+//     TMA bulk copies (cp.async.bulk, completion on an mbarrier), several
+//     stages ahead, so the bytes in flight do not depend on registers;
+//   * lane l handles block l of every chunk for all R rows; it reuses one
+//     activation block (staged once per CTA in shared memory) for R rows and
+//     one weight block for M rows, holding R x M fp32 partial sums;
+//   * a transpose-reduction sums the partials over the 32 lanes with the same
+//     butterfly tree for every output, so an output's value does not depend on
+//     where its row sits (duplicated rows give identical floats).
+// Every weight byte is read from HBM once.  When the activation tile does not
+// fit next to the rings (M * K large), a lock-step variant stages K in chunks
+// and reads the weights with streaming loads (same arithmetic, same order).
 #pragma once
 
 #include "qgemv_common.cuh"
 
 namespace qgemv {
 
-constexpr int MMVQ_THREADS = 512;
-constexpr int MMVQ_WARPS = MMVQ_THREADS / 32;
+constexpr int MMVQ_MAX_THREADS = 512;
+constexpr int MMVQ_MAX_WARPS = MMVQ_MAX_THREADS / 32;
 
 // Rows per warp for a given M: R * M partial sums per lane.
 template <int M>
@@ -81,6 +84,88 @@ __device__ __forceinline__ bool reduced_value_owner(int lane)
 }
 
 // ---------------------------------------------------------------------------
+// TMA bulk copies and mbarriers (inline PTX).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Order this thread's earlier shared-memory accesses before later TMA writes.
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for an mbarrier phase, giving up after about a second (returns false).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 1000000000ull) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing `bytes` of transaction on `bar`; weights are streamed once, so
+// they are marked evict-first in L2.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Activation staging into the shared tile.
 // ---------------------------------------------------------------------------
 
@@ -106,167 +191,78 @@ __device__ __forceinline__ void stage_from_q8_1(const ActTile& t, const uint8_t*
     }
 }
 
-// From fp32 activations, quantizing to Q8_1 on the fly (one warp per block),
+// From fp32 activations, quantizing to Q8_1 on the fly (one thread per block),
 // bit-identical to the standalone quantize_q8_1 kernel.
 template <int FMT, int M>
 __device__ __forceinline__ void stage_from_f32(const ActTile& t, const float* x, int64_t ldx, int kb0, int kb1)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int nbc = kb1 - kb0;
-    int8_t* qbytes = reinterpret_cast<int8_t*>(t.aq);
-    for (int i = warp; i < M * nbc; i += nw) {
+    const bool vec4 = ((reinterpret_cast<uintptr_t>(x) | ((uintptr_t)ldx * 4)) & 15u) == 0;
+    for (int i = threadIdx.x; i < M * nbc; i += blockDim.x) {
         const int m = i / nbc, bl = i - m * nbc;
-        const float xv = x[(int64_t)m * ldx + (int64_t)(kb0 + bl) * QK + lane];
-        const Q81Lane r = q8_1_quantize_lane(xv);
-        const int hsum = halfwarp_sum_i32(r.q);
-        const int s1 = __shfl_sync(0xffffffffu, hsum, 16);
-        qbytes[((m * 2 + (lane >> 4)) * t.KC + bl) * 16 + (lane & 15)] = (int8_t)r.q;
-        if (lane == 0) {
-            const float da = __half2float(__float2half_rn(r.d));
-            uint2 meta;
-            meta.x = __float_as_uint(da);
-            meta.y = FMT == FMT_Q4_0 ? (uint32_t)(-8 * (hsum + s1))
-                                     : (((uint32_t)hsum & 0xFFFFu) | ((uint32_t)s1 << 16));
-            t.am[m * t.KC + bl] = meta;
-        }
+        Q81Block qb;
+        q8_1_quantize_block(x + (int64_t)m * ldx + (int64_t)(kb0 + bl) * QK, vec4, qb);
+        t.aq[(m * 2 + 0) * t.KC + bl] = make_uint4(qb.q[0], qb.q[1], qb.q[2], qb.q[3]);
+        t.aq[(m * 2 + 1) * t.KC + bl] = make_uint4(qb.q[4], qb.q[5], qb.q[6], qb.q[7]);
+        uint2 meta;
+        meta.x = __float_as_uint(__half2float(__float2half_rn(qb.d)));
+        meta.y = act_meta_from_sums<FMT>(qb.s_lo, qb.s_hi);
+        t.am[m * t.KC + bl] = meta;
     }
 }
 
 // ---------------------------------------------------------------------------
-// One row group over one K chunk.
+// Per-block accumulation, shared by both kernel variants.
 // ---------------------------------------------------------------------------
 
-template <int M, int R, int U>
-__device__ __forceinline__ void rowgroup_chunk_q4_0(const PackQ40& pk, int NB, const int (&rows)[R], int kb0, int kb1,
-                                                    const ActTile& t, int lane, float (&acc)[R][M])
+// Q4_0: w16[r] = the block's 16 code bytes of row r, dw[r] = its scale.
+template <int M, int R>
+__device__ __forceinline__ void accumulate_q4_0(const uint4 (&w16)[R], const float (&dw)[R], const ActTile& t, int ti,
+                                                float (&acc)[R][M])
 {
-    const uint4* nib[R];
-    const __half* dsc[R];
+    uint32_t w[R][8];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        nib[r] = pk.nib + (int64_t)rows[r] * NB;
-        dsc[r] = pk.d + (int64_t)rows[r] * NB;
-    }
-    for (int b = kb0 + lane; b < kb1; b += 32 * U) {
-        uint4 wv[U][R];
-        uint16_t dh[U][R];
+    for (int r = 0; r < R; ++r) q4_0_unpack(w16[r], w[r]);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int bb = b + 32 * u;
+    for (int m = 0; m < M; ++m) {
+        const uint4 lo = t.aq[(m * 2 + 0) * t.KC + ti];
+        const uint4 hi = t.aq[(m * 2 + 1) * t.KC + ti];
+        const uint2 mt = t.am[m * t.KC + ti];
+        const float da = __uint_as_float(mt.x);
+        const int init = (int)mt.y + MAGIC_I2F_BITS;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (bb < kb1) {
-                    wv[u][r] = ld_stream_v4(nib[r] + bb);
-                    dh[u][r] = ld_stream_u16(dsc[r] + bb);
-                } else {
-                    wv[u][r] = make_uint4(0, 0, 0, 0);
-                    dh[u][r] = 0;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int bb = b + 32 * u;
-            if (bb < kb1) {
-                const int ti = bb - kb0;
-                uint32_t w[R][8];
-                float dw[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    q4_0_unpack(wv[u][r], w[r]);
-                    dw[r] = __half2float(__ushort_as_half(dh[u][r]));
-                }
-#pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    const uint4 lo = t.aq[(m * 2 + 0) * t.KC + ti];
-                    const uint4 hi = t.aq[(m * 2 + 1) * t.KC + ti];
-                    const uint2 mt = t.am[m * t.KC + ti];
-                    const float da = __uint_as_float(mt.x);
-                    const int init = (int)mt.y + MAGIC_I2F_BITS;
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const int s = q4_0_dot(w[r], lo, hi, init);
-                        const float f = __int_as_float(s) - MAGIC_I2F;  // exact I
-                        acc[r][m] = fmaf(dw[r] * da, f, acc[r][m]);
-                    }
-                }
-            }
+        for (int r = 0; r < R; ++r) {
+            const int s = q4_0_dot(w[r], lo, hi, init);
+            const float f = __int_as_float(s) - MAGIC_I2F;  // exact I
+            acc[r][m] = fmaf(dw[r] * da, f, acc[r][m]);
         }
     }
 }
 
-template <int M, int R, int U>
-__device__ __forceinline__ void rowgroup_chunk_q6_k(const PackQ6K& pk, int NB, const int (&rows)[R], int kb0, int kb1,
-                                                    const ActTile& t, int lane, float (&acc)[R][M])
+// Q6_K: ql/qh/sc of the block for row r, dw[r] = its superblock scale.
+template <int M, int R>
+__device__ __forceinline__ void accumulate_q6_k(const uint4 (&ql)[R], const uint2 (&qh)[R], const uint32_t (&sc)[R],
+                                                const float (&dw)[R], const ActTile& t, int ti, float (&acc)[R][M])
 {
-    const int NSB = NB / 8;
-    const uint4* ql[R];
-    const uint2* qh[R];
-    const uint16_t* sc[R];
-    const __half* dd[R];
+    uint32_t w[R][8];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        ql[r] = pk.ql + (int64_t)rows[r] * NB;
-        qh[r] = pk.qh + (int64_t)rows[r] * NB;
-        sc[r] = pk.sc + (int64_t)rows[r] * NB;
-        dd[r] = pk.d + (int64_t)rows[r] * NSB;
-    }
-    for (int b = kb0 + lane; b < kb1; b += 32 * U) {
-        uint4 vl[U][R];
-        uint2 vh[U][R];
-        uint16_t vs[U][R], vd[U][R];
+    for (int r = 0; r < R; ++r) q6_k_unpack(ql[r], qh[r], w[r]);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int bb = b + 32 * u;
+    for (int m = 0; m < M; ++m) {
+        const uint4 lo = t.aq[(m * 2 + 0) * t.KC + ti];
+        const uint4 hi = t.aq[(m * 2 + 1) * t.KC + ti];
+        const uint2 mt = t.am[m * t.KC + ti];
+        const float da = __uint_as_float(mt.x);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (bb < kb1) {
-                    vl[u][r] = ld_stream_v4(ql[r] + bb);
-                    vh[u][r] = ld_stream_v2(qh[r] + bb);
-                    vs[u][r] = ld_stream_u16(sc[r] + bb);
-                    vd[u][r] = ld_stream_u16(dd[r] + (bb >> 3));
-                } else {
-                    vl[u][r] = make_uint4(0, 0, 0, 0);
-                    vh[u][r] = make_uint2(0, 0);
-                    vs[u][r] = 0;
-                    vd[u][r] = 0;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int bb = b + 32 * u;
-            if (bb < kb1) {
-                const int ti = bb - kb0;
-                uint32_t w[R][8];
-                float dw[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    q6_k_unpack(vl[u][r], vh[u][r], w[r]);
-                    dw[r] = __half2float(__ushort_as_half(vd[u][r]));
-                }
-#pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    const uint4 lo = t.aq[(m * 2 + 0) * t.KC + ti];
-                    const uint4 hi = t.aq[(m * 2 + 1) * t.KC + ti];
-                    const uint2 mt = t.am[m * t.KC + ti];
-                    const float da = __uint_as_float(mt.x);
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const int J = q6_k_dot(w[r], lo, hi, mt.y, vs[u][r]);
-                        acc[r][m] = fmaf(dw[r] * da, (float)J, acc[r][m]);
-                    }
-                }
-            }
+        for (int r = 0; r < R; ++r) {
+            const int J = q6_k_dot(w[r], lo, hi, mt.y, sc[r]);
+            acc[r][m] = fmaf(dw[r] * da, (float)J, acc[r][m]);
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.
-//   TOP1 = false: y[m * ldy + n] = result (activation from Q8_1 in xq).
-//   TOP1 = true : activation quantized from fp32 x in the prologue; each row's
-//                 greedy token id goes to ids[m]; no logits are written.
+// Kernel arguments and epilogue.
 // ---------------------------------------------------------------------------
 
 struct MmvqArgs {
@@ -276,165 +272,346 @@ struct MmvqArgs {
     int64_t ldx;
     float* y;
     int64_t ldy;
-    int K, N, KC;
+    int K, N;
+    int KC;      // activation blocks staged at once (lock-step kernel)
+    int stages;  // ring stages per warp (ring kernel)
     Top1Workspace* ws;
     int32_t* ids;
 };
 
-template <int FMT, int M, bool TOP1>
-__global__ void __launch_bounds__(MMVQ_THREADS, 1) mmvq_kernel(const MmvqArgs a)
+// Reduce one row group's partial sums over the warp and write them (TOP1 =
+// false) or fold their keys into the warp's running best per row (TOP1).
+template <int M, int R, bool TOP1>
+__device__ __forceinline__ void finish_rowgroup(const MmvqArgs& a, int n0, float (&acc)[R][M], int lane,
+                                                unsigned long long* wk, unsigned long long& best)
 {
-    constexpr int R = RowsPerWarp<M>::value;
     constexpr int V = R * M;
     constexpr int P = next_pow2(V);
     constexpr int C = P >= 32 ? P / 32 : 1;
-    constexpr int U = FMT == FMT_Q4_0 ? 2 : 1;
+    float v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) v[i] = i < V ? acc[i / M][i % M] : 0.0f;
+    warp_transpose_reduce<P>(v, lane);
+    if (!TOP1) {
+        if (reduced_value_owner<P>(lane)) {
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                const int vi = reduced_value_index<P>(lane, j);
+                if (vi < V) {
+                    const int r = vi / M, m = vi - (vi / M) * M;
+                    const int n = n0 + r;
+                    if (n < a.N) a.y[(int64_t)m * a.ldy + n] = v[j];
+                }
+            }
+        }
+    } else {
+        if (reduced_value_owner<P>(lane)) {
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                const int vi = reduced_value_index<P>(lane, j);
+                if (vi < V) {
+                    const int n = n0 + vi / M;
+                    wk[vi] = n < a.N ? top1_key(v[j], n) : 0ull;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane < M) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const unsigned long long k = wk[r * M + lane];
+                best = k > best ? k : best;
+            }
+        }
+        __syncwarp();
+    }
+}
 
-    extern __shared__ uint4 smem[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int NB = a.K / QK;
-    const int KC = a.KC;
+// Combine the warps' best keys, then across CTAs with one 64-bit atomicMax per
+// row; the last CTA to finish writes the ids and leaves the workspace zeroed.
+template <int M>
+__device__ __forceinline__ void top1_finish(const MmvqArgs& a, unsigned long long* s_best, int* s_last,
+                                            unsigned long long best, int lane, int warp, int nwarps)
+{
+    if (lane < M) s_best[warp * MAX_M + lane] = best;
+    __syncthreads();
+    if (threadIdx.x < M) {
+        unsigned long long k = 0ull;
+        for (int w = 0; w < nwarps; ++w) {
+            const unsigned long long kw = s_best[w * MAX_M + threadIdx.x];
+            k = kw > k ? kw : k;
+        }
+        atomicMax(&a.ws->keys[threadIdx.x], k);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.ws->done, 1u);
+        *s_last = prev == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (*s_last) {
+        __threadfence();
+        if (threadIdx.x < M) {
+            const unsigned long long k = atomicExch(&a.ws->keys[threadIdx.x], 0ull);
+            a.ids[threadIdx.x] = top1_key_to_id(k);
+        }
+        if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
+    }
+}
+
+// Shared memory besides the activation tile and the rings, for TOP1.
+inline size_t top1_scratch_bytes(int nwarps) { return (size_t)nwarps * 64 * 8 + (size_t)nwarps * MAX_M * 8 + 16; }
+
+template <int FMT>
+__host__ __device__ inline Geom fmt_geom(int K)
+{
+    return FMT == FMT_Q4_0 ? geom_q4_0(K) : geom_q6_k(K);
+}
+
+// ---------------------------------------------------------------------------
+// Ring kernel: the whole activation in shared memory, weights streamed by
+// per-warp TMA rings.
+//   shared memory: rings [W][S][R * full_tile] | aq [M][2][NB] | am [M][NB] |
+//                  mbarriers [W][S] | TOP1 scratch
+// The CTA's row groups are rg0 .. rg1-1; warp w takes rg0 + w, rg0 + w + W, ...
+// Job j of a warp = (its group j / nch, chunk j % nch), in stage j % S.
+// Waits are bounded: a warp that waits about a second for a copy counts a
+// timeout in *timeouts, stops, and gives its copies in flight a bounded wait.
+// ---------------------------------------------------------------------------
+
+template <int FMT, int M, bool TOP1>
+__global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
+{
+    constexpr int R = RowsPerWarp<M>::value;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+    const int S = a.stages;
+    const Geom g = fmt_geom<FMT>(a.K);
+    const int NB = g.NB, nch = g.nch;
+    const int stage_bytes = R * g.full_tile;
+
+    uint8_t* rings = smem;
     ActTile t;
-    t.aq = smem;
-    t.am = reinterpret_cast<uint2*>(smem + 2 * M * KC);
-    t.KC = KC;
-    unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(t.am + M * KC);  // [warps][64]
-    unsigned long long* s_best = s_keys + MMVQ_WARPS * 64;                               // [warps][MAX_M], flag
+    t.aq = reinterpret_cast<uint4*>(rings + (size_t)W * S * stage_bytes);
+    t.am = reinterpret_cast<uint2*>(t.aq + 2 * M * NB);
+    t.KC = NB;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(t.am + M * NB);
+    unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(bars + W * S);  // [W][64]
+    unsigned long long* s_best = s_keys + W * 64;                                     // [W][MAX_M]
+    int* s_last = reinterpret_cast<int*>(s_best + W * MAX_M);
 
     const int n_rg = (a.N + R - 1) / R;
-    const int n_items = (n_rg + MMVQ_WARPS - 1) / MMVQ_WARPS;
-    const int nchunks = (NB + KC - 1) / KC;
+    const int rg0 = (int)((int64_t)blockIdx.x * n_rg / gridDim.x);
+    const int rg1 = (int)((int64_t)(blockIdx.x + 1) * n_rg / gridDim.x);
+    const int n_my = warp < rg1 - rg0 ? (rg1 - rg0 - warp + W - 1) / W : 0;
+    const int J = n_my * nch;
 
-    PackQ40 p4 = pack_q4_0(a.w_pack, a.N, NB);
-    PackQ6K p6 = pack_q6_k(a.w_pack, a.N, NB);
+    uint64_t* wbar = bars + warp * S;
+    uint8_t* wring = rings + (size_t)warp * S * stage_bytes;
+    const uint8_t* wbase = static_cast<const uint8_t*>(a.w_pack);
+    const uint64_t pol = l2_evict_first_policy();
 
-    if (TOP1) {
-        // Start this CTA's first weight rows on their way to L2 while the
-        // activation is being quantized.
-        const int rg = blockIdx.x * MMVQ_WARPS + warp;
-        const int boff = (lane / R) * 32;  // one 512-byte segment per lane, inside the row
-        if (rg < n_rg && boff < NB) {
-            const int n = min(rg * R + (lane & (R - 1)), a.N - 1);
-            if (FMT == FMT_Q6_K) prefetch_l2(p6.ql + (int64_t)n * NB + boff);
-            else prefetch_l2(p4.nib + (int64_t)n * NB + boff);
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&wbar[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    int issued = 0;
+    // Lane 0 issues the next job: R bulk copies of its rows' tiles for one chunk.
+    auto issue_next = [&]() {
+        const int j = issued++;
+        const int i = j / nch, c = j - i * nch;
+        const int rg = rg0 + warp + i * W;
+        const int tb = g.tile(c);
+        uint64_t* bar = &wbar[j % S];
+        uint8_t* dst = wring + (size_t)(j % S) * stage_bytes;
+        mbar_arrive_expect_tx(bar, (uint32_t)(R * tb));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t n = min(rg * R + r, a.N - 1);
+            bulk_g2s(dst + r * tb, wbase + n * g.row + (int64_t)c * g.full_tile, (uint32_t)tb, bar, pol);
         }
+    };
+    if (lane == 0) {
+        while (issued < S - 1 && issued < J) issue_next();
     }
 
-    if (nchunks == 1) {
-        if (TOP1) stage_from_f32<FMT, M>(t, a.x, a.ldx, 0, NB);
-        else stage_from_q8_1<FMT, M>(t, a.xq, NB, 0, NB);
-        __syncthreads();
-    }
+    // The activation is staged while the first weight tiles are in flight.
+    if (TOP1) stage_from_f32<FMT, M>(t, a.x, a.ldx, 0, NB);
+    else stage_from_q8_1<FMT, M>(t, a.xq, NB, 0, NB);
+    __syncthreads();
 
-    unsigned long long best = 0ull;  // lane m < M: best key of row m seen by this warp
+    const __half* d6 = FMT == FMT_Q6_K ? q6_k_scales(a.w_pack, g, a.N) : nullptr;
+    const int NSB = NB / 8;
+    // Q6_K superblock scales of job j for this lane, fetched one job ahead.
+    auto load_d6 = [&](int j, uint16_t (&d)[R]) {
+        const int i = j / nch, c = j - i * nch;
+        const int rg = rg0 + warp + i * W;
+        const int b = min(c * CHUNK + lane, NB - 1);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t n = min(rg * R + r, a.N - 1);
+            d[r] = ld_stream_u16(d6 + n * NSB + (b >> 3));
+        }
+    };
+    uint16_t dnext[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) dnext[r] = 0;
+    if (FMT == FMT_Q6_K && J > 0) load_d6(0, dnext);
+
+    unsigned long long best = 0ull;
+    float acc[R][M];
+    int consumed = 0;
+    for (int j = 0; j < J; ++j) {
+        const int i = j / nch, c = j - i * nch;
+        const int rg = rg0 + warp + i * W;
+        if (lane == 0 && issued < J) {
+            fence_proxy_async();
+            issue_next();
+        }
+        uint16_t dcur[R];
+        if (FMT == FMT_Q6_K) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) dcur[r] = dnext[r];
+            if (j + 1 < J) load_d6(j + 1, dnext);
+        }
+        if (c == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+        }
+        const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&wbar[j % S], (uint32_t)((j / S) & 1)));
+        if (!ready) {
+            if (lane == 0) atomicAdd(timeouts, 1u);
+            break;
+        }
+        consumed = j + 1;
+        const int nb = g.nb(c), tb = g.tile(c);
+        const uint8_t* st = wring + (size_t)(j % S) * stage_bytes;
+        if (lane < nb) {
+            const int ti = c * CHUNK + lane;
+            if (FMT == FMT_Q4_0) {
+                uint4 w16[R];
+                float dw[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    w16[r] = *reinterpret_cast<const uint4*>(st + r * tb + lane * 16);
+                    dw[r] = __half2float(
+                        __ushort_as_half(*reinterpret_cast<const uint16_t*>(st + r * tb + nb * 16 + lane * 2)));
+                }
+                accumulate_q4_0<M, R>(w16, dw, t, ti, acc);
+            } else {
+                uint4 ql[R];
+                uint2 qh[R];
+                uint32_t sc[R];
+                float dw[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    ql[r] = *reinterpret_cast<const uint4*>(st + r * tb + lane * 16);
+                    qh[r] = *reinterpret_cast<const uint2*>(st + r * tb + nb * 16 + lane * 8);
+                    sc[r] = *reinterpret_cast<const uint16_t*>(st + r * tb + nb * 24 + lane * 2);
+                    dw[r] = __half2float(__ushort_as_half(dcur[r]));
+                }
+                accumulate_q6_k<M, R>(ql, qh, sc, dw, t, ti, acc);
+            }
+        }
+        __syncwarp();
+        if (c == nch - 1) finish_rowgroup<M, R, TOP1>(a, rg * R, acc, lane, s_keys + warp * 64, best);
+    }
+    // After a timeout, give the copies still in flight a bounded wait before
+    // the shared memory is released.
+    if (lane == 0) {
+        for (int j = consumed; j < issued; ++j) mbar_wait_bounded(&wbar[j % S], (uint32_t)((j / S) & 1));
+    }
+    __syncwarp();
+
+    if (TOP1) top1_finish<M>(a, s_best, s_last, best, lane, warp, W);
+}
+
+// ---------------------------------------------------------------------------
+// Lock-step kernel: for activations too large for shared memory next to the
+// rings.  K is staged in chunks of KC blocks (a multiple of 32); all warps
+// move through the chunks together; weights are read with streaming loads.
+//   shared memory: aq [M][2][KC] | am [M][KC] | TOP1 scratch
+// ---------------------------------------------------------------------------
+
+template <int FMT, int M, bool TOP1>
+__global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_lockstep_kernel(const MmvqArgs a)
+{
+    constexpr int R = RowsPerWarp<M>::value;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+    const Geom g = fmt_geom<FMT>(a.K);
+    const int NB = g.NB, KC = a.KC;
+    ActTile t;
+    t.aq = reinterpret_cast<uint4*>(smem);
+    t.am = reinterpret_cast<uint2*>(t.aq + 2 * M * KC);
+    t.KC = KC;
+    unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(t.am + M * KC);
+    unsigned long long* s_best = s_keys + W * 64;
+    int* s_last = reinterpret_cast<int*>(s_best + W * MAX_M);
+
+    const int n_rg = (a.N + R - 1) / R;
+    const int n_items = (n_rg + W - 1) / W;
+    const int nchunks = (NB + KC - 1) / KC;
+    const __half* d6 = FMT == FMT_Q6_K ? q6_k_scales(a.w_pack, g, a.N) : nullptr;
+    const int NSB = NB / 8;
+    unsigned long long best = 0ull;
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int rg = item * MMVQ_WARPS + warp;
+        const int rg = item * W + warp;
         const bool active = rg < n_rg;
-        const int n0 = rg * R;
         int rows[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) rows[r] = min(n0 + r, a.N - 1);
-
+        for (int r = 0; r < R; ++r) rows[r] = min(rg * R + r, a.N - 1);
         float acc[R][M];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
-
-        for (int c = 0; c < nchunks; ++c) {
-            const int kb0 = c * KC, kb1 = min(NB, kb0 + KC);
-            if (nchunks > 1) {
-                __syncthreads();
-                if (TOP1) stage_from_f32<FMT, M>(t, a.x, a.ldx, kb0, kb1);
-                else stage_from_q8_1<FMT, M>(t, a.xq, NB, kb0, kb1);
-                __syncthreads();
-            }
-            if (active) {
-                if (FMT == FMT_Q4_0) rowgroup_chunk_q4_0<M, R, U>(p4, NB, rows, kb0, kb1, t, lane, acc);
-                else rowgroup_chunk_q6_k<M, R, U>(p6, NB, rows, kb0, kb1, t, lane, acc);
-            }
-        }
-        if (!active) continue;
-
-        float v[P];
+        for (int cc = 0; cc < nchunks; ++cc) {
+            const int kb0 = cc * KC, kb1 = min(NB, kb0 + KC);
+            __syncthreads();
+            if (TOP1) stage_from_f32<FMT, M>(t, a.x, a.ldx, kb0, kb1);
+            else stage_from_q8_1<FMT, M>(t, a.xq, NB, kb0, kb1);
+            __syncthreads();
+            if (!active) continue;
+            for (int b = kb0 + lane; b < kb1; b += 32) {
+                const int ti = b - kb0;
+                if (FMT == FMT_Q4_0) {
+                    uint4 w16[R];
+                    float dw[R];
 #pragma unroll
-        for (int i = 0; i < P; ++i) v[i] = i < V ? acc[i / M][i % M] : 0.0f;
-        warp_transpose_reduce<P>(v, lane);
-
-        if (!TOP1) {
-            if (reduced_value_owner<P>(lane)) {
-#pragma unroll
-                for (int j = 0; j < C; ++j) {
-                    const int vi = reduced_value_index<P>(lane, j);
-                    if (vi < V) {
-                        const int r = vi / M, m = vi - (vi / M) * M;
-                        const int n = n0 + r;
-                        if (n < a.N) a.y[(int64_t)m * a.ldy + n] = v[j];
+                    for (int r = 0; r < R; ++r) {
+                        const BlockAddr ad = block_addr(a.w_pack, g, rows[r], b);
+                        w16[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.tile + ad.j * 16));
+                        dw[r] = __half2float(__ushort_as_half(ld_stream_u16(ad.tile + ad.nb * 16 + ad.j * 2)));
                     }
-                }
-            }
-        } else {
-            unsigned long long* wk = s_keys + warp * 64;
-            if (reduced_value_owner<P>(lane)) {
+                    accumulate_q4_0<M, R>(w16, dw, t, ti, acc);
+                } else {
+                    uint4 ql[R];
+                    uint2 qh[R];
+                    uint32_t sc[R];
+                    float dw[R];
 #pragma unroll
-                for (int j = 0; j < C; ++j) {
-                    const int vi = reduced_value_index<P>(lane, j);
-                    if (vi < V) {
-                        const int n = n0 + vi / M;
-                        wk[vi] = n < a.N ? top1_key(v[j], n) : 0ull;
+                    for (int r = 0; r < R; ++r) {
+                        const BlockAddr ad = block_addr(a.w_pack, g, rows[r], b);
+                        ql[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.tile + ad.j * 16));
+                        qh[r] = ld_stream_v2(reinterpret_cast<const uint2*>(ad.tile + ad.nb * 16 + ad.j * 8));
+                        sc[r] = ld_stream_u16(ad.tile + ad.nb * 24 + ad.j * 2);
+                        dw[r] = __half2float(
+                            __ushort_as_half(ld_stream_u16(d6 + (int64_t)rows[r] * NSB + (b >> 3))));
                     }
+                    accumulate_q6_k<M, R>(ql, qh, sc, dw, t, ti, acc);
                 }
             }
-            __syncwarp();
-            if (lane < M) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const unsigned long long k = wk[r * M + lane];
-                    best = k > best ? k : best;
-                }
-            }
-            __syncwarp();
         }
+        if (active) finish_rowgroup<M, R, TOP1>(a, rg * R, acc, lane, s_keys + warp * 64, best);
     }
-
-    if (TOP1) {
-        int& s_last = *reinterpret_cast<int*>(s_best + MMVQ_WARPS * MAX_M);
-        if (lane < M) s_best[warp * MAX_M + lane] = best;
-        __syncthreads();
-        if (threadIdx.x < M) {
-            unsigned long long k = 0ull;
-            for (int w = 0; w < MMVQ_WARPS; ++w) {
-                const unsigned long long kw = s_best[w * MAX_M + threadIdx.x];
-                k = kw > k ? kw : k;
-            }
-            atomicMax(&a.ws->keys[threadIdx.x], k);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            const unsigned prev = atomicAdd(&a.ws->done, 1u);
-            s_last = prev == gridDim.x - 1;
-        }
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            if (threadIdx.x < M) {
-                const unsigned long long k = atomicExch(&a.ws->keys[threadIdx.x], 0ull);
-                a.ids[threadIdx.x] = top1_key_to_id(k);
-            }
-            if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
-        }
-    }
-}
-
-// Shared memory for one launch: activation tile + top-1 scratch.
-template <int M, bool TOP1>
-inline size_t mmvq_smem_bytes(int KC)
-{
-    size_t s = (size_t)M * KC * ACT_BYTES_PER_BLOCK;
-    if (TOP1) s += (size_t)MMVQ_WARPS * 64 * 8 + (size_t)MMVQ_WARPS * MAX_M * 8 + 16;
-    return s;
+    if (TOP1) top1_finish<M>(a, s_best, s_last, best, lane, warp, W);
 }
 
 }  // namespace qgemv

@@ -1,4 +1,4 @@
-// Instantiations of the Q6_K x Q8_1 MMVQ kernel for M = 1..17.
+// Instantiations of the Q6_K x Q8_1 MMVQ kernels for M = 1..17.
 #include "launch.cuh"
 
 namespace qgemv {
@@ -26,5 +26,7 @@ int launch_mmvq_q6_k(const MmvqArgs& a, int M, cudaStream_t s)
     default: return QGEMV_UNSUPPORTED_SHAPE;
     }
 }
+
+unsigned int take_wait_timeouts_q6_k() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

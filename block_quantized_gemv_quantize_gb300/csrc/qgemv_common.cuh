@@ -26,55 +26,89 @@ constexpr int Q6_K_BYTES = 210;
 constexpr int MAX_M = 17;
 
 // ---------------------------------------------------------------------------
-// Packed weight layouts (same total bytes as the canonical blocks).
+// Packed weight layouts.  A row of NB = K/32 blocks is cut into chunks of 32
+// blocks (the last chunk may be shorter, nb_tail blocks); each (row, chunk) is
+// one contiguous 16-byte-aligned tile, so a warp can fetch the tiles of its
+// rows with one bulk copy each and its lanes read consecutive blocks.
 //
-// Q4_0 pack, for N rows of K/32 blocks (NB = K/32), two streams:
-//   nib[N*NB]  16 B each: the canonical qs[16] bytes of block (n, b) unchanged
-//              (value i < 16 = low nibble of byte i, value i + 16 = high nibble)
-//   d  [N*NB]  fp16 bits of the block scale, copied raw
-// stream offsets: nib at 0, d at N*NB*16.
-//
-// Q6_K pack, per 32-value block (n, b), four streams:
-//   ql[N*NB]   16 B: byte t = low4(q[t]) | low4(q[t + 16]) << 4
-//   qh[N*NB]    8 B: byte t, bits 2s..2s+1 = high2(q[t + 8 s]), s = 0..3
-//   sc[N*NB]    2 B: the two int8 subscales of the block's 16-value halves
-//   d [N*NSB]  fp16 bits of the superblock scale (NSB = K/256), copied raw
-// stream offsets: ql at 0, qh at N*NB*16, sc at N*NB*24, d at N*NB*26.
-// With these layouts, 32 consecutive blocks of one row are 512 contiguous bytes
-// of nib / ql, so a warp whose lanes take consecutive blocks issues fully
-// coalesced 16-byte loads.
+// Q4_0 tile of nb blocks: nib[nb] (16 B each: the canonical qs bytes of the
+//   block, unchanged) | d[nb] (fp16 bits, copied raw) | zero pad to 16 B.
+//   Full tile 576 B; row = tiles back to back.  For K % 256 == 0 the pad is
+//   empty and the pack is exactly the canonical 18 B per block.
+// Q6_K tile of nb blocks (nb a multiple of 8):
+//   ql[nb] 16 B: byte t = low4(q[t]) | low4(q[t + 16]) << 4
+//   qh[nb]  8 B: byte t, bits 2s..2s+1 = high2(q[t + 8 s]), s = 0..3
+//   sc[nb]  2 B: the int8 subscales of the block's two 16-value halves
+//   Full tile 832 B.  After all N rows: d[N][K/256], fp16 superblock scales.
+//   Total = N * K/256 * 210 B, the canonical size.
 // ---------------------------------------------------------------------------
 
-struct PackQ40 {
-    const uint4* nib;
-    const __half* d;
+constexpr int CHUNK = 32;  // blocks per tile
+
+__host__ __device__ inline int pad16(int v) { return (v + 15) & ~15; }
+
+struct Geom {
+    int NB;          // blocks per row
+    int nch;         // chunks per row
+    int nb_tail;     // blocks in the last chunk
+    int full_tile;   // bytes of a 32-block tile
+    int tail_tile;   // bytes of the last tile
+    int64_t row;     // bytes of one row's tiles
+    __host__ __device__ int nb(int c) const { return c == nch - 1 ? nb_tail : CHUNK; }
+    __host__ __device__ int tile(int c) const { return c == nch - 1 ? tail_tile : full_tile; }
 };
 
-struct PackQ6K {
-    const uint4* ql;
-    const uint2* qh;
-    const uint16_t* sc;
-    const __half* d;
-};
+__host__ __device__ inline int q4_0_tile_bytes(int nb) { return nb * 16 + pad16(nb * 2); }
+__host__ __device__ inline int q6_k_tile_bytes(int nb) { return nb * 26; }
 
-__host__ __device__ inline PackQ40 pack_q4_0(const void* base, int64_t N, int NB)
+__host__ __device__ inline Geom geom_q4_0(int K)
 {
-    const char* p = static_cast<const char*>(base);
-    PackQ40 r;
-    r.nib = reinterpret_cast<const uint4*>(p);
-    r.d = reinterpret_cast<const __half*>(p + N * NB * 16);
+    Geom g;
+    g.NB = K / QK;
+    g.nch = (g.NB + CHUNK - 1) / CHUNK;
+    g.nb_tail = g.NB - (g.nch - 1) * CHUNK;
+    g.full_tile = q4_0_tile_bytes(CHUNK);
+    g.tail_tile = q4_0_tile_bytes(g.nb_tail);
+    g.row = (int64_t)(g.nch - 1) * g.full_tile + g.tail_tile;
+    return g;
+}
+
+__host__ __device__ inline Geom geom_q6_k(int K)
+{
+    Geom g;
+    g.NB = K / QK;
+    g.nch = (g.NB + CHUNK - 1) / CHUNK;
+    g.nb_tail = g.NB - (g.nch - 1) * CHUNK;
+    g.full_tile = q6_k_tile_bytes(CHUNK);
+    g.tail_tile = q6_k_tile_bytes(g.nb_tail);
+    g.row = (int64_t)g.NB * 26;
+    return g;
+}
+
+__host__ __device__ inline int64_t q4_0_pack_size(int64_t N, int K) { return N * geom_q4_0(K).row; }
+__host__ __device__ inline int64_t q6_k_pack_size(int64_t N, int K) { return N * ((int64_t)(K / QK) * 26 + (K / QK_K) * 2); }
+
+// Addresses of block b of row n inside a tile layout.
+struct BlockAddr {
+    const uint8_t* tile;  // start of the (row, chunk) tile
+    int j;                // block index inside the tile
+    int nb;               // blocks in the tile
+};
+
+__host__ __device__ inline BlockAddr block_addr(const void* base, const Geom& g, int64_t n, int b)
+{
+    const int c = b / CHUNK;
+    BlockAddr r;
+    r.tile = static_cast<const uint8_t*>(base) + n * g.row + (int64_t)c * g.full_tile;
+    r.j = b - c * CHUNK;
+    r.nb = g.nb(c);
     return r;
 }
 
-__host__ __device__ inline PackQ6K pack_q6_k(const void* base, int64_t N, int NB)
+// Q6_K superblock scales follow the N rows of tiles.
+__host__ __device__ inline const __half* q6_k_scales(const void* base, const Geom& g, int64_t N)
 {
-    const char* p = static_cast<const char*>(base);
-    PackQ6K r;
-    r.ql = reinterpret_cast<const uint4*>(p);
-    r.qh = reinterpret_cast<const uint2*>(p + N * NB * 16);
-    r.sc = reinterpret_cast<const uint16_t*>(p + N * NB * 24);
-    r.d = reinterpret_cast<const __half*>(p + N * NB * 26);
-    return r;
+    return reinterpret_cast<const __half*>(static_cast<const uint8_t*>(base) + N * g.row);
 }
 
 // ---------------------------------------------------------------------------
@@ -114,51 +148,57 @@ __device__ __forceinline__ void prefetch_l2(const void* p)
 }
 
 // ---------------------------------------------------------------------------
-// Q8_1 quantization of one 32-value block by one warp: lane i holds x_i.
+// Q8_1 quantization of one 32-value block by one thread.
 // d = max|x| / 127 (IEEE fp32 divide), q_i = round(x_i / d) with round half
 // away from zero; an all-zero block gives d = 0 and q = 0.  The stored scale is
 // the fp16 rounding (nearest even) of d; x is divided by the fp32 d.
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ float warp_max_f32(float v)
-{
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ int warp_sum_i32(int v)
-{
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Sum over the 16 lanes of this lane's half-warp.
-__device__ __forceinline__ int halfwarp_sum_i32(int v)
-{
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-struct Q81Lane {
-    int q;      // this lane's code
-    float d;    // fp32 scale of the block (before fp16 rounding)
+struct Q81Block {
+    uint32_t q[8];  // codes, 4 per word, value order
+    float d;        // fp32 scale (before fp16 rounding)
+    int s_lo, s_hi; // sum of codes 0..15 and 16..31
 };
 
-__device__ __forceinline__ Q81Lane q8_1_quantize_lane(float x)
+// xb: 32 consecutive fp32 values; vec4: xb is 16-byte aligned.
+__device__ __forceinline__ void q8_1_quantize_block(const float* xb, bool vec4, Q81Block& o)
 {
-    float amax = warp_max_f32(fabsf(x));
-    Q81Lane r;
-    r.d = __fdiv_rn(amax, 127.0f);
-    int q = 0;
-    if (amax != 0.0f) {
-        q = (int)roundf(__fdiv_rn(x, r.d));
-        q = max(-127, min(127, q));
+    float v[32];
+    if (vec4) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 f = reinterpret_cast<const float4*>(xb)[k];
+            v[4 * k + 0] = f.x;
+            v[4 * k + 1] = f.y;
+            v[4 * k + 2] = f.z;
+            v[4 * k + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = xb[k];
     }
-    r.q = q;
-    return r;
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+    o.d = __fdiv_rn(amax, 127.0f);
+    int s0 = 0, s1 = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            int q = 0;
+            if (amax != 0.0f) {
+                q = (int)roundf(__fdiv_rn(v[4 * w + t], o.d));
+                q = max(-127, min(127, q));
+            }
+            word |= ((uint32_t)q & 0xFFu) << (8 * t);
+            if (w < 4) s0 += q; else s1 += q;
+        }
+        o.q[w] = word;
+    }
+    o.s_lo = s0;
+    o.s_hi = s1;
 }
 
 // ---------------------------------------------------------------------------
@@ -187,6 +227,13 @@ __device__ __forceinline__ uint32_t act_meta_sums(const uint32_t (&q)[8])
     for (int i = 4; i < 8; ++i) s1 = __dp4a((int)q[i], 0x01010101, s1);
     if (FMT == FMT_Q4_0) return (uint32_t)(-8 * (s0 + s1));
     return ((uint32_t)s0 & 0xFFFFu) | ((uint32_t)s1 << 16);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t act_meta_from_sums(int s_lo, int s_hi)
+{
+    if (FMT == FMT_Q4_0) return (uint32_t)(-8 * (s_lo + s_hi));
+    return ((uint32_t)s_lo & 0xFFFFu) | ((uint32_t)s_hi << 16);
 }
 
 // Read one canonical Q8_1 block from global memory (4-byte aligned) into the

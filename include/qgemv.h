@@ -62,8 +62,9 @@ const char* qgemv_status_string(int status);
 
 /* Bytes of the Q8_1 activation for M rows of K values: M * (K/32) * 36. */
 size_t q8_1_bytes(int M, int K);
-/* Bytes of a packed Q4_0 weight of N rows of K values: N * (K/32) * 18
- * (the canonical size; the pack only reorders bytes). */
+/* Bytes of a packed Q4_0 weight of N rows of K values.  Equal to the
+ * canonical N * (K/32) * 18 when K % 256 == 0; otherwise each row's last
+ * tile is padded to 16 bytes (at most 14 bytes per row). */
 size_t q4_0_pack_bytes(int N, int K);
 /* Bytes of a packed Q6_K weight: N * (K/256) * 210 (the canonical size). */
 size_t q6_k_pack_bytes(int N, int K);
@@ -85,9 +86,10 @@ int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* str
 
 /* ---- A2: weight repackers (offline) ------------------------------------ */
 
-/* qpack_q4_0 - reorder canonical Q4_0 blocks into the kernel's coalesced
- * streams (a nibble stream of 16-byte blocks, then the fp16 scales; raw
- * bits, same total size).  [closure] "What materially worked" item 3
+/* qpack_q4_0 - reorder canonical Q4_0 blocks into the kernel's tiles: each
+ * row is cut into chunks of 32 blocks, and each (row, chunk) tile holds the
+ * chunk's 16-byte code blocks followed by its fp16 scales (raw bits), padded
+ * to 16 bytes; one tile is one aligned bulk copy.  [closure] "What materially worked" item 3
  * (offline-packed projections) and "Transfer" rule 7 (copy fp16 storage
  * bits, never convert them).
  *   w_canon  uint8 [N][K/32][18] device   (read)
@@ -95,8 +97,10 @@ int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* str
  *   N >= 1, K % 32 == 0. */
 int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream);
 
-/* qpack_q6_k - reorder canonical Q6_K superblocks into four streams (low
- * nibbles, high bit pairs, subscales, fp16 scales; raw bits, same size).
+/* qpack_q6_k - reorder canonical Q6_K superblocks into the kernel's tiles:
+ * per (row, 32-block chunk) the low nibbles (16 B per block), the high bit
+ * pairs (8 B per block) and the subscales (2 B per block), all rows' tiles
+ * back to back, then the fp16 superblock scales (raw bits); same size.
  * [record] "Why this was slow" (the Q6_K output tensor is packed once).
  *   w_canon  uint8 [N][K/256][210] device (read)
  *   w_pack   q6_k_pack_bytes(N, K) device (written; must not alias w_canon)
@@ -165,6 +169,13 @@ int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, 
  *   out  int32 [M][N][K/32] device (written). */
 int qgemv_block_dots_q4_0(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream);
 int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream);
+
+/* qgemv_take_wait_timeouts - number of warps that, since the previous call,
+ * waited about a second for a weight copy that never completed and gave up
+ * (their outputs are then invalid); resets the count.  Synchronous: it reads
+ * a device counter.  0 in normal operation.  (Not from the pages: a guard of
+ * this implementation's bounded waits.) */
+int qgemv_take_wait_timeouts(unsigned int* count);
 
 #ifdef __cplusplus
 }

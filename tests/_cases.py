@@ -7,41 +7,98 @@ import numpy as np
 # ---------------------------------------------------------------- pack layouts (inverse, numpy)
 
 
+CHUNK = 32
+
+
+def _pad16(v: int) -> int:
+    return (v + 15) & ~15
+
+
+def _chunks(nb: int):
+    """(first block, blocks) of each 32-block chunk of a row."""
+    return [(c, min(CHUNK, nb - c)) for c in range(0, nb, CHUNK)]
+
+
+def pack_q4_0(w: np.ndarray) -> np.ndarray:
+    """Canonical Q4_0 [N, K/32, 18] -> the documented tile layout: per
+    (row, 32-block chunk) the 16-byte code blocks, then their fp16 scales,
+    zero-padded to 16 bytes."""
+    N, nb, _ = w.shape
+    rows = []
+    for c0, n in _chunks(nb):
+        nib = w[:, c0:c0 + n, 2:18].reshape(N, n * 16)
+        d = w[:, c0:c0 + n, 0:2].reshape(N, n * 2)
+        pad = np.zeros((N, _pad16(n * 2) - n * 2), dtype=np.uint8)
+        rows += [nib, d, pad]
+    return np.concatenate(rows, axis=1).reshape(-1)
+
+
 def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
-    """Packed Q4_0 bytes -> canonical [N, K/32, 18]: a 16-byte nibble stream
-    followed by a stream of fp16 scales."""
+    """Inverse of pack_q4_0."""
     nb = K // 32
-    nib = pack[: N * nb * 16].reshape(N, nb, 16)
-    d = pack[N * nb * 16: N * nb * 18].reshape(N, nb, 2)
-    return np.concatenate([d, nib], axis=2)
+    row_bytes = sum(n * 16 + _pad16(n * 2) for _, n in _chunks(nb))
+    rows = pack[: N * row_bytes].reshape(N, row_bytes)
+    out = np.zeros((N, nb, 18), dtype=np.uint8)
+    off = 0
+    for c0, n in _chunks(nb):
+        out[:, c0:c0 + n, 2:18] = rows[:, off:off + n * 16].reshape(N, n, 16)
+        out[:, c0:c0 + n, 0:2] = rows[:, off + n * 16: off + n * 18].reshape(N, n, 2)
+        off += n * 16 + _pad16(n * 2)
+    return out
+
+
+def _q6_k_codes(w: np.ndarray) -> np.ndarray:
+    """Canonical Q6_K [N, K/256, 210] -> codes [N, K] (sequential packing)."""
+    N, ns, _ = w.shape
+    ql = w[:, :, 0:128].astype(np.int64)
+    qh = w[:, :, 128:192].astype(np.int64)
+    lo = np.stack([ql & 0x0F, ql >> 4], axis=3).reshape(N, ns, 256)
+    hi = np.stack([(qh >> s) & 3 for s in (0, 2, 4, 6)], axis=3).reshape(N, ns, 256)
+    return (lo | (hi << 4)).reshape(N, ns * 256)
+
+
+def pack_q6_k(w: np.ndarray) -> np.ndarray:
+    """Canonical Q6_K -> the documented tile layout: per (row, 32-block chunk)
+    ql (byte t = low4(q_t) | low4(q_t+16) << 4), qh (byte t, bits 2s =
+    high2(q_t+8s)), sc (the block's two subscales); then all fp16 scales."""
+    N, ns, _ = w.shape
+    nb = ns * 8
+    q = _q6_k_codes(w).reshape(N, nb, 32)
+    ql = ((q[:, :, 0:16] & 0x0F) | ((q[:, :, 16:32] & 0x0F) << 4)).astype(np.uint8)
+    hi = q >> 4
+    qh = np.zeros((N, nb, 8), dtype=np.int64)
+    for s in range(4):
+        qh |= hi[:, :, 8 * s: 8 * s + 8] << (2 * s)
+    qh = qh.astype(np.uint8)
+    sc = w[:, :, 192:208].reshape(N, nb, 2)
+    parts = []
+    for c0, n in _chunks(nb):
+        parts += [ql[:, c0:c0 + n].reshape(N, -1), qh[:, c0:c0 + n].reshape(N, -1), sc[:, c0:c0 + n].reshape(N, -1)]
+    tiles = np.concatenate(parts, axis=1).reshape(-1)
+    return np.concatenate([tiles, w[:, :, 208:210].reshape(-1)])
 
 
 def unpack_q6_k(pack: np.ndarray, N: int, K: int) -> np.ndarray:
-    """Packed Q6_K bytes -> canonical [N, K/256, 210].
-
-    Per 32-value block: ql byte t = low4(q[t]) | low4(q[t+16]) << 4;
-    qh byte t, bits 2s = high2(q[t + 8 s]); sc = the block's two subscales;
-    then one fp16 scale per superblock."""
+    """Inverse of pack_q6_k."""
     nb, ns = K // 32, K // 256
-    nblk = N * nb
-    ql = pack[: nblk * 16].reshape(nblk, 16).astype(np.int64)
-    qh = pack[nblk * 16: nblk * 24].reshape(nblk, 8).astype(np.int64)
-    sc = pack[nblk * 24: nblk * 26].reshape(N, ns, 16)
-    d = pack[nblk * 26: nblk * 26 + N * ns * 2].reshape(N, ns, 2)
-    q = np.zeros((nblk, 32), dtype=np.int64)
-    q[:, 0:16] = ql & 0x0F
-    q[:, 16:32] = ql >> 4
+    rows = pack[: N * nb * 26].reshape(N, nb * 26)
+    ql = np.zeros((N, nb, 16), dtype=np.int64)
+    qh = np.zeros((N, nb, 8), dtype=np.int64)
+    sc = np.zeros((N, nb, 2), dtype=np.uint8)
+    off = 0
+    for c0, n in _chunks(nb):
+        ql[:, c0:c0 + n] = rows[:, off:off + 16 * n].reshape(N, n, 16)
+        qh[:, c0:c0 + n] = rows[:, off + 16 * n: off + 24 * n].reshape(N, n, 8)
+        sc[:, c0:c0 + n] = rows[:, off + 24 * n: off + 26 * n].reshape(N, n, 2)
+        off += 26 * n
+    q = np.zeros((N, nb, 32), dtype=np.int64)
+    q[:, :, 0:16] = ql & 0x0F
+    q[:, :, 16:32] = ql >> 4
     for s in range(4):
-        q[:, 8 * s: 8 * s + 8] |= ((qh >> (2 * s)) & 3) << 4
-    q = q.reshape(N, ns, 256)
-    canon = np.zeros((N, ns, 210), dtype=np.uint8)
-    lo = (q & 0x0F).reshape(N, ns, 128, 2)
-    canon[:, :, 0:128] = (lo[..., 0] | (lo[..., 1] << 4)).astype(np.uint8)
-    hi = (q >> 4).reshape(N, ns, 64, 4)
-    canon[:, :, 128:192] = (hi[..., 0] | (hi[..., 1] << 2) | (hi[..., 2] << 4) | (hi[..., 3] << 6)).astype(np.uint8)
-    canon[:, :, 192:208] = sc
-    canon[:, :, 208:210] = d
-    return canon
+        q[:, :, 8 * s: 8 * s + 8] |= ((qh >> (2 * s)) & 3) << 4
+    d = pack[N * nb * 26: N * nb * 26 + N * ns * 2].reshape(N, ns, 2)
+    return q6_k_from_codes(q.reshape(N, K), sc.reshape(N, K // 16).view(np.int8),
+                           d.copy().view(np.uint16).reshape(N, ns))
 
 
 def q6_k_from_codes(codes: np.ndarray, sc: np.ndarray, d16_bits: np.ndarray) -> np.ndarray:

@@ -56,19 +56,21 @@ def test_quantize_q8_1_bit_exact(ops, M, K, ldx):
 
 # ---------------------------------------------------------------- A2 pack
 
-@pytest.mark.parametrize("N,K", [(1, 32), (7, 256), (300, 5120)])
-def test_qpack_q4_0_round_trip(ops, N, K):
+@pytest.mark.parametrize("N,K", [(1, 32), (3, 96), (7, 256), (5, 1056), (300, 5120)])
+def test_qpack_q4_0_layout(ops, N, K):
     w = synth.q4_0_weights(N, K, seed=N)
     p = _np(ops.qpack_q4_0(_t(w), N, K))
-    assert p.size == w.size
+    assert p.size == ops.q4_0_pack_bytes(N, K)
+    assert np.array_equal(p, C.pack_q4_0(w))
     assert np.array_equal(C.unpack_q4_0(p, N, K), w)
 
 
-@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (300, 5120)])
-def test_qpack_q6_k_round_trip(ops, N, K):
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (3, 768), (300, 5120)])
+def test_qpack_q6_k_layout(ops, N, K):
     w = synth.q6_k_weights(N, K, seed=N)
     p = _np(ops.qpack_q6_k(_t(w), N, K))
     assert p.size == w.size
+    assert np.array_equal(p, C.pack_q6_k(w))
     assert np.array_equal(C.unpack_q6_k(p, N, K), w)
 
 
@@ -108,7 +110,8 @@ def _gemv_case(ops, fmt, M, K, N, seed):
     return _np(y), y_ref, S
 
 
-@pytest.mark.parametrize("M,K,N", GEMV_SHAPES)
+@pytest.mark.parametrize("M,K,N", GEMV_SHAPES + [(M, K, N) for M in (1, 6, 17) for (K, N) in ((32, 5), (96, 37),
+                                                                                           (1056, 129))])
 def test_qgemv_q4_0_matches_oracle(ops, M, K, N):
     y, y_ref, S = _gemv_case(ops, "q4_0", M, K, N, seed=10 * M + K)
     r = C.check_close(y, y_ref, S)
@@ -221,3 +224,8 @@ def test_errors_are_reported_before_launch(ops):
         ops.lmhead_q6_k_top1(w, torch.zeros((2, 256), device=DEV), 256, 5,
                              ws=torch.zeros(8, dtype=torch.uint8, device=DEV))
     assert e.value.status == -4
+
+
+def test_no_wait_timeouts(ops):
+    # every bounded wait for a weight copy in this process completed
+    assert ops.qgemv_take_wait_timeouts() == 0

@@ -184,3 +184,7 @@ def test_adversarial_near_tie(ops, vocab):
         assert _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V)).tolist() == ids.tolist()
     finally:
         _set_rows(ops, vocab, pair, saved)
+
+
+def test_no_wait_timeouts(ops):
+    assert ops.qgemv_take_wait_timeouts() == 0

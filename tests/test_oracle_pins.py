@@ -296,3 +296,26 @@ def test_top1_matches_brute_force_argmax():
     ids, y, _ = oracle.lmhead_q6_k_top1(w, x)
     ref = oracle.dequant_q8_1_np(oracle.quantize_q8_1(x)) @ oracle.dequant_q6_k_np(w).T
     assert ids.tolist() == np.argmax(ref, axis=1).tolist()
+
+
+# ---------------------------------------------------------------- pack layout model (test helpers)
+
+@pytest.mark.parametrize("N,K", [(3, 32), (2, 96), (5, 256), (4, 1056), (3, 5120)])
+def test_pack_q4_0_model_round_trip(N, K):
+    from tests import _cases as C
+
+    w = synth.q4_0_weights(N, K, seed=K)
+    p = C.pack_q4_0(w)
+    if K % 256 == 0:
+        assert p.size == w.size
+    assert np.array_equal(C.unpack_q4_0(p, N, K), w)
+
+
+@pytest.mark.parametrize("N,K", [(3, 256), (2, 768), (4, 5120)])
+def test_pack_q6_k_model_round_trip(N, K):
+    from tests import _cases as C
+
+    w = synth.q6_k_weights(N, K, seed=K)
+    p = C.pack_q6_k(w)
+    assert p.size == w.size
+    assert np.array_equal(C.unpack_q6_k(p, N, K), w)
