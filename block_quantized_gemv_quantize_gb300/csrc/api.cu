@@ -52,8 +52,14 @@ const char* qgemv_status_string(int status)
 }
 
 size_t q8_1_bytes(int M, int K) { return (M < 0 || K < 0) ? 0 : (size_t)M * (size_t)(K / QK) * Q8_1_BYTES; }
-size_t q4_0_pack_bytes(int N, int K) { return (N < 1 || K < QK) ? 0 : (size_t)q4_0_pack_size(N, K); }
-size_t q6_k_pack_bytes(int N, int K) { return (N < 1 || K < QK_K) ? 0 : (size_t)q6_k_pack_size(N, K); }
+size_t q4_0_pack_bytes(int N, int K)
+{
+    return (N < 1 || K < QK) ? 0 : (size_t)make_layout(FMT_Q4_0, N, K).total_bytes();
+}
+size_t q6_k_pack_bytes(int N, int K)
+{
+    return (N < 1 || K < QK_K) ? 0 : (size_t)make_layout(FMT_Q6_K, N, K).total_bytes();
+}
 size_t lmhead_q6_k_top1_workspace_bytes(int, int, int) { return top1_ws_bytes(); }
 size_t argmax_f32_rows_workspace_bytes(int, int) { return top1_ws_bytes(); }
 

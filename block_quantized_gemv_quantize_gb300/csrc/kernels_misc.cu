@@ -66,35 +66,34 @@ int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cu
 
 __global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
 {
-    const Geom g = geom_q4_0(K);
-    const int64_t nblocks = (int64_t)N * g.NB;
+    const Layout L = make_layout(FMT_Q4_0, N, K);
+    const int64_t nblocks = (int64_t)N * L.NB;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t n = i / g.NB;
-        const int b = (int)(i - n * g.NB);
+        const int64_t n = i / L.NB;
+        const int b = (int)(i - n * L.NB);
         const uint16_t* src = reinterpret_cast<const uint16_t*>(canon + i * Q4_0_BYTES);  // 2-byte aligned
         uint32_t q[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) q[k] = (uint32_t)src[1 + 2 * k] | ((uint32_t)src[2 + 2 * k] << 16);
-        const BlockAddr ad = block_addr(pack, g, n, b);
+        const BlockAddr ad = block_addr(pack, L, n, b);
         uint8_t* tile = const_cast<uint8_t*>(ad.tile);
         reinterpret_cast<uint4*>(tile)[ad.j] = make_uint4(q[0], q[1], q[2], q[3]);
         reinterpret_cast<uint16_t*>(tile + ad.nb * 16)[ad.j] = src[0];
         if (ad.j == 0) {  // zero the tile's pad bytes (present only when nb % 8 != 0)
-            for (int p = ad.nb * 18; p < q4_0_tile_bytes(ad.nb); ++p) tile[p] = 0;
+            for (int p = ad.nb * 18; p < pad16(ad.nb * 2) + ad.nb * 16; ++p) tile[p] = 0;
         }
     }
 }
 
 __global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
 {
-    const Geom g = geom_q6_k(K);
-    const int64_t nblocks = (int64_t)N * g.NB;
-    uint16_t* dd = reinterpret_cast<uint16_t*>(pack + (int64_t)N * g.row);
+    const Layout L = make_layout(FMT_Q6_K, N, K);
+    const int64_t nblocks = (int64_t)N * L.NB;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t n = i / g.NB;
-        const int b = (int)(i - n * g.NB);
+        const int64_t n = i / L.NB;
+        const int b = (int)(i - n * L.NB);
         const int64_t sbi = i >> 3;  // superblock index (n * NSB + b / 8)
         const int bb = b & 7;
         const uint8_t* sb = canon + sbi * Q6_K_BYTES;
@@ -123,13 +122,20 @@ __global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
             for (int s2 = 0; s2 < 4; ++s2) byte |= (uint32_t)(q[t + 8 * s2] >> 4) << (2 * s2);
             wh[t >> 2] |= byte << (8 * (t & 3));
         }
-        const BlockAddr ad = block_addr(pack, g, n, b);
+        const BlockAddr ad = block_addr(pack, L, n, b);
         uint8_t* tile = const_cast<uint8_t*>(ad.tile);
         reinterpret_cast<uint4*>(tile)[ad.j] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         reinterpret_cast<uint2*>(tile + ad.nb * 16)[ad.j] = make_uint2(wh[0], wh[1]);
         reinterpret_cast<uint16_t*>(tile + ad.nb * 24)[ad.j] =
             (uint16_t)sb[192 + 2 * bb] | ((uint16_t)sb[192 + 2 * bb + 1] << 8);
-        if (bb == 0) dd[sbi] = (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
+        uint8_t* dq = const_cast<uint8_t*>(ad.dq6);
+        if (bb == 0)
+            reinterpret_cast<uint16_t*>(dq)[ad.r * (ad.nb >> 3) + (ad.j >> 3)] =
+                (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
+        if (ad.r == 0 && ad.j == 0) {  // zero the scale part's pad bytes
+            const int rows = L.rows_in(n / GROUP);
+            for (int p = rows * (ad.nb >> 3) * 2; p < pad16(rows * (ad.nb >> 3) * 2); ++p) dq[p] = 0;
+        }
     }
 }
 
@@ -293,11 +299,11 @@ __global__ void block_dots_kernel(const void* __restrict__ w_pack, const uint8_t
         act_from_q8_1<FMT>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES, lo, hi, meta);
         uint32_t w[8];
         if (FMT == FMT_Q4_0) {
-            const BlockAddr ad = block_addr(w_pack, geom_q4_0(NB * QK), n, b);
+            const BlockAddr ad = block_addr(w_pack, make_layout(FMT_Q4_0, N, NB * QK), n, b);
             q4_0_unpack(reinterpret_cast<const uint4*>(ad.tile)[ad.j], w);
             out[i] = q4_0_dot(w, lo, hi, (int)meta.y);
         } else {
-            const BlockAddr ad = block_addr(w_pack, geom_q6_k(NB * QK), n, b);
+            const BlockAddr ad = block_addr(w_pack, make_layout(FMT_Q6_K, N, NB * QK), n, b);
             q6_k_unpack(reinterpret_cast<const uint4*>(ad.tile)[ad.j],
                         reinterpret_cast<const uint2*>(ad.tile + ad.nb * 16)[ad.j], w);
             out[i] = q6_k_dot(w, lo, hi, meta.y, reinterpret_cast<const uint16_t*>(ad.tile + ad.nb * 24)[ad.j]);

@@ -45,32 +45,31 @@ struct MmvqPlan {
 template <int FMT, int M, bool TOP1>
 MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N)
 {
-    constexpr int R = RowsPerWarp<M>::value;
-    const Geom g = fmt_geom<FMT>(K);
-    const int n_rg = (N + R - 1) / R;
+    const Layout L = make_layout(FMT, N, K);
+    const int max_warps = MmvqThreads<M>::value / 32;
     MmvqPlan p{};
-    p.grid = n_rg < di.sms ? n_rg : di.sms;
-    const int per_cta = (n_rg + p.grid - 1) / p.grid;
-    p.warps = per_cta < MMVQ_MAX_WARPS ? per_cta : MMVQ_MAX_WARPS;
-    const size_t act = (size_t)M * g.NB * ACT_BYTES_PER_BLOCK;
+    p.grid = L.n_groups < di.sms ? (int)L.n_groups : di.sms;
+    const int64_t per_cta = (L.n_groups + p.grid - 1) / p.grid;
+    p.warps = per_cta < max_warps ? (int)per_cta : max_warps;
+    const size_t act = (size_t)M * L.NB * ACT_BYTES_PER_BLOCK;
     const size_t extra = TOP1 ? top1_scratch_bytes(p.warps) : 0;
-    const size_t stage = (size_t)R * g.full_tile;
+    const size_t stage = (size_t)L.chunk_bytes(GROUP, 0);
     const size_t fixed = act + extra + 128;
     long long s = fixed < (size_t)di.smem_optin ? (long long)(((size_t)di.smem_optin - fixed) / (p.warps * (stage + 8))) : 0;
     if (s > MAX_RING_STAGES) s = MAX_RING_STAGES;
     if (s >= 2) {
         p.ring = true;
         p.stages = (int)s;
-        p.KC = g.NB;
+        p.KC = L.NB;
         p.smem = (size_t)p.warps * p.stages * (stage + 8) + act + extra;
         return p;
     }
     p.ring = false;
-    p.warps = MMVQ_MAX_WARPS;
-    const int n_items = (n_rg + p.warps - 1) / p.warps;
-    p.grid = n_items < di.sms ? n_items : di.sms;
+    p.warps = max_warps;
+    const int64_t n_items = (L.n_groups + p.warps - 1) / p.warps;
+    p.grid = n_items < di.sms ? (int)n_items : di.sms;
     const size_t ex = TOP1 ? top1_scratch_bytes(p.warps) : 0;
-    p.KC = mmvq_chunk_blocks(di, M, g.NB, ex);
+    p.KC = mmvq_chunk_blocks(di, M, L.NB, ex);
     p.stages = 0;
     p.smem = (size_t)M * p.KC * ACT_BYTES_PER_BLOCK + ex;
     return p;

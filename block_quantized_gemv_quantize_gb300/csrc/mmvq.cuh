@@ -33,11 +33,15 @@ namespace qgemv {
 constexpr int MMVQ_MAX_THREADS = 512;
 constexpr int MMVQ_MAX_WARPS = MMVQ_MAX_THREADS / 32;
 
-// Rows per warp for a given M: R * M partial sums per lane.
+// Threads per CTA: 16 warps while the R x M partial sums are few; 8 warps
+// (and so up to 255 registers per thread) for M > 8.
 template <int M>
-struct RowsPerWarp {
-    static constexpr int value = M <= 8 ? 4 : 2;
+struct MmvqThreads {
+    static constexpr int value = M <= 8 ? 512 : 256;
 };
+
+// Rows per warp: one 4-row group of the packed layout.
+constexpr int R_ROWS = GROUP;
 
 constexpr int next_pow2(int v) { return v <= 1 ? 1 : 2 * next_pow2((v + 1) / 2); }
 constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
@@ -363,33 +367,28 @@ __device__ __forceinline__ void top1_finish(const MmvqArgs& a, unsigned long lon
 // Shared memory besides the activation tile and the rings, for TOP1.
 inline size_t top1_scratch_bytes(int nwarps) { return (size_t)nwarps * 64 * 8 + (size_t)nwarps * MAX_M * 8 + 16; }
 
-template <int FMT>
-__host__ __device__ inline Geom fmt_geom(int K)
-{
-    return FMT == FMT_Q4_0 ? geom_q4_0(K) : geom_q6_k(K);
-}
-
 // ---------------------------------------------------------------------------
 // Ring kernel: the whole activation in shared memory, weights streamed by
 // per-warp TMA rings.
-//   shared memory: rings [W][S][R * full_tile] | aq [M][2][NB] | am [M][NB] |
+//   shared memory: rings [W][S][stage] | aq [M][2][NB] | am [M][NB] |
 //                  mbarriers [W][S] | TOP1 scratch
-// The CTA's row groups are rg0 .. rg1-1; warp w takes rg0 + w, rg0 + w + W, ...
-// Job j of a warp = (its group j / nch, chunk j % nch), in stage j % S.
+// The CTA's groups are g0 .. g1-1; warp w takes g0 + w, g0 + w + W, ...
+// Job j of a warp = (its group j / nch, chunk j % nch), in stage j % S: one
+// bulk copy of the group-chunk (4 rows' tiles and, for Q6_K, their scales).
 // Waits are bounded: a warp that waits about a second for a copy counts a
 // timeout in *timeouts, stops, and gives its copies in flight a bounded wait.
 // ---------------------------------------------------------------------------
 
 template <int FMT, int M, bool TOP1>
-__global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
+__global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
 {
-    constexpr int R = RowsPerWarp<M>::value;
+    constexpr int R = R_ROWS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
     const int S = a.stages;
-    const Geom g = fmt_geom<FMT>(a.K);
-    const int NB = g.NB, nch = g.nch;
-    const int stage_bytes = R * g.full_tile;
+    const Layout L = make_layout(FMT, a.N, a.K);
+    const int NB = L.NB, nch = L.nch;
+    const int stage_bytes = L.chunk_bytes(R, 0);
 
     uint8_t* rings = smem;
     ActTile t;
@@ -401,10 +400,9 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const Mm
     unsigned long long* s_best = s_keys + W * 64;                                     // [W][MAX_M]
     int* s_last = reinterpret_cast<int*>(s_best + W * MAX_M);
 
-    const int n_rg = (a.N + R - 1) / R;
-    const int rg0 = (int)((int64_t)blockIdx.x * n_rg / gridDim.x);
-    const int rg1 = (int)((int64_t)(blockIdx.x + 1) * n_rg / gridDim.x);
-    const int n_my = warp < rg1 - rg0 ? (rg1 - rg0 - warp + W - 1) / W : 0;
+    const int64_t g0 = (int64_t)blockIdx.x * L.n_groups / gridDim.x;
+    const int64_t g1 = (int64_t)(blockIdx.x + 1) * L.n_groups / gridDim.x;
+    const int n_my = warp < g1 - g0 ? (int)((g1 - g0 - warp + W - 1) / W) : 0;
     const int J = n_my * nch;
 
     uint64_t* wbar = bars + warp * S;
@@ -418,20 +416,20 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const Mm
     }
     __syncwarp();
 
-    int issued = 0;
-    // Lane 0 issues the next job: R bulk copies of its rows' tiles for one chunk.
+    // Issue cursor (lane 0): next job's group, chunk and stage.
+    int issued = 0, iss_c = 0, iss_slot = 0;
+    int64_t iss_g = g0 + warp;
     auto issue_next = [&]() {
-        const int j = issued++;
-        const int i = j / nch, c = j - i * nch;
-        const int rg = rg0 + warp + i * W;
-        const int tb = g.tile(c);
-        uint64_t* bar = &wbar[j % S];
-        uint8_t* dst = wring + (size_t)(j % S) * stage_bytes;
-        mbar_arrive_expect_tx(bar, (uint32_t)(R * tb));
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int64_t n = min(rg * R + r, a.N - 1);
-            bulk_g2s(dst + r * tb, wbase + n * g.row + (int64_t)c * g.full_tile, (uint32_t)tb, bar, pol);
+        const int rows = L.rows_in(iss_g);
+        const uint32_t bytes = (uint32_t)L.chunk_bytes(rows, iss_c);
+        uint64_t* bar = &wbar[iss_slot];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(wring + (size_t)iss_slot * stage_bytes, wbase + L.chunk_offset(iss_g, iss_c), bytes, bar, pol);
+        ++issued;
+        if (++iss_slot == S) iss_slot = 0;
+        if (++iss_c == nch) {
+            iss_c = 0;
+            iss_g += W;
         }
     };
     if (lane == 0) {
@@ -443,39 +441,16 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const Mm
     else stage_from_q8_1<FMT, M>(t, a.xq, NB, 0, NB);
     __syncthreads();
 
-    const __half* d6 = FMT == FMT_Q6_K ? q6_k_scales(a.w_pack, g, a.N) : nullptr;
-    const int NSB = NB / 8;
-    // Q6_K superblock scales of job j for this lane, fetched one job ahead.
-    auto load_d6 = [&](int j, uint16_t (&d)[R]) {
-        const int i = j / nch, c = j - i * nch;
-        const int rg = rg0 + warp + i * W;
-        const int b = min(c * CHUNK + lane, NB - 1);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int64_t n = min(rg * R + r, a.N - 1);
-            d[r] = ld_stream_u16(d6 + n * NSB + (b >> 3));
-        }
-    };
-    uint16_t dnext[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) dnext[r] = 0;
-    if (FMT == FMT_Q6_K && J > 0) load_d6(0, dnext);
-
     unsigned long long best = 0ull;
     float acc[R][M];
     int consumed = 0;
+    int c = 0, slot = 0;
+    uint32_t phase = 0;
+    int64_t g = g0 + warp;
     for (int j = 0; j < J; ++j) {
-        const int i = j / nch, c = j - i * nch;
-        const int rg = rg0 + warp + i * W;
         if (lane == 0 && issued < J) {
             fence_proxy_async();
             issue_next();
-        }
-        uint16_t dcur[R];
-        if (FMT == FMT_Q6_K) {
-#pragma unroll
-            for (int r = 0; r < R; ++r) dcur[r] = dnext[r];
-            if (j + 1 < J) load_d6(j + 1, dnext);
         }
         if (c == 0) {
 #pragma unroll
@@ -483,14 +458,14 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const Mm
 #pragma unroll
                 for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
         }
-        const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&wbar[j % S], (uint32_t)((j / S) & 1)));
+        const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&wbar[slot], phase));
         if (!ready) {
             if (lane == 0) atomicAdd(timeouts, 1u);
             break;
         }
         consumed = j + 1;
-        const int nb = g.nb(c), tb = g.tile(c);
-        const uint8_t* st = wring + (size_t)(j % S) * stage_bytes;
+        const int nb = L.nb(c), tb = L.tile(c);
+        const uint8_t* st = wring + (size_t)slot * stage_bytes;
         if (lane < nb) {
             const int ti = c * CHUNK + lane;
             if (FMT == FMT_Q4_0) {
@@ -504,6 +479,8 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const Mm
                 }
                 accumulate_q4_0<M, R>(w16, dw, t, ti, acc);
             } else {
+                const int rows = L.rows_in(g);
+                const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * tb);
                 uint4 ql[R];
                 uint2 qh[R];
                 uint32_t sc[R];
@@ -513,18 +490,27 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const Mm
                     ql[r] = *reinterpret_cast<const uint4*>(st + r * tb + lane * 16);
                     qh[r] = *reinterpret_cast<const uint2*>(st + r * tb + nb * 16 + lane * 8);
                     sc[r] = *reinterpret_cast<const uint16_t*>(st + r * tb + nb * 24 + lane * 2);
-                    dw[r] = __half2float(__ushort_as_half(dcur[r]));
+                    // rows past the group's end read stale scales; their sums are discarded
+                    dw[r] = __half2float(__ushort_as_half(dq[min(r, rows - 1) * (nb >> 3) + (lane >> 3)]));
                 }
                 accumulate_q6_k<M, R>(ql, qh, sc, dw, t, ti, acc);
             }
         }
         __syncwarp();
-        if (c == nch - 1) finish_rowgroup<M, R, TOP1>(a, rg * R, acc, lane, s_keys + warp * 64, best);
+        if (c == nch - 1) finish_rowgroup<M, R, TOP1>(a, (int)(g * GROUP), acc, lane, s_keys + warp * 64, best);
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+        if (++c == nch) {
+            c = 0;
+            g += W;
+        }
     }
     // After a timeout, give the copies still in flight a bounded wait before
     // the shared memory is released.
     if (lane == 0) {
-        for (int j = consumed; j < issued; ++j) mbar_wait_bounded(&wbar[j % S], (uint32_t)((j / S) & 1));
+        for (int jj = consumed; jj < issued; ++jj) mbar_wait_bounded(&wbar[jj % S], (uint32_t)((jj / S) & 1));
     }
     __syncwarp();
 
@@ -539,13 +525,13 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_ring_kernel(const Mm
 // ---------------------------------------------------------------------------
 
 template <int FMT, int M, bool TOP1>
-__global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_lockstep_kernel(const MmvqArgs a)
+__global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_lockstep_kernel(const MmvqArgs a)
 {
-    constexpr int R = RowsPerWarp<M>::value;
+    constexpr int R = R_ROWS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
-    const Geom g = fmt_geom<FMT>(a.K);
-    const int NB = g.NB, KC = a.KC;
+    const Layout L = make_layout(FMT, a.N, a.K);
+    const int NB = L.NB, KC = a.KC;
     ActTile t;
     t.aq = reinterpret_cast<uint4*>(smem);
     t.am = reinterpret_cast<uint2*>(t.aq + 2 * M * KC);
@@ -554,19 +540,16 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_lockstep_kernel(cons
     unsigned long long* s_best = s_keys + W * 64;
     int* s_last = reinterpret_cast<int*>(s_best + W * MAX_M);
 
-    const int n_rg = (a.N + R - 1) / R;
-    const int n_items = (n_rg + W - 1) / W;
+    const int64_t n_items = (L.n_groups + W - 1) / W;
     const int nchunks = (NB + KC - 1) / KC;
-    const __half* d6 = FMT == FMT_Q6_K ? q6_k_scales(a.w_pack, g, a.N) : nullptr;
-    const int NSB = NB / 8;
     unsigned long long best = 0ull;
 
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int rg = item * W + warp;
-        const bool active = rg < n_rg;
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int64_t g = item * W + warp;
+        const bool active = g < L.n_groups;
         int rows[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) rows[r] = min(rg * R + r, a.N - 1);
+        for (int r = 0; r < R; ++r) rows[r] = (int)min(g * GROUP + r, (int64_t)a.N - 1);
         float acc[R][M];
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -586,7 +569,7 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_lockstep_kernel(cons
                     float dw[R];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const BlockAddr ad = block_addr(a.w_pack, g, rows[r], b);
+                        const BlockAddr ad = block_addr(a.w_pack, L, rows[r], b);
                         w16[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.tile + ad.j * 16));
                         dw[r] = __half2float(__ushort_as_half(ld_stream_u16(ad.tile + ad.nb * 16 + ad.j * 2)));
                     }
@@ -598,18 +581,18 @@ __global__ void __launch_bounds__(MMVQ_MAX_THREADS, 1) mmvq_lockstep_kernel(cons
                     float dw[R];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const BlockAddr ad = block_addr(a.w_pack, g, rows[r], b);
+                        const BlockAddr ad = block_addr(a.w_pack, L, rows[r], b);
                         ql[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.tile + ad.j * 16));
                         qh[r] = ld_stream_v2(reinterpret_cast<const uint2*>(ad.tile + ad.nb * 16 + ad.j * 8));
                         sc[r] = ld_stream_u16(ad.tile + ad.nb * 24 + ad.j * 2);
                         dw[r] = __half2float(
-                            __ushort_as_half(ld_stream_u16(d6 + (int64_t)rows[r] * NSB + (b >> 3))));
+                            __ushort_as_half(ld_stream_u16(ad.dq6 + (ad.r * (ad.nb >> 3) + (ad.j >> 3)) * 2)));
                     }
                     accumulate_q6_k<M, R>(ql, qh, sc, dw, t, ti, acc);
                 }
             }
         }
-        if (active) finish_rowgroup<M, R, TOP1>(a, rg * R, acc, lane, s_keys + warp * 64, best);
+        if (active) finish_rowgroup<M, R, TOP1>(a, (int)(g * GROUP), acc, lane, s_keys + warp * 64, best);
     }
     if (TOP1) top1_finish<M>(a, s_best, s_last, best, lane, warp, W);
 }

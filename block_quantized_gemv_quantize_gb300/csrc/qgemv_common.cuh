@@ -26,89 +26,100 @@ constexpr int Q6_K_BYTES = 210;
 constexpr int MAX_M = 17;
 
 // ---------------------------------------------------------------------------
-// Packed weight layouts.  A row of NB = K/32 blocks is cut into chunks of 32
-// blocks (the last chunk may be shorter, nb_tail blocks); each (row, chunk) is
-// one contiguous 16-byte-aligned tile, so a warp can fetch the tiles of its
-// rows with one bulk copy each and its lanes read consecutive blocks.
+// Packed weight layouts.  Rows are taken in groups of 4 (the last group may
+// hold fewer) and each row of NB = K/32 blocks is cut into chunks of 32
+// blocks (the last chunk may be shorter, nb_tail blocks).  One (group, chunk)
+// is one contiguous, 16-byte-aligned region, so a warp fetches the chunk of
+// its 4 rows with a single bulk copy, and a whole group is contiguous too.
+// Groups follow one another; inside a group the chunks follow one another.
 //
-// Q4_0 tile of nb blocks: nib[nb] (16 B each: the canonical qs bytes of the
-//   block, unchanged) | d[nb] (fp16 bits, copied raw) | zero pad to 16 B.
-//   Full tile 576 B; row = tiles back to back.  For K % 256 == 0 the pad is
-//   empty and the pack is exactly the canonical 18 B per block.
-// Q6_K tile of nb blocks (nb a multiple of 8):
+// Q4_0 group-chunk of `rows` rows and nb blocks: per row one tile
+//   nib[nb] (16 B each: the canonical qs bytes, unchanged) | d[nb] (fp16 bits,
+//   copied raw) | zero pad to 16 B;  full row tile 576 B, group-chunk 2304 B.
+// Q6_K group-chunk (nb a multiple of 8): per row one tile
 //   ql[nb] 16 B: byte t = low4(q[t]) | low4(q[t + 16]) << 4
 //   qh[nb]  8 B: byte t, bits 2s..2s+1 = high2(q[t + 8 s]), s = 0..3
 //   sc[nb]  2 B: the int8 subscales of the block's two 16-value halves
-//   Full tile 832 B.  After all N rows: d[N][K/256], fp16 superblock scales.
-//   Total = N * K/256 * 210 B, the canonical size.
+// then the fp16 superblock scales of the chunk, d[rows][nb / 8], zero padded
+// to 16 B;  full row tile 832 B, group-chunk 4 * 832 + 32 = 3360 B.
+// For N % 4 == 0 and K % 1024 == 0 there is no padding and the pack has
+// exactly the canonical size (18 B per Q4_0 block, 210 B per Q6_K superblock).
 // ---------------------------------------------------------------------------
 
-constexpr int CHUNK = 32;  // blocks per tile
+constexpr int CHUNK = 32;  // blocks per chunk
+constexpr int GROUP = 4;   // rows per group
 
 __host__ __device__ inline int pad16(int v) { return (v + 15) & ~15; }
 
-struct Geom {
-    int NB;          // blocks per row
-    int nch;         // chunks per row
-    int nb_tail;     // blocks in the last chunk
-    int full_tile;   // bytes of a 32-block tile
-    int tail_tile;   // bytes of the last tile
-    int64_t row;     // bytes of one row's tiles
+struct Layout {
+    int fmt;            // 0 = Q4_0, 1 = Q6_K
+    int N, NB, nch, nb_tail;
+    int64_t n_groups;
     __host__ __device__ int nb(int c) const { return c == nch - 1 ? nb_tail : CHUNK; }
-    __host__ __device__ int tile(int c) const { return c == nch - 1 ? tail_tile : full_tile; }
+    // bytes of one row's tile in chunk c
+    __host__ __device__ int tile(int c) const
+    {
+        const int n = nb(c);
+        return fmt == 0 ? n * 16 + pad16(n * 2) : n * 26;
+    }
+    // bytes of the Q6_K scale part of a group-chunk
+    __host__ __device__ int dpart(int rows, int c) const { return fmt == 0 ? 0 : pad16(rows * (nb(c) / 8) * 2); }
+    __host__ __device__ int chunk_bytes(int rows, int c) const { return rows * tile(c) + dpart(rows, c); }
+    __host__ __device__ int64_t group_bytes(int rows) const
+    {
+        return (int64_t)(nch - 1) * chunk_bytes(rows, 0) + chunk_bytes(rows, nch - 1);
+    }
+    __host__ __device__ int rows_in(int64_t g) const
+    {
+        const int64_t r = (int64_t)N - g * GROUP;
+        return r < GROUP ? (int)r : GROUP;
+    }
+    // every group but the last is full
+    __host__ __device__ int64_t group_offset(int64_t g) const { return g * group_bytes(GROUP); }
+    __host__ __device__ int64_t chunk_offset(int64_t g, int c) const
+    {
+        return group_offset(g) + (int64_t)c * chunk_bytes(rows_in(g), 0);
+    }
+    __host__ __device__ int64_t total_bytes() const
+    {
+        return group_offset(n_groups - 1) + group_bytes(rows_in(n_groups - 1));
+    }
 };
 
-__host__ __device__ inline int q4_0_tile_bytes(int nb) { return nb * 16 + pad16(nb * 2); }
-__host__ __device__ inline int q6_k_tile_bytes(int nb) { return nb * 26; }
-
-__host__ __device__ inline Geom geom_q4_0(int K)
+__host__ __device__ inline Layout make_layout(int fmt, int N, int K)
 {
-    Geom g;
-    g.NB = K / QK;
-    g.nch = (g.NB + CHUNK - 1) / CHUNK;
-    g.nb_tail = g.NB - (g.nch - 1) * CHUNK;
-    g.full_tile = q4_0_tile_bytes(CHUNK);
-    g.tail_tile = q4_0_tile_bytes(g.nb_tail);
-    g.row = (int64_t)(g.nch - 1) * g.full_tile + g.tail_tile;
-    return g;
+    Layout L;
+    L.fmt = fmt;
+    L.N = N;
+    L.NB = K / QK;
+    L.nch = (L.NB + CHUNK - 1) / CHUNK;
+    L.nb_tail = L.NB - (L.nch - 1) * CHUNK;
+    L.n_groups = ((int64_t)N + GROUP - 1) / GROUP;
+    return L;
 }
 
-__host__ __device__ inline Geom geom_q6_k(int K)
-{
-    Geom g;
-    g.NB = K / QK;
-    g.nch = (g.NB + CHUNK - 1) / CHUNK;
-    g.nb_tail = g.NB - (g.nch - 1) * CHUNK;
-    g.full_tile = q6_k_tile_bytes(CHUNK);
-    g.tail_tile = q6_k_tile_bytes(g.nb_tail);
-    g.row = (int64_t)g.NB * 26;
-    return g;
-}
-
-__host__ __device__ inline int64_t q4_0_pack_size(int64_t N, int K) { return N * geom_q4_0(K).row; }
-__host__ __device__ inline int64_t q6_k_pack_size(int64_t N, int K) { return N * ((int64_t)(K / QK) * 26 + (K / QK_K) * 2); }
-
-// Addresses of block b of row n inside a tile layout.
+// Where block b of row n lives.
 struct BlockAddr {
-    const uint8_t* tile;  // start of the (row, chunk) tile
-    int j;                // block index inside the tile
-    int nb;               // blocks in the tile
+    const uint8_t* tile;  // the row's tile in the block's chunk
+    const uint8_t* dq6;   // Q6_K: the chunk's scale part (d[rows][nb / 8])
+    int r;                // row inside its group
+    int j;                // block inside the chunk
+    int nb;               // blocks in the chunk
 };
 
-__host__ __device__ inline BlockAddr block_addr(const void* base, const Geom& g, int64_t n, int b)
+__host__ __device__ inline BlockAddr block_addr(const void* base, const Layout& L, int64_t n, int b)
 {
+    const int64_t g = n / GROUP;
     const int c = b / CHUNK;
-    BlockAddr r;
-    r.tile = static_cast<const uint8_t*>(base) + n * g.row + (int64_t)c * g.full_tile;
-    r.j = b - c * CHUNK;
-    r.nb = g.nb(c);
-    return r;
-}
-
-// Q6_K superblock scales follow the N rows of tiles.
-__host__ __device__ inline const __half* q6_k_scales(const void* base, const Geom& g, int64_t N)
-{
-    return reinterpret_cast<const __half*>(static_cast<const uint8_t*>(base) + N * g.row);
+    const int rows = L.rows_in(g);
+    const uint8_t* gc = static_cast<const uint8_t*>(base) + L.chunk_offset(g, c);
+    BlockAddr a;
+    a.r = (int)(n - g * GROUP);
+    a.j = b - c * CHUNK;
+    a.nb = L.nb(c);
+    a.tile = gc + a.r * L.tile(c);
+    a.dq6 = gc + rows * L.tile(c);
+    return a;
 }
 
 // ---------------------------------------------------------------------------

@@ -7,7 +7,8 @@ import numpy as np
 # ---------------------------------------------------------------- pack layouts (inverse, numpy)
 
 
-CHUNK = 32
+CHUNK = 32   # blocks per chunk
+GROUP = 4    # rows per group
 
 
 def _pad16(v: int) -> int:
@@ -19,31 +20,37 @@ def _chunks(nb: int):
     return [(c, min(CHUNK, nb - c)) for c in range(0, nb, CHUNK)]
 
 
+def _groups(N: int):
+    return [(g, min(GROUP, N - g)) for g in range(0, N, GROUP)]
+
+
 def pack_q4_0(w: np.ndarray) -> np.ndarray:
-    """Canonical Q4_0 [N, K/32, 18] -> the documented tile layout: per
-    (row, 32-block chunk) the 16-byte code blocks, then their fp16 scales,
-    zero-padded to 16 bytes."""
+    """Canonical Q4_0 [N, K/32, 18] -> the documented layout: groups of 4 rows;
+    per (group, 32-block chunk) each row's tile = its 16-byte code blocks, then
+    their fp16 scales, zero-padded to 16 bytes."""
     N, nb, _ = w.shape
-    rows = []
-    for c0, n in _chunks(nb):
-        nib = w[:, c0:c0 + n, 2:18].reshape(N, n * 16)
-        d = w[:, c0:c0 + n, 0:2].reshape(N, n * 2)
-        pad = np.zeros((N, _pad16(n * 2) - n * 2), dtype=np.uint8)
-        rows += [nib, d, pad]
-    return np.concatenate(rows, axis=1).reshape(-1)
+    out = []
+    for g0, rows in _groups(N):
+        for c0, n in _chunks(nb):
+            for r in range(rows):
+                out.append(w[g0 + r, c0:c0 + n, 2:18].reshape(-1))
+                out.append(w[g0 + r, c0:c0 + n, 0:2].reshape(-1))
+                out.append(np.zeros(_pad16(2 * n) - 2 * n, dtype=np.uint8))
+    return np.concatenate(out)
 
 
 def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
     """Inverse of pack_q4_0."""
     nb = K // 32
-    row_bytes = sum(n * 16 + _pad16(n * 2) for _, n in _chunks(nb))
-    rows = pack[: N * row_bytes].reshape(N, row_bytes)
     out = np.zeros((N, nb, 18), dtype=np.uint8)
     off = 0
-    for c0, n in _chunks(nb):
-        out[:, c0:c0 + n, 2:18] = rows[:, off:off + n * 16].reshape(N, n, 16)
-        out[:, c0:c0 + n, 0:2] = rows[:, off + n * 16: off + n * 18].reshape(N, n, 2)
-        off += n * 16 + _pad16(n * 2)
+    for g0, rows in _groups(N):
+        for c0, n in _chunks(nb):
+            for r in range(rows):
+                out[g0 + r, c0:c0 + n, 2:18] = pack[off:off + 16 * n].reshape(n, 16)
+                out[g0 + r, c0:c0 + n, 0:2] = pack[off + 16 * n:off + 18 * n].reshape(n, 2)
+                off += 16 * n + _pad16(2 * n)
+    assert off == pack.size
     return out
 
 
@@ -58,9 +65,11 @@ def _q6_k_codes(w: np.ndarray) -> np.ndarray:
 
 
 def pack_q6_k(w: np.ndarray) -> np.ndarray:
-    """Canonical Q6_K -> the documented tile layout: per (row, 32-block chunk)
-    ql (byte t = low4(q_t) | low4(q_t+16) << 4), qh (byte t, bits 2s =
-    high2(q_t+8s)), sc (the block's two subscales); then all fp16 scales."""
+    """Canonical Q6_K -> the documented layout: groups of 4 rows; per
+    (group, 32-block chunk) each row's tile = ql (byte t = low4(q_t) |
+    low4(q_t+16) << 4), qh (byte t, bits 2s = high2(q_t+8s)), sc (the block's
+    two subscales); then the chunk's fp16 scales d[rows][blocks / 8], zero
+    padded to 16 bytes."""
     N, ns, _ = w.shape
     nb = ns * 8
     q = _q6_k_codes(w).reshape(N, nb, 32)
@@ -71,32 +80,42 @@ def pack_q6_k(w: np.ndarray) -> np.ndarray:
         qh |= hi[:, :, 8 * s: 8 * s + 8] << (2 * s)
     qh = qh.astype(np.uint8)
     sc = w[:, :, 192:208].reshape(N, nb, 2)
-    parts = []
-    for c0, n in _chunks(nb):
-        parts += [ql[:, c0:c0 + n].reshape(N, -1), qh[:, c0:c0 + n].reshape(N, -1), sc[:, c0:c0 + n].reshape(N, -1)]
-    tiles = np.concatenate(parts, axis=1).reshape(-1)
-    return np.concatenate([tiles, w[:, :, 208:210].reshape(-1)])
+    d = w[:, :, 208:210]  # [N, ns, 2]
+    out = []
+    for g0, rows in _groups(N):
+        for c0, n in _chunks(nb):
+            for r in range(rows):
+                out += [ql[g0 + r, c0:c0 + n].reshape(-1), qh[g0 + r, c0:c0 + n].reshape(-1),
+                        sc[g0 + r, c0:c0 + n].reshape(-1)]
+            dpart = d[g0:g0 + rows, c0 // 8:(c0 + n) // 8].reshape(-1)
+            out += [dpart, np.zeros(_pad16(dpart.size) - dpart.size, dtype=np.uint8)]
+    return np.concatenate(out)
 
 
 def unpack_q6_k(pack: np.ndarray, N: int, K: int) -> np.ndarray:
     """Inverse of pack_q6_k."""
     nb, ns = K // 32, K // 256
-    rows = pack[: N * nb * 26].reshape(N, nb * 26)
     ql = np.zeros((N, nb, 16), dtype=np.int64)
     qh = np.zeros((N, nb, 8), dtype=np.int64)
     sc = np.zeros((N, nb, 2), dtype=np.uint8)
+    d = np.zeros((N, ns, 2), dtype=np.uint8)
     off = 0
-    for c0, n in _chunks(nb):
-        ql[:, c0:c0 + n] = rows[:, off:off + 16 * n].reshape(N, n, 16)
-        qh[:, c0:c0 + n] = rows[:, off + 16 * n: off + 24 * n].reshape(N, n, 8)
-        sc[:, c0:c0 + n] = rows[:, off + 24 * n: off + 26 * n].reshape(N, n, 2)
-        off += 26 * n
+    for g0, rows in _groups(N):
+        for c0, n in _chunks(nb):
+            for r in range(rows):
+                ql[g0 + r, c0:c0 + n] = pack[off:off + 16 * n].reshape(n, 16)
+                qh[g0 + r, c0:c0 + n] = pack[off + 16 * n:off + 24 * n].reshape(n, 8)
+                sc[g0 + r, c0:c0 + n] = pack[off + 24 * n:off + 26 * n].reshape(n, 2)
+                off += 26 * n
+            dn = rows * (n // 8) * 2
+            d[g0:g0 + rows, c0 // 8:(c0 + n) // 8] = pack[off:off + dn].reshape(rows, n // 8, 2)
+            off += _pad16(dn)
+    assert off == pack.size
     q = np.zeros((N, nb, 32), dtype=np.int64)
     q[:, :, 0:16] = ql & 0x0F
     q[:, :, 16:32] = ql >> 4
     for s in range(4):
         q[:, :, 8 * s: 8 * s + 8] |= ((qh >> (2 * s)) & 3) << 4
-    d = pack[N * nb * 26: N * nb * 26 + N * ns * 2].reshape(N, ns, 2)
     return q6_k_from_codes(q.reshape(N, K), sc.reshape(N, K // 16).view(np.int8),
                            d.copy().view(np.uint16).reshape(N, ns))
 

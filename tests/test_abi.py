@@ -55,6 +55,7 @@ def test_sizes(lib):
     assert lib.q8_1_bytes(5, 5120) == 28800
     assert lib.q4_0_pack_bytes(17408, 5120) == 50135040
     assert lib.q4_0_pack_bytes(1, 96) == 3 * 16 + 16  # a 3-block tile pads its 6 scale bytes to 16
+    assert lib.q6_k_pack_bytes(1, 256) == 8 * 26 + 16  # one row's 2 scale bytes pad to 16
     assert lib.q4_0_pack_bytes(5120, 17408) == 50135040
     assert lib.q4_0_pack_bytes(248320, 5120) == 715161600
     assert lib.q6_k_pack_bytes(248320, 5120) == 1042944000

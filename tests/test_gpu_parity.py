@@ -65,11 +65,11 @@ def test_qpack_q4_0_layout(ops, N, K):
     assert np.array_equal(C.unpack_q4_0(p, N, K), w)
 
 
-@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (3, 768), (300, 5120)])
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (3, 768), (300, 5120), (6, 1024)])
 def test_qpack_q6_k_layout(ops, N, K):
     w = synth.q6_k_weights(N, K, seed=N)
     p = _np(ops.qpack_q6_k(_t(w), N, K))
-    assert p.size == w.size
+    assert p.size == ops.q6_k_pack_bytes(N, K)
     assert np.array_equal(p, C.pack_q6_k(w))
     assert np.array_equal(C.unpack_q6_k(p, N, K), w)
 
