@@ -40,6 +40,7 @@ SIGNATURES = {
     "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
+    "lmhead_q6_k_top1_noalloc": (_I, [_P, _P, _L, _P, _I, _I, _I, _P]),
 }
 
 
@@ -188,6 +189,21 @@ def lmhead_q6_k_top1(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, ids:
     _check("lmhead_q6_k_top1", LIB.lmhead_q6_k_top1(_dev(w_pack, "w_pack"), _dev(x, "x"), x.stride(0),
                                                     _dev(ids, "ids"), _dev(ws, "workspace"), ws.numel(),
                                                     M, K, N, _stream(x)))
+    return ids
+
+
+def lmhead_q6_k_top1_noalloc(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int,
+                             ids: torch.Tensor | None = None) -> torch.Tensor:
+    """As lmhead_q6_k_top1, with the library's fixed device scratch instead of
+    a caller workspace (for callers that cannot allocate; calls on one device
+    must not overlap)."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    if ids is None:
+        ids = torch.empty(M, dtype=torch.int32, device=x.device)
+    _check("lmhead_q6_k_top1_noalloc", LIB.lmhead_q6_k_top1_noalloc(_dev(w_pack, "w_pack"), _dev(x, "x"),
+                                                                    x.stride(0), _dev(ids, "ids"), M, K, N,
+                                                                    _stream(x)))
     return ids
 
 

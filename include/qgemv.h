@@ -159,6 +159,31 @@ int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* i
 int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, size_t ws_bytes, int M, int N,
                     void* stream);
 
+/* ---- fused top-1 without a caller workspace -------------------------------- */
+
+#define QGEMV_NOALLOC_MAX_M 17
+
+/* lmhead_q6_k_top1_noalloc - lmhead_q6_k_top1 (same inputs, same ids) for
+ * callers that cannot allocate device memory where they run it: a host whose
+ * memory pool owns the whole device and forbids side allocations, a latency
+ * path on which cudaMalloc could stall or synchronize the device, or a plugin
+ * that is only handed input and output pointers.  It allocates nothing; the
+ * cross-CTA scratch (one 64-bit key per row plus a counter) lives in a fixed
+ * 256-byte array inside this library's device memory, which every GPU that
+ * loads the library keeps until the process exits.
+ * The pages have no counterpart: it exists for callers of this library.
+ *   w_pack, x, ldx, ids, M, K, N, stream as lmhead_q6_k_top1.
+ *   M > QGEMV_NOALLOC_MAX_M (17, the rows the fixed scratch holds) returns
+ *   QGEMV_UNSUPPORTED_SHAPE before anything is enqueued.
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  Each call clears the scratch on `stream`
+ *   before its kernel.  All calls on a device share the one array: calls
+ *   that overlap on the GPU (other streams, other host threads) race and may
+ *   return wrong ids; serialize them. */
+int lmhead_q6_k_top1_noalloc(const void* w_pack, const float* x, int64_t ldx, int32_t* ids, int M, int K, int N,
+                             void* stream);
+
 /* ---- checking aid --------------------------------------------------------- */
 
 /* qgemv_block_dots_q4_0 / _q6_k - out[(m * N + n) * (K/32) + b] = the exact
