@@ -231,16 +231,14 @@ def run_native(args, rank, world):
         step()
     torch.cuda.synchronize()
 
-    # timed region: K steps, per-call events, clocks sampled meanwhile
-    per = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
-           for _ in range(args.steps)]
+    # timed region: K steps bracketed by two events, clocks sampled meanwhile
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         t0.record(stream)
-        for s in range(args.steps):
-            step(per[s])
+        for _ in range(args.steps):
+            step()
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -250,7 +248,16 @@ def run_native(args, rank, world):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    call_ms = {n: statistics.mean(per[s][i][0].elapsed_time(per[s][i][1]) for s in range(args.steps))
+
+    # per-call breakdown: a second timed region with an event pair around every call
+    n_break = max(3, min(args.steps, 200))
+    per = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
+           for _ in range(n_break)]
+    torch.cuda.synchronize()
+    for s_ in range(n_break):
+        step(per[s_])
+    torch.cuda.synchronize()
+    call_ms = {n: statistics.mean(per[s_][i][0].elapsed_time(per[s_][i][1]) for s_ in range(n_break))
                for i, n in enumerate(names)}
 
     nbytes = step_bytes()
@@ -359,6 +366,7 @@ def run_native(args, rank, world):
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": len(calls) * args.steps,
+            "breakdown_steps": n_break,
             "clocks": clocks,
         }
     return result

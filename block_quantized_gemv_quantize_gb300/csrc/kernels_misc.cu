@@ -77,11 +77,12 @@ __global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __
 #pragma unroll
         for (int k = 0; k < 4; ++k) q[k] = (uint32_t)src[1 + 2 * k] | ((uint32_t)src[2 + 2 * k] << 16);
         const BlockAddr ad = block_addr(pack, L, n, b);
-        uint8_t* tile = const_cast<uint8_t*>(ad.tile);
-        reinterpret_cast<uint4*>(tile)[ad.j] = make_uint4(q[0], q[1], q[2], q[3]);
-        reinterpret_cast<uint16_t*>(tile + ad.nb * 16)[ad.j] = src[0];
-        if (ad.j == 0) {  // zero the tile's pad bytes (present only when nb % 8 != 0)
-            for (int p = ad.nb * 18; p < pad16(ad.nb * 2) + ad.nb * 16; ++p) tile[p] = 0;
+        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(ad.q)) = make_uint4(q[0], q[1], q[2], q[3]);
+        *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.d)) = src[0];
+        const int rows = L.rows_in(n / GROUP), c = b / CHUNK, nb = L.nb(c);
+        if ((n % GROUP) == 0 && b % CHUNK == 0) {  // zero the group-chunk's pad bytes
+            uint8_t* gc = pack + L.chunk_offset(n / GROUP, c);
+            for (int p = nb * rows * 18; p < L.chunk_bytes(rows, c); ++p) gc[p] = 0;
         }
     }
 }
@@ -123,18 +124,15 @@ __global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
             wh[t >> 2] |= byte << (8 * (t & 3));
         }
         const BlockAddr ad = block_addr(pack, L, n, b);
-        uint8_t* tile = const_cast<uint8_t*>(ad.tile);
-        reinterpret_cast<uint4*>(tile)[ad.j] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        reinterpret_cast<uint2*>(tile + ad.nb * 16)[ad.j] = make_uint2(wh[0], wh[1]);
-        reinterpret_cast<uint16_t*>(tile + ad.nb * 24)[ad.j] =
+        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(ad.q)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        *reinterpret_cast<uint2*>(const_cast<uint8_t*>(ad.qh)) = make_uint2(wh[0], wh[1]);
+        *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.sc)) =
             (uint16_t)sb[192 + 2 * bb] | ((uint16_t)sb[192 + 2 * bb + 1] << 8);
-        uint8_t* dq = const_cast<uint8_t*>(ad.dq6);
-        if (bb == 0)
-            reinterpret_cast<uint16_t*>(dq)[ad.r * (ad.nb >> 3) + (ad.j >> 3)] =
-                (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
-        if (ad.r == 0 && ad.j == 0) {  // zero the scale part's pad bytes
-            const int rows = L.rows_in(n / GROUP);
-            for (int p = rows * (ad.nb >> 3) * 2; p < pad16(rows * (ad.nb >> 3) * 2); ++p) dq[p] = 0;
+        if (bb == 0) *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.d)) = (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
+        const int rows = L.rows_in(n / GROUP), c = b / CHUNK, nb = L.nb(c);
+        if ((n % GROUP) == 0 && b % CHUNK == 0) {  // zero the scale part's pad bytes
+            uint8_t* dq = pack + L.chunk_offset(n / GROUP, c) + rows * nb * 26;
+            for (int p = rows * (nb / 8) * 2; p < pad16(rows * (nb / 8) * 2); ++p) dq[p] = 0;
         }
     }
 }
@@ -298,15 +296,13 @@ __global__ void block_dots_kernel(const void* __restrict__ w_pack, const uint8_t
         uint2 meta;
         act_from_q8_1<FMT>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES, lo, hi, meta);
         uint32_t w[8];
+        const BlockAddr ad = block_addr(w_pack, make_layout(FMT, N, NB * QK), n, b);
         if (FMT == FMT_Q4_0) {
-            const BlockAddr ad = block_addr(w_pack, make_layout(FMT_Q4_0, N, NB * QK), n, b);
-            q4_0_unpack(reinterpret_cast<const uint4*>(ad.tile)[ad.j], w);
+            q4_0_unpack(*reinterpret_cast<const uint4*>(ad.q), w);
             out[i] = q4_0_dot(w, lo, hi, (int)meta.y);
         } else {
-            const BlockAddr ad = block_addr(w_pack, make_layout(FMT_Q6_K, N, NB * QK), n, b);
-            q6_k_unpack(reinterpret_cast<const uint4*>(ad.tile)[ad.j],
-                        reinterpret_cast<const uint2*>(ad.tile + ad.nb * 16)[ad.j], w);
-            out[i] = q6_k_dot(w, lo, hi, meta.y, reinterpret_cast<const uint16_t*>(ad.tile + ad.nb * 24)[ad.j]);
+            q6_k_unpack(*reinterpret_cast<const uint4*>(ad.q), *reinterpret_cast<const uint2*>(ad.qh), w);
+            out[i] = q6_k_dot(w, lo, hi, meta.y, *reinterpret_cast<const uint16_t*>(ad.sc));
         }
     }
 }

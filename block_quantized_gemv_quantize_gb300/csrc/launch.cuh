@@ -51,7 +51,7 @@ MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N)
     p.grid = L.n_groups < di.sms ? (int)L.n_groups : di.sms;
     const int64_t per_cta = (L.n_groups + p.grid - 1) / p.grid;
     p.warps = per_cta < max_warps ? (int)per_cta : max_warps;
-    const size_t act = (size_t)M * L.NB * ACT_BYTES_PER_BLOCK;
+    const size_t act = (size_t)L.NB * (BlockAct<M>::STRIDE + 8 * M);
     const size_t extra = TOP1 ? top1_scratch_bytes(p.warps) : 0;
     const size_t stage = (size_t)L.chunk_bytes(GROUP, 0);
     const size_t fixed = act + extra + 128;

@@ -266,6 +266,106 @@ __device__ __forceinline__ void accumulate_q6_k(const uint4 (&ql)[R], const uint
 }
 
 // ---------------------------------------------------------------------------
+// Block-major activation tile of the Q6_K ring kernel: for block b the codes
+// of rows m = 0..M-1 lie at ab[b] + 32 m (two 16-byte halves), with a block
+// stride of (2M + 1) * 16 bytes (an odd number of 16-byte units, so that the
+// 32 lanes, which read 32 consecutive blocks, hit distinct bank groups), and
+// the per-(block, row) meta word at am[b * M + m].  One base address per lane
+// and compile-time offsets per row m.
+// ---------------------------------------------------------------------------
+
+template <int M>
+struct BlockAct {
+    static constexpr int STRIDE = (2 * M + 1) * 16;
+    uint8_t* q;  // [NB][STRIDE]
+    uint2* am;   // [NB][M]
+};
+
+template <int FMT, int M>
+__device__ __forceinline__ void block_act_from_q8_1(const BlockAct<M>& t, const uint8_t* xq, int NB)
+{
+    for (int i = threadIdx.x; i < M * NB; i += blockDim.x) {
+        const int m = i / NB, b = i - m * NB;
+        uint4 lo, hi;
+        uint2 meta;
+        act_from_q8_1<FMT>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES, lo, hi, meta);
+        uint4* dst = reinterpret_cast<uint4*>(t.q + b * BlockAct<M>::STRIDE + 32 * m);
+        dst[0] = lo;
+        dst[1] = hi;
+        t.am[b * M + m] = meta;
+    }
+}
+
+template <int FMT, int M>
+__device__ __forceinline__ void block_act_from_f32(const BlockAct<M>& t, const float* x, int64_t ldx, int NB)
+{
+    const bool vec4 = ((reinterpret_cast<uintptr_t>(x) | ((uintptr_t)ldx * 4)) & 15u) == 0;
+    for (int i = threadIdx.x; i < M * NB; i += blockDim.x) {
+        const int m = i / NB, b = i - m * NB;
+        Q81Block qb;
+        q8_1_quantize_block(x + (int64_t)m * ldx + (int64_t)b * QK, vec4, qb);
+        uint4* dst = reinterpret_cast<uint4*>(t.q + b * BlockAct<M>::STRIDE + 32 * m);
+        dst[0] = make_uint4(qb.q[0], qb.q[1], qb.q[2], qb.q[3]);
+        dst[1] = make_uint4(qb.q[4], qb.q[5], qb.q[6], qb.q[7]);
+        uint2 meta;
+        meta.x = __float_as_uint(__half2float(__float2half_rn(qb.d)));
+        meta.y = act_meta_from_sums<FMT>(qb.s_lo, qb.s_hi);
+        t.am[b * M + m] = meta;
+    }
+}
+
+// Q4_0 block of R rows against the block-major tile (block index ti).
+template <int M, int R>
+__device__ __forceinline__ void accumulate_q4_0_blk(const uint4 (&w16)[R], const float (&dw)[R],
+                                                    const BlockAct<M>& t, int ti, float (&acc)[R][M])
+{
+    uint32_t w[R][8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) q4_0_unpack(w16[r], w[r]);
+    const uint8_t* ab = t.q + ti * BlockAct<M>::STRIDE;
+    const uint2* am = t.am + ti * M;
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
+        const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
+        const uint2 mt = am[m];
+        const float da = __uint_as_float(mt.x);
+        const int init = (int)mt.y + MAGIC_I2F_BITS;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int sI = q4_0_dot(w[r], lo, hi, init);
+            const float f = __int_as_float(sI) - MAGIC_I2F;  // exact I
+            acc[r][m] = fmaf(dw[r] * da, f, acc[r][m]);
+        }
+    }
+}
+
+// Q6_K block of R rows against the block-major tile (block index ti).
+template <int M, int R>
+__device__ __forceinline__ void accumulate_q6_k_blk(const uint4 (&ql)[R], const uint2 (&qh)[R],
+                                                    const uint32_t (&sc)[R], const float (&dw)[R],
+                                                    const BlockAct<M>& t, int ti, float (&acc)[R][M])
+{
+    uint32_t w[R][8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) q6_k_unpack(ql[r], qh[r], w[r]);
+    const uint8_t* ab = t.q + ti * BlockAct<M>::STRIDE;
+    const uint2* am = t.am + ti * M;
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
+        const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
+        const uint2 mt = am[m];
+        const float da = __uint_as_float(mt.x);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int J = q6_k_dot(w[r], lo, hi, mt.y, sc[r]);
+            acc[r][m] = fmaf(dw[r] * da, (float)J, acc[r][m]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Kernel arguments and epilogue.
 // ---------------------------------------------------------------------------
 
@@ -391,10 +491,9 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(con
     const int stage_bytes = L.chunk_bytes(R, 0);
 
     uint8_t* rings = smem;
-    ActTile t;
-    t.aq = reinterpret_cast<uint4*>(rings + (size_t)W * S * stage_bytes);
-    t.am = reinterpret_cast<uint2*>(t.aq + 2 * M * NB);
-    t.KC = NB;
+    BlockAct<M> t;
+    t.q = rings + (size_t)W * S * stage_bytes;
+    t.am = reinterpret_cast<uint2*>(t.q + (size_t)NB * BlockAct<M>::STRIDE);
     uint64_t* bars = reinterpret_cast<uint64_t*>(t.am + M * NB);
     unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(bars + W * S);  // [W][64]
     unsigned long long* s_best = s_keys + W * 64;                                     // [W][MAX_M]
@@ -419,12 +518,16 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(con
     // Issue cursor (lane 0): next job's group, chunk and stage.
     int issued = 0, iss_c = 0, iss_slot = 0;
     int64_t iss_g = g0 + warp;
+    const int64_t GB = L.group_bytes(GROUP);  // bytes of a full group
+    const int CB = L.chunk_bytes(GROUP, 0);    // bytes of a full chunk of a full group
     auto issue_next = [&]() {
         const int rows = L.rows_in(iss_g);
-        const uint32_t bytes = (uint32_t)L.chunk_bytes(rows, iss_c);
+        const bool full = rows == GROUP && (iss_c < nch - 1 || L.nb_tail == CHUNK);
+        const uint32_t bytes = full ? (uint32_t)CB : (uint32_t)L.chunk_bytes(rows, iss_c);
+        const int64_t off = iss_g * GB + (int64_t)iss_c * (rows == GROUP ? CB : L.chunk_bytes(rows, 0));
         uint64_t* bar = &wbar[iss_slot];
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(wring + (size_t)iss_slot * stage_bytes, wbase + L.chunk_offset(iss_g, iss_c), bytes, bar, pol);
+        bulk_g2s(wring + (size_t)iss_slot * stage_bytes, wbase + off, bytes, bar, pol);
         ++issued;
         if (++iss_slot == S) iss_slot = 0;
         if (++iss_c == nch) {
@@ -437,8 +540,8 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(con
     }
 
     // The activation is staged while the first weight tiles are in flight.
-    if (TOP1) stage_from_f32<FMT, M>(t, a.x, a.ldx, 0, NB);
-    else stage_from_q8_1<FMT, M>(t, a.xq, NB, 0, NB);
+    if (TOP1) block_act_from_f32<FMT, M>(t, a.x, a.ldx, NB);
+    else block_act_from_q8_1<FMT, M>(t, a.xq, NB);
     __syncthreads();
 
     unsigned long long best = 0ull;
@@ -464,37 +567,77 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(con
             break;
         }
         consumed = j + 1;
-        const int nb = L.nb(c), tb = L.tile(c);
         const uint8_t* st = wring + (size_t)slot * stage_bytes;
-        if (lane < nb) {
-            const int ti = c * CHUNK + lane;
-            if (FMT == FMT_Q4_0) {
-                uint4 w16[R];
-                float dw[R];
+        const int rows = L.rows_in(g);
+        const int ti = c * CHUNK + lane;
+        const bool full_chunk = c != nch - 1 || L.nb_tail == CHUNK;
+        if (FMT == FMT_Q4_0) {
+            // block-major group-chunk: nib[block][row] then d[block][row]
+            uint4 w16[R];
+            float dw[R];
+            if (full_chunk && rows == R) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) w16[r] = *reinterpret_cast<const uint4*>(st + (lane * R + r) * 16);
+                const uint2 dd = *reinterpret_cast<const uint2*>(st + CHUNK * R * 16 + lane * R * 2);
+                dw[0] = __half2float(__ushort_as_half((unsigned short)(dd.x & 0xFFFFu)));
+                dw[1] = __half2float(__ushort_as_half((unsigned short)(dd.x >> 16)));
+                dw[2] = __half2float(__ushort_as_half((unsigned short)(dd.y & 0xFFFFu)));
+                dw[3] = __half2float(__ushort_as_half((unsigned short)(dd.y >> 16)));
+                accumulate_q4_0_blk<M, R>(w16, dw, t, ti, acc);
+            } else if (lane < L.nb(c)) {
+                // rows past the group's end read stale data; their sums are discarded
+                const int nb = L.nb(c);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    w16[r] = *reinterpret_cast<const uint4*>(st + r * tb + lane * 16);
-                    dw[r] = __half2float(
-                        __ushort_as_half(*reinterpret_cast<const uint16_t*>(st + r * tb + nb * 16 + lane * 2)));
+                    const int rr = min(r, rows - 1);
+                    w16[r] = *reinterpret_cast<const uint4*>(st + (lane * rows + rr) * 16);
+                    dw[r] = __half2float(__ushort_as_half(
+                        *reinterpret_cast<const uint16_t*>(st + nb * rows * 16 + (lane * rows + rr) * 2)));
                 }
-                accumulate_q4_0<M, R>(w16, dw, t, ti, acc);
-            } else {
-                const int rows = L.rows_in(g);
-                const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * tb);
-                uint4 ql[R];
-                uint2 qh[R];
-                uint32_t sc[R];
-                float dw[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    ql[r] = *reinterpret_cast<const uint4*>(st + r * tb + lane * 16);
-                    qh[r] = *reinterpret_cast<const uint2*>(st + r * tb + nb * 16 + lane * 8);
-                    sc[r] = *reinterpret_cast<const uint16_t*>(st + r * tb + nb * 24 + lane * 2);
-                    // rows past the group's end read stale scales; their sums are discarded
-                    dw[r] = __half2float(__ushort_as_half(dq[min(r, rows - 1) * (nb >> 3) + (lane >> 3)]));
-                }
-                accumulate_q6_k<M, R>(ql, qh, sc, dw, t, ti, acc);
+                accumulate_q4_0_blk<M, R>(w16, dw, t, ti, acc);
             }
+        } else {
+        uint4 ql[R];
+        uint2 qh[R];
+        uint32_t sc[R];
+        float dw[R];
+        if (full_chunk) {
+            if (rows == R) {
+                // full chunk of a full group: every offset is a compile-time constant
+                constexpr int TB = CHUNK * 26;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    ql[r] = *reinterpret_cast<const uint4*>(st + r * TB + lane * 16);
+                    qh[r] = *reinterpret_cast<const uint2*>(st + r * TB + CHUNK * 16 + lane * 8);
+                    sc[r] = *reinterpret_cast<const uint16_t*>(st + r * TB + CHUNK * 24 + lane * 2);
+                    dw[r] = __half2float(__ushort_as_half(
+                        *reinterpret_cast<const uint16_t*>(st + R * TB + (r * (CHUNK / 8) + (lane >> 3)) * 2)));
+                }
+            } else {
+                constexpr int TB = CHUNK * 26;
+                const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * TB);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    // rows past the group's end read stale data; their sums are discarded
+                    ql[r] = *reinterpret_cast<const uint4*>(st + r * TB + lane * 16);
+                    qh[r] = *reinterpret_cast<const uint2*>(st + r * TB + CHUNK * 16 + lane * 8);
+                    sc[r] = *reinterpret_cast<const uint16_t*>(st + r * TB + CHUNK * 24 + lane * 2);
+                    dw[r] = __half2float(__ushort_as_half(dq[min(r, rows - 1) * (CHUNK / 8) + (lane >> 3)]));
+                }
+            }
+            accumulate_q6_k_blk<M, R>(ql, qh, sc, dw, t, ti, acc);
+        } else if (lane < L.nb_tail) {
+            const int nb = L.nb_tail, tb = nb * 26;
+            const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * tb);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                ql[r] = *reinterpret_cast<const uint4*>(st + r * tb + lane * 16);
+                qh[r] = *reinterpret_cast<const uint2*>(st + r * tb + nb * 16 + lane * 8);
+                sc[r] = *reinterpret_cast<const uint16_t*>(st + r * tb + nb * 24 + lane * 2);
+                dw[r] = __half2float(__ushort_as_half(dq[min(r, rows - 1) * (nb >> 3) + (lane >> 3)]));
+            }
+            accumulate_q6_k_blk<M, R>(ql, qh, sc, dw, t, ti, acc);
+        }
         }
         __syncwarp();
         if (c == nch - 1) finish_rowgroup<M, R, TOP1>(a, (int)(g * GROUP), acc, lane, s_keys + warp * 64, best);
@@ -570,8 +713,8 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_lockstep_kernel
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const BlockAddr ad = block_addr(a.w_pack, L, rows[r], b);
-                        w16[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.tile + ad.j * 16));
-                        dw[r] = __half2float(__ushort_as_half(ld_stream_u16(ad.tile + ad.nb * 16 + ad.j * 2)));
+                        w16[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.q));
+                        dw[r] = __half2float(__ushort_as_half(ld_stream_u16(ad.d)));
                     }
                     accumulate_q4_0<M, R>(w16, dw, t, ti, acc);
                 } else {
@@ -582,11 +725,10 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_lockstep_kernel
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const BlockAddr ad = block_addr(a.w_pack, L, rows[r], b);
-                        ql[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.tile + ad.j * 16));
-                        qh[r] = ld_stream_v2(reinterpret_cast<const uint2*>(ad.tile + ad.nb * 16 + ad.j * 8));
-                        sc[r] = ld_stream_u16(ad.tile + ad.nb * 24 + ad.j * 2);
-                        dw[r] = __half2float(
-                            __ushort_as_half(ld_stream_u16(ad.dq6 + (ad.r * (ad.nb >> 3) + (ad.j >> 3)) * 2)));
+                        ql[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.q));
+                        qh[r] = ld_stream_v2(reinterpret_cast<const uint2*>(ad.qh));
+                        sc[r] = ld_stream_u16(ad.sc);
+                        dw[r] = __half2float(__ushort_as_half(ld_stream_u16(ad.d)));
                     }
                     accumulate_q6_k<M, R>(ql, qh, sc, dw, t, ti, acc);
                 }

@@ -29,14 +29,17 @@ constexpr int MAX_M = 17;
 // Packed weight layouts.  Rows are taken in groups of 4 (the last group may
 // hold fewer) and each row of NB = K/32 blocks is cut into chunks of 32
 // blocks (the last chunk may be shorter, nb_tail blocks).  One (group, chunk)
-// is one contiguous, 16-byte-aligned region, so a warp fetches the chunk of
-// its 4 rows with a single bulk copy, and a whole group is contiguous too.
+// is one contiguous, 16-byte-aligned region, so the chunk of a row group is
+// fetched with a single bulk copy, and a whole group is contiguous too.
 // Groups follow one another; inside a group the chunks follow one another.
 //
-// Q4_0 group-chunk of `rows` rows and nb blocks: per row one tile
-//   nib[nb] (16 B each: the canonical qs bytes, unchanged) | d[nb] (fp16 bits,
-//   copied raw) | zero pad to 16 B;  full row tile 576 B, group-chunk 2304 B.
-// Q6_K group-chunk (nb a multiple of 8): per row one tile
+// Q4_0 group-chunk of `rows` rows and nb blocks, block-major:
+//   nib[nb][rows] (16 B each: the canonical qs bytes of the block, unchanged)
+//   d[nb][rows] (fp16 bits, copied raw), zero padded to 16 B.
+//   4 rows x 32 blocks = 2048 + 256 = 2304 B.  Block-major order puts the four
+//   rows of one block next to each other, so a lane reads its block's four
+//   scales with one 8-byte load.
+// Q6_K group-chunk (nb a multiple of 8), row-major: per row one tile
 //   ql[nb] 16 B: byte t = low4(q[t]) | low4(q[t + 16]) << 4
 //   qh[nb]  8 B: byte t, bits 2s..2s+1 = high2(q[t + 8 s]), s = 0..3
 //   sc[nb]  2 B: the int8 subscales of the block's two 16-value halves
@@ -56,15 +59,13 @@ struct Layout {
     int N, NB, nch, nb_tail;
     int64_t n_groups;
     __host__ __device__ int nb(int c) const { return c == nch - 1 ? nb_tail : CHUNK; }
-    // bytes of one row's tile in chunk c
-    __host__ __device__ int tile(int c) const
+    // Q6_K: bytes of one row's tile in chunk c
+    __host__ __device__ int tile(int c) const { return nb(c) * 26; }
+    __host__ __device__ int chunk_bytes(int rows, int c) const
     {
         const int n = nb(c);
-        return fmt == 0 ? n * 16 + pad16(n * 2) : n * 26;
+        return fmt == 0 ? rows * n * 16 + pad16(rows * n * 2) : rows * n * 26 + pad16(rows * (n / 8) * 2);
     }
-    // bytes of the Q6_K scale part of a group-chunk
-    __host__ __device__ int dpart(int rows, int c) const { return fmt == 0 ? 0 : pad16(rows * (nb(c) / 8) * 2); }
-    __host__ __device__ int chunk_bytes(int rows, int c) const { return rows * tile(c) + dpart(rows, c); }
     __host__ __device__ int64_t group_bytes(int rows) const
     {
         return (int64_t)(nch - 1) * chunk_bytes(rows, 0) + chunk_bytes(rows, nch - 1);
@@ -98,13 +99,12 @@ __host__ __device__ inline Layout make_layout(int fmt, int N, int K)
     return L;
 }
 
-// Where block b of row n lives.
+// Where the pieces of block b of row n live.
 struct BlockAddr {
-    const uint8_t* tile;  // the row's tile in the block's chunk
-    const uint8_t* dq6;   // Q6_K: the chunk's scale part (d[rows][nb / 8])
-    int r;                // row inside its group
-    int j;                // block inside the chunk
-    int nb;               // blocks in the chunk
+    const uint8_t* q;   // Q4_0: the 16 code bytes;  Q6_K: ql (16 B)
+    const uint8_t* qh;  // Q6_K: qh (8 B)
+    const uint8_t* sc;  // Q6_K: the two subscales
+    const uint8_t* d;   // fp16 scale (Q4_0: the block's; Q6_K: the superblock's)
 };
 
 __host__ __device__ inline BlockAddr block_addr(const void* base, const Layout& L, int64_t n, int b)
@@ -112,13 +112,20 @@ __host__ __device__ inline BlockAddr block_addr(const void* base, const Layout& 
     const int64_t g = n / GROUP;
     const int c = b / CHUNK;
     const int rows = L.rows_in(g);
+    const int r = (int)(n - g * GROUP), j = b - c * CHUNK, nb = L.nb(c);
     const uint8_t* gc = static_cast<const uint8_t*>(base) + L.chunk_offset(g, c);
     BlockAddr a;
-    a.r = (int)(n - g * GROUP);
-    a.j = b - c * CHUNK;
-    a.nb = L.nb(c);
-    a.tile = gc + a.r * L.tile(c);
-    a.dq6 = gc + rows * L.tile(c);
+    if (L.fmt == 0) {
+        a.q = gc + (j * rows + r) * 16;
+        a.d = gc + nb * rows * 16 + (j * rows + r) * 2;
+        a.qh = a.sc = nullptr;
+    } else {
+        const uint8_t* t = gc + r * nb * 26;
+        a.q = t + j * 16;
+        a.qh = t + nb * 16 + j * 8;
+        a.sc = t + nb * 24 + j * 2;
+        a.d = gc + rows * nb * 26 + (r * (nb / 8) + j / 8) * 2;
+    }
     return a;
 }
 

@@ -26,16 +26,15 @@ def _groups(N: int):
 
 def pack_q4_0(w: np.ndarray) -> np.ndarray:
     """Canonical Q4_0 [N, K/32, 18] -> the documented layout: groups of 4 rows;
-    per (group, 32-block chunk) each row's tile = its 16-byte code blocks, then
-    their fp16 scales, zero-padded to 16 bytes."""
+    per (group, 32-block chunk), block-major: the 16-byte code blocks [block][row],
+    then the fp16 scales [block][row], zero-padded to 16 bytes."""
     N, nb, _ = w.shape
     out = []
     for g0, rows in _groups(N):
         for c0, n in _chunks(nb):
-            for r in range(rows):
-                out.append(w[g0 + r, c0:c0 + n, 2:18].reshape(-1))
-                out.append(w[g0 + r, c0:c0 + n, 0:2].reshape(-1))
-                out.append(np.zeros(_pad16(2 * n) - 2 * n, dtype=np.uint8))
+            nib = w[g0:g0 + rows, c0:c0 + n, 2:18].transpose(1, 0, 2).reshape(-1)
+            d = w[g0:g0 + rows, c0:c0 + n, 0:2].transpose(1, 0, 2).reshape(-1)
+            out += [nib, d, np.zeros(_pad16(d.size) - d.size, dtype=np.uint8)]
     return np.concatenate(out)
 
 
@@ -46,10 +45,10 @@ def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
     off = 0
     for g0, rows in _groups(N):
         for c0, n in _chunks(nb):
-            for r in range(rows):
-                out[g0 + r, c0:c0 + n, 2:18] = pack[off:off + 16 * n].reshape(n, 16)
-                out[g0 + r, c0:c0 + n, 0:2] = pack[off + 16 * n:off + 18 * n].reshape(n, 2)
-                off += 16 * n + _pad16(2 * n)
+            out[g0:g0 + rows, c0:c0 + n, 2:18] = pack[off:off + 16 * n * rows].reshape(n, rows, 16).transpose(1, 0, 2)
+            off += 16 * n * rows
+            out[g0:g0 + rows, c0:c0 + n, 0:2] = pack[off:off + 2 * n * rows].reshape(n, rows, 2).transpose(1, 0, 2)
+            off += _pad16(2 * n * rows)
     assert off == pack.size
     return out
 
