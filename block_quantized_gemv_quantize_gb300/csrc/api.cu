@@ -34,6 +34,15 @@ int check_gemv(const void* w, const void* xq, const void* y, int64_t ldy, int M,
 
 size_t top1_ws_bytes() { return sizeof(Top1Workspace); }
 
+// lmhead workspace: the top-1 keys and counter, then (from byte
+// LMHEAD_Q8_OFFSET) the Q8_1 copy of x that the pre-pass writes.
+constexpr size_t LMHEAD_Q8_OFFSET = 256;
+static_assert(sizeof(Top1Workspace) <= LMHEAD_Q8_OFFSET, "top-1 scratch does not fit");
+size_t lmhead_ws_bytes(int M, int K)
+{
+    return LMHEAD_Q8_OFFSET + (((size_t)(M > 0 ? M : 0) * (size_t)(K > 0 ? K / QK : 0) * Q8_1_BYTES + 15) & ~(size_t)15);
+}
+
 }  // namespace
 
 extern "C" {
@@ -60,7 +69,7 @@ size_t q6_k_pack_bytes(int N, int K)
 {
     return (N < 1 || K < QK_K) ? 0 : (size_t)make_layout(FMT_Q6_K, N, K).total_bytes();
 }
-size_t lmhead_q6_k_top1_workspace_bytes(int, int, int) { return top1_ws_bytes(); }
+size_t lmhead_q6_k_top1_workspace_bytes(int M, int K, int) { return lmhead_ws_bytes(M, K); }
 size_t argmax_f32_rows_workspace_bytes(int, int) { return top1_ws_bytes(); }
 
 int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* stream)
@@ -124,17 +133,24 @@ int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* i
     int st = check_mk(M, K, QK_K);
     if (st) return st;
     if (N < 1 || ldx < K) return QGEMV_INVALID_ARG;
-    if (ws_bytes < top1_ws_bytes()) return QGEMV_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < lmhead_ws_bytes(M, K)) return QGEMV_WORKSPACE_TOO_SMALL;
     if (!aligned16(w_pack) || !aligned16(x) || !aligned16(ids) || !aligned16(workspace)) return QGEMV_MISALIGNED;
+    // Pre-pass: x -> Q8_1 in the workspace (the same kernel as quantize_q8_1),
+    // then the MMVQ kernel with the top-1 epilogue reads that copy.
+    uint8_t* xq = static_cast<uint8_t*>(workspace) + LMHEAD_Q8_OFFSET;
+    cudaStream_t s = as_stream(stream);
+    st = launch_quantize_q8_1(x, ldx, xq, M, K, s);
+    if (st != QGEMV_OK) return st;
     MmvqArgs a{};
     a.w_pack = w_pack;
     a.x = x;
     a.ldx = ldx;
+    a.xq = xq;
     a.K = K;
     a.N = N;
     a.ws = static_cast<Top1Workspace*>(workspace);
     a.ids = ids;
-    return launch_lmhead_q6_k(a, M, as_stream(stream));
+    return launch_lmhead_q6_k(a, M, s);
 }
 
 int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, size_t ws_bytes, int M, int N,

@@ -22,26 +22,37 @@ DeviceInfo device_info()
 }
 
 // ---------------------------------------------------------------------------
-// quantize_q8_1: one thread per 32-value block ("Qwen3.6 27B B70 follow-up: Q8
-// activation cache", Q8_1 activation cache prototype: the activation is
-// quantized once and the Q8_1 copy is reused by sibling matmuls).
+// quantize_q8_1: eight lanes per 32-value block, four blocks per warp step
+// ("Qwen3.6 27B B70 follow-up: Q8 activation cache", Q8_1 activation cache
+// prototype: the activation is quantized once and the Q8_1 copy is reused by
+// sibling matmuls).  Lane sub of a block writes code word sub; lane 0 of the
+// block also writes the fp16 pair (d, s).
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
-                                                            uint8_t* __restrict__ xq, int M, int NB)
+constexpr int QUANT_THREADS = 128;
+
+__global__ void __launch_bounds__(QUANT_THREADS) quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
+                                                                      uint8_t* __restrict__ xq, int M, int NB)
 {
     const int64_t nblk = (int64_t)M * NB;
     const bool vec4 = ((reinterpret_cast<uintptr_t>(x) | ((uintptr_t)ldx * 4)) & 15u) == 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
+    const int lane = threadIdx.x & 31, sub = lane & 7;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t i0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4; i0 < nblk;
+         i0 += warps * 4) {  // warp-uniform
+        const int64_t mine = i0 + (lane >> 3);
+        const int64_t i = mine < nblk ? mine : nblk - 1;  // spare lanes redo the last block, unwritten
         const int m = (int)(i / NB), b = (int)(i - (int64_t)m * NB);
-        Q81Block qb;
-        q8_1_quantize_block(x + (int64_t)m * ldx + (int64_t)b * QK, vec4, qb);
-        const __half d16 = __float2half_rn(qb.d);
-        const __half s16 = __float2half_rn(__fmul_rn(qb.d, (float)(qb.s_lo + qb.s_hi)));
-        uint32_t* o = reinterpret_cast<uint32_t*>(xq + i * Q8_1_BYTES);  // 4-byte aligned
-        o[0] = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(s16) << 16);
-#pragma unroll
-        for (int w = 0; w < 8; ++w) o[1 + w] = qb.q[w];
+        const Q81Lanes o = q8_1_quantize_8lanes(load_4_values(x + (int64_t)m * ldx + (int64_t)b * QK + 4 * sub, vec4));
+        if (mine < nblk) {
+            uint32_t* blk = reinterpret_cast<uint32_t*>(xq + mine * Q8_1_BYTES);  // 4-byte aligned
+            blk[1 + sub] = o.word;
+            if (sub == 0) {
+                const __half d16 = __float2half_rn(o.d);
+                const __half s16 = __float2half_rn(__fmul_rn(o.d, (float)o.s_all));
+                blk[0] = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(s16) << 16);
+            }
+        }
     }
 }
 
@@ -51,9 +62,10 @@ int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cu
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     const int NB = K / QK;
     const int64_t nblk = (int64_t)M * NB;
-    int64_t grid = (nblk + 63) / 64;
-    if (grid > (int64_t)di.sms * 8) grid = (int64_t)di.sms * 8;
-    quantize_q8_1_kernel<<<(int)grid, 64, 0, s>>>(x, ldx, static_cast<uint8_t*>(xq), M, NB);
+    const int64_t per_cta = (QUANT_THREADS / 32) * 4;  // blocks per CTA step
+    int64_t grid = (nblk + per_cta - 1) / per_cta;
+    if (grid > (int64_t)di.sms * 16) grid = (int64_t)di.sms * 16;
+    quantize_q8_1_kernel<<<(int)grid, QUANT_THREADS, 0, s>>>(x, ldx, static_cast<uint8_t*>(xq), M, NB);
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

@@ -38,33 +38,68 @@ constexpr int MAX_RING_STAGES = 8;
 // Launch configuration of one MMVQ call.
 struct MmvqPlan {
     bool ring;
-    int grid, warps, stages, KC;
+    int grid, warps, stages, parts, KC;
     size_t smem;
 };
+
+// K parts per row group for the ring kernel (part p: chunks p nch / P ..
+// (p + 1) nch / P - 1).  A CTA's G groups become G * P items dealt
+// round-robin to its W warps, so it runs ceil(G P / W) rounds of at most
+// ceil(nch / P) jobs plus one reduction (about a third of a job) each; take
+// the P with the fewest job-times (the smallest on a tie).  The top-1 kernel
+// keeps P = 1.
+inline int ring_parts(int64_t groups_per_cta, int nch, int max_warps, bool top1)
+{
+    if (top1) return 1;
+    int best_p = 1;
+    double best = 0.0;
+    for (int P = 1; P <= nch && P <= 32; ++P) {
+        const int64_t items = groups_per_cta * P;
+        const int64_t w = items < max_warps ? items : max_warps;
+        const int64_t rounds = (items + w - 1) / w;
+        const double cost = (double)rounds * ((double)((nch + P - 1) / P) + 0.35);
+        if (P == 1 || cost < best - 1e-9) {
+            best = cost;
+            best_p = P;
+        }
+    }
+    return best_p;
+}
 
 template <int FMT, int M, bool TOP1>
 MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N)
 {
     const Layout L = make_layout(FMT, N, K);
-    const int max_warps = MmvqThreads<M>::value / 32;
+    const int max_warps = MmvqThreads<FMT, M, TOP1>::value / 32;
     MmvqPlan p{};
     p.grid = L.n_groups < di.sms ? (int)L.n_groups : di.sms;
-    const int64_t per_cta = (L.n_groups + p.grid - 1) / p.grid;
-    p.warps = per_cta < max_warps ? (int)per_cta : max_warps;
-    const size_t act = (size_t)L.NB * (BlockAct<M>::STRIDE + 8 * M);
-    const size_t extra = TOP1 ? top1_scratch_bytes(p.warps) : 0;
-    const size_t stage = (size_t)L.chunk_bytes(GROUP, 0);
+    const int64_t per_cta = (L.n_groups + p.grid - 1) / p.grid;  // groups
+    p.parts = ring_parts(per_cta, L.nch, max_warps, TOP1);
+    const int64_t items = per_cta * p.parts;
+    p.warps = items < max_warps ? (int)items : max_warps;
+    const size_t act = RingAct<FMT, M>::bytes(L.NB);
+    const size_t extra = ring_extra_bytes<M, TOP1>((int)per_cta, p.parts, max_warps);
+    const size_t stage = (size_t)L.chunk_bytes(GROUP, 0) + 8;  // a group-chunk and its mbarrier
     const size_t fixed = act + extra + 128;
-    long long s = fixed < (size_t)di.smem_optin ? (long long)(((size_t)di.smem_optin - fixed) / (p.warps * (stage + 8))) : 0;
+    long long s = fixed < (size_t)di.smem_optin ? (long long)(((size_t)di.smem_optin - fixed) / (p.warps * stage)) : 0;
+    if (s < 2 && fixed < (size_t)di.smem_optin) {
+        // fewer warps with two stages each, if at least four fit
+        const long long w = (long long)(((size_t)di.smem_optin - fixed) / (2 * stage));
+        if (w >= 4) {
+            p.warps = (int)(w < p.warps ? w : p.warps);
+            s = 2;
+        }
+    }
     if (s > MAX_RING_STAGES) s = MAX_RING_STAGES;
     if (s >= 2) {
         p.ring = true;
         p.stages = (int)s;
         p.KC = L.NB;
-        p.smem = (size_t)p.warps * p.stages * (stage + 8) + act + extra;
+        p.smem = (size_t)p.warps * p.stages * stage + act + extra;
         return p;
     }
     p.ring = false;
+    p.parts = 1;
     p.warps = max_warps;
     const int64_t n_items = (L.n_groups + p.warps - 1) / p.warps;
     p.grid = n_items < di.sms ? (int)n_items : di.sms;
@@ -86,6 +121,7 @@ int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
     if (p.smem > (size_t)di.smem_optin) return QGEMV_UNSUPPORTED_SHAPE;
     a.KC = p.KC;
     a.stages = p.stages;
+    a.parts = p.parts;
     // Opt in to the device's full shared memory once per device and kernel.
     static bool opted_ring[64], opted_lock[64];
     static unsigned int* timeouts[64];

@@ -33,11 +33,14 @@ namespace qgemv {
 constexpr int MMVQ_MAX_THREADS = 512;
 constexpr int MMVQ_MAX_WARPS = MMVQ_MAX_THREADS / 32;
 
-// Threads per CTA: 16 warps while the R x M partial sums are few; 8 warps
-// (and so up to 255 registers per thread) for M > 8.
-template <int M>
+// Threads per CTA of the ring and lock-step kernels: 16 warps while the
+// R x M partial sums and the unpacked weights fit in 128 registers; 12 warps
+// (168 registers) for the few (format, M) that would spill; 8 warps (255
+// registers) for M > 8.
+template <int FMT, int M, bool TOP1>
 struct MmvqThreads {
-    static constexpr int value = M <= 8 ? 512 : 256;
+    static constexpr bool wide = FMT == FMT_Q4_0 ? (M == 7 || M == 8) : (M == 7 || M == 8 || (TOP1 && (M == 4 || M == 6)));
+    static constexpr int value = M > 8 ? 256 : (wide ? 384 : 512);
 };
 
 // Rows per warp: one 4-row group of the packed layout.
@@ -266,100 +269,138 @@ __device__ __forceinline__ void accumulate_q6_k(const uint4 (&ql)[R], const uint
 }
 
 // ---------------------------------------------------------------------------
-// Block-major activation tile of the Q6_K ring kernel: for block b the codes
-// of rows m = 0..M-1 lie at ab[b] + 32 m (two 16-byte halves), with a block
-// stride of (2M + 1) * 16 bytes (an odd number of 16-byte units, so that the
-// 32 lanes, which read 32 consecutive blocks, hit distinct bank groups), and
-// the per-(block, row) meta word at am[b * M + m].  One base address per lane
-// and compile-time offsets per row m.
+// Activation tile of the ring kernel, block-major: block b's codes for rows
+// m = 0..M-1 lie at q + b * QSTRIDE + 32 m (two 16-byte halves); QSTRIDE is an
+// odd number of 16-byte units, so the 32 lanes of a warp, which read 32
+// consecutive blocks, touch 32 distinct 16-byte bank groups (4 wavefronts,
+// no conflict).  Block b's per-row words lie at meta + (b * MROWS + m) * META
+// with MROWS = M rounded up to odd, for the same reason:
+//   Q4_0 (8 B):  fp32 bits of the fp16 scale d_a;  -8 * sum(q) + 0x4B400000
+//   Q6_K (16 B): fp32 bits of d_a; -32 * sum(q[0..15]); -32 * sum(q[16..31]); 0
+// The integer words start the dp4a chains, folding the weight offsets
+// (q_w - 8, q_w - 32) in exactly; the Q4_0 one also carries the bias of the
+// int -> float conversion below.
 // ---------------------------------------------------------------------------
 
-template <int M>
-struct BlockAct {
-    static constexpr int STRIDE = (2 * M + 1) * 16;
-    uint8_t* q;  // [NB][STRIDE]
-    uint2* am;   // [NB][M]
+template <int FMT, int M>
+struct RingAct {
+    static constexpr int QSTRIDE = (2 * M + 1) * 16;
+    static constexpr int MROWS = M | 1;
+    static constexpr int META = FMT == FMT_Q4_0 ? 8 : 16;
+    __host__ __device__ static constexpr size_t bytes(int NB)
+    {
+        return (size_t)NB * (size_t)(QSTRIDE + MROWS * META);
+    }
+    uint8_t* q;
+    uint8_t* meta;
 };
 
-template <int FMT, int M>
-__device__ __forceinline__ void block_act_from_q8_1(const BlockAct<M>& t, const uint8_t* xq, int NB)
+template <int FMT>
+__device__ __forceinline__ void ring_meta_store(uint8_t* p, float da, int s_lo, int s_hi)
 {
-    for (int i = threadIdx.x; i < M * NB; i += blockDim.x) {
-        const int m = i / NB, b = i - m * NB;
-        uint4 lo, hi;
-        uint2 meta;
-        act_from_q8_1<FMT>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES, lo, hi, meta);
-        uint4* dst = reinterpret_cast<uint4*>(t.q + b * BlockAct<M>::STRIDE + 32 * m);
-        dst[0] = lo;
-        dst[1] = hi;
-        t.am[b * M + m] = meta;
+    if (FMT == FMT_Q4_0) {
+        *reinterpret_cast<uint2*>(p) =
+            make_uint2(__float_as_uint(da), (uint32_t)(-8 * (s_lo + s_hi) + MAGIC_I2F_BITS));
+    } else {
+        *reinterpret_cast<uint4*>(p) = make_uint4(__float_as_uint(da), (uint32_t)(-32 * s_lo), (uint32_t)(-32 * s_hi), 0u);
     }
 }
 
+// From caller-supplied Q8_1 blocks in global memory (one thread per block).
 template <int FMT, int M>
-__device__ __forceinline__ void block_act_from_f32(const BlockAct<M>& t, const float* x, int64_t ldx, int NB)
+__device__ __forceinline__ void ring_act_from_q8_1(const RingAct<FMT, M>& t, const uint8_t* xq, int NB)
 {
+    using A = RingAct<FMT, M>;
+    for (int i = threadIdx.x; i < M * NB; i += blockDim.x) {
+        const int m = i / NB, b = i - m * NB;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES);
+        uint32_t q[8];
+        const uint32_t ds = w[0];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = w[1 + k];
+        uint4* dst = reinterpret_cast<uint4*>(t.q + b * A::QSTRIDE + 32 * m);
+        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        int s0 = 0, s1 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s0 = __dp4a((int)q[k], 0x01010101, s0);
+#pragma unroll
+        for (int k = 4; k < 8; ++k) s1 = __dp4a((int)q[k], 0x01010101, s1);
+        const float da = __half2float(__ushort_as_half((unsigned short)(ds & 0xFFFFu)));
+        ring_meta_store<FMT>(t.meta + (b * A::MROWS + m) * A::META, da, s0, s1);
+    }
+}
+
+// From fp32 activations, quantizing to Q8_1 on the fly with 8 lanes per block
+// (four blocks per warp step), bit-identical to the quantize_q8_1 kernel.
+template <int FMT, int M>
+__device__ __forceinline__ void ring_act_from_f32(const RingAct<FMT, M>& t, const float* x, int64_t ldx, int NB)
+{
+    using A = RingAct<FMT, M>;
     const bool vec4 = ((reinterpret_cast<uintptr_t>(x) | ((uintptr_t)ldx * 4)) & 15u) == 0;
-    for (int i = threadIdx.x; i < M * NB; i += blockDim.x) {
+    const int lane = threadIdx.x & 31, sub = lane & 7, W = blockDim.x >> 5;
+    const int nblk = M * NB;
+    for (int i0 = (threadIdx.x >> 5) * 4; i0 < nblk; i0 += W * 4) {  // warp-uniform
+        const int mine = i0 + (lane >> 3);
+        const int i = mine < nblk ? mine : nblk - 1;  // spare lanes redo the last block, unwritten
         const int m = i / NB, b = i - m * NB;
-        Q81Block qb;
-        q8_1_quantize_block(x + (int64_t)m * ldx + (int64_t)b * QK, vec4, qb);
-        uint4* dst = reinterpret_cast<uint4*>(t.q + b * BlockAct<M>::STRIDE + 32 * m);
-        dst[0] = make_uint4(qb.q[0], qb.q[1], qb.q[2], qb.q[3]);
-        dst[1] = make_uint4(qb.q[4], qb.q[5], qb.q[6], qb.q[7]);
-        uint2 meta;
-        meta.x = __float_as_uint(__half2float(__float2half_rn(qb.d)));
-        meta.y = act_meta_from_sums<FMT>(qb.s_lo, qb.s_hi);
-        t.am[b * M + m] = meta;
+        const Q81Lanes o = q8_1_quantize_8lanes(load_4_values(x + (int64_t)m * ldx + b * QK + 4 * sub, vec4));
+        if (mine < nblk) {
+            *reinterpret_cast<uint32_t*>(t.q + b * A::QSTRIDE + 32 * m + 4 * sub) = o.word;
+            if (sub == 0)
+                ring_meta_store<FMT>(t.meta + (b * A::MROWS + m) * A::META, __half2float(__float2half_rn(o.d)),
+                                     o.s_half, o.s_all - o.s_half);
+        }
     }
 }
 
-// Q4_0 block of R rows against the block-major tile (block index ti).
+// Q4_0 block (one per lane) of R rows against the tile.  ab, am: the block's
+// codes and meta words in the tile.
 template <int M, int R>
-__device__ __forceinline__ void accumulate_q4_0_blk(const uint4 (&w16)[R], const float (&dw)[R],
-                                                    const BlockAct<M>& t, int ti, float (&acc)[R][M])
+__device__ __forceinline__ void ring_dot_q4_0(const uint4 (&w16)[R], const float (&dw)[R], const uint8_t* ab,
+                                              const uint8_t* am, float (&acc)[R][M])
 {
     uint32_t w[R][8];
 #pragma unroll
     for (int r = 0; r < R; ++r) q4_0_unpack(w16[r], w[r]);
-    const uint8_t* ab = t.q + ti * BlockAct<M>::STRIDE;
-    const uint2* am = t.am + ti * M;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
         const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
         const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
-        const uint2 mt = am[m];
+        const uint2 mt = *reinterpret_cast<const uint2*>(am + 8 * m);
         const float da = __uint_as_float(mt.x);
-        const int init = (int)mt.y + MAGIC_I2F_BITS;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int sI = q4_0_dot(w[r], lo, hi, init);
+            const int sI = q4_0_dot(w[r], lo, hi, (int)mt.y);
             const float f = __int_as_float(sI) - MAGIC_I2F;  // exact I
             acc[r][m] = fmaf(dw[r] * da, f, acc[r][m]);
         }
     }
 }
 
-// Q6_K block of R rows against the block-major tile (block index ti).
+// Q6_K block (one per lane) of R rows against the tile.
 template <int M, int R>
-__device__ __forceinline__ void accumulate_q6_k_blk(const uint4 (&ql)[R], const uint2 (&qh)[R],
-                                                    const uint32_t (&sc)[R], const float (&dw)[R],
-                                                    const BlockAct<M>& t, int ti, float (&acc)[R][M])
+__device__ __forceinline__ void ring_dot_q6_k(const uint4 (&ql)[R], const uint2 (&qh)[R], const uint32_t (&sc2)[R],
+                                              const float (&dw)[R], const uint8_t* ab, const uint8_t* am,
+                                              float (&acc)[R][M])
 {
     uint32_t w[R][8];
+    int sc0[R], sc1[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) q6_k_unpack(ql[r], qh[r], w[r]);
-    const uint8_t* ab = t.q + ti * BlockAct<M>::STRIDE;
-    const uint2* am = t.am + ti * M;
+    for (int r = 0; r < R; ++r) {
+        q6_k_unpack(ql[r], qh[r], w[r]);
+        sc0[r] = (int)(int8_t)(sc2[r] & 0xFFu);
+        sc1[r] = (int)(int8_t)((sc2[r] >> 8) & 0xFFu);
+    }
 #pragma unroll
     for (int m = 0; m < M; ++m) {
         const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
         const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
-        const uint2 mt = am[m];
+        const uint4 mt = *reinterpret_cast<const uint4*>(am + 16 * m);
         const float da = __uint_as_float(mt.x);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int J = q6_k_dot(w[r], lo, hi, mt.y, sc[r]);
+            const int J = q6_k_dot_init(w[r], lo, hi, (int)mt.y, (int)mt.z, sc0[r], sc1[r]);
             acc[r][m] = fmaf(dw[r] * da, (float)J, acc[r][m]);
         }
     }
@@ -371,14 +412,15 @@ __device__ __forceinline__ void accumulate_q6_k_blk(const uint4 (&ql)[R], const 
 
 struct MmvqArgs {
     const void* w_pack;
-    const uint8_t* xq;  // Q8_1 [M][NB] (TOP1 = false)
-    const float* x;     // fp32 [M][ldx] (TOP1 = true)
+    const uint8_t* xq;  // Q8_1 [M][NB]; null (top-1 kernels only): quantize x in the kernel
+    const float* x;     // fp32 [M][ldx] (when xq is null)
     int64_t ldx;
     float* y;
     int64_t ldy;
     int K, N;
     int KC;      // activation blocks staged at once (lock-step kernel)
     int stages;  // ring stages per warp (ring kernel)
+    int parts;   // K parts per row group (ring kernel)
     Top1Workspace* ws;
     int32_t* ids;
 };
@@ -468,186 +510,371 @@ __device__ __forceinline__ void top1_finish(const MmvqArgs& a, unsigned long lon
 inline size_t top1_scratch_bytes(int nwarps) { return (size_t)nwarps * 64 * 8 + (size_t)nwarps * MAX_M * 8 + 16; }
 
 // ---------------------------------------------------------------------------
-// Ring kernel: the whole activation in shared memory, weights streamed by
-// per-warp TMA rings.
-//   shared memory: rings [W][S][stage] | aq [M][2][NB] | am [M][NB] |
-//                  mbarriers [W][S] | TOP1 scratch
-// The CTA's groups are g0 .. g1-1; warp w takes g0 + w, g0 + w + W, ...
-// Job j of a warp = (its group j / nch, chunk j % nch), in stage j % S: one
-// bulk copy of the group-chunk (4 rows' tiles and, for Q6_K, their scales).
-// Waits are bounded: a warp that waits about a second for a copy counts a
-// timeout in *timeouts, stops, and gives its copies in flight a bounded wait.
+// Ring kernel: the whole activation in shared memory, the weights streamed
+// through a private ring of S stages per warp, filled by TMA bulk copies.
+//   shared memory: rings [W][S][CB] | tile codes | tile meta | mbarriers
+//                  [W][S] | partial sums [groups][P][4 M] (P > 1) | top-1 keys
+// The CTA owns row groups g0 .. g1-1 (4 rows each).  Each group's K is cut
+// into the same P parts (chunks p nch / P .. (p + 1) nch / P - 1), so a group
+// is P items; warp w takes items w, w + W, ...  A job is one chunk of an item: one bulk copy of
+// the group-chunk (CB bytes) into the warp's next stage, completing on the
+// stage's mbarrier; lane 0 issues it S - 1 jobs ahead.  Lane l works on block
+// l of the chunk for the four rows, so one activation block feeds four rows
+// and one weight block M rows.  With P > 1 the parts' sums meet in shared
+// memory and are added in part order, so every output is summed the same way
+// wherever its row sits.  Waits are bounded: a warp that waits about a second
+// for a copy counts a timeout in *timeouts, stops, and gives its copies in
+// flight a bounded wait.
 // ---------------------------------------------------------------------------
 
+// Warp reduction of a row group's V = R * M sums, 32 at a time: chunk k
+// (sums 32 k .. 32 k + 31, the last one shorter) is transpose-reduced, and
+// lane `lane` keeps the total of value ring_value_index<V>(k, lane).
+template <int V>
+__device__ __forceinline__ int ring_value_index(int k, int lane)
+{
+    constexpr int LAST = 32 * ((V - 1) / 32);
+    constexpr int PL = next_pow2(V - LAST);
+    return 32 * k + (32 * k == LAST ? reduced_value_index<PL>(lane, 0) : lane);
+}
+
+template <int V>
+__device__ __forceinline__ bool ring_value_owner(int k, int lane)
+{
+    constexpr int LAST = 32 * ((V - 1) / 32);
+    constexpr int PL = next_pow2(V - LAST);
+    return 32 * k != LAST || (reduced_value_owner<PL>(lane) && reduced_value_index<PL>(lane, 0) < V - LAST);
+}
+
+template <int M, int R>
+__device__ __forceinline__ void ring_reduce(const float (&acc)[R][M], float (&out)[(R * M + 31) / 32], int lane)
+{
+    constexpr int V = R * M;
+    constexpr int NRED = (V + 31) / 32;
+    constexpr int LAST = 32 * (NRED - 1);
+    constexpr int PL = next_pow2(V - LAST);
+#pragma unroll
+    for (int k = 0; k < NRED - 1; ++k) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = acc[(32 * k + i) / M][(32 * k + i) % M];
+        warp_transpose_reduce<32>(v, lane);
+        out[k] = v[0];
+    }
+    float v[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        constexpr int dummy = 0;
+        const int vi = LAST + i < V ? LAST + i : dummy;
+        v[i] = LAST + i < V ? acc[vi / M][vi % M] : 0.0f;
+    }
+    warp_transpose_reduce<PL>(v, lane);
+    out[NRED - 1] = v[0];
+}
+
+// Bulk prefetch of global memory into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+constexpr int RING_PREFETCH_JOBS = 4;  // jobs per warp prefetched into L2 while the activation is staged
+
+// A warp's copy stream (kept by lane 0): the next chunk's source, the chunk
+// sizes of the current group (all but a row's last chunk, the last), the
+// chunk, the item's end chunk and the item.
+struct RingStream {
+    const uint8_t* src;
+    uint32_t cbr, cbl;
+    int c, c1, it, pad;
+};
+static_assert(sizeof(RingStream) % 8 == 0, "RingStream keeps the next shared array 8-byte aligned");
+
+__device__ __forceinline__ void ring_stream_at(RingStream& k, const Layout& L, const uint8_t* base, int64_t g0,
+                                               int n_items, int P, uint32_t CB, uint32_t CBL, int64_t GB, int it)
+{
+    k.it = it;
+    if (it >= n_items) return;
+    const int q = P == 1 ? it : it / P;
+    const int p = it - q * P;
+    const int64_t g = g0 + q;
+    const int rows = L.rows_in(g);
+    k.c = P == 1 ? 0 : p * L.nch / P;
+    k.c1 = P == 1 ? L.nch : (p + 1) * L.nch / P;
+    k.cbr = rows == GROUP ? CB : (uint32_t)L.chunk_bytes(rows, 0);
+    k.cbl = rows == GROUP ? CBL : (uint32_t)L.chunk_bytes(rows, L.nch - 1);
+    k.src = base + g * GB + (int64_t)k.c * k.cbr;
+}
+
+// Loads of one 4-row group's chunk from a ring stage.  whole: 4 rows and 32
+// blocks (compile-time offsets); otherwise `rows` rows and nb blocks (lanes
+// >= nb are idle): rows past the group's end repeat its last row (Q4_0) or
+// read stale bytes of the stage (Q6_K); their sums are discarded.
+template <int FMT>
+struct HalfLoads;
+
+template <>
+struct HalfLoads<FMT_Q4_0> {
+    uint4 w16[R_ROWS];
+    float dw[R_ROWS];
+    __device__ __forceinline__ void whole(const uint8_t* st, int lane)
+    {
+#pragma unroll
+        for (int q = 0; q < R_ROWS; ++q) w16[q] = *reinterpret_cast<const uint4*>(st + q * (CHUNK * 16) + lane * 16);
+        const uint2 dd = *reinterpret_cast<const uint2*>(st + R_ROWS * CHUNK * 16 + lane * 8);
+        dw[0] = __half2float(__ushort_as_half((unsigned short)(dd.x & 0xFFFFu)));
+        dw[1] = __half2float(__ushort_as_half((unsigned short)(dd.x >> 16)));
+        dw[2] = __half2float(__ushort_as_half((unsigned short)(dd.y & 0xFFFFu)));
+        dw[3] = __half2float(__ushort_as_half((unsigned short)(dd.y >> 16)));
+    }
+    __device__ __forceinline__ void part(const uint8_t* st, int lane, int rows, int nb)
+    {
+#pragma unroll
+        for (int q = 0; q < R_ROWS; ++q) {
+            const int rq = min(q, rows - 1);
+            w16[q] = *reinterpret_cast<const uint4*>(st + (rq * nb + lane) * 16);
+            dw[q] = __half2float(
+                __ushort_as_half(*reinterpret_cast<const uint16_t*>(st + nb * rows * 16 + (lane * rows + rq) * 2)));
+        }
+    }
+};
+
+template <>
+struct HalfLoads<FMT_Q6_K> {
+    uint4 ql[R_ROWS];
+    uint2 qh[R_ROWS];
+    uint32_t sc[R_ROWS];
+    float dw[R_ROWS];
+    __device__ __forceinline__ void whole(const uint8_t* st, int lane)
+    {
+        constexpr int TB = CHUNK * 26;
+#pragma unroll
+        for (int q = 0; q < R_ROWS; ++q) {
+            ql[q] = *reinterpret_cast<const uint4*>(st + q * TB + lane * 16);
+            qh[q] = *reinterpret_cast<const uint2*>(st + q * TB + CHUNK * 16 + lane * 8);
+            sc[q] = *reinterpret_cast<const uint16_t*>(st + q * TB + CHUNK * 24 + lane * 2);
+            dw[q] = __half2float(__ushort_as_half(
+                *reinterpret_cast<const uint16_t*>(st + R_ROWS * TB + (q * (CHUNK / 8) + (lane >> 3)) * 2)));
+        }
+    }
+    __device__ __forceinline__ void part(const uint8_t* st, int lane, int rows, int nb)
+    {
+        const int tb = nb * 26;
+        const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * tb);
+#pragma unroll
+        for (int q = 0; q < R_ROWS; ++q) {
+            ql[q] = *reinterpret_cast<const uint4*>(st + q * tb + lane * 16);
+            qh[q] = *reinterpret_cast<const uint2*>(st + q * tb + nb * 16 + lane * 8);
+            sc[q] = *reinterpret_cast<const uint16_t*>(st + q * tb + nb * 24 + lane * 2);
+            dw[q] = __half2float(__ushort_as_half(dq[min(q, rows - 1) * (nb >> 3) + (lane >> 3)]));
+        }
+    }
+};
+
+// One lane's block of a 4-row group against the tile.
+template <int M>
+__device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q4_0>& H, const uint8_t* ab, const uint8_t* am,
+                                          float (&acc)[R_ROWS][M])
+{
+    uint32_t w[R_ROWS][8];
+#pragma unroll
+    for (int q = 0; q < R_ROWS; ++q) q4_0_unpack(H.w16[q], w[q]);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
+        const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
+        const uint2 mt = *reinterpret_cast<const uint2*>(am + 8 * m);
+        const float da = __uint_as_float(mt.x);
+#pragma unroll
+        for (int q = 0; q < R_ROWS; ++q) {
+            const int sI = q4_0_dot(w[q], lo, hi, (int)mt.y);
+            acc[q][m] = fmaf(H.dw[q] * da, __int_as_float(sI) - MAGIC_I2F, acc[q][m]);
+        }
+    }
+}
+
+template <int M>
+__device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q6_K>& H, const uint8_t* ab, const uint8_t* am,
+                                          float (&acc)[R_ROWS][M])
+{
+    uint32_t w[R_ROWS][8];
+    int sc0[R_ROWS], sc1[R_ROWS];
+#pragma unroll
+    for (int q = 0; q < R_ROWS; ++q) {
+        q6_k_unpack(H.ql[q], H.qh[q], w[q]);
+        sc0[q] = (int)(int8_t)(H.sc[q] & 0xFFu);
+        sc1[q] = (int)(int8_t)((H.sc[q] >> 8) & 0xFFu);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
+        const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
+        const uint4 mt = *reinterpret_cast<const uint4*>(am + 16 * m);
+        const float da = __uint_as_float(mt.x);
+#pragma unroll
+        for (int q = 0; q < R_ROWS; ++q) {
+            const int J = q6_k_dot_init(w[q], lo, hi, (int)mt.y, (int)mt.z, sc0[q], sc1[q]);
+            acc[q][m] = fmaf(H.dw[q] * da, (float)J, acc[q][m]);
+        }
+    }
+}
+
 template <int FMT, int M, bool TOP1>
-__global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
+__global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
 {
     constexpr int R = R_ROWS;
+    constexpr int V = R * M;              // sums per row group
+    constexpr int NRED = (V + 31) / 32;   // reduced sums per lane
+    using Act = RingAct<FMT, M>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
-    const int S = a.stages;
+    const int S = a.stages, P = a.parts;
     const Layout L = make_layout(FMT, a.N, a.K);
     const int NB = L.NB, nch = L.nch;
-    const int stage_bytes = L.chunk_bytes(R, 0);
-
-    uint8_t* rings = smem;
-    BlockAct<M> t;
-    t.q = rings + (size_t)W * S * stage_bytes;
-    t.am = reinterpret_cast<uint2*>(t.q + (size_t)NB * BlockAct<M>::STRIDE);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(t.am + M * NB);
-    unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(bars + W * S);  // [W][64]
-    unsigned long long* s_best = s_keys + W * 64;                                     // [W][MAX_M]
-    int* s_last = reinterpret_cast<int*>(s_best + W * MAX_M);
-
+    const uint32_t CB = (uint32_t)L.chunk_bytes(R, 0), CBL = (uint32_t)L.chunk_bytes(R, nch - 1);
+    const int64_t GB = L.group_bytes(R);
     const int64_t g0 = (int64_t)blockIdx.x * L.n_groups / gridDim.x;
     const int64_t g1 = (int64_t)(blockIdx.x + 1) * L.n_groups / gridDim.x;
-    const int n_my = warp < g1 - g0 ? (int)((g1 - g0 - warp + W - 1) / W) : 0;
-    const int J = n_my * nch;
+    const int ng = (int)(g1 - g0);
+    const int n_items = ng * P;
+
+    uint8_t* rings = smem;
+    Act t;
+    t.q = rings + (size_t)W * S * CB;
+    t.meta = t.q + (size_t)NB * Act::QSTRIDE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(t.meta + (size_t)NB * Act::MROWS * Act::META);
+    RingStream* streams = reinterpret_cast<RingStream*>(bars + W * S);
+    float* part = reinterpret_cast<float*>(streams + W);
+    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(part + (P > 1 ? (size_t)ng * P * V : 0));
+    int* s_last = reinterpret_cast<int*>(s_best + MAX_M);
+    // top-1: running key of each reduced sum a lane holds, [NRED][W * 32]
+    unsigned long long* s_lane_best = reinterpret_cast<unsigned long long*>(s_best + MAX_M + 2);
+    static_assert(Act::META % 8 == 0 && (V * sizeof(float)) % 8 == 0, "ring shared-memory alignment");
 
     uint64_t* wbar = bars + warp * S;
-    uint8_t* wring = rings + (size_t)warp * S * stage_bytes;
+    uint8_t* wring = rings + (size_t)warp * S * CB;
     const uint8_t* wbase = static_cast<const uint8_t*>(a.w_pack);
     const uint64_t pol = l2_evict_first_policy();
 
+    if (TOP1) {
+        if (threadIdx.x < MAX_M) s_best[threadIdx.x] = 0ull;
+#pragma unroll
+        for (int j = 0; j < NRED; ++j) s_lane_best[j * blockDim.x + threadIdx.x] = 0ull;
+    }
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&wbar[s], 1);
         fence_barrier_init();
     }
     __syncwarp();
 
-    // Issue cursor (lane 0): next job's group, chunk and stage.
-    int issued = 0, iss_c = 0, iss_slot = 0;
-    int64_t iss_g = g0 + warp;
-    const int64_t GB = L.group_bytes(GROUP);  // bytes of a full group
-    const int CB = L.chunk_bytes(GROUP, 0);    // bytes of a full chunk of a full group
+    // Lane 0's copy stream, kept in shared memory so that it holds no
+    // registers in the main loop.
+    RingStream& k = streams[warp];
+    if (lane == 0) ring_stream_at(k, L, wbase, g0, n_items, P, CB, CBL, GB, warp);
+    int issued = 0, iss_slot = 0;
     auto issue_next = [&]() {
-        const int rows = L.rows_in(iss_g);
-        const bool full = rows == GROUP && (iss_c < nch - 1 || L.nb_tail == CHUNK);
-        const uint32_t bytes = full ? (uint32_t)CB : (uint32_t)L.chunk_bytes(rows, iss_c);
-        const int64_t off = iss_g * GB + (int64_t)iss_c * (rows == GROUP ? CB : L.chunk_bytes(rows, 0));
-        uint64_t* bar = &wbar[iss_slot];
+        const uint32_t bytes = k.c == nch - 1 ? k.cbl : k.cbr;
+        uint64_t* bar = wbar + iss_slot;
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(wring + (size_t)iss_slot * stage_bytes, wbase + off, bytes, bar, pol);
+        bulk_g2s(wring + (size_t)iss_slot * CB, k.src, bytes, bar, pol);
+        k.src += bytes;
         ++issued;
         if (++iss_slot == S) iss_slot = 0;
-        if (++iss_c == nch) {
-            iss_c = 0;
-            iss_g += W;
-        }
+        if (++k.c == k.c1) ring_stream_at(k, L, wbase, g0, n_items, P, CB, CBL, GB, k.it + W);
     };
     if (lane == 0) {
-        while (issued < S - 1 && issued < J) issue_next();
+        for (int s = 0; s < S - 1 && k.it < n_items; ++s) issue_next();
+        // Start HBM on the next jobs while the activation is staged.
+        RingStream pf = k;
+        for (int j = 0; j < RING_PREFETCH_JOBS && pf.it < n_items; ++j) {
+            const uint32_t bytes = pf.c == nch - 1 ? pf.cbl : pf.cbr;
+            bulk_prefetch_l2(pf.src, bytes);
+            pf.src += bytes;
+            if (++pf.c == pf.c1) ring_stream_at(pf, L, wbase, g0, n_items, P, CB, CBL, GB, pf.it + W);
+        }
     }
 
-    // The activation is staged while the first weight tiles are in flight.
-    if (TOP1) block_act_from_f32<FMT, M>(t, a.x, a.ldx, NB);
-    else block_act_from_q8_1<FMT, M>(t, a.xq, NB);
+    if (!TOP1 || a.xq) ring_act_from_q8_1<FMT, M>(t, a.xq, NB);
+    else ring_act_from_f32<FMT, M>(t, a.x, a.ldx, NB);
     __syncthreads();
 
-    unsigned long long best = 0ull;
-    float acc[R][M];
-    int consumed = 0;
-    int c = 0, slot = 0;
+    int consumed = 0, slot = 0;
     uint32_t phase = 0;
-    int64_t g = g0 + warp;
-    for (int j = 0; j < J; ++j) {
-        if (lane == 0 && issued < J) {
-            fence_proxy_async();
-            issue_next();
-        }
-        if (c == 0) {
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
-        }
-        const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&wbar[slot], phase));
-        if (!ready) {
-            if (lane == 0) atomicAdd(timeouts, 1u);
-            break;
-        }
-        consumed = j + 1;
-        const uint8_t* st = wring + (size_t)slot * stage_bytes;
+    bool alive = true;
+    // item it = (group gl, part p); it -> it + W moves (gl, p) by (W / P, W % P)
+    const int step_g = W / P, step_p = W - (W / P) * P;
+    int gl = warp / P, p = warp - (warp / P) * P;
+    for (int it = warp; it < n_items; it += W) {
+        const int64_t g = g0 + gl;
         const int rows = L.rows_in(g);
-        const int ti = c * CHUNK + lane;
-        const bool full_chunk = c != nch - 1 || L.nb_tail == CHUNK;
-        if (FMT == FMT_Q4_0) {
-            // block-major group-chunk: nib[block][row] then d[block][row]
-            uint4 w16[R];
-            float dw[R];
-            if (full_chunk && rows == R) {
+        float acc[R][M];
 #pragma unroll
-                for (int r = 0; r < R; ++r) w16[r] = *reinterpret_cast<const uint4*>(st + (lane * R + r) * 16);
-                const uint2 dd = *reinterpret_cast<const uint2*>(st + CHUNK * R * 16 + lane * R * 2);
-                dw[0] = __half2float(__ushort_as_half((unsigned short)(dd.x & 0xFFFFu)));
-                dw[1] = __half2float(__ushort_as_half((unsigned short)(dd.x >> 16)));
-                dw[2] = __half2float(__ushort_as_half((unsigned short)(dd.y & 0xFFFFu)));
-                dw[3] = __half2float(__ushort_as_half((unsigned short)(dd.y >> 16)));
-                accumulate_q4_0_blk<M, R>(w16, dw, t, ti, acc);
-            } else if (lane < L.nb(c)) {
-                // rows past the group's end read stale data; their sums are discarded
-                const int nb = L.nb(c);
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int rr = min(r, rows - 1);
-                    w16[r] = *reinterpret_cast<const uint4*>(st + (lane * rows + rr) * 16);
-                    dw[r] = __half2float(__ushort_as_half(
-                        *reinterpret_cast<const uint16_t*>(st + nb * rows * 16 + (lane * rows + rr) * 2)));
-                }
-                accumulate_q4_0_blk<M, R>(w16, dw, t, ti, acc);
+            for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
+        const int c0 = P == 1 ? 0 : p * nch / P, c1 = P == 1 ? nch : (p + 1) * nch / P;
+        for (int c = c0; c < c1; ++c) {
+            if (lane == 0 && k.it < n_items) {
+                fence_proxy_async();
+                issue_next();
             }
-        } else {
-        uint4 ql[R];
-        uint2 qh[R];
-        uint32_t sc[R];
-        float dw[R];
-        if (full_chunk) {
-            if (rows == R) {
-                // full chunk of a full group: every offset is a compile-time constant
-                constexpr int TB = CHUNK * 26;
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    ql[r] = *reinterpret_cast<const uint4*>(st + r * TB + lane * 16);
-                    qh[r] = *reinterpret_cast<const uint2*>(st + r * TB + CHUNK * 16 + lane * 8);
-                    sc[r] = *reinterpret_cast<const uint16_t*>(st + r * TB + CHUNK * 24 + lane * 2);
-                    dw[r] = __half2float(__ushort_as_half(
-                        *reinterpret_cast<const uint16_t*>(st + R * TB + (r * (CHUNK / 8) + (lane >> 3)) * 2)));
-                }
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wbar[slot], phase))) {
+                if (lane == 0) atomicAdd(timeouts, 1u);
+                alive = false;
+                break;
+            }
+            ++consumed;
+            const uint8_t* st = wring + (size_t)slot * CB;
+            const int ti = c * CHUNK + lane;
+            const uint8_t* ab = t.q + ti * Act::QSTRIDE;
+            const uint8_t* am = t.meta + ti * (Act::MROWS * Act::META);
+            HalfLoads<FMT> H;
+            if (rows == R && (c != nch - 1 || L.nb_tail == CHUNK)) {
+                H.whole(st, lane);
+                ring_dot4<M>(H, ab, am, acc);
             } else {
-                constexpr int TB = CHUNK * 26;
-                const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * TB);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    // rows past the group's end read stale data; their sums are discarded
-                    ql[r] = *reinterpret_cast<const uint4*>(st + r * TB + lane * 16);
-                    qh[r] = *reinterpret_cast<const uint2*>(st + r * TB + CHUNK * 16 + lane * 8);
-                    sc[r] = *reinterpret_cast<const uint16_t*>(st + r * TB + CHUNK * 24 + lane * 2);
-                    dw[r] = __half2float(__ushort_as_half(dq[min(r, rows - 1) * (CHUNK / 8) + (lane >> 3)]));
+                const int nb = L.nb(c);
+                if (lane < nb) {
+                    H.part(st, lane, rows, nb);
+                    ring_dot4<M>(H, ab, am, acc);
                 }
             }
-            accumulate_q6_k_blk<M, R>(ql, qh, sc, dw, t, ti, acc);
-        } else if (lane < L.nb_tail) {
-            const int nb = L.nb_tail, tb = nb * 26;
-            const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * tb);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                ql[r] = *reinterpret_cast<const uint4*>(st + r * tb + lane * 16);
-                qh[r] = *reinterpret_cast<const uint2*>(st + r * tb + nb * 16 + lane * 8);
-                sc[r] = *reinterpret_cast<const uint16_t*>(st + r * tb + nb * 24 + lane * 2);
-                dw[r] = __half2float(__ushort_as_half(dq[min(r, rows - 1) * (nb >> 3) + (lane >> 3)]));
+            __syncwarp();
+            if (++slot == S) {
+                slot = 0;
+                phase ^= 1u;
             }
-            accumulate_q6_k_blk<M, R>(ql, qh, sc, dw, t, ti, acc);
         }
+        if (!alive) break;
+
+        float v[NRED];
+        ring_reduce<M, R>(acc, v, lane);
+#pragma unroll
+        for (int j = 0; j < NRED; ++j) {
+            const int vi = ring_value_index<V>(j, lane);
+            if (!ring_value_owner<V>(j, lane)) continue;
+            if (P > 1) {
+                part[((size_t)gl * P + p) * V + vi] = v[j];
+                continue;
+            }
+            const int rr = vi / M, m = vi - rr * M;
+            if (rr < rows) {
+                const int n = (int)(g * GROUP) + rr;
+                if (TOP1) {
+                    // the lane's running key for value vi (chunk j of the reduction)
+                    unsigned long long& b = s_lane_best[j * blockDim.x + threadIdx.x];
+                    const unsigned long long key = top1_key(v[j], n);
+                    if (key > b) b = key;
+                } else {
+                    a.y[(int64_t)m * a.ldy + n] = v[j];
+                }
+            }
         }
-        __syncwarp();
-        if (c == nch - 1) finish_rowgroup<M, R, TOP1>(a, (int)(g * GROUP), acc, lane, s_keys + warp * 64, best);
-        if (++slot == S) {
-            slot = 0;
-            phase ^= 1u;
-        }
-        if (++c == nch) {
-            c = 0;
-            g += W;
+        gl += step_g;
+        p += step_p;
+        if (p >= P) {
+            p -= P;
+            ++gl;
         }
     }
     // After a timeout, give the copies still in flight a bounded wait before
@@ -657,7 +884,59 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(con
     }
     __syncwarp();
 
-    if (TOP1) top1_finish<M>(a, s_best, s_last, best, lane, warp, W);
+    if (P > 1) {
+        // Add the parts of every output in part order.
+        __syncthreads();
+        for (int o = threadIdx.x; o < ng * V; o += blockDim.x) {
+            const int q = o / V, vi = o - q * V;
+            const float* pp = part + (size_t)q * P * V + vi;
+            float sum = pp[0];
+            for (int j = 1; j < P; ++j) sum += pp[(size_t)j * V];
+            const int rr = vi / M, m = vi - rr * M;
+            const int64_t n = (g0 + q) * GROUP + rr;
+            if (n < a.N) {
+                if (TOP1) atomicMax(&s_best[m], top1_key(sum, (int)n));
+                else a.y[(int64_t)m * a.ldy + n] = sum;
+            }
+        }
+    }
+    if (TOP1) {
+        if (P == 1) {
+#pragma unroll
+            for (int j = 0; j < NRED; ++j) {
+                const unsigned long long b = s_lane_best[j * blockDim.x + threadIdx.x];
+                if (b != 0ull) atomicMax(&s_best[ring_value_index<V>(j, lane) % M], b);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < M) atomicMax(&a.ws->keys[threadIdx.x], s_best[threadIdx.x]);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const unsigned prev = atomicAdd(&a.ws->done, 1u);
+            *s_last = prev == gridDim.x - 1;
+        }
+        __syncthreads();
+        if (*s_last) {
+            __threadfence();
+            if (threadIdx.x < M) {
+                const unsigned long long key = atomicExch(&a.ws->keys[threadIdx.x], 0ull);
+                a.ids[threadIdx.x] = top1_key_to_id(key);
+            }
+            if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
+        }
+    }
+}
+
+// Shared memory of the ring kernel besides the rings, their mbarriers and
+// the tile.
+template <int M, bool TOP1>
+inline size_t ring_extra_bytes(int max_groups_per_cta, int P, int warps)
+{
+    const size_t streams = (size_t)warps * sizeof(RingStream);
+    const size_t part = P > 1 ? (size_t)max_groups_per_cta * P * R_ROWS * M * sizeof(float) : 0;
+    const size_t nred = (R_ROWS * M + 31) / 32;
+    return streams + part + (TOP1 ? (size_t)(MAX_M + 2) * 8 + nred * warps * 32 * 8 : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -668,7 +947,7 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_ring_kernel(con
 // ---------------------------------------------------------------------------
 
 template <int FMT, int M, bool TOP1>
-__global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_lockstep_kernel(const MmvqArgs a)
+__global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lockstep_kernel(const MmvqArgs a)
 {
     constexpr int R = R_ROWS;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -701,8 +980,8 @@ __global__ void __launch_bounds__(MmvqThreads<M>::value, 1) mmvq_lockstep_kernel
         for (int cc = 0; cc < nchunks; ++cc) {
             const int kb0 = cc * KC, kb1 = min(NB, kb0 + KC);
             __syncthreads();
-            if (TOP1) stage_from_f32<FMT, M>(t, a.x, a.ldx, kb0, kb1);
-            else stage_from_q8_1<FMT, M>(t, a.xq, NB, kb0, kb1);
+            if (!TOP1 || a.xq) stage_from_q8_1<FMT, M>(t, a.xq, NB, kb0, kb1);
+            else stage_from_f32<FMT, M>(t, a.x, a.ldx, kb0, kb1);
             __syncthreads();
             if (!active) continue;
             for (int b = kb0 + lane; b < kb1; b += 32) {

@@ -33,12 +33,13 @@ constexpr int MAX_M = 17;
 // fetched with a single bulk copy, and a whole group is contiguous too.
 // Groups follow one another; inside a group the chunks follow one another.
 //
-// Q4_0 group-chunk of `rows` rows and nb blocks, block-major:
-//   nib[nb][rows] (16 B each: the canonical qs bytes of the block, unchanged)
+// Q4_0 group-chunk of `rows` rows and nb blocks:
+//   nib[rows][nb] (16 B each: the canonical qs bytes of the block, unchanged)
 //   d[nb][rows] (fp16 bits, copied raw), zero padded to 16 B.
-//   4 rows x 32 blocks = 2048 + 256 = 2304 B.  Block-major order puts the four
-//   rows of one block next to each other, so a lane reads its block's four
-//   scales with one 8-byte load.
+//   4 rows x 32 blocks = 2048 + 256 = 2304 B.  Row-major codes let the 32
+//   lanes of a warp (one block each) read 512 consecutive bytes per row; the
+//   block-major scales put the four rows of one block next to each other, so
+//   a lane reads its block's four scales with one 8-byte load.
 // Q6_K group-chunk (nb a multiple of 8), row-major: per row one tile
 //   ql[nb] 16 B: byte t = low4(q[t]) | low4(q[t + 16]) << 4
 //   qh[nb]  8 B: byte t, bits 2s..2s+1 = high2(q[t + 8 s]), s = 0..3
@@ -116,7 +117,7 @@ __host__ __device__ inline BlockAddr block_addr(const void* base, const Layout& 
     const uint8_t* gc = static_cast<const uint8_t*>(base) + L.chunk_offset(g, c);
     BlockAddr a;
     if (L.fmt == 0) {
-        a.q = gc + (j * rows + r) * 16;
+        a.q = gc + (r * nb + j) * 16;
         a.d = gc + nb * rows * 16 + (j * rows + r) * 2;
         a.qh = a.sc = nullptr;
     } else {
@@ -217,6 +218,50 @@ __device__ __forceinline__ void q8_1_quantize_block(const float* xb, bool vec4, 
     }
     o.s_lo = s0;
     o.s_hi = s1;
+}
+
+// The same quantization of one 32-value block by 8 consecutive lanes of a
+// warp (lanes 8k .. 8k+7; sub = lane & 7 holds values 4 sub .. 4 sub + 3).
+// Every lane of the warp must call it (full-warp shuffles).  The maximum, the
+// divides and the rounding are the single-thread routine's, so the codes and
+// scales are bit-identical to it.
+struct Q81Lanes {
+    uint32_t word;  // codes 4 sub .. 4 sub + 3 (word `sub` of the block's codes)
+    float d;        // fp32 scale (before fp16 rounding), same in all 8 lanes
+    int s_half;     // sum of codes 0..15 (sub < 4) or 16..31 (sub >= 4)
+    int s_all;      // sum of all 32 codes
+};
+
+__device__ __forceinline__ Q81Lanes q8_1_quantize_8lanes(const float4 v)
+{
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    Q81Lanes o;
+    o.d = __fdiv_rn(amax, 127.0f);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+    if (amax != 0.0f) {
+        q0 = max(-127, min(127, (int)roundf(__fdiv_rn(v.x, o.d))));
+        q1 = max(-127, min(127, (int)roundf(__fdiv_rn(v.y, o.d))));
+        q2 = max(-127, min(127, (int)roundf(__fdiv_rn(v.z, o.d))));
+        q3 = max(-127, min(127, (int)roundf(__fdiv_rn(v.w, o.d))));
+    }
+    o.word = ((uint32_t)q0 & 0xFFu) | (((uint32_t)q1 & 0xFFu) << 8) | (((uint32_t)q2 & 0xFFu) << 16) |
+             ((uint32_t)q3 << 24);
+    int s = q0 + q1 + q2 + q3;
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    o.s_half = s;
+    o.s_all = s + __shfl_xor_sync(0xffffffffu, s, 4);
+    return o;
+}
+
+// Four values of a block for q8_1_quantize_8lanes (vec4: p is 16-byte aligned).
+__device__ __forceinline__ float4 load_4_values(const float* p, bool vec4)
+{
+    if (vec4) return *reinterpret_cast<const float4*>(p);
+    return make_float4(p[0], p[1], p[2], p[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -320,13 +365,12 @@ __device__ __forceinline__ void q6_k_unpack(const uint4 ql, const uint2 qh, uint
     w[7] = ((ql.w >> 4) & m4) | ((qh.y >> 2) & m2);
 }
 
-// J = sc0 * sum_{i<16} (q - 32) q_a + sc1 * sum_{i>=16} (q - 32) q_a.
-// sums = sum(q_a[0..15]) | sum(q_a[16..31]) << 16; sc2 = the two int8 subscales.
-__device__ __forceinline__ int q6_k_dot(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, uint32_t sums,
-                                        uint32_t sc2)
+// J = sc0 * sum_{i<16} (q - 32) q_a + sc1 * sum_{i>=16} (q - 32) q_a, with the
+// offsets folded into the chain starts: g0 = -32 * sum(q_a[0..15]),
+// g1 = -32 * sum(q_a[16..31]); sc0, sc1 = the block's two int8 subscales.
+__device__ __forceinline__ int q6_k_dot_init(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, int g0, int g1,
+                                             int sc0, int sc1)
 {
-    int g0 = -32 * (int)(int16_t)(sums & 0xFFFFu);
-    int g1 = -32 * (int)(int16_t)(sums >> 16);
     g0 = __dp4a((int)w[0], (int)lo.x, g0);
     g0 = __dp4a((int)w[1], (int)lo.y, g0);
     g0 = __dp4a((int)w[2], (int)lo.z, g0);
@@ -335,9 +379,16 @@ __device__ __forceinline__ int q6_k_dot(const uint32_t (&w)[8], const uint4 lo, 
     g1 = __dp4a((int)w[5], (int)hi.y, g1);
     g1 = __dp4a((int)w[6], (int)hi.z, g1);
     g1 = __dp4a((int)w[7], (int)hi.w, g1);
-    int sc0 = (int)(int8_t)(sc2 & 0xFFu);
-    int sc1 = (int)(int8_t)(sc2 >> 8);
     return sc0 * g0 + sc1 * g1;
+}
+
+// Same, from the packed activation sums (sum(q_a[0..15]) | sum(q_a[16..31])
+// << 16, int16 pair) and the two subscale bytes sc2.
+__device__ __forceinline__ int q6_k_dot(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, uint32_t sums,
+                                        uint32_t sc2)
+{
+    return q6_k_dot_init(w, lo, hi, -32 * (int)(int16_t)(sums & 0xFFFFu), -32 * (int)(int16_t)(sums >> 16),
+                         (int)(int8_t)(sc2 & 0xFFu), (int)(int8_t)((sc2 >> 8) & 0xFFu));
 }
 
 // Exact int -> float for |i| < 2^22 without a conversion instruction: the

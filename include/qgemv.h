@@ -68,7 +68,8 @@ size_t q8_1_bytes(int M, int K);
 size_t q4_0_pack_bytes(int N, int K);
 /* Bytes of a packed Q6_K weight: N * (K/256) * 210 (the canonical size). */
 size_t q6_k_pack_bytes(int N, int K);
-/* Workspace bytes of lmhead_q6_k_top1 and argmax_f32_rows (a few hundred). */
+/* Workspace bytes of lmhead_q6_k_top1 (256 + M * (K/32) * 36, rounded up to
+ * 16) and argmax_f32_rows (256). */
 size_t lmhead_q6_k_top1_workspace_bytes(int M, int K, int N);
 size_t argmax_f32_rows_workspace_bytes(int M, int N);
 
@@ -139,9 +140,13 @@ int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
  *   x          fp32 [M][ldx], ldx >= K (read); pass row 1 of a [6][K] block
  *              with M = 5 for the rows-1..5 view
  *   ids        int32 [M] (written)
- *   workspace  lmhead_q6_k_top1_workspace_bytes(M, K, N) bytes, zero-filled
- *              before its first use; every call leaves it zero-filled again.
- *              Calls that share a workspace must not overlap in time.
+ *   workspace  lmhead_q6_k_top1_workspace_bytes(M, K, N) bytes.  Its first
+ *              256 bytes (the cross-CTA top-1 keys and counter) must be
+ *              zero-filled before the first use, and every call leaves them
+ *              zero-filled again; the rest receives the Q8_1 copy of x that
+ *              a quantize_q8_1 pre-pass writes on `stream` before the MMVQ
+ *              kernel reads it.  Calls that share a workspace must not
+ *              overlap in time.
  *   1 <= M <= 17, K % 256 == 0, N >= 1. */
 int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* ids, void* workspace,
                      size_t ws_bytes, int M, int K, int N, void* stream);

@@ -26,13 +26,13 @@ def _groups(N: int):
 
 def pack_q4_0(w: np.ndarray) -> np.ndarray:
     """Canonical Q4_0 [N, K/32, 18] -> the documented layout: groups of 4 rows;
-    per (group, 32-block chunk), block-major: the 16-byte code blocks [block][row],
-    then the fp16 scales [block][row], zero-padded to 16 bytes."""
+    per (group, 32-block chunk): the 16-byte code blocks [row][block], then the
+    fp16 scales [block][row], zero-padded to 16 bytes."""
     N, nb, _ = w.shape
     out = []
     for g0, rows in _groups(N):
         for c0, n in _chunks(nb):
-            nib = w[g0:g0 + rows, c0:c0 + n, 2:18].transpose(1, 0, 2).reshape(-1)
+            nib = w[g0:g0 + rows, c0:c0 + n, 2:18].reshape(-1)
             d = w[g0:g0 + rows, c0:c0 + n, 0:2].transpose(1, 0, 2).reshape(-1)
             out += [nib, d, np.zeros(_pad16(d.size) - d.size, dtype=np.uint8)]
     return np.concatenate(out)
@@ -45,7 +45,7 @@ def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
     off = 0
     for g0, rows in _groups(N):
         for c0, n in _chunks(nb):
-            out[g0:g0 + rows, c0:c0 + n, 2:18] = pack[off:off + 16 * n * rows].reshape(n, rows, 16).transpose(1, 0, 2)
+            out[g0:g0 + rows, c0:c0 + n, 2:18] = pack[off:off + 16 * n * rows].reshape(rows, n, 16)
             off += 16 * n * rows
             out[g0:g0 + rows, c0:c0 + n, 0:2] = pack[off:off + 2 * n * rows].reshape(n, rows, 2).transpose(1, 0, 2)
             off += _pad16(2 * n * rows)
