@@ -34,6 +34,8 @@ constexpr int QUANT_THREADS = 128;
 __global__ void __launch_bounds__(QUANT_THREADS) quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
                                                                       uint8_t* __restrict__ xq, int M, int NB)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t nblk = (int64_t)M * NB;
     const bool vec4 = ((reinterpret_cast<uintptr_t>(x) | ((uintptr_t)ldx * 4)) & 15u) == 0;
     const int lane = threadIdx.x & 31, sub = lane & 7;
@@ -65,7 +67,9 @@ int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cu
     const int64_t per_cta = (QUANT_THREADS / 32) * 4;  // blocks per CTA step
     int64_t grid = (nblk + per_cta - 1) / per_cta;
     if (grid > (int64_t)di.sms * 16) grid = (int64_t)di.sms * 16;
-    quantize_q8_1_kernel<<<(int)grid, QUANT_THREADS, 0, s>>>(x, ldx, static_cast<uint8_t*>(xq), M, NB);
+    if (launch_pdl(quantize_q8_1_kernel, dim3((unsigned)grid), dim3(QUANT_THREADS), 0, s, x, ldx,
+                   static_cast<uint8_t*>(xq), M, NB) != cudaSuccess)
+        return QGEMV_CUDA_ERROR;
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -194,6 +198,8 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float
 {
     __shared__ unsigned long long s_red[ARGMAX_THREADS / 32][M];
     __shared__ int s_last;
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned long long k[M];
 #pragma unroll
@@ -262,10 +268,10 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float
 }
 
 template <int M>
-static void launch_argmax_m(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int N, int grid,
-                            cudaStream_t s)
+static cudaError_t launch_argmax_m(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int N, int grid,
+                                   cudaStream_t s)
 {
-    argmax_rows_kernel<M><<<grid, ARGMAX_THREADS, 0, s>>>(y, ldy, ids, ws, N);
+    return launch_pdl(argmax_rows_kernel<M>, dim3(grid), dim3(ARGMAX_THREADS), 0, s, y, ldy, ids, ws, N);
 }
 
 int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int M, int N, cudaStream_t s)
@@ -275,9 +281,10 @@ int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace*
     int grid = (int)(((int64_t)N + ARGMAX_THREADS * 4 - 1) / (ARGMAX_THREADS * 4));
     if (grid > di.sms * 2) grid = di.sms * 2;
     if (grid < 1) grid = 1;
+    cudaError_t e = cudaSuccess;
     switch (M) {
 #define QGEMV_ARGMAX_CASE(m) \
-    case m: launch_argmax_m<m>(y, ldy, ids, ws, N, grid, s); break;
+    case m: e = launch_argmax_m<m>(y, ldy, ids, ws, N, grid, s); break;
     QGEMV_ARGMAX_CASE(1) QGEMV_ARGMAX_CASE(2) QGEMV_ARGMAX_CASE(3) QGEMV_ARGMAX_CASE(4) QGEMV_ARGMAX_CASE(5)
     QGEMV_ARGMAX_CASE(6) QGEMV_ARGMAX_CASE(7) QGEMV_ARGMAX_CASE(8) QGEMV_ARGMAX_CASE(9) QGEMV_ARGMAX_CASE(10)
     QGEMV_ARGMAX_CASE(11) QGEMV_ARGMAX_CASE(12) QGEMV_ARGMAX_CASE(13) QGEMV_ARGMAX_CASE(14)
@@ -285,7 +292,7 @@ int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace*
 #undef QGEMV_ARGMAX_CASE
     default: return QGEMV_UNSUPPORTED_SHAPE;
     }
-    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
 // ---------------------------------------------------------------------------

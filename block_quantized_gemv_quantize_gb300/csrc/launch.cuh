@@ -17,6 +17,25 @@ struct DeviceInfo {
 // Per-device properties, queried once per device.
 DeviceInfo device_info();
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream drains; it orders itself after that
+// kernel with pdl_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Counts warps that gave up waiting for a weight copy (one per translation
 // unit that instantiates the ring kernel).
 static __device__ unsigned int g_wait_timeouts;
@@ -134,7 +153,8 @@ int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
                 return QGEMV_CUDA_ERROR;
             opted_ring[dev] = true;
         }
-        kern<<<p.grid, p.warps * 32, p.smem, s>>>(a, timeouts[dev]);
+        if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a, timeouts[dev]) != cudaSuccess)
+            return QGEMV_CUDA_ERROR;
     } else {
         auto kern = mmvq_lockstep_kernel<FMT, M, TOP1>;
         if (!opted_lock[dev]) {
@@ -142,7 +162,7 @@ int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
                 return QGEMV_CUDA_ERROR;
             opted_lock[dev] = true;
         }
-        kern<<<p.grid, p.warps * 32, p.smem, s>>>(a);
+        if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a) != cudaSuccess) return QGEMV_CUDA_ERROR;
     }
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }

@@ -512,8 +512,9 @@ inline size_t top1_scratch_bytes(int nwarps) { return (size_t)nwarps * 64 * 8 + 
 // ---------------------------------------------------------------------------
 // Ring kernel: the whole activation in shared memory, the weights streamed
 // through a private ring of S stages per warp, filled by TMA bulk copies.
-//   shared memory: rings [W][S][CB] | tile codes | tile meta | mbarriers
-//                  [W][S] | partial sums [groups][P][4 M] (P > 1) | top-1 keys
+//   shared memory: copy streams [W] | rings [W][S][CB] | tile codes |
+//                  tile meta | mbarriers [W][S] | partial sums [groups][P][4 M]
+//                  (P > 1) | top-1 keys
 // The CTA owns row groups g0 .. g1-1 (4 rows each).  Each group's K is cut
 // into the same P parts (chunks p nch / P .. (p + 1) nch / P - 1), so a group
 // is P items; warp w takes items w, w + W, ...  A job is one chunk of an item: one bulk copy of
@@ -578,17 +579,17 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-constexpr int RING_PREFETCH_JOBS = 4;  // jobs per warp prefetched into L2 while the activation is staged
+constexpr int RING_PREFETCH_JOBS = 6;  // jobs per warp prefetched into L2 beyond the ring's first S - 1
 
 // A warp's copy stream (kept by lane 0): the next chunk's source, the chunk
 // sizes of the current group (all but a row's last chunk, the last), the
 // chunk, the item's end chunk and the item.
-struct RingStream {
+struct alignas(16) RingStream {
     const uint8_t* src;
     uint32_t cbr, cbl;
     int c, c1, it, pad;
 };
-static_assert(sizeof(RingStream) % 8 == 0, "RingStream keeps the next shared array 8-byte aligned");
+static_assert(sizeof(RingStream) == 32, "RingStream is two 16-byte words");
 
 __device__ __forceinline__ void ring_stream_at(RingStream& k, const Layout& L, const uint8_t* base, int64_t g0,
                                                int n_items, int P, uint32_t CB, uint32_t CBL, int64_t GB, int it)
@@ -727,24 +728,26 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
     constexpr int NRED = (V + 31) / 32;   // reduced sums per lane
     using Act = RingAct<FMT, M>;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, W = blockDim.x >> 5;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);  // warp-uniform
     const int S = a.stages, P = a.parts;
     const Layout L = make_layout(FMT, a.N, a.K);
     const int NB = L.NB, nch = L.nch;
     const uint32_t CB = (uint32_t)L.chunk_bytes(R, 0), CBL = (uint32_t)L.chunk_bytes(R, nch - 1);
+    pdl_launch_dependents();
     const int64_t GB = L.group_bytes(R);
     const int64_t g0 = (int64_t)blockIdx.x * L.n_groups / gridDim.x;
     const int64_t g1 = (int64_t)(blockIdx.x + 1) * L.n_groups / gridDim.x;
     const int ng = (int)(g1 - g0);
     const int n_items = ng * P;
 
-    uint8_t* rings = smem;
+    RingStream* streams = reinterpret_cast<RingStream*>(smem);  // [W], first: 16-byte aligned
+    uint8_t* rings = smem + (size_t)W * sizeof(RingStream);
     Act t;
     t.q = rings + (size_t)W * S * CB;
     t.meta = t.q + (size_t)NB * Act::QSTRIDE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(t.meta + (size_t)NB * Act::MROWS * Act::META);
-    RingStream* streams = reinterpret_cast<RingStream*>(bars + W * S);
-    float* part = reinterpret_cast<float*>(streams + W);
+    float* part = reinterpret_cast<float*>(bars + W * S);
     unsigned long long* s_best = reinterpret_cast<unsigned long long*>(part + (P > 1 ? (size_t)ng * P * V : 0));
     int* s_last = reinterpret_cast<int*>(s_best + MAX_M);
     // top-1: running key of each reduced sum a lane holds, [NRED][W * 32]
@@ -771,28 +774,63 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
     // registers in the main loop.
     RingStream& k = streams[warp];
     if (lane == 0) ring_stream_at(k, L, wbase, g0, n_items, P, CB, CBL, GB, warp);
+    // The next item is usually the whole group W groups on (P = 1): its first
+    // chunk starts (W - 1) * GB past the end of the current group.
+    const int64_t skip = (int64_t)(W - 1) * GB;
+    const int64_t last_whole = (a.N % GROUP) ? L.n_groups - 2 : L.n_groups - 1;  // last full group
+    // Lane 0 takes the next job off its stream (bytes = 0: none left).
+    auto next_job = [&](const uint8_t*& src) -> uint32_t {
+        RingStream ks = k;  // one copy in, one copy out
+        if (ks.it >= n_items) return 0;
+        const uint32_t bytes = ks.c == nch - 1 ? ks.cbl : ks.cbr;
+        src = ks.src;
+        ks.src += bytes;
+        if (++ks.c == ks.c1) {
+            const int nit = ks.it + W;
+            if (P == 1 && ks.cbr == CB && g0 + nit <= last_whole && nit < n_items) {
+                ks.src += skip;
+                ks.c = 0;
+                ks.it = nit;
+            } else {
+                ring_stream_at(ks, L, wbase, g0, n_items, P, CB, CBL, GB, nit);
+            }
+        }
+        k = ks;
+        return bytes;
+    };
+    // The whole warp: the copy's operands are made warp-uniform (broadcast
+    // from lane 0, slot counted by every lane) and lane 0 issues it.
     int issued = 0, iss_slot = 0;
+    const uint64_t pol_u = __shfl_sync(0xffffffffu, pol, 0);
     auto issue_next = [&]() {
-        const uint32_t bytes = k.c == nch - 1 ? k.cbl : k.cbr;
+        const uint8_t* src = wbase;
+        uint32_t bytes = 0;
+        if (lane == 0) bytes = next_job(src);
+        bytes = __shfl_sync(0xffffffffu, bytes, 0);
+        if (bytes == 0) return;
+        src = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), 0));
         uint64_t* bar = wbar + iss_slot;
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(wring + (size_t)iss_slot * CB, k.src, bytes, bar, pol);
-        k.src += bytes;
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(wring + (size_t)iss_slot * CB, src, bytes, bar, pol_u);
+        }
         ++issued;
         if (++iss_slot == S) iss_slot = 0;
-        if (++k.c == k.c1) ring_stream_at(k, L, wbase, g0, n_items, P, CB, CBL, GB, k.it + W);
     };
     if (lane == 0) {
-        for (int s = 0; s < S - 1 && k.it < n_items; ++s) issue_next();
-        // Start HBM on the next jobs while the activation is staged.
+        // Start HBM on the first jobs (L2 prefetch) while the previous kernel
+        // of the stream drains and the activation is staged.
         RingStream pf = k;
-        for (int j = 0; j < RING_PREFETCH_JOBS && pf.it < n_items; ++j) {
+        for (int j = 0; j < S - 1 + RING_PREFETCH_JOBS && pf.it < n_items; ++j) {
             const uint32_t bytes = pf.c == nch - 1 ? pf.cbl : pf.cbr;
             bulk_prefetch_l2(pf.src, bytes);
             pf.src += bytes;
             if (++pf.c == pf.c1) ring_stream_at(pf, L, wbase, g0, n_items, P, CB, CBL, GB, pf.it + W);
         }
     }
+    pdl_wait();  // the previous kernel's writes (activation, weights, workspace) are visible from here
+    for (int s = 0; s < S - 1; ++s) issue_next();
 
     if (!TOP1 || a.xq) ring_act_from_q8_1<FMT, M>(t, a.xq, NB);
     else ring_act_from_f32<FMT, M>(t, a.x, a.ldx, NB);
@@ -814,10 +852,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
         const int c0 = P == 1 ? 0 : p * nch / P, c1 = P == 1 ? nch : (p + 1) * nch / P;
         for (int c = c0; c < c1; ++c) {
-            if (lane == 0 && k.it < n_items) {
-                fence_proxy_async();
-                issue_next();
-            }
+            issue_next();
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wbar[slot], phase))) {
                 if (lane == 0) atomicAdd(timeouts, 1u);
                 alive = false;
@@ -949,6 +984,8 @@ inline size_t ring_extra_bytes(int max_groups_per_cta, int P, int warps)
 template <int FMT, int M, bool TOP1>
 __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lockstep_kernel(const MmvqArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int R = R_ROWS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;

@@ -131,6 +131,19 @@ __host__ __device__ inline BlockAddr block_addr(const void* base, const Layout& 
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch (the library's kernels are launched with
+// programmatic stream serialization): a kernel lets the next kernel of the
+// stream be scheduled as soon as it starts, and waits for the previous one
+// (its completion and memory) before touching anything that kernel may
+// write or read.  Only L2 prefetches of weights run before the wait: they
+// cannot observe stale data, since writes are made in L2.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // Loads
 // ---------------------------------------------------------------------------
 
