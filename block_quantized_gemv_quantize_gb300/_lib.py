@@ -35,6 +35,7 @@ SIGNATURES = {
     "qpack_q6_k": (_I, [_P, _P, _I, _I, _P]),
     "qgemv_q4_0": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
     "qgemv_q6_k": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
+    "qgemv_q4_0_pair": (_I, [_P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _P]),
     "lmhead_q6_k_top1": (_I, [_P, _P, _L, _P, _P, _S, _I, _I, _I, _P]),
     "argmax_f32_rows": (_I, [_P, _L, _P, _P, _S, _I, _I, _P]),
     "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
@@ -168,6 +169,21 @@ def qgemv_q4_0(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
                y: torch.Tensor | None = None) -> torch.Tensor:
     """y [M, N] fp32 = Q4_0 weight (packed) x Q8_1 activation."""
     return _gemv("qgemv_q4_0", w_pack, xq, M, K, N, y)
+
+
+def qgemv_q4_0_pair(w_a: torch.Tensor, w_b: torch.Tensor, xq: torch.Tensor, M: int, K: int, N_a: int, N_b: int,
+                    y_a: torch.Tensor | None = None, y_b: torch.Tensor | None = None):
+    """(y_a, y_b) = (W_a x, W_b x) for two packed Q4_0 weights of the same K, in one launch."""
+    if y_a is None:
+        y_a = torch.empty((M, max(N_a, N_b)), dtype=torch.float32, device=xq.device)[:, :N_a]
+    if y_b is None:
+        y_b = torch.empty((M, y_a.stride(0)), dtype=torch.float32, device=xq.device)[:, :N_b]
+    assert y_a.dtype == torch.float32 and y_b.dtype == torch.float32 and y_a.stride(1) == 1 and y_b.stride(1) == 1
+    assert y_a.stride(0) == y_b.stride(0), "y_a and y_b share one row stride"
+    _check("qgemv_q4_0_pair", LIB.qgemv_q4_0_pair(_dev(w_a, "w_pack_a"), _dev(w_b, "w_pack_b"), _dev(xq, "xq"),
+                                                  _dev(y_a, "y_a"), _dev(y_b, "y_b"), y_a.stride(0), M, K, N_a,
+                                                  N_b, _stream(xq)))
+    return y_a, y_b
 
 
 def qgemv_q6_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,

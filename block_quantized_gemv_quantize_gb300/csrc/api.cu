@@ -112,6 +112,26 @@ int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
     return launch_mmvq_q4_0(a, M, as_stream(stream));
 }
 
+int qgemv_q4_0_pair(const void* w_pack_a, const void* w_pack_b, const void* xq, float* y_a, float* y_b, int64_t ldy,
+                    int M, int K, int N_a, int N_b, void* stream)
+{
+    int st = check_gemv(w_pack_a, xq, y_a, ldy, M, K, N_a, QK);
+    if (st) return st;
+    st = check_gemv(w_pack_b, xq, y_b, ldy, M, K, N_b, QK);
+    if (st) return st;
+    MmvqArgs a{};
+    a.w_pack = w_pack_a;
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.y = y_a;
+    a.ldy = ldy;
+    a.K = K;
+    a.N = N_a;
+    a.w_pack2 = w_pack_b;
+    a.y2 = y_b;
+    a.N2 = N_b;
+    return launch_mmvq_q4_0_pair(a, M, as_stream(stream));
+}
+
 int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
 {
     int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK_K);
@@ -181,7 +201,8 @@ int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int 
 int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;
-    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead();
+    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q6_k() +
+             take_wait_timeouts_lmhead();
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

@@ -85,19 +85,22 @@ inline int ring_parts(int64_t groups_per_cta, int nch, int max_warps, bool top1)
     return best_p;
 }
 
-template <int FMT, int M, bool TOP1>
-MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N)
+// N2 > 0: a second weight of N2 rows and the same K, whose row groups the
+// ring kernel takes after the first's.
+template <int FMT, int M, bool TOP1, bool PAIR = false>
+MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N, int N2 = 0)
 {
     const Layout L = make_layout(FMT, N, K);
     const int max_warps = MmvqThreads<FMT, M, TOP1>::value / 32;
     MmvqPlan p{};
-    p.grid = L.n_groups < di.sms ? (int)L.n_groups : di.sms;
-    const int64_t per_cta = (L.n_groups + p.grid - 1) / p.grid;  // groups
+    const int64_t n_groups = L.n_groups + (N2 > 0 ? ((int64_t)N2 + GROUP - 1) / GROUP : 0);
+    p.grid = n_groups < di.sms ? (int)n_groups : di.sms;
+    const int64_t per_cta = (n_groups + p.grid - 1) / p.grid;  // groups
     p.parts = ring_parts(per_cta, L.nch, max_warps, TOP1);
     const int64_t items = per_cta * p.parts;
     p.warps = items < max_warps ? (int)items : max_warps;
     const size_t act = RingAct<FMT, M>::bytes(L.NB);
-    const size_t extra = ring_extra_bytes<M, TOP1>((int)per_cta, p.parts, max_warps);
+    const size_t extra = ring_extra_bytes<M, TOP1, PAIR>((int)per_cta, p.parts, max_warps);
     const size_t stage = (size_t)L.chunk_bytes(GROUP, 0) + 8;  // a group-chunk and its mbarrier
     const size_t fixed = act + extra + 128;
     long long s = fixed < (size_t)di.smem_optin ? (long long)(((size_t)di.smem_optin - fixed) / (p.warps * stage)) : 0;
@@ -117,7 +120,7 @@ MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N)
         p.smem = (size_t)p.warps * p.stages * stage + act + extra;
         return p;
     }
-    p.ring = false;
+    p.ring = false;  // (the lock-step kernel takes one weight at a time)
     p.parts = 1;
     p.warps = max_warps;
     const int64_t n_items = (L.n_groups + p.warps - 1) / p.warps;
@@ -129,14 +132,14 @@ MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N)
     return p;
 }
 
-template <int FMT, int M, bool TOP1>
-int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
+template <int FMT, int M, bool TOP1, bool PAIR>
+int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
 {
     const DeviceInfo di = device_info();
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QGEMV_CUDA_ERROR;
-    const MmvqPlan p = mmvq_plan<FMT, M, TOP1>(di, a.K, a.N);
+    const MmvqPlan p = mmvq_plan<FMT, M, TOP1, PAIR>(di, a.K, a.N, PAIR ? a.N2 : 0);
     if (p.smem > (size_t)di.smem_optin) return QGEMV_UNSUPPORTED_SHAPE;
     a.KC = p.KC;
     a.stages = p.stages;
@@ -145,7 +148,7 @@ int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
     static bool opted_ring[64], opted_lock[64];
     static unsigned int* timeouts[64];
     if (p.ring) {
-        auto kern = mmvq_ring_kernel<FMT, M, TOP1>;
+        auto kern = mmvq_ring_kernel<FMT, M, TOP1, PAIR>;
         if (!opted_ring[dev]) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
                 return QGEMV_CUDA_ERROR;
@@ -163,8 +166,29 @@ int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
             opted_lock[dev] = true;
         }
         if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a) != cudaSuccess) return QGEMV_CUDA_ERROR;
+        if (PAIR) {  // the lock-step kernel takes the second weight in a launch of its own
+            MmvqArgs b = a;
+            b.w_pack = a.w_pack2;
+            b.y = a.y2;
+            b.N = a.N2;
+            b.w_pack2 = nullptr;
+            b.y2 = nullptr;
+            b.N2 = 0;
+            const MmvqPlan p2 = mmvq_plan<FMT, M, TOP1>(di, b.K, b.N);
+            b.KC = p2.KC;
+            if (launch_pdl(kern, dim3(p2.grid), dim3(p2.warps * 32), p2.smem, s, b) != cudaSuccess)
+                return QGEMV_CUDA_ERROR;
+        }
     }
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+// One weight (a.N2 == 0); the pair form is instantiated only for Q4_0 (the
+// gate/up projections), via launch_mmvq_pm<..., true> directly.
+template <int FMT, int M, bool TOP1>
+int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
+{
+    return launch_mmvq_pm<FMT, M, TOP1, false>(a, s);
 }
 
 // Reads and clears this translation unit's timeout counter (synchronous).
@@ -177,9 +201,11 @@ inline unsigned int take_wait_timeouts_tu()
 }
 
 int launch_mmvq_q4_0(const MmvqArgs& a, int M, cudaStream_t s);
+int launch_mmvq_q4_0_pair(const MmvqArgs& a, int M, cudaStream_t s);
 int launch_mmvq_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 unsigned int take_wait_timeouts_q4_0();
+unsigned int take_wait_timeouts_q4_0_pair();
 unsigned int take_wait_timeouts_q6_k();
 unsigned int take_wait_timeouts_lmhead();
 

@@ -418,6 +418,11 @@ struct MmvqArgs {
     float* y;
     int64_t ldy;
     int K, N;
+    // optional second weight of the same K against the same activation (a
+    // pair such as gate and up): its row groups follow the first's
+    const void* w_pack2;
+    float* y2;
+    int N2;
     int KC;      // activation blocks staged at once (lock-step kernel)
     int stages;  // ring stages per warp (ring kernel)
     int parts;   // K parts per row group (ring kernel)
@@ -512,7 +517,7 @@ inline size_t top1_scratch_bytes(int nwarps) { return (size_t)nwarps * 64 * 8 + 
 // ---------------------------------------------------------------------------
 // Ring kernel: the whole activation in shared memory, the weights streamed
 // through a private ring of S stages per warp, filled by TMA bulk copies.
-//   shared memory: copy streams [W] | rings [W][S][CB] | tile codes |
+//   shared memory: row space | copy streams [W] | rings [W][S][CB] | tile codes |
 //                  tile meta | mbarriers [W][S] | partial sums [groups][P][4 M]
 //                  (P > 1) | top-1 keys
 // The CTA owns row groups g0 .. g1-1 (4 rows each).  Each group's K is cut
@@ -591,20 +596,48 @@ struct alignas(16) RingStream {
 };
 static_assert(sizeof(RingStream) == 32, "RingStream is two 16-byte words");
 
-__device__ __forceinline__ void ring_stream_at(RingStream& k, const Layout& L, const uint8_t* base, int64_t g0,
-                                               int n_items, int P, uint32_t CB, uint32_t CBL, int64_t GB, int it)
+// The row groups a ring kernel covers: those of one packed weight, or of two
+// with the same K (the second's groups numbered after the first's), each
+// with its own output.
+// (Kernels of one weight do not use it: they read the kernel parameters.)
+struct alignas(16) RowSpace {
+    const uint8_t* w0;
+    const uint8_t* w1;
+    float* y0;
+    float* y1;
+    int64_t G0;  // groups of the first weight
+    int N0, N1;
+    __device__ __forceinline__ bool second(int64_t g) const { return g >= G0; }
+    __device__ __forceinline__ int rows(int64_t g) const
+    {
+        const int64_t r = !second(g) ? (int64_t)N0 - g * GROUP : (int64_t)N1 - (g - G0) * GROUP;
+        return r < GROUP ? (int)r : GROUP;
+    }
+    __device__ __forceinline__ const uint8_t* group_src(int64_t g, int64_t GB) const
+    {
+        return !second(g) ? w0 + g * GB : w1 + (g - G0) * GB;
+    }
+    __device__ __forceinline__ float* y_of(int64_t g) const { return !second(g) ? y0 : y1; }
+    __device__ __forceinline__ int64_t local(int64_t g) const { return !second(g) ? g : g - G0; }
+};
+
+// sp: the pair's row space, or null for one weight at `base`.
+template <bool PAIR>
+__device__ __forceinline__ void ring_stream_at(RingStream& k, const RowSpace* sp, const uint8_t* base, const Layout& L,
+                                               int64_t g0, int n_items, int P, uint32_t CB, uint32_t CBL, int64_t GB,
+                                               int it)
 {
     k.it = it;
     if (it >= n_items) return;
     const int q = P == 1 ? it : it / P;
     const int p = it - q * P;
     const int64_t g = g0 + q;
-    const int rows = L.rows_in(g);
+    const int rows = PAIR ? sp->rows(g) : L.rows_in(g);
     k.c = P == 1 ? 0 : p * L.nch / P;
     k.c1 = P == 1 ? L.nch : (p + 1) * L.nch / P;
     k.cbr = rows == GROUP ? CB : (uint32_t)L.chunk_bytes(rows, 0);
     k.cbl = rows == GROUP ? CBL : (uint32_t)L.chunk_bytes(rows, L.nch - 1);
-    k.src = base + g * GB + (int64_t)k.c * k.cbr;
+    k.src = (PAIR ? sp->group_src(g, GB) : base + g * GB) + (int64_t)k.c * k.cbr;
 }
 
 // Loads of one 4-row group's chunk from a ring stage.  whole: 4 rows and 32
@@ -720,7 +753,7 @@ __device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q6_K>& H, const ui
     }
 }
 
-template <int FMT, int M, bool TOP1>
+template <int FMT, int M, bool TOP1, bool PAIR>
 __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
 {
     constexpr int R = R_ROWS;
@@ -736,13 +769,29 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
     const uint32_t CB = (uint32_t)L.chunk_bytes(R, 0), CBL = (uint32_t)L.chunk_bytes(R, nch - 1);
     pdl_launch_dependents();
     const int64_t GB = L.group_bytes(R);
-    const int64_t g0 = (int64_t)blockIdx.x * L.n_groups / gridDim.x;
-    const int64_t g1 = (int64_t)(blockIdx.x + 1) * L.n_groups / gridDim.x;
+    // A pair's row space lives in shared memory (read where needed), so that
+    // it holds no registers in the main loop; one weight uses the kernel
+    // parameters themselves.
+    RowSpace* sp = PAIR ? reinterpret_cast<RowSpace*>(smem) : nullptr;
+    if (PAIR && threadIdx.x == 0) {
+        sp->w0 = static_cast<const uint8_t*>(a.w_pack);
+        sp->w1 = static_cast<const uint8_t*>(a.w_pack2);
+        sp->y0 = a.y;
+        sp->y1 = a.y2;
+        sp->G0 = L.n_groups;
+        sp->N0 = a.N;
+        sp->N1 = a.N2;
+    }
+    const uint8_t* wbase = static_cast<const uint8_t*>(a.w_pack);
+    const int64_t n_groups = L.n_groups + (PAIR ? ((int64_t)a.N2 + GROUP - 1) / GROUP : 0);
+    const int64_t g0 = (int64_t)blockIdx.x * n_groups / gridDim.x;
+    const int64_t g1 = (int64_t)(blockIdx.x + 1) * n_groups / gridDim.x;
     const int ng = (int)(g1 - g0);
     const int n_items = ng * P;
 
-    RingStream* streams = reinterpret_cast<RingStream*>(smem);  // [W], first: 16-byte aligned
-    uint8_t* rings = smem + (size_t)W * sizeof(RingStream);
+    constexpr size_t SP_BYTES = PAIR ? sizeof(RowSpace) : 0;
+    RingStream* streams = reinterpret_cast<RingStream*>(smem + SP_BYTES);  // [W], 16-byte aligned
+    uint8_t* rings = smem + SP_BYTES + (size_t)W * sizeof(RingStream);
     Act t;
     t.q = rings + (size_t)W * S * CB;
     t.meta = t.q + (size_t)NB * Act::QSTRIDE;
@@ -756,7 +805,6 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
 
     uint64_t* wbar = bars + warp * S;
     uint8_t* wring = rings + (size_t)warp * S * CB;
-    const uint8_t* wbase = static_cast<const uint8_t*>(a.w_pack);
     const uint64_t pol = l2_evict_first_policy();
 
     if (TOP1) {
@@ -768,16 +816,18 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
         for (int s = 0; s < S; ++s) mbar_init(&wbar[s], 1);
         fence_barrier_init();
     }
-    __syncwarp();
+    if (PAIR) __syncthreads();  // the row space is visible to every warp
+    else __syncwarp();
 
     // Lane 0's copy stream, kept in shared memory so that it holds no
     // registers in the main loop.
     RingStream& k = streams[warp];
-    if (lane == 0) ring_stream_at(k, L, wbase, g0, n_items, P, CB, CBL, GB, warp);
-    // The next item is usually the whole group W groups on (P = 1): its first
-    // chunk starts (W - 1) * GB past the end of the current group.
+    if (lane == 0) ring_stream_at<PAIR>(k, sp, wbase, L, g0, n_items, P, CB, CBL, GB, warp);
+    // The next item is usually the whole group W groups on (P = 1) of the
+    // same weight: its first chunk starts (W - 1) * GB past the end of the
+    // current group.
     const int64_t skip = (int64_t)(W - 1) * GB;
-    const int64_t last_whole = (a.N % GROUP) ? L.n_groups - 2 : L.n_groups - 1;  // last full group
+    const int64_t last_whole = (a.N % GROUP) ? L.n_groups - 2 : L.n_groups - 1;  // one weight: its last full group
     // Lane 0 takes the next job off its stream (bytes = 0: none left).
     auto next_job = [&](const uint8_t*& src) -> uint32_t {
         RingStream ks = k;  // one copy in, one copy out
@@ -787,12 +837,15 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
         ks.src += bytes;
         if (++ks.c == ks.c1) {
             const int nit = ks.it + W;
-            if (P == 1 && ks.cbr == CB && g0 + nit <= last_whole && nit < n_items) {
+            // next group whole and of the same weight
+            const bool next_whole = PAIR ? sp->rows(g0 + nit) == GROUP && sp->second(g0 + nit) == sp->second(g0 + ks.it)
+                                         : g0 + nit <= last_whole;
+            if (P == 1 && ks.cbr == CB && nit < n_items && next_whole) {
                 ks.src += skip;
                 ks.c = 0;
                 ks.it = nit;
             } else {
-                ring_stream_at(ks, L, wbase, g0, n_items, P, CB, CBL, GB, nit);
+                ring_stream_at<PAIR>(ks, sp, wbase, L, g0, n_items, P, CB, CBL, GB, nit);
             }
         }
         k = ks;
@@ -826,7 +879,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             const uint32_t bytes = pf.c == nch - 1 ? pf.cbl : pf.cbr;
             bulk_prefetch_l2(pf.src, bytes);
             pf.src += bytes;
-            if (++pf.c == pf.c1) ring_stream_at(pf, L, wbase, g0, n_items, P, CB, CBL, GB, pf.it + W);
+            if (++pf.c == pf.c1) ring_stream_at<PAIR>(pf, sp, wbase, L, g0, n_items, P, CB, CBL, GB, pf.it + W);
         }
     }
     pdl_wait();  // the previous kernel's writes (activation, weights, workspace) are visible from here
@@ -844,7 +897,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
     int gl = warp / P, p = warp - (warp / P) * P;
     for (int it = warp; it < n_items; it += W) {
         const int64_t g = g0 + gl;
-        const int rows = L.rows_in(g);
+        const int rows = PAIR ? sp->rows(g) : L.rows_in(g);
         float acc[R][M];
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -894,14 +947,14 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             }
             const int rr = vi / M, m = vi - rr * M;
             if (rr < rows) {
-                const int n = (int)(g * GROUP) + rr;
+                const int n = (int)((PAIR ? sp->local(g) : g) * GROUP) + rr;
                 if (TOP1) {
                     // the lane's running key for value vi (chunk j of the reduction)
                     unsigned long long& b = s_lane_best[j * blockDim.x + threadIdx.x];
                     const unsigned long long key = top1_key(v[j], n);
                     if (key > b) b = key;
                 } else {
-                    a.y[(int64_t)m * a.ldy + n] = v[j];
+                    (PAIR ? sp->y_of(g) : a.y)[(int64_t)m * a.ldy + n] = v[j];
                 }
             }
         }
@@ -928,10 +981,11 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             float sum = pp[0];
             for (int j = 1; j < P; ++j) sum += pp[(size_t)j * V];
             const int rr = vi / M, m = vi - rr * M;
-            const int64_t n = (g0 + q) * GROUP + rr;
-            if (n < a.N) {
+            const int64_t g = g0 + q;
+            if (rr < (PAIR ? sp->rows(g) : L.rows_in(g))) {
+                const int64_t n = (PAIR ? sp->local(g) : g) * GROUP + rr;
                 if (TOP1) atomicMax(&s_best[m], top1_key(sum, (int)n));
-                else a.y[(int64_t)m * a.ldy + n] = sum;
+                else (PAIR ? sp->y_of(g) : a.y)[(int64_t)m * a.ldy + n] = sum;
             }
         }
     }
@@ -965,10 +1019,10 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
 
 // Shared memory of the ring kernel besides the rings, their mbarriers and
 // the tile.
-template <int M, bool TOP1>
+template <int M, bool TOP1, bool PAIR>
 inline size_t ring_extra_bytes(int max_groups_per_cta, int P, int warps)
 {
-    const size_t streams = (size_t)warps * sizeof(RingStream);
+    const size_t streams = (PAIR ? sizeof(RowSpace) : 0) + (size_t)warps * sizeof(RingStream);
     const size_t part = P > 1 ? (size_t)max_groups_per_cta * P * R_ROWS * M * sizeof(float) : 0;
     const size_t nred = (R_ROWS * M + 31) / 32;
     return streams + part + (TOP1 ? (size_t)(MAX_M + 2) * 8 + nred * warps * 32 * 8 : 0);

@@ -128,6 +128,19 @@ int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
  *   1 <= M <= 17, K % 256 == 0, N >= 1. */
 int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
 
+/* qgemv_q4_0_pair - qgemv_q4_0 of two weights with the same K against one
+ * Q8_1 activation in a single launch (the verifier MLP's gate and up):
+ * y_a = W_a x, y_b = W_b x, each exactly as qgemv_q4_0 would compute it.
+ * [record] "Strict run identity" (joint gate/up enabled) and [closure] "What
+ * materially worked" item 3 (packed width-6 gate/up projections); one launch
+ * pays the activation staging, the launch and the tail once for both.
+ *   w_pack_a, w_pack_b  packed Q4_0 of N_a and N_b rows of K values (read)
+ *   xq                  Q8_1 [M][K/32][36] (read)
+ *   y_a, y_b            fp32 [M][ldy] (written), ldy >= max(N_a, N_b)
+ *   1 <= M <= 17, K % 32 == 0, N_a >= 1, N_b >= 1. */
+int qgemv_q4_0_pair(const void* w_pack_a, const void* w_pack_b, const void* xq, float* y_a, float* y_b, int64_t ldy,
+                    int M, int K, int N_a, int N_b, void* stream);
+
 /* ---- A5: fused LM-head top-1 -------------------------------------------- */
 
 /* lmhead_q6_k_top1 - for each of M fp32 rows of x: quantize to Q8_1, project

@@ -5,6 +5,8 @@ Gates: Q8_1 and the int32 block dots bit-exact; fp32 outputs within
 where the oracle's top-2 gap exceeds 1e-4 * |top1| (otherwise any id within
 that tolerance), planted exact ties resolved to the lower id; argmax over the
 GPU's own fp32 logits bit-exact."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -123,6 +125,41 @@ def test_qgemv_q6_k_matches_oracle(ops, M, K, N):
     y, y_ref, S = _gemv_case(ops, "q6_k", M, K, N, seed=10 * M + K + 7)
     r = C.check_close(y, y_ref, S)
     assert r["ok"], r
+
+
+@pytest.mark.parametrize("M,K,Na,Nb", [(1, 256, 512, 512), (6, 512, 37, 64), (6, 1024, 4096, 130),
+                                       (17, 256, 9, 11), (3, 3072, 1, 5), (6, 5120, 1536, 1539),
+                                       (2, 17408, 64, 63)])
+def test_qgemv_q4_0_pair_matches_oracle(ops, M, K, Na, Nb):
+    # two weights of the same K against one activation in one launch (their
+    # row groups are dealt out as one range): each output as its own qgemv
+    x = synth.activations(M, K, seed=M + K, outlier_frac=0.01)
+    xq_ref = oracle.quantize_q8_1(x)
+    xq = ops.quantize_q8_1(_t(x))
+    wa = synth.q4_0_weights(Na, K, seed=Na + 3)
+    wb = synth.q4_0_weights(Nb, K, seed=Nb + 4)
+    ya, yb = ops.qgemv_q4_0_pair(ops.qpack_q4_0(_t(wa), Na, K), ops.qpack_q4_0(_t(wb), Nb, K), xq, M, K, Na, Nb)
+    for y, w in ((ya, wa), (yb, wb)):
+        y_ref, S = oracle.qgemv_q4_0(w, xq_ref)
+        r = C.check_close(_np(y), y_ref, S)
+        assert r["ok"], r
+
+
+def test_qgemv_q4_0_pair_padding_untouched_and_errors(ops):
+    M, K, Na, Nb, ldy = 6, 512, 70, 33, 80
+    x = synth.activations(M, K, seed=8)
+    xq = ops.quantize_q8_1(_t(x))
+    wa = ops.qpack_q4_0(_t(synth.q4_0_weights(Na, K, seed=1)), Na, K)
+    wb = ops.qpack_q4_0(_t(synth.q4_0_weights(Nb, K, seed=2)), Nb, K)
+    ya = torch.full((M, ldy), 3.0, device=DEV)
+    yb = torch.full((M, ldy), 5.0, device=DEV)
+    ops.qgemv_q4_0_pair(wa, wb, xq, M, K, Na, Nb, y_a=ya[:, :Na], y_b=yb[:, :Nb])
+    assert np.all(_np(ya)[:, Na:] == 3.0) and np.all(_np(yb)[:, Nb:] == 5.0)
+    L = ops.LIB
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    assert L.qgemv_q4_0_pair(p(wa), None, p(xq), p(ya), p(yb), ldy, M, K, Na, Nb, None) == -1
+    assert L.qgemv_q4_0_pair(p(wa), p(wb), p(xq), p(ya), p(yb), 50, M, K, Na, Nb, None) == -1  # ldy < N_a
+    assert L.qgemv_q4_0_pair(p(wa), p(wb), p(xq), p(ya), p(yb), ldy, 18, K, Na, Nb, None) == -2
 
 
 def test_qgemv_output_stride_and_untouched_padding(ops):

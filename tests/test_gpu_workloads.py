@@ -74,6 +74,23 @@ def vocab(ops):
     return dict(w=w, x6=x6, wd=wd, wp=wp, y_ref=y_ref, S=S)
 
 
+def test_verifier_gate_up_pair_full(ops):
+    # gate and up in one launch, as the benchmark runs them
+    c = synth.WORKLOADS["verifier_gate_up"]
+    M, K, N = c["M"], c["K"], c["N"]
+    wg = synth.q4_0_weights(N, K, seed=c["seed"])
+    wu = synth.q4_0_weights(N, K, seed=c["seed"] + 1)
+    x = synth.activations(M, K, seed=c["seed"] + 100, outlier_frac=c["outlier_frac"])
+    xq_ref = oracle.quantize_q8_1(x)
+    yg, yu = ops.qgemv_q4_0_pair(ops.qpack_q4_0(_t(wg), N, K), ops.qpack_q4_0(_t(wu), N, K),
+                                 ops.quantize_q8_1(_t(x)), M, K, N, N)
+    for y, w in ((yg, wg), (yu, wu)):
+        y_ref, S = oracle.qgemv_q4_0(w, xq_ref)
+        r = C.check_close(_np(y), y_ref, S)
+        print("pair", r)
+        assert r["ok"], r
+
+
 def test_lmhead_top1_full(ops, vocab):
     x6d = _t(vocab["x6"])
     ids = _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V))
