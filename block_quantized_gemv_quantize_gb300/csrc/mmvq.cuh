@@ -306,28 +306,44 @@ __device__ __forceinline__ void ring_meta_store(uint8_t* p, float da, int s_lo, 
     }
 }
 
-// From caller-supplied Q8_1 blocks in global memory (one thread per block).
+// From caller-supplied Q8_1 blocks in global memory: each thread takes U
+// blocks per round and issues all their loads before using any, so a round
+// costs one L2 round trip.  U = 4 for the short Q4_0 calls, whose staging is
+// a visible part of the call (the down projection stages 3264 blocks); the
+// Q6_K heads keep U = 1, which leaves their main loop's registers alone.
 template <int FMT, int M>
 __device__ __forceinline__ void ring_act_from_q8_1(const RingAct<FMT, M>& t, const uint8_t* xq, int NB)
 {
     using A = RingAct<FMT, M>;
-    for (int i = threadIdx.x; i < M * NB; i += blockDim.x) {
-        const int m = i / NB, b = i - m * NB;
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES);
-        uint32_t q[8];
-        const uint32_t ds = w[0];
+    constexpr int U = FMT == FMT_Q4_0 ? 4 : 1;
+    const int total = M * NB;
+    for (int i0 = threadIdx.x; i0 < total; i0 += U * blockDim.x) {
+        uint32_t w[U][9];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = w[1 + k];
-        uint4* dst = reinterpret_cast<uint4*>(t.q + b * A::QSTRIDE + 32 * m);
-        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        int s0 = 0, s1 = 0;
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i < total) {
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + (int64_t)i * Q8_1_BYTES);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) s0 = __dp4a((int)q[k], 0x01010101, s0);
+                for (int k = 0; k < 9; ++k) w[u][k] = src[k];
+            }
+        }
 #pragma unroll
-        for (int k = 4; k < 8; ++k) s1 = __dp4a((int)q[k], 0x01010101, s1);
-        const float da = __half2float(__ushort_as_half((unsigned short)(ds & 0xFFFFu)));
-        ring_meta_store<FMT>(t.meta + (b * A::MROWS + m) * A::META, da, s0, s1);
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i >= total) break;
+            const int m = i / NB, b = i - m * NB;
+            uint4* dst = reinterpret_cast<uint4*>(t.q + b * A::QSTRIDE + 32 * m);
+            dst[0] = make_uint4(w[u][1], w[u][2], w[u][3], w[u][4]);
+            dst[1] = make_uint4(w[u][5], w[u][6], w[u][7], w[u][8]);
+            int s0 = 0, s1 = 0;
+#pragma unroll
+            for (int k = 1; k < 5; ++k) s0 = __dp4a((int)w[u][k], 0x01010101, s0);
+#pragma unroll
+            for (int k = 5; k < 9; ++k) s1 = __dp4a((int)w[u][k], 0x01010101, s1);
+            const float da = __half2float(__ushort_as_half((unsigned short)(w[u][0] & 0xFFFFu)));
+            ring_meta_store<FMT>(t.meta + (b * A::MROWS + m) * A::META, da, s0, s1);
+        }
     }
 }
 
@@ -896,6 +912,19 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
     const int step_g = W / P, step_p = W - (W / P) * P;
     int gl = warp / P, p = warp - (warp / P) * P;
     for (int it = warp; it < n_items; it += W) {
+        if (FMT == FMT_Q4_0 && lane == 0 && it + 2 * W < n_items) {
+            // keep the short Q4_0 rings fed from L2: prefetch this warp's
+            // item after next (its chunks are one contiguous region) while
+            // this one is worked on
+            const int ia = it + 2 * W;
+            const int qa = P == 1 ? ia : ia / P, pa = ia - qa * P;
+            const int64_t ga = g0 + qa;
+            if (PAIR ? sp->rows(ga) == GROUP : ga <= last_whole) {
+                const int ca = P == 1 ? 0 : pa * nch / P, cb = P == 1 ? nch : (pa + 1) * nch / P;
+                const uint32_t span = (uint32_t)(cb - ca) * CB - (cb == nch ? CB - CBL : 0u);
+                bulk_prefetch_l2((PAIR ? sp->group_src(ga, GB) : wbase + ga * GB) + (int64_t)ca * CB, span);
+            }
+        }
         const int64_t g = g0 + gl;
         const int rows = PAIR ? sp->rows(g) : L.rows_in(g);
         float acc[R][M];
