@@ -887,6 +887,28 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
         ++issued;
         if (++iss_slot == S) iss_slot = 0;
     };
+    // Common case (one weight, P = 1, all groups whole, S <= nch): the copy
+    // S - 1 jobs ahead of job (item it, chunk c) follows from it and c alone,
+    // which every lane knows, so no stream state is read or written.
+    const bool direct = !PAIR && P == 1 && (a.N % GROUP) == 0 && S <= nch;
+    auto issue_direct = [&](int it, int c) {
+        int ci = c + S - 1, iti = it;
+        if (ci >= nch) {
+            ci -= nch;
+            iti += W;
+        }
+        if (iti >= n_items) return;
+        const uint32_t bytes = ci == nch - 1 ? CBL : CB;
+        const uint8_t* src = wbase + (g0 + iti) * GB + (int64_t)ci * CB;
+        uint64_t* bar = wbar + iss_slot;
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(wring + (size_t)iss_slot * CB, src, bytes, bar, pol_u);
+        }
+        ++issued;
+        if (++iss_slot == S) iss_slot = 0;
+    };
     if (lane == 0) {
         // Start HBM on the first jobs (L2 prefetch) while the previous kernel
         // of the stream drains and the activation is staged.
@@ -934,7 +956,8 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             for (int m = 0; m < M; ++m) acc[r][m] = 0.0f;
         const int c0 = P == 1 ? 0 : p * nch / P, c1 = P == 1 ? nch : (p + 1) * nch / P;
         for (int c = c0; c < c1; ++c) {
-            issue_next();
+            if (direct) issue_direct(it, c);
+            else issue_next();
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wbar[slot], phase))) {
                 if (lane == 0) atomicAdd(timeouts, 1u);
                 alive = false;
