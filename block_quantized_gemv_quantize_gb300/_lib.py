@@ -37,6 +37,7 @@ SIGNATURES = {
     "qgemv_q6_k": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
     "qgemv_q4_0_pair": (_I, [_P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _P]),
     "lmhead_q6_k_top1": (_I, [_P, _P, _L, _P, _P, _S, _I, _I, _I, _P]),
+    "lmhead_q6_k_candmax": (_I, [_P, _P, _L, _P, _P, _P, _P, _P, _S, _I, _I, _I, _P]),
     "argmax_f32_rows": (_I, [_P, _L, _P, _P, _S, _I, _I, _P]),
     "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
@@ -206,6 +207,26 @@ def lmhead_q6_k_top1(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, ids:
                                                     _dev(ids, "ids"), _dev(ws, "workspace"), ws.numel(),
                                                     M, K, N, _stream(x)))
     return ids
+
+
+def lmhead_q6_k_candmax(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, cand: torch.Tensor,
+                        ws: torch.Tensor | None = None):
+    """(ids, top_vals, cand_vals): the greedy id of each row of fp32 x, its
+    logit, and the logit of the row's candidate id cand[m] (int32 [M])."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    assert cand.dtype == torch.int32 and cand.numel() == x.shape[0]
+    M = x.shape[0]
+    ids = torch.empty(M, dtype=torch.int32, device=x.device)
+    top_vals = torch.empty(M, dtype=torch.float32, device=x.device)
+    cand_vals = torch.empty(M, dtype=torch.float32, device=x.device)
+    nb = lmhead_q6_k_top1_workspace_bytes(M, K, N)
+    if ws is None:
+        ws = workspace(x.device, nb)
+    _check("lmhead_q6_k_candmax", LIB.lmhead_q6_k_candmax(_dev(w_pack, "w_pack"), _dev(x, "x"), x.stride(0),
+                                                          _dev(cand, "cand"), _dev(ids, "ids"),
+                                                          _dev(top_vals, "top_vals"), _dev(cand_vals, "cand_vals"),
+                                                          _dev(ws, "workspace"), ws.numel(), M, K, N, _stream(x)))
+    return ids, top_vals, cand_vals
 
 
 def lmhead_q6_k_top1_noalloc(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int,

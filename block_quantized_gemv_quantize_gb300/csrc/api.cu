@@ -173,6 +173,39 @@ int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* i
     return launch_lmhead_q6_k(a, M, s);
 }
 
+int lmhead_q6_k_candmax(const void* w_pack, const float* x, int64_t ldx, const int32_t* cand, int32_t* ids,
+                        float* top_vals, float* cand_vals, void* workspace, size_t ws_bytes, int M, int K, int N,
+                        void* stream)
+{
+    if (!w_pack || !x || !cand || !ids || !top_vals || !cand_vals || !workspace) return QGEMV_INVALID_ARG;
+    int st = check_mk(M, K, QK_K);
+    if (st) return st;
+    if (N < 1 || ldx < K) return QGEMV_INVALID_ARG;
+    if (ws_bytes < lmhead_ws_bytes(M, K)) return QGEMV_WORKSPACE_TOO_SMALL;
+    if (!aligned16(w_pack) || !aligned16(x) || !aligned16(cand) || !aligned16(ids) || !aligned16(top_vals) ||
+        !aligned16(cand_vals) || !aligned16(workspace))
+        return QGEMV_MISALIGNED;
+    cudaStream_t s = as_stream(stream);
+    // a candidate outside 0 .. N-1 keeps this NaN (all-ones bits)
+    if (cudaMemsetAsync(cand_vals, 0xFF, (size_t)M * sizeof(float), s) != cudaSuccess) return QGEMV_CUDA_ERROR;
+    uint8_t* xq = static_cast<uint8_t*>(workspace) + LMHEAD_Q8_OFFSET;
+    st = launch_quantize_q8_1(x, ldx, xq, M, K, s);
+    if (st != QGEMV_OK) return st;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.x = x;
+    a.ldx = ldx;
+    a.xq = xq;
+    a.K = K;
+    a.N = N;
+    a.ws = static_cast<Top1Workspace*>(workspace);
+    a.ids = ids;
+    a.top_vals = top_vals;
+    a.cand = cand;
+    a.cand_vals = cand_vals;
+    return launch_lmhead_q6_k(a, M, s);
+}
+
 int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, size_t ws_bytes, int M, int N,
                     void* stream)
 {

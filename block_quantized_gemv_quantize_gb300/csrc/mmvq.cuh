@@ -444,6 +444,11 @@ struct MmvqArgs {
     int parts;   // K parts per row group (ring kernel)
     Top1Workspace* ws;
     int32_t* ids;
+    // candidate-max (top-1 kernels, all optional): the top value of each row,
+    // and the logit of a given candidate id per row
+    float* top_vals;
+    const int32_t* cand;
+    float* cand_vals;
 };
 
 // Reduce one row group's partial sums over the warp and write them (TOP1 =
@@ -479,6 +484,7 @@ __device__ __forceinline__ void finish_rowgroup(const MmvqArgs& a, int n0, float
                 if (vi < V) {
                     const int n = n0 + vi / M;
                     wk[vi] = n < a.N ? top1_key(v[j], n) : 0ull;
+                    if (a.cand_vals && n < a.N && n == a.cand[vi % M]) a.cand_vals[vi % M] = v[j];
                 }
             }
         }
@@ -522,6 +528,7 @@ __device__ __forceinline__ void top1_finish(const MmvqArgs& a, unsigned long lon
         if (threadIdx.x < M) {
             const unsigned long long k = atomicExch(&a.ws->keys[threadIdx.x], 0ull);
             a.ids[threadIdx.x] = top1_key_to_id(k);
+            if (a.top_vals) a.top_vals[threadIdx.x] = top1_key_to_value(k);
         }
         if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
     }
@@ -1005,6 +1012,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
                     unsigned long long& b = s_lane_best[j * blockDim.x + threadIdx.x];
                     const unsigned long long key = top1_key(v[j], n);
                     if (key > b) b = key;
+                    if (a.cand_vals && n == a.cand[m]) a.cand_vals[m] = v[j];
                 } else {
                     (PAIR ? sp->y_of(g) : a.y)[(int64_t)m * a.ldy + n] = v[j];
                 }
@@ -1063,6 +1071,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             if (threadIdx.x < M) {
                 const unsigned long long key = atomicExch(&a.ws->keys[threadIdx.x], 0ull);
                 a.ids[threadIdx.x] = top1_key_to_id(key);
+                if (a.top_vals) a.top_vals[threadIdx.x] = top1_key_to_value(key);
             }
             if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
         }

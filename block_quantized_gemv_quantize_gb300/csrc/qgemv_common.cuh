@@ -432,6 +432,15 @@ __host__ __device__ inline int top1_key_to_id(unsigned long long k)
     return k == 0ull ? 0 : (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
 }
 
+// The fp32 value a top-1 key was made from (+0 for a zero; NaN for key 0,
+// i.e. a row that held only NaN).
+__device__ __forceinline__ float top1_key_to_value(unsigned long long k)
+{
+    if (k == 0ull) return __int_as_float(0x7fffffff);
+    const uint32_t ord = (uint32_t)(k >> 32);
+    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 {
 #pragma unroll

@@ -9,6 +9,7 @@
  *   [closure]  "Qwen3.6 27B Q4_0 DFlash/SYCL closure"
  *   [record]   "Q6_K M=6 fused DFlash top-1 production record"
  *   [q8cache]  "Qwen3.6 27B B70 follow-up: Q8 activation cache..."
+ *   [handoff]  "Qwen3.6 27B AutoRound Handoff"
  *
  * Block formats (named on the pages, defined here as in llama.cpp):
  *   Q8_1  32 activations: fp16 d, fp16 s = d * sum(q), int8 q[32]      36 B
@@ -163,6 +164,28 @@ int qgemv_q4_0_pair(const void* w_pack_a, const void* w_pack_b, const void* xq, 
  *   1 <= M <= 17, K % 256 == 0, N >= 1. */
 int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* ids, void* workspace,
                      size_t ws_bytes, int M, int K, int N, void* stream);
+
+/* lmhead_q6_k_candmax - the verifier's candidate-max over the same fused
+ * LM-head: for each row m, the greedy id (ids[m], the lmhead_q6_k_top1
+ * contract), its logit top_vals[m], and the logit of a given candidate id
+ * cand[m] (a drafted token) in cand_vals[m].  No logits are written.
+ * [handoff] "Current next-execution plan", the candidate-max precheck: a
+ * target-verified speculation step needs each row's greedy id and value and
+ * the score of the drafted candidate, not the logits.
+ *   w_pack, x, ldx, workspace, ws_bytes, M, K, N  as lmhead_q6_k_top1
+ *   cand       int32 [M] (read): the candidate id of each row; one outside
+ *              0 .. N-1 gives cand_vals[m] = NaN
+ *   ids        int32 [M] (written)
+ *   top_vals   fp32 [M] (written): the greedy id's logit (NaN for a row of
+ *              only NaN logits)
+ *   cand_vals  fp32 [M] (written): the candidate's logit; equal, bit for
+ *              bit, to top_vals[m] when cand[m] == ids[m]
+ *   Both are the fused kernel's fp32 sums, within the library's fp32
+ *   tolerance of the oracle's logits (and of qgemv_q6_k's, which may split K
+ *   differently for small shapes). */
+int lmhead_q6_k_candmax(const void* w_pack, const float* x, int64_t ldx, const int32_t* cand, int32_t* ids,
+                        float* top_vals, float* cand_vals, void* workspace, size_t ws_bytes, int M, int K, int N,
+                        void* stream);
 
 /* ---- A6: row argmax (the unfused control) -------------------------------- */
 

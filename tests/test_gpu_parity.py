@@ -185,6 +185,42 @@ def test_chunked_k_matches_single_chunk(ops):
     assert C.check_close(y6, y6_ref, S6)["ok"]
 
 
+# ---------------------------------------------------------------- dependent launches
+
+def test_dependent_chain_without_host_sync(ops):
+    # Every kernel of the library starts while the previous one drains and
+    # waits for it before touching its inputs (programmatic dependent
+    # launch).  Chain calls whose inputs are the previous calls' outputs, with
+    # no host synchronization in between, then check every link against the
+    # oracle applied to the GPU's own previous output.
+    M, K, N = 6, 1024, 1024
+    w = synth.q4_0_weights(N, K, seed=31)
+    wp = ops.qpack_q4_0(_t(w), N, K)
+    wv = synth.q6_k_weights(3000, K, seed=32)
+    wvp = ops.qpack_q6_k(_t(wv), 3000, K)
+    x0 = synth.activations(M, K, seed=33)
+    ys = [torch.empty((M, N), device=DEV) for _ in range(4)]
+    xqs = [torch.empty(ops.q8_1_bytes(M, K), dtype=torch.uint8, device=DEV) for _ in range(4)]
+    ids = [torch.empty(M, dtype=torch.int32, device=DEV) for _ in range(4)]
+    cur = _t(x0)
+    for i in range(4):
+        ops.quantize_q8_1(cur, out=xqs[i])
+        ops.qgemv_q4_0(wp, xqs[i], M, K, N, y=ys[i])
+        ops.lmhead_q6_k_top1(wvp, ys[i], K, 3000, ids=ids[i])  # reads the GEMV output directly
+        cur = ys[i]
+    torch.cuda.synchronize()
+    prev = x0
+    for i in range(4):
+        xq_ref = oracle.quantize_q8_1(prev)
+        assert np.array_equal(_np(xqs[i]).reshape(xq_ref.shape), xq_ref), i
+        y_ref, S = oracle.qgemv_q4_0(w, xq_ref)
+        yi = _np(ys[i])
+        assert C.check_close(yi, y_ref, S)["ok"], i
+        ids_ref, y6, S6 = oracle.lmhead_q6_k_top1(wv, yi)
+        assert C.check_top1(_np(ids[i]), y6) == [], i
+        prev = yi
+
+
 # ---------------------------------------------------------------- position independence, determinism
 
 def test_duplicated_and_permuted_rows_bit_identical(ops):
@@ -240,6 +276,38 @@ def test_lmhead_small_matches_oracle_and_unfused(ops, M, K, N):
     assert C.check_top1(ids, y_ref) == []
     y = ops.qgemv_q6_k(wp, ops.quantize_q8_1(xd), M, K, N)
     assert _np(ops.argmax_f32_rows(y)).tolist() == ids.tolist()
+
+
+@pytest.mark.parametrize("M,K,N", [(5, 1024, 3001), (6, 2048, 777), (1, 256, 64), (17, 512, 1025)])
+def test_lmhead_candmax_matches_oracle_and_logits(ops, M, K, N):
+    # greedy id and value of each row plus the logit of a candidate id, within
+    # the fp32 gate of the oracle's logits (qgemv_q6_k may split K differently
+    # at these small shapes, so it is not compared bit for bit here)
+    w = synth.q6_k_weights(N, K, seed=M + N + 1)
+    x = synth.activations(M, K, seed=K + 1)
+    ids_ref, y_ref, S = oracle.lmhead_q6_k_top1(w, x)
+    wp = ops.qpack_q6_k(_t(w), N, K)
+    xd = _t(x)
+    rng = np.random.default_rng(M * N)
+    cand = rng.integers(0, N, size=M).astype(np.int32)
+    cand[0] = ids_ref[0]                  # the greedy token itself
+    if M > 1:
+        cand[1] = N + 5                   # out of range -> NaN
+    if M > 2:
+        cand[2] = N - 1                   # last row, possibly in a partial group
+    ids, top_vals, cand_vals = (_np(t) for t in ops.lmhead_q6_k_candmax(wp, xd, K, N, _t(cand)))
+    assert C.check_top1(ids, y_ref) == []
+
+    def close(v, m, n):
+        return abs(float(v) - y_ref[m, n]) <= 1e-5 * max(abs(y_ref[m, n]), S[m, n])
+
+    for m in range(M):
+        assert close(top_vals[m], m, ids[m]), m
+        if 0 <= cand[m] < N:
+            assert close(cand_vals[m], m, cand[m]), m
+        else:
+            assert np.isnan(cand_vals[m]), m
+    assert cand_vals[0] == top_vals[0]  # the same sum, bit for bit
 
 
 # ---------------------------------------------------------------- errors

@@ -105,6 +105,24 @@ def test_lmhead_top1_full(ops, vocab):
     assert _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V)).tolist() == ids.tolist()
 
 
+def test_lmhead_candmax_full(ops, vocab):
+    # rows 1..5 at the full vocabulary: greedy ids and values, and candidate
+    # logits equal to the unfused logits (both kernels take K whole here)
+    x6d = _t(vocab["x6"])
+    y_ref = vocab["y_ref"]
+    ids_ref = y_ref.argmax(axis=1)
+    cand = np.array([ids_ref[0], 0, N_V - 1, 123456, ids_ref[4]], dtype=np.int32)
+    ids, top_vals, cand_vals = (_np(t) for t in ops.lmhead_q6_k_candmax(vocab["wp"], x6d[1:6], K_H, N_V, _t(cand)))
+    assert C.check_top1(ids, y_ref) == []
+    y = _np(ops.qgemv_q6_k(vocab["wp"], ops.quantize_q8_1(x6d[1:6]), 5, K_H, N_V))
+    S = vocab["S"]
+    for m in range(5):
+        assert top_vals[m] == y[m, ids[m]]
+        assert cand_vals[m] == y[m, cand[m]]
+        assert abs(float(cand_vals[m]) - y_ref[m, cand[m]]) <= 1e-5 * max(abs(y_ref[m, cand[m]]), S[m, cand[m]])
+    assert cand_vals[0] == top_vals[0] and cand_vals[4] == top_vals[4]
+
+
 def _sample_rows(N, seed=0):
     g = np.random.default_rng(seed)
     return np.unique(np.concatenate([np.arange(min(64, N)), np.arange(max(0, N - 64), N),
