@@ -157,6 +157,29 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- ranks
+
+
+def max_over_ranks(ms: float, world: int) -> float:
+    """The slowest rank's time: every rank of a replicas run ends its timed
+    region at a barrier, and the job is as fast as its slowest replica."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job effective GB/s: the bytes every replica streams per step,
+    over the (slowest rank's) step time."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- native arm
 
 
@@ -242,11 +265,7 @@ def run_native(args, rank, world):
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_per_step = total_ms / args.steps
 
     # per-call breakdown: a second timed region with an event pair around every call
@@ -262,7 +281,7 @@ def run_native(args, rank, world):
 
     nbytes = step_bytes()
     step_total = sum(nbytes.values())
-    value = world * step_total / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(world, step_total, ms_per_step)
 
     # e2e: the same step through the public API with host buffers: per step the
     # activations are copied in from pinned host memory and the results
@@ -293,12 +312,8 @@ def run_native(args, rank, world):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_total / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    e2e_value = job_gbs(world, step_total, e2e_ms)
 
     # fused vs unfused LM-head on identical inputs (rows 1..5), interleaved A/B
     y5 = torch.empty((5, N_V), device=dev)
@@ -313,9 +328,14 @@ def run_native(args, rank, world):
         ops.qgemv_q6_k(w["w_vocab"], xq5, 5, K_H, N_V, y=y5)
         ops.argmax_f32_rows(y5, ids=ids_u, ws=ws2)
 
-    ab = {"fused": [], "unfused": []}
+    cand = ids_d.clone()  # the verifier's candidate-max on the same rows, candidates = the draft's ids
+
+    def candmax():
+        ops.lmhead_q6_k_candmax(w["w_vocab"], xd_rows, K_H, N_V, cand, ws=ws1)
+
+    ab = {"fused": [], "unfused": [], "candmax": []}
     for _ in range(5):
-        for name, fn in (("fused", fused), ("unfused", unfused)):
+        for name, fn in (("fused", fused), ("unfused", unfused), ("candmax", candmax)):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for _ in range(10):
@@ -358,6 +378,7 @@ def run_native(args, rank, world):
             "fused_vs_unfused_us": {"fused": round(statistics.median(ab["fused"]), 2),
                                     "unfused": round(statistics.median(ab["unfused"]), 2),
                                     "same_ids": same_ids},
+            "candmax_us": round(statistics.median(ab["candmax"]), 2),
             "per_call_us": {n: round(call_ms[n] * 1e3, 2) for n in names},
             "per_call_gbs": {n: round(nbytes[n] / (call_ms[n] * 1e-3) / 1e9, 1) for n in names},
             "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
