@@ -58,6 +58,9 @@ def parse():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded oracle sample length")
+    p.add_argument("--sweep", action="store_true",
+                   help="instead of the step: time qgemv_q4_0/qgemv_q6_k over M in {1,2,4,6,9,12,17}, "
+                        "K=5120, N in {5120, 17408, 248320} (one JSON line per shape)")
     return p.parse_args()
 
 
@@ -415,6 +418,57 @@ def load_traffic(kernel: str):
     return d.get("per_launch_dram_bytes", {}).get(kernel)
 
 
+# ---------------------------------------------------------------- M sweep
+
+
+def run_sweep(args):
+    """Per-call time and effective GB/s of the MMVQ over the M sweep, each
+    call timed alone (CUDA events) right after an L2 flush that is not timed,
+    on random packed weights (timing does not depend on the bytes)."""
+    import torch
+
+    from block_quantized_gemv_quantize_gb300 import build
+
+    build.build()
+    from block_quantized_gemv_quantize_gb300 import ops
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device="cpu").manual_seed(0)
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)  # twice the L2
+    reps = max(3, min(args.steps, 20))
+    peak, _ = peaks()
+    for fmt in ("q4_0", "q6_k"):
+        for N in (5120, 17408, 248320):
+            nbytes_w = (ops.q4_0_pack_bytes if fmt == "q4_0" else ops.q6_k_pack_bytes)(N, K_H)
+            w = torch.randint(0, 256, (nbytes_w,), dtype=torch.uint8, generator=g).to(dev)
+            for M in (1, 2, 4, 6, 9, 12, 17):
+                x = torch.randn(M, K_H, generator=g).to(dev)
+                xq = ops.quantize_q8_1(x)
+                y = torch.empty((M, N), device=dev)
+                call = (lambda: ops.qgemv_q4_0(w, xq, M, K_H, N, y=y)) if fmt == "q4_0" else \
+                    (lambda: ops.qgemv_q6_k(w, xq, M, K_H, N, y=y))
+                for _ in range(3):
+                    call()
+                ts = []
+                for _ in range(reps):
+                    flush.fill_(1)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    call()
+                    b.record()
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b))
+                us = statistics.median(ts) * 1e3
+                nbytes = nbytes_w + ops.q8_1_bytes(M, K_H)
+                gbs = nbytes / (us * 1e-6) / 1e9
+                print(json.dumps({"sweep": fmt, "M": M, "K": K_H, "N": N, "us": round(us, 2),
+                                  "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+                                  "l2": "flushed before every call"}), flush=True)
+            del w
+            torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 
@@ -507,6 +561,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
         return
     if world > 1:
         import torch.distributed as dist
