@@ -42,6 +42,8 @@ SIGNATURES = {
     "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
+    "qgemv_set_q4_0_tensor_cores": (_I, [_I]),
+    "qgemv_q4_0_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "lmhead_q6_k_top1_noalloc": (_I, [_P, _P, _L, _P, _I, _I, _I, _P]),
 }
 
@@ -270,6 +272,19 @@ def qgemv_block_dots_q6_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int
     _check("qgemv_block_dots_q6_k", LIB.qgemv_block_dots_q6_k(_dev(w_pack, "w_pack"), _dev(xq, "xq"),
                                                               out.data_ptr(), M, K, N, _stream(xq)))
     return out
+
+
+def set_q4_0_tensor_cores(enable: bool) -> bool:
+    """Run qgemv_q4_0 / qgemv_q4_0_pair on the tensor cores where the shape
+    allows (default) or always on the SIMT kernels; returns the previous setting."""
+    return bool(LIB.qgemv_set_q4_0_tensor_cores(1 if enable else 0))
+
+
+def qgemv_q4_0_plan(M: int, K: int, N: int, N_b: int = 0) -> dict:
+    """The kernel qgemv_q4_0 (N_b = 0) or the pair call would launch."""
+    info = (ctypes.c_int * 4)()
+    _check("qgemv_q4_0_plan", LIB.qgemv_q4_0_plan(M, K, N, N_b, info))
+    return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3]}
 
 
 def qgemv_take_wait_timeouts() -> int:

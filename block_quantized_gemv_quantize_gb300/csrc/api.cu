@@ -109,6 +109,8 @@ int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
     a.ldy = ldy;
     a.K = K;
     a.N = N;
+    const int tc = launch_mmvq_q4_0_tc(a, M, false, as_stream(stream));
+    if (tc != TC_NOT_TAKEN) return tc;
     return launch_mmvq_q4_0(a, M, as_stream(stream));
 }
 
@@ -129,6 +131,8 @@ int qgemv_q4_0_pair(const void* w_pack_a, const void* w_pack_b, const void* xq, 
     a.w_pack2 = w_pack_b;
     a.y2 = y_b;
     a.N2 = N_b;
+    const int tc = launch_mmvq_q4_0_tc(a, M, true, as_stream(stream));
+    if (tc != TC_NOT_TAKEN) return tc;
     return launch_mmvq_q4_0_pair(a, M, as_stream(stream));
 }
 
@@ -231,11 +235,26 @@ int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int 
     return launch_block_dots(FMT_Q6_K, w_pack, xq, out, M, K, N, as_stream(stream));
 }
 
+int qgemv_set_q4_0_tensor_cores(int enable) { return set_q4_0_tensor_cores(enable); }
+
+int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info)
+{
+    if (!info || M < 1 || K < QK || N < 1 || N_b < 0) return QGEMV_INVALID_ARG;
+    if (M > QGEMV_MAX_M || K % QK) return QGEMV_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < 4; ++i) info[i] = 0;
+    MmvqArgs a{};
+    a.K = K;
+    a.N = N;
+    a.N2 = N_b;
+    const int st = launch_mmvq_q4_0_tc(a, M, N_b > 0, nullptr, info);
+    return st == TC_NOT_TAKEN ? QGEMV_OK : st;
+}
+
 int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;
-    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q6_k() +
-             take_wait_timeouts_lmhead();
+    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() +
+             take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead();
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

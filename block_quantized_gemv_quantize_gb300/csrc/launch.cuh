@@ -201,6 +201,14 @@ inline unsigned int take_wait_timeouts_tu()
 }
 
 int launch_mmvq_q4_0(const MmvqArgs& a, int M, cudaStream_t s);
+// The tensor-core Q4_0 path (one weight or a pair); TC_NOT_TAKEN when it is
+// switched off or the shape is not one it takes (the caller then uses the
+// SIMT kernels).
+constexpr int TC_NOT_TAKEN = 1;
+// info (when not null): nothing is launched; the plan is written instead.
+int launch_mmvq_q4_0_tc(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int* info = nullptr);
+int set_q4_0_tensor_cores(int enable);
+unsigned int take_wait_timeouts_q4_0_tc();
 int launch_mmvq_q4_0_pair(const MmvqArgs& a, int M, cudaStream_t s);
 int launch_mmvq_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);

@@ -1,0 +1,598 @@
+// Q4_0 x Q8_1 MMVQ on the tensor cores: exact per-block integer dots from
+// f16 mma.sync (m16n8k16, fp32 accumulate), block scales applied in fp32.
+//
+// What is computed is exactly what the SIMT kernel computes ("Qwen3.6 27B
+// Q4_0 DFlash/SYCL closure", What materially worked, item 2):
+//     y[m][n] = sum_b fp16(d_w[n,b]) * fp16(d_a[m,b]) * I[m,n,b],
+//     I[m,n,b] = sum_i (q_w[n,b,i] - 8) * q_a[m,b,i]   (an exact integer).
+// Why tensor cores here: at M = 6 the dp4a formulation needs 48 dp4a per
+// (row, block), and dp4a issues at half rate on this part, so the integer
+// pipe alone takes as long as streaming the 18-byte block from HBM.  One
+// m16n8k16 pair covers 16 rows x 32 values x 8 activation rows.
+//
+// Exactness.  The A operand (weights) is built from the 4-bit codes with one
+// LOP3 per two values: f16 bits 0x6400 | q = 1024 + q (values 0..15 of the
+// block's low nibbles) and 0x6400 | q << 4 = 1024 + 16 q (the high nibbles,
+// whose B operand is staged as q_a / 16, exact in f16).  Every product is an
+// integer (f16 x f16 is exact in fp32), and the accumulator is started at
+//     C = -1032 * sum_{i<16} q_a - 72 * sum_{i>=16} q_a,
+// so the MMA pair returns I exactly: all partial sums are integers below
+// 2^23 in magnitude.  The scales are then applied per block in fp32:
+//     y += (d_w * d_a) * I, summed per job of 8 blocks, then across jobs.
+//
+// Work decomposition (one CTA per SM, 16 warps):
+//   * a tile is 16 weight rows (four 4-row groups of the packed layout); a
+//     job is one tile x 8 blocks = 2 KB of codes + 256 B of scales, fetched
+//     by two TMA tensor copies: the code box is 128-byte swizzled, so the 8
+//     rows a warp reads at once fall in distinct bank groups;
+//   * a CTA owns a balanced, contiguous range of tiles and, in a cluster of C
+//     CTAs, the C-th part of K (so only that part of the activation is staged);
+//   * the CTA's jobs (tile-major) are cut into W equal contiguous ranges, one
+//     per warp, each streaming through a private ring of S stages; a tile
+//     that straddles two warps is summed from their pieces in warp order, and
+//     the C parts of a tile in rank order (through distributed shared
+//     memory), so the result does not depend on timing.
+#pragma once
+
+#include <cuda.h>
+
+#include "mmvq.cuh"
+
+namespace qgemv {
+
+constexpr int TC_ROWS = 16;                     // weight rows per tile
+constexpr int TC_JB = 8;                        // blocks per job
+constexpr int TC_NIB = TC_ROWS * TC_JB * 16;    // 2048 B of codes per job
+constexpr int TC_DS = TC_ROWS * TC_JB * 2;      // 256 B of scales per job
+constexpr int TC_THREADS = 512;
+constexpr int TC_MAX_STAGES = 6;
+
+struct TcArgs {
+    const uint8_t* xq;  // Q8_1 [M][NB]
+    float* y;           // first weight's output
+    float* y2;          // second weight's output (pairs)
+    int64_t ldy;
+    int K, N, N2;       // N, N2 multiples of 16; K a multiple of 1024
+    int stages;         // ring stages per warp
+    int nkb_max;        // activation blocks staged per CTA (the largest K part)
+    int out_tiles;      // clusters: tiles per cluster the result buffer holds
+};
+
+// Shared-memory layout, identical on the host (sizing) and the device.
+struct TcSmem {
+    uint32_t nib, ds, act, meta, out, tab, bar, bytes;
+};
+
+constexpr int TC_TAB_INTS = 4 + 3 * (TC_THREADS / 32);  // the split-tile table
+
+__host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_tiles)
+{
+    const uint32_t NT = (uint32_t)(M + 7) / 8;
+    TcSmem s;
+    uint32_t o = 0;
+    s.nib = o;  o += (uint32_t)W * S * TC_NIB;     // 1024-byte aligned stages (128-byte swizzle atoms)
+    s.ds = o;   o += (uint32_t)W * S * TC_DS;
+    s.act = o;  o += (uint32_t)nkb * M * 64;        // B fragments, [block][row][4 lanes] x 16 B
+    s.meta = o; o += (uint32_t)nkb * NT * 64;       // [block][8-row tile][4 lanes] x {d_a, d_a, C, C}
+    s.out = o;  o += (uint32_t)out_tiles * 32 * NT * 16;
+    s.tab = o;  o += TC_TAB_INTS * 4;
+    s.bar = o;  o += ((uint32_t)W * S + 1) * 8;     // ring barriers, then the activation's
+    s.bytes = o + 1024;                              // room to align the base to 1024 B
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// PTX: TMA tensor copies, clusters, distributed shared memory, mma.sync.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar,
+                                            uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+// Bulk copy global -> shared without a cache hint (the activation, which
+// every CTA reads).
+__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; shared-memory writes before it
+// are visible to the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load a float from CTA `rank`'s shared memory at the address `p` has in ours.
+__device__ __forceinline__ float ld_dsmem_f32(const float* p, uint32_t rank)
+{
+    uint32_t ra;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+// D = A B + C, m16n8k16, f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                              float c0, float c1, float c2, float c3)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
+// f16x2 of (1024 + nibble) from bits 0..3 of each 16-bit half of v (mask
+// 0x000F000F), or of (1024 + 16 nibble) from bits 4..7 (mask 0x00F000F0).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t nib_f16x2(uint32_t v)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "n"(MASK), "n"(0x64006400));  // (v & MASK) | 0x6400..
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Activation staging: the CTA's K part of the Q8_1 activation as B fragments.
+// Lane (g, t) of an m16n8k16 holds B[k][n = g] for k = 2t, 2t+1 (register 0)
+// and k = 2t+8, 2t+9 (register 1).  The K order inside a block is chosen to
+// match the code unpacking (one 4-byte word per lane and row):
+//   first MMA:  k = 2t, 2t+1   <- values 4t, 4t+2;   k = 2t+8, 2t+9 <- 4t+1, 4t+3
+//   second MMA: the same with values 16 + ..., staged as q_a / 16.
+// Block b, row n: 4 x 16 B at act + ((b * M + n) * 4 + t) * 16.
+// Meta of block b, 8-row tile nt, lane t (rows 8 nt + 2t, + 1):
+//   {d_a, d_a', C, C'} at meta + ((b * NT + nt) * 4 + t) * 16, zero for rows >= M.
+// ---------------------------------------------------------------------------
+
+// (block, row slot) items of the activation conversion per thread: the plan
+// keeps nkb * NT * 8 within TC_STAGE_ITEMS * TC_THREADS.
+constexpr int TC_STAGE_ITEMS = 4;
+
+// Bytes 0, 2 (sel 0x4240) or 1, 3 (sel 0x4341) of the int8 word w as f16x2,
+// scaled by 1 or 1/16, exactly: (w ^ 0x80) is q + 128, and the f16 with bits
+// 0x6400 | (q + 128) is 1024 + 128 + q.
+template <uint32_t SEL, bool SIXTEENTH>
+__device__ __forceinline__ uint32_t q8_f16x2(uint32_t w)
+{
+    const uint32_t b = __byte_perm(w ^ 0x80808080u, 0x64646464u, SEL);
+    const __half2 h = *reinterpret_cast<const __half2*>(&b);
+    const __half2 r = SIXTEENTH ? __hfma2(h, __float2half2_rn(0.0625f), __float2half2_rn(-72.0f))
+                                : __hsub2(h, __float2half2_rn(1152.0f));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// raw: the K part's Q8_1 blocks in shared memory, row n's at raw + n * nkb * 36,
+// lying in the tail of the act region.  One thread per (block, row slot):
+// phase 1 reads its block's 32 codes (and writes the meta), phase 2, after
+// every raw byte has been read, writes the four lanes' B fragments.
+template <int M>
+__device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const uint8_t* raw, int nkb)
+{
+    constexpr int NT = (M + 7) / 8;
+    const int total = nkb * NT * 8;
+    uint32_t q[TC_STAGE_ITEMS][8];
+#pragma unroll
+    for (int u = 0; u < TC_STAGE_ITEMS; ++u) {
+        const int i = threadIdx.x + u * TC_THREADS;
+        if (i >= total) break;
+        const int b = i / (NT * 8), n = i - b * (NT * 8);
+        float da = 0.0f;
+        int s_lo = 0, s_hi = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[u][k] = 0;
+        if (n < M) {
+            const uint8_t* blk = raw + ((size_t)n * nkb + b) * Q8_1_BYTES;
+            da = __half2float(*reinterpret_cast<const __half*>(blk));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q[u][k] = *reinterpret_cast<const uint32_t*>(blk + 4 + 4 * k);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                s_lo = __dp4a((int)q[u][k], 0x01010101, s_lo);
+                s_hi = __dp4a((int)q[u][k + 4], 0x01010101, s_hi);
+            }
+        }
+        const int nt = n >> 3, c = n & 7;
+        float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
+        mp[c & 1] = da;
+        mp[2 + (c & 1)] = (float)(-1032 * s_lo - 72 * s_hi);
+    }
+    __syncthreads();  // the raw bytes are all read
+#pragma unroll
+    for (int u = 0; u < TC_STAGE_ITEMS; ++u) {
+        const int i = threadIdx.x + u * TC_THREADS;
+        if (i >= total) break;
+        const int b = i / (NT * 8), n = i - b * (NT * 8);
+        if (n >= M) continue;
+        uint4* dst = reinterpret_cast<uint4*>(act + ((size_t)b * M + n) * 64);
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+            uint4 v;  // lane t's registers: values 4t, 4t+2 | 4t+1, 4t+3 | and the same + 16 (scaled)
+            v.x = q8_f16x2<0x4240u, false>(q[u][tt]);
+            v.y = q8_f16x2<0x4341u, false>(q[u][tt]);
+            v.z = q8_f16x2<0x4240u, true>(q[u][tt + 4]);
+            v.w = q8_f16x2<0x4341u, true>(q[u][tt + 4]);
+            dst[tt] = v;
+        }
+    }
+}
+
+// One job: 8 blocks of the tile in ring stage (sn codes, sd scales) against
+// staged blocks kb .. kb + 7.  acc[nt][i]: rows g, g, g+8, g+8 and columns
+// 8 nt + 2t, +1, +0, +1 (the mma accumulator layout).
+template <int M>
+__device__ __forceinline__ void tc_job(const uint8_t* sn, const uint8_t* sd, const uint8_t* act, const float* meta,
+                                       int kb, int g, int t, float (&acc)[(M + 7) / 8][4])
+{
+    constexpr int NT = (M + 7) / 8;
+    float jacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) jacc[nt][i] = 0.0f;
+    const uint8_t* rg = sn + g * 128 + 4 * t;             // row g; row g + 8 is 1024 B on
+    const uint8_t* dg = sd + (g >> 2) * 64 + (g & 3) * 2;  // its scales; row g + 8's are 128 B on
+#pragma unroll
+    for (int p = 0; p < TC_JB; ++p) {
+        const int sw = (p ^ g) << 4;  // 16-byte piece p of line L sits at piece p ^ (L & 7)
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(rg + sw);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(rg + 1024 + sw);
+        const float dwa = __half2float(*reinterpret_cast<const __half*>(dg + p * 8));
+        const float dwb = __half2float(*reinterpret_cast<const __half*>(dg + 128 + p * 8));
+        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+        const uint32_t A0[4] = {nib_f16x2<0x000F000Fu>(wa), nib_f16x2<0x000F000Fu>(wb), nib_f16x2<0x000F000Fu>(wa8),
+                                nib_f16x2<0x000F000Fu>(wb8)};
+        const uint32_t A1[4] = {nib_f16x2<0x00F000F0u>(wa), nib_f16x2<0x00F000F0u>(wb), nib_f16x2<0x00F000F0u>(wa8),
+                                nib_f16x2<0x00F000F0u>(wb8)};
+        const int b = kb + p;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int n = nt * 8 + g < M ? nt * 8 + g : M - 1;  // rows past M: any staged row (unused)
+            const uint4 B = *reinterpret_cast<const uint4*>(act + (((size_t)b * M + n) * 4 + t) * 16);
+            const float4 md = *reinterpret_cast<const float4*>(meta + (((size_t)b * NT + nt) * 4 + t) * 4);
+            float d[4];
+            mma_f16_16816(d, A0, B.x, B.y, md.z, md.w, md.z, md.w);
+            mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
+            jacc[nt][0] = fmaf(dwa * md.x, d[0], jacc[nt][0]);
+            jacc[nt][1] = fmaf(dwa * md.y, d[1], jacc[nt][1]);
+            jacc[nt][2] = fmaf(dwb * md.x, d[2], jacc[nt][2]);
+            jacc[nt][3] = fmaf(dwb * md.y, d[3], jacc[nt][3]);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] += jacc[nt][i];
+}
+
+// Write one tile's values, given as value index v of the fragment layout
+// (lane = v / (4 NT), nt, i), to y.
+template <int M>
+__device__ __forceinline__ void tc_store(const TcArgs& a, int64_t T1, int64_t tau, int v, float val)
+{
+    constexpr int NT = (M + 7) / 8;
+    const int ln = v / (4 * NT), rem = v - ln * (4 * NT), nt = rem >> 2, i = rem & 3;
+    const int m = nt * 8 + 2 * (ln & 3) + (i & 1);
+    if (m >= M) return;
+    const bool second = tau >= T1;
+    const int64_t n = (second ? tau - T1 : tau) * TC_ROWS + (ln >> 2) + (i >> 1) * 8;
+    (second ? a.y2 : a.y)[(int64_t)m * a.ldy + n] = val;
+}
+
+template <int M, bool PAIR>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    mmvq_q4_0_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tn0, const __grid_constant__ CUtensorMap td0,
+                        const __grid_constant__ CUtensorMap tn1, const __grid_constant__ CUtensorMap td1,
+                        unsigned int* timeouts)
+{
+    constexpr int NT = (M + 7) / 8;
+    constexpr int VT = 32 * NT * 4;  // values per tile
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    constexpr int W = TC_THREADS / 32;  // launched with exactly TC_THREADS threads
+    const int lane = threadIdx.x & 31;
+    const int warp = __shfl_sync(FULL, (int)(threadIdx.x >> 5), 0);
+    const int g = lane >> 2, t = lane & 3;
+    const int S = a.stages;
+    pdl_launch_dependents();
+
+    // This CTA's tiles (its cluster's) and K part (its rank's).  The special
+    // registers are broadcast so that everything derived from them, down to
+    // the copy coordinates, is warp-uniform.
+    const int C = __shfl_sync(FULL, (int)cluster_nctarank(), 0);
+    const int rank = __shfl_sync(FULL, (int)cluster_ctarank(), 0);
+    const int ncl = __shfl_sync(FULL, (int)cluster_count_x(), 0);
+    const int cl = __shfl_sync(FULL, (int)cluster_id_x(), 0);
+    const int NB = a.K / QK;
+    const int T1 = a.N / TC_ROWS, T = T1 + (PAIR ? a.N2 / TC_ROWS : 0);
+    // (32-bit divisions where the products fit, which they do below 2^24 tiles)
+    const int t0 = T < (1 << 24) ? (int)((uint32_t)(cl * T) / (uint32_t)ncl) : (int)((int64_t)cl * T / ncl);
+    const int t1 = T < (1 << 24) ? (int)((uint32_t)((cl + 1) * T) / (uint32_t)ncl) : (int)((int64_t)(cl + 1) * T / ncl);
+    const int ntile = t1 - t0;
+    const int njb = NB / TC_JB;
+    const int jb0 = rank * njb / C, jb1 = (rank + 1) * njb / C;
+    const int jpt = jb1 - jb0;  // jobs per tile
+    const int J = ntile * jpt;
+    const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
+    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0);
+    uint8_t* nib = smem + sl.nib;
+    uint8_t* ds = smem + sl.ds;
+    uint8_t* act = smem + sl.act;
+    float* meta = reinterpret_cast<float*>(smem + sl.meta);
+    float* outb = reinterpret_cast<float*>(smem + sl.out);
+    int* tab = reinterpret_cast<int*>(smem + sl.tab);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bar);
+    uint64_t* wbar = bars + warp * S;
+    uint64_t* abar = bars + W * S;  // the activation copy
+    uint8_t* wnib = nib + (size_t)warp * S * TC_NIB;
+    uint8_t* wds = ds + (size_t)warp * S * TC_DS;
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&wbar[s], 1);
+        if (warp == 0) mbar_init(abar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1 && lane < (PAIR ? 4 : 2)) {
+        // bring the copies' descriptors on chip while the prologue runs
+        const CUtensorMap* map = lane == 0 ? &tn0 : lane == 1 ? &td0 : lane == 2 ? &tn1 : &td1;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+    }
+    __syncthreads();  // barriers initialized
+    const uint64_t pol = __shfl_sync(FULL, l2_evict_first_policy(), 0);  // warp-uniform copy operand
+
+    // Jobs are walked in order by a cursor (the next copy to issue), a
+    // (CTA-local tile, job within the tile) pair.
+    struct Cursor {
+        int tau, kj;
+    };
+    auto start = [&](int j) {
+        Cursor c;
+        c.tau = jpt > 0 ? j / jpt : 0;
+        c.kj = j - c.tau * jpt;
+        return c;
+    };
+    auto advance = [&](Cursor& c) {
+        if (++c.kj == jpt) {
+            c.kj = 0;
+            ++c.tau;
+        }
+    };
+    // copy coordinates of the job under a cursor
+    auto coords = [&](const Cursor& cu, bool& second, int& x, int& c, int& grp) {
+        const int tg = t0 + cu.tau, kg = jb0 + cu.kj;
+        second = PAIR && tg >= T1;
+        x = kg & 3;  // which 8 blocks of the 32-block chunk
+        c = kg >> 2;
+        grp = (second ? tg - T1 : tg) * (TC_ROWS / GROUP);
+    };
+    Cursor ic = start(j0);  // the next copy
+    int issued = 0, iss_slot = 0;
+    const int n_jobs = j1 - j0;
+    // Copy operands are broadcast from lane 0 so that the compiler sees them
+    // warp-uniform (which keeps the single-lane issue short).
+    auto uni = [&](int v) { return __shfl_sync(FULL, v, 0); };
+    auto issue = [&]() {
+        bool second;
+        int x, c, grp;
+        coords(ic, second, x, c, grp);
+        x = uni(x);
+        c = uni(c);
+        grp = uni(grp);
+        second = uni(second);
+        if (lane == 0) {
+            uint64_t* bar = &wbar[iss_slot];
+            fence_proxy_async();
+            mbar_arrive_expect_tx(bar, TC_NIB + TC_DS);
+            tma_load_4d(wnib + (size_t)iss_slot * TC_NIB, second ? &tn1 : &tn0, x * 128, 0, c, grp, bar, pol);
+            tma_load_3d(wds + (size_t)iss_slot * TC_DS, second ? &td1 : &td0, x * 64, c, grp, bar, pol);
+        }
+        advance(ic);
+        ++issued;
+        if (++iss_slot == S) iss_slot = 0;
+    };
+    pdl_wait();
+
+    // The activation's K part: one bulk copy per row into the tail of the
+    // tile region; the ring starts at once (every earlier kernel's writes are
+    // visible from here) and fills while the copy is converted.
+    bool alive = true;
+    const uint32_t row_bytes = (uint32_t)jpt * TC_JB * Q8_1_BYTES;
+    uint8_t* raw = act + (size_t)a.nkb_max * M * 64 - (size_t)M * row_bytes;
+    if (threadIdx.x == 0 && row_bytes > 0) {
+        mbar_arrive_expect_tx(abar, (uint32_t)M * row_bytes);
+        for (int n = 0; n < M; ++n)
+            bulk_g2s_plain(raw + (size_t)n * row_bytes, a.xq + ((int64_t)n * NB + (int64_t)jb0 * TC_JB) * Q8_1_BYTES,
+                           row_bytes, abar);
+    }
+    while (issued < n_jobs && issued < S - 1) issue();
+    if (warp == W - 1) {  // while the activation copy is in flight
+        // Tiles cut by a warp boundary (found at the first boundary strictly
+        // inside them): the tile, the warps holding its pieces (a mask), and
+        // whether the first of them holds it in its second slot.
+        const int w = lane + 1;
+        bool split = false;
+        int tau = 0, mask = 0, sa = 0;
+        if (w < W && jpt > 0) {
+            const int bnd = w * J / W, prev = (w - 1) * J / W;
+            tau = bnd / jpt;
+            split = bnd % jpt != 0 && prev <= tau * jpt;
+            if (split) {
+                const int first = tau * jpt, last = first + jpt - 1;
+                const int wa = ((first + 1) * W - 1) / J, wb = ((last + 1) * W - 1) / J;
+                for (int ww = wa; ww <= wb; ++ww)
+                    if (ww * J / W != (ww + 1) * J / W) mask |= 1 << ww;  // skip empty warps
+                sa = wa * J / W < first ? 1 : 0;
+            }
+        }
+        const unsigned sel = __ballot_sync(FULL, split);
+        if (split) {
+            const int e = __popc(sel & ((1u << lane) - 1));
+            tab[1 + 3 * e] = tau;
+            tab[2 + 3 * e] = mask;
+            tab[3 + 3 * e] = sa;
+        }
+        if (lane == 0) tab[0] = __popc(sel);
+    }
+
+    if (row_bytes > 0 && !__all_sync(FULL, mbar_wait_bounded(abar, 0))) {
+        if (lane == 0) atomicAdd(timeouts, 1u);
+        alive = false;
+    }
+    alive = __syncthreads_and(alive);
+    if (alive) tc_stage_act<M>(act, meta, raw, jpt * TC_JB);
+    __syncthreads();  // the tile is built
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+    // A warp's pieces of cut tiles (its first segment, its last) wait in
+    // registers until the loop ends; they go to the ring area afterwards.
+    float first_piece[NT][4];
+    bool has_first = false, has_last = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) first_piece[nt][i] = 0.0f;
+    int slot = 0, consumed = 0, seg_begin = j0;
+    uint32_t phase = 0;
+    const Cursor first = start(j0);
+    int tl = first.tau, kj = first.kj;  // the job being worked on: tile (CTA-local) and job within it
+    for (int j = j0; alive && j < j1; ++j) {
+        if (issued < n_jobs) issue();
+        if (!__all_sync(FULL, mbar_wait_bounded(&wbar[slot], phase))) {
+            if (lane == 0) atomicAdd(timeouts, 1u);
+            break;
+        }
+        ++consumed;
+        tc_job<M>(wnib + (size_t)slot * TC_NIB, wds + (size_t)slot * TC_DS, act, meta, kj * TC_JB, g, t, acc);
+        __syncwarp();
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+        const bool tile_end = ++kj == jpt;
+        if (tile_end || j + 1 == j1) {
+            // a segment of tile tl ends: whole tiles go out; a piece of a cut
+            // tile is the warp's first segment (kept) or its last (left in acc)
+            const bool whole = tile_end && seg_begin == tl * jpt;
+            if (whole || seg_begin == j0) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (!whole) first_piece[nt][i] = acc[nt][i];
+                        else if (C > 1) outb[(size_t)tl * VT + lane * NT * 4 + nt * 4 + i] = acc[nt][i];
+                        else tc_store<M>(a, T1, t0 + tl, lane * NT * 4 + nt * 4 + i, acc[nt][i]);
+                        acc[nt][i] = 0.0f;
+                    }
+                has_first = has_first || !whole;
+            } else {
+                has_last = true;  // ends at j1: the loop ends with it
+            }
+            seg_begin = j + 1;
+            if (tile_end) {
+                ++tl;
+                kj = 0;
+            }
+        }
+    }
+    // After a timeout, give the copies still in flight a bounded wait before
+    // the shared memory is released.
+    if (lane == 0) {
+        for (int jj = consumed; jj < issued; ++jj) mbar_wait_bounded(&wbar[jj % S], (uint32_t)((jj / S) & 1));
+        if (!alive && warp == 0) mbar_wait_bounded(abar, 0);
+    }
+    __syncthreads();  // the ring area is free
+    float* slots = reinterpret_cast<float*>(nib);  // [warp][first, last][lane] x 4 NT floats
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (has_first) slots[((size_t)(warp * 2) * 32 + lane) * NT * 4 + nt * 4 + i] = first_piece[nt][i];
+            if (has_last) slots[((size_t)(warp * 2 + 1) * 32 + lane) * NT * 4 + nt * 4 + i] = acc[nt][i];
+        }
+    __syncthreads();
+
+    // Tiles cut by a warp boundary: their pieces added in warp order.
+    const int ne = tab[0];
+    for (int o = threadIdx.x; o < ne * VT; o += blockDim.x) {
+        const int e = o / VT, v = o - e * VT;
+        const int tau = tab[1 + 3 * e];
+        unsigned mask = (unsigned)tab[2 + 3 * e];
+        const int wa = __ffs(mask) - 1;
+        float sum = slots[(size_t)(wa * 2 + tab[3 + 3 * e]) * VT + v];
+        mask &= mask - 1;
+        while (mask) {
+            const int ww = __ffs(mask) - 1;
+            mask &= mask - 1;
+            sum += slots[(size_t)(ww * 2) * VT + v];
+        }
+        if (C > 1) outb[(size_t)tau * VT + v] = sum;
+        else tc_store<M>(a, T1, t0 + tau, v, sum);
+    }
+    if (C > 1) {
+        // The K parts of each tile, added in rank order; rank r writes its
+        // share of the cluster's tiles.
+        cluster_sync_all();
+        const int ta = rank * ntile / C, tb = (rank + 1) * ntile / C;
+        for (int o = threadIdx.x; o < (tb - ta) * VT; o += blockDim.x) {
+            const int tau = ta + o / VT, v = o - (tau - ta) * VT;
+            const float* p = outb + (size_t)tau * VT + v;
+            float sum = ld_dsmem_f32(p, 0);
+            for (int rr = 1; rr < C; ++rr) sum += ld_dsmem_f32(p, (uint32_t)rr);
+            tc_store<M>(a, T1, t0 + tau, v, sum);
+        }
+        cluster_sync_all();  // no CTA leaves while its shared memory is read
+    }
+}
+
+}  // namespace qgemv

@@ -145,6 +145,70 @@ def test_qgemv_q4_0_pair_matches_oracle(ops, M, K, Na, Nb):
         assert r["ok"], r
 
 
+# Tensor-core Q4_0 path: shapes it takes (N, N_b multiples of 16, K of 1024),
+# over several tiles per CTA, warp ranges that cut tiles, clusters that split
+# K (large K or few tiles), and M across the 8-row MMA tiles; each against the
+# oracle with the tensor cores on and off.
+TC_SHAPES = [(1, 1024, 16), (6, 1024, 48), (2, 2048, 160), (6, 5120, 2448), (8, 3072, 512), (9, 1024, 4096),
+             (12, 5120, 336), (16, 2048, 1040), (17, 5120, 272), (6, 17408, 320), (2, 17408, 64), (5, 9216, 784),
+             (3, 1024, 9728)]
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("M,K,N", TC_SHAPES)
+def test_qgemv_q4_0_tensor_core_shapes(ops, M, K, N, tc):
+    prev = ops.set_q4_0_tensor_cores(tc)
+    try:
+        assert ops.qgemv_q4_0_plan(M, K, N)["tensor_cores"] == tc
+        y, y_ref, S = _gemv_case(ops, "q4_0", M, K, N, seed=3 * M + K + N)
+    finally:
+        ops.set_q4_0_tensor_cores(prev)
+    r = C.check_close(y, y_ref, S)
+    assert r["ok"], r
+
+
+def test_qgemv_q4_0_tensor_core_plans(ops):
+    # the shapes above reach every cluster size the planner uses
+    p = ops.qgemv_q4_0_plan(6, 5120, 17408, 17408)
+    assert p["tensor_cores"] and p["cluster"] == 1
+    assert ops.qgemv_q4_0_plan(6, 17408, 5120)["cluster"] > 1
+    assert ops.qgemv_q4_0_plan(2, 17408, 64)["cluster"] == 8
+    assert not ops.qgemv_q4_0_plan(6, 5120, 17400)["tensor_cores"]  # N % 16
+    assert not ops.qgemv_q4_0_plan(6, 5056, 17408)["tensor_cores"]  # K % 1024
+    for M, K, N in TC_SHAPES:
+        p = ops.qgemv_q4_0_plan(M, K, N)
+        assert p["tensor_cores"] and p["grid"] % p["cluster"] == 0 and p["stages"] >= 2, (M, K, N, p)
+
+
+@pytest.mark.parametrize("M,K,Na,Nb", [(1, 1024, 16, 32), (6, 5120, 1536, 1552), (6, 17408, 64, 128),
+                                       (17, 2048, 256, 80), (4, 3072, 4096, 16)])
+def test_qgemv_q4_0_pair_tensor_cores(ops, M, K, Na, Nb):
+    assert ops.qgemv_q4_0_plan(M, K, Na, Nb)["tensor_cores"]
+    x = synth.activations(M, K, seed=M + K + 1, outlier_frac=0.01)
+    xq_ref = oracle.quantize_q8_1(x)
+    xq = ops.quantize_q8_1(_t(x))
+    wa = synth.q4_0_weights(Na, K, seed=Na + 13)
+    wb = synth.q4_0_weights(Nb, K, seed=Nb + 14)
+    ya, yb = ops.qgemv_q4_0_pair(ops.qpack_q4_0(_t(wa), Na, K), ops.qpack_q4_0(_t(wb), Nb, K), xq, M, K, Na, Nb)
+    for y, w in ((ya, wa), (yb, wb)):
+        y_ref, S = oracle.qgemv_q4_0(w, xq_ref)
+        r = C.check_close(_np(y), y_ref, S)
+        assert r["ok"], r
+
+
+def test_qgemv_q4_0_tensor_cores_stride_and_padding(ops):
+    M, K, N, ldy = 6, 2048, 96, 112
+    w = synth.q4_0_weights(N, K, seed=15)
+    x = synth.activations(M, K, seed=16)
+    y = torch.full((M, ldy), 7.0, device=DEV)
+    ops.qgemv_q4_0(ops.qpack_q4_0(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N, y=y[:, :N])
+    yy = _np(y)
+    y_ref, S = oracle.qgemv_q4_0(w, oracle.quantize_q8_1(x))
+    assert C.check_close(yy[:, :N], y_ref, S)["ok"]
+    assert np.all(yy[:, N:] == 7.0)
+    assert ops.qgemv_take_wait_timeouts() == 0
+
+
 def test_qgemv_q4_0_pair_padding_untouched_and_errors(ops):
     M, K, Na, Nb, ldy = 6, 512, 70, 33, 80
     x = synth.activations(M, K, seed=8)
