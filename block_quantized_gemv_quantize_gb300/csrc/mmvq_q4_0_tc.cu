@@ -273,6 +273,9 @@ int set_q4_0_tensor_cores(int enable) { return g_tc_enabled.exchange(enable ? 1 
 int launch_mmvq_q4_0_tc(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int* info)
 {
     if (!g_tc_enabled.load()) return TC_NOT_TAKEN;
+    // Below 5 rows the SIMT kernels are as fast or faster (measured on GB300:
+    // M <= 4 loses up to 12% on the tensor cores, M >= 5 gains up to 34%).
+    if (M < TC_MIN_M) return TC_NOT_TAKEN;
     if (a.N % TC_ROWS || (pair && a.N2 % TC_ROWS) || a.K % (CHUNK * QK)) return TC_NOT_TAKEN;
     return pair ? launch_tc<true>(a, M, s, info) : launch_tc<false>(a, M, s, info);
 }

@@ -45,6 +45,7 @@ constexpr int TC_JB = 8;                        // blocks per job
 constexpr int TC_NIB = TC_ROWS * TC_JB * 16;    // 2048 B of codes per job
 constexpr int TC_DS = TC_ROWS * TC_JB * 2;      // 256 B of scales per job
 constexpr int TC_THREADS = 512;
+constexpr int TC_MIN_M = 5;  // activation rows from which the tensor-core path is taken
 constexpr int TC_MAX_STAGES = 6;
 
 struct TcArgs {

@@ -237,8 +237,8 @@ int qgemv_block_dots_q4_0(const void* w_pack, const void* xq, int32_t* out, int 
 int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream);
 
 /* qgemv_set_q4_0_tensor_cores - choose the kernel family of qgemv_q4_0 and
- * qgemv_q4_0_pair: 1 (the default) runs shapes with N (and N_b) a multiple
- * of 16 and K a multiple of 1024 on the tensor cores (f16 mma.sync with exact
+ * qgemv_q4_0_pair: 1 (the default) runs shapes with M >= 5, N (and N_b) a
+ * multiple of 16 and K a multiple of 1024 on the tensor cores (f16 mma.sync with exact
  * integer block dots, the scales applied per block in fp32); 0 runs every
  * shape on the SIMT dp4a kernels.  Both compute the formula of qgemv_q4_0
  * within its fp32 rounding; the fp32 summation order differs, so the two may

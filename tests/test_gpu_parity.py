@@ -149,9 +149,9 @@ def test_qgemv_q4_0_pair_matches_oracle(ops, M, K, Na, Nb):
 # over several tiles per CTA, warp ranges that cut tiles, clusters that split
 # K (large K or few tiles), and M across the 8-row MMA tiles; each against the
 # oracle with the tensor cores on and off.
-TC_SHAPES = [(1, 1024, 16), (6, 1024, 48), (2, 2048, 160), (6, 5120, 2448), (8, 3072, 512), (9, 1024, 4096),
-             (12, 5120, 336), (16, 2048, 1040), (17, 5120, 272), (6, 17408, 320), (2, 17408, 64), (5, 9216, 784),
-             (3, 1024, 9728)]
+TC_SHAPES = [(5, 1024, 16), (6, 1024, 48), (7, 2048, 160), (6, 5120, 2448), (8, 3072, 512), (9, 1024, 4096),
+             (12, 5120, 336), (16, 2048, 1040), (17, 5120, 272), (6, 17408, 320), (5, 17408, 64), (5, 9216, 784),
+             (7, 1024, 9728)]
 
 
 @pytest.mark.parametrize("tc", [True, False])
@@ -172,7 +172,8 @@ def test_qgemv_q4_0_tensor_core_plans(ops):
     p = ops.qgemv_q4_0_plan(6, 5120, 17408, 17408)
     assert p["tensor_cores"] and p["cluster"] == 1
     assert ops.qgemv_q4_0_plan(6, 17408, 5120)["cluster"] > 1
-    assert ops.qgemv_q4_0_plan(2, 17408, 64)["cluster"] == 8
+    assert ops.qgemv_q4_0_plan(5, 17408, 64)["cluster"] == 8
+    assert not ops.qgemv_q4_0_plan(4, 5120, 17408)["tensor_cores"]  # M < 5: the SIMT kernels
     assert not ops.qgemv_q4_0_plan(6, 5120, 17400)["tensor_cores"]  # N % 16
     assert not ops.qgemv_q4_0_plan(6, 5056, 17408)["tensor_cores"]  # K % 1024
     for M, K, N in TC_SHAPES:
@@ -180,8 +181,8 @@ def test_qgemv_q4_0_tensor_core_plans(ops):
         assert p["tensor_cores"] and p["grid"] % p["cluster"] == 0 and p["stages"] >= 2, (M, K, N, p)
 
 
-@pytest.mark.parametrize("M,K,Na,Nb", [(1, 1024, 16, 32), (6, 5120, 1536, 1552), (6, 17408, 64, 128),
-                                       (17, 2048, 256, 80), (4, 3072, 4096, 16)])
+@pytest.mark.parametrize("M,K,Na,Nb", [(5, 1024, 16, 32), (6, 5120, 1536, 1552), (6, 17408, 64, 128),
+                                       (17, 2048, 256, 80), (8, 3072, 4096, 16)])
 def test_qgemv_q4_0_pair_tensor_cores(ops, M, K, Na, Nb):
     assert ops.qgemv_q4_0_plan(M, K, Na, Nb)["tensor_cores"]
     x = synth.activations(M, K, seed=M + K + 1, outlier_frac=0.01)
