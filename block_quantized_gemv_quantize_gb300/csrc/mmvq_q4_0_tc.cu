@@ -145,7 +145,7 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
         if (njb < C) break;
         const int jpt = (njb + C - 1) / C;
         const int nkb = jpt * TC_JB;
-        if (nkb * ((M + 7) / 8) * 8 > TC_STAGE_ITEMS * TC_THREADS) continue;  // staging items per thread
+        if (nkb * ((M + 7) / 8) * 8 > tc_stage_items(M) * TC_THREADS) continue;  // staging items per thread
         // shared memory at the deepest ring that fits, with a worst-case
         // cluster count for the result buffer (fixed below)
         int64_t ncl = C == 1 ? di.sms : 0;

@@ -193,9 +193,10 @@ __device__ __forceinline__ uint32_t nib_f16x2(uint32_t v)
 //   {d_a, d_a', C, C'} at meta + ((b * NT + nt) * 4 + t) * 16, zero for rows >= M.
 // ---------------------------------------------------------------------------
 
-// (block, row slot) items of the activation conversion per thread: the plan
-// keeps nkb * NT * 8 within TC_STAGE_ITEMS * TC_THREADS.
-constexpr int TC_STAGE_ITEMS = 4;
+// (block, row slot) items of the activation conversion per thread (four
+// threads each): the plan keeps nkb * NT * 8 within tc_stage_items(M) *
+// TC_THREADS (K = 5120 fits in one CTA up to M = 12).
+__host__ __device__ constexpr int tc_stage_items(int M) { return M > 8 ? 6 : 4; }
 
 // Bytes 0, 2 (sel 0x4240) or 1, 3 (sel 0x4341) of the int8 word w as f16x2,
 // scaled by 1 or 1/16, exactly: (w ^ 0x80) is q + 128, and the f16 with bits
@@ -210,58 +211,57 @@ __device__ __forceinline__ uint32_t q8_f16x2(uint32_t w)
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// raw: the K part's Q8_1 blocks in shared memory, row n's at raw + n * nkb * 36,
-// lying in the tail of the act region.  One thread per (block, row slot):
-// phase 1 reads its block's 32 codes (and writes the meta), phase 2, after
-// every raw byte has been read, writes the four lanes' B fragments.
+// raw: the K part's Q8_1 blocks in shared memory, row n's at raw + n * rstride
+// (rstride = nkb * 36 + 16: the pad puts the rows in distinct bank groups),
+// lying in the tail of the act region.  Thread item (block b, row n, lane t),
+// t fastest, then n: phase 1 reads the lane's two code words (and the meta is
+// written), phase 2, after every raw byte has been read, writes the lane's
+// 16-byte B fragment; both are free of bank conflicts.
 template <int M>
-__device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const uint8_t* raw, int nkb)
+__device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const uint8_t* raw, int nkb, int rstride)
 {
     constexpr int NT = (M + 7) / 8;
-    const int total = nkb * NT * 8;
-    uint32_t q[TC_STAGE_ITEMS][8];
+    constexpr int IT = 4 * tc_stage_items(M);
+    const int total = nkb * NT * 32;
+    uint32_t w0[IT], w1[IT];
 #pragma unroll
-    for (int u = 0; u < TC_STAGE_ITEMS; ++u) {
+    for (int u = 0; u < IT; ++u) {
         const int i = threadIdx.x + u * TC_THREADS;
-        if (i >= total) break;
-        const int b = i / (NT * 8), n = i - b * (NT * 8);
+        w0[u] = w1[u] = 0;
+        if (i >= total) break;  // warp-uniform: total is a multiple of 32
+        const int tt = i & 3, n = ((i >> 5) % NT) * 8 + ((i >> 2) & 7), b = (i >> 5) / NT;
         float da = 0.0f;
-        int s_lo = 0, s_hi = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) q[u][k] = 0;
         if (n < M) {
-            const uint8_t* blk = raw + ((size_t)n * nkb + b) * Q8_1_BYTES;
-            da = __half2float(*reinterpret_cast<const __half*>(blk));
-#pragma unroll
-            for (int k = 0; k < 8; ++k) q[u][k] = *reinterpret_cast<const uint32_t*>(blk + 4 + 4 * k);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                s_lo = __dp4a((int)q[u][k], 0x01010101, s_lo);
-                s_hi = __dp4a((int)q[u][k + 4], 0x01010101, s_hi);
-            }
+            const uint8_t* blk = raw + (size_t)n * rstride + (size_t)b * Q8_1_BYTES;
+            w0[u] = *reinterpret_cast<const uint32_t*>(blk + 4 + 4 * tt);
+            w1[u] = *reinterpret_cast<const uint32_t*>(blk + 20 + 4 * tt);
+            if (tt == 0) da = __half2float(*reinterpret_cast<const __half*>(blk));
         }
-        const int nt = n >> 3, c = n & 7;
-        float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
-        mp[c & 1] = da;
-        mp[2 + (c & 1)] = (float)(-1032 * s_lo - 72 * s_hi);
+        int s_lo = __dp4a((int)w0[u], 0x01010101, 0), s_hi = __dp4a((int)w1[u], 0x01010101, 0);
+        s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 1);
+        s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 1);
+        s_lo += __shfl_xor_sync(0xffffffffu, s_lo, 2);
+        s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 2);
+        if (tt == 0) {
+            const int nt = n >> 3, c = n & 7;
+            float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
+            mp[c & 1] = da;
+            mp[2 + (c & 1)] = (float)(-1032 * s_lo - 72 * s_hi);
+        }
     }
     __syncthreads();  // the raw bytes are all read
 #pragma unroll
-    for (int u = 0; u < TC_STAGE_ITEMS; ++u) {
+    for (int u = 0; u < IT; ++u) {
         const int i = threadIdx.x + u * TC_THREADS;
         if (i >= total) break;
-        const int b = i / (NT * 8), n = i - b * (NT * 8);
+        const int tt = i & 3, n = ((i >> 5) % NT) * 8 + ((i >> 2) & 7), b = (i >> 5) / NT;
         if (n >= M) continue;
-        uint4* dst = reinterpret_cast<uint4*>(act + ((size_t)b * M + n) * 64);
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-            uint4 v;  // lane t's registers: values 4t, 4t+2 | 4t+1, 4t+3 | and the same + 16 (scaled)
-            v.x = q8_f16x2<0x4240u, false>(q[u][tt]);
-            v.y = q8_f16x2<0x4341u, false>(q[u][tt]);
-            v.z = q8_f16x2<0x4240u, true>(q[u][tt + 4]);
-            v.w = q8_f16x2<0x4341u, true>(q[u][tt + 4]);
-            dst[tt] = v;
-        }
+        uint4 v;  // lane t's registers: values 4t, 4t+2 | 4t+1, 4t+3 | and the same + 16 (scaled)
+        v.x = q8_f16x2<0x4240u, false>(w0[u]);
+        v.y = q8_f16x2<0x4341u, false>(w0[u]);
+        v.z = q8_f16x2<0x4240u, true>(w1[u]);
+        v.w = q8_f16x2<0x4341u, true>(w1[u]);
+        *reinterpret_cast<uint4*>(act + (((size_t)b * M + n) * 4 + tt) * 16) = v;
     }
 }
 
@@ -389,8 +389,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();  // barriers initialized
     const uint64_t pol = __shfl_sync(FULL, l2_evict_first_policy(), 0);  // warp-uniform copy operand
 
-    // Jobs are walked in order by a cursor (the next copy to issue), a
-    // (CTA-local tile, job within the tile) pair.
+    // The consumer walks the jobs as (CTA-local tile, job within the tile);
+    // the copy issue keeps its own running coordinates.
     struct Cursor {
         int tau, kj;
     };
@@ -400,42 +400,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         c.kj = j - c.tau * jpt;
         return c;
     };
-    auto advance = [&](Cursor& c) {
-        if (++c.kj == jpt) {
-            c.kj = 0;
-            ++c.tau;
-        }
-    };
-    // copy coordinates of the job under a cursor
-    auto coords = [&](const Cursor& cu, bool& second, int& x, int& c, int& grp) {
-        const int tg = t0 + cu.tau, kg = jb0 + cu.kj;
-        second = PAIR && tg >= T1;
-        x = kg & 3;  // which 8 blocks of the 32-block chunk
-        c = kg >> 2;
-        grp = (second ? tg - T1 : tg) * (TC_ROWS / GROUP);
-    };
-    Cursor ic = start(j0);  // the next copy
     int issued = 0, iss_slot = 0;
     const int n_jobs = j1 - j0;
-    // Copy operands are broadcast from lane 0 so that the compiler sees them
-    // warp-uniform (which keeps the single-lane issue short).
-    auto uni = [&](int v) { return __shfl_sync(FULL, v, 0); };
+    // next copy: job ikj of the tile whose first group is igrp (of the
+    // second weight when isec), blocks 8 ikg .. 8 ikg + 7 of the row
+    int ikj, ikg, igrp;
+    bool isec;
+    {
+        const Cursor c = start(j0);
+        const int tg = t0 + c.tau;
+        ikj = c.kj;
+        ikg = jb0 + c.kj;
+        isec = PAIR && tg >= T1;
+        igrp = (isec ? tg - T1 : tg) * (TC_ROWS / GROUP);
+    }
     auto issue = [&]() {
-        bool second;
-        int x, c, grp;
-        coords(ic, second, x, c, grp);
-        x = uni(x);
-        c = uni(c);
-        grp = uni(grp);
-        second = uni(second);
+        const int x = ikg & 3, c = ikg >> 2;  // which 8 blocks of which 32-block chunk
         if (lane == 0) {
             uint64_t* bar = &wbar[iss_slot];
             fence_proxy_async();
             mbar_arrive_expect_tx(bar, TC_NIB + TC_DS);
-            tma_load_4d(wnib + (size_t)iss_slot * TC_NIB, second ? &tn1 : &tn0, x * 128, 0, c, grp, bar, pol);
-            tma_load_3d(wds + (size_t)iss_slot * TC_DS, second ? &td1 : &td0, x * 64, c, grp, bar, pol);
+            tma_load_4d(wnib + (size_t)iss_slot * TC_NIB, isec ? &tn1 : &tn0, x * 128, 0, c, igrp, bar, pol);
+            tma_load_3d(wds + (size_t)iss_slot * TC_DS, isec ? &td1 : &td0, x * 64, c, igrp, bar, pol);
         }
-        advance(ic);
+        ++ikg;
+        if (++ikj == jpt) {  // next tile
+            ikj = 0;
+            ikg = jb0;
+            igrp += TC_ROWS / GROUP;
+            if (PAIR && !isec && igrp == T1 * (TC_ROWS / GROUP)) {
+                isec = true;
+                igrp = 0;
+            }
+        }
         ++issued;
         if (++iss_slot == S) iss_slot = 0;
     };
@@ -445,12 +442,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // tile region; the ring starts at once (every earlier kernel's writes are
     // visible from here) and fills while the copy is converted.
     bool alive = true;
-    const uint32_t row_bytes = (uint32_t)jpt * TC_JB * Q8_1_BYTES;
-    uint8_t* raw = act + (size_t)a.nkb_max * M * 64 - (size_t)M * row_bytes;
+    const uint32_t row_bytes = (uint32_t)jpt * TC_JB * Q8_1_BYTES, rstride = row_bytes + 16;
+    uint8_t* raw = act + (size_t)a.nkb_max * M * 64 - (size_t)M * rstride;
     if (threadIdx.x == 0 && row_bytes > 0) {
         mbar_arrive_expect_tx(abar, (uint32_t)M * row_bytes);
         for (int n = 0; n < M; ++n)
-            bulk_g2s_plain(raw + (size_t)n * row_bytes, a.xq + ((int64_t)n * NB + (int64_t)jb0 * TC_JB) * Q8_1_BYTES,
+            bulk_g2s_plain(raw + (size_t)n * rstride, a.xq + ((int64_t)n * NB + (int64_t)jb0 * TC_JB) * Q8_1_BYTES,
                            row_bytes, abar);
     }
     while (issued < n_jobs && issued < S - 1) issue();
@@ -488,7 +485,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         alive = false;
     }
     alive = __syncthreads_and(alive);
-    if (alive) tc_stage_act<M>(act, meta, raw, jpt * TC_JB);
+    if (alive) tc_stage_act<M>(act, meta, raw, jpt * TC_JB, (int)rstride);
     __syncthreads();  // the tile is built
     float acc[NT][4];
 #pragma unroll

@@ -197,6 +197,48 @@ def test_qgemv_q4_0_pair_tensor_cores(ops, M, K, Na, Nb):
         assert r["ok"], r
 
 
+def _unit_scale_case(M, K, N, seed):
+    """Q4_0 weights with d = 1 and integer activations whose every block holds
+    a 127 (so d_a = 1 and q_a = x): every output is an exact integer below
+    2^24, so any correct fp32 path must reproduce the oracle bit for bit."""
+    w = synth.q4_0_weights(N, K, seed=seed, d_lo=1.0, d_hi=1.0)
+    g = np.random.default_rng(seed + 1)
+    x = g.integers(-127, 128, size=(M, K)).astype(np.float32)
+    x[:, ::32] = np.where(g.integers(0, 2, size=(M, K // 32)) == 1, 127.0, -127.0).astype(np.float32)
+    return w, x
+
+
+@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("M,K,N", [(6, 5120, 64), (5, 1024, 4096), (9, 2048, 48), (17, 1024, 32), (6, 8192, 64)])
+def test_qgemv_q4_0_unit_scales_exact(ops, M, K, N, tc):
+    # pins the exactness of the block dots on both paths: with unit scales the
+    # output is the integer sum of the exact block dots (|y| <= K * 8 * 127 < 2^24)
+    w, x = _unit_scale_case(M, K, N, seed=M * 31 + K + N)
+    xq_ref = oracle.quantize_q8_1(x)
+    assert np.all(xq_ref[:, :, 0:2].view(np.float16) == 1.0)
+    y_ref, _ = oracle.qgemv_q4_0(w, xq_ref)
+    assert np.all(y_ref == np.round(y_ref))
+    prev = ops.set_q4_0_tensor_cores(tc)
+    try:
+        assert ops.qgemv_q4_0_plan(M, K, N)["tensor_cores"] == (tc and M >= 5)
+        y = _np(ops.qgemv_q4_0(ops.qpack_q4_0(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
+    finally:
+        ops.set_q4_0_tensor_cores(prev)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def test_qgemv_q4_0_pair_unit_scales_exact(ops):
+    M, K, Na, Nb = 6, 4096, 48, 80
+    wa, x = _unit_scale_case(M, K, Na, seed=5)
+    wb, _ = _unit_scale_case(M, K, Nb, seed=6)
+    xq_ref = oracle.quantize_q8_1(x)
+    ya, yb = ops.qgemv_q4_0_pair(ops.qpack_q4_0(_t(wa), Na, K), ops.qpack_q4_0(_t(wb), Nb, K),
+                                 ops.quantize_q8_1(_t(x)), M, K, Na, Nb)
+    for y, w in ((ya, wa), (yb, wb)):
+        y_ref, _ = oracle.qgemv_q4_0(w, xq_ref)
+        assert np.array_equal(_np(y).astype(np.float64), y_ref)
+
+
 def test_qgemv_q4_0_tensor_cores_stride_and_padding(ops):
     M, K, N, ldy = 6, 2048, 96, 112
     w = synth.q4_0_weights(N, K, seed=15)
