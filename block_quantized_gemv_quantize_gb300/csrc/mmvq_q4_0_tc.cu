@@ -32,11 +32,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // (N % 16 == 0, K % 1024 == 0): every group-chunk is 2304 B, codes
 // nib[4 rows][32 blocks][16 B] then scales d[32 blocks][4 rows].
 //   codes:  bytes of a row's chunk (512) x row (4) x chunk (nch) x group,
-//           box 128 B x 4 rows x 1 chunk x 4 groups = one job's 16 rows x
-//           8 blocks, 128-byte swizzled;
-//   scales: bytes of the chunk's scales (256) x chunk x group, box 64 B x 1
-//           x 4 groups.
-bool q4_0_tensor_maps(const void* w, int N, int K, CUtensorMap* nib, CUtensorMap* d)
+//           box 128 B x 4 rows x 1 chunk x 4 groups = 16 rows x 8 blocks,
+//           128-byte swizzled (a job takes two);
+//   scales: bytes of the chunk's scales (256) x chunk x group, box jb * 8 B
+//           x 1 x 4 groups = a job's 16 rows x jb blocks.
+bool q4_0_tensor_maps(const void* w, int N, int K, int jb, CUtensorMap* nib, CUtensorMap* d)
 {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
@@ -46,7 +46,7 @@ bool q4_0_tensor_maps(const void* w, int N, int K, CUtensorMap* nib, CUtensorMap
     {
         const cuuint64_t dims[4] = {(cuuint64_t)CHUNK * 16, GROUP, (cuuint64_t)L.nch, (cuuint64_t)L.n_groups};
         const cuuint64_t strides[3] = {(cuuint64_t)CHUNK * 16, gc, gs};
-        const cuuint32_t box[4] = {TC_JB * 16, GROUP, 1, TC_ROWS / GROUP};
+        const cuuint32_t box[4] = {TC_LINE_JB * 16, GROUP, 1, TC_ROWS / GROUP};
         const cuuint32_t es[4] = {1, 1, 1, 1};
         if (enc(nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(w), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -56,7 +56,7 @@ bool q4_0_tensor_maps(const void* w, int N, int K, CUtensorMap* nib, CUtensorMap
     {
         const cuuint64_t dims[3] = {(cuuint64_t)CHUNK * GROUP * 2, (cuuint64_t)L.nch, (cuuint64_t)L.n_groups};
         const cuuint64_t strides[2] = {gc, gs};
-        const cuuint32_t box[3] = {TC_JB * GROUP * 2, 1, TC_ROWS / GROUP};
+        const cuuint32_t box[3] = {(cuuint32_t)jb * GROUP * 2, 1, TC_ROWS / GROUP};
         const cuuint32_t es[3] = {1, 1, 1};
         void* base = static_cast<uint8_t*>(const_cast<void*>(w)) + (size_t)GROUP * CHUNK * 16;
         if (enc(d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -68,7 +68,7 @@ bool q4_0_tensor_maps(const void* w, int N, int K, CUtensorMap* nib, CUtensorMap
 }
 
 struct TcPlan {
-    int C, grid, S, nkb_max, out_tiles;
+    int C, grid, S, jb, nkb_max, out_tiles;
     size_t smem;
 };
 
@@ -129,53 +129,58 @@ int tc_max_clusters(int dev, int ci, size_t smem)
     return cache[dev][ci];
 }
 
-// The cheapest plan: per cluster size C, the largest per-CTA job count over
-// 16 warps (the critical path), plus two jobs for the cross-CTA combine when
-// C > 1.  Returns false when no C fits in shared memory.
+// The cheapest plan over job sizes JB (16 or 8 blocks) and cluster sizes C:
+// the largest per-CTA job count over 16 warps (the critical path) in units of
+// 8 blocks, where a 16-block job counts 0.85 x 2 units (measured: it halves
+// the per-job copy issue and loop overhead), plus two units for the
+// cross-CTA combine when C > 1.  Returns false when nothing fits.
 template <int M, bool PAIR>
 bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
 {
     const int W = TC_THREADS / 32;
-    const int NB = K / QK, njb = NB / TC_JB;
+    const int NB = K / QK;
     const int64_t T = N / TC_ROWS + (PAIR ? N2 / TC_ROWS : 0);
     double best_cost = 0.0;
     bool found = false;
-    for (int ci = 0; ci < 4; ++ci) {
-        const int C = TC_CLUSTERS[ci];
-        if (njb < C) break;
-        const int jpt = (njb + C - 1) / C;
-        const int nkb = jpt * TC_JB;
-        if (nkb * ((M + 7) / 8) * 8 > tc_stage_items(M) * TC_THREADS) continue;  // staging items per thread
-        // shared memory at the deepest ring that fits, with a worst-case
-        // cluster count for the result buffer (fixed below)
-        int64_t ncl = C == 1 ? di.sms : 0;
-        if (C > 1) {
-            const TcSmem s2 = tc_smem(M, W, 2, nkb, 0);
-            if (s2.bytes > (uint32_t)di.smem_optin) continue;
-            ncl = tc_max_clusters<M, PAIR>(dev, ci, (size_t)di.smem_optin);
-            if (ncl <= 0) continue;
-        }
-        if (ncl > T) ncl = T;
-        const int tiles = (int)((T + ncl - 1) / ncl);
-        const int out_tiles = C > 1 ? tiles : 0;
-        int S = 0;
-        for (int s = TC_MAX_STAGES; s >= 2; --s) {
-            if (tc_smem(M, W, s, nkb, out_tiles).bytes <= (uint32_t)di.smem_optin) {
-                S = s;
-                break;
+    for (int jb = 2 * TC_LINE_JB; jb >= TC_LINE_JB; jb -= TC_LINE_JB) {
+        const int njb = NB / jb;
+        for (int ci = 0; ci < 4; ++ci) {
+            const int C = TC_CLUSTERS[ci];
+            if (njb < C) break;
+            const int jpt = (njb + C - 1) / C;
+            const int nkb = jpt * jb;
+            if (nkb * ((M + 7) / 8) * 8 > tc_stage_items(M) * TC_THREADS) continue;  // staging items per thread
+            // shared memory at the deepest ring that fits
+            int64_t ncl = C == 1 ? di.sms : 0;
+            if (C > 1) {
+                if (tc_smem(M, W, 2, nkb, 0, jb).bytes > (uint32_t)di.smem_optin) continue;
+                ncl = tc_max_clusters<M, PAIR>(dev, ci, (size_t)di.smem_optin);
+                if (ncl <= 0) continue;
             }
-        }
-        if (S == 0) continue;
-        const double cost = (double)(((int64_t)tiles * jpt + W - 1) / W) + (C > 1 ? 2.0 : 0.0);
-        if (!found || cost < best_cost - 1e-9) {
-            found = true;
-            best_cost = cost;
-            best.C = C;
-            best.grid = (int)(ncl * C);
-            best.S = S;
-            best.nkb_max = nkb;
-            best.out_tiles = out_tiles;
-            best.smem = tc_smem(M, W, S, nkb, out_tiles).bytes;
+            if (ncl > T) ncl = T;
+            const int tiles = (int)((T + ncl - 1) / ncl);
+            const int out_tiles = C > 1 ? tiles : 0;
+            int S = 0;
+            for (int s = TC_MAX_STAGES; s >= 2; --s) {
+                if (tc_smem(M, W, s, nkb, out_tiles, jb).bytes <= (uint32_t)di.smem_optin) {
+                    S = s;
+                    break;
+                }
+            }
+            if (S == 0) continue;
+            const double unit = jb > TC_LINE_JB ? 0.85 * jb / TC_LINE_JB : 1.0;
+            const double cost = (double)(((int64_t)tiles * jpt + W - 1) / W) * unit + (C > 1 ? 2.0 : 0.0);
+            if (!found || cost < best_cost - 1e-9) {
+                found = true;
+                best_cost = cost;
+                best.C = C;
+                best.grid = (int)(ncl * C);
+                best.S = S;
+                best.jb = jb;
+                best.nkb_max = nkb;
+                best.out_tiles = out_tiles;
+                best.smem = tc_smem(M, W, S, nkb, out_tiles, jb).bytes;
+            }
         }
     }
     return found;
@@ -219,9 +224,9 @@ int launch_tc_m(const MmvqArgs& m, cudaStream_t s, int* info)
         return QGEMV_OK;
     }
     CUtensorMap n0, d0, n1, d1;
-    if (!q4_0_tensor_maps(m.w_pack, m.N, m.K, &n0, &d0)) return QGEMV_CUDA_ERROR;
+    if (!q4_0_tensor_maps(m.w_pack, m.N, m.K, p.jb, &n0, &d0)) return QGEMV_CUDA_ERROR;
     if (PAIR) {
-        if (!q4_0_tensor_maps(m.w_pack2, m.N2, m.K, &n1, &d1)) return QGEMV_CUDA_ERROR;
+        if (!q4_0_tensor_maps(m.w_pack2, m.N2, m.K, p.jb, &n1, &d1)) return QGEMV_CUDA_ERROR;
     } else {
         n1 = n0;
         d1 = d0;
@@ -235,6 +240,7 @@ int launch_tc_m(const MmvqArgs& m, cudaStream_t s, int* info)
     a.N = m.N;
     a.N2 = PAIR ? m.N2 : 0;
     a.stages = p.S;
+    a.jb = p.jb;
     a.nkb_max = p.nkb_max;
     a.out_tiles = p.out_tiles;
     if (tc_launch<M, PAIR>(p, a, n0, d0, n1, d1, timeouts, s) != cudaSuccess) return QGEMV_CUDA_ERROR;

@@ -22,9 +22,10 @@
 //
 // Work decomposition (one CTA per SM, 16 warps):
 //   * a tile is 16 weight rows (four 4-row groups of the packed layout); a
-//     job is one tile x 8 blocks = 2 KB of codes + 256 B of scales, fetched
-//     by two TMA tensor copies: the code box is 128-byte swizzled, so the 8
-//     rows a warp reads at once fall in distinct bank groups;
+//     job is one tile x 16 blocks (4 KB of codes + 512 B of scales, three TMA
+//     tensor copies), or x 8 blocks where shared memory is short; the code
+//     boxes (8 blocks each) are 128-byte swizzled, so the 8 rows a warp reads
+//     at once fall in distinct bank groups;
 //   * a CTA owns a balanced, contiguous range of tiles and, in a cluster of C
 //     CTAs, the C-th part of K (so only that part of the activation is staged);
 //   * the CTA's jobs (tile-major) are cut into W equal contiguous ranges, one
@@ -41,9 +42,12 @@
 namespace qgemv {
 
 constexpr int TC_ROWS = 16;                     // weight rows per tile
-constexpr int TC_JB = 8;                        // blocks per job
-constexpr int TC_NIB = TC_ROWS * TC_JB * 16;    // 2048 B of codes per job
-constexpr int TC_DS = TC_ROWS * TC_JB * 2;      // 256 B of scales per job
+constexpr int TC_LINE_JB = 8;                   // blocks per 128-byte line of a code box
+constexpr int TC_BOX = TC_ROWS * TC_LINE_JB * 16;  // 2048 B: one code box (16 rows x 8 blocks)
+// Blocks per job, chosen per launch: 16 (two code boxes, fewer jobs) where two
+// ring stages of them fit next to the activation tile, else 8.
+__host__ __device__ inline int tc_nib_bytes(int jb) { return TC_ROWS * jb * 16; }
+__host__ __device__ inline int tc_ds_bytes(int jb) { return TC_ROWS * jb * 2; }
 constexpr int TC_THREADS = 512;
 constexpr int TC_MIN_M = 5;  // activation rows from which the tensor-core path is taken
 constexpr int TC_MAX_STAGES = 6;
@@ -55,6 +59,7 @@ struct TcArgs {
     int64_t ldy;
     int K, N, N2;       // N, N2 multiples of 16; K a multiple of 1024
     int stages;         // ring stages per warp
+    int jb;             // blocks per job (8 or 16)
     int nkb_max;        // activation blocks staged per CTA (the largest K part)
     int out_tiles;      // clusters: tiles per cluster the result buffer holds
 };
@@ -66,13 +71,13 @@ struct TcSmem {
 
 constexpr int TC_TAB_INTS = 4 + 3 * (TC_THREADS / 32);  // the split-tile table
 
-__host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_tiles)
+__host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_tiles, int jb)
 {
     const uint32_t NT = (uint32_t)(M + 7) / 8;
     TcSmem s;
     uint32_t o = 0;
-    s.nib = o;  o += (uint32_t)W * S * TC_NIB;     // 1024-byte aligned stages (128-byte swizzle atoms)
-    s.ds = o;   o += (uint32_t)W * S * TC_DS;
+    s.nib = o;  o += (uint32_t)W * S * tc_nib_bytes(jb);  // 1024-byte aligned stages (128-byte swizzle atoms)
+    s.ds = o;   o += (uint32_t)W * S * tc_ds_bytes(jb);
     s.act = o;  o += (uint32_t)nkb * M * 64;        // B fragments, [block][row][4 lanes] x 16 B
     s.meta = o; o += (uint32_t)nkb * NT * 64;       // [block][8-row tile][4 lanes] x {d_a, d_a, C, C}
     s.out = o;  o += (uint32_t)out_tiles * 32 * NT * 16;
@@ -265,12 +270,12 @@ __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const ui
     }
 }
 
-// One job: 8 blocks of the tile in ring stage (sn codes, sd scales) against
+// One job: 16 blocks of the tile in ring stage (sn codes, sd scales) against
 // staged blocks kb .. kb + 7.  acc[nt][i]: rows g, g, g+8, g+8 and columns
 // 8 nt + 2t, +1, +0, +1 (the mma accumulator layout).
 template <int M>
 __device__ __forceinline__ void tc_job(const uint8_t* sn, const uint8_t* sd, const uint8_t* act, const float* meta,
-                                       int kb, int g, int t, float (&acc)[(M + 7) / 8][4])
+                                       int kb, int jb, int g, int t, float (&acc)[(M + 7) / 8][4])
 {
     constexpr int NT = (M + 7) / 8;
     float jacc[NT][4];
@@ -278,15 +283,21 @@ __device__ __forceinline__ void tc_job(const uint8_t* sn, const uint8_t* sd, con
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) jacc[nt][i] = 0.0f;
-    const uint8_t* rg = sn + g * 128 + 4 * t;             // row g; row g + 8 is 1024 B on
-    const uint8_t* dg = sd + (g >> 2) * 64 + (g & 3) * 2;  // its scales; row g + 8's are 128 B on
+    // codes: box h (blocks 8h .. 8h + 7) at sn + 2048 h, row g in line g,
+    // row g + 8 1024 B on; scales: [group][16 blocks][4 rows]
+    const uint8_t* rg = sn + g * 128 + 4 * t;
+    const uint8_t* dg = sd + (g >> 2) * (jb * 8) + (g & 3) * 2;  // row g + 8's are 2 groups on
+#pragma unroll 1
+    for (int p0 = 0; p0 < jb; p0 += TC_LINE_JB)  // one code box at a time
 #pragma unroll
-    for (int p = 0; p < TC_JB; ++p) {
-        const int sw = (p ^ g) << 4;  // 16-byte piece p of line L sits at piece p ^ (L & 7)
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(rg + sw);
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(rg + 1024 + sw);
+    for (int pp = 0; pp < TC_LINE_JB; ++pp) {
+        const int p = p0 + pp;
+        const int sw = (pp ^ g) << 4;  // 16-byte piece pp of line L sits at piece pp ^ (L & 7)
+        const uint8_t* rp = rg + (p0 / TC_LINE_JB) * TC_BOX;
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(rp + sw);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(rp + 1024 + sw);
         const float dwa = __half2float(*reinterpret_cast<const __half*>(dg + p * 8));
-        const float dwb = __half2float(*reinterpret_cast<const __half*>(dg + 128 + p * 8));
+        const float dwb = __half2float(*reinterpret_cast<const __half*>(dg + 2 * jb * 8 + p * 8));
         const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
         const uint32_t A0[4] = {nib_f16x2<0x000F000Fu>(wa), nib_f16x2<0x000F000Fu>(wb), nib_f16x2<0x000F000Fu>(wa8),
                                 nib_f16x2<0x000F000Fu>(wb8)};
@@ -358,12 +369,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int t0 = T < (1 << 24) ? (int)((uint32_t)(cl * T) / (uint32_t)ncl) : (int)((int64_t)cl * T / ncl);
     const int t1 = T < (1 << 24) ? (int)((uint32_t)((cl + 1) * T) / (uint32_t)ncl) : (int)((int64_t)(cl + 1) * T / ncl);
     const int ntile = t1 - t0;
-    const int njb = NB / TC_JB;
+    const int JB = a.jb, NIB = tc_nib_bytes(JB), DSB = tc_ds_bytes(JB);
+    const int JPC = CHUNK / JB, JPC_LOG = JB > TC_LINE_JB ? 1 : 2;  // jobs per 32-block chunk
+    const int njb = NB / JB;
     const int jb0 = rank * njb / C, jb1 = (rank + 1) * njb / C;
     const int jpt = jb1 - jb0;  // jobs per tile
     const int J = ntile * jpt;
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
-    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0);
+    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, a.jb);
     uint8_t* nib = smem + sl.nib;
     uint8_t* ds = smem + sl.ds;
     uint8_t* act = smem + sl.act;
@@ -373,8 +386,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bar);
     uint64_t* wbar = bars + warp * S;
     uint64_t* abar = bars + W * S;  // the activation copy
-    uint8_t* wnib = nib + (size_t)warp * S * TC_NIB;
-    uint8_t* wds = ds + (size_t)warp * S * TC_DS;
+    uint8_t* wnib = nib + (size_t)warp * S * NIB;
+    uint8_t* wds = ds + (size_t)warp * S * DSB;
 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&wbar[s], 1);
@@ -415,13 +428,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         igrp = (isec ? tg - T1 : tg) * (TC_ROWS / GROUP);
     }
     auto issue = [&]() {
-        const int x = ikg & 3, c = ikg >> 2;  // which 8 blocks of which 32-block chunk
+        const int h = ikg & (JPC - 1), c = ikg >> JPC_LOG;  // which JB blocks of which 32-block chunk
         if (lane == 0) {
             uint64_t* bar = &wbar[iss_slot];
+            uint8_t* dst = wnib + (size_t)iss_slot * NIB;
+            const CUtensorMap* map = isec ? &tn1 : &tn0;
             fence_proxy_async();
-            mbar_arrive_expect_tx(bar, TC_NIB + TC_DS);
-            tma_load_4d(wnib + (size_t)iss_slot * TC_NIB, isec ? &tn1 : &tn0, x * 128, 0, c, igrp, bar, pol);
-            tma_load_3d(wds + (size_t)iss_slot * TC_DS, isec ? &td1 : &td0, x * 64, c, igrp, bar, pol);
+            mbar_arrive_expect_tx(bar, NIB + DSB);
+            tma_load_4d(dst, map, h * JB * 16, 0, c, igrp, bar, pol);
+            if (JB > TC_LINE_JB) tma_load_4d(dst + TC_BOX, map, h * JB * 16 + 128, 0, c, igrp, bar, pol);
+            tma_load_3d(wds + (size_t)iss_slot * DSB, isec ? &td1 : &td0, h * JB * 8, c, igrp, bar, pol);
         }
         ++ikg;
         if (++ikj == jpt) {  // next tile
@@ -442,12 +458,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // tile region; the ring starts at once (every earlier kernel's writes are
     // visible from here) and fills while the copy is converted.
     bool alive = true;
-    const uint32_t row_bytes = (uint32_t)jpt * TC_JB * Q8_1_BYTES, rstride = row_bytes + 16;
+    const uint32_t row_bytes = (uint32_t)jpt * JB * Q8_1_BYTES, rstride = row_bytes + 16;
     uint8_t* raw = act + (size_t)a.nkb_max * M * 64 - (size_t)M * rstride;
     if (threadIdx.x == 0 && row_bytes > 0) {
         mbar_arrive_expect_tx(abar, (uint32_t)M * row_bytes);
         for (int n = 0; n < M; ++n)
-            bulk_g2s_plain(raw + (size_t)n * rstride, a.xq + ((int64_t)n * NB + (int64_t)jb0 * TC_JB) * Q8_1_BYTES,
+            bulk_g2s_plain(raw + (size_t)n * rstride, a.xq + ((int64_t)n * NB + (int64_t)jb0 * JB) * Q8_1_BYTES,
                            row_bytes, abar);
     }
     while (issued < n_jobs && issued < S - 1) issue();
@@ -485,7 +501,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         alive = false;
     }
     alive = __syncthreads_and(alive);
-    if (alive) tc_stage_act<M>(act, meta, raw, jpt * TC_JB, (int)rstride);
+    if (alive) tc_stage_act<M>(act, meta, raw, jpt * JB, (int)rstride);
     __syncthreads();  // the tile is built
     float acc[NT][4];
 #pragma unroll
@@ -511,7 +527,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             break;
         }
         ++consumed;
-        tc_job<M>(wnib + (size_t)slot * TC_NIB, wds + (size_t)slot * TC_DS, act, meta, kj * TC_JB, g, t, acc);
+        tc_job<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB, JB, g, t, acc);
         __syncwarp();
         if (++slot == S) {
             slot = 0;

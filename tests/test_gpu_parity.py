@@ -168,11 +168,11 @@ def test_qgemv_q4_0_tensor_core_shapes(ops, M, K, N, tc):
 
 
 def test_qgemv_q4_0_tensor_core_plans(ops):
-    # the shapes above reach every cluster size the planner uses
+    # the shapes above reach K split over clusters (2 and 4 CTAs) and one CTA
     p = ops.qgemv_q4_0_plan(6, 5120, 17408, 17408)
     assert p["tensor_cores"] and p["cluster"] == 1
     assert ops.qgemv_q4_0_plan(6, 17408, 5120)["cluster"] > 1
-    assert ops.qgemv_q4_0_plan(5, 17408, 64)["cluster"] == 8
+    assert ops.qgemv_q4_0_plan(5, 17408, 64)["cluster"] >= 4
     assert not ops.qgemv_q4_0_plan(4, 5120, 17408)["tensor_cores"]  # M < 5: the SIMT kernels
     assert not ops.qgemv_q4_0_plan(6, 5120, 17400)["tensor_cores"]  # N % 16
     assert not ops.qgemv_q4_0_plan(6, 5056, 17408)["tensor_cores"]  # K % 1024
