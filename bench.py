@@ -336,9 +336,23 @@ def run_native(args, rank, world):
     def candmax():
         ops.lmhead_q6_k_candmax(w["w_vocab"], xd_rows, K_H, N_V, cand, ws=ws1)
 
-    ab = {"fused": [], "unfused": [], "candmax": []}
+    # the target side with all six rows fused (no logits) against the step's
+    # unfused target head (quantize + qgemv_q6_k + argmax), same inputs
+    ws6 = torch.zeros(ops.lmhead_q6_k_top1_workspace_bytes(M_T, K_H, N_V), dtype=torch.uint8, device=dev)
+    ids_tf = torch.empty(M_T, dtype=torch.int32, device=dev)
+
+    def target_fused():
+        ops.lmhead_q6_k_top1(w["w_vocab"], xt, K_H, N_V, ids=ids_tf, ws=ws6)
+
+    def target_unfused():
+        ops.quantize_q8_1(xt, out=xq3)
+        ops.qgemv_q6_k(w["w_vocab"], xq3, M_T, K_H, N_V, y=logits)
+        ops.argmax_f32_rows(logits, ids=ids_t, ws=ws2)
+
+    ab = {"fused": [], "unfused": [], "candmax": [], "target_fused": [], "target_unfused": []}
     for _ in range(5):
-        for name, fn in (("fused", fused), ("unfused", unfused), ("candmax", candmax)):
+        for name, fn in (("fused", fused), ("unfused", unfused), ("candmax", candmax), ("target_fused", target_fused),
+                         ("target_unfused", target_unfused)):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for _ in range(10):
@@ -347,6 +361,7 @@ def run_native(args, rank, world):
             torch.cuda.synchronize()
             ab[name].append(a.elapsed_time(b) * 1e3 / 10)
     same_ids = ids_d.cpu().tolist() == ids_u.cpu().tolist()
+    same_ids_t = ids_tf.cpu().tolist() == ids_t.cpu().tolist()
 
     peak, peak_kind = peaks()
     dominant = max(("lmhead_top1", "target_head", "gate_up", "down"), key=lambda n: call_ms[n])
@@ -382,6 +397,9 @@ def run_native(args, rank, world):
                                     "unfused": round(statistics.median(ab["unfused"]), 2),
                                     "same_ids": same_ids},
             "candmax_us": round(statistics.median(ab["candmax"]), 2),
+            "target_m6_fused_vs_unfused_us": {"fused": round(statistics.median(ab["target_fused"]), 2),
+                                              "unfused": round(statistics.median(ab["target_unfused"]), 2),
+                                              "same_ids": same_ids_t},
             "per_call_us": {n: round(call_ms[n] * 1e3, 2) for n in names},
             "per_call_gbs": {n: round(nbytes[n] / (call_ms[n] * 1e-3) / 1e9, 1) for n in names},
             "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,

@@ -43,6 +43,7 @@ SIGNATURES = {
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "qgemv_set_q4_0_tensor_cores": (_I, [_I]),
+    "qgemv_q4_0_residual": (_I, [_P, _P, _P, _L, _P, _L, _I, _I, _I, _P]),
     "qgemv_q4_0_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "lmhead_q6_k_top1_noalloc": (_I, [_P, _P, _L, _P, _I, _I, _I, _P]),
 }
@@ -172,6 +173,19 @@ def qgemv_q4_0(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
                y: torch.Tensor | None = None) -> torch.Tensor:
     """y [M, N] fp32 = Q4_0 weight (packed) x Q8_1 activation."""
     return _gemv("qgemv_q4_0", w_pack, xq, M, K, N, y)
+
+
+def qgemv_q4_0_residual(w_pack: torch.Tensor, xq: torch.Tensor, residual: torch.Tensor, M: int, K: int, N: int,
+                        y: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp32 = Q4_0 weight x Q8_1 activation + residual (fp32 [M, >= N],
+    row stride residual.stride(0)); y may be the residual itself (in-place add)."""
+    assert residual.dtype == torch.float32 and residual.dim() == 2 and residual.stride(1) == 1
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=residual.device)
+    _check("qgemv_q4_0_residual",
+           LIB.qgemv_q4_0_residual(_dev(w_pack, "w_pack"), _dev(xq, "xq"), _dev(residual, "residual"),
+                                   residual.stride(0), _dev(y, "y"), y.stride(0), M, K, N, _stream(y)))
+    return y
 
 
 def qgemv_q4_0_pair(w_a: torch.Tensor, w_b: torch.Tensor, xq: torch.Tensor, M: int, K: int, N_a: int, N_b: int,

@@ -34,6 +34,16 @@ int check_gemv(const void* w, const void* xq, const void* y, int64_t ldy, int M,
 
 size_t top1_ws_bytes() { return sizeof(Top1Workspace); }
 
+// Whether the fp32 matrices [M][lda] at a and [M][ldb] at b share any byte
+// (other than being the same matrix).
+bool ranges_overlap(const float* a, int64_t lda, const float* b, int64_t ldb, int M, int N)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    const uintptr_t a1 = a0 + (uintptr_t)(((int64_t)(M - 1) * lda + N) * 4);
+    const uintptr_t b1 = b0 + (uintptr_t)(((int64_t)(M - 1) * ldb + N) * 4);
+    return a0 < b1 && b0 < a1;
+}
+
 // lmhead workspace: the top-1 keys and counter, then (from byte
 // LMHEAD_Q8_OFFSET) the Q8_1 copy of x that the pre-pass writes.
 constexpr size_t LMHEAD_Q8_OFFSET = 256;
@@ -112,6 +122,28 @@ int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
     const int tc = launch_mmvq_q4_0_tc(a, M, false, as_stream(stream));
     if (tc != TC_NOT_TAKEN) return tc;
     return launch_mmvq_q4_0(a, M, as_stream(stream));
+}
+
+int qgemv_q4_0_residual(const void* w_pack, const void* xq, const float* residual, int64_t ldr, float* y, int64_t ldy,
+                        int M, int K, int N, void* stream)
+{
+    int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK);
+    if (st) return st;
+    if (!residual || ldr < N) return QGEMV_INVALID_ARG;
+    if (!aligned16(residual)) return QGEMV_MISALIGNED;
+    if (residual == y ? ldr != ldy : ranges_overlap(residual, ldr, y, ldy, M, N)) return QGEMV_INVALID_ARG;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.y = y;
+    a.ldy = ldy;
+    a.K = K;
+    a.N = N;
+    a.x = residual;  // the residual instantiations read it from the activation field
+    a.ldx = ldr;
+    const int tc = launch_mmvq_q4_0_tc(a, M, false, as_stream(stream));
+    if (tc != TC_NOT_TAKEN) return tc;
+    return launch_mmvq_q4_0_residual(a, M, as_stream(stream));
 }
 
 int qgemv_q4_0_pair(const void* w_pack_a, const void* w_pack_b, const void* xq, float* y_a, float* y_b, int64_t ldy,
@@ -254,7 +286,7 @@ int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;
     *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() +
-             take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead();
+             take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead();
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

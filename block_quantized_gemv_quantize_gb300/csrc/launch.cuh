@@ -132,7 +132,7 @@ MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N, int N2 = 0)
     return p;
 }
 
-template <int FMT, int M, bool TOP1, bool PAIR>
+template <int FMT, int M, bool TOP1, bool PAIR, bool RES = false>
 int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
 {
     const DeviceInfo di = device_info();
@@ -148,7 +148,7 @@ int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
     static bool opted_ring[64], opted_lock[64];
     static unsigned int* timeouts[64];
     if (p.ring) {
-        auto kern = mmvq_ring_kernel<FMT, M, TOP1, PAIR>;
+        auto kern = mmvq_ring_kernel<FMT, M, TOP1, PAIR, RES>;
         if (!opted_ring[dev]) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
                 return QGEMV_CUDA_ERROR;
@@ -159,7 +159,7 @@ int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
         if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a, timeouts[dev]) != cudaSuccess)
             return QGEMV_CUDA_ERROR;
     } else {
-        auto kern = mmvq_lockstep_kernel<FMT, M, TOP1>;
+        auto kern = mmvq_lockstep_kernel<FMT, M, TOP1, RES>;
         if (!opted_lock[dev]) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
                 return QGEMV_CUDA_ERROR;
@@ -210,6 +210,9 @@ int launch_mmvq_q4_0_tc(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int
 int set_q4_0_tensor_cores(int enable);
 unsigned int take_wait_timeouts_q4_0_tc();
 int launch_mmvq_q4_0_pair(const MmvqArgs& a, int M, cudaStream_t s);
+// y = W x + residual on the SIMT kernels; the residual travels in a.x / a.ldx
+int launch_mmvq_q4_0_residual(const MmvqArgs& a, int M, cudaStream_t s);
+unsigned int take_wait_timeouts_q4_0_residual();
 int launch_mmvq_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 unsigned int take_wait_timeouts_q4_0();

@@ -429,7 +429,7 @@ __device__ __forceinline__ void ring_dot_q6_k(const uint4 (&ql)[R], const uint2 
 struct MmvqArgs {
     const void* w_pack;
     const uint8_t* xq;  // Q8_1 [M][NB]; null (top-1 kernels only): quantize x in the kernel
-    const float* x;     // fp32 [M][ldx] (when xq is null)
+    const float* x;     // fp32 [M][ldx] (when xq is null); the residual of a RES kernel
     int64_t ldx;
     float* y;
     int64_t ldy;
@@ -451,9 +451,19 @@ struct MmvqArgs {
     float* cand_vals;
 };
 
+// Output store of a plain MMVQ; the residual instantiation (RES) adds the
+// residual, which such calls pass in the fp32-activation field x (row stride
+// ldx), as each output is stored (the same thread reads and writes the
+// element, so the residual may be y itself).
+template <bool RES>
+__device__ __forceinline__ void mmvq_store(const MmvqArgs& a, float* y, int m, int64_t n, float v)
+{
+    y[(int64_t)m * a.ldy + n] = RES ? v + a.x[(int64_t)m * a.ldx + n] : v;
+}
+
 // Reduce one row group's partial sums over the warp and write them (TOP1 =
 // false) or fold their keys into the warp's running best per row (TOP1).
-template <int M, int R, bool TOP1>
+template <int M, int R, bool TOP1, bool RES = false>
 __device__ __forceinline__ void finish_rowgroup(const MmvqArgs& a, int n0, float (&acc)[R][M], int lane,
                                                 unsigned long long* wk, unsigned long long& best)
 {
@@ -472,7 +482,7 @@ __device__ __forceinline__ void finish_rowgroup(const MmvqArgs& a, int n0, float
                 if (vi < V) {
                     const int r = vi / M, m = vi - (vi / M) * M;
                     const int n = n0 + r;
-                    if (n < a.N) a.y[(int64_t)m * a.ldy + n] = v[j];
+                    if (n < a.N) mmvq_store<RES>(a, a.y, m, n, v[j]);
                 }
             }
         }
@@ -776,7 +786,7 @@ __device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q6_K>& H, const ui
     }
 }
 
-template <int FMT, int M, bool TOP1, bool PAIR>
+template <int FMT, int M, bool TOP1, bool PAIR, bool RES = false>
 __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
 {
     constexpr int R = R_ROWS;
@@ -1014,7 +1024,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
                     if (key > b) b = key;
                     if (a.cand_vals && n == a.cand[m]) a.cand_vals[m] = v[j];
                 } else {
-                    (PAIR ? sp->y_of(g) : a.y)[(int64_t)m * a.ldy + n] = v[j];
+                    mmvq_store<RES>(a, PAIR ? sp->y_of(g) : a.y, m, n, v[j]);
                 }
             }
         }
@@ -1045,7 +1055,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             if (rr < (PAIR ? sp->rows(g) : L.rows_in(g))) {
                 const int64_t n = (PAIR ? sp->local(g) : g) * GROUP + rr;
                 if (TOP1) atomicMax(&s_best[m], top1_key(sum, (int)n));
-                else (PAIR ? sp->y_of(g) : a.y)[(int64_t)m * a.ldy + n] = sum;
+                else mmvq_store<RES>(a, PAIR ? sp->y_of(g) : a.y, m, n, sum);
             }
         }
     }
@@ -1096,7 +1106,7 @@ inline size_t ring_extra_bytes(int max_groups_per_cta, int P, int warps)
 //   shared memory: aq [M][2][KC] | am [M][KC] | TOP1 scratch
 // ---------------------------------------------------------------------------
 
-template <int FMT, int M, bool TOP1>
+template <int FMT, int M, bool TOP1, bool RES = false>
 __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lockstep_kernel(const MmvqArgs a)
 {
     pdl_launch_dependents();
@@ -1165,7 +1175,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lock
                 }
             }
         }
-        if (active) finish_rowgroup<M, R, TOP1>(a, (int)(g * GROUP), acc, lane, s_keys + warp * 64, best);
+        if (active) finish_rowgroup<M, R, TOP1, RES>(a, (int)(g * GROUP), acc, lane, s_keys + warp * 64, best);
     }
     if (TOP1) top1_finish<M>(a, s_best, s_last, best, lane, warp, W);
 }

@@ -1,0 +1,33 @@
+// Instantiations of the Q4_0 x Q8_1 MMVQ kernels with the residual epilogue
+// (y = W x + residual) for M = 1..17.
+#include "launch.cuh"
+
+namespace qgemv {
+
+int launch_mmvq_q4_0_residual(const MmvqArgs& a, int M, cudaStream_t s)
+{
+    switch (M) {
+    case 1: return launch_mmvq_pm<FMT_Q4_0, 1, false, false, true>(a, s);
+    case 2: return launch_mmvq_pm<FMT_Q4_0, 2, false, false, true>(a, s);
+    case 3: return launch_mmvq_pm<FMT_Q4_0, 3, false, false, true>(a, s);
+    case 4: return launch_mmvq_pm<FMT_Q4_0, 4, false, false, true>(a, s);
+    case 5: return launch_mmvq_pm<FMT_Q4_0, 5, false, false, true>(a, s);
+    case 6: return launch_mmvq_pm<FMT_Q4_0, 6, false, false, true>(a, s);
+    case 7: return launch_mmvq_pm<FMT_Q4_0, 7, false, false, true>(a, s);
+    case 8: return launch_mmvq_pm<FMT_Q4_0, 8, false, false, true>(a, s);
+    case 9: return launch_mmvq_pm<FMT_Q4_0, 9, false, false, true>(a, s);
+    case 10: return launch_mmvq_pm<FMT_Q4_0, 10, false, false, true>(a, s);
+    case 11: return launch_mmvq_pm<FMT_Q4_0, 11, false, false, true>(a, s);
+    case 12: return launch_mmvq_pm<FMT_Q4_0, 12, false, false, true>(a, s);
+    case 13: return launch_mmvq_pm<FMT_Q4_0, 13, false, false, true>(a, s);
+    case 14: return launch_mmvq_pm<FMT_Q4_0, 14, false, false, true>(a, s);
+    case 15: return launch_mmvq_pm<FMT_Q4_0, 15, false, false, true>(a, s);
+    case 16: return launch_mmvq_pm<FMT_Q4_0, 16, false, false, true>(a, s);
+    case 17: return launch_mmvq_pm<FMT_Q4_0, 17, false, false, true>(a, s);
+    default: return QGEMV_UNSUPPORTED_SHAPE;
+    }
+}
+
+unsigned int take_wait_timeouts_q4_0_residual() { return take_wait_timeouts_tu(); }
+
+}  // namespace qgemv

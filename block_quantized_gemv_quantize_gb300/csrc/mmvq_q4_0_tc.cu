@@ -236,6 +236,8 @@ int launch_tc_m(const MmvqArgs& m, cudaStream_t s, int* info)
     a.y = m.y;
     a.y2 = PAIR ? m.y2 : nullptr;
     a.ldy = m.ldy;
+    a.res = PAIR ? nullptr : m.x;  // a residual call passes the residual in the activation field
+    a.ldr = m.ldx;
     a.K = m.K;
     a.N = m.N;
     a.N2 = PAIR ? m.N2 : 0;

@@ -57,6 +57,8 @@ struct TcArgs {
     float* y;           // first weight's output
     float* y2;          // second weight's output (pairs)
     int64_t ldy;
+    const float* res;   // optional residual, y = W x + res (one weight): [M][ldr], may be y
+    int64_t ldr;
     int K, N, N2;       // N, N2 multiples of 16; K a multiple of 1024
     int stages;         // ring stages per warp
     int jb;             // blocks per job (8 or 16)
@@ -335,7 +337,7 @@ __device__ __forceinline__ void tc_store(const TcArgs& a, int64_t T1, int64_t ta
     if (m >= M) return;
     const bool second = tau >= T1;
     const int64_t n = (second ? tau - T1 : tau) * TC_ROWS + (ln >> 2) + (i >> 1) * 8;
-    (second ? a.y2 : a.y)[(int64_t)m * a.ldy + n] = val;
+    (second ? a.y2 : a.y)[(int64_t)m * a.ldy + n] = a.res ? val + a.res[(int64_t)m * a.ldr + n] : val;
 }
 
 template <int M, bool PAIR>

@@ -129,6 +129,23 @@ int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
  *   1 <= M <= 17, K % 256 == 0, N >= 1. */
 int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
 
+/* qgemv_q4_0_residual - qgemv_q4_0 with a residual epilogue:
+ *   y[m][n] = (W x)[m][n] + residual[m * ldr + n],
+ * the sum taken in fp32 when the output is stored (the MMVQ part exactly as
+ * qgemv_q4_0 computes it, then one fp32 addition).  [closure] "Qwen3.6 27B
+ * Q4_0 DFlash/SYCL closure", What did not clear the gate: an MMVQ with a
+ * residual epilogue (the down projection writing its output plus the
+ * residual stream in one pass).
+ *   residual  DEVICE fp32, M rows of N values, row stride ldr >= N; it may be
+ *             y itself (then ldr must equal ldy: an in-place residual add),
+ *             otherwise it must not overlap y;
+ *   other arguments as qgemv_q4_0.
+ * Errors: QGEMV_INVALID_ARG for a null residual, ldr < N, or a residual that
+ * partly overlaps y (or aliases it with ldr != ldy); QGEMV_MISALIGNED if it is
+ * not 16-byte aligned; otherwise as qgemv_q4_0. */
+int qgemv_q4_0_residual(const void* w_pack, const void* xq, const float* residual, int64_t ldr, float* y,
+                        int64_t ldy, int M, int K, int N, void* stream);
+
 /* qgemv_q4_0_pair - qgemv_q4_0 of two weights with the same K against one
  * Q8_1 activation in a single launch (the verifier MLP's gate and up):
  * y_a = W_a x, y_b = W_b x, each exactly as qgemv_q4_0 would compute it.

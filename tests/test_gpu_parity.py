@@ -269,6 +269,48 @@ def test_qgemv_q4_0_pair_padding_untouched_and_errors(ops):
     assert L.qgemv_q4_0_pair(p(wa), p(wb), p(xq), p(ya), p(yb), ldy, 18, K, Na, Nb, None) == -2
 
 
+@pytest.mark.parametrize("M,K,N,inplace", [(6, 5120, 2448, False), (6, 5120, 2448, True), (6, 17408, 320, True),
+                                           (3, 1024, 1001, False), (8, 2048, 96, True), (17, 17408, 64, False)])
+def test_qgemv_q4_0_residual_epilogue(ops, M, K, N, inplace):
+    # y = W x + r: the MMVQ within the fp32 gate, then one fp32 addition
+    x = synth.activations(M, K, seed=M + K, outlier_frac=0.01)
+    w = synth.q4_0_weights(N, K, seed=N + 7)
+    r = (synth.activations(M, N, seed=N + 9) * 3.0).astype(np.float32)
+    xq_ref = oracle.quantize_q8_1(x)
+    y_ref, S = oracle.qgemv_q4_0(w, xq_ref)
+    ldr = N + 8
+    rt = torch.zeros((M, ldr), device=DEV)
+    rt[:, :N] = _t(r)
+    wp, xq = ops.qpack_q4_0(_t(w), N, K), ops.quantize_q8_1(_t(x))
+    if inplace:
+        y = ops.qgemv_q4_0_residual(wp, xq, rt[:, :N], M, K, N, y=rt[:, :N])
+    else:
+        y = ops.qgemv_q4_0_residual(wp, xq, rt[:, :N], M, K, N)
+    yy = _np(y).astype(np.float64)
+    want = y_ref + r.astype(np.float64)
+    tol = 1e-5 * np.maximum(np.abs(y_ref), S) + 2.0 ** -23 * np.abs(want)
+    assert np.all(np.abs(yy - want) <= tol), float(np.max(np.abs(yy - want) - tol))
+    if inplace:
+        assert np.all(_np(rt)[:, N:] == 0.0)
+
+
+def test_qgemv_q4_0_residual_errors(ops):
+    M, K, N = 6, 1024, 64
+    wp = ops.qpack_q4_0(_t(synth.q4_0_weights(N, K, seed=1)), N, K)
+    xq = ops.quantize_q8_1(_t(synth.activations(M, K, seed=2)))
+    buf = torch.zeros((2 * M, 2 * N), device=DEV)
+    L = ops.LIB
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    y, r = buf[:M, :N], buf[M:, :N]
+    ld = buf.stride(0)
+    assert L.qgemv_q4_0_residual(p(wp), p(xq), p(r), ld, p(y), ld, M, K, N, None) == 0
+    assert L.qgemv_q4_0_residual(p(wp), p(xq), None, ld, p(y), ld, M, K, N, None) == -1
+    assert L.qgemv_q4_0_residual(p(wp), p(xq), p(r), N - 1, p(y), ld, M, K, N, None) == -1  # ldr < N
+    assert L.qgemv_q4_0_residual(p(wp), p(xq), p(buf[1:, :N]), ld, p(y), ld, M, K, N, None) == -1  # overlap
+    assert L.qgemv_q4_0_residual(p(wp), p(xq), p(y), N, p(y), ld, M, K, N, None) == -1  # alias, ldr != ldy
+    torch.cuda.synchronize()
+
+
 def test_qgemv_output_stride_and_untouched_padding(ops):
     M, K, N, ldy = 6, 512, 100, 128
     w = synth.q4_0_weights(N, K, seed=5)
