@@ -349,10 +349,21 @@ def run_native(args, rank, world):
         ops.qgemv_q6_k(w["w_vocab"], xq3, M_T, K_H, N_V, y=logits)
         ops.argmax_f32_rows(logits, ids=ids_t, ws=ws2)
 
-    ab = {"fused": [], "unfused": [], "candmax": [], "target_fused": [], "target_unfused": []}
+    # RMSNorm fused into the Q8_1 quantizer against the quantizer alone, on
+    # the gate/up input rows [6, 5120]
+    gamma = torch.linspace(0.5, 1.5, K_H, device=dev)
+
+    def rms_q8():
+        ops.rmsnorm_quantize_q8_1(x, gamma, 1e-6, out=xq1)
+
+    def q8_only():
+        ops.quantize_q8_1(x, out=xq1)
+
+    ab = {"fused": [], "unfused": [], "candmax": [], "target_fused": [], "target_unfused": [], "rms_q8": [],
+          "q8_only": []}
     for _ in range(5):
         for name, fn in (("fused", fused), ("unfused", unfused), ("candmax", candmax), ("target_fused", target_fused),
-                         ("target_unfused", target_unfused)):
+                         ("target_unfused", target_unfused), ("rms_q8", rms_q8), ("q8_only", q8_only)):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for _ in range(10):
@@ -397,6 +408,8 @@ def run_native(args, rank, world):
                                     "unfused": round(statistics.median(ab["unfused"]), 2),
                                     "same_ids": same_ids},
             "candmax_us": round(statistics.median(ab["candmax"]), 2),
+            "rmsnorm_q8_1_vs_quantize_us": {"rmsnorm_q8_1": round(statistics.median(ab["rms_q8"]), 2),
+                                            "quantize_q8_1": round(statistics.median(ab["q8_only"]), 2)},
             "target_m6_fused_vs_unfused_us": {"fused": round(statistics.median(ab["target_fused"]), 2),
                                               "unfused": round(statistics.median(ab["target_unfused"]), 2),
                                               "same_ids": same_ids_t},

@@ -43,6 +43,7 @@ SIGNATURES = {
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "qgemv_set_q4_0_tensor_cores": (_I, [_I]),
+    "rmsnorm_quantize_q8_1": (_I, [_P, _L, _P, ctypes.c_float, _P, _I, _I, _P]),
     "qgemv_q4_0_residual": (_I, [_P, _P, _P, _L, _P, _L, _I, _I, _I, _P]),
     "qgemv_q4_0_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "lmhead_q6_k_top1_noalloc": (_I, [_P, _P, _L, _P, _I, _I, _I, _P]),
@@ -143,6 +144,20 @@ def quantize_q8_1(x: torch.Tensor, K: int | None = None, out: torch.Tensor | Non
     if out is None:
         out = torch.empty((M, q8_1_bytes(1, K)), dtype=torch.uint8, device=x.device)
     _check("quantize_q8_1", LIB.quantize_q8_1(_dev(x, "x"), x.stride(0), _dev(out, "xq"), M, K, _stream(x)))
+    return out
+
+
+def rmsnorm_quantize_q8_1(x: torch.Tensor, gamma: torch.Tensor, eps: float, K: int | None = None,
+                          out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32 x [M, ldx] -> Q8_1 of RMSNorm(x) * gamma, uint8 [M, K/32*36]."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    assert gamma.dtype == torch.float32 and gamma.is_contiguous()
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    if out is None:
+        out = torch.empty((M, q8_1_bytes(1, K)), dtype=torch.uint8, device=x.device)
+    _check("rmsnorm_quantize_q8_1", LIB.rmsnorm_quantize_q8_1(_dev(x, "x"), x.stride(0), _dev(gamma, "gamma"), eps,
+                                                              _dev(out, "xq"), M, K, _stream(x)))
     return out
 
 

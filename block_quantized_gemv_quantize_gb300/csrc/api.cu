@@ -92,6 +92,18 @@ int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* str
     return launch_quantize_q8_1(x, ldx, xq, M, K, as_stream(stream));
 }
 
+int rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, void* xq, int M, int K,
+                          void* stream)
+{
+    if (!x || !gamma || !xq) return QGEMV_INVALID_ARG;
+    int st = check_mk(M, K, QK);
+    if (st) return st;
+    if (ldx < K || !(eps >= 0.0f) || eps > 3.0e38f) return QGEMV_INVALID_ARG;
+    if (K >= (1 << 24)) return QGEMV_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(xq)) return QGEMV_MISALIGNED;
+    return launch_rmsnorm_quantize_q8_1(x, ldx, gamma, eps, xq, M, K, as_stream(stream));
+}
+
 int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
 {
     if (!w_canon || !w_pack || N < 1 || K < QK) return QGEMV_INVALID_ARG;

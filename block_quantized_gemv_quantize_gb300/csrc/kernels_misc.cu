@@ -74,6 +74,70 @@ int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cu
 }
 
 // ---------------------------------------------------------------------------
+// RMSNorm fused with the Q8_1 quantizer ("Qwen3.6 27B Q4_0 DFlash/SYCL
+// closure", What did not clear the gate: the down-to-next-RMSNorm/Q8
+// boundary): one CTA of RMS_THREADS threads per row,
+//   S = sum_k x_k^2 in fp32: thread t adds x_k * x_k for k = t, t + 512, ...
+//       in increasing k (separate multiply and add, no contraction), then the
+//       512 partial sums are added pairwise, t += t + h for h = 256, ..., 1;
+//   r = 1 / sqrt(S / K + eps), x^_k = (x_k * r) * gamma_k, all fp32 IEEE;
+// and x^ is quantized to Q8_1 exactly as quantize_q8_1 does.
+// ---------------------------------------------------------------------------
+
+constexpr int RMS_THREADS = 512;
+
+__global__ void __launch_bounds__(RMS_THREADS) rmsnorm_quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
+                                                                          const float* __restrict__ gamma, float eps,
+                                                                          uint8_t* __restrict__ xq, int K)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ float part[RMS_THREADS];
+    __shared__ float s_r;
+    const int m = blockIdx.x, t = threadIdx.x;
+    const float* xr = x + (int64_t)m * ldx;
+    float s = 0.0f;
+    for (int k = t; k < K; k += RMS_THREADS) s = __fadd_rn(s, __fmul_rn(xr[k], xr[k]));
+    part[t] = s;
+    for (int h = RMS_THREADS / 2; h > 0; h >>= 1) {
+        __syncthreads();
+        if (t < h) part[t] = __fadd_rn(part[t], part[t + h]);
+    }
+    if (t == 0) s_r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(part[0], (float)K), eps)));
+    __syncthreads();
+    const float r = s_r;
+    const int NB = K / QK, lane = t & 31, sub = lane & 7;
+    const bool vec4 = ((reinterpret_cast<uintptr_t>(xr) | reinterpret_cast<uintptr_t>(gamma)) & 15u) == 0;
+    for (int b0 = (t >> 5) * 4; b0 < NB; b0 += (RMS_THREADS / 32) * 4) {  // warp-uniform: 4 blocks per warp step
+        const int mine = b0 + (lane >> 3);
+        const int b = mine < NB ? mine : NB - 1;  // spare lanes redo the last block, unwritten
+        const float4 xv = load_4_values(xr + (int64_t)b * QK + 4 * sub, vec4);
+        const float4 gv = load_4_values(gamma + (int64_t)b * QK + 4 * sub, vec4);
+        const float4 v = make_float4(__fmul_rn(__fmul_rn(xv.x, r), gv.x), __fmul_rn(__fmul_rn(xv.y, r), gv.y),
+                                     __fmul_rn(__fmul_rn(xv.z, r), gv.z), __fmul_rn(__fmul_rn(xv.w, r), gv.w));
+        const Q81Lanes o = q8_1_quantize_8lanes(v);
+        if (mine < NB) {
+            uint32_t* blk = reinterpret_cast<uint32_t*>(xq + ((int64_t)m * NB + mine) * Q8_1_BYTES);
+            blk[1 + sub] = o.word;
+            if (sub == 0) {
+                const __half d16 = __float2half_rn(o.d);
+                const __half s16 = __float2half_rn(__fmul_rn(o.d, (float)o.s_all));
+                blk[0] = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(s16) << 16);
+            }
+        }
+    }
+}
+
+int launch_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, void* xq, int M, int K,
+                                 cudaStream_t s)
+{
+    if (launch_pdl(rmsnorm_quantize_q8_1_kernel, dim3(M), dim3(RMS_THREADS), 0, s, x, ldx, gamma, eps,
+                   static_cast<uint8_t*>(xq), K) != cudaSuccess)
+        return QGEMV_CUDA_ERROR;
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+// ---------------------------------------------------------------------------
 // Repackers: canonical blocks -> coalesced streams.  Pure bit moves; fp16
 // scales are copied as raw bits ("Qwen3.6 27B Q4_0 DFlash/SYCL closure",
 // Transfer, rule 7: converting fp16 storage objects numerically once produced

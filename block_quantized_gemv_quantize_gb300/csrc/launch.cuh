@@ -221,6 +221,8 @@ unsigned int take_wait_timeouts_q6_k();
 unsigned int take_wait_timeouts_lmhead();
 
 int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cudaStream_t s);
+int launch_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, void* xq, int M, int K,
+                                 cudaStream_t s);
 int launch_qpack_q4_0(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_qpack_q6_k(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int M, int N, cudaStream_t s);

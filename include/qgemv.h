@@ -86,6 +86,28 @@ size_t argmax_f32_rows_workspace_bytes(int M, int N);
  * calls. */
 int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* stream);
 
+/* rmsnorm_quantize_q8_1 - RMSNorm fused with the Q8_1 quantizer: the rows of
+ * x normalized by their RMS and scaled by gamma, written as Q8_1 without an
+ * fp32 copy.  [closure] "Qwen3.6 27B Q4_0 DFlash/SYCL closure", What did not
+ * clear the gate: the down-to-next-RMSNorm/Q8 boundary (RMSNorm fused with
+ * the Q8 quantization).  Exact contract (all fp32, round to nearest, no
+ * fused multiply-add), per row:
+ *   s_t = sum over k = t, t + 512, ... < K, in increasing k, of x_k * x_k
+ *         (t = 0..511, each added as s_t = s_t + (x_k * x_k));
+ *   for h = 256, 128, ..., 1: s_t = s_t + s_{t+h} for t < h;   S = s_0;
+ *   r = 1 / sqrt(S / K + eps);   xh_k = (x_k * r) * gamma_k;
+ * then xq = quantize_q8_1(xh), bit for bit.  (The reduction order is part of
+ * the definition so that the Q8_1 codes are reproducible.)
+ *   x      fp32 [M][ldx] device, ldx >= K      (read)
+ *   gamma  fp32 [K] device                      (read)
+ *   eps    finite, >= 0
+ *   xq     uint8 [M][K/32][36] device           (written)
+ *   1 <= M <= 17, K % 32 == 0, 32 <= K < 2^24.
+ * Errors: QGEMV_INVALID_ARG (null pointer, ldx < K, bad eps),
+ * QGEMV_UNSUPPORTED_SHAPE (M, K), QGEMV_MISALIGNED. */
+int rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, void* xq, int M, int K,
+                          void* stream);
+
 /* ---- A2: weight repackers (offline) ------------------------------------ */
 
 /* qpack_q4_0 - reorder canonical Q4_0 blocks into the kernel's tiles: each

@@ -140,6 +140,43 @@ void oracle_quantize_q8_1(const float* x, int64_t ldx, int M, int K, uint8_t* ou
     }
 }
 
+/* RMSNorm fused with the Q8_1 quantizer, the contract of the library's
+ * rmsnorm_quantize_q8_1 ("Qwen3.6 27B Q4_0 DFlash/SYCL closure", What did not
+ * clear the gate: the down-to-next-RMSNorm/Q8 boundary), step by step in fp32
+ * (this file is compiled without contraction): the sum of squares over 512
+ * strided slices in increasing k, the slices added pairwise (h = 256 .. 1),
+ * r = 1 / sqrt(S / K + eps), xh_k = (x_k * r) * gamma_k, then the Q8_1
+ * quantization of xh above. */
+void oracle_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, int M, int K,
+                                  uint8_t* out)
+{
+    enum { T = 512 };
+    float part[T];
+    float* xh = (float*)malloc(sizeof(float) * (size_t)K);
+    if (!xh) return;
+    for (int m = 0; m < M; ++m) {
+        const float* xr = x + (int64_t)m * ldx;
+        for (int t = 0; t < T; ++t) {
+            float s = 0.0f;
+            for (int k = t; k < K; k += T) {
+                const float sq = xr[k] * xr[k];
+                s = s + sq;
+            }
+            part[t] = s;
+        }
+        for (int h = T / 2; h > 0; h >>= 1)
+            for (int t = 0; t < h; ++t) part[t] = part[t] + part[t + h];
+        const float mean = part[0] / (float)K;
+        const float r = 1.0f / sqrtf(mean + eps);
+        for (int k = 0; k < K; ++k) {
+            const float a = xr[k] * r;
+            xh[k] = a * gamma[k];
+        }
+        oracle_quantize_q8_1(xh, K, 1, K, out + (int64_t)m * (K / 32) * Q8_1_BYTES);
+    }
+    free(xh);
+}
+
 /* ------------------------------------------------------------------ */
 /* Weight decoding from the canonical block bytes                        */
 /* ------------------------------------------------------------------ */

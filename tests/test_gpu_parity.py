@@ -311,6 +311,34 @@ def test_qgemv_q4_0_residual_errors(ops):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("M,K,ldx,eps", [(1, 32, 32, 1e-6), (6, 5120, 5120, 1e-5), (6, 17408, 17416, 1e-6),
+                                         (17, 1024, 1024, 0.0), (3, 96, 100, 1e-3)])
+def test_rmsnorm_quantize_q8_1_bit_exact(ops, M, K, ldx, eps):
+    g = np.random.default_rng(M * 7 + K)
+    x = (g.standard_normal((M, ldx)) * g.uniform(0.1, 10.0, (M, 1))).astype(np.float32)
+    gamma = g.uniform(-2.0, 2.0, K).astype(np.float32)
+    ref = oracle.rmsnorm_quantize_q8_1(x, gamma, eps, K=K)
+    got = _np(ops.rmsnorm_quantize_q8_1(_t(x), _t(gamma), eps, K=K)).reshape(M, K // 32, 36)
+    assert np.array_equal(got, ref)
+
+
+def test_rmsnorm_quantize_q8_1_errors(ops):
+    x, gamma = torch.zeros((2, 64), device=DEV), torch.ones(64, device=DEV)
+    xq = torch.empty(ops.q8_1_bytes(2, 64), dtype=torch.uint8, device=DEV)
+    L = ops.LIB
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    assert L.rmsnorm_quantize_q8_1(p(x), 64, p(gamma), 1e-6, p(xq), 2, 64, None) == 0
+    assert L.rmsnorm_quantize_q8_1(p(x), 64, None, 1e-6, p(xq), 2, 64, None) == -1
+    assert L.rmsnorm_quantize_q8_1(p(x), 32, p(gamma), 1e-6, p(xq), 2, 64, None) == -1  # ldx < K
+    assert L.rmsnorm_quantize_q8_1(p(x), 64, p(gamma), -1.0, p(xq), 2, 64, None) == -1  # eps < 0
+    assert L.rmsnorm_quantize_q8_1(p(x), 64, p(gamma), 1e-6, p(xq), 18, 64, None) == -2  # M > 17
+    assert L.rmsnorm_quantize_q8_1(p(x), 64, p(gamma), 1e-6, p(xq), 2, 48, None) == -2  # K % 32
+    torch.cuda.synchronize()
+    # the accepted call: zero rows with eps > 0 normalize to zero, the
+    # quantizer's all-zero blocks
+    assert np.all(_np(xq) == 0)
+
+
 def test_qgemv_output_stride_and_untouched_padding(ops):
     M, K, N, ldy = 6, 512, 100, 128
     w = synth.q4_0_weights(N, K, seed=5)
