@@ -43,6 +43,9 @@ SIGNATURES = {
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "qgemv_set_q4_0_tensor_cores": (_I, [_I]),
+    "q8_0_pack_bytes": (_S, [_I, _I]),
+    "qpack_q8_0": (_I, [_P, _P, _I, _I, _P]),
+    "qgemv_q8_0": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
     "rmsnorm_quantize_q8_1": (_I, [_P, _L, _P, ctypes.c_float, _P, _I, _I, _P]),
     "qgemv_q4_0_residual": (_I, [_P, _P, _P, _L, _P, _L, _I, _I, _I, _P]),
     "qgemv_q4_0_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
@@ -188,6 +191,24 @@ def qgemv_q4_0(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
                y: torch.Tensor | None = None) -> torch.Tensor:
     """y [M, N] fp32 = Q4_0 weight (packed) x Q8_1 activation."""
     return _gemv("qgemv_q4_0", w_pack, xq, M, K, N, y)
+
+
+def q8_0_pack_bytes(N: int, K: int) -> int:
+    return LIB.q8_0_pack_bytes(N, K)
+
+
+def qpack_q8_0(w_canon: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """canonical Q8_0 bytes [N, K/32, 34] -> the tensor-core pack."""
+    if out is None:
+        out = torch.empty(q8_0_pack_bytes(N, K), dtype=torch.uint8, device=w_canon.device)
+    _check("qpack_q8_0", LIB.qpack_q8_0(_dev(w_canon, "w_canon"), _dev(out, "w_pack"), N, K, _stream(w_canon)))
+    return out
+
+
+def qgemv_q8_0(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
+               y: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp32 = Q8_0 weight (packed) x Q8_1 activation."""
+    return _gemv("qgemv_q8_0", w_pack, xq, M, K, N, y)
 
 
 def qgemv_q4_0_residual(w_pack: torch.Tensor, xq: torch.Tensor, residual: torch.Tensor, M: int, K: int, N: int,

@@ -75,6 +75,12 @@ size_t q4_0_pack_bytes(int N, int K)
 {
     return (N < 1 || K < QK) ? 0 : (size_t)make_layout(FMT_Q4_0, N, K).total_bytes();
 }
+size_t q8_0_pack_bytes(int N, int K)
+{
+    if (N < 1 || K < 256 || K % 256) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)(K / 256) * 4352;
+}
+
 size_t q6_k_pack_bytes(int N, int K)
 {
     return (N < 1 || K < QK_K) ? 0 : (size_t)make_layout(FMT_Q6_K, N, K).total_bytes();
@@ -102,6 +108,28 @@ int rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float
     if (K >= (1 << 24)) return QGEMV_UNSUPPORTED_SHAPE;
     if (!aligned16(x) || !aligned16(gamma) || !aligned16(xq)) return QGEMV_MISALIGNED;
     return launch_rmsnorm_quantize_q8_1(x, ldx, gamma, eps, xq, M, K, as_stream(stream));
+}
+
+int qpack_q8_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
+{
+    if (!w_canon || !w_pack || N < 1 || K < 256) return QGEMV_INVALID_ARG;
+    if (K % 256) return QGEMV_UNSUPPORTED_SHAPE;
+    if (!aligned16(w_pack) || (reinterpret_cast<uintptr_t>(w_canon) & 1u)) return QGEMV_MISALIGNED;
+    return launch_qpack_q8_0(w_canon, w_pack, N, K, as_stream(stream));
+}
+
+int qgemv_q8_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
+{
+    int st = check_gemv(w_pack, xq, y, ldy, M, K, N, 256);
+    if (st) return st;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.y = y;
+    a.ldy = ldy;
+    a.K = K;
+    a.N = N;
+    return launch_mmvq_q8_0(a, M, as_stream(stream));
 }
 
 int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
@@ -298,7 +326,8 @@ int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;
     *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() +
-             take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead();
+             take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead() +
+             take_wait_timeouts_q8_0();
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

@@ -144,6 +144,56 @@ int launch_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma
 // an all-zero kernel).
 // ---------------------------------------------------------------------------
 
+// Q8_0 pack for the tensor-core kernel: per 16-row tile and job of 8 blocks
+// one 4352-byte region = codes [block p][lane l = 4g + t][16 B] then scales
+// [block p][row r] (fp16 bits).  Lane l's 16 bytes are values 2t, 2t+1,
+// 2t+8, 2t+9, 16+2t, 17+2t, 24+2t, 25+2t of row g, then of row g + 8, each
+// stored as q + 128 (q ^ 0x80).  Rows past N are zero codes and zero scales.
+// One thread per (tile, block, lane); scales are raw bit copies.
+__global__ void qpack_q8_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
+{
+    const int NB = K / QK, NJ = NB / 8;
+    const int64_t T = (N + 15) / 16;
+    const int64_t total = T * NB * 32;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int l = (int)(i & 31);
+        const int64_t tb = i >> 5;
+        const int64_t tau = tb / NB;
+        const int b = (int)(tb - tau * NB), j = b / 8, p = b % 8;
+        const int g = l >> 2, t = l & 3;
+        uint8_t* region = pack + (tau * NJ + j) * 4352;
+        uint32_t words[4];
+        for (int h = 0; h < 2; ++h) {
+            const int64_t n = tau * 16 + g + 8 * h;
+            const uint8_t* q = canon + (n * NB + b) * 34 + 2;
+            const int e[8] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9, 16 + 2 * t, 17 + 2 * t, 24 + 2 * t, 25 + 2 * t};
+            uint32_t w0 = 0, w1 = 0;
+            for (int k = 0; k < 4; ++k) {
+                w0 |= (uint32_t)((n < N ? q[e[k]] : 0) ^ 0x80u) << (8 * k);
+                w1 |= (uint32_t)((n < N ? q[e[k + 4]] : 0) ^ 0x80u) << (8 * k);
+            }
+            words[2 * h] = w0;
+            words[2 * h + 1] = w1;
+        }
+        *reinterpret_cast<uint4*>(region + (p * 32 + l) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+        if (l < 16) {
+            const int64_t n = tau * 16 + l;
+            const uint16_t d = n < N ? *reinterpret_cast<const uint16_t*>(canon + (n * NB + b) * 34) : (uint16_t)0;
+            *reinterpret_cast<uint16_t*>(region + 4096 + (p * 16 + l) * 2) = d;
+        }
+    }
+}
+
+int launch_qpack_q8_0(const void* canon, void* pack, int N, int K, cudaStream_t s)
+{
+    const int64_t total = (int64_t)((N + 15) / 16) * (K / QK) * 32;
+    const int64_t grid = total / 256 + 1 < 65535 ? total / 256 + 1 : 65535;
+    qpack_q8_0_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon), static_cast<uint8_t*>(pack),
+                                                     N, K);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
 __global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
 {
     const Layout L = make_layout(FMT_Q4_0, N, K);

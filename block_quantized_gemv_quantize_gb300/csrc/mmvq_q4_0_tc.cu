@@ -5,8 +5,7 @@
 
 #include <atomic>
 
-#include "launch.cuh"
-#include "mmvq_tc.cuh"
+#include "mmvq_tc_host.cuh"
 
 namespace qgemv {
 
@@ -67,143 +66,6 @@ bool q4_0_tensor_maps(const void* w, int N, int K, int jb, CUtensorMap* nib, CUt
     return true;
 }
 
-struct TcPlan {
-    int C, grid, S, jb, nkb_max, out_tiles;
-    size_t smem;
-};
-
-constexpr int TC_CLUSTERS[4] = {1, 2, 4, 8};
-
-template <int M, bool PAIR>
-cudaError_t tc_launch(const TcPlan& p, const TcArgs& a, const CUtensorMap& n0, const CUtensorMap& d0,
-                      const CUtensorMap& n1, const CUtensorMap& d1, unsigned int* timeouts, cudaStream_t s)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.grid);
-    cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    int na = 1;
-    if (p.C > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = p.C;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        na = 2;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, mmvq_q4_0_tc_kernel<M, PAIR>, a, n0, d0, n1, d1, timeouts);
-}
-
-// Clusters of C CTAs of this kernel (one per SM) that can be resident at once.
-template <int M, bool PAIR>
-int tc_max_clusters(int dev, int ci, size_t smem)
-{
-    static int cache[64][4];
-    static bool have[64][4];
-    if (!have[dev][ci]) {
-        const int C = TC_CLUSTERS[ci];
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(C);
-        cfg.blockDim = dim3(TC_THREADS);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mmvq_q4_0_tc_kernel<M, PAIR>, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            n = 0;
-        }
-        cache[dev][ci] = n;
-        have[dev][ci] = true;
-    }
-    return cache[dev][ci];
-}
-
-// The cheapest plan over job sizes JB (16 or 8 blocks) and cluster sizes C:
-// the largest per-CTA job count over 16 warps (the critical path) in units of
-// 8 blocks, where a 16-block job counts 0.85 x 2 units (measured: it halves
-// the per-job copy issue and loop overhead), plus two units for the
-// cross-CTA combine when C > 1.  Returns false when nothing fits.
-template <int M, bool PAIR>
-bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
-{
-    const int W = TC_THREADS / 32;
-    const int NB = K / QK;
-    const int64_t T = N / TC_ROWS + (PAIR ? N2 / TC_ROWS : 0);
-    double best_cost = 0.0;
-    bool found = false;
-    for (int jb = 2 * TC_LINE_JB; jb >= TC_LINE_JB; jb -= TC_LINE_JB) {
-        const int njb = NB / jb;
-        for (int ci = 0; ci < 4; ++ci) {
-            const int C = TC_CLUSTERS[ci];
-            if (njb < C) break;
-            const int jpt = (njb + C - 1) / C;
-            const int nkb = jpt * jb;
-            if (nkb * ((M + 7) / 8) * 8 > tc_stage_items(M) * TC_THREADS) continue;  // staging items per thread
-            // shared memory at the deepest ring that fits
-            int64_t ncl = C == 1 ? di.sms : 0;
-            if (C > 1) {
-                if (tc_smem(M, W, 2, nkb, 0, jb).bytes > (uint32_t)di.smem_optin) continue;
-                ncl = tc_max_clusters<M, PAIR>(dev, ci, (size_t)di.smem_optin);
-                if (ncl <= 0) continue;
-            }
-            if (ncl > T) ncl = T;
-            const int tiles = (int)((T + ncl - 1) / ncl);
-            const int out_tiles = C > 1 ? tiles : 0;
-            int S = 0;
-            for (int s = TC_MAX_STAGES; s >= 2; --s) {
-                if (tc_smem(M, W, s, nkb, out_tiles, jb).bytes <= (uint32_t)di.smem_optin) {
-                    S = s;
-                    break;
-                }
-            }
-            if (S == 0) continue;
-            const double unit = jb > TC_LINE_JB ? 0.85 * jb / TC_LINE_JB : 1.0;
-            const double cost = (double)(((int64_t)tiles * jpt + W - 1) / W) * unit + (C > 1 ? 2.0 : 0.0);
-            if (!found || cost < best_cost - 1e-9) {
-                found = true;
-                best_cost = cost;
-                best.C = C;
-                best.grid = (int)(ncl * C);
-                best.S = S;
-                best.jb = jb;
-                best.nkb_max = nkb;
-                best.out_tiles = out_tiles;
-                best.smem = tc_smem(M, W, S, nkb, out_tiles, jb).bytes;
-            }
-        }
-    }
-    return found;
-}
-
-// Opt the kernel in to the device's full shared memory (once per device);
-// returns the device's timeout counter, or null on failure.
-template <int M, bool PAIR>
-unsigned int* tc_prepare(const DeviceInfo& di, int dev)
-{
-    static bool opted[64];
-    static unsigned int* timeouts[64];
-    if (!opted[dev]) {
-        if (cudaFuncSetAttribute(mmvq_q4_0_tc_kernel<M, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 di.smem_optin) != cudaSuccess)
-            return nullptr;
-        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) != cudaSuccess)
-            return nullptr;
-        opted[dev] = true;
-    }
-    return timeouts[dev];
-}
-
 // info (when not null): {1, cluster size, grid, ring stages} of the plan.
 template <int M, bool PAIR>
 int launch_tc_m(const MmvqArgs& m, cudaStream_t s, int* info)
@@ -212,10 +74,10 @@ int launch_tc_m(const MmvqArgs& m, cudaStream_t s, int* info)
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QGEMV_CUDA_ERROR;
-    unsigned int* timeouts = tc_prepare<M, PAIR>(di, dev);
+    unsigned int* timeouts = tc_prepare<TCF_Q4_0, M, PAIR>(di, dev);
     if (!timeouts) return QGEMV_CUDA_ERROR;
     TcPlan p{};
-    if (!tc_plan<M, PAIR>(di, dev, m.K, m.N, PAIR ? m.N2 : 0, p)) return TC_NOT_TAKEN;
+    if (!tc_plan<TCF_Q4_0, M, PAIR>(di, dev, m.K, m.N, PAIR ? m.N2 : 0, p)) return TC_NOT_TAKEN;
     if (info) {
         info[0] = 1;
         info[1] = p.C;
@@ -245,7 +107,7 @@ int launch_tc_m(const MmvqArgs& m, cudaStream_t s, int* info)
     a.jb = p.jb;
     a.nkb_max = p.nkb_max;
     a.out_tiles = p.out_tiles;
-    if (tc_launch<M, PAIR>(p, a, n0, d0, n1, d1, timeouts, s) != cudaSuccess) return QGEMV_CUDA_ERROR;
+    if (tc_launch<TCF_Q4_0, M, PAIR>(p, a, n0, d0, n1, d1, timeouts, s) != cudaSuccess) return QGEMV_CUDA_ERROR;
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

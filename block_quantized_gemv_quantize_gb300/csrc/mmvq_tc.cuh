@@ -49,6 +49,11 @@ constexpr int TC_BOX = TC_ROWS * TC_LINE_JB * 16;  // 2048 B: one code box (16 r
 __host__ __device__ inline int tc_nib_bytes(int jb) { return TC_ROWS * jb * 16; }
 __host__ __device__ inline int tc_ds_bytes(int jb) { return TC_ROWS * jb * 2; }
 constexpr int TC_THREADS = 512;
+// Weight formats of the tensor-core kernel: Q4_0 (the existing pack, read by
+// tensor maps) and Q8_0 (its own pack, one contiguous region per job).
+enum TcFormat { TCF_Q4_0 = 0, TCF_Q8_0 = 2 };
+constexpr int TC_Q8_0_CODES = TC_ROWS * 8 * 32;            // 4096 B: 16 rows x 8 blocks of int8 codes
+constexpr int TC_Q8_0_JOB = TC_Q8_0_CODES + TC_ROWS * 8 * 2;  // + 256 B of scales = 4352 B
 constexpr int TC_MIN_M = 5;  // activation rows from which the tensor-core path is taken
 constexpr int TC_MAX_STAGES = 6;
 
@@ -59,7 +64,9 @@ struct TcArgs {
     int64_t ldy;
     const float* res;   // optional residual, y = W x + res (one weight): [M][ldr], may be y
     int64_t ldr;
-    int K, N, N2;       // N, N2 multiples of 16; K a multiple of 1024
+    const uint8_t* w0;  // Q8_0: the packed weights (the copies read them directly)
+    const uint8_t* w1;
+    int K, N, N2;       // Q4_0: N, N2 multiples of 16 and K of 1024; Q8_0: K a multiple of 256
     int stages;         // ring stages per warp
     int jb;             // blocks per job (8 or 16)
     int nkb_max;        // activation blocks staged per CTA (the largest K part)
@@ -73,13 +80,14 @@ struct TcSmem {
 
 constexpr int TC_TAB_INTS = 4 + 3 * (TC_THREADS / 32);  // the split-tile table
 
-__host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_tiles, int jb)
+// nibs / dsb: bytes of a ring stage's codes / scales (Q8_0: the whole job / 0)
+__host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_tiles, int nibs, int dsb)
 {
     const uint32_t NT = (uint32_t)(M + 7) / 8;
     TcSmem s;
     uint32_t o = 0;
-    s.nib = o;  o += (uint32_t)W * S * tc_nib_bytes(jb);  // 1024-byte aligned stages (128-byte swizzle atoms)
-    s.ds = o;   o += (uint32_t)W * S * tc_ds_bytes(jb);
+    s.nib = o;  o += (uint32_t)W * S * nibs;  // Q4_0: 1024-byte aligned stages (128-byte swizzle atoms)
+    s.ds = o;   o += (uint32_t)W * S * dsb;
     s.act = o;  o += (uint32_t)nkb * M * 64;        // B fragments, [block][row][4 lanes] x 16 B
     s.meta = o; o += (uint32_t)nkb * NT * 64;       // [block][8-row tile][4 lanes] x {d_a, d_a, C, C}
     s.out = o;  o += (uint32_t)out_tiles * 32 * NT * 16;
@@ -326,6 +334,121 @@ __device__ __forceinline__ void tc_job(const uint8_t* sn, const uint8_t* sd, con
         for (int i = 0; i < 4; ++i) acc[nt][i] += jacc[nt][i];
 }
 
+// ---------------------------------------------------------------------------
+// Q8_0 (fp16 d, int8 q[32], value d * q).  Its pack (qpack_q8_0) is built for
+// this kernel: per 16-row tile, per job of 8 blocks one contiguous 4352-byte
+// region = codes [block p][lane l][16 B] then scales [block p][row r] fp16,
+// where lane l = 4g + t holds, as q + 128, values
+//   2t, 2t+1, 2t+8, 2t+9, 16+2t, 17+2t, 24+2t, 25+2t
+// of row g (bytes 0..7) and of row g + 8 (bytes 8..15): exactly its A
+// fragments of the block's two m16n8k16 steps in natural K order, so one
+// 16-byte load and one byte permute + one f16 subtract per register build them.
+// The activation is staged in the same natural order, the accumulator starts
+// at 0, and the block dot sum q_w q_a is exact (|partial sums| < 2^19).
+// ---------------------------------------------------------------------------
+
+// Bytes 0, 1 (sel 0x4140) or 2, 3 (sel 0x4342) of a word of biased codes
+// (q + 128) as the f16x2 (q, q'), exactly: 0x6400 | (q + 128) is 1152 + q.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t q8u_f16x2(uint32_t w)
+{
+    const uint32_t b = __byte_perm(w, 0x64646464u, SEL);
+    const __half2 h = *reinterpret_cast<const __half2*>(&b);
+    const __half2 r = __hsub2(h, __float2half2_rn(1152.0f));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// The activation for Q8_0: B fragments in natural K order, lane t of (block
+// b, row n): (x[2t], x[2t+1]), (x[2t+8], x[2t+9]), (x[16+2t], ..), (x[24+2t], ..);
+// meta {d_a, d_a', 0, 0}.  Same items and two phases as tc_stage_act.
+template <int M>
+__device__ __forceinline__ void tc_stage_act_q8_0(uint8_t* act, float* meta, const uint8_t* raw, int nkb, int rstride)
+{
+    constexpr int NT = (M + 7) / 8;
+    constexpr int IT = 4 * tc_stage_items(M);
+    const int total = nkb * NT * 32;
+    uint32_t w0[IT], w1[IT];  // the lane's four code pairs, two per word
+#pragma unroll
+    for (int u = 0; u < IT; ++u) {
+        const int i = threadIdx.x + u * TC_THREADS;
+        w0[u] = w1[u] = 0;
+        if (i >= total) break;
+        const int tt = i & 3, n = ((i >> 5) % NT) * 8 + ((i >> 2) & 7), b = (i >> 5) / NT;
+        float da = 0.0f;
+        if (n < M) {
+            const uint8_t* q = raw + (size_t)n * rstride + (size_t)b * Q8_1_BYTES + 4 + 2 * tt;
+            const uint32_t p0 = *reinterpret_cast<const uint16_t*>(q), p1 = *reinterpret_cast<const uint16_t*>(q + 8);
+            const uint32_t p2 = *reinterpret_cast<const uint16_t*>(q + 16), p3 = *reinterpret_cast<const uint16_t*>(q + 24);
+            w0[u] = (p0 | p1 << 16) ^ 0x80808080u;
+            w1[u] = (p2 | p3 << 16) ^ 0x80808080u;
+            if (tt == 0) da = __half2float(*reinterpret_cast<const __half*>(q - 4));
+        }
+        if (tt == 0) {
+            const int nt = n >> 3, c = n & 7;
+            float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
+            mp[c & 1] = da;
+            mp[2 + (c & 1)] = 0.0f;
+        }
+    }
+    __syncthreads();  // the raw bytes are all read
+#pragma unroll
+    for (int u = 0; u < IT; ++u) {
+        const int i = threadIdx.x + u * TC_THREADS;
+        if (i >= total) break;
+        const int tt = i & 3, n = ((i >> 5) % NT) * 8 + ((i >> 2) & 7), b = (i >> 5) / NT;
+        if (n >= M) continue;
+        uint4 v;
+        v.x = q8u_f16x2<0x4140u>(w0[u]);
+        v.y = q8u_f16x2<0x4342u>(w0[u]);
+        v.z = q8u_f16x2<0x4140u>(w1[u]);
+        v.w = q8u_f16x2<0x4342u>(w1[u]);
+        *reinterpret_cast<uint4*>(act + (((size_t)b * M + n) * 4 + tt) * 16) = v;
+    }
+}
+
+// One Q8_0 job: 8 blocks in ring stage sn against staged blocks kb .. kb + 7.
+template <int M>
+__device__ __forceinline__ void tc_job_q8_0(const uint8_t* sn, const uint8_t* act, const float* meta, int kb, int g,
+                                            int t, float (&acc)[(M + 7) / 8][4])
+{
+    constexpr int NT = (M + 7) / 8;
+    float jacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) jacc[nt][i] = 0.0f;
+    const uint8_t* codes = sn + (g * 4 + t) * 16;
+    const uint8_t* dg = sn + TC_Q8_0_CODES + g * 2;  // row g's scale; row g + 8's is 16 B on
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const uint4 w = *reinterpret_cast<const uint4*>(codes + p * 32 * 16);
+        const float dwa = __half2float(*reinterpret_cast<const __half*>(dg + p * 32));
+        const float dwb = __half2float(*reinterpret_cast<const __half*>(dg + p * 32 + 16));
+        const uint32_t A0[4] = {q8u_f16x2<0x4140u>(w.x), q8u_f16x2<0x4140u>(w.z), q8u_f16x2<0x4342u>(w.x),
+                                q8u_f16x2<0x4342u>(w.z)};
+        const uint32_t A1[4] = {q8u_f16x2<0x4140u>(w.y), q8u_f16x2<0x4140u>(w.w), q8u_f16x2<0x4342u>(w.y),
+                                q8u_f16x2<0x4342u>(w.w)};
+        const int b = kb + p;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int n = nt * 8 + g < M ? nt * 8 + g : M - 1;
+            const uint4 B = *reinterpret_cast<const uint4*>(act + (((size_t)b * M + n) * 4 + t) * 16);
+            const float4 md = *reinterpret_cast<const float4*>(meta + (((size_t)b * NT + nt) * 4 + t) * 4);
+            float d[4];
+            mma_f16_16816(d, A0, B.x, B.y, 0.0f, 0.0f, 0.0f, 0.0f);
+            mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
+            jacc[nt][0] = fmaf(dwa * md.x, d[0], jacc[nt][0]);
+            jacc[nt][1] = fmaf(dwa * md.y, d[1], jacc[nt][1]);
+            jacc[nt][2] = fmaf(dwb * md.x, d[2], jacc[nt][2]);
+            jacc[nt][3] = fmaf(dwb * md.y, d[3], jacc[nt][3]);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] += jacc[nt][i];
+}
+
 // Write one tile's values, given as value index v of the fragment layout
 // (lane = v / (4 NT), nt, i), to y.
 template <int M>
@@ -337,12 +460,13 @@ __device__ __forceinline__ void tc_store(const TcArgs& a, int64_t T1, int64_t ta
     if (m >= M) return;
     const bool second = tau >= T1;
     const int64_t n = (second ? tau - T1 : tau) * TC_ROWS + (ln >> 2) + (i >> 1) * 8;
+    if (n >= (second ? a.N2 : a.N)) return;  // rows padding the last tile
     (second ? a.y2 : a.y)[(int64_t)m * a.ldy + n] = a.res ? val + a.res[(int64_t)m * a.ldr + n] : val;
 }
 
-template <int M, bool PAIR>
+template <int FMT, int M, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    mmvq_q4_0_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tn0, const __grid_constant__ CUtensorMap td0,
+    mmvq_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tn0, const __grid_constant__ CUtensorMap td0,
                         const __grid_constant__ CUtensorMap tn1, const __grid_constant__ CUtensorMap td1,
                         unsigned int* timeouts)
 {
@@ -366,19 +490,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int ncl = __shfl_sync(FULL, (int)cluster_count_x(), 0);
     const int cl = __shfl_sync(FULL, (int)cluster_id_x(), 0);
     const int NB = a.K / QK;
-    const int T1 = a.N / TC_ROWS, T = T1 + (PAIR ? a.N2 / TC_ROWS : 0);
+    const int T1 = (a.N + TC_ROWS - 1) / TC_ROWS, T = T1 + (PAIR ? (a.N2 + TC_ROWS - 1) / TC_ROWS : 0);
     // (32-bit divisions where the products fit, which they do below 2^24 tiles)
     const int t0 = T < (1 << 24) ? (int)((uint32_t)(cl * T) / (uint32_t)ncl) : (int)((int64_t)cl * T / ncl);
     const int t1 = T < (1 << 24) ? (int)((uint32_t)((cl + 1) * T) / (uint32_t)ncl) : (int)((int64_t)(cl + 1) * T / ncl);
     const int ntile = t1 - t0;
-    const int JB = a.jb, NIB = tc_nib_bytes(JB), DSB = tc_ds_bytes(JB);
+    const int JB = a.jb;
+    const int NIB = FMT == TCF_Q8_0 ? TC_Q8_0_JOB : tc_nib_bytes(JB), DSB = FMT == TCF_Q8_0 ? 0 : tc_ds_bytes(JB);
     const int JPC = CHUNK / JB, JPC_LOG = JB > TC_LINE_JB ? 1 : 2;  // jobs per 32-block chunk
     const int njb = NB / JB;
     const int jb0 = rank * njb / C, jb1 = (rank + 1) * njb / C;
     const int jpt = jb1 - jb0;  // jobs per tile
     const int J = ntile * jpt;
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
-    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, a.jb);
+    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB);
     uint8_t* nib = smem + sl.nib;
     uint8_t* ds = smem + sl.ds;
     uint8_t* act = smem + sl.act;
@@ -396,7 +521,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (warp == 0) mbar_init(abar, 1);
         fence_barrier_init();
     }
-    if (warp == 1 && lane < (PAIR ? 4 : 2)) {
+    if (FMT == TCF_Q4_0 && warp == 1 && lane < (PAIR ? 4 : 2)) {
         // bring the copies' descriptors on chip while the prologue runs
         const CUtensorMap* map = lane == 0 ? &tn0 : lane == 1 ? &td0 : lane == 2 ? &tn1 : &td1;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -434,12 +559,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
             uint64_t* bar = &wbar[iss_slot];
             uint8_t* dst = wnib + (size_t)iss_slot * NIB;
-            const CUtensorMap* map = isec ? &tn1 : &tn0;
             fence_proxy_async();
             mbar_arrive_expect_tx(bar, NIB + DSB);
-            tma_load_4d(dst, map, h * JB * 16, 0, c, igrp, bar, pol);
-            if (JB > TC_LINE_JB) tma_load_4d(dst + TC_BOX, map, h * JB * 16 + 128, 0, c, igrp, bar, pol);
-            tma_load_3d(wds + (size_t)iss_slot * DSB, isec ? &td1 : &td0, h * JB * 8, c, igrp, bar, pol);
+            if constexpr (FMT == TCF_Q8_0) {
+                // the job's region of the Q8_0 pack: tile igrp / 4, job ikg
+                const uint8_t* src = (isec ? a.w1 : a.w0) + ((int64_t)(igrp >> 2) * njb + ikg) * TC_Q8_0_JOB;
+                bulk_g2s(dst, src, TC_Q8_0_JOB, bar, pol);
+            } else {
+                const CUtensorMap* map = isec ? &tn1 : &tn0;
+                tma_load_4d(dst, map, h * JB * 16, 0, c, igrp, bar, pol);
+                if (JB > TC_LINE_JB) tma_load_4d(dst + TC_BOX, map, h * JB * 16 + 128, 0, c, igrp, bar, pol);
+                tma_load_3d(wds + (size_t)iss_slot * DSB, isec ? &td1 : &td0, h * JB * 8, c, igrp, bar, pol);
+            }
         }
         ++ikg;
         if (++ikj == jpt) {  // next tile
@@ -503,7 +634,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         alive = false;
     }
     alive = __syncthreads_and(alive);
-    if (alive) tc_stage_act<M>(act, meta, raw, jpt * JB, (int)rstride);
+    if (alive) {
+        if constexpr (FMT == TCF_Q8_0) tc_stage_act_q8_0<M>(act, meta, raw, jpt * JB, (int)rstride);
+        else tc_stage_act<M>(act, meta, raw, jpt * JB, (int)rstride);
+    }
     __syncthreads();  // the tile is built
     float acc[NT][4];
 #pragma unroll
@@ -529,7 +663,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             break;
         }
         ++consumed;
-        tc_job<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB, JB, g, t, acc);
+        if constexpr (FMT == TCF_Q8_0) tc_job_q8_0<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, g, t, acc);
+        else tc_job<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB, JB, g, t, acc);
         __syncwarp();
         if (++slot == S) {
             slot = 0;

@@ -46,6 +46,17 @@ def q4_0_weights(N: int, K: int, seed: int, d_lo: float = 0.001, d_hi: float = 0
     return out
 
 
+def q8_0_weights(N: int, K: int, seed: int, d_lo: float = 0.0005, d_hi: float = 0.005) -> np.ndarray:
+    """Canonical Q8_0 bytes uint8 [N, K/32, 34] = {fp16 d, int8 q[32]}, q ~ U{-127..127}."""
+    assert K % 32 == 0
+    nb = K // 32
+    g_d, g_q = streams(seed, 2)
+    out = np.empty((N, nb, 34), dtype=np.uint8)
+    out[:, :, 0:2] = _f16_bits(g_d, d_lo, d_hi, (N, nb)).view(np.uint8).reshape(N, nb, 2)
+    out[:, :, 2:34] = g_q.integers(-127, 128, size=(N, nb, 32), dtype=np.int8).view(np.uint8)
+    return out
+
+
 def q6_k_weights(N: int, K: int, seed: int, d_lo: float = 1e-4, d_hi: float = 1e-3) -> np.ndarray:
     """Canonical Q6_K bytes uint8 [N, K/256, 210] = {ql[128], qh[64], int8 sc[16], fp16 d}."""
     assert K % 256 == 0

@@ -69,6 +69,9 @@ size_t q8_1_bytes(int M, int K);
 size_t q4_0_pack_bytes(int N, int K);
 /* Bytes of a packed Q6_K weight: N * (K/256) * 210 (the canonical size). */
 size_t q6_k_pack_bytes(int N, int K);
+/* Bytes of a packed Q8_0 weight (qpack_q8_0): ceil(N/16) * (K/256) * 4352,
+ * the canonical N * (K/32) * 34 when N % 16 == 0; 0 unless K % 256 == 0. */
+size_t q8_0_pack_bytes(int N, int K);
 /* Workspace bytes of lmhead_q6_k_top1 (256 + M * (K/32) * 36, rounded up to
  * 16) and argmax_f32_rows (256). */
 size_t lmhead_q6_k_top1_workspace_bytes(int M, int K, int N);
@@ -291,6 +294,26 @@ int qgemv_set_q4_0_tensor_cores(int enable);
  * size, ring stages per warp}, zeros for the SIMT kernels.  Enqueues
  * nothing; may query the current device.  (Not from the pages.) */
 int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info);
+
+/* ---- NEXT-4: a further format, Q8_0 ------------------------------------ */
+
+/* Q8_0 (named on the pages among further quantization formats, defined as in
+ * llama.cpp): 32 weights, fp16 d then int8 q[32]; value d * q.       34 B
+ * [closure] "Qwen3.6 27B Q4_0 DFlash/SYCL closure" lists further K-quant
+ * formats as the next coverage; this one runs on the tensor-core MMVQ.
+ *
+ * qpack_q8_0 - canonical [N][K/32] x 34 B -> the tensor-core pack: per
+ * 16-row tile and job of 8 blocks one 4352-byte region (codes in MMA
+ * fragment order as q + 128, then the 8 x 16 fp16 scales); rows padded to 16
+ * with zeros.  K % 256 == 0; w_canon 2-byte aligned, w_pack 16-byte aligned
+ * (q8_0_pack_bytes(N, K) bytes).
+ *
+ * qgemv_q8_0 - y[m][n] = sum_b d_w[n,b] * d_a[m,b] * sum_i q_w q_a (the block
+ * dots exact, the scales in fp32), M = 1..17, K % 256 == 0, any N >= 1;
+ * arguments as qgemv_q4_0.  QGEMV_UNSUPPORTED_SHAPE also when the activation
+ * tile does not fit a plan (very large M * K). */
+int qpack_q8_0(const void* w_canon, void* w_pack, int N, int K, void* stream);
+int qgemv_q8_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
 
 /* qgemv_take_wait_timeouts - number of warps that, since the previous call,
  * waited about a second for a weight copy that never completed and gave up

@@ -54,11 +54,11 @@ def _load():
             lib.oracle_f16_to_f64.restype = ctypes.c_double
             lib.oracle_quantize_q8_1.argtypes = [P, L, I, I, P]
             lib.oracle_rmsnorm_quantize_q8_1.argtypes = [P, L, P, ctypes.c_float, I, I, P]
-            for name in ("oracle_dequant_q4_0", "oracle_dequant_q6_k", "oracle_dequant_q8_1"):
+            for name in ("oracle_dequant_q4_0", "oracle_dequant_q6_k", "oracle_dequant_q8_1", "oracle_dequant_q8_0"):
                 getattr(lib, name).argtypes = [P, I, I, P]
             for name in ("oracle_block_dots_q4_0", "oracle_block_dots_q6_k"):
                 getattr(lib, name).argtypes = [P, P, I, I, I, P]
-            for name in ("oracle_qgemv_q4_0", "oracle_qgemv_q6_k"):
+            for name in ("oracle_qgemv_q4_0", "oracle_qgemv_q6_k", "oracle_qgemv_q8_0"):
                 getattr(lib, name).argtypes = [P, P, I, I, I, P, P, I]
             lib.oracle_top1_f64.argtypes = [P, L, I, I, P]
             lib.oracle_top1_f32.argtypes = [P, L, I, I, P]
@@ -139,6 +139,29 @@ def qgemv_q4_0(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
     _load().oracle_qgemv_q4_0(_ptr(w), _ptr(xq), M, nb * 32, N, _ptr(y), _ptr(S),
                               nthreads or default_threads())
     return y, S
+
+
+def qgemv_q8_0(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
+    """canonical Q8_0 w [N, K/32, 34] = {fp16 d, int8 q[32]}, Q8_1 xq [M, K/32, 36]
+    -> (y, S) fp64 [M, N]: y = sum_b d_w * d_a * sum_i q_w q_a."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    N, nb, _ = w.shape
+    M = xq.shape[0]
+    K = nb * 32
+    y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_qgemv_q8_0(_ptr(w), _ptr(xq), M, K, N, _ptr(y), _ptr(S), nthreads or default_threads())
+    return y, S
+
+
+def dequant_q8_0(w: np.ndarray) -> np.ndarray:
+    """[N, K/32, 34] -> fp64 [N, K] (the C dequantizer)."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    N, nb, _ = w.shape
+    out = np.zeros((N, nb * 32), dtype=np.float64)
+    _load().oracle_dequant_q8_0(_ptr(w), N, nb * 32, _ptr(out))
+    return out
 
 
 def qgemv_q6_k(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
@@ -229,6 +252,13 @@ def dequant_q6_k_np(w: np.ndarray) -> np.ndarray:
     q = lo | (hi << 4)
     scale = np.repeat(sc, 16, axis=2)
     return (d * scale * (q - 32)).reshape(N, ns * 256)
+
+
+def dequant_q8_0_np(w: np.ndarray) -> np.ndarray:
+    """[N, K/32, 34] -> fp64 [N, K]: d * q (numpy, independent of the C code)."""
+    d = _f16(w[:, :, 0:2].copy().view(np.uint16)[:, :, 0])
+    q = w[:, :, 2:34].copy().view(np.int8).astype(np.float64)
+    return (d[:, :, None] * q).reshape(w.shape[0], -1)
 
 
 def dequant_q8_1_np(xq: np.ndarray) -> np.ndarray:

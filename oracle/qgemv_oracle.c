@@ -103,6 +103,7 @@ static void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (u
 /* Q8_1 activation quantization                                          */
 /* ------------------------------------------------------------------ */
 
+#define Q8_0_BYTES 34
 #define Q8_1_BYTES 36
 #define Q4_0_BYTES 18
 #define Q6_K_BYTES 210
@@ -227,6 +228,19 @@ void oracle_dequant_q6_k(const uint8_t* w, int N, int K, double* out)
         }
 }
 
+/* Q8_0 ("further K-quant formats"; the llama.cpp-family block): 32 weights,
+ * fp16 d then int8 q[32], value d * q. */
+void oracle_dequant_q8_0(const uint8_t* w, int N, int K, double* out)
+{
+    int nb = K / 32;
+    for (int n = 0; n < N; ++n)
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t* blk = w + ((int64_t)n * nb + b) * Q8_0_BYTES;
+            double d = oracle_f16_to_f64(rd16(blk));
+            for (int i = 0; i < 32; ++i) out[(int64_t)n * K + 32 * b + i] = d * (double)(int8_t)blk[2 + i];
+        }
+}
+
 void oracle_dequant_q8_1(const uint8_t* xq, int M, int K, double* out)
 {
     int nb = K / 32;
@@ -249,6 +263,14 @@ static int32_t block_dot_q4_0(const uint8_t* wblk, const uint8_t* ablk)
     int32_t I = 0;
     for (int i = 0; i < 32; ++i)
         I += (q4_0_code(wblk, i) - 8) * (int32_t)(int8_t)ablk[4 + i];
+    return I;
+}
+
+/* I = sum_i q_w(i) * q_a(i) over one 32-value Q8_0 block. */
+static int32_t block_dot_q8_0(const uint8_t* wblk, const uint8_t* ablk)
+{
+    int32_t I = 0;
+    for (int i = 0; i < 32; ++i) I += (int32_t)(int8_t)wblk[2 + i] * (int32_t)(int8_t)ablk[4 + i];
     return I;
 }
 
@@ -297,7 +319,7 @@ void oracle_block_dots_q6_k(const uint8_t* w, const uint8_t* xq, int M, int K, i
 /* ------------------------------------------------------------------ */
 
 typedef struct {
-    int fmt; /* 0 = Q4_0, 1 = Q6_K */
+    int fmt; /* 0 = Q4_0, 1 = Q6_K, 2 = Q8_0 */
     const uint8_t* w;
     const uint8_t* xq;
     int M, K, N;
@@ -321,10 +343,14 @@ static void gemv_rows(const gemv_job* j)
                     const uint8_t* wblk = j->w + ((int64_t)n * nb + b) * Q4_0_BYTES;
                     dw = oracle_f16_to_f64(rd16(wblk));
                     I = block_dot_q4_0(wblk, ablk);
-                } else {
+                } else if (j->fmt == 1) {
                     const uint8_t* sb = j->w + ((int64_t)n * ns + b / 8) * Q6_K_BYTES;
                     dw = oracle_f16_to_f64(q6_k_d(sb));
                     I = block_dot_q6_k(sb, b % 8, ablk);
+                } else {
+                    const uint8_t* wblk = j->w + ((int64_t)n * nb + b) * Q8_0_BYTES;
+                    dw = oracle_f16_to_f64(rd16(wblk));
+                    I = block_dot_q8_0(wblk, ablk);
                 }
                 double t = dw * da * (double)I;
                 acc += t;
@@ -359,6 +385,13 @@ static void gemv_run(int fmt, const uint8_t* w, const uint8_t* xq, int M, int K,
     for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
     free(jobs);
     free(th);
+}
+
+/* w: canonical Q8_0 [N][K/32] x 34 B; otherwise as oracle_qgemv_q4_0. */
+void oracle_qgemv_q8_0(const uint8_t* w, const uint8_t* xq, int M, int K, int N,
+                       double* y, double* S, int nthreads)
+{
+    gemv_run(2, w, xq, M, K, N, y, S, nthreads);
 }
 
 /* w: canonical Q4_0 [N][K/32] x 18 B; xq: Q8_1 [M][K/32] x 36 B;

@@ -38,6 +38,35 @@ def pack_q4_0(w: np.ndarray) -> np.ndarray:
     return np.concatenate(out)
 
 
+def pack_q8_0(w: np.ndarray) -> np.ndarray:
+    """Canonical Q8_0 [N, K/32, 34] -> the documented tensor-core pack: per
+    16-row tile, per job of 8 blocks, codes [block p][lane 4g + t][16 B] (values
+    2t, 2t+1, 2t+8, 2t+9, 16+2t, 17+2t, 24+2t, 25+2t of row g, then of row
+    g + 8, each as q + 128) and the fp16 scales [block p][row r]; rows past N
+    are zero."""
+    N, nb, _ = w.shape
+    T = (N + 15) // 16
+    wp = np.zeros((T * 16, nb, 34), dtype=np.uint8)
+    wp[:N] = w
+    q = (wp[:, :, 2:].view(np.int8).astype(np.int16) + 128).astype(np.uint8)  # [rows, nb, 32]
+    d = wp[:, :, 0:2]
+    out = np.zeros((T, nb // 8, 4352), dtype=np.uint8)
+    for tau in range(T):
+        for j in range(nb // 8):
+            reg = out[tau, j]
+            for p in range(8):
+                b = 8 * j + p
+                for g in range(8):
+                    for t in range(4):
+                        e = [2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9, 16 + 2 * t, 17 + 2 * t, 24 + 2 * t, 25 + 2 * t]
+                        o = (p * 32 + 4 * g + t) * 16
+                        reg[o:o + 8] = q[16 * tau + g, b, e]
+                        reg[o + 8:o + 16] = q[16 * tau + g + 8, b, e]
+                for r in range(16):
+                    reg[4096 + (p * 16 + r) * 2:4096 + (p * 16 + r) * 2 + 2] = d[16 * tau + r, b]
+    return out.reshape(-1)
+
+
 def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
     """Inverse of pack_q4_0."""
     nb = K // 32

@@ -60,6 +60,10 @@ def test_sizes(lib):
     assert lib.q4_0_pack_bytes(248320, 5120) == 715161600
     assert lib.q6_k_pack_bytes(248320, 5120) == 1042944000
     assert lib.q6_k_pack_bytes(5120, 5120) == 21504000
+    lib.q8_0_pack_bytes.restype = ctypes.c_size_t
+    assert lib.q8_0_pack_bytes(17408, 5120) == 17408 * 160 * 34  # the canonical size when N % 16 == 0
+    assert lib.q8_0_pack_bytes(17, 256) == 2 * 1 * 4352  # two tiles, rows padded to 32
+    assert lib.q8_0_pack_bytes(16, 96) == 0  # K % 256
 
 
 def test_status_strings(lib):

@@ -339,6 +339,65 @@ def test_rmsnorm_quantize_q8_1_errors(ops):
     assert np.all(_np(xq) == 0)
 
 
+# ---------------------------------------------------------------- Q8_0 (tensor cores)
+
+@pytest.mark.parametrize("N,K", [(1, 256), (16, 512), (37, 1024), (130, 5120)])
+def test_qpack_q8_0_layout(ops, N, K):
+    w = synth.q8_0_weights(N, K, seed=N + K)
+    got = _np(ops.qpack_q8_0(_t(w), N, K))
+    assert np.array_equal(got, C.pack_q8_0(w))
+
+
+Q8_0_SHAPES = [(M, K, N) for M in (1, 2, 5, 6, 8, 9, 12, 16, 17) for (K, N) in ((256, 1), (512, 37), (5120, 611))] + [
+    (6, 17408, 320), (2, 17408, 64), (6, 5120, 4096), (1, 8192, 16)]
+
+
+@pytest.mark.parametrize("M,K,N", Q8_0_SHAPES)
+def test_qgemv_q8_0_matches_oracle(ops, M, K, N):
+    x = synth.activations(M, K, seed=M + 5 * K, outlier_frac=0.01)
+    w = synth.q8_0_weights(N, K, seed=N + 3 * K)
+    y_ref, S = oracle.qgemv_q8_0(w, oracle.quantize_q8_1(x))
+    y = _np(ops.qgemv_q8_0(ops.qpack_q8_0(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
+    r = C.check_close(y, y_ref, S)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("M,K,N", [(6, 5120, 64), (1, 1024, 33), (17, 2048, 48), (6, 8192, 16)])
+def test_qgemv_q8_0_unit_scales_exact(ops, M, K, N):
+    # d_w = 1 and integer activations whose blocks hold +-127 (d_a = 1): the
+    # output is the integer sum of the exact block dots (|y| <= K * 127^2 < 2^24
+    # for K <= 1024; for larger K the random sums stay far below it)
+    w = synth.q8_0_weights(N, K, seed=M + K, d_lo=1.0, d_hi=1.0)
+    g = np.random.default_rng(M + N)
+    x = g.integers(-127, 128, size=(M, K)).astype(np.float32)
+    x[:, ::32] = 127.0
+    xq_ref = oracle.quantize_q8_1(x)
+    y_ref, _ = oracle.qgemv_q8_0(w, xq_ref)
+    assert np.all(np.abs(y_ref) < 2.0 ** 24)
+    y = _np(ops.qgemv_q8_0(ops.qpack_q8_0(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def test_qgemv_q8_0_stride_padding_and_errors(ops):
+    M, K, N, ldy = 6, 1024, 40, 48
+    w = synth.q8_0_weights(N, K, seed=9)
+    x = synth.activations(M, K, seed=10)
+    wp, xq = ops.qpack_q8_0(_t(w), N, K), ops.quantize_q8_1(_t(x))
+    y = torch.full((M, ldy), 7.0, device=DEV)
+    ops.qgemv_q8_0(wp, xq, M, K, N, y=y[:, :N])
+    yy = _np(y)
+    y_ref, S = oracle.qgemv_q8_0(w, oracle.quantize_q8_1(x))
+    assert C.check_close(yy[:, :N], y_ref, S)["ok"]
+    assert np.all(yy[:, N:] == 7.0)
+    L = ops.LIB
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    assert L.qgemv_q8_0(p(wp), p(xq), p(y), ldy, M, 384, N, None) == -2  # K % 256
+    assert L.qgemv_q8_0(p(wp), p(xq), p(y), ldy, M, 96, N, None) == -1  # K < 256
+    assert L.qgemv_q8_0(p(wp), p(xq), p(y), ldy, 18, K, N, None) == -2  # M > 17
+    assert L.qgemv_q8_0(None, p(xq), p(y), ldy, M, K, N, None) == -1
+    assert ops.qgemv_take_wait_timeouts() == 0
+
+
 def test_qgemv_output_stride_and_untouched_padding(ops):
     M, K, N, ldy = 6, 512, 100, 128
     w = synth.q4_0_weights(N, K, seed=5)

@@ -320,3 +320,44 @@ def test_pack_q6_k_model_round_trip(N, K):
     if N % 4 == 0 and K % 1024 == 0:
         assert p.size == w.size
     assert np.array_equal(C.unpack_q6_k(p, N, K), w)
+
+
+# ---------------------------------------------------------------- Q8_0 (a further format)
+
+def test_q8_0_hand_block():
+    # one block: d = 0.5, q = (i - 16) for i = 0..31, against a Q8_1 block of
+    # all 2s with d = 1/64 (stored exactly): y = 0.5 * (1/64) * 2 * sum(i - 16)
+    w = np.zeros((1, 1, 34), dtype=np.uint8)
+    w[0, 0, 0:2] = np.array([0.5], dtype=np.float16).view(np.uint8)
+    w[0, 0, 2:] = (np.arange(32) - 16).astype(np.int8).view(np.uint8)
+    xq = np.zeros((1, 1, 36), dtype=np.uint8)
+    xq[0, 0, 0:2] = np.array([1.0 / 64], dtype=np.float16).view(np.uint8)
+    xq[0, 0, 4:] = 2
+    y, S = oracle.qgemv_q8_0(w, xq)
+    assert y[0, 0] == 0.5 * (1.0 / 64) * 2 * float(np.sum(np.arange(32) - 16)) == -0.25
+    assert S[0, 0] == 0.25
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 32, 1), (3, 256, 7), (2, 512, 33), (5, 1024, 16)])
+def test_q8_0_matches_fp64_dequant_matmul(M, K, N):
+    w = synth.q8_0_weights(N, K, seed=300 + K + N)
+    xq = oracle.quantize_q8_1(synth.activations(M, K, seed=400 + M))
+    y, S = oracle.qgemv_q8_0(w, xq)
+    ref = oracle.dequant_q8_1_np(xq) @ oracle.dequant_q8_0_np(w).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * np.maximum(S, 1e-300))
+    assert np.array_equal(oracle.dequant_q8_0(w), oracle.dequant_q8_0_np(w))
+
+
+def test_q8_0_code_sign_and_position():
+    # a single code +1 at position i of block b must pick activation value (b, i)
+    # with its sign; -1 flips it (no offset in Q8_0, unlike Q4_0's q - 8)
+    K, N = 128, 1
+    x = synth.activations(1, K, seed=5)
+    xq = oracle.quantize_q8_1(x)
+    xd = oracle.dequant_q8_1_np(xq)[0]
+    for b, i, s in ((0, 0, 1), (1, 31, -1), (3, 17, 1)):
+        w = np.zeros((N, K // 32, 34), dtype=np.uint8)
+        w[0, b, 0:2] = np.array([1.0], dtype=np.float16).view(np.uint8)
+        w[0, b, 2 + i] = np.int8(s).view(np.uint8)
+        y, _ = oracle.qgemv_q8_0(w, xq)
+        assert y[0, 0] == s * xd[32 * b + i]
