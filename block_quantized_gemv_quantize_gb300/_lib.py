@@ -49,6 +49,7 @@ SIGNATURES = {
     "rmsnorm_quantize_q8_1": (_I, [_P, _L, _P, ctypes.c_float, _P, _I, _I, _P]),
     "qgemv_q4_0_residual": (_I, [_P, _P, _P, _L, _P, _L, _I, _I, _I, _P]),
     "qgemv_q4_0_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+    "qgemv_q8_0_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "lmhead_q6_k_top1_noalloc": (_I, [_P, _P, _L, _P, _I, _I, _I, _P]),
 }
 
@@ -335,6 +336,14 @@ def qgemv_q4_0_plan(M: int, K: int, N: int, N_b: int = 0) -> dict:
     info = (ctypes.c_int * 4)()
     _check("qgemv_q4_0_plan", LIB.qgemv_q4_0_plan(M, K, N, N_b, info))
     return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3]}
+
+
+def qgemv_q8_0_plan(M: int, K: int, N: int) -> dict:
+    """The launch qgemv_q8_0 would make for this shape."""
+    info = (ctypes.c_int * 5)()
+    _check("qgemv_q8_0_plan", LIB.qgemv_q8_0_plan(M, K, N, info))
+    return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3],
+            "job_blocks": info[4]}
 
 
 def qgemv_take_wait_timeouts() -> int:

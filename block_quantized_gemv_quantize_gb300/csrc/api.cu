@@ -322,6 +322,17 @@ int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info)
     return st == TC_NOT_TAKEN ? QGEMV_OK : st;
 }
 
+int qgemv_q8_0_plan(int M, int K, int N, int* info)
+{
+    if (!info || M < 1 || K < QK || N < 1) return QGEMV_INVALID_ARG;
+    if (M > QGEMV_MAX_M || K % (QK * 8)) return QGEMV_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < 5; ++i) info[i] = 0;
+    MmvqArgs a{};
+    a.K = K;
+    a.N = N;
+    return launch_mmvq_q8_0(a, M, nullptr, info);
+}
+
 int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;

@@ -7,8 +7,10 @@ namespace qgemv {
 
 namespace {
 
+// info (when not null): {1, cluster size, grid, ring stages, blocks per job}
+// of the plan; nothing is launched.
 template <int M>
-int launch_q8_0_m(const MmvqArgs& m, cudaStream_t s)
+int launch_q8_0_m(const MmvqArgs& m, cudaStream_t s, int* info)
 {
     const DeviceInfo di = device_info();
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
@@ -18,6 +20,14 @@ int launch_q8_0_m(const MmvqArgs& m, cudaStream_t s)
     if (!timeouts) return QGEMV_CUDA_ERROR;
     TcPlan p{};
     if (!tc_plan<TCF_Q8_0, M, false>(di, dev, m.K, m.N, 0, p)) return QGEMV_UNSUPPORTED_SHAPE;
+    if (info) {
+        info[0] = 1;
+        info[1] = p.C;
+        info[2] = p.grid;
+        info[3] = p.S;
+        info[4] = p.jb;
+        return QGEMV_OK;
+    }
     CUtensorMap none{};  // the Q8_0 kernel reads the pack directly
     TcArgs a{};
     a.xq = m.xq;
@@ -38,26 +48,26 @@ int launch_q8_0_m(const MmvqArgs& m, cudaStream_t s)
 
 }  // namespace
 
-int launch_mmvq_q8_0(const MmvqArgs& a, int M, cudaStream_t s)
+int launch_mmvq_q8_0(const MmvqArgs& a, int M, cudaStream_t s, int* info)
 {
     switch (M) {
-    case 1: return launch_q8_0_m<1>(a, s);
-    case 2: return launch_q8_0_m<2>(a, s);
-    case 3: return launch_q8_0_m<3>(a, s);
-    case 4: return launch_q8_0_m<4>(a, s);
-    case 5: return launch_q8_0_m<5>(a, s);
-    case 6: return launch_q8_0_m<6>(a, s);
-    case 7: return launch_q8_0_m<7>(a, s);
-    case 8: return launch_q8_0_m<8>(a, s);
-    case 9: return launch_q8_0_m<9>(a, s);
-    case 10: return launch_q8_0_m<10>(a, s);
-    case 11: return launch_q8_0_m<11>(a, s);
-    case 12: return launch_q8_0_m<12>(a, s);
-    case 13: return launch_q8_0_m<13>(a, s);
-    case 14: return launch_q8_0_m<14>(a, s);
-    case 15: return launch_q8_0_m<15>(a, s);
-    case 16: return launch_q8_0_m<16>(a, s);
-    case 17: return launch_q8_0_m<17>(a, s);
+    case 1: return launch_q8_0_m<1>(a, s, info);
+    case 2: return launch_q8_0_m<2>(a, s, info);
+    case 3: return launch_q8_0_m<3>(a, s, info);
+    case 4: return launch_q8_0_m<4>(a, s, info);
+    case 5: return launch_q8_0_m<5>(a, s, info);
+    case 6: return launch_q8_0_m<6>(a, s, info);
+    case 7: return launch_q8_0_m<7>(a, s, info);
+    case 8: return launch_q8_0_m<8>(a, s, info);
+    case 9: return launch_q8_0_m<9>(a, s, info);
+    case 10: return launch_q8_0_m<10>(a, s, info);
+    case 11: return launch_q8_0_m<11>(a, s, info);
+    case 12: return launch_q8_0_m<12>(a, s, info);
+    case 13: return launch_q8_0_m<13>(a, s, info);
+    case 14: return launch_q8_0_m<14>(a, s, info);
+    case 15: return launch_q8_0_m<15>(a, s, info);
+    case 16: return launch_q8_0_m<16>(a, s, info);
+    case 17: return launch_q8_0_m<17>(a, s, info);
     default: return QGEMV_UNSUPPORTED_SHAPE;
     }
 }

@@ -54,6 +54,10 @@ constexpr int TC_THREADS = 512;
 enum TcFormat { TCF_Q4_0 = 0, TCF_Q8_0 = 2 };
 constexpr int TC_Q8_0_CODES = TC_ROWS * 8 * 32;            // 4096 B: 16 rows x 8 blocks of int8 codes
 constexpr int TC_Q8_0_JOB = TC_Q8_0_CODES + TC_ROWS * 8 * 2;  // + 256 B of scales = 4352 B
+constexpr int TC_Q8_0_JOB_BLOCKS = 8;                          // blocks of a pack region
+// ring-stage bytes of a Q8_0 job of jb blocks (8: a whole region; 4: half of
+// its codes and half of its scales)
+__host__ __device__ inline int tc_q8_0_job_bytes(int jb) { return jb * (512 + 32); }
 constexpr int TC_MIN_M = 5;  // activation rows from which the tensor-core path is taken
 constexpr int TC_MAX_STAGES = 6;
 
@@ -406,10 +410,12 @@ __device__ __forceinline__ void tc_stage_act_q8_0(uint8_t* act, float* meta, con
     }
 }
 
-// One Q8_0 job: 8 blocks in ring stage sn against staged blocks kb .. kb + 7.
+// One Q8_0 job: nblk (8, or 4 where shared memory is short) blocks in ring
+// stage sn (their codes, then their scales at nblk * 512) against staged
+// blocks kb .. kb + nblk - 1.
 template <int M>
-__device__ __forceinline__ void tc_job_q8_0(const uint8_t* sn, const uint8_t* act, const float* meta, int kb, int g,
-                                            int t, float (&acc)[(M + 7) / 8][4])
+__device__ __forceinline__ void tc_job_q8_0(const uint8_t* sn, const uint8_t* act, const float* meta, int kb, int nblk,
+                                            int g, int t, float (&acc)[(M + 7) / 8][4])
 {
     constexpr int NT = (M + 7) / 8;
     float jacc[NT][4];
@@ -418,9 +424,12 @@ __device__ __forceinline__ void tc_job_q8_0(const uint8_t* sn, const uint8_t* ac
 #pragma unroll
         for (int i = 0; i < 4; ++i) jacc[nt][i] = 0.0f;
     const uint8_t* codes = sn + (g * 4 + t) * 16;
-    const uint8_t* dg = sn + TC_Q8_0_CODES + g * 2;  // row g's scale; row g + 8's is 16 B on
+    const uint8_t* dg = sn + nblk * 512 + g * 2;  // row g's scale; row g + 8's is 16 B on
+#pragma unroll 1
+    for (int p0 = 0; p0 < nblk; p0 += 4)
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
+    for (int pp = 0; pp < 4; ++pp) {
+        const int p = p0 + pp;
         const uint4 w = *reinterpret_cast<const uint4*>(codes + p * 32 * 16);
         const float dwa = __half2float(*reinterpret_cast<const __half*>(dg + p * 32));
         const float dwb = __half2float(*reinterpret_cast<const __half*>(dg + p * 32 + 16));
@@ -491,12 +500,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int cl = __shfl_sync(FULL, (int)cluster_id_x(), 0);
     const int NB = a.K / QK;
     const int T1 = (a.N + TC_ROWS - 1) / TC_ROWS, T = T1 + (PAIR ? (a.N2 + TC_ROWS - 1) / TC_ROWS : 0);
-    // (32-bit divisions where the products fit, which they do below 2^24 tiles)
-    const int t0 = T < (1 << 24) ? (int)((uint32_t)(cl * T) / (uint32_t)ncl) : (int)((int64_t)cl * T / ncl);
-    const int t1 = T < (1 << 24) ? (int)((uint32_t)((cl + 1) * T) / (uint32_t)ncl) : (int)((int64_t)(cl + 1) * T / ncl);
+    // (32-bit divisions where the products fit)
+    const bool narrow = (int64_t)ncl * T <= (int64_t)0xFFFFFFFFu;
+    const int t0 = narrow ? (int)((uint32_t)cl * (uint32_t)T / (uint32_t)ncl) : (int)((int64_t)cl * T / ncl);
+    const int t1 = narrow ? (int)((uint32_t)(cl + 1) * (uint32_t)T / (uint32_t)ncl) : (int)((int64_t)(cl + 1) * T / ncl);
     const int ntile = t1 - t0;
     const int JB = a.jb;
-    const int NIB = FMT == TCF_Q8_0 ? TC_Q8_0_JOB : tc_nib_bytes(JB), DSB = FMT == TCF_Q8_0 ? 0 : tc_ds_bytes(JB);
+    const int NIB = FMT == TCF_Q8_0 ? tc_q8_0_job_bytes(JB) : tc_nib_bytes(JB), DSB = FMT == TCF_Q8_0 ? 0 : tc_ds_bytes(JB);
     const int JPC = CHUNK / JB, JPC_LOG = JB > TC_LINE_JB ? 1 : 2;  // jobs per 32-block chunk
     const int njb = NB / JB;
     const int jb0 = rank * njb / C, jb1 = (rank + 1) * njb / C;
@@ -562,9 +572,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             fence_proxy_async();
             mbar_arrive_expect_tx(bar, NIB + DSB);
             if constexpr (FMT == TCF_Q8_0) {
-                // the job's region of the Q8_0 pack: tile igrp / 4, job ikg
-                const uint8_t* src = (isec ? a.w1 : a.w0) + ((int64_t)(igrp >> 2) * njb + ikg) * TC_Q8_0_JOB;
-                bulk_g2s(dst, src, TC_Q8_0_JOB, bar, pol);
+                // the job's part of the Q8_0 pack: tile igrp / 4, region (8
+                // blocks) ikg * JB / 8, all of it or the half h of its codes
+                // and of its scales
+                const int per = TC_Q8_0_JOB_BLOCKS / JB, reg = ikg / per, hh = ikg - reg * per;
+                const uint8_t* src = (isec ? a.w1 : a.w0) +
+                                     ((int64_t)(igrp >> 2) * (njb / per) + reg) * TC_Q8_0_JOB;
+                if (per == 1) {
+                    bulk_g2s(dst, src, TC_Q8_0_JOB, bar, pol);
+                } else {
+                    bulk_g2s(dst, src + hh * JB * 512, JB * 512, bar, pol);
+                    bulk_g2s(dst + JB * 512, src + TC_Q8_0_CODES + hh * JB * 32, JB * 32, bar, pol);
+                }
             } else {
                 const CUtensorMap* map = isec ? &tn1 : &tn0;
                 tma_load_4d(dst, map, h * JB * 16, 0, c, igrp, bar, pol);
@@ -663,7 +682,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             break;
         }
         ++consumed;
-        if constexpr (FMT == TCF_Q8_0) tc_job_q8_0<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, g, t, acc);
+        if constexpr (FMT == TCF_Q8_0) tc_job_q8_0<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, JB, g, t, acc);
         else tc_job<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB, JB, g, t, acc);
         __syncwarp();
         if (++slot == S) {

@@ -71,12 +71,14 @@ int tc_max_clusters(int dev, int ci, size_t smem)
     return cache[dev][ci];
 }
 
-// The cheapest plan over job sizes JB (Q4_0: 16 or 8 blocks; Q8_0: 8) and
-// cluster sizes C:
+// The cheapest plan over job sizes JB (Q4_0: 16 or 8 blocks; Q8_0: 8 or 4)
+// and cluster sizes C:
 // the largest per-CTA job count over 16 warps (the critical path) in units of
-// 8 blocks, where a 16-block job counts 0.85 x 2 units (measured: it halves
-// the per-job copy issue and loop overhead), plus two units for the
-// cross-CTA combine when C > 1.  Returns false when nothing fits.
+// 8 blocks, where a 16-block Q4_0 job counts 0.85 x 2 units (measured: it
+// halves the per-job copy issue and loop overhead) and a 4-block Q8_0 job 0.75
+// (its copy issue and loop overhead stay whole), plus two units for the
+// cross-CTA combine when C > 1, times the waves when more clusters are
+// launched than are resident.  Returns false when nothing fits.
 template <int FMT, int M, bool PAIR>
 bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
 {
@@ -85,9 +87,13 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
     const int64_t T = (N + TC_ROWS - 1) / TC_ROWS + (PAIR ? (N2 + TC_ROWS - 1) / TC_ROWS : 0);
     double best_cost = 0.0;
     bool found = false;
-    for (int jb = FMT == TCF_Q8_0 ? TC_LINE_JB : 2 * TC_LINE_JB; jb >= TC_LINE_JB; jb -= TC_LINE_JB) {
+    // Q4_0: 16- then 8-block jobs; Q8_0: whole 8-block regions, then halves
+    const int jb_first = FMT == TCF_Q8_0 ? TC_Q8_0_JOB_BLOCKS : 2 * TC_LINE_JB;
+    const int jb_last = FMT == TCF_Q8_0 ? TC_Q8_0_JOB_BLOCKS / 2 : TC_LINE_JB;
+    for (int jb = jb_first; jb >= jb_last; jb /= 2) {
         const int njb = NB / jb;
-        const int nibs = FMT == TCF_Q8_0 ? TC_Q8_0_JOB : tc_nib_bytes(jb), dsb = FMT == TCF_Q8_0 ? 0 : tc_ds_bytes(jb);
+        const int nibs = FMT == TCF_Q8_0 ? tc_q8_0_job_bytes(jb) : tc_nib_bytes(jb);
+        const int dsb = FMT == TCF_Q8_0 ? 0 : tc_ds_bytes(jb);
         for (int ci = 0; ci < 4; ++ci) {
             const int C = TC_CLUSTERS[ci];
             if (njb < C) break;
@@ -102,23 +108,40 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
                 if (ncl <= 0) continue;
             }
             if (ncl > T) ncl = T;
-            const int tiles = (int)((T + ncl - 1) / ncl);
-            const int out_tiles = C > 1 ? tiles : 0;
-            int S = 0;
-            for (int s = TC_MAX_STAGES; s >= 2; --s) {
-                if (tc_smem(M, W, s, nkb, out_tiles, nibs, dsb).bytes <= (uint32_t)di.smem_optin) {
-                    S = s;
-                    break;
+            int64_t ngrid = ncl;  // clusters launched
+            int tiles = (int)((T + ncl - 1) / ncl);
+            int64_t waves = 1;
+            auto deepest = [&](int out_tiles) {
+                for (int s = TC_MAX_STAGES; s >= 2; --s)
+                    if (tc_smem(M, W, s, nkb, out_tiles, nibs, dsb).bytes <= (uint32_t)di.smem_optin) return s;
+                return 0;
+            };
+            int S = deepest(C > 1 ? tiles : 0);
+            if (S == 0 && C > 1) {
+                // The combine area of one resident wave's tiles does not fit
+                // (very large N): launch more clusters than are resident, in
+                // waves, each with as many tiles as the area holds.
+                const int64_t per_tile = tc_smem(M, W, 2, nkb, 1, nibs, dsb).bytes - tc_smem(M, W, 2, nkb, 0, nibs, dsb).bytes;
+                const int64_t room = (int64_t)di.smem_optin - tc_smem(M, W, 2, nkb, 0, nibs, dsb).bytes;
+                const int64_t fit = room / per_tile;
+                if (fit >= 1) {
+                    ngrid = (T + fit - 1) / fit;
+                    tiles = (int)((T + ngrid - 1) / ngrid);
+                    waves = (ngrid + ncl - 1) / ncl;
+                    S = deepest(tiles);
                 }
             }
             if (S == 0) continue;
-            const double unit = jb > TC_LINE_JB ? 0.85 * jb / TC_LINE_JB : 1.0;
-            const double cost = (double)(((int64_t)tiles * jpt + W - 1) / W) * unit + (C > 1 ? 2.0 : 0.0);
+            const int out_tiles = C > 1 ? tiles : 0;
+            const double unit = FMT == TCF_Q8_0 ? (jb < TC_Q8_0_JOB_BLOCKS ? 0.75 : 1.0)
+                                : (jb > TC_LINE_JB ? 0.85 * jb / TC_LINE_JB : 1.0);
+            const double cost =
+                (double)waves * ((double)(((int64_t)tiles * jpt + W - 1) / W) * unit + (C > 1 ? 2.0 : 0.0));
             if (!found || cost < best_cost - 1e-9) {
                 found = true;
                 best_cost = cost;
                 best.C = C;
-                best.grid = (int)(ncl * C);
+                best.grid = (int)(ngrid * C);
                 best.S = S;
                 best.jb = jb;
                 best.nkb_max = nkb;

@@ -315,6 +315,14 @@ int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info);
 int qpack_q8_0(const void* w_canon, void* w_pack, int N, int K, void* stream);
 int qgemv_q8_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
 
+/* qgemv_q8_0_plan - the launch qgemv_q8_0 would make for this shape; writes
+ * info[5] = {1, CTAs per cluster (the K parts), grid size, ring stages per
+ * warp, blocks per job (8: a whole pack region; 4: half of one, taken where
+ * 8-block stages do not fit shared memory)}.  QGEMV_UNSUPPORTED_SHAPE when no
+ * plan fits.  Enqueues nothing; may query the current device.  (Not from
+ * the pages.) */
+int qgemv_q8_0_plan(int M, int K, int N, int* info);
+
 /* qgemv_take_wait_timeouts - number of warps that, since the previous call,
  * waited about a second for a weight copy that never completed and gave up
  * (their outputs are then invalid); resets the count.  Synchronous: it reads

@@ -349,7 +349,7 @@ def test_qpack_q8_0_layout(ops, N, K):
 
 
 Q8_0_SHAPES = [(M, K, N) for M in (1, 2, 5, 6, 8, 9, 12, 16, 17) for (K, N) in ((256, 1), (512, 37), (5120, 611))] + [
-    (6, 17408, 320), (2, 17408, 64), (6, 5120, 4096), (1, 8192, 16)]
+    (6, 17408, 320), (2, 17408, 64), (6, 5120, 4096), (1, 8192, 16), (17, 17408, 64), (16, 17408, 80)]
 
 
 @pytest.mark.parametrize("M,K,N", Q8_0_SHAPES)
@@ -376,6 +376,48 @@ def test_qgemv_q8_0_unit_scales_exact(ops, M, K, N):
     assert np.all(np.abs(y_ref) < 2.0 ** 24)
     y = _np(ops.qgemv_q8_0(ops.qpack_q8_0(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
     assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def test_qgemv_q8_0_plans(ops):
+    # 8-block jobs where two stages of them fit, 4-block jobs (half a pack
+    # region) where they do not; very large N launches clusters in waves
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    p = ops.qgemv_q8_0_plan(6, 5120, 17408)
+    assert p["tensor_cores"] and p["job_blocks"] == 8
+    assert ops.qgemv_q8_0_plan(17, 17408, 64)["job_blocks"] == 4
+    assert ops.qgemv_q8_0_plan(17, 5120, 611)["job_blocks"] == 4
+    p = ops.qgemv_q8_0_plan(17, 5120, 248320)
+    assert p["cluster"] > 1 and p["grid"] > sms
+    for M, K, N in Q8_0_SHAPES + [(17, 5120, 17408), (17, 17408, 5120), (17, 5120, 40000)]:
+        p = ops.qgemv_q8_0_plan(M, K, N)
+        assert p["stages"] >= 2 and p["grid"] % p["cluster"] == 0 and p["job_blocks"] in (4, 8)
+    with pytest.raises(ops.QgemvError):
+        ops.qgemv_q8_0_plan(18, 5120, 64)
+
+
+@pytest.mark.parametrize("fmt,M,N", [("q8_0", 17, 40000), ("q8_0", 12, 40000), ("q4_0", 17, 40000),
+                                     ("q4_0", 12, 40000)])
+def test_large_n_wave_plans_sampled_rows(ops, fmt, M, N):
+    # more clusters than are resident (the combine area holds a wave's tiles
+    # only): outputs checked on a sample of rows, which the oracle computes
+    # row by row
+    K = 5120
+    x = synth.activations(M, K, seed=M + N, outlier_frac=0.01)
+    xq = ops.quantize_q8_1(_t(x))
+    if fmt == "q8_0":
+        w = synth.q8_0_weights(N, K, seed=N + M)
+        y = _np(ops.qgemv_q8_0(ops.qpack_q8_0(_t(w), N, K), xq, M, K, N))
+        ref = oracle.qgemv_q8_0
+    else:
+        assert ops.qgemv_q4_0_plan(M, K, N)["tensor_cores"]
+        w = synth.q4_0_weights(N, K, seed=N + M)
+        y = _np(ops.qgemv_q4_0(ops.qpack_q4_0(_t(w), N, K), xq, M, K, N))
+        ref = oracle.qgemv_q4_0
+    rows = np.unique(np.concatenate([np.arange(0, N, 97), np.arange(N - 40, N)]))
+    y_ref, S = ref(w[rows], oracle.quantize_q8_1(x))
+    r = C.check_close(y[:, rows], y_ref, S)
+    assert r["ok"], r
+    assert np.isfinite(y).all()
 
 
 def test_qgemv_q8_0_stride_padding_and_errors(ops):
