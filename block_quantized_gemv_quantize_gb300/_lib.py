@@ -43,6 +43,7 @@ SIGNATURES = {
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "qgemv_set_q4_0_tensor_cores": (_I, [_I]),
+    "qgemv_set_q6_k_tensor_cores": (_I, [_I]),
     "q8_0_pack_bytes": (_S, [_I, _I]),
     "qpack_q8_0": (_I, [_P, _P, _I, _I, _P]),
     "qgemv_q8_0": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
@@ -50,6 +51,7 @@ SIGNATURES = {
     "qgemv_q4_0_residual": (_I, [_P, _P, _P, _L, _P, _L, _I, _I, _I, _P]),
     "qgemv_q4_0_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "qgemv_q8_0_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+    "qgemv_q6_k_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "lmhead_q6_k_top1_noalloc": (_I, [_P, _P, _L, _P, _I, _I, _I, _P]),
 }
 
@@ -331,10 +333,24 @@ def set_q4_0_tensor_cores(enable: bool) -> bool:
     return bool(LIB.qgemv_set_q4_0_tensor_cores(1 if enable else 0))
 
 
+def set_q6_k_tensor_cores(mode: int) -> int:
+    """qgemv_q6_k's kernel family: 1 = the tensor cores where they measured
+    faster (default), 2 = wherever the shape allows, 0 = never (dp4a);
+    returns the previous mode."""
+    return int(LIB.qgemv_set_q6_k_tensor_cores(int(mode)))
+
+
 def qgemv_q4_0_plan(M: int, K: int, N: int, N_b: int = 0) -> dict:
     """The kernel qgemv_q4_0 (N_b = 0) or the pair call would launch."""
     info = (ctypes.c_int * 4)()
     _check("qgemv_q4_0_plan", LIB.qgemv_q4_0_plan(M, K, N, N_b, info))
+    return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3]}
+
+
+def qgemv_q6_k_plan(M: int, K: int, N: int) -> dict:
+    """The kernel qgemv_q6_k would launch for this shape."""
+    info = (ctypes.c_int * 4)()
+    _check("qgemv_q6_k_plan", LIB.qgemv_q6_k_plan(M, K, N, info))
     return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3]}
 
 

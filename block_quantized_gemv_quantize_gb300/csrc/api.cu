@@ -219,6 +219,8 @@ int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
     a.ldy = ldy;
     a.K = K;
     a.N = N;
+    st = launch_mmvq_q6_k_tc(a, M, as_stream(stream));
+    if (st != TC_NOT_TAKEN) return st;
     return launch_mmvq_q6_k(a, M, as_stream(stream));
 }
 
@@ -322,6 +324,20 @@ int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info)
     return st == TC_NOT_TAKEN ? QGEMV_OK : st;
 }
 
+int qgemv_set_q6_k_tensor_cores(int mode) { return set_q6_k_tensor_cores(mode); }
+
+int qgemv_q6_k_plan(int M, int K, int N, int* info)
+{
+    if (!info || M < 1 || K < QK_K || N < 1) return QGEMV_INVALID_ARG;
+    if (M > QGEMV_MAX_M || K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < 4; ++i) info[i] = 0;
+    MmvqArgs a{};
+    a.K = K;
+    a.N = N;
+    const int st = launch_mmvq_q6_k_tc(a, M, nullptr, info);
+    return st == TC_NOT_TAKEN ? QGEMV_OK : st;
+}
+
 int qgemv_q8_0_plan(int M, int K, int N, int* info)
 {
     if (!info || M < 1 || K < QK || N < 1) return QGEMV_INVALID_ARG;
@@ -337,8 +353,8 @@ int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;
     *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() +
-             take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_lmhead() +
-             take_wait_timeouts_q8_0();
+             take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_q6_k_tc() +
+             take_wait_timeouts_lmhead() + take_wait_timeouts_q8_0();
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

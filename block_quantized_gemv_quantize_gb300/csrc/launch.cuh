@@ -209,6 +209,11 @@ constexpr int TC_NOT_TAKEN = 1;
 int launch_mmvq_q4_0_tc(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int* info = nullptr);
 int set_q4_0_tensor_cores(int enable);
 unsigned int take_wait_timeouts_q4_0_tc();
+// The tensor-core Q6_K path (M >= TC_Q6_K_MIN_M, N % 16 == 0, K % 1024 == 0);
+// TC_NOT_TAKEN otherwise.
+int launch_mmvq_q6_k_tc(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
+int set_q6_k_tensor_cores(int mode);
+unsigned int take_wait_timeouts_q6_k_tc();
 int launch_mmvq_q4_0_pair(const MmvqArgs& a, int M, cudaStream_t s);
 // y = W x + residual on the SIMT kernels; the residual travels in a.x / a.ldx
 int launch_mmvq_q4_0_residual(const MmvqArgs& a, int M, cudaStream_t s);

@@ -1,8 +1,6 @@
 // Host side of the tensor-core Q4_0 MMVQ: tensor maps over the packed
 // weight, the launch plan (cluster size, ring depth) and the launch, for
 // M = 1..17, one weight or a pair.
-#include <cudaTypedefs.h>
-
 #include <atomic>
 
 #include "mmvq_tc_host.cuh"
@@ -12,20 +10,6 @@ namespace qgemv {
 namespace {
 
 std::atomic<int> g_tc_enabled{1};
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
 
 // Tensor maps of a packed Q4_0 weight whose groups and chunks are all whole
 // (N % 16 == 0, K % 1024 == 0): every group-chunk is 2304 B, codes

@@ -49,16 +49,23 @@ constexpr int TC_BOX = TC_ROWS * TC_LINE_JB * 16;  // 2048 B: one code box (16 r
 __host__ __device__ inline int tc_nib_bytes(int jb) { return TC_ROWS * jb * 16; }
 __host__ __device__ inline int tc_ds_bytes(int jb) { return TC_ROWS * jb * 2; }
 constexpr int TC_THREADS = 512;
-// Weight formats of the tensor-core kernel: Q4_0 (the existing pack, read by
-// tensor maps) and Q8_0 (its own pack, one contiguous region per job).
-enum TcFormat { TCF_Q4_0 = 0, TCF_Q8_0 = 2 };
+// Weight formats of the tensor-core kernel: Q4_0 and Q6_K (the existing packs,
+// read by tensor maps) and Q8_0 (its own pack, one contiguous region per job).
+enum TcFormat { TCF_Q4_0 = 0, TCF_Q6_K = 1, TCF_Q8_0 = 2 };
+// A Q6_K job is one superblock (8 blocks) of 16 rows: ring stage = ql box
+// (16 x 128 B, 128-byte swizzle) + qh box (16 x 64 B, 64-byte swizzle), then
+// in the scale ring the sc box (16 x 16 B) + the chunk's superblock scales
+// (4 groups x 32 B).
+constexpr int TC_Q6_K_NIB = TC_ROWS * 128 + TC_ROWS * 64;  // 3072 B
+constexpr int TC_Q6_K_DS = TC_ROWS * 16 + 4 * 32;          // 384 B
 constexpr int TC_Q8_0_CODES = TC_ROWS * 8 * 32;            // 4096 B: 16 rows x 8 blocks of int8 codes
 constexpr int TC_Q8_0_JOB = TC_Q8_0_CODES + TC_ROWS * 8 * 2;  // + 256 B of scales = 4352 B
 constexpr int TC_Q8_0_JOB_BLOCKS = 8;                          // blocks of a pack region
 // ring-stage bytes of a Q8_0 job of jb blocks (8: a whole region; 4: half of
 // its codes and half of its scales)
 __host__ __device__ inline int tc_q8_0_job_bytes(int jb) { return jb * (512 + 32); }
-constexpr int TC_MIN_M = 5;  // activation rows from which the tensor-core path is taken
+constexpr int TC_MIN_M = 5;  // activation rows from which the tensor-core path is taken (Q4_0)
+constexpr int TC_Q6_K_MIN_M = 7;  // the same for Q6_K
 constexpr int TC_MAX_STAGES = 6;
 
 struct TcArgs {
@@ -70,7 +77,7 @@ struct TcArgs {
     int64_t ldr;
     const uint8_t* w0;  // Q8_0: the packed weights (the copies read them directly)
     const uint8_t* w1;
-    int K, N, N2;       // Q4_0: N, N2 multiples of 16 and K of 1024; Q8_0: K a multiple of 256
+    int K, N, N2;       // Q4_0, Q6_K: N, N2 multiples of 16 and K of 1024; Q8_0: K a multiple of 256
     int stages;         // ring stages per warp
     int jb;             // blocks per job (8 or 16)
     int nkb_max;        // activation blocks staged per CTA (the largest K part)
@@ -84,8 +91,11 @@ struct TcSmem {
 
 constexpr int TC_TAB_INTS = 4 + 3 * (TC_THREADS / 32);  // the split-tile table
 
-// nibs / dsb: bytes of a ring stage's codes / scales (Q8_0: the whole job / 0)
-__host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_tiles, int nibs, int dsb)
+// nibs / dsb: bytes of a ring stage's codes / scales (Q8_0: the whole job / 0);
+// metab: meta bytes per (block, 8-row tile): 64, or 128 for Q6_K (two
+// accumulator starts)
+__host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_tiles, int nibs, int dsb,
+                                          int metab = 64)
 {
     const uint32_t NT = (uint32_t)(M + 7) / 8;
     TcSmem s;
@@ -93,7 +103,7 @@ __host__ __device__ inline TcSmem tc_smem(int M, int W, int S, int nkb, int out_
     s.nib = o;  o += (uint32_t)W * S * nibs;  // Q4_0: 1024-byte aligned stages (128-byte swizzle atoms)
     s.ds = o;   o += (uint32_t)W * S * dsb;
     s.act = o;  o += (uint32_t)nkb * M * 64;        // B fragments, [block][row][4 lanes] x 16 B
-    s.meta = o; o += (uint32_t)nkb * NT * 64;       // [block][8-row tile][4 lanes] x {d_a, d_a, C, C}
+    s.meta = o; o += (uint32_t)nkb * NT * metab;    // [block][8-row tile][4 lanes] x {d_a, d_a, C, C (, C1, C1, -, -)}
     s.out = o;  o += (uint32_t)out_tiles * 32 * NT * 16;
     s.tab = o;  o += TC_TAB_INTS * 4;
     s.bar = o;  o += ((uint32_t)W * S + 1) * 8;     // ring barriers, then the activation's
@@ -236,7 +246,11 @@ __device__ __forceinline__ uint32_t q8_f16x2(uint32_t w)
 // t fastest, then n: phase 1 reads the lane's two code words (and the meta is
 // written), phase 2, after every raw byte has been read, writes the lane's
 // 16-byte B fragment; both are free of bank conflicts.
-template <int M>
+// Q6: the Q6_K meta, 32 B per lane: {d_a, d_a', C0, C0', C1, C1', 0, 0} with
+// the two MMAs' own starts, C0 = -1056 sum_{i<16} q_a (codes 1024 + q against
+// q_a: (q - 32) q_a = (1024 + q) q_a - 1056 q_a) and C1 = -96 sum_{i>=16} q_a
+// (codes 1024 + 16 q against q_a / 16: 64 q_a + q q_a - 96 q_a).
+template <int M, bool Q6 = false>
 __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const uint8_t* raw, int nkb, int rstride)
 {
     constexpr int NT = (M + 7) / 8;
@@ -263,9 +277,17 @@ __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const ui
         s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 2);
         if (tt == 0) {
             const int nt = n >> 3, c = n & 7;
-            float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
-            mp[c & 1] = da;
-            mp[2 + (c & 1)] = (float)(-1032 * s_lo - 72 * s_hi);
+            if constexpr (Q6) {
+                float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 8;
+                mp[c & 1] = da;
+                mp[2 + (c & 1)] = (float)(-1056 * s_lo);
+                mp[4 + (c & 1)] = (float)(-96 * s_hi);
+                mp[6 + (c & 1)] = 0.0f;
+            } else {
+                float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
+                mp[c & 1] = da;
+                mp[2 + (c & 1)] = (float)(-1032 * s_lo - 72 * s_hi);
+            }
         }
     }
     __syncthreads();  // the raw bytes are all read
@@ -336,6 +358,109 @@ __device__ __forceinline__ void tc_job(const uint8_t* sn, const uint8_t* sd, con
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[nt][i] += jacc[nt][i];
+}
+
+// ---------------------------------------------------------------------------
+// Q6_K over the existing pack (a row's chunk tile: ql[32 blocks][16 B], then
+// qh[32][8 B], then sc[32][2 B]; the chunk's superblock scales d[4 rows][4]
+// after the four tiles).  Block value v < 16 is the low nibble of ql byte v
+// and v >= 16 the high nibble of byte v - 16; its two high bits are bits
+// 2 (v / 8) of qh byte v % 8.  Lane t takes values 4t .. 4t+3 and 16 + 4t ..
+// 16 + 4t + 3 (the K order the activation is staged in): one ql word and one
+// qh word per row and block, the qh word shifted right by 2 (t / 2) so that
+// byte j holds value 4t + j's high bits at bits 0-1 and value 16 + 4t + j's
+// at bits 4-5.
+// ---------------------------------------------------------------------------
+
+// Four codes of a row as two f16x2 A registers per MMA: (ql & LO) | (hi & HM)
+// | 0x6400 per half = 1024 + q (LO = 0x000F000F, HM = 0x00300030) or
+// 1024 + 16 q (LO = 0x00F000F0, HM = 0x03000300), exactly.
+template <uint32_t LO, uint32_t HM>
+__device__ __forceinline__ uint32_t q6_f16x2(uint32_t ql, uint32_t hi)
+{
+    return (ql & LO) | (hi & HM) | 0x64006400u;
+}
+
+// int8 byte k of w (stored biased: byte ^ 0x80) as a float, exactly:
+// 0x4B0000XX is 2^23 + XX.  (k is a constant once the caller's loop unrolls.)
+__device__ __forceinline__ float sc_f32(uint32_t w_biased, int k)
+{
+    return __int_as_float((int)__byte_perm(w_biased, 0x4B000000u, 0x7540u | (uint32_t)k)) - 8388736.0f;
+}
+
+// One Q6_K job: superblock h of the chunk (8 blocks) in ring stage sq (ql box,
+// then the qh box at 2048) and ss (sc box, then the superblock scales at 256)
+// against staged blocks kb .. kb + 7.  Per block the two MMAs return the
+// exact integer dots of the two 16-value halves, combined with the int8
+// subscales (exact) and scaled by d_a in fp32; d6 once per job.
+template <int M>
+__device__ __forceinline__ void tc_job_q6_k(const uint8_t* sq, const uint8_t* ss, const uint8_t* act,
+                                            const float* meta, int kb, int h, int g, int t,
+                                            float (&acc)[(M + 7) / 8][4])
+{
+    constexpr int NT = (M + 7) / 8;
+    float jacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) jacc[nt][i] = 0.0f;
+    // ql: row g in line g (128-byte swizzle: piece p at p ^ (g & 7)), row g + 8
+    // 1024 B on; qh: row g in line g of 64 B (64-byte swizzle: piece c at
+    // c ^ ((g / 2) & 3)), row g + 8 512 B on
+    const uint8_t* qlg = sq + g * 128 + 4 * t;
+    const uint8_t* qhg = sq + 2048 + g * 64 + 4 * (t & 1);
+    const int hsw = (g >> 1) & 3, sh = 2 * (t >> 1);
+    const uint4 sva = *reinterpret_cast<const uint4*>(ss + g * 16);  // rows g, g + 8: sc of the 8 blocks
+    const uint4 svb = *reinterpret_cast<const uint4*>(ss + (g + 8) * 16);
+    const uint32_t sca[4] = {sva.x ^ 0x80808080u, sva.y ^ 0x80808080u, sva.z ^ 0x80808080u, sva.w ^ 0x80808080u};
+    const uint32_t scb[4] = {svb.x ^ 0x80808080u, svb.y ^ 0x80808080u, svb.z ^ 0x80808080u, svb.w ^ 0x80808080u};
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int swq = (p ^ g) << 4;
+        const int hoff = (((p >> 1) ^ hsw) << 4) + (p & 1) * 8;
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(qlg + swq);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(qlg + 1024 + swq);
+        const uint32_t ha = *reinterpret_cast<const uint32_t*>(qhg + hoff) >> sh;
+        const uint32_t hb = *reinterpret_cast<const uint32_t*>(qhg + 512 + hoff) >> sh;
+        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+        const uint32_t ha4 = ha << 4, hb4 = hb << 4, ha_4 = ha >> 4, hb_4 = hb >> 4;
+        const uint32_t A0[4] = {q6_f16x2<0x000F000Fu, 0x00300030u>(wa, ha4), q6_f16x2<0x000F000Fu, 0x00300030u>(wb, hb4),
+                                q6_f16x2<0x000F000Fu, 0x00300030u>(wa8, ha_4),
+                                q6_f16x2<0x000F000Fu, 0x00300030u>(wb8, hb_4)};
+        const uint32_t A1[4] = {q6_f16x2<0x00F000F0u, 0x03000300u>(wa, ha4), q6_f16x2<0x00F000F0u, 0x03000300u>(wb, hb4),
+                                q6_f16x2<0x00F000F0u, 0x03000300u>(wa8, ha_4),
+                                q6_f16x2<0x00F000F0u, 0x03000300u>(wb8, hb_4)};
+        // subscales of halves 0 and 1 of block p: bytes 2p, 2p + 1 of the row's 16
+        const float s0a = sc_f32(sca[p >> 1], 2 * (p & 1)), s1a = sc_f32(sca[p >> 1], 2 * (p & 1) + 1);
+        const float s0b = sc_f32(scb[p >> 1], 2 * (p & 1)), s1b = sc_f32(scb[p >> 1], 2 * (p & 1) + 1);
+        const int b = kb + p;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int n = nt * 8 + g < M ? nt * 8 + g : M - 1;  // rows past M: any staged row (unused)
+            const uint4 B = *reinterpret_cast<const uint4*>(act + (((size_t)b * M + n) * 4 + t) * 16);
+            const float* mp = meta + (((size_t)b * NT + nt) * 4 + t) * 8;
+            const float4 md = *reinterpret_cast<const float4*>(mp);
+            const float2 mc = *reinterpret_cast<const float2*>(mp + 4);
+            float d0[4], d1[4];
+            mma_f16_16816(d0, A0, B.x, B.y, md.z, md.w, md.z, md.w);
+            mma_f16_16816(d1, A1, B.z, B.w, mc.x, mc.y, mc.x, mc.y);
+            jacc[nt][0] = fmaf(md.x, fmaf(s1a, d1[0], s0a * d0[0]), jacc[nt][0]);
+            jacc[nt][1] = fmaf(md.y, fmaf(s1a, d1[1], s0a * d0[1]), jacc[nt][1]);
+            jacc[nt][2] = fmaf(md.x, fmaf(s1b, d1[2], s0b * d0[2]), jacc[nt][2]);
+            jacc[nt][3] = fmaf(md.y, fmaf(s1b, d1[3], s0b * d0[3]), jacc[nt][3]);
+        }
+    }
+    // superblock scales of rows g, g + 8: group g / 4, row g % 4, superblock h
+    const uint8_t* dp = ss + 256 + (g >> 2) * 32 + (g & 3) * 8 + h * 2;
+    const float da6 = __half2float(*reinterpret_cast<const __half*>(dp));
+    const float db6 = __half2float(*reinterpret_cast<const __half*>(dp + 64));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        acc[nt][0] = fmaf(da6, jacc[nt][0], acc[nt][0]);
+        acc[nt][1] = fmaf(da6, jacc[nt][1], acc[nt][1]);
+        acc[nt][2] = fmaf(db6, jacc[nt][2], acc[nt][2]);
+        acc[nt][3] = fmaf(db6, jacc[nt][3], acc[nt][3]);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -506,14 +631,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int t1 = narrow ? (int)((uint32_t)(cl + 1) * (uint32_t)T / (uint32_t)ncl) : (int)((int64_t)(cl + 1) * T / ncl);
     const int ntile = t1 - t0;
     const int JB = a.jb;
-    const int NIB = FMT == TCF_Q8_0 ? tc_q8_0_job_bytes(JB) : tc_nib_bytes(JB), DSB = FMT == TCF_Q8_0 ? 0 : tc_ds_bytes(JB);
+    const int NIB = FMT == TCF_Q8_0 ? tc_q8_0_job_bytes(JB) : FMT == TCF_Q6_K ? TC_Q6_K_NIB : tc_nib_bytes(JB);
+    const int DSB = FMT == TCF_Q8_0 ? 0 : FMT == TCF_Q6_K ? TC_Q6_K_DS : tc_ds_bytes(JB);
     const int JPC = CHUNK / JB, JPC_LOG = JB > TC_LINE_JB ? 1 : 2;  // jobs per 32-block chunk
     const int njb = NB / JB;
     const int jb0 = rank * njb / C, jb1 = (rank + 1) * njb / C;
     const int jpt = jb1 - jb0;  // jobs per tile
     const int J = ntile * jpt;
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
-    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB);
+    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB, FMT == TCF_Q6_K ? 128 : 64);
     uint8_t* nib = smem + sl.nib;
     uint8_t* ds = smem + sl.ds;
     uint8_t* act = smem + sl.act;
@@ -531,7 +657,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (warp == 0) mbar_init(abar, 1);
         fence_barrier_init();
     }
-    if (FMT == TCF_Q4_0 && warp == 1 && lane < (PAIR ? 4 : 2)) {
+    if (FMT != TCF_Q8_0 && warp == 1 && lane < (PAIR || FMT == TCF_Q6_K ? 4 : 2)) {
         // bring the copies' descriptors on chip while the prologue runs
         const CUtensorMap* map = lane == 0 ? &tn0 : lane == 1 ? &td0 : lane == 2 ? &tn1 : &td1;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -584,6 +710,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     bulk_g2s(dst, src + hh * JB * 512, JB * 512, bar, pol);
                     bulk_g2s(dst + JB * 512, src + TC_Q8_0_CODES + hh * JB * 32, JB * 32, bar, pol);
                 }
+            } else if constexpr (FMT == TCF_Q6_K) {
+                // superblock h of chunk c for the tile's 16 rows: ql, qh and sc
+                // boxes of the row tiles, then the chunk's superblock scales
+                uint8_t* ds = wds + (size_t)iss_slot * DSB;
+                tma_load_4d(dst, &tn0, h * 128, 0, c, igrp, bar, pol);
+                tma_load_4d(dst + TC_ROWS * 128, &td0, CHUNK * 16 + h * 64, 0, c, igrp, bar, pol);
+                tma_load_4d(ds, &tn1, CHUNK * 24 + h * 16, 0, c, igrp, bar, pol);
+                tma_load_3d(ds + TC_ROWS * 16, &td1, 0, c, igrp, bar, pol);
             } else {
                 const CUtensorMap* map = isec ? &tn1 : &tn0;
                 tma_load_4d(dst, map, h * JB * 16, 0, c, igrp, bar, pol);
@@ -655,7 +789,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     alive = __syncthreads_and(alive);
     if (alive) {
         if constexpr (FMT == TCF_Q8_0) tc_stage_act_q8_0<M>(act, meta, raw, jpt * JB, (int)rstride);
-        else tc_stage_act<M>(act, meta, raw, jpt * JB, (int)rstride);
+        else tc_stage_act<M, FMT == TCF_Q6_K>(act, meta, raw, jpt * JB, (int)rstride);
     }
     __syncthreads();  // the tile is built
     float acc[NT][4];
@@ -683,6 +817,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         ++consumed;
         if constexpr (FMT == TCF_Q8_0) tc_job_q8_0<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, JB, g, t, acc);
+        else if constexpr (FMT == TCF_Q6_K)
+            tc_job_q6_k<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB,
+                           (jb0 + kj) & (JPC - 1), g, t, acc);
         else tc_job<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB, JB, g, t, acc);
         __syncwarp();
         if (++slot == S) {

@@ -3,11 +3,29 @@
 // the per-device opt-in.  Included by one translation unit per format.
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include "launch.cuh"
 #include "mmvq_tc.cuh"
 
 namespace qgemv {
 namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
 
 struct TcPlan {
     int C, grid, S, jb, nkb_max, out_tiles;
@@ -71,7 +89,8 @@ int tc_max_clusters(int dev, int ci, size_t smem)
     return cache[dev][ci];
 }
 
-// The cheapest plan over job sizes JB (Q4_0: 16 or 8 blocks; Q8_0: 8 or 4)
+// The cheapest plan over job sizes JB (Q4_0: 16 or 8 blocks; Q8_0: 8 or 4;
+// Q6_K: 8)
 // and cluster sizes C:
 // the largest per-CTA job count over 16 warps (the critical path) in units of
 // 8 blocks, where a 16-block Q4_0 job counts 0.85 x 2 units (measured: it
@@ -88,12 +107,13 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
     double best_cost = 0.0;
     bool found = false;
     // Q4_0: 16- then 8-block jobs; Q8_0: whole 8-block regions, then halves
-    const int jb_first = FMT == TCF_Q8_0 ? TC_Q8_0_JOB_BLOCKS : 2 * TC_LINE_JB;
+    const int jb_first = FMT == TCF_Q8_0 ? TC_Q8_0_JOB_BLOCKS : FMT == TCF_Q6_K ? TC_LINE_JB : 2 * TC_LINE_JB;
     const int jb_last = FMT == TCF_Q8_0 ? TC_Q8_0_JOB_BLOCKS / 2 : TC_LINE_JB;
+    const int metab = FMT == TCF_Q6_K ? 128 : 64;
     for (int jb = jb_first; jb >= jb_last; jb /= 2) {
         const int njb = NB / jb;
-        const int nibs = FMT == TCF_Q8_0 ? tc_q8_0_job_bytes(jb) : tc_nib_bytes(jb);
-        const int dsb = FMT == TCF_Q8_0 ? 0 : tc_ds_bytes(jb);
+        const int nibs = FMT == TCF_Q8_0 ? tc_q8_0_job_bytes(jb) : FMT == TCF_Q6_K ? TC_Q6_K_NIB : tc_nib_bytes(jb);
+        const int dsb = FMT == TCF_Q8_0 ? 0 : FMT == TCF_Q6_K ? TC_Q6_K_DS : tc_ds_bytes(jb);
         for (int ci = 0; ci < 4; ++ci) {
             const int C = TC_CLUSTERS[ci];
             if (njb < C) break;
@@ -103,7 +123,7 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
             // shared memory at the deepest ring that fits
             int64_t ncl = C == 1 ? di.sms : 0;
             if (C > 1) {
-                if (tc_smem(M, W, 2, nkb, 0, nibs, dsb).bytes > (uint32_t)di.smem_optin) continue;
+                if (tc_smem(M, W, 2, nkb, 0, nibs, dsb, metab).bytes > (uint32_t)di.smem_optin) continue;
                 ncl = tc_max_clusters<FMT, M, PAIR>(dev, ci, (size_t)di.smem_optin);
                 if (ncl <= 0) continue;
             }
@@ -113,7 +133,7 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
             int64_t waves = 1;
             auto deepest = [&](int out_tiles) {
                 for (int s = TC_MAX_STAGES; s >= 2; --s)
-                    if (tc_smem(M, W, s, nkb, out_tiles, nibs, dsb).bytes <= (uint32_t)di.smem_optin) return s;
+                    if (tc_smem(M, W, s, nkb, out_tiles, nibs, dsb, metab).bytes <= (uint32_t)di.smem_optin) return s;
                 return 0;
             };
             int S = deepest(C > 1 ? tiles : 0);
@@ -121,8 +141,8 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
                 // The combine area of one resident wave's tiles does not fit
                 // (very large N): launch more clusters than are resident, in
                 // waves, each with as many tiles as the area holds.
-                const int64_t per_tile = tc_smem(M, W, 2, nkb, 1, nibs, dsb).bytes - tc_smem(M, W, 2, nkb, 0, nibs, dsb).bytes;
-                const int64_t room = (int64_t)di.smem_optin - tc_smem(M, W, 2, nkb, 0, nibs, dsb).bytes;
+                const int64_t per_tile = tc_smem(M, W, 2, nkb, 1, nibs, dsb, metab).bytes - tc_smem(M, W, 2, nkb, 0, nibs, dsb, metab).bytes;
+                const int64_t room = (int64_t)di.smem_optin - tc_smem(M, W, 2, nkb, 0, nibs, dsb, metab).bytes;
                 const int64_t fit = room / per_tile;
                 if (fit >= 1) {
                     ngrid = (T + fit - 1) / fit;
@@ -146,7 +166,7 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
                 best.jb = jb;
                 best.nkb_max = nkb;
                 best.out_tiles = out_tiles;
-                best.smem = tc_smem(M, W, S, nkb, out_tiles, nibs, dsb).bytes;
+                best.smem = tc_smem(M, W, S, nkb, out_tiles, nibs, dsb, metab).bytes;
             }
         }
     }

@@ -295,6 +295,23 @@ int qgemv_set_q4_0_tensor_cores(int enable);
  * nothing; may query the current device.  (Not from the pages.) */
 int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info);
 
+/* qgemv_set_q6_k_tensor_cores - the kernel family of qgemv_q6_k.  The
+ * tensor-core kernel takes shapes with M >= 7, N a multiple of 16 and K a
+ * multiple of 1024 (per block two f16 mma.sync steps return the exact integer
+ * dots of the two 16-value halves, combined with the int8 subscales exactly,
+ * then d_a per block and d6 per superblock in fp32).  mode 1 (the default)
+ * takes it only where it measured faster than the dp4a kernel: N below 16
+ * row groups of 4 per SM and either M >= 12 or K >= 16384; mode 2 takes it
+ * for every shape it accepts; mode 0 never.  The LM-head calls
+ * (lmhead_q6_k_*) always run on the dp4a kernel.  Process-wide; returns the
+ * previous mode.  (Not from the pages.)
+ *
+ * qgemv_q6_k_plan - which kernel qgemv_q6_k would launch for this shape;
+ * writes info[4] as qgemv_q4_0_plan.  Enqueues nothing.  (Not from the
+ * pages.) */
+int qgemv_set_q6_k_tensor_cores(int mode);
+int qgemv_q6_k_plan(int M, int K, int N, int* info);
+
 /* ---- NEXT-4: a further format, Q8_0 ------------------------------------ */
 
 /* Q8_0 (named on the pages among further quantization formats, defined as in

@@ -239,6 +239,98 @@ def test_qgemv_q4_0_pair_unit_scales_exact(ops):
         assert np.array_equal(_np(y).astype(np.float64), y_ref)
 
 
+# ---------------------------------------------------------------- Q6_K on the tensor cores
+Q6_TC_SHAPES = [(7, 1024, 16), (8, 2048, 160), (9, 5120, 336), (12, 1024, 4096), (16, 2048, 1040),
+                (17, 5120, 272), (9, 17408, 320), (12, 17408, 64), (7, 9216, 784), (17, 1024, 48)]
+
+
+@pytest.mark.parametrize("mode", [2, 0])  # 2: the tensor cores for every shape they take; 0: dp4a
+@pytest.mark.parametrize("M,K,N", Q6_TC_SHAPES)
+def test_qgemv_q6_k_tensor_core_shapes(ops, M, K, N, mode):
+    prev = ops.set_q6_k_tensor_cores(mode)
+    try:
+        assert ops.qgemv_q6_k_plan(M, K, N)["tensor_cores"] == (mode == 2)
+        y, y_ref, S = _gemv_case(ops, "q6_k", M, K, N, seed=5 * M + K + N)
+    finally:
+        ops.set_q6_k_tensor_cores(prev)
+    r = C.check_close(y, y_ref, S)
+    assert r["ok"], r
+
+
+def test_qgemv_q6_k_tensor_core_plans(ops):
+    # default mode: only where they measured faster (the dp4a kernel splits K:
+    # N < 16 row groups per SM; and M >= 12 or K >= 16384)
+    assert ops.qgemv_q6_k_plan(7, 17408, 5120)["tensor_cores"]
+    assert ops.qgemv_q6_k_plan(9, 17408, 5120)["cluster"] > 1
+    assert ops.qgemv_q6_k_plan(12, 5120, 5120)["tensor_cores"]
+    assert not ops.qgemv_q6_k_plan(9, 5120, 5120)["tensor_cores"]
+    assert not ops.qgemv_q6_k_plan(12, 5120, 17408)["tensor_cores"]
+    assert not ops.qgemv_q6_k_plan(17, 5120, 248320)["tensor_cores"]
+    assert not ops.qgemv_q6_k_plan(6, 17408, 5120)["tensor_cores"]  # M < 7: the dp4a kernel
+    prev = ops.set_q6_k_tensor_cores(2)
+    try:
+        assert not ops.qgemv_q6_k_plan(9, 5120, 17400)["tensor_cores"]  # N % 16
+        assert not ops.qgemv_q6_k_plan(9, 5376, 17408)["tensor_cores"]  # K % 1024
+        assert not ops.qgemv_q6_k_plan(6, 5120, 248320)["tensor_cores"]  # M < 7
+        assert ops.qgemv_q6_k_plan(17, 5120, 248320)["tensor_cores"]
+        for M, K, N in Q6_TC_SHAPES:
+            p = ops.qgemv_q6_k_plan(M, K, N)
+            assert p["tensor_cores"] and p["stages"] >= 2 and p["grid"] % p["cluster"] == 0
+    finally:
+        ops.set_q6_k_tensor_cores(prev)
+
+
+def _q6_k_unit_case(M, K, N, seed, sc_lo, sc_hi):
+    """Q6_K weights with d6 = 1 and subscales in [sc_lo, sc_hi], integer
+    activations in [-2, 2] whose every block holds a +-127 (d_a = 1): every
+    output is an integer sum of exact block dots."""
+    w = synth.q6_k_weights(N, K, seed=seed, d_lo=1.0, d_hi=1.0)
+    g = np.random.default_rng(seed + 1)
+    w[:, :, 192:208] = g.integers(sc_lo, sc_hi + 1, size=(N, K // 256, 16)).astype(np.int8).view(np.uint8)
+    x = g.integers(-2, 3, size=(M, K)).astype(np.float32)
+    x[:, ::32] = np.where(g.integers(0, 2, size=(M, K // 32)) == 1, 127.0, -127.0).astype(np.float32)
+    return w, x
+
+
+@pytest.mark.parametrize("mode", [2, 0])
+@pytest.mark.parametrize("M,K,N,sc", [(9, 1024, 48, (-3, 3)), (17, 2048, 32, (-3, 3)), (12, 1024, 64, (-128, -127)),
+                                      (8, 1024, 32, (126, 127))])
+def test_qgemv_q6_k_unit_scales_exact(ops, M, K, N, sc, mode):
+    # with d6 = 1 and d_a = 1 every partial sum is an integer below 2^24 (S
+    # bounds them), so both paths must reproduce the oracle bit for bit,
+    # including the subscale extremes -128 and 127
+    w, x = _q6_k_unit_case(M, K, N, M + K + N, *sc)
+    xq_ref = oracle.quantize_q8_1(x)
+    assert np.all(xq_ref[:, :, 0:2].view(np.float16) == 1.0)
+    y_ref, S = oracle.qgemv_q6_k(w, xq_ref)
+    assert np.all(S < 2.0 ** 24) and np.all(y_ref == np.round(y_ref))
+    prev = ops.set_q6_k_tensor_cores(mode)
+    try:
+        assert ops.qgemv_q6_k_plan(M, K, N)["tensor_cores"] == (mode == 2)
+        y = _np(ops.qgemv_q6_k(ops.qpack_q6_k(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
+    finally:
+        ops.set_q6_k_tensor_cores(prev)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def test_qgemv_q6_k_tensor_cores_stride(ops):
+    M, K, N, ldy = 9, 2048, 96, 112
+    w = synth.q6_k_weights(N, K, seed=25)
+    x = synth.activations(M, K, seed=26)
+    prev = ops.set_q6_k_tensor_cores(2)
+    try:
+        assert ops.qgemv_q6_k_plan(M, K, N)["tensor_cores"]
+        y = torch.full((M, ldy), 5.0, device=DEV)
+        ops.qgemv_q6_k(ops.qpack_q6_k(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N, y=y[:, :N])
+    finally:
+        ops.set_q6_k_tensor_cores(prev)
+    yy = _np(y)
+    y_ref, S = oracle.qgemv_q6_k(w, oracle.quantize_q8_1(x))
+    assert C.check_close(yy[:, :N], y_ref, S)["ok"]
+    assert np.all(yy[:, N:] == 5.0)
+    assert ops.qgemv_take_wait_timeouts() == 0
+
+
 def test_qgemv_q4_0_tensor_cores_stride_and_padding(ops):
     M, K, N, ldy = 6, 2048, 96, 112
     w = synth.q4_0_weights(N, K, seed=15)
@@ -396,7 +488,7 @@ def test_qgemv_q8_0_plans(ops):
 
 
 @pytest.mark.parametrize("fmt,M,N", [("q8_0", 17, 40000), ("q8_0", 12, 40000), ("q4_0", 17, 40000),
-                                     ("q4_0", 12, 40000)])
+                                     ("q4_0", 12, 40000), ("q6_k", 17, 40000), ("q6_k", 12, 40000)])
 def test_large_n_wave_plans_sampled_rows(ops, fmt, M, N):
     # more clusters than are resident (the combine area holds a wave's tiles
     # only): outputs checked on a sample of rows, which the oracle computes
@@ -408,6 +500,15 @@ def test_large_n_wave_plans_sampled_rows(ops, fmt, M, N):
         w = synth.q8_0_weights(N, K, seed=N + M)
         y = _np(ops.qgemv_q8_0(ops.qpack_q8_0(_t(w), N, K), xq, M, K, N))
         ref = oracle.qgemv_q8_0
+    elif fmt == "q6_k":
+        w = synth.q6_k_weights(N, K, seed=N + M)
+        prev = ops.set_q6_k_tensor_cores(2)  # large N: taken only when forced
+        try:
+            assert ops.qgemv_q6_k_plan(M, K, N)["tensor_cores"]
+            y = _np(ops.qgemv_q6_k(ops.qpack_q6_k(_t(w), N, K), xq, M, K, N))
+        finally:
+            ops.set_q6_k_tensor_cores(prev)
+        ref = oracle.qgemv_q6_k
     else:
         assert ops.qgemv_q4_0_plan(M, K, N)["tensor_cores"]
         w = synth.q4_0_weights(N, K, seed=N + M)
