@@ -54,11 +54,12 @@ def _load():
             lib.oracle_f16_to_f64.restype = ctypes.c_double
             lib.oracle_quantize_q8_1.argtypes = [P, L, I, I, P]
             lib.oracle_rmsnorm_quantize_q8_1.argtypes = [P, L, P, ctypes.c_float, I, I, P]
-            for name in ("oracle_dequant_q4_0", "oracle_dequant_q6_k", "oracle_dequant_q8_1", "oracle_dequant_q8_0"):
+            for name in ("oracle_dequant_q4_0", "oracle_dequant_q6_k", "oracle_dequant_q8_1", "oracle_dequant_q8_0",
+                         "oracle_dequant_q4_k"):
                 getattr(lib, name).argtypes = [P, I, I, P]
             for name in ("oracle_block_dots_q4_0", "oracle_block_dots_q6_k"):
                 getattr(lib, name).argtypes = [P, P, I, I, I, P]
-            for name in ("oracle_qgemv_q4_0", "oracle_qgemv_q6_k", "oracle_qgemv_q8_0"):
+            for name in ("oracle_qgemv_q4_0", "oracle_qgemv_q6_k", "oracle_qgemv_q8_0", "oracle_qgemv_q4_k"):
                 getattr(lib, name).argtypes = [P, P, I, I, I, P, P, I]
             lib.oracle_top1_f64.argtypes = [P, L, I, I, P]
             lib.oracle_top1_f32.argtypes = [P, L, I, I, P]
@@ -164,6 +165,32 @@ def dequant_q8_0(w: np.ndarray) -> np.ndarray:
     return out
 
 
+def qgemv_q4_k(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
+    """canonical Q4_K w [N, K/256, 144] = {fp16 d, fp16 dmin, scales[12], qs[128]},
+    Q8_1 xq [M, K/32, 36] -> (y, S) fp64 [M, N]:
+    y = sum_b (d sc_b d_a I_b - dmin m_b d_a A_b), I_b = sum q_w q_a, A_b = sum q_a;
+    S = sum_b (|first term| + |second term|)."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    N, ns = w.shape[0], w.shape[1]
+    M = xq.shape[0]
+    assert xq.shape[1] == ns * 8 and w.shape[2] == 144
+    y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_qgemv_q4_k(_ptr(w), _ptr(xq), M, ns * 256, N, _ptr(y), _ptr(S),
+                              nthreads or default_threads())
+    return y, S
+
+
+def dequant_q4_k(w: np.ndarray) -> np.ndarray:
+    """[N, K/256, 144] -> fp64 [N, K] (the C dequantizer)."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    N, ns, _ = w.shape
+    out = np.zeros((N, ns * 256), dtype=np.float64)
+    _load().oracle_dequant_q4_k(_ptr(w), N, ns * 256, _ptr(out))
+    return out
+
+
 def qgemv_q6_k(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
     """canonical Q6_K w [N, K/256, 210], Q8_1 xq [M, K/32, 36] -> (y, S) fp64 [M, N]."""
     w = np.ascontiguousarray(w, dtype=np.uint8)
@@ -259,6 +286,22 @@ def dequant_q8_0_np(w: np.ndarray) -> np.ndarray:
     d = _f16(w[:, :, 0:2].copy().view(np.uint16)[:, :, 0])
     q = w[:, :, 2:34].copy().view(np.int8).astype(np.float64)
     return (d[:, :, None] * q).reshape(w.shape[0], -1)
+
+
+def dequant_q4_k_np(w: np.ndarray) -> np.ndarray:
+    """[N, K/256, 144] -> fp64 [N, K] (numpy, written apart from the C code):
+    the eight (scale, min) pairs unpacked with array bit operations, the codes
+    as 4 chunks x (32 low nibbles, then the 32 high nibbles)."""
+    N, ns, _ = w.shape
+    d = _f16(w[:, :, 0:2].copy().view(np.uint16)[:, :, 0])
+    dmin = _f16(w[:, :, 2:4].copy().view(np.uint16)[:, :, 0])
+    s = w[:, :, 4:16].astype(np.int64)
+    sc = np.concatenate([s[:, :, 0:4] & 63, (s[:, :, 8:12] & 15) | ((s[:, :, 0:4] >> 6) << 4)], axis=2)
+    mn = np.concatenate([s[:, :, 4:8] & 63, (s[:, :, 8:12] >> 4) | ((s[:, :, 4:8] >> 6) << 4)], axis=2)
+    qs = w[:, :, 16:144].astype(np.int64).reshape(N, ns, 4, 32)
+    q = np.stack([qs & 15, qs >> 4], axis=3).reshape(N, ns, 8, 32)  # sub-block 2c: low, 2c + 1: high
+    v = d[:, :, None, None] * sc[:, :, :, None] * q - dmin[:, :, None, None] * mn[:, :, :, None]
+    return v.reshape(N, ns * 256)
 
 
 def dequant_q8_1_np(xq: np.ndarray) -> np.ndarray:

@@ -24,6 +24,11 @@
  *     production record", sections "Why this was slow" and "Exactness and
  *     safety contracts" ([5120, 248320] Q6_K output weight) and "Memory and
  *     startup" (16 subscales and one fp16 scale per 256 values).
+ *   - Q8_0 and Q4_K weights (named among the further K-quant formats of
+ *     "Qwen3.6 27B Q4_0 DFlash/SYCL closure" and of the DFlash KV-cache
+ *     page): Q8_0 = blocks of 32, fp16 d, int8 q, value d * q; Q4_K =
+ *     superblocks of 256, fp16 d and dmin, eight 6-bit scales and eight
+ *     6-bit mins (one per 32 values), 4-bit q, value d * sc * q - dmin * m.
  *   - Top-1 with the lowest-token-ID finite-tie rule: same page, "Exactness and
  *     safety contracts", item 3.
  *
@@ -43,6 +48,12 @@
  *     with plain sequential packing: the low 4 bits of value i are nibble
  *     (i & 1) of ql[i >> 1], its high 2 bits are bits 2*(i & 3) of qh[i >> 2];
  *     subscale index i >> 4.
+ *   - Q4_K superblock = {fp16 d, fp16 dmin, uint8 scales[12], uint8 qs[128]}
+ *     as in llama.cpp: sub-block j < 4 has scale scales[j] & 63 and min
+ *     scales[j + 4] & 63; j >= 4 has scale (scales[j + 4] & 15) | (scales[j - 4]
+ *     >> 6) << 4 and min (scales[j + 4] >> 4) | (scales[j] >> 6) << 4.  Values
+ *     64 c .. 64 c + 31 are the low nibbles of qs[32 c .. 32 c + 31] and values
+ *     64 c + 32 .. 64 c + 63 their high nibbles; value i is in sub-block i / 32.
  *
  * Build: cc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread (no fast-math).
  */
@@ -104,6 +115,7 @@ static void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (u
 /* ------------------------------------------------------------------ */
 
 #define Q8_0_BYTES 34
+#define Q4_K_BYTES 144
 #define Q8_1_BYTES 36
 #define Q4_0_BYTES 18
 #define Q6_K_BYTES 210
@@ -241,6 +253,42 @@ void oracle_dequant_q8_0(const uint8_t* w, int N, int K, double* out)
         }
 }
 
+/* Q4_K: the scale and min of sub-block j (0..7) of a superblock. */
+static void q4_k_scale_min(const uint8_t* sb, int j, int* sc, int* m)
+{
+    const uint8_t* s = sb + 4;
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *m = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+        *m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+/* Q4_K: the 4-bit code of value i (0..255) of a superblock. */
+static int q4_k_code(const uint8_t* sb, int i)
+{
+    const uint8_t* qs = sb + 16;
+    int c = i / 64, r = i % 64;
+    return r < 32 ? (qs[32 * c + r] & 15) : (qs[32 * c + r - 32] >> 4);
+}
+
+void oracle_dequant_q4_k(const uint8_t* w, int N, int K, double* out)
+{
+    int ns = K / 256;
+    for (int n = 0; n < N; ++n)
+        for (int s = 0; s < ns; ++s) {
+            const uint8_t* sb = w + ((int64_t)n * ns + s) * Q4_K_BYTES;
+            double d = oracle_f16_to_f64(rd16(sb)), dmin = oracle_f16_to_f64(rd16(sb + 2));
+            for (int i = 0; i < 256; ++i) {
+                int sc, m;
+                q4_k_scale_min(sb, i / 32, &sc, &m);
+                out[(int64_t)n * K + 256 * s + i] = d * (double)sc * (double)q4_k_code(sb, i) - dmin * (double)m;
+            }
+        }
+}
+
 void oracle_dequant_q8_1(const uint8_t* xq, int M, int K, double* out)
 {
     int nb = K / 32;
@@ -291,6 +339,21 @@ static int32_t block_dot_q6_k(const uint8_t* sb, int bb, const uint8_t* ablk)
     return J;
 }
 
+/* Q4_K, block bb (sub-block bb) of superblock sb: I = sum_i q(i) * q_a(i)
+ * and A = sum_i q_a(i), the two exact integers of
+ * sum_i (d sc q(i) - dmin m) * d_a q_a(i) = d sc d_a I - dmin m d_a A. */
+static void block_dot_q4_k(const uint8_t* sb, int bb, const uint8_t* ablk, int32_t* I, int32_t* A)
+{
+    int32_t i1 = 0, a1 = 0;
+    for (int t = 0; t < 32; ++t) {
+        int32_t qa = (int32_t)(int8_t)ablk[4 + t];
+        i1 += q4_k_code(sb, 32 * bb + t) * qa;
+        a1 += qa;
+    }
+    *I = i1;
+    *A = a1;
+}
+
 /* I[m][n][b] for every block: the integer dots before any scaling. */
 void oracle_block_dots_q4_0(const uint8_t* w, const uint8_t* xq, int M, int K, int N, int32_t* I)
 {
@@ -319,7 +382,7 @@ void oracle_block_dots_q6_k(const uint8_t* w, const uint8_t* xq, int M, int K, i
 /* ------------------------------------------------------------------ */
 
 typedef struct {
-    int fmt; /* 0 = Q4_0, 1 = Q6_K, 2 = Q8_0 */
+    int fmt; /* 0 = Q4_0, 1 = Q6_K, 2 = Q8_0, 3 = Q4_K */
     const uint8_t* w;
     const uint8_t* xq;
     int M, K, N;
@@ -339,6 +402,19 @@ static void gemv_rows(const gemv_job* j)
                 double da = oracle_f16_to_f64(rd16(ablk));
                 double dw;
                 int32_t I;
+                if (j->fmt == 3) {
+                    /* two terms: d sc d_a I and - dmin m d_a A */
+                    const uint8_t* sb = j->w + ((int64_t)n * ns + b / 8) * Q4_K_BYTES;
+                    int sc, mn;
+                    int32_t A;
+                    q4_k_scale_min(sb, b % 8, &sc, &mn);
+                    block_dot_q4_k(sb, b % 8, ablk, &I, &A);
+                    double t1 = oracle_f16_to_f64(rd16(sb)) * (double)sc * da * (double)I;
+                    double t2 = -oracle_f16_to_f64(rd16(sb + 2)) * (double)mn * da * (double)A;
+                    acc += t1 + t2;
+                    sabs += fabs(t1) + fabs(t2);
+                    continue;
+                }
                 if (j->fmt == 0) {
                     const uint8_t* wblk = j->w + ((int64_t)n * nb + b) * Q4_0_BYTES;
                     dw = oracle_f16_to_f64(rd16(wblk));
@@ -392,6 +468,13 @@ void oracle_qgemv_q8_0(const uint8_t* w, const uint8_t* xq, int M, int K, int N,
                        double* y, double* S, int nthreads)
 {
     gemv_run(2, w, xq, M, K, N, y, S, nthreads);
+}
+
+/* w: canonical Q4_K [N][K/256] x 144 B; S sums both terms' magnitudes. */
+void oracle_qgemv_q4_k(const uint8_t* w, const uint8_t* xq, int M, int K, int N,
+                       double* y, double* S, int nthreads)
+{
+    gemv_run(3, w, xq, M, K, N, y, S, nthreads);
 }
 
 /* w: canonical Q4_0 [N][K/32] x 18 B; xq: Q8_1 [M][K/32] x 36 B;

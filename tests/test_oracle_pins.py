@@ -361,3 +361,75 @@ def test_q8_0_code_sign_and_position():
         w[0, b, 2 + i] = np.int8(s).view(np.uint8)
         y, _ = oracle.qgemv_q8_0(w, xq)
         assert y[0, 0] == s * xd[32 * b + i]
+
+
+# ---------------------------------------------------------------- Q4_K (a further format)
+
+# Twelve scale bytes chosen to exercise every field of the packing, with the
+# (scale, min) pairs worked out by hand from the llama.cpp layout:
+#   j < 4:  scale = byte j & 63, min = byte j + 4 & 63
+#   j >= 4: scale = (byte j + 4 & 15) | (byte j - 4 >> 6) << 4,
+#           min   = (byte j + 4 >> 4) | (byte j >> 6) << 4
+Q4_K_SCALE_BYTES = [0x41, 0x02, 0xC3, 0x04, 0x85, 0x46, 0x07, 0xC8, 0x9A, 0x0B, 0xFC, 0x3D]
+Q4_K_HAND_SC = [1, 2, 3, 4, 26, 11, 60, 13]   # e.g. j = 4: 0x9A & 15 = 10, 0x41 >> 6 = 1 -> 26
+Q4_K_HAND_M = [5, 6, 7, 8, 41, 16, 15, 51]    # e.g. j = 7: 0x3D >> 4 = 3, 0xC8 >> 6 = 3 -> 51
+
+
+def _q4_k_superblock(d: float, dmin: float, scale_bytes, qs) -> np.ndarray:
+    sb = np.zeros(144, dtype=np.uint8)
+    sb[0:2] = np.array([d], dtype=np.float16).view(np.uint8)
+    sb[2:4] = np.array([dmin], dtype=np.float16).view(np.uint8)
+    sb[4:16] = np.asarray(scale_bytes, dtype=np.uint8)
+    sb[16:144] = np.asarray(qs, dtype=np.uint8)
+    return sb
+
+
+def test_q4_k_scale_min_hand_table():
+    # every code 1 (qs bytes 0x11), d = dmin = 1: value = sc_j - m_j per 32-value sub-block
+    w = _q4_k_superblock(1.0, 1.0, Q4_K_SCALE_BYTES, np.full(128, 0x11))[None, None]
+    expect = np.repeat(np.array(Q4_K_HAND_SC, dtype=np.float64) - np.array(Q4_K_HAND_M), 32)
+    assert np.array_equal(oracle.dequant_q4_k(w)[0], expect)
+    assert np.array_equal(oracle.dequant_q4_k_np(w)[0], expect)
+    # codes 0 leave -dmin * m; codes 15 give 15 sc - m
+    w0 = _q4_k_superblock(1.0, 0.5, Q4_K_SCALE_BYTES, np.zeros(128))[None, None]
+    assert np.array_equal(oracle.dequant_q4_k(w0)[0], np.repeat(-0.5 * np.array(Q4_K_HAND_M, dtype=np.float64), 32))
+    w15 = _q4_k_superblock(1.0, 1.0, Q4_K_SCALE_BYTES, np.full(128, 0xFF))[None, None]
+    assert np.array_equal(oracle.dequant_q4_k(w15)[0],
+                          np.repeat(15.0 * np.array(Q4_K_HAND_SC) - np.array(Q4_K_HAND_M), 32))
+
+
+def test_q4_k_code_order_hand_example():
+    # qs[0] = 0x21 and qs[37] = 0x0A, every other byte 0; unit scales, no mins:
+    # value 0 = 1 (low nibble of qs[0]), value 32 = 2 (its high nibble);
+    # qs[37] sits in the second 32-byte group, so value 64 + 5 = 10 and value
+    # 64 + 32 + 5 = 0; everything else is 0
+    unit = [1, 1, 1, 1, 0, 0, 0, 0, 0x01, 0x01, 0x01, 0x01]
+    qs = np.zeros(128, dtype=np.uint8)
+    qs[0], qs[37] = 0x21, 0x0A
+    v = oracle.dequant_q4_k(_q4_k_superblock(1.0, 0.0, unit, qs)[None, None])[0]
+    expect = np.zeros(256)
+    expect[0], expect[32], expect[69] = 1.0, 2.0, 10.0
+    assert np.array_equal(v, expect)
+    assert np.array_equal(oracle.dequant_q4_k_np(_q4_k_superblock(1.0, 0.0, unit, qs)[None, None])[0], expect)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 256, 1), (3, 256, 7), (2, 512, 33), (5, 1024, 16)])
+def test_q4_k_matches_fp64_dequant_matmul(M, K, N):
+    w = synth.q4_k_weights(N, K, seed=500 + K + N)
+    xq = oracle.quantize_q8_1(synth.activations(M, K, seed=600 + M))
+    y, S = oracle.qgemv_q4_k(w, xq)
+    ref = oracle.dequant_q8_1_np(xq) @ oracle.dequant_q4_k_np(w).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * np.maximum(S, 1e-300))
+    assert np.array_equal(oracle.dequant_q4_k(w), oracle.dequant_q4_k_np(w))
+
+
+def test_q4_k_min_term_closed_form():
+    # all codes 0, every min 1 (scale bytes 0x00 x4, 0x01 x4, then 0x10 x4), dmin = 2:
+    # y = -2 * sum of the (dequantized) activation values
+    K, N = 512, 1
+    mins = [0, 0, 0, 0, 1, 1, 1, 1, 0x10, 0x10, 0x10, 0x10]
+    w = np.stack([_q4_k_superblock(0.25, 2.0, mins, np.zeros(128)) for _ in range(K // 256)])[None]
+    x = synth.activations(2, K, seed=7)
+    xq = oracle.quantize_q8_1(x)
+    y, _ = oracle.qgemv_q4_k(w, xq)
+    assert np.allclose(y[:, 0], -2.0 * oracle.dequant_q8_1_np(xq).sum(axis=1), rtol=1e-13, atol=0)
