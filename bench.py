@@ -469,11 +469,15 @@ def run_sweep(args):
     flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)  # twice the L2
     reps = max(3, min(args.steps, 20))
     peak, _ = peaks()
-    pack_bytes = {"q4_0": ops.q4_0_pack_bytes, "q6_k": ops.q6_k_pack_bytes, "q8_0": ops.q8_0_pack_bytes}
-    gemv = {"q4_0": ops.qgemv_q4_0, "q6_k": ops.qgemv_q6_k, "q8_0": ops.qgemv_q8_0}
-    for fmt in ("q4_0", "q6_k", "q8_0"):
+    pack_bytes = {"q4_0": ops.q4_0_pack_bytes, "q6_k": ops.q6_k_pack_bytes, "q8_0": ops.q8_0_pack_bytes,
+                  "q4_k": ops.q4_k_pack_bytes}
+    gemv = {"q4_0": ops.qgemv_q4_0, "q6_k": ops.qgemv_q6_k, "q8_0": ops.qgemv_q8_0, "q4_k": ops.qgemv_q4_k}
+    for fmt in ("q4_0", "q6_k", "q8_0", "q4_k"):
         for N in (5120, 17408, 248320):
             nbytes_w = pack_bytes[fmt](N, K_H)
+            # algorithmic bytes: the canonical size (Q4_K's pack carries 148 B per
+            # 256 values against the canonical 144; the others are equal)
+            nbytes_alg = N * (K_H // 256) * 144 if fmt == "q4_k" else nbytes_w
             w = torch.randint(0, 256, (nbytes_w,), dtype=torch.uint8, generator=g).to(dev)
             for M in (1, 2, 4, 6, 9, 12, 17):
                 x = torch.randn(M, K_H, generator=g).to(dev)
@@ -497,7 +501,7 @@ def run_sweep(args):
                     torch.cuda.synchronize()
                     ts.append(a.elapsed_time(b))
                 us = statistics.median(ts) * 1e3
-                nbytes = nbytes_w + ops.q8_1_bytes(M, K_H)
+                nbytes = nbytes_alg + ops.q8_1_bytes(M, K_H)
                 gbs = nbytes / (us * 1e-6) / 1e9
                 print(json.dumps({"sweep": fmt, "M": M, "K": K_H, "N": N, "us": round(us, 2),
                                   "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),

@@ -194,6 +194,80 @@ int launch_qpack_q8_0(const void* canon, void* pack, int N, int K, cudaStream_t 
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
+// Q4_K (llama.cpp superblock of 256: fp16 d, fp16 dmin, 12 bytes holding
+// eight 6-bit scales and eight 6-bit mins, 128 bytes of 4-bit codes; values
+// 64c .. 64c+31 are the low nibbles of code bytes 32c .. 32c+31, values
+// 64c+32 .. 64c+63 their high nibbles) into the tensor-core pack: per 16-row
+// tile and superblock one 2368-byte region = codes [block p][lane 4g + t] 8 B
+// (word t of row g's, then of row g + 8's, 16 bytes in the Q4_0 nibble order:
+// byte k = value k | value k + 16 << 4 of block p), then [row][p] {scale,
+// min}, then [row] {d, dmin} bits.  Rows past N are zeros.  One thread per
+// (tile, superblock, row).
+__device__ __forceinline__ void q4_k_unpack_scale_min(const uint8_t* s, int j, uint32_t& sc, uint32_t& m)
+{
+    if (j < 4) {
+        sc = s[j] & 63u;
+        m = s[j + 4] & 63u;
+    } else {
+        sc = (s[j + 4] & 15u) | ((uint32_t)(s[j - 4] >> 6) << 4);
+        m = (uint32_t)(s[j + 4] >> 4) | ((uint32_t)(s[j] >> 6) << 4);
+    }
+}
+
+__global__ void qpack_q4_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
+{
+    const int NS = K / QK_K;
+    const int64_t T = (N + 15) / 16;
+    const int64_t total = T * NS * 16;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i & 15);
+        const int64_t ts = i >> 4;
+        const int64_t tau = ts / NS;
+        const int sbi = (int)(ts - tau * NS);
+        const int64_t n = tau * 16 + r;
+        uint8_t* region = pack + (tau * NS + sbi) * 2368;
+        const int g = r & 7, half = r >> 3;
+        if (n >= N) {
+            for (int p = 0; p < 8; ++p) {
+                for (int t = 0; t < 4; ++t)
+                    *reinterpret_cast<uint32_t*>(region + p * 256 + (4 * g + t) * 8 + 4 * half) = 0u;
+                *reinterpret_cast<uint16_t*>(region + 2048 + (r * 8 + p) * 2) = 0;
+            }
+            *reinterpret_cast<uint32_t*>(region + 2304 + r * 4) = 0u;
+            continue;
+        }
+        const uint8_t* sb = canon + (n * NS + sbi) * 144;
+        const uint8_t* qs = sb + 16;
+        for (int p = 0; p < 8; ++p) {
+            const int base = 32 * (p >> 1), shift = 4 * (p & 1);
+            for (int t = 0; t < 4; ++t) {
+                uint32_t word = 0;
+                for (int k = 0; k < 4; ++k) {
+                    const int v = 4 * t + k;  // values v and v + 16 of block p
+                    const uint32_t lo = (qs[base + v] >> shift) & 15u, hi = (qs[base + v + 16] >> shift) & 15u;
+                    word |= (lo | hi << 4) << (8 * k);
+                }
+                *reinterpret_cast<uint32_t*>(region + p * 256 + (4 * g + t) * 8 + 4 * half) = word;
+            }
+            uint32_t sc, m;
+            q4_k_unpack_scale_min(sb + 4, p, sc, m);
+            *reinterpret_cast<uint16_t*>(region + 2048 + (r * 8 + p) * 2) = (uint16_t)(sc | m << 8);
+        }
+        *reinterpret_cast<uint32_t*>(region + 2304 + r * 4) =
+            (uint32_t)sb[0] | (uint32_t)sb[1] << 8 | (uint32_t)sb[2] << 16 | (uint32_t)sb[3] << 24;
+    }
+}
+
+int launch_qpack_q4_k(const void* canon, void* pack, int N, int K, cudaStream_t s)
+{
+    const int64_t total = (int64_t)((N + 15) / 16) * (K / QK_K) * 16;
+    const int64_t grid = total / 256 + 1 < 65535 ? total / 256 + 1 : 65535;
+    qpack_q4_k_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon), static_cast<uint8_t*>(pack),
+                                                     N, K);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
 __global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
 {
     const Layout L = make_layout(FMT_Q4_0, N, K);

@@ -50,8 +50,14 @@ __host__ __device__ inline int tc_nib_bytes(int jb) { return TC_ROWS * jb * 16; 
 __host__ __device__ inline int tc_ds_bytes(int jb) { return TC_ROWS * jb * 2; }
 constexpr int TC_THREADS = 512;
 // Weight formats of the tensor-core kernel: Q4_0 and Q6_K (the existing packs,
-// read by tensor maps) and Q8_0 (its own pack, one contiguous region per job).
-enum TcFormat { TCF_Q4_0 = 0, TCF_Q6_K = 1, TCF_Q8_0 = 2 };
+// read by tensor maps), Q8_0 and Q4_K (their own packs, one contiguous region
+// per job).
+enum TcFormat { TCF_Q4_0 = 0, TCF_Q6_K = 1, TCF_Q8_0 = 2, TCF_Q4_K = 3 };
+// A Q4_K job is one superblock (8 blocks) of a 16-row tile: codes [block
+// p][lane 4g + t] 8 B (word t of row g's then of row g + 8's Q4_0-ordered
+// 16 code bytes: byte k = value k | value k + 16 << 4), then [row][p] {scale,
+// min} bytes (16 B per row), then [row] {fp16 d, fp16 dmin}.
+constexpr int TC_Q4_K_JOB = 8 * 256 + 8 * TC_ROWS * 2 + TC_ROWS * 4;  // 2368 B
 // A Q6_K job is one superblock (8 blocks) of 16 rows: ring stage = ql box
 // (16 x 128 B, 128-byte swizzle) + qh box (16 x 64 B, 64-byte swizzle), then
 // in the scale ring the sc box (16 x 16 B) + the chunk's superblock scales
@@ -246,11 +252,14 @@ __device__ __forceinline__ uint32_t q8_f16x2(uint32_t w)
 // t fastest, then n: phase 1 reads the lane's two code words (and the meta is
 // written), phase 2, after every raw byte has been read, writes the lane's
 // 16-byte B fragment; both are free of bank conflicts.
-// Q6: the Q6_K meta, 32 B per lane: {d_a, d_a', C0, C0', C1, C1', 0, 0} with
-// the two MMAs' own starts, C0 = -1056 sum_{i<16} q_a (codes 1024 + q against
-// q_a: (q - 32) q_a = (1024 + q) q_a - 1056 q_a) and C1 = -96 sum_{i>=16} q_a
-// (codes 1024 + 16 q against q_a / 16: 64 q_a + q q_a - 96 q_a).
-template <int M, bool Q6 = false>
+// FMT = TCF_Q6_K: the meta is 32 B per lane, {d_a, d_a', C0, C0', C1, C1', 0,
+// 0} with the two MMAs' own starts, C0 = -1056 sum_{i<16} q_a (codes 1024 + q
+// against q_a: (q - 32) q_a = (1024 + q) q_a - 1056 q_a) and C1 = -96
+// sum_{i>=16} q_a (codes 1024 + 16 q against q_a / 16: 64 q_a + q q_a - 96 q_a).
+// FMT = TCF_Q4_K: 32 B per lane, {d_a, d_a', C, C', d_a A, d_a' A', 0, 0} with
+// C = -1024 sum_{i<16} q_a - 64 sum_{i>=16} q_a (no code offset) and A = sum
+// q_a (the min term; d_a A is exact in fp32).
+template <int M, int FMT = TCF_Q4_0>
 __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const uint8_t* raw, int nkb, int rstride)
 {
     constexpr int NT = (M + 7) / 8;
@@ -277,11 +286,17 @@ __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const ui
         s_hi += __shfl_xor_sync(0xffffffffu, s_hi, 2);
         if (tt == 0) {
             const int nt = n >> 3, c = n & 7;
-            if constexpr (Q6) {
+            if constexpr (FMT == TCF_Q6_K) {
                 float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 8;
                 mp[c & 1] = da;
                 mp[2 + (c & 1)] = (float)(-1056 * s_lo);
                 mp[4 + (c & 1)] = (float)(-96 * s_hi);
+                mp[6 + (c & 1)] = 0.0f;
+            } else if constexpr (FMT == TCF_Q4_K) {
+                float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 8;
+                mp[c & 1] = da;
+                mp[2 + (c & 1)] = (float)(-1024 * s_lo - 64 * s_hi);
+                mp[4 + (c & 1)] = da * (float)(s_lo + s_hi);
                 mp[6 + (c & 1)] = 0.0f;
             } else {
                 float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
@@ -464,6 +479,71 @@ __device__ __forceinline__ void tc_job_q6_k(const uint8_t* sq, const uint8_t* ss
 }
 
 // ---------------------------------------------------------------------------
+// Q4_K: value d sc_b q - dmin m_b per 32-value block b.  The codes are in the
+// Q4_0 nibble order, so the A registers and the staged activation are those
+// of Q4_0 (no -8 offset: the start is C = -1024 sum lo - 64 sum hi); the
+// scale and min terms in fp32: y += (d sc_b d_a) I_b - (dmin m_b) (d_a A_b).
+// ---------------------------------------------------------------------------
+
+// f * (unsigned byte k of w), exactly when the product fits fp32: the float
+// with bits 0x4B0000XX is 2^23 + XX, and one fma of f with it against
+// f_neg23 = -f * 2^23 leaves f * XX rounded once.
+__device__ __forceinline__ float mul_u8(float f, float f_neg23, uint32_t w, int k)
+{
+    return fmaf(f, __int_as_float((int)__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)k)), f_neg23);
+}
+
+template <int M>
+__device__ __forceinline__ void tc_job_q4_k(const uint8_t* sn, const uint8_t* act, const float* meta, int kb, int g,
+                                            int t, float (&acc)[(M + 7) / 8][4])
+{
+    constexpr int NT = (M + 7) / 8;
+    const uint8_t* codes = sn + (g * 4 + t) * 8;
+    // rows g, g + 8: {scale, min} of the 8 blocks (16 B each), {d, dmin}
+    const uint4 sma = *reinterpret_cast<const uint4*>(sn + 8 * 256 + g * 16);
+    const uint4 smb = *reinterpret_cast<const uint4*>(sn + 8 * 256 + (g + 8) * 16);
+    const uint32_t sa[4] = {sma.x, sma.y, sma.z, sma.w}, sb[4] = {smb.x, smb.y, smb.z, smb.w};
+    const uint32_t dda = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + 8 * TC_ROWS * 2 + g * 4);
+    const uint32_t ddb = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + 8 * TC_ROWS * 2 + (g + 8) * 4);
+    const float da_w = __half2float(__ushort_as_half((unsigned short)(dda & 0xFFFFu)));
+    const float dma_w = __half2float(__ushort_as_half((unsigned short)(dda >> 16)));
+    const float db_w = __half2float(__ushort_as_half((unsigned short)(ddb & 0xFFFFu)));
+    const float dmb_w = __half2float(__ushort_as_half((unsigned short)(ddb >> 16)));
+    const float da_n = -8388608.0f * da_w, dma_n = -8388608.0f * dma_w;  // exact
+    const float db_n = -8388608.0f * db_w, dmb_n = -8388608.0f * dmb_w;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const uint2 w = *reinterpret_cast<const uint2*>(codes + p * 256);
+        const uint32_t wa8 = w.x >> 8, wb8 = w.y >> 8;
+        const uint32_t A0[4] = {nib_f16x2<0x000F000Fu>(w.x), nib_f16x2<0x000F000Fu>(w.y), nib_f16x2<0x000F000Fu>(wa8),
+                                nib_f16x2<0x000F000Fu>(wb8)};
+        const uint32_t A1[4] = {nib_f16x2<0x00F000F0u>(w.x), nib_f16x2<0x00F000F0u>(w.y), nib_f16x2<0x00F000F0u>(wa8),
+                                nib_f16x2<0x00F000F0u>(wb8)};
+        // d sc and dmin m of block p, exact (fp16 x 6 bits): bytes 2 (p & 1),
+        // + 1 of word p / 2
+        const int k = 2 * (p & 1);
+        const float Da = mul_u8(da_w, da_n, sa[p >> 1], k), Ma = mul_u8(dma_w, dma_n, sa[p >> 1], k + 1);
+        const float Db = mul_u8(db_w, db_n, sb[p >> 1], k), Mb = mul_u8(dmb_w, dmb_n, sb[p >> 1], k + 1);
+        const int b = kb + p;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int n = nt * 8 + g < M ? nt * 8 + g : M - 1;  // rows past M: any staged row (unused)
+            const uint4 B = *reinterpret_cast<const uint4*>(act + (((size_t)b * M + n) * 4 + t) * 16);
+            const float* mp = meta + (((size_t)b * NT + nt) * 4 + t) * 8;
+            const float4 md = *reinterpret_cast<const float4*>(mp);
+            const float2 me = *reinterpret_cast<const float2*>(mp + 4);
+            float d[4];
+            mma_f16_16816(d, A0, B.x, B.y, md.z, md.w, md.z, md.w);
+            mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
+            acc[nt][0] = fmaf(-Ma, me.x, fmaf(Da * md.x, d[0], acc[nt][0]));
+            acc[nt][1] = fmaf(-Ma, me.y, fmaf(Da * md.y, d[1], acc[nt][1]));
+            acc[nt][2] = fmaf(-Mb, me.x, fmaf(Db * md.x, d[2], acc[nt][2]));
+            acc[nt][3] = fmaf(-Mb, me.y, fmaf(Db * md.y, d[3], acc[nt][3]));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Q8_0 (fp16 d, int8 q[32], value d * q).  Its pack (qpack_q8_0) is built for
 // this kernel: per 16-row tile, per job of 8 blocks one contiguous 4352-byte
 // region = codes [block p][lane l][16 B] then scales [block p][row r] fp16,
@@ -631,15 +711,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int t1 = narrow ? (int)((uint32_t)(cl + 1) * (uint32_t)T / (uint32_t)ncl) : (int)((int64_t)(cl + 1) * T / ncl);
     const int ntile = t1 - t0;
     const int JB = a.jb;
-    const int NIB = FMT == TCF_Q8_0 ? tc_q8_0_job_bytes(JB) : FMT == TCF_Q6_K ? TC_Q6_K_NIB : tc_nib_bytes(JB);
-    const int DSB = FMT == TCF_Q8_0 ? 0 : FMT == TCF_Q6_K ? TC_Q6_K_DS : tc_ds_bytes(JB);
+    const int NIB = FMT == TCF_Q8_0   ? tc_q8_0_job_bytes(JB)
+                    : FMT == TCF_Q6_K ? TC_Q6_K_NIB
+                    : FMT == TCF_Q4_K ? TC_Q4_K_JOB
+                                      : tc_nib_bytes(JB);
+    const int DSB = FMT == TCF_Q6_K ? TC_Q6_K_DS : FMT == TCF_Q4_0 ? tc_ds_bytes(JB) : 0;
     const int JPC = CHUNK / JB, JPC_LOG = JB > TC_LINE_JB ? 1 : 2;  // jobs per 32-block chunk
     const int njb = NB / JB;
     const int jb0 = rank * njb / C, jb1 = (rank + 1) * njb / C;
     const int jpt = jb1 - jb0;  // jobs per tile
     const int J = ntile * jpt;
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
-    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB, FMT == TCF_Q6_K ? 128 : 64);
+    const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB,
+                              FMT == TCF_Q6_K || FMT == TCF_Q4_K ? 128 : 64);
     uint8_t* nib = smem + sl.nib;
     uint8_t* ds = smem + sl.ds;
     uint8_t* act = smem + sl.act;
@@ -657,7 +741,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (warp == 0) mbar_init(abar, 1);
         fence_barrier_init();
     }
-    if (FMT != TCF_Q8_0 && warp == 1 && lane < (PAIR || FMT == TCF_Q6_K ? 4 : 2)) {
+    if ((FMT == TCF_Q4_0 || FMT == TCF_Q6_K) && warp == 1 && lane < (PAIR || FMT == TCF_Q6_K ? 4 : 2)) {
         // bring the copies' descriptors on chip while the prologue runs
         const CUtensorMap* map = lane == 0 ? &tn0 : lane == 1 ? &td0 : lane == 2 ? &tn1 : &td1;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -710,6 +794,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     bulk_g2s(dst, src + hh * JB * 512, JB * 512, bar, pol);
                     bulk_g2s(dst + JB * 512, src + TC_Q8_0_CODES + hh * JB * 32, JB * 32, bar, pol);
                 }
+            } else if constexpr (FMT == TCF_Q4_K) {
+                // the job's region of the Q4_K pack: tile igrp / 4, superblock ikg
+                bulk_g2s(dst, a.w0 + ((int64_t)(igrp >> 2) * njb + ikg) * TC_Q4_K_JOB, TC_Q4_K_JOB, bar, pol);
             } else if constexpr (FMT == TCF_Q6_K) {
                 // superblock h of chunk c for the tile's 16 rows: ql, qh and sc
                 // boxes of the row tiles, then the chunk's superblock scales
@@ -789,7 +876,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     alive = __syncthreads_and(alive);
     if (alive) {
         if constexpr (FMT == TCF_Q8_0) tc_stage_act_q8_0<M>(act, meta, raw, jpt * JB, (int)rstride);
-        else tc_stage_act<M, FMT == TCF_Q6_K>(act, meta, raw, jpt * JB, (int)rstride);
+        else tc_stage_act<M, FMT>(act, meta, raw, jpt * JB, (int)rstride);
     }
     __syncthreads();  // the tile is built
     float acc[NT][4];
@@ -817,6 +904,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         ++consumed;
         if constexpr (FMT == TCF_Q8_0) tc_job_q8_0<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, JB, g, t, acc);
+        else if constexpr (FMT == TCF_Q4_K) tc_job_q4_k<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, g, t, acc);
         else if constexpr (FMT == TCF_Q6_K)
             tc_job_q6_k<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB,
                            (jb0 + kj) & (JPC - 1), g, t, acc);

@@ -332,6 +332,38 @@ int qgemv_q6_k_plan(int M, int K, int N, int* info);
 int qpack_q8_0(const void* w_canon, void* w_pack, int N, int K, void* stream);
 int qgemv_q8_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
 
+/* ---- NEXT-4: a further format, Q4_K ------------------------------------ */
+
+/* Q4_K (named on the pages among the further K-quant formats; the Q4_K_M
+ * draft models are built from it; defined as in llama.cpp): superblocks of
+ * 256 weights = fp16 d, fp16 dmin, 12 bytes holding eight 6-bit scales sc_j
+ * and eight 6-bit mins m_j (sub-block j < 4: sc = byte j & 63, m = byte j+4 &
+ * 63; j >= 4: sc = (byte j+4 & 15) | (byte j-4 >> 6) << 4, m = (byte j+4 >> 4)
+ * | (byte j >> 6) << 4), then 128 bytes of 4-bit codes (values 64c .. 64c+31
+ * are the low nibbles of bytes 32c .. 32c+31, values 64c+32 .. 64c+63 their
+ * high nibbles); value i = d * sc_{i/32} * q_i - dmin * m_{i/32}.      144 B
+ * [closure] "Qwen3.6 27B Q4_0 DFlash/SYCL closure" lists further K-quant
+ * formats as the next coverage; this one runs on the tensor-core MMVQ.
+ *
+ * qpack_q4_k - canonical [N][K/256] x 144 B -> the tensor-core pack: per
+ * 16-row tile and superblock one 2368-byte region (codes in MMA fragment
+ * order, per row and block 4 bytes per lane; the {scale, min} bytes, row by
+ * row; the {d, dmin} bits); rows padded to 16 with zeros (148 B per row and
+ * superblock).  K % 256 == 0; w_pack 16-byte aligned (q4_k_pack_bytes(N, K)
+ * bytes, 0 when K % 256).
+ *
+ * qgemv_q4_k - y[m][n] = sum_b (d sc_b d_a[m,b] I - dmin m_b d_a[m,b] A), with
+ * I = sum_i q_w q_a and A = sum_i q_a exact per 32-value block, the two terms
+ * in fp32; M = 1..17, K % 256 == 0, any N >= 1; arguments as qgemv_q4_0.
+ * QGEMV_UNSUPPORTED_SHAPE also when no launch plan fits (very large M * K).
+ *
+ * qgemv_q4_k_plan - as qgemv_q8_0_plan (blocks per job: 8).  (Not from the
+ * pages.) */
+size_t q4_k_pack_bytes(int N, int K);
+int qpack_q4_k(const void* w_canon, void* w_pack, int N, int K, void* stream);
+int qgemv_q4_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
+int qgemv_q4_k_plan(int M, int K, int N, int* info);
+
 /* qgemv_q8_0_plan - the launch qgemv_q8_0 would make for this shape; writes
  * info[5] = {1, CTAs per cluster (the K parts), grid size, ring stages per
  * warp, blocks per job (8: a whole pack region; 4: half of one, taken where

@@ -67,6 +67,39 @@ def pack_q8_0(w: np.ndarray) -> np.ndarray:
     return out.reshape(-1)
 
 
+def pack_q4_k(w: np.ndarray) -> np.ndarray:
+    """Canonical Q4_K [N, K/256, 144] -> the documented tensor-core pack: per
+    16-row tile and superblock a 2368-byte region = codes [block p][lane 4g + t]
+    8 B (word t of row g's then of row g + 8's 16 code bytes, byte k = value k
+    | value k + 16 << 4 of block p), then [row r][p] {scale, min}, then [row]
+    {d, dmin} bits; rows past N are zero."""
+    N, ns, _ = w.shape
+    T = (N + 15) // 16
+    wp = np.zeros((T * 16, ns, 144), dtype=np.uint8)
+    wp[:N] = w
+    qs = wp[:, :, 16:144].astype(np.int64).reshape(T * 16, ns, 4, 32)
+    vals = np.stack([qs & 15, qs >> 4], axis=3).reshape(T * 16, ns, 8, 32)  # [row, sb, block, value]
+    code16 = (vals[..., :16] | (vals[..., 16:] << 4)).astype(np.uint8)  # [row, sb, block, 16 bytes]
+    sb = wp[:, :, 4:16].astype(np.int64)
+    sc = np.concatenate([sb[..., 0:4] & 63, (sb[..., 8:12] & 15) | ((sb[..., 0:4] >> 6) << 4)], axis=2)
+    mn = np.concatenate([sb[..., 4:8] & 63, (sb[..., 8:12] >> 4) | ((sb[..., 4:8] >> 6) << 4)], axis=2)
+    out = np.zeros((T, ns, 2368), dtype=np.uint8)
+    for tau in range(T):
+        rows = slice(16 * tau, 16 * tau + 16)
+        c = code16[rows]  # [16, ns, 8, 16]
+        for p in range(8):
+            for g in range(8):
+                for t in range(4):
+                    o = p * 256 + (4 * g + t) * 8
+                    out[tau, :, o:o + 4] = c[g, :, p, 4 * t:4 * t + 4]
+                    out[tau, :, o + 4:o + 8] = c[g + 8, :, p, 4 * t:4 * t + 4]
+            for r in range(16):
+                out[tau, :, 2048 + r * 16 + 2 * p] = sc[16 * tau + r, :, p]
+                out[tau, :, 2048 + r * 16 + 2 * p + 1] = mn[16 * tau + r, :, p]
+        out[tau, :, 2304:2368] = wp[rows, :, 0:4].transpose(1, 0, 2).reshape(ns, 64)
+    return out.reshape(-1)
+
+
 def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
     """Inverse of pack_q4_0."""
     nb = K // 32

@@ -64,6 +64,10 @@ def test_sizes(lib):
     assert lib.q8_0_pack_bytes(17408, 5120) == 17408 * 160 * 34  # the canonical size when N % 16 == 0
     assert lib.q8_0_pack_bytes(17, 256) == 2 * 1 * 4352  # two tiles, rows padded to 32
     assert lib.q8_0_pack_bytes(16, 96) == 0  # K % 256
+    lib.q4_k_pack_bytes.restype = ctypes.c_size_t
+    assert lib.q4_k_pack_bytes(16, 5120) == 20 * 2368  # 148 B per row and superblock
+    assert lib.q4_k_pack_bytes(17, 256) == 2 * 2368  # rows padded to 32
+    assert lib.q4_k_pack_bytes(16, 384) == 0  # K % 256
 
 
 def test_status_strings(lib):
