@@ -71,6 +71,20 @@ def q4_k_weights(N: int, K: int, seed: int, d_lo: float = 2e-4, d_hi: float = 2e
     return out
 
 
+def q5_k_weights(N: int, K: int, seed: int, d_lo: float = 1e-4, d_hi: float = 1e-3, dmin_lo: float = 1e-4,
+                 dmin_hi: float = 1e-3) -> np.ndarray:
+    """Canonical Q5_K bytes uint8 [N, K/256, 176] = {fp16 d, fp16 dmin, scales[12], qh[32], qs[128]};
+    the scale, high-bit and code bytes uniform random."""
+    assert K % 256 == 0
+    ns = K // 256
+    g_q, g_d, g_m = streams(seed, 3)
+    out = np.empty((N, ns, 176), dtype=np.uint8)
+    out[:, :, 0:2] = _f16_bits(g_d, d_lo, d_hi, (N, ns)).view(np.uint8).reshape(N, ns, 2)
+    out[:, :, 2:4] = _f16_bits(g_m, dmin_lo, dmin_hi, (N, ns)).view(np.uint8).reshape(N, ns, 2)
+    out[:, :, 4:176] = _random_bytes(g_q, (N, ns, 172))
+    return out
+
+
 def q6_k_weights(N: int, K: int, seed: int, d_lo: float = 1e-4, d_hi: float = 1e-3) -> np.ndarray:
     """Canonical Q6_K bytes uint8 [N, K/256, 210] = {ql[128], qh[64], int8 sc[16], fp16 d}."""
     assert K % 256 == 0

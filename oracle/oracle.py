@@ -55,11 +55,12 @@ def _load():
             lib.oracle_quantize_q8_1.argtypes = [P, L, I, I, P]
             lib.oracle_rmsnorm_quantize_q8_1.argtypes = [P, L, P, ctypes.c_float, I, I, P]
             for name in ("oracle_dequant_q4_0", "oracle_dequant_q6_k", "oracle_dequant_q8_1", "oracle_dequant_q8_0",
-                         "oracle_dequant_q4_k"):
+                         "oracle_dequant_q4_k", "oracle_dequant_q5_k"):
                 getattr(lib, name).argtypes = [P, I, I, P]
             for name in ("oracle_block_dots_q4_0", "oracle_block_dots_q6_k"):
                 getattr(lib, name).argtypes = [P, P, I, I, I, P]
-            for name in ("oracle_qgemv_q4_0", "oracle_qgemv_q6_k", "oracle_qgemv_q8_0", "oracle_qgemv_q4_k"):
+            for name in ("oracle_qgemv_q4_0", "oracle_qgemv_q6_k", "oracle_qgemv_q8_0", "oracle_qgemv_q4_k",
+                         "oracle_qgemv_q5_k"):
                 getattr(lib, name).argtypes = [P, P, I, I, I, P, P, I]
             lib.oracle_top1_f64.argtypes = [P, L, I, I, P]
             lib.oracle_top1_f32.argtypes = [P, L, I, I, P]
@@ -191,6 +192,30 @@ def dequant_q4_k(w: np.ndarray) -> np.ndarray:
     return out
 
 
+def qgemv_q5_k(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
+    """canonical Q5_K w [N, K/256, 176] = {fp16 d, fp16 dmin, scales[12], qh[32], qs[128]},
+    Q8_1 xq [M, K/32, 36] -> (y, S) fp64 [M, N], the formula of qgemv_q4_k with 5-bit codes."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    N, ns = w.shape[0], w.shape[1]
+    M = xq.shape[0]
+    assert xq.shape[1] == ns * 8 and w.shape[2] == 176
+    y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_qgemv_q5_k(_ptr(w), _ptr(xq), M, ns * 256, N, _ptr(y), _ptr(S),
+                              nthreads or default_threads())
+    return y, S
+
+
+def dequant_q5_k(w: np.ndarray) -> np.ndarray:
+    """[N, K/256, 176] -> fp64 [N, K] (the C dequantizer)."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    N, ns, _ = w.shape
+    out = np.zeros((N, ns * 256), dtype=np.float64)
+    _load().oracle_dequant_q5_k(_ptr(w), N, ns * 256, _ptr(out))
+    return out
+
+
 def qgemv_q6_k(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):
     """canonical Q6_K w [N, K/256, 210], Q8_1 xq [M, K/32, 36] -> (y, S) fp64 [M, N]."""
     w = np.ascontiguousarray(w, dtype=np.uint8)
@@ -302,6 +327,20 @@ def dequant_q4_k_np(w: np.ndarray) -> np.ndarray:
     q = np.stack([qs & 15, qs >> 4], axis=3).reshape(N, ns, 8, 32)  # sub-block 2c: low, 2c + 1: high
     v = d[:, :, None, None] * sc[:, :, :, None] * q - dmin[:, :, None, None] * mn[:, :, :, None]
     return v.reshape(N, ns * 256)
+
+
+def dequant_q5_k_np(w: np.ndarray) -> np.ndarray:
+    """[N, K/256, 176] -> fp64 [N, K] (numpy, written apart from the C code):
+    the Q4_K decode of scales, mins and nibbles (the codes after the 32 qh
+    bytes), plus 16 x bit j of qh[l] for value l of sub-block j."""
+    N, ns, _ = w.shape
+    base = dequant_q4_k_np(np.concatenate([w[:, :, 0:16], w[:, :, 48:176]], axis=2))
+    d = _f16(w[:, :, 0:2].copy().view(np.uint16)[:, :, 0])
+    s = w[:, :, 4:16].astype(np.int64)
+    sc = np.concatenate([s[:, :, 0:4] & 63, (s[:, :, 8:12] & 15) | ((s[:, :, 0:4] >> 6) << 4)], axis=2)
+    qh = w[:, :, 16:48].astype(np.int64)  # [N, ns, 32]
+    bits = (qh[:, :, None, :] >> np.arange(8)[None, None, :, None]) & 1  # [N, ns, sub-block j, l]
+    return base + (16.0 * d[:, :, None, None] * sc[:, :, :, None] * bits).reshape(N, ns * 256)
 
 
 def dequant_q8_1_np(xq: np.ndarray) -> np.ndarray:

@@ -24,11 +24,12 @@
  *     production record", sections "Why this was slow" and "Exactness and
  *     safety contracts" ([5120, 248320] Q6_K output weight) and "Memory and
  *     startup" (16 subscales and one fp16 scale per 256 values).
- *   - Q8_0 and Q4_K weights (named among the further K-quant formats of
- *     "Qwen3.6 27B Q4_0 DFlash/SYCL closure" and of the DFlash KV-cache
+ *   - Q8_0, Q4_K and Q5_K weights (named among the further K-quant formats
+ *     of "Qwen3.6 27B Q4_0 DFlash/SYCL closure" and of the DFlash KV-cache
  *     page): Q8_0 = blocks of 32, fp16 d, int8 q, value d * q; Q4_K =
  *     superblocks of 256, fp16 d and dmin, eight 6-bit scales and eight
- *     6-bit mins (one per 32 values), 4-bit q, value d * sc * q - dmin * m.
+ *     6-bit mins (one per 32 values), 4-bit q, value d * sc * q - dmin * m;
+ *     Q5_K = the same with 5-bit q.
  *   - Top-1 with the lowest-token-ID finite-tie rule: same page, "Exactness and
  *     safety contracts", item 3.
  *
@@ -54,6 +55,9 @@
  *     >> 6) << 4 and min (scales[j + 4] >> 4) | (scales[j] >> 6) << 4.  Values
  *     64 c .. 64 c + 31 are the low nibbles of qs[32 c .. 32 c + 31] and values
  *     64 c + 32 .. 64 c + 63 their high nibbles; value i is in sub-block i / 32.
+ *   - Q5_K superblock = {fp16 d, fp16 dmin, uint8 scales[12], uint8 qh[32],
+ *     uint8 qs[128]} as in llama.cpp: scales, mins and the low 4 bits as Q4_K;
+ *     the fifth bit of value i is bit (i / 32) of qh[i % 32].
  *
  * Build: cc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread (no fast-math).
  */
@@ -116,6 +120,7 @@ static void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (u
 
 #define Q8_0_BYTES 34
 #define Q4_K_BYTES 144
+#define Q5_K_BYTES 176
 #define Q8_1_BYTES 36
 #define Q4_0_BYTES 18
 #define Q6_K_BYTES 210
@@ -253,7 +258,7 @@ void oracle_dequant_q8_0(const uint8_t* w, int N, int K, double* out)
         }
 }
 
-/* Q4_K: the scale and min of sub-block j (0..7) of a superblock. */
+/* Q4_K and Q5_K: the scale and min of sub-block j (0..7) of a superblock. */
 static void q4_k_scale_min(const uint8_t* sb, int j, int* sc, int* m)
 {
     const uint8_t* s = sb + 4;
@@ -272,6 +277,32 @@ static int q4_k_code(const uint8_t* sb, int i)
     const uint8_t* qs = sb + 16;
     int c = i / 64, r = i % 64;
     return r < 32 ? (qs[32 * c + r] & 15) : (qs[32 * c + r - 32] >> 4);
+}
+
+/* Q5_K: the 5-bit code of value i (0..255): the Q4_K nibble of the code
+ * bytes (after the 32 qh bytes) plus 16 times bit i / 32 of qh[i % 32]. */
+static int q5_k_code(const uint8_t* sb, int i)
+{
+    const uint8_t* qh = sb + 16;
+    const uint8_t* qs = sb + 48;
+    int c = i / 64, r = i % 64;
+    int lo = r < 32 ? (qs[32 * c + r] & 15) : (qs[32 * c + r - 32] >> 4);
+    return lo + 16 * ((qh[i % 32] >> (i / 32)) & 1);
+}
+
+void oracle_dequant_q5_k(const uint8_t* w, int N, int K, double* out)
+{
+    int ns = K / 256;
+    for (int n = 0; n < N; ++n)
+        for (int s = 0; s < ns; ++s) {
+            const uint8_t* sb = w + ((int64_t)n * ns + s) * Q5_K_BYTES;
+            double d = oracle_f16_to_f64(rd16(sb)), dmin = oracle_f16_to_f64(rd16(sb + 2));
+            for (int i = 0; i < 256; ++i) {
+                int sc, m;
+                q4_k_scale_min(sb, i / 32, &sc, &m);
+                out[(int64_t)n * K + 256 * s + i] = d * (double)sc * (double)q5_k_code(sb, i) - dmin * (double)m;
+            }
+        }
 }
 
 void oracle_dequant_q4_k(const uint8_t* w, int N, int K, double* out)
@@ -342,12 +373,12 @@ static int32_t block_dot_q6_k(const uint8_t* sb, int bb, const uint8_t* ablk)
 /* Q4_K, block bb (sub-block bb) of superblock sb: I = sum_i q(i) * q_a(i)
  * and A = sum_i q_a(i), the two exact integers of
  * sum_i (d sc q(i) - dmin m) * d_a q_a(i) = d sc d_a I - dmin m d_a A. */
-static void block_dot_q4_k(const uint8_t* sb, int bb, const uint8_t* ablk, int32_t* I, int32_t* A)
+static void block_dot_q4_k(const uint8_t* sb, int bb, const uint8_t* ablk, int32_t* I, int32_t* A, int five)
 {
     int32_t i1 = 0, a1 = 0;
     for (int t = 0; t < 32; ++t) {
         int32_t qa = (int32_t)(int8_t)ablk[4 + t];
-        i1 += q4_k_code(sb, 32 * bb + t) * qa;
+        i1 += (five ? q5_k_code(sb, 32 * bb + t) : q4_k_code(sb, 32 * bb + t)) * qa;
         a1 += qa;
     }
     *I = i1;
@@ -382,7 +413,7 @@ void oracle_block_dots_q6_k(const uint8_t* w, const uint8_t* xq, int M, int K, i
 /* ------------------------------------------------------------------ */
 
 typedef struct {
-    int fmt; /* 0 = Q4_0, 1 = Q6_K, 2 = Q8_0, 3 = Q4_K */
+    int fmt; /* 0 = Q4_0, 1 = Q6_K, 2 = Q8_0, 3 = Q4_K, 4 = Q5_K */
     const uint8_t* w;
     const uint8_t* xq;
     int M, K, N;
@@ -402,13 +433,14 @@ static void gemv_rows(const gemv_job* j)
                 double da = oracle_f16_to_f64(rd16(ablk));
                 double dw;
                 int32_t I;
-                if (j->fmt == 3) {
+                if (j->fmt == 3 || j->fmt == 4) {
                     /* two terms: d sc d_a I and - dmin m d_a A */
-                    const uint8_t* sb = j->w + ((int64_t)n * ns + b / 8) * Q4_K_BYTES;
+                    const uint8_t* sb =
+                        j->w + ((int64_t)n * ns + b / 8) * (j->fmt == 3 ? Q4_K_BYTES : Q5_K_BYTES);
                     int sc, mn;
                     int32_t A;
                     q4_k_scale_min(sb, b % 8, &sc, &mn);
-                    block_dot_q4_k(sb, b % 8, ablk, &I, &A);
+                    block_dot_q4_k(sb, b % 8, ablk, &I, &A, j->fmt == 4);
                     double t1 = oracle_f16_to_f64(rd16(sb)) * (double)sc * da * (double)I;
                     double t2 = -oracle_f16_to_f64(rd16(sb + 2)) * (double)mn * da * (double)A;
                     acc += t1 + t2;
@@ -475,6 +507,13 @@ void oracle_qgemv_q4_k(const uint8_t* w, const uint8_t* xq, int M, int K, int N,
                        double* y, double* S, int nthreads)
 {
     gemv_run(3, w, xq, M, K, N, y, S, nthreads);
+}
+
+/* w: canonical Q5_K [N][K/256] x 176 B; as oracle_qgemv_q4_k. */
+void oracle_qgemv_q5_k(const uint8_t* w, const uint8_t* xq, int M, int K, int N,
+                       double* y, double* S, int nthreads)
+{
+    gemv_run(4, w, xq, M, K, N, y, S, nthreads);
 }
 
 /* w: canonical Q4_0 [N][K/32] x 18 B; xq: Q8_1 [M][K/32] x 36 B;

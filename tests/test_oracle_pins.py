@@ -433,3 +433,55 @@ def test_q4_k_min_term_closed_form():
     xq = oracle.quantize_q8_1(x)
     y, _ = oracle.qgemv_q4_k(w, xq)
     assert np.allclose(y[:, 0], -2.0 * oracle.dequant_q8_1_np(xq).sum(axis=1), rtol=1e-13, atol=0)
+
+
+# ---------------------------------------------------------------- Q5_K (a further format)
+
+def _q5_k_superblock(d: float, dmin: float, scale_bytes, qh, qs) -> np.ndarray:
+    sb = np.zeros(176, dtype=np.uint8)
+    sb[0:2] = np.array([d], dtype=np.float16).view(np.uint8)
+    sb[2:4] = np.array([dmin], dtype=np.float16).view(np.uint8)
+    sb[4:16] = np.asarray(scale_bytes, dtype=np.uint8)
+    sb[16:48] = np.asarray(qh, dtype=np.uint8)
+    sb[48:176] = np.asarray(qs, dtype=np.uint8)
+    return sb
+
+
+def test_q5_k_fifth_bit_hand_example():
+    # unit scales, no mins; qh[0] = 0x81 sets the fifth bit of value 0 (bit 0:
+    # sub-block 0, position 0) and of value 224 (bit 7: sub-block 7, position 0);
+    # qh[3] = 0x04 that of value 67 (sub-block 2, position 3); qs[0] = 0x0F adds
+    # 15 to value 0: values 0 = 31, 67 = 16, 224 = 16, all others 0
+    unit = [1, 1, 1, 1, 0, 0, 0, 0, 0x01, 0x01, 0x01, 0x01]
+    qh = np.zeros(32, dtype=np.uint8)
+    qh[0], qh[3] = 0x81, 0x04
+    qs = np.zeros(128, dtype=np.uint8)
+    qs[0] = 0x0F
+    w = _q5_k_superblock(1.0, 0.0, unit, qh, qs)[None, None]
+    expect = np.zeros(256)
+    expect[0], expect[67], expect[224] = 31.0, 16.0, 16.0
+    assert np.array_equal(oracle.dequant_q5_k(w)[0], expect)
+    assert np.array_equal(oracle.dequant_q5_k_np(w)[0], expect)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 256, 1), (3, 256, 7), (2, 512, 33), (5, 1024, 16)])
+def test_q5_k_matches_fp64_dequant_matmul(M, K, N):
+    w = synth.q5_k_weights(N, K, seed=700 + K + N)
+    xq = oracle.quantize_q8_1(synth.activations(M, K, seed=800 + M))
+    y, S = oracle.qgemv_q5_k(w, xq)
+    ref = oracle.dequant_q8_1_np(xq) @ oracle.dequant_q5_k_np(w).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * np.maximum(S, 1e-300))
+    assert np.array_equal(oracle.dequant_q5_k(w), oracle.dequant_q5_k_np(w))
+
+
+def test_q5_k_without_fifth_bits_is_q4_k():
+    # with every qh bit clear a Q5_K superblock is the Q4_K superblock of the
+    # same d, dmin, scales and codes
+    K, N = 1024, 9
+    w5 = synth.q5_k_weights(N, K, seed=31)
+    w5[:, :, 16:48] = 0
+    w4 = np.concatenate([w5[:, :, 0:16], w5[:, :, 48:176]], axis=2)
+    xq = oracle.quantize_q8_1(synth.activations(3, K, seed=32))
+    y5, S5 = oracle.qgemv_q5_k(w5, xq)
+    y4, S4 = oracle.qgemv_q4_k(w4, xq)
+    assert np.array_equal(y5, y4) and np.array_equal(S5, S4)
