@@ -470,14 +470,16 @@ def run_sweep(args):
     reps = max(3, min(args.steps, 20))
     peak, _ = peaks()
     pack_bytes = {"q4_0": ops.q4_0_pack_bytes, "q6_k": ops.q6_k_pack_bytes, "q8_0": ops.q8_0_pack_bytes,
-                  "q4_k": ops.q4_k_pack_bytes}
-    gemv = {"q4_0": ops.qgemv_q4_0, "q6_k": ops.qgemv_q6_k, "q8_0": ops.qgemv_q8_0, "q4_k": ops.qgemv_q4_k}
-    for fmt in ("q4_0", "q6_k", "q8_0", "q4_k"):
+                  "q4_k": ops.q4_k_pack_bytes, "q5_k": ops.q5_k_pack_bytes}
+    gemv = {"q4_0": ops.qgemv_q4_0, "q6_k": ops.qgemv_q6_k, "q8_0": ops.qgemv_q8_0, "q4_k": ops.qgemv_q4_k,
+            "q5_k": ops.qgemv_q5_k}
+    canonical = {"q4_k": 144, "q5_k": 176}  # bytes per 256 values
+    for fmt in ("q4_0", "q6_k", "q8_0", "q4_k", "q5_k"):
         for N in (5120, 17408, 248320):
             nbytes_w = pack_bytes[fmt](N, K_H)
-            # algorithmic bytes: the canonical size (Q4_K's pack carries 148 B per
-            # 256 values against the canonical 144; the others are equal)
-            nbytes_alg = N * (K_H // 256) * 144 if fmt == "q4_k" else nbytes_w
+            # algorithmic bytes: the canonical size (the Q4_K / Q5_K packs carry
+            # 148 / 180 B per 256 values against 144 / 176; the others are equal)
+            nbytes_alg = N * (K_H // 256) * canonical[fmt] if fmt in canonical else nbytes_w
             w = torch.randint(0, 256, (nbytes_w,), dtype=torch.uint8, generator=g).to(dev)
             for M in (1, 2, 4, 6, 9, 12, 17):
                 x = torch.randn(M, K_H, generator=g).to(dev)

@@ -46,6 +46,10 @@ SIGNATURES = {
     "qgemv_set_q6_k_tensor_cores": (_I, [_I]),
     "q8_0_pack_bytes": (_S, [_I, _I]),
     "q4_k_pack_bytes": (_S, [_I, _I]),
+    "q5_k_pack_bytes": (_S, [_I, _I]),
+    "qpack_q5_k": (_I, [_P, _P, _I, _I, _P]),
+    "qgemv_q5_k": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
+    "qgemv_q5_k_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "qpack_q4_k": (_I, [_P, _P, _I, _I, _P]),
     "qgemv_q4_k": (_I, [_P, _P, _P, _L, _I, _I, _I, _P]),
     "qgemv_q4_k_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
@@ -236,6 +240,24 @@ def qgemv_q4_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
     return _gemv("qgemv_q4_k", w_pack, xq, M, K, N, y)
 
 
+def q5_k_pack_bytes(N: int, K: int) -> int:
+    return LIB.q5_k_pack_bytes(N, K)
+
+
+def qpack_q5_k(w_canon: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """canonical Q5_K bytes [N, K/256, 176] -> the tensor-core pack."""
+    if out is None:
+        out = torch.empty(q5_k_pack_bytes(N, K), dtype=torch.uint8, device=w_canon.device)
+    _check("qpack_q5_k", LIB.qpack_q5_k(_dev(w_canon, "w_canon"), _dev(out, "w_pack"), N, K, _stream(w_canon)))
+    return out
+
+
+def qgemv_q5_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int, N: int,
+               y: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp32 = Q5_K weight (packed) x Q8_1 activation."""
+    return _gemv("qgemv_q5_k", w_pack, xq, M, K, N, y)
+
+
 def qgemv_q4_0_residual(w_pack: torch.Tensor, xq: torch.Tensor, residual: torch.Tensor, M: int, K: int, N: int,
                         y: torch.Tensor | None = None) -> torch.Tensor:
     """y [M, N] fp32 = Q4_0 weight x Q8_1 activation + residual (fp32 [M, >= N],
@@ -388,6 +410,14 @@ def qgemv_q4_k_plan(M: int, K: int, N: int) -> dict:
     """The launch qgemv_q4_k would make for this shape."""
     info = (ctypes.c_int * 5)()
     _check("qgemv_q4_k_plan", LIB.qgemv_q4_k_plan(M, K, N, info))
+    return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3],
+            "job_blocks": info[4]}
+
+
+def qgemv_q5_k_plan(M: int, K: int, N: int) -> dict:
+    """The launch qgemv_q5_k would make for this shape."""
+    info = (ctypes.c_int * 5)()
+    _check("qgemv_q5_k_plan", LIB.qgemv_q5_k_plan(M, K, N, info))
     return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3],
             "job_blocks": info[4]}
 

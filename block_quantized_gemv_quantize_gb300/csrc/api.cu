@@ -87,6 +87,12 @@ size_t q4_k_pack_bytes(int N, int K)
     return (size_t)((N + 15) / 16) * (size_t)(K / QK_K) * 2368;
 }
 
+size_t q5_k_pack_bytes(int N, int K)
+{
+    if (N < 1 || K < QK_K || K % QK_K) return 0;
+    return (size_t)((N + 15) / 16) * (size_t)(K / QK_K) * 2880;
+}
+
 size_t q6_k_pack_bytes(int N, int K)
 {
     return (N < 1 || K < QK_K) ? 0 : (size_t)make_layout(FMT_Q6_K, N, K).total_bytes();
@@ -158,6 +164,28 @@ int qgemv_q4_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
     a.K = K;
     a.N = N;
     return launch_mmvq_q4_k(a, M, as_stream(stream));
+}
+
+int qpack_q5_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
+{
+    if (!w_canon || !w_pack || N < 1 || K < QK_K) return QGEMV_INVALID_ARG;
+    if (K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
+    if (!aligned16(w_pack)) return QGEMV_MISALIGNED;
+    return launch_qpack_q5_k(w_canon, w_pack, N, K, as_stream(stream));
+}
+
+int qgemv_q5_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
+{
+    int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK_K);
+    if (st) return st;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.y = y;
+    a.ldy = ldy;
+    a.K = K;
+    a.N = N;
+    return launch_mmvq_q5_k(a, M, as_stream(stream));
 }
 
 int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
@@ -377,6 +405,17 @@ int qgemv_q4_k_plan(int M, int K, int N, int* info)
     return launch_mmvq_q4_k(a, M, nullptr, info);
 }
 
+int qgemv_q5_k_plan(int M, int K, int N, int* info)
+{
+    if (!info || M < 1 || K < QK_K || N < 1) return QGEMV_INVALID_ARG;
+    if (M > QGEMV_MAX_M || K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < 5; ++i) info[i] = 0;
+    MmvqArgs a{};
+    a.K = K;
+    a.N = N;
+    return launch_mmvq_q5_k(a, M, nullptr, info);
+}
+
 int qgemv_q8_0_plan(int M, int K, int N, int* info)
 {
     if (!info || M < 1 || K < QK || N < 1) return QGEMV_INVALID_ARG;
@@ -393,7 +432,8 @@ int qgemv_take_wait_timeouts(unsigned int* count)
     if (!count) return QGEMV_INVALID_ARG;
     *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() +
              take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_q6_k_tc() +
-             take_wait_timeouts_lmhead() + take_wait_timeouts_q8_0() + take_wait_timeouts_q4_k();
+             take_wait_timeouts_lmhead() + take_wait_timeouts_q8_0() + take_wait_timeouts_q4_k() +
+             take_wait_timeouts_q5_k();
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

@@ -214,8 +214,14 @@ __device__ __forceinline__ void q4_k_unpack_scale_min(const uint8_t* s, int j, u
     }
 }
 
+// Q5_K (Q4_K plus qh[32] after the scale bytes: the fifth bit of value i is
+// bit i / 32 of qh[i % 32]) into the same layout with, after the codes, a
+// [p][row] word of fifth bits (byte k bit s = value k + 4 s of block p);
+// region 2880 B.
+template <bool FIVE>
 __global__ void qpack_q4_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
 {
+    constexpr int CB = FIVE ? 176 : 144, RB = FIVE ? 2880 : 2368, SCM = FIVE ? 2560 : 2048;
     const int NS = K / QK_K;
     const int64_t T = (N + 15) / 16;
     const int64_t total = T * NS * 16;
@@ -226,19 +232,20 @@ __global__ void qpack_q4_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
         const int64_t tau = ts / NS;
         const int sbi = (int)(ts - tau * NS);
         const int64_t n = tau * 16 + r;
-        uint8_t* region = pack + (tau * NS + sbi) * 2368;
+        uint8_t* region = pack + (tau * NS + sbi) * RB;
         const int g = r & 7, half = r >> 3;
         if (n >= N) {
             for (int p = 0; p < 8; ++p) {
                 for (int t = 0; t < 4; ++t)
                     *reinterpret_cast<uint32_t*>(region + p * 256 + (4 * g + t) * 8 + 4 * half) = 0u;
-                *reinterpret_cast<uint16_t*>(region + 2048 + (r * 8 + p) * 2) = 0;
+                if (FIVE) *reinterpret_cast<uint32_t*>(region + 2048 + (p * 16 + r) * 4) = 0u;
+                *reinterpret_cast<uint16_t*>(region + SCM + (r * 8 + p) * 2) = 0;
             }
-            *reinterpret_cast<uint32_t*>(region + 2304 + r * 4) = 0u;
+            *reinterpret_cast<uint32_t*>(region + SCM + 256 + r * 4) = 0u;
             continue;
         }
-        const uint8_t* sb = canon + (n * NS + sbi) * 144;
-        const uint8_t* qs = sb + 16;
+        const uint8_t* sb = canon + (n * NS + sbi) * CB;
+        const uint8_t* qs = sb + (FIVE ? 48 : 16);
         for (int p = 0; p < 8; ++p) {
             const int base = 32 * (p >> 1), shift = 4 * (p & 1);
             for (int t = 0; t < 4; ++t) {
@@ -250,11 +257,17 @@ __global__ void qpack_q4_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
                 }
                 *reinterpret_cast<uint32_t*>(region + p * 256 + (4 * g + t) * 8 + 4 * half) = word;
             }
+            if (FIVE) {
+                uint32_t hw = 0;
+                for (int k = 0; k < 4; ++k)
+                    for (int s2 = 0; s2 < 8; ++s2) hw |= (uint32_t)((sb[16 + k + 4 * s2] >> p) & 1) << (8 * k + s2);
+                *reinterpret_cast<uint32_t*>(region + 2048 + (p * 16 + r) * 4) = hw;
+            }
             uint32_t sc, m;
             q4_k_unpack_scale_min(sb + 4, p, sc, m);
-            *reinterpret_cast<uint16_t*>(region + 2048 + (r * 8 + p) * 2) = (uint16_t)(sc | m << 8);
+            *reinterpret_cast<uint16_t*>(region + SCM + (r * 8 + p) * 2) = (uint16_t)(sc | m << 8);
         }
-        *reinterpret_cast<uint32_t*>(region + 2304 + r * 4) =
+        *reinterpret_cast<uint32_t*>(region + SCM + 256 + r * 4) =
             (uint32_t)sb[0] | (uint32_t)sb[1] << 8 | (uint32_t)sb[2] << 16 | (uint32_t)sb[3] << 24;
     }
 }
@@ -263,8 +276,17 @@ int launch_qpack_q4_k(const void* canon, void* pack, int N, int K, cudaStream_t 
 {
     const int64_t total = (int64_t)((N + 15) / 16) * (K / QK_K) * 16;
     const int64_t grid = total / 256 + 1 < 65535 ? total / 256 + 1 : 65535;
-    qpack_q4_k_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon), static_cast<uint8_t*>(pack),
-                                                     N, K);
+    qpack_q4_k_kernel<false><<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon),
+                                                            static_cast<uint8_t*>(pack), N, K);
+    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+}
+
+int launch_qpack_q5_k(const void* canon, void* pack, int N, int K, cudaStream_t s)
+{
+    const int64_t total = (int64_t)((N + 15) / 16) * (K / QK_K) * 16;
+    const int64_t grid = total / 256 + 1 < 65535 ? total / 256 + 1 : 65535;
+    qpack_q4_k_kernel<true><<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon),
+                                                           static_cast<uint8_t*>(pack), N, K);
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

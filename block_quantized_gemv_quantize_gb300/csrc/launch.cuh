@@ -226,6 +226,9 @@ int launch_qpack_q8_0(const void* canon, void* pack, int N, int K, cudaStream_t 
 int launch_mmvq_q4_k(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
 unsigned int take_wait_timeouts_q4_k();
 int launch_qpack_q4_k(const void* canon, void* pack, int N, int K, cudaStream_t s);
+int launch_mmvq_q5_k(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
+unsigned int take_wait_timeouts_q5_k();
+int launch_qpack_q5_k(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 unsigned int take_wait_timeouts_q4_0();
 unsigned int take_wait_timeouts_q4_0_pair();

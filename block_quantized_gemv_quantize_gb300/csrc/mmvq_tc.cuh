@@ -52,12 +52,15 @@ constexpr int TC_THREADS = 512;
 // Weight formats of the tensor-core kernel: Q4_0 and Q6_K (the existing packs,
 // read by tensor maps), Q8_0 and Q4_K (their own packs, one contiguous region
 // per job).
-enum TcFormat { TCF_Q4_0 = 0, TCF_Q6_K = 1, TCF_Q8_0 = 2, TCF_Q4_K = 3 };
+enum TcFormat { TCF_Q4_0 = 0, TCF_Q6_K = 1, TCF_Q8_0 = 2, TCF_Q4_K = 3, TCF_Q5_K = 4 };
 // A Q4_K job is one superblock (8 blocks) of a 16-row tile: codes [block
 // p][lane 4g + t] 8 B (word t of row g's then of row g + 8's Q4_0-ordered
 // 16 code bytes: byte k = value k | value k + 16 << 4), then [row][p] {scale,
 // min} bytes (16 B per row), then [row] {fp16 d, fp16 dmin}.
 constexpr int TC_Q4_K_JOB = 8 * 256 + 8 * TC_ROWS * 2 + TC_ROWS * 4;  // 2368 B
+// Q5_K adds, after the codes, the fifth bits: [p][row] a 4-byte word whose
+// byte k bit s is the fifth bit of value k + 4 s of block p.
+constexpr int TC_Q5_K_JOB = TC_Q4_K_JOB + 8 * TC_ROWS * 4;  // 2880 B
 // A Q6_K job is one superblock (8 blocks) of 16 rows: ring stage = ql box
 // (16 x 128 B, 128-byte swizzle) + qh box (16 x 64 B, 64-byte swizzle), then
 // in the scale ring the sc box (16 x 16 B) + the chunk's superblock scales
@@ -292,7 +295,7 @@ __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const ui
                 mp[2 + (c & 1)] = (float)(-1056 * s_lo);
                 mp[4 + (c & 1)] = (float)(-96 * s_hi);
                 mp[6 + (c & 1)] = 0.0f;
-            } else if constexpr (FMT == TCF_Q4_K) {
+            } else if constexpr (FMT == TCF_Q4_K || FMT == TCF_Q5_K) {
                 float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 8;
                 mp[c & 1] = da;
                 mp[2 + (c & 1)] = (float)(-1024 * s_lo - 64 * s_hi);
@@ -493,18 +496,22 @@ __device__ __forceinline__ float mul_u8(float f, float f_neg23, uint32_t w, int 
     return fmaf(f, __int_as_float((int)__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)k)), f_neg23);
 }
 
-template <int M>
+// FIVE: Q5_K, whose fifth code bits (the word of row g, shifted right by t:
+// byte k bit 0 = value 4t + k, bit 4 = value 16 + 4t + k) go to bit 4 (16 in
+// the code 1024 + q) or bit 8 (16 in 1024 + 16 q) of each f16.
+template <int M, bool FIVE>
 __device__ __forceinline__ void tc_job_q4_k(const uint8_t* sn, const uint8_t* act, const float* meta, int kb, int g,
                                             int t, float (&acc)[(M + 7) / 8][4])
 {
     constexpr int NT = (M + 7) / 8;
+    constexpr int SCM = 8 * 256 + (FIVE ? 8 * TC_ROWS * 4 : 0);  // the {scale, min} bytes
     const uint8_t* codes = sn + (g * 4 + t) * 8;
     // rows g, g + 8: {scale, min} of the 8 blocks (16 B each), {d, dmin}
-    const uint4 sma = *reinterpret_cast<const uint4*>(sn + 8 * 256 + g * 16);
-    const uint4 smb = *reinterpret_cast<const uint4*>(sn + 8 * 256 + (g + 8) * 16);
+    const uint4 sma = *reinterpret_cast<const uint4*>(sn + SCM + g * 16);
+    const uint4 smb = *reinterpret_cast<const uint4*>(sn + SCM + (g + 8) * 16);
     const uint32_t sa[4] = {sma.x, sma.y, sma.z, sma.w}, sb[4] = {smb.x, smb.y, smb.z, smb.w};
-    const uint32_t dda = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + 8 * TC_ROWS * 2 + g * 4);
-    const uint32_t ddb = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + 8 * TC_ROWS * 2 + (g + 8) * 4);
+    const uint32_t dda = *reinterpret_cast<const uint32_t*>(sn + SCM + 8 * TC_ROWS * 2 + g * 4);
+    const uint32_t ddb = *reinterpret_cast<const uint32_t*>(sn + SCM + 8 * TC_ROWS * 2 + (g + 8) * 4);
     const float da_w = __half2float(__ushort_as_half((unsigned short)(dda & 0xFFFFu)));
     const float dma_w = __half2float(__ushort_as_half((unsigned short)(dda >> 16)));
     const float db_w = __half2float(__ushort_as_half((unsigned short)(ddb & 0xFFFFu)));
@@ -515,10 +522,29 @@ __device__ __forceinline__ void tc_job_q4_k(const uint8_t* sn, const uint8_t* ac
     for (int p = 0; p < 8; ++p) {
         const uint2 w = *reinterpret_cast<const uint2*>(codes + p * 256);
         const uint32_t wa8 = w.x >> 8, wb8 = w.y >> 8;
-        const uint32_t A0[4] = {nib_f16x2<0x000F000Fu>(w.x), nib_f16x2<0x000F000Fu>(w.y), nib_f16x2<0x000F000Fu>(wa8),
-                                nib_f16x2<0x000F000Fu>(wb8)};
-        const uint32_t A1[4] = {nib_f16x2<0x00F000F0u>(w.x), nib_f16x2<0x00F000F0u>(w.y), nib_f16x2<0x00F000F0u>(wa8),
-                                nib_f16x2<0x00F000F0u>(wb8)};
+        uint32_t A0[4], A1[4];
+        if constexpr (FIVE) {
+            const uint32_t ha = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + (p * TC_ROWS + g) * 4) >> t;
+            const uint32_t hb = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + (p * TC_ROWS + g + 8) * 4) >> t;
+            const uint32_t ha4 = ha << 4, hb4 = hb << 4, ha_4 = ha >> 4, hb_4 = hb >> 4;
+            A0[0] = q6_f16x2<0x000F000Fu, 0x00100010u>(w.x, ha4);
+            A0[1] = q6_f16x2<0x000F000Fu, 0x00100010u>(w.y, hb4);
+            A0[2] = q6_f16x2<0x000F000Fu, 0x00100010u>(wa8, ha_4);
+            A0[3] = q6_f16x2<0x000F000Fu, 0x00100010u>(wb8, hb_4);
+            A1[0] = q6_f16x2<0x00F000F0u, 0x01000100u>(w.x, ha4);
+            A1[1] = q6_f16x2<0x00F000F0u, 0x01000100u>(w.y, hb4);
+            A1[2] = q6_f16x2<0x00F000F0u, 0x01000100u>(wa8, ha_4);
+            A1[3] = q6_f16x2<0x00F000F0u, 0x01000100u>(wb8, hb_4);
+        } else {
+            A0[0] = nib_f16x2<0x000F000Fu>(w.x);
+            A0[1] = nib_f16x2<0x000F000Fu>(w.y);
+            A0[2] = nib_f16x2<0x000F000Fu>(wa8);
+            A0[3] = nib_f16x2<0x000F000Fu>(wb8);
+            A1[0] = nib_f16x2<0x00F000F0u>(w.x);
+            A1[1] = nib_f16x2<0x00F000F0u>(w.y);
+            A1[2] = nib_f16x2<0x00F000F0u>(wa8);
+            A1[3] = nib_f16x2<0x00F000F0u>(wb8);
+        }
         // d sc and dmin m of block p, exact (fp16 x 6 bits): bytes 2 (p & 1),
         // + 1 of word p / 2
         const int k = 2 * (p & 1);
@@ -714,6 +740,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int NIB = FMT == TCF_Q8_0   ? tc_q8_0_job_bytes(JB)
                     : FMT == TCF_Q6_K ? TC_Q6_K_NIB
                     : FMT == TCF_Q4_K ? TC_Q4_K_JOB
+                    : FMT == TCF_Q5_K ? TC_Q5_K_JOB
                                       : tc_nib_bytes(JB);
     const int DSB = FMT == TCF_Q6_K ? TC_Q6_K_DS : FMT == TCF_Q4_0 ? tc_ds_bytes(JB) : 0;
     const int JPC = CHUNK / JB, JPC_LOG = JB > TC_LINE_JB ? 1 : 2;  // jobs per 32-block chunk
@@ -723,7 +750,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int J = ntile * jpt;
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
     const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB,
-                              FMT == TCF_Q6_K || FMT == TCF_Q4_K ? 128 : 64);
+                              FMT == TCF_Q6_K || FMT == TCF_Q4_K || FMT == TCF_Q5_K ? 128 : 64);
     uint8_t* nib = smem + sl.nib;
     uint8_t* ds = smem + sl.ds;
     uint8_t* act = smem + sl.act;
@@ -794,9 +821,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     bulk_g2s(dst, src + hh * JB * 512, JB * 512, bar, pol);
                     bulk_g2s(dst + JB * 512, src + TC_Q8_0_CODES + hh * JB * 32, JB * 32, bar, pol);
                 }
-            } else if constexpr (FMT == TCF_Q4_K) {
-                // the job's region of the Q4_K pack: tile igrp / 4, superblock ikg
-                bulk_g2s(dst, a.w0 + ((int64_t)(igrp >> 2) * njb + ikg) * TC_Q4_K_JOB, TC_Q4_K_JOB, bar, pol);
+            } else if constexpr (FMT == TCF_Q4_K || FMT == TCF_Q5_K) {
+                // the job's region of the pack: tile igrp / 4, superblock ikg
+                bulk_g2s(dst, a.w0 + ((int64_t)(igrp >> 2) * njb + ikg) * NIB, NIB, bar, pol);
             } else if constexpr (FMT == TCF_Q6_K) {
                 // superblock h of chunk c for the tile's 16 rows: ql, qh and sc
                 // boxes of the row tiles, then the chunk's superblock scales
@@ -904,7 +931,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         ++consumed;
         if constexpr (FMT == TCF_Q8_0) tc_job_q8_0<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, JB, g, t, acc);
-        else if constexpr (FMT == TCF_Q4_K) tc_job_q4_k<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, g, t, acc);
+        else if constexpr (FMT == TCF_Q4_K || FMT == TCF_Q5_K)
+            tc_job_q4_k<M, FMT == TCF_Q5_K>(wnib + (size_t)slot * NIB, act, meta, kj * JB, g, t, acc);
         else if constexpr (FMT == TCF_Q6_K)
             tc_job_q6_k<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB,
                            (jb0 + kj) & (JPC - 1), g, t, acc);

@@ -364,6 +364,26 @@ int qpack_q4_k(const void* w_canon, void* w_pack, int N, int K, void* stream);
 int qgemv_q4_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
 int qgemv_q4_k_plan(int M, int K, int N, int* info);
 
+/* ---- NEXT-4: a further format, Q5_K ------------------------------------ */
+
+/* Q5_K (named with Q4_K among the further K-quant formats; defined as in
+ * llama.cpp): superblocks of 256 = fp16 d, fp16 dmin, the 12 scale/min bytes
+ * of Q4_K, qh[32], then the 128 code bytes of Q4_K; the fifth bit of value i
+ * is bit i/32 of qh[i % 32], so q_i = nibble + 16 * that bit (0..31) and
+ * value i = d * sc_{i/32} * q_i - dmin * m_{i/32}.                     176 B
+ *
+ * qpack_q5_k - canonical [N][K/256] x 176 B -> the Q4_K pack layout with, after
+ * the codes, a [block][row] 4-byte word of fifth bits (byte k, bit s = value
+ * k + 4s of the block): 2880 B per 16-row tile and superblock (180 B per row
+ * and superblock); q5_k_pack_bytes(N, K) bytes, 0 when K % 256.
+ *
+ * qgemv_q5_k / qgemv_q5_k_plan - as qgemv_q4_k / qgemv_q4_k_plan with 5-bit
+ * codes.  (The plan query is not from the pages.) */
+size_t q5_k_pack_bytes(int N, int K);
+int qpack_q5_k(const void* w_canon, void* w_pack, int N, int K, void* stream);
+int qgemv_q5_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);
+int qgemv_q5_k_plan(int M, int K, int N, int* info);
+
 /* qgemv_q8_0_plan - the launch qgemv_q8_0 would make for this shape; writes
  * info[5] = {1, CTAs per cluster (the K parts), grid size, ring stages per
  * warp, blocks per job (8: a whole pack region; 4: half of one, taken where

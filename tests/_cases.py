@@ -100,6 +100,31 @@ def pack_q4_k(w: np.ndarray) -> np.ndarray:
     return out.reshape(-1)
 
 
+def pack_q5_k(w: np.ndarray) -> np.ndarray:
+    """Canonical Q5_K [N, K/256, 176] -> the documented tensor-core pack: the
+    Q4_K pack of the same d, dmin, scales and nibbles, with a [block p][row]
+    4-byte word of fifth bits (byte k, bit s = the fifth bit of value k + 4s of
+    block p = bit p of qh[k + 4s]) inserted after the 2048 code bytes."""
+    N, ns, _ = w.shape
+    T = (N + 15) // 16
+    q4 = pack_q4_k(np.concatenate([w[:, :, 0:16], w[:, :, 48:176]], axis=2)).reshape(T, ns, 2368)
+    wp = np.zeros((T * 16, ns, 176), dtype=np.uint8)
+    wp[:N] = w
+    out = np.zeros((T, ns, 2880), dtype=np.uint8)
+    out[:, :, 0:2048] = q4[:, :, 0:2048]
+    out[:, :, 2560:2880] = q4[:, :, 2048:2368]
+    qh = wp[:, :, 16:48].astype(np.int64)  # [rows, ns, 32]
+    for p in range(8):
+        for k in range(4):
+            byte = np.zeros((T * 16, ns), dtype=np.int64)
+            for s2 in range(8):
+                byte |= ((qh[:, :, k + 4 * s2] >> p) & 1) << s2
+            for tau in range(T):
+                for r in range(16):
+                    out[tau, :, 2048 + (p * 16 + r) * 4 + k] = byte[16 * tau + r]
+    return out.reshape(-1)
+
+
 def unpack_q4_0(pack: np.ndarray, N: int, K: int) -> np.ndarray:
     """Inverse of pack_q4_0."""
     nb = K // 32

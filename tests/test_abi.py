@@ -68,6 +68,9 @@ def test_sizes(lib):
     assert lib.q4_k_pack_bytes(16, 5120) == 20 * 2368  # 148 B per row and superblock
     assert lib.q4_k_pack_bytes(17, 256) == 2 * 2368  # rows padded to 32
     assert lib.q4_k_pack_bytes(16, 384) == 0  # K % 256
+    lib.q5_k_pack_bytes.restype = ctypes.c_size_t
+    assert lib.q5_k_pack_bytes(16, 5120) == 20 * 2880  # 180 B per row and superblock
+    assert lib.q5_k_pack_bytes(16, 384) == 0  # K % 256
 
 
 def test_status_strings(lib):

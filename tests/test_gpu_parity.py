@@ -534,6 +534,61 @@ def test_qgemv_q4_k_stride_errors_and_plans(ops):
         assert pl["tensor_cores"] and pl["stages"] >= 2 and pl["grid"] % pl["cluster"] == 0 and pl["job_blocks"] == 8
 
 
+# ---------------------------------------------------------------- Q5_K (tensor cores)
+@pytest.mark.parametrize("N,K", [(16, 256), (37, 512), (5, 1024)])
+def test_qpack_q5_k_layout(ops, N, K):
+    w = synth.q5_k_weights(N, K, seed=N + K + 1)
+    got = _np(ops.qpack_q5_k(_t(w), N, K))
+    assert np.array_equal(got, C.pack_q5_k(w))
+
+
+Q5_K_SHAPES = [(M, K, N) for M in (1, 5, 6, 9, 12, 17) for (K, N) in ((256, 1), (512, 37), (5120, 611))] + [
+    (6, 17408, 320), (17, 17408, 64), (6, 5120, 4096), (12, 5120, 17408)]
+
+
+@pytest.mark.parametrize("M,K,N", Q5_K_SHAPES)
+def test_qgemv_q5_k_matches_oracle(ops, M, K, N):
+    x = synth.activations(M, K, seed=M + 9 * K, outlier_frac=0.01)
+    w = synth.q5_k_weights(N, K, seed=N + 7 * K)
+    y_ref, S = oracle.qgemv_q5_k(w, oracle.quantize_q8_1(x))
+    y = _np(ops.qgemv_q5_k(ops.qpack_q5_k(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
+    r = C.check_close(y, y_ref, S)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("M,K,N", [(6, 2048, 64), (1, 1024, 33), (17, 2048, 48), (9, 4096, 16)])
+def test_qgemv_q5_k_unit_scales_exact(ops, M, K, N):
+    # as the Q4_K case: d = dmin = 1, d_a = 1, every partial sum an integer
+    # below 2^24, so the fifth bits must land exactly
+    w = synth.q5_k_weights(N, K, seed=M + K + 3, d_lo=1.0, d_hi=1.0, dmin_lo=1.0, dmin_hi=1.0)
+    g = np.random.default_rng(M + N + 3)
+    x = g.integers(-3, 4, size=(M, K)).astype(np.float32)
+    x[:, ::32] = np.where(g.integers(0, 2, size=(M, K // 32)) == 1, 127.0, -127.0).astype(np.float32)
+    xq_ref = oracle.quantize_q8_1(x)
+    assert np.all(xq_ref[:, :, 0:2].view(np.float16) == 1.0)
+    y_ref, S = oracle.qgemv_q5_k(w, xq_ref)
+    assert np.all(S < 2.0 ** 24)
+    y = _np(ops.qgemv_q5_k(ops.qpack_q5_k(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def test_qgemv_q5_k_errors_and_plans(ops):
+    M, K, N = 6, 1024, 40
+    w = synth.q5_k_weights(N, K, seed=21)
+    x = synth.activations(M, K, seed=22)
+    wp, xq = ops.qpack_q5_k(_t(w), N, K), ops.quantize_q8_1(_t(x))
+    y = torch.empty((M, N), device=DEV)
+    L = ops.LIB
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    assert L.qgemv_q5_k(p(wp), p(xq), p(y), N, M, 384, N, None) == -2  # K % 256
+    assert L.qgemv_q5_k(p(wp), p(xq), p(y), N, 18, K, N, None) == -2  # M > 17
+    assert L.qgemv_q5_k(None, p(xq), p(y), N, M, K, N, None) == -1
+    assert ops.qgemv_take_wait_timeouts() == 0
+    for M2, K2, N2 in Q5_K_SHAPES + [(17, 5120, 248320), (6, 5120, 248320)]:
+        pl = ops.qgemv_q5_k_plan(M2, K2, N2)
+        assert pl["tensor_cores"] and pl["stages"] >= 2 and pl["grid"] % pl["cluster"] == 0 and pl["job_blocks"] == 8
+
+
 def test_qgemv_q8_0_plans(ops):
     # 8-block jobs where two stages of them fit, 4-block jobs (half a pack
     # region) where they do not; very large N launches clusters in waves
@@ -553,7 +608,7 @@ def test_qgemv_q8_0_plans(ops):
 
 @pytest.mark.parametrize("fmt,M,N", [("q8_0", 17, 40000), ("q8_0", 12, 40000), ("q4_0", 17, 40000),
                                      ("q4_0", 12, 40000), ("q6_k", 17, 40000), ("q6_k", 12, 40000),
-                                     ("q4_k", 17, 40000)])
+                                     ("q4_k", 17, 40000), ("q5_k", 17, 40000)])
 def test_large_n_wave_plans_sampled_rows(ops, fmt, M, N):
     # more clusters than are resident (the combine area holds a wave's tiles
     # only): outputs checked on a sample of rows, which the oracle computes
@@ -565,6 +620,10 @@ def test_large_n_wave_plans_sampled_rows(ops, fmt, M, N):
         w = synth.q8_0_weights(N, K, seed=N + M)
         y = _np(ops.qgemv_q8_0(ops.qpack_q8_0(_t(w), N, K), xq, M, K, N))
         ref = oracle.qgemv_q8_0
+    elif fmt == "q5_k":
+        w = synth.q5_k_weights(N, K, seed=N + M)
+        y = _np(ops.qgemv_q5_k(ops.qpack_q5_k(_t(w), N, K), xq, M, K, N))
+        ref = oracle.qgemv_q5_k
     elif fmt == "q4_k":
         w = synth.q4_k_weights(N, K, seed=N + M)
         y = _np(ops.qgemv_q4_k(ops.qpack_q4_k(_t(w), N, K), xq, M, K, N))
