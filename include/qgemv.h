@@ -20,6 +20,7 @@
  *   Q6_K  256 weights: uint8 ql[128], uint8 qh[64], int8 sc[16], fp16 d;
  *         low 4 bits of value i = nibble (i & 1) of ql[i >> 1], high 2 bits
  *         = bits 2 (i & 3) of qh[i >> 2]; w = d * sc[i >> 4] * (q - 32) 210 B
+ *   Q8_0, Q4_K, Q5_K  the further formats, defined with their calls below.
  * All multi-byte fields are little endian.
  *
  * Conventions for every call:
