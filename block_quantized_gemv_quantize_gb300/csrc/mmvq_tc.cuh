@@ -324,6 +324,27 @@ __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const ui
     }
 }
 
+// Packed fp32 pairs (sm_100 and later): (ax, ay) = (bx, by) * (cx, cy) + (ax, ay)
+// and (dx, dy) = (bx, by) * (cx, cy), each lane one IEEE fma / mul, so the
+// results equal the scalar ones bit for bit with half the instructions.
+__device__ __forceinline__ void fma_f32x2(float& ax, float& ay, float bx, float by, float cx, float cy)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\t"
+        "mov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
+        "fma.rn.f32x2 a, b, c, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(ax), "+f"(ay)
+        : "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+
+__device__ __forceinline__ void mul_f32x2(float& dx, float& dy, float bx, float by, float cx, float cy)
+{
+    asm("{\n\t.reg .b64 d, b, c;\n\t"
+        "mov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(dx), "=f"(dy)
+        : "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+
 // One job: 16 blocks of the tile in ring stage (sn codes, sd scales) against
 // staged blocks kb .. kb + 7.  acc[nt][i]: rows g, g, g+8, g+8 and columns
 // 8 nt + 2t, +1, +0, +1 (the mma accumulator layout).
@@ -366,10 +387,12 @@ __device__ __forceinline__ void tc_job(const uint8_t* sn, const uint8_t* sd, con
             float d[4];
             mma_f16_16816(d, A0, B.x, B.y, md.z, md.w, md.z, md.w);
             mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
-            jacc[nt][0] = fmaf(dwa * md.x, d[0], jacc[nt][0]);
-            jacc[nt][1] = fmaf(dwa * md.y, d[1], jacc[nt][1]);
-            jacc[nt][2] = fmaf(dwb * md.x, d[2], jacc[nt][2]);
-            jacc[nt][3] = fmaf(dwb * md.y, d[3], jacc[nt][3]);
+            // jacc += (d_w d_a) D, the exact fp16 x fp16 product first
+            float sa0, sa1, sb0, sb1;
+            mul_f32x2(sa0, sa1, dwa, dwa, md.x, md.y);
+            mul_f32x2(sb0, sb1, dwb, dwb, md.x, md.y);
+            fma_f32x2(jacc[nt][0], jacc[nt][1], sa0, sa1, d[0], d[1]);
+            fma_f32x2(jacc[nt][2], jacc[nt][3], sb0, sb1, d[2], d[3]);
         }
     }
 #pragma unroll
@@ -561,10 +584,13 @@ __device__ __forceinline__ void tc_job_q4_k(const uint8_t* sn, const uint8_t* ac
             float d[4];
             mma_f16_16816(d, A0, B.x, B.y, md.z, md.w, md.z, md.w);
             mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
-            acc[nt][0] = fmaf(-Ma, me.x, fmaf(Da * md.x, d[0], acc[nt][0]));
-            acc[nt][1] = fmaf(-Ma, me.y, fmaf(Da * md.y, d[1], acc[nt][1]));
-            acc[nt][2] = fmaf(-Mb, me.x, fmaf(Db * md.x, d[2], acc[nt][2]));
-            acc[nt][3] = fmaf(-Mb, me.y, fmaf(Db * md.y, d[3], acc[nt][3]));
+            float sa0, sa1, sb0, sb1;
+            mul_f32x2(sa0, sa1, Da, Da, md.x, md.y);
+            mul_f32x2(sb0, sb1, Db, Db, md.x, md.y);
+            fma_f32x2(acc[nt][0], acc[nt][1], sa0, sa1, d[0], d[1]);
+            fma_f32x2(acc[nt][2], acc[nt][3], sb0, sb1, d[2], d[3]);
+            fma_f32x2(acc[nt][0], acc[nt][1], -Ma, -Ma, me.x, me.y);
+            fma_f32x2(acc[nt][2], acc[nt][3], -Mb, -Mb, me.x, me.y);
         }
     }
 }
@@ -677,10 +703,11 @@ __device__ __forceinline__ void tc_job_q8_0(const uint8_t* sn, const uint8_t* ac
             float d[4];
             mma_f16_16816(d, A0, B.x, B.y, 0.0f, 0.0f, 0.0f, 0.0f);
             mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
-            jacc[nt][0] = fmaf(dwa * md.x, d[0], jacc[nt][0]);
-            jacc[nt][1] = fmaf(dwa * md.y, d[1], jacc[nt][1]);
-            jacc[nt][2] = fmaf(dwb * md.x, d[2], jacc[nt][2]);
-            jacc[nt][3] = fmaf(dwb * md.y, d[3], jacc[nt][3]);
+            float sa0, sa1, sb0, sb1;
+            mul_f32x2(sa0, sa1, dwa, dwa, md.x, md.y);
+            mul_f32x2(sb0, sb1, dwb, dwb, md.x, md.y);
+            fma_f32x2(jacc[nt][0], jacc[nt][1], sa0, sa1, d[0], d[1]);
+            fma_f32x2(jacc[nt][2], jacc[nt][3], sb0, sb1, d[2], d[3]);
         }
     }
 #pragma unroll
