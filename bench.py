@@ -59,8 +59,12 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded oracle sample length")
     p.add_argument("--sweep", action="store_true",
-                   help="instead of the step: time qgemv_q4_0/qgemv_q6_k over M in {1,2,4,6,9,12,17}, "
-                        "K=5120, N in {5120, 17408, 248320} (one JSON line per shape)")
+                   help="instead of the step: time qgemv_<format> over M in {1,2,4,6,9,12,17}, K=5120, "
+                        "N in {5120, 17408, 248320} for Q4_0, Q6_K, Q8_0, Q4_K, Q5_K (one JSON line per shape)")
+    p.add_argument("--sweep-formats", default="q4_0,q6_k,q8_0,q4_k,q5_k", help="sweep: comma-separated formats")
+    p.add_argument("--sweep-m", default="1,2,4,6,9,12,17", help="sweep: comma-separated row counts M")
+    p.add_argument("--sweep-n", default="5120,17408,248320", help="sweep: comma-separated output sizes N")
+    p.add_argument("--sweep-k", type=int, default=5120, help="sweep: the reduction size K")
     return p.parse_args()
 
 
@@ -474,22 +478,23 @@ def run_sweep(args):
     gemv = {"q4_0": ops.qgemv_q4_0, "q6_k": ops.qgemv_q6_k, "q8_0": ops.qgemv_q8_0, "q4_k": ops.qgemv_q4_k,
             "q5_k": ops.qgemv_q5_k}
     canonical = {"q4_k": 144, "q5_k": 176}  # bytes per 256 values
-    for fmt in ("q4_0", "q6_k", "q8_0", "q4_k", "q5_k"):
-        for N in (5120, 17408, 248320):
-            nbytes_w = pack_bytes[fmt](N, K_H)
+    K = args.sweep_k
+    for fmt in args.sweep_formats.split(","):
+        for N in (int(v) for v in args.sweep_n.split(",")):
+            nbytes_w = pack_bytes[fmt](N, K)
             # algorithmic bytes: the canonical size (the Q4_K / Q5_K packs carry
             # 148 / 180 B per 256 values against 144 / 176; the others are equal)
-            nbytes_alg = N * (K_H // 256) * canonical[fmt] if fmt in canonical else nbytes_w
+            nbytes_alg = N * (K // 256) * canonical[fmt] if fmt in canonical else nbytes_w
             w = torch.randint(0, 256, (nbytes_w,), dtype=torch.uint8, generator=g).to(dev)
-            for M in (1, 2, 4, 6, 9, 12, 17):
-                x = torch.randn(M, K_H, generator=g).to(dev)
+            for M in (int(v) for v in args.sweep_m.split(",")):
+                x = torch.randn(M, K, generator=g).to(dev)
                 xq = ops.quantize_q8_1(x)
                 y = torch.empty((M, N), device=dev)
-                call = (lambda f=gemv[fmt]: f(w, xq, M, K_H, N, y=y))
+                call = (lambda f=gemv[fmt]: f(w, xq, M, K, N, y=y))
                 try:
                     call()
                 except ops.QgemvError as e:  # a shape the library declines: recorded, not timed
-                    print(json.dumps({"sweep": fmt, "M": M, "K": K_H, "N": N, "unsupported": str(e)}), flush=True)
+                    print(json.dumps({"sweep": fmt, "M": M, "K": K, "N": N, "unsupported": str(e)}), flush=True)
                     continue
                 for _ in range(3):
                     call()
@@ -503,9 +508,9 @@ def run_sweep(args):
                     torch.cuda.synchronize()
                     ts.append(a.elapsed_time(b))
                 us = statistics.median(ts) * 1e3
-                nbytes = nbytes_alg + ops.q8_1_bytes(M, K_H)
+                nbytes = nbytes_alg + ops.q8_1_bytes(M, K)
                 gbs = nbytes / (us * 1e-6) / 1e9
-                print(json.dumps({"sweep": fmt, "M": M, "K": K_H, "N": N, "us": round(us, 2),
+                print(json.dumps({"sweep": fmt, "M": M, "K": K, "N": N, "us": round(us, 2),
                                   "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
                                   "l2": "flushed before every call"}), flush=True)
             del w
