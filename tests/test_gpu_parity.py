@@ -649,6 +649,24 @@ def test_large_n_wave_plans_sampled_rows(ops, fmt, M, N):
     assert np.isfinite(y).all()
 
 
+@pytest.mark.parametrize("wq,xv", [(127, 127), (-127, 127), (127, -127), (-128, 127), ("alt", 127), ("alt", -127)])
+def test_qgemv_q8_0_extreme_codes_exact(ops, wq, xv):
+    # the largest products and accumulator starts the tensor-core path sees
+    # (codes at the int8 extremes, activations all +-127, d_w = d_a = 1): the
+    # block dots and their sum over K = 256 (|y| <= 8 * 32 * 128 * 127) are
+    # integers below 2^24, so the output must equal the oracle's exactly;
+    # "alt" alternates +-127 so that the products cancel against the start
+    M, K, N = 9, 256, 32
+    w = synth.q8_0_weights(N, K, seed=1, d_lo=1.0, d_hi=1.0)
+    codes = np.full(32, wq, dtype=np.int64) if wq != "alt" else np.tile([127, -127], 16)
+    w[:, :, 2:] = codes.astype(np.int8).view(np.uint8)
+    x = np.full((M, K), float(xv), dtype=np.float32)
+    xq_ref = oracle.quantize_q8_1(x)
+    y_ref, _ = oracle.qgemv_q8_0(w, xq_ref)
+    y = _np(ops.qgemv_q8_0(ops.qpack_q8_0(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
 def test_qgemv_q8_0_stride_padding_and_errors(ops):
     M, K, N, ldy = 6, 1024, 40, 48
     w = synth.q8_0_weights(N, K, seed=9)
