@@ -485,10 +485,14 @@ __device__ __forceinline__ void tc_job_q6_k(const uint8_t* sq, const uint8_t* ss
             float d0[4], d1[4];
             mma_f16_16816(d0, A0, B.x, B.y, md.z, md.w, md.z, md.w);
             mma_f16_16816(d1, A1, B.z, B.w, mc.x, mc.y, mc.x, mc.y);
-            jacc[nt][0] = fmaf(md.x, fmaf(s1a, d1[0], s0a * d0[0]), jacc[nt][0]);
-            jacc[nt][1] = fmaf(md.y, fmaf(s1a, d1[1], s0a * d0[1]), jacc[nt][1]);
-            jacc[nt][2] = fmaf(md.x, fmaf(s1b, d1[2], s0b * d0[2]), jacc[nt][2]);
-            jacc[nt][3] = fmaf(md.y, fmaf(s1b, d1[3], s0b * d0[3]), jacc[nt][3]);
+            // J = sc0 I0 + sc1 I1 (exact), then jacc += d_a J, in column pairs
+            float ja0, ja1, jb0, jb1;
+            mul_f32x2(ja0, ja1, s0a, s0a, d0[0], d0[1]);
+            mul_f32x2(jb0, jb1, s0b, s0b, d0[2], d0[3]);
+            fma_f32x2(ja0, ja1, s1a, s1a, d1[0], d1[1]);
+            fma_f32x2(jb0, jb1, s1b, s1b, d1[2], d1[3]);
+            fma_f32x2(jacc[nt][0], jacc[nt][1], md.x, md.y, ja0, ja1);
+            fma_f32x2(jacc[nt][2], jacc[nt][3], md.x, md.y, jb0, jb1);
         }
     }
     // superblock scales of rows g, g + 8: group g / 4, row g % 4, superblock h
