@@ -365,7 +365,8 @@ def run_native(args, rank, world):
 
     ab = {"fused": [], "unfused": [], "candmax": [], "target_fused": [], "target_unfused": [], "rms_q8": [],
           "q8_only": []}
-    for _ in range(5):
+    ab_rounds = 20  # interleaved A/B rounds of 10 calls each
+    for _ in range(ab_rounds):
         for name, fn in (("fused", fused), ("unfused", unfused), ("candmax", candmax), ("target_fused", target_fused),
                          ("target_unfused", target_unfused), ("rms_q8", rms_q8), ("q8_only", q8_only)):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -377,6 +378,17 @@ def run_native(args, rank, world):
             ab[name].append(a.elapsed_time(b) * 1e3 / 10)
     same_ids = ids_d.cpu().tolist() == ids_u.cpu().tolist()
     same_ids_t = ids_tf.cpu().tolist() == ids_t.cpu().tolist()
+
+    def ab_pair(a_name, b_name, keys, extra):
+        """Medians of two interleaved arms, and the median, p10 and p90 of
+        their per-round difference (b - a, us)."""
+        diff = [y - x for x, y in zip(ab[a_name], ab[b_name])]
+        q = statistics.quantiles(diff, n=10)
+        out = {keys[0]: round(statistics.median(ab[a_name]), 2), keys[1]: round(statistics.median(ab[b_name]), 2),
+               "diff_median": round(statistics.median(diff), 2), "diff_p10": round(q[0], 2),
+               "diff_p90": round(q[-1], 2), "rounds": ab_rounds}
+        out.update(extra)
+        return out
 
     peak, peak_kind = peaks()
     dominant = max(("lmhead_top1", "target_head", "gate_up", "down"), key=lambda n: call_ms[n])
@@ -408,15 +420,11 @@ def run_native(args, rank, world):
             "mmvq_m6_q4_0": {"gbs": round(mmvq_gbs, 1), "frac_of_hbm_peak": round(mmvq_gbs / peak, 4),
                              "us": {n: round(call_ms[n] * 1e3, 2) for n in mmvq_names}},
             "lmhead_top1_us": round(call_ms["lmhead_top1"] * 1e3, 2),
-            "fused_vs_unfused_us": {"fused": round(statistics.median(ab["fused"]), 2),
-                                    "unfused": round(statistics.median(ab["unfused"]), 2),
-                                    "same_ids": same_ids},
+            "fused_vs_unfused_us": ab_pair("fused", "unfused", ("fused", "unfused"), {"same_ids": same_ids}),
             "candmax_us": round(statistics.median(ab["candmax"]), 2),
-            "rmsnorm_q8_1_vs_quantize_us": {"rmsnorm_q8_1": round(statistics.median(ab["rms_q8"]), 2),
-                                            "quantize_q8_1": round(statistics.median(ab["q8_only"]), 2)},
-            "target_m6_fused_vs_unfused_us": {"fused": round(statistics.median(ab["target_fused"]), 2),
-                                              "unfused": round(statistics.median(ab["target_unfused"]), 2),
-                                              "same_ids": same_ids_t},
+            "rmsnorm_q8_1_vs_quantize_us": ab_pair("q8_only", "rms_q8", ("quantize_q8_1", "rmsnorm_q8_1"), {}),
+            "target_m6_fused_vs_unfused_us": ab_pair("target_fused", "target_unfused", ("fused", "unfused"),
+                                                     {"same_ids": same_ids_t}),
             "per_call_us": {n: round(call_ms[n] * 1e3, 2) for n in names},
             "per_call_gbs": {n: round(nbytes[n] / (call_ms[n] * 1e-3) / 1e9, 1) for n in names},
             "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
@@ -569,9 +577,15 @@ def cpu_baseline(inp, seconds: float):
         total_t += dt
         total_b += nb
         reps += 1
+    # the same oracle on one core, on a smaller row fraction (about a quarter
+    # of the time above), for the single-thread figure
+    frac1 = calibrate_fraction(inp, seconds / 4, 1)
+    t1, b1 = oracle_sample_step(inp, frac1, 1)
     return {"value": round(total_b / total_t / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
             "sample": f"{reps} oracle step(s) over the first {frac:.2%} of the rows of every weight "
-                      f"({total_t:.1f} s, {total_b / 1e6:.0f} MB)"}
+                      f"({total_t:.1f} s, {total_b / 1e6:.0f} MB)",
+            "single_core": {"value": round(b1 / t1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                            "sample": f"one oracle step over the first {frac1:.2%} of the rows ({t1:.1f} s)"}}
 
 
 def run_reference(args):
