@@ -269,7 +269,7 @@ def top1(y: np.ndarray) -> np.ndarray:
 def lmhead_q6_k_top1(w: np.ndarray, x: np.ndarray, nthreads: int | None = None):
     """Fused LM-head top-1, step by step: quantize the rows of x to Q8_1, project
     them through the Q6_K weight, take the lowest-ID argmax of each row.
-    Returns (ids, y, S) so that callers can judge near-ties."""
+    Returns (ids, y, S) so that callers can decide near-ties."""
     xq = quantize_q8_1(x)
     y, S = qgemv_q6_k(w, xq, nthreads)
     return top1(y), y, S
