@@ -285,6 +285,11 @@ def run_native(args, rank, world):
     torch.cuda.synchronize()
     call_ms = {n: statistics.mean(per[s_][i][0].elapsed_time(per[s_][i][1]) for s_ in range(n_break))
                for i, n in enumerate(names)}
+    call_spread = {}  # median, p10, p90 of each call over the n_break steps (us)
+    for i, n in enumerate(names):
+        v = [per[s_][i][0].elapsed_time(per[s_][i][1]) * 1e3 for s_ in range(n_break)]
+        q = statistics.quantiles(v, n=10)
+        call_spread[n] = {"median": round(statistics.median(v), 2), "p10": round(q[0], 2), "p90": round(q[-1], 2)}
 
     nbytes = step_bytes()
     step_total = sum(nbytes.values())
@@ -426,6 +431,7 @@ def run_native(args, rank, world):
             "target_m6_fused_vs_unfused_us": ab_pair("target_fused", "target_unfused", ("fused", "unfused"),
                                                      {"same_ids": same_ids_t}),
             "per_call_us": {n: round(call_ms[n] * 1e3, 2) for n in names},
+            "per_call_us_spread": call_spread,
             "per_call_gbs": {n: round(nbytes[n] / (call_ms[n] * 1e-3) / 1e9, 1) for n in names},
             "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
