@@ -100,6 +100,13 @@ struct TcSmem {
 
 constexpr int TC_TAB_INTS = 4 + 3 * (TC_THREADS / 32);  // the split-tile table
 
+// meta bytes per (block, 8-row tile): {d_a, d_a', C, C'} per lane (64), the
+// Q6_K pair of starts (128), or the Q4_K / Q5_K columns of d_a, C, d_a A (96)
+__host__ __device__ constexpr int tc_meta_bytes(int fmt)
+{
+    return fmt == TCF_Q6_K ? 128 : (fmt == TCF_Q4_K || fmt == TCF_Q5_K) ? 96 : 64;
+}
+
 // nibs / dsb: bytes of a ring stage's codes / scales (Q8_0: the whole job / 0);
 // metab: meta bytes per (block, 8-row tile): 64, or 128 for Q6_K (two
 // accumulator starts)
@@ -259,9 +266,9 @@ __device__ __forceinline__ uint32_t q8_f16x2(uint32_t w)
 // 0} with the two MMAs' own starts, C0 = -1056 sum_{i<16} q_a (codes 1024 + q
 // against q_a: (q - 32) q_a = (1024 + q) q_a - 1056 q_a) and C1 = -96
 // sum_{i>=16} q_a (codes 1024 + 16 q against q_a / 16: 64 q_a + q q_a - 96 q_a).
-// FMT = TCF_Q4_K: 32 B per lane, {d_a, d_a', C, C', d_a A, d_a' A', 0, 0} with
-// C = -1024 sum_{i<16} q_a - 64 sum_{i>=16} q_a (no code offset) and A = sum
-// q_a (the min term; d_a A is exact in fp32).
+// FMT = TCF_Q4_K / TCF_Q5_K: 96 B per (block, 8-row tile), [d_a x 8][C x
+// 8][d_a A x 8] by column, with C = -1024 sum_{i<16} q_a - 64 sum_{i>=16} q_a
+// (no code offset) and A = sum q_a (the min term; d_a A is exact in fp32).
 template <int M, int FMT = TCF_Q4_0>
 __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const uint8_t* raw, int nkb, int rstride)
 {
@@ -296,11 +303,10 @@ __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const ui
                 mp[4 + (c & 1)] = (float)(-96 * s_hi);
                 mp[6 + (c & 1)] = 0.0f;
             } else if constexpr (FMT == TCF_Q4_K || FMT == TCF_Q5_K) {
-                float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 8;
-                mp[c & 1] = da;
-                mp[2 + (c & 1)] = (float)(-1024 * s_lo - 64 * s_hi);
-                mp[4 + (c & 1)] = da * (float)(s_lo + s_hi);
-                mp[6 + (c & 1)] = 0.0f;
+                float* mp = meta + ((size_t)b * NT + nt) * 24;  // [d_a x 8][C x 8][d_a A x 8]
+                mp[c] = da;
+                mp[8 + c] = (float)(-1024 * s_lo - 64 * s_hi);
+                mp[16 + c] = da * (float)(s_lo + s_hi);
             } else {
                 float* mp = meta + (((size_t)b * NT + nt) * 4 + (c >> 1)) * 4;
                 mp[c & 1] = da;
@@ -582,15 +588,16 @@ __device__ __forceinline__ void tc_job_q4_k(const uint8_t* sn, const uint8_t* ac
         for (int nt = 0; nt < NT; ++nt) {
             const int n = nt * 8 + g < M ? nt * 8 + g : M - 1;  // rows past M: any staged row (unused)
             const uint4 B = *reinterpret_cast<const uint4*>(act + (((size_t)b * M + n) * 4 + t) * 16);
-            const float* mp = meta + (((size_t)b * NT + nt) * 4 + t) * 8;
-            const float4 md = *reinterpret_cast<const float4*>(mp);
-            const float2 me = *reinterpret_cast<const float2*>(mp + 4);
+            const float* mp = meta + ((size_t)b * NT + nt) * 24 + 2 * t;
+            const float2 mda = *reinterpret_cast<const float2*>(mp);
+            const float2 mc = *reinterpret_cast<const float2*>(mp + 8);
+            const float2 me = *reinterpret_cast<const float2*>(mp + 16);
             float d[4];
-            mma_f16_16816(d, A0, B.x, B.y, md.z, md.w, md.z, md.w);
+            mma_f16_16816(d, A0, B.x, B.y, mc.x, mc.y, mc.x, mc.y);
             mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
             float sa0, sa1, sb0, sb1;
-            mul_f32x2(sa0, sa1, Da, Da, md.x, md.y);
-            mul_f32x2(sb0, sb1, Db, Db, md.x, md.y);
+            mul_f32x2(sa0, sa1, Da, Da, mda.x, mda.y);
+            mul_f32x2(sb0, sb1, Db, Db, mda.x, mda.y);
             fma_f32x2(acc[nt][0], acc[nt][1], sa0, sa1, d[0], d[1]);
             fma_f32x2(acc[nt][2], acc[nt][3], sb0, sb1, d[2], d[3]);
             fma_f32x2(acc[nt][0], acc[nt][1], -Ma, -Ma, me.x, me.y);
@@ -770,8 +777,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int JB = a.jb;
     const int NIB = FMT == TCF_Q8_0   ? tc_q8_0_job_bytes(JB)
                     : FMT == TCF_Q6_K ? TC_Q6_K_NIB
-                    : FMT == TCF_Q4_K ? TC_Q4_K_JOB
-                    : FMT == TCF_Q5_K ? TC_Q5_K_JOB
+                    : FMT == TCF_Q4_K ? TC_Q4_K_JOB * (JB / 8)
+                    : FMT == TCF_Q5_K ? TC_Q5_K_JOB * (JB / 8)
                                       : tc_nib_bytes(JB);
     const int DSB = FMT == TCF_Q6_K ? TC_Q6_K_DS : FMT == TCF_Q4_0 ? tc_ds_bytes(JB) : 0;
     const int JPC = CHUNK / JB, JPC_LOG = JB > TC_LINE_JB ? 1 : 2;  // jobs per 32-block chunk
@@ -781,7 +788,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int J = ntile * jpt;
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
     const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB,
-                              FMT == TCF_Q6_K || FMT == TCF_Q4_K || FMT == TCF_Q5_K ? 128 : 64);
+                              tc_meta_bytes(FMT));
     uint8_t* nib = smem + sl.nib;
     uint8_t* ds = smem + sl.ds;
     uint8_t* act = smem + sl.act;
@@ -853,7 +860,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     bulk_g2s(dst + JB * 512, src + TC_Q8_0_CODES + hh * JB * 32, JB * 32, bar, pol);
                 }
             } else if constexpr (FMT == TCF_Q4_K || FMT == TCF_Q5_K) {
-                // the job's region of the pack: tile igrp / 4, superblock ikg
+                // the job's JB / 8 regions of the pack (adjacent): tile igrp / 4,
+                // superblocks ikg * JB / 8 ..
                 bulk_g2s(dst, a.w0 + ((int64_t)(igrp >> 2) * njb + ikg) * NIB, NIB, bar, pol);
             } else if constexpr (FMT == TCF_Q6_K) {
                 // superblock h of chunk c for the tile's 16 rows: ql, qh and sc
@@ -962,8 +970,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         ++consumed;
         if constexpr (FMT == TCF_Q8_0) tc_job_q8_0<M>(wnib + (size_t)slot * NIB, act, meta, kj * JB, JB, g, t, acc);
-        else if constexpr (FMT == TCF_Q4_K || FMT == TCF_Q5_K)
-            tc_job_q4_k<M, FMT == TCF_Q5_K>(wnib + (size_t)slot * NIB, act, meta, kj * JB, g, t, acc);
+        else if constexpr (FMT == TCF_Q4_K || FMT == TCF_Q5_K) {
+            constexpr int RB = FMT == TCF_Q5_K ? TC_Q5_K_JOB : TC_Q4_K_JOB;
+#pragma unroll 1
+            for (int r = 0; r < JB / 8; ++r)  // one superblock region at a time
+                tc_job_q4_k<M, FMT == TCF_Q5_K>(wnib + (size_t)slot * NIB + r * RB, act, meta, kj * JB + 8 * r, g, t,
+                                                acc);
+        }
         else if constexpr (FMT == TCF_Q6_K)
             tc_job_q6_k<M>(wnib + (size_t)slot * NIB, wds + (size_t)slot * DSB, act, meta, kj * JB,
                            (jb0 + kj) & (JPC - 1), g, t, acc);

@@ -89,8 +89,8 @@ int tc_max_clusters(int dev, int ci, size_t smem)
     return cache[dev][ci];
 }
 
-// The cheapest plan over job sizes JB (Q4_0: 16 or 8 blocks; Q8_0: 8 or 4;
-// Q6_K, Q4_K and Q5_K: 8)
+// The cheapest plan over job sizes JB (Q4_0: 16 or 8 blocks; Q4_K, Q5_K: the
+// same up to M = 8, then 8; Q8_0: 8 or 4; Q6_K: 8)
 // and cluster sizes C:
 // the largest per-CTA job count over 16 warps (the critical path) in units of
 // 8 blocks, where a 16-block Q4_0 job counts 0.85 x 2 units (measured: it
@@ -107,15 +107,22 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
     double best_cost = 0.0;
     bool found = false;
     // Q4_0: 16- then 8-block jobs; Q8_0: whole 8-block regions, then halves
-    const int jb_first = FMT == TCF_Q8_0 ? TC_Q8_0_JOB_BLOCKS : FMT == TCF_Q4_0 ? 2 * TC_LINE_JB : TC_LINE_JB;
+    // (Q4_K / Q5_K: 16-block jobs only up to M = 8, where they measured faster
+    // at every N; above it they traded ring depth for waves and measured
+    // slower about as often as faster)
+    const int jb_first = FMT == TCF_Q8_0                                       ? TC_Q8_0_JOB_BLOCKS
+                         : FMT == TCF_Q6_K                                     ? TC_LINE_JB
+                         : (FMT == TCF_Q4_K || FMT == TCF_Q5_K) && M > 8 ? TC_LINE_JB
+                                                                               : 2 * TC_LINE_JB;
     const int jb_last = FMT == TCF_Q8_0 ? TC_Q8_0_JOB_BLOCKS / 2 : TC_LINE_JB;
-    const int metab = FMT == TCF_Q6_K || FMT == TCF_Q4_K || FMT == TCF_Q5_K ? 128 : 64;
+    const int metab = tc_meta_bytes(FMT);
     for (int jb = jb_first; jb >= jb_last; jb /= 2) {
+        if (NB % jb) continue;  // whole jobs only
         const int njb = NB / jb;
         const int nibs = FMT == TCF_Q8_0   ? tc_q8_0_job_bytes(jb)
                          : FMT == TCF_Q6_K ? TC_Q6_K_NIB
-                         : FMT == TCF_Q4_K ? TC_Q4_K_JOB
-                         : FMT == TCF_Q5_K ? TC_Q5_K_JOB
+                         : FMT == TCF_Q4_K ? TC_Q4_K_JOB * (jb / 8)
+                         : FMT == TCF_Q5_K ? TC_Q5_K_JOB * (jb / 8)
                                            : tc_nib_bytes(jb);
         const int dsb = FMT == TCF_Q6_K ? TC_Q6_K_DS : FMT == TCF_Q4_0 ? tc_ds_bytes(jb) : 0;
         for (int ci = 0; ci < 4; ++ci) {

@@ -358,8 +358,9 @@ int qgemv_q8_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
  * in fp32; M = 1..17, K % 256 == 0, any N >= 1; arguments as qgemv_q4_0.
  * QGEMV_UNSUPPORTED_SHAPE also when no launch plan fits (very large M * K).
  *
- * qgemv_q4_k_plan - as qgemv_q8_0_plan (blocks per job: 8).  (Not from the
- * pages.) */
+ * qgemv_q4_k_plan - as qgemv_q8_0_plan (blocks per job: 16, two adjacent
+ * superblock regions in one copy, for M <= 8 where two stages of them fit
+ * and K/32 is a multiple of 16; else 8).  (Not from the pages.) */
 size_t q4_k_pack_bytes(int N, int K);
 int qpack_q4_k(const void* w_canon, void* w_pack, int N, int K, void* stream);
 int qgemv_q4_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream);

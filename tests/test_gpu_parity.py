@@ -479,7 +479,8 @@ def test_qpack_q4_k_layout(ops, N, K):
 
 
 Q4_K_SHAPES = [(M, K, N) for M in (1, 2, 5, 6, 8, 9, 12, 16, 17) for (K, N) in ((256, 1), (512, 37), (5120, 611))] + [
-    (6, 17408, 320), (2, 17408, 64), (6, 5120, 4096), (1, 8192, 16), (17, 17408, 64), (12, 5120, 17408)]
+    (6, 17408, 320), (2, 17408, 64), (6, 5120, 4096), (1, 8192, 16), (17, 17408, 64), (12, 5120, 17408),
+    (6, 768, 48), (13, 2304, 80)]
 
 
 @pytest.mark.parametrize("M,K,N", Q4_K_SHAPES)
@@ -531,7 +532,11 @@ def test_qgemv_q4_k_stride_errors_and_plans(ops):
     assert ops.qgemv_take_wait_timeouts() == 0
     for M2, K2, N2 in Q4_K_SHAPES + [(17, 5120, 248320), (6, 5120, 248320)]:
         pl = ops.qgemv_q4_k_plan(M2, K2, N2)
-        assert pl["tensor_cores"] and pl["stages"] >= 2 and pl["grid"] % pl["cluster"] == 0 and pl["job_blocks"] == 8
+        assert pl["tensor_cores"] and pl["stages"] >= 2 and pl["grid"] % pl["cluster"] == 0
+        assert pl["job_blocks"] in (8, 16) and (K2 // 32) % pl["job_blocks"] == 0  # whole jobs only
+    assert ops.qgemv_q4_k_plan(6, 5120, 17408)["job_blocks"] == 16  # two superblocks per copy
+    assert ops.qgemv_q4_k_plan(6, 768, 48)["job_blocks"] == 8  # 24 blocks: 8-block jobs
+    assert ops.qgemv_q4_k_plan(12, 5120, 17408)["job_blocks"] == 8  # M > 8: 8-block jobs
 
 
 # ---------------------------------------------------------------- Q5_K (tensor cores)
@@ -543,7 +548,7 @@ def test_qpack_q5_k_layout(ops, N, K):
 
 
 Q5_K_SHAPES = [(M, K, N) for M in (1, 5, 6, 9, 12, 17) for (K, N) in ((256, 1), (512, 37), (5120, 611))] + [
-    (6, 17408, 320), (17, 17408, 64), (6, 5120, 4096), (12, 5120, 17408)]
+    (6, 17408, 320), (17, 17408, 64), (6, 5120, 4096), (12, 5120, 17408), (6, 768, 48), (13, 2304, 80)]
 
 
 @pytest.mark.parametrize("M,K,N", Q5_K_SHAPES)
@@ -586,7 +591,8 @@ def test_qgemv_q5_k_errors_and_plans(ops):
     assert ops.qgemv_take_wait_timeouts() == 0
     for M2, K2, N2 in Q5_K_SHAPES + [(17, 5120, 248320), (6, 5120, 248320)]:
         pl = ops.qgemv_q5_k_plan(M2, K2, N2)
-        assert pl["tensor_cores"] and pl["stages"] >= 2 and pl["grid"] % pl["cluster"] == 0 and pl["job_blocks"] == 8
+        assert pl["tensor_cores"] and pl["stages"] >= 2 and pl["grid"] % pl["cluster"] == 0
+        assert pl["job_blocks"] in (8, 16) and (K2 // 32) % pl["job_blocks"] == 0
 
 
 def test_qgemv_q8_0_plans(ops):
