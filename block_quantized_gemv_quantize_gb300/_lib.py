@@ -371,10 +371,12 @@ def qgemv_block_dots_q6_k(w_pack: torch.Tensor, xq: torch.Tensor, M: int, K: int
     return out
 
 
-def set_q4_0_tensor_cores(enable: bool) -> bool:
-    """Run qgemv_q4_0 / qgemv_q4_0_pair on the tensor cores where the shape
-    allows (default) or always on the SIMT kernels; returns the previous setting."""
-    return bool(LIB.qgemv_set_q4_0_tensor_cores(1 if enable else 0))
+def set_q4_0_tensor_cores(mode) -> int:
+    """Kernel family of qgemv_q4_0 / qgemv_q4_0_pair: 1 or True (default) the
+    tensor cores where the shape allows (the small-M kernel for M <= 8), 2 the
+    general tensor-core kernel for every such M, 0 or False the SIMT kernels
+    only; returns the previous setting."""
+    return int(LIB.qgemv_set_q4_0_tensor_cores(int(mode)))
 
 
 def set_q6_k_tensor_cores(mode: int) -> int:
@@ -388,7 +390,8 @@ def qgemv_q4_0_plan(M: int, K: int, N: int, N_b: int = 0) -> dict:
     """The kernel qgemv_q4_0 (N_b = 0) or the pair call would launch."""
     info = (ctypes.c_int * 4)()
     _check("qgemv_q4_0_plan", LIB.qgemv_q4_0_plan(M, K, N, N_b, info))
-    return {"tensor_cores": bool(info[0]), "cluster": info[1], "grid": info[2], "stages": info[3]}
+    return {"tensor_cores": bool(info[0]), "kernel": {0: "simt", 1: "tc", 2: "tc_small_m"}[info[0]],
+            "cluster": info[1], "grid": info[2], "stages": info[3]}
 
 
 def qgemv_q6_k_plan(M: int, K: int, N: int) -> dict:

@@ -430,7 +430,7 @@ int qgemv_q8_0_plan(int M, int K, int N, int* info)
 int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;
-    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() +
+    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() + take_wait_timeouts_q4_0_mma() + take_wait_timeouts_q4_0_mma_pair() +
              take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_q6_k_tc() +
              take_wait_timeouts_lmhead() + take_wait_timeouts_q8_0() + take_wait_timeouts_q4_k() +
              take_wait_timeouts_q5_k();

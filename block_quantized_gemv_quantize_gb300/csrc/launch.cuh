@@ -207,7 +207,12 @@ int launch_mmvq_q4_0(const MmvqArgs& a, int M, cudaStream_t s);
 constexpr int TC_NOT_TAKEN = 1;
 // info (when not null): nothing is launched; the plan is written instead.
 int launch_mmvq_q4_0_tc(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int* info = nullptr);
-int set_q4_0_tensor_cores(int enable);
+int set_q4_0_tensor_cores(int mode);
+// The small-M tensor-core Q4_0 path (M <= 8, N % 16 == 0, K % 1024 == 0,
+// checked by the caller); TC_NOT_TAKEN when no launch plan fits.
+int launch_mmvq_q4_0_mma(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int* info = nullptr);
+unsigned int take_wait_timeouts_q4_0_mma();
+unsigned int take_wait_timeouts_q4_0_mma_pair();
 unsigned int take_wait_timeouts_q4_0_tc();
 // The tensor-core Q6_K path (M >= TC_Q6_K_MIN_M, N % 16 == 0, K % 1024 == 0);
 // TC_NOT_TAKEN otherwise.

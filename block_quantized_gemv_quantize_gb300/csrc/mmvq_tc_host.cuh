@@ -27,6 +27,47 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
+// Tensor maps of a packed Q4_0 weight whose groups and chunks are all whole
+// (N % 16 == 0, K % 1024 == 0): every group-chunk is 2304 B, codes
+// nib[4 rows][32 blocks][16 B] then scales d[32 blocks][4 rows].
+//   codes:  bytes of a row's chunk (512) x row (4) x chunk (nch) x group,
+//           box 128 B x 4 rows x 1 chunk x 4 groups = 16 rows x 8 blocks,
+//           128-byte swizzled (a job takes two);
+//   scales: bytes of the chunk's scales (256) x chunk x group, box jb * 8 B
+//           x 1 x 4 groups = a job's 16 rows x jb blocks.
+// tiles: 16-row tiles per box (the general kernel's boxes hold one; the
+// small-M kernel's may hold two).
+bool q4_0_tensor_maps(const void* w, int N, int K, int jb, CUtensorMap* nib, CUtensorMap* d, int tiles = 1)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const Layout L = make_layout(FMT_Q4_0, N, K);
+    const cuuint64_t gc = (cuuint64_t)L.chunk_bytes(GROUP, 0);  // 2304
+    const cuuint64_t gs = (cuuint64_t)L.nch * gc;
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)CHUNK * 16, GROUP, (cuuint64_t)L.nch, (cuuint64_t)L.n_groups};
+        const cuuint64_t strides[3] = {(cuuint64_t)CHUNK * 16, gc, gs};
+        const cuuint32_t box[4] = {TC_LINE_JB * 16, GROUP, 1, (cuuint32_t)(tiles * TC_ROWS / GROUP)};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(w), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)CHUNK * GROUP * 2, (cuuint64_t)L.nch, (cuuint64_t)L.n_groups};
+        const cuuint64_t strides[2] = {gc, gs};
+        const cuuint32_t box[3] = {(cuuint32_t)jb * GROUP * 2, 1, (cuuint32_t)(tiles * TC_ROWS / GROUP)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        void* base = static_cast<uint8_t*>(const_cast<void*>(w)) + (size_t)GROUP * CHUNK * 16;
+        if (enc(d, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
 struct TcPlan {
     int C, grid, S, jb, nkb_max, out_tiles;
     size_t smem;
