@@ -115,7 +115,7 @@ const QmDevice& qm_device(const DeviceInfo& di, int dev)
 
 // The cheapest plan over job shapes and cluster sizes (1, 2, 4, 8): the
 // critical warp's jobs times a job's cost in 16-row x 8-block units (a
-// two-tile job costs 1.7 of them: it shares the activation loads; a 16-block
+// two-tile job costs 1.6 of them: it shares the activation loads; a 16-block
 // job 1.9: it halves the per-job copy and loop overhead), plus two units for
 // the cross-CTA combine when C > 1.  A plan needs at least two ring stages
 // next to the activation and the cluster's combine area, and at most
@@ -147,7 +147,7 @@ bool qm_plan(const DeviceInfo& di, const QmDevice& qd, int K, int N, int N2, QmP
             for (int s = QM_MAX_STAGES; s >= 2 && S == 0; --s)
                 if (qm_smem(M, s, jb, TL, nkb, out_units).bytes <= (uint32_t)di.smem_optin) S = s;
             if (S == 0) continue;
-            const double unit = TL == 2 ? 1.7 : jb == 16 ? 1.9 : 1.0;
+            const double unit = TL == 2 ? 1.6 : jb == 16 ? 1.9 : 1.0;
             const double cost =
                 (double)(((int64_t)units * jpt + QM_WARPS - 1) / QM_WARPS) * unit + (C > 1 ? 2.0 : 0.0);
             if (!found || cost < best_cost - 1e-9) {
