@@ -123,14 +123,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 20):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -160,8 +161,10 @@ class ClockSampler:
             for nm, v in zip(names, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_min_mhz": min(sm) if sm else None,
+                "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm), "interval_ms": self.interval_ms,
+                "window": "the whole GPU part of the native run (warm-up, timed steps, per-call, e2e, A/B and chain "
+                          "measurements)"}
 
 
 # ---------------------------------------------------------------- ranks
@@ -199,10 +202,13 @@ def run_native(args, rank, world):
     build.build()
     from block_quantized_gemv_quantize_gb300 import ops
 
+    from block_quantized_gemv_quantize_gb300 import synth
+
     local = int(os.environ.get("LOCAL_RANK", 0))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = make_inputs()
+    c_sweep_seed = synth.WORKLOADS["lmhead_q6_k"]["seed"] + 300
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -257,21 +263,24 @@ def run_native(args, rank, world):
         if world > 1:
             dist.barrier()
 
+    # clocks are sampled over the whole GPU part of the run (the timed region
+    # alone can be a few milliseconds, shorter than nvidia-smi's interval)
+    clk = ClockSampler(dev.index if dev.index is not None else 0)
+    clk.__enter__()
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
 
-    # timed region: K steps bracketed by two events, clocks sampled meanwhile
+    # timed region: K steps bracketed by two events
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        t0.record(stream)
-        for _ in range(args.steps):
-            step()
-        t1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     ms_per_step = total_ms / args.steps
 
@@ -384,6 +393,76 @@ def run_native(args, rank, world):
     same_ids = ids_d.cpu().tolist() == ids_u.cpu().tolist()
     same_ids_t = ids_tf.cpu().tolist() == ids_t.cpu().tolist()
 
+    # Fused against unfused LM-head over the M sweep (BASELINE config 3's
+    # control): for each M, rows 0..M-1 of a [17, 5120] activation, the
+    # fused top-1 against quantize + qgemv_q6_k + argmax_f32_rows on the same
+    # inputs, interleaved rounds of 10 calls each.
+    xs = up(synth.activations(17, K_H, seed=c_sweep_seed))
+    ys = torch.empty((17, N_V), device=dev)
+    xqs = torch.empty(ops.q8_1_bytes(17, K_H), dtype=torch.uint8, device=dev)
+    ws17 = torch.zeros(ops.lmhead_q6_k_top1_workspace_bytes(17, K_H, N_V), dtype=torch.uint8, device=dev)
+    m_sweep = {}
+    for Ms in (1, 2, 4, 6, 9, 12, 17):
+        xm = xs[:Ms]
+        idf = torch.empty(Ms, dtype=torch.int32, device=dev)
+        idu = torch.empty(Ms, dtype=torch.int32, device=dev)
+        fm = (lambda xm=xm, idf=idf: ops.lmhead_q6_k_top1(w["w_vocab"], xm, K_H, N_V, ids=idf, ws=ws17))
+
+        def um(xm=xm, idu=idu, Ms=Ms):
+            ops.quantize_q8_1(xm, out=xqs[: ops.q8_1_bytes(Ms, K_H)])
+            ops.qgemv_q6_k(w["w_vocab"], xqs[: ops.q8_1_bytes(Ms, K_H)], Ms, K_H, N_V, y=ys[:Ms])
+            ops.argmax_f32_rows(ys[:Ms], ids=idu, ws=ws2)
+
+        tf, tu = [], []
+        for _ in range(8):
+            for lst, fn in ((tf, fm), (tu, um)):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(10):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                lst.append(a.elapsed_time(b) * 1e3 / 10)
+        diff = [u_ - f_ for f_, u_ in zip(tf, tu)]
+        m_sweep[str(Ms)] = {"fused_us": round(statistics.median(tf), 2), "unfused_us": round(statistics.median(tu), 2),
+                            "diff_median_us": round(statistics.median(diff), 2), "diff_min_us": round(min(diff), 2),
+                            "diff_max_us": round(max(diff), 2),
+                            "same_ids": idf.cpu().tolist() == idu.cpu().tolist()}
+    del ys, xqs
+
+    # The verifier MLP projections as a layer stack runs them: the gate/up
+    # pair and the down projection of L layers with distinct weights (so no
+    # call finds its weights in L2), back to back on the stream, the
+    # activations quantized once beforehand; events around the whole chain.
+    L_LAYERS = 4
+    lw = [(w["w_gate"], w["w_up"], w["w_down"])]
+    for i in range(1, L_LAYERS):
+        g_ = torch.randint(0, 256, (w["w_gate"].numel(),), dtype=torch.uint8, device=dev)
+        u_ = torch.randint(0, 256, (w["w_up"].numel(),), dtype=torch.uint8, device=dev)
+        d_ = torch.randint(0, 256, (w["w_down"].numel(),), dtype=torch.uint8, device=dev)
+        lw.append((g_, u_, d_))
+    ops.quantize_q8_1(x, out=xq1)
+    ops.quantize_q8_1(h, out=xq2)
+
+    def mlp_chain():
+        for wg_, wu_, wd_ in lw:
+            ops.qgemv_q4_0_pair(wg_, wu_, xq1, M_T, K_H, N_FF, N_FF, y_a=y_gate, y_b=y_up)
+            ops.qgemv_q4_0(wd_, xq2, M_T, N_FF, K_H, y=y_down)
+
+    for _ in range(3):
+        mlp_chain()
+    torch.cuda.synchronize()
+    chain_rounds = 25
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(chain_rounds):
+        mlp_chain()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    chain_us_layer = c0.elapsed_time(c1) * 1e3 / (chain_rounds * L_LAYERS)
+    del lw
+    clk.__exit__(None, None, None)
+
     def ab_pair(a_name, b_name, keys, extra):
         """Medians of two interleaved arms, and the median, p10 and p90 of
         their per-round difference (b - a, us)."""
@@ -400,7 +479,9 @@ def run_native(args, rank, world):
     achieved = nbytes[dominant] / (call_ms[dominant] * 1e-3) / 1e9
     traffic = load_traffic(dominant)
     mmvq_names = ("gate_up", "down")
-    mmvq_gbs = sum(nbytes[n] for n in mmvq_names) / (sum(call_ms[n] for n in mmvq_names) * 1e-3) / 1e9
+    mmvq_bytes = sum(nbytes[n] for n in mmvq_names)
+    mmvq_lone_gbs = mmvq_bytes / (sum(call_ms[n] for n in mmvq_names) * 1e-3) / 1e9
+    mmvq_gbs = mmvq_bytes / (chain_us_layer * 1e-6) / 1e9
 
     result = None
     if rank == 0:
@@ -423,13 +504,21 @@ def run_native(args, rank, world):
                        "l2": "inputs larger than L2: ~2.2 GB of weights streamed per step, no flush needed",
                        "replicas": world},
             "mmvq_m6_q4_0": {"gbs": round(mmvq_gbs, 1), "frac_of_hbm_peak": round(mmvq_gbs / peak, 4),
-                             "us": {n: round(call_ms[n] * 1e3, 2) for n in mmvq_names}},
+                             "timing": f"back-to-back chain of the gate/up pair and the down projection of "
+                                       f"{L_LAYERS} layers with distinct weights, {chain_rounds} rounds, events "
+                                       "around the chain",
+                             "us_per_layer": round(chain_us_layer, 2), "bytes_per_layer": mmvq_bytes,
+                             "lone_call": {"gbs": round(mmvq_lone_gbs, 1),
+                                           "frac_of_hbm_peak": round(mmvq_lone_gbs / peak, 4),
+                                           "us": {n: round(call_ms[n] * 1e3, 2) for n in mmvq_names},
+                                           "timing": "an event pair around each call inside the step"}},
             "lmhead_top1_us": round(call_ms["lmhead_top1"] * 1e3, 2),
             "fused_vs_unfused_us": ab_pair("fused", "unfused", ("fused", "unfused"), {"same_ids": same_ids}),
             "candmax_us": round(statistics.median(ab["candmax"]), 2),
             "rmsnorm_q8_1_vs_quantize_us": ab_pair("q8_only", "rms_q8", ("quantize_q8_1", "rmsnorm_q8_1"), {}),
             "target_m6_fused_vs_unfused_us": ab_pair("target_fused", "target_unfused", ("fused", "unfused"),
                                                      {"same_ids": same_ids_t}),
+            "fused_vs_unfused_m_sweep_us": m_sweep,
             "per_call_us": {n: round(call_ms[n] * 1e3, 2) for n in names},
             "per_call_us_spread": call_spread,
             "per_call_gbs": {n: round(nbytes[n] / (call_ms[n] * 1e-3) / 1e9, 1) for n in names},
@@ -565,6 +654,31 @@ def oracle_sample_step(inp, frac: float, nthreads: int):
     return time.perf_counter() - t, nbytes
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), with the
+    architecture."""
+    import platform
+
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                name = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not name:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith("model name"):
+                    name = ln.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return f"{name or 'unknown'} ({platform.machine()})"
+
+
 def calibrate_fraction(inp, seconds: float, nthreads: int) -> float:
     dt, _ = oracle_sample_step(inp, 0.002, nthreads)
     return min(1.0, max(0.0005, 0.002 * seconds / max(dt, 1e-3)))
@@ -588,6 +702,7 @@ def cpu_baseline(inp, seconds: float):
     frac1 = calibrate_fraction(inp, seconds / 4, 1)
     t1, b1 = oracle_sample_step(inp, frac1, 1)
     return {"value": round(total_b / total_t / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{reps} oracle step(s) over the first {frac:.2%} of the rows of every weight "
                       f"({total_t:.1f} s, {total_b / 1e6:.0f} MB)",
             "single_core": {"value": round(b1 / t1 / 1e9, 4), "unit": UNIT, "cores": 1,
@@ -617,7 +732,8 @@ def run_reference(args):
         "dtype": "int32 block dots, fp64 accumulate (CPU oracle)",
         "data": "synthetic (seeded; same inputs as the native arm)",
         "config": {"workload": WORKLOAD, "sampled": sample},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -48,9 +48,10 @@ struct QmSmem {
 
 // Shared-memory layout, identical on the host (sizing) and the device: ring
 // stages of codes (1024-byte aligned: 128-byte swizzle atoms), of scales, the
-// activation's B fragments [block][row][lane t] x 16 B, its meta [block][lane
-// t] x {d_a, d_a', C, C'}, the cluster combine area, the cut-tile table and
-// the ring barriers.
+// activation's B fragments [block][row][lane t] x 16 B, its meta per block
+// ([lane t] x {C, C', C, C'}, the accumulator start as a ready register quad,
+// then [lane t] x {d_a, d_a'}), the cluster combine area, the cut-unit table
+// and the ring barriers.
 // TL: 16-row tiles per unit (a job is TL tiles x JB blocks); out_units:
 // the units of the cluster combine area.
 __host__ __device__ inline QmSmem qm_smem(int M, int S, int JB, int TL, int nkb, int out_units)
@@ -60,7 +61,7 @@ __host__ __device__ inline QmSmem qm_smem(int M, int S, int JB, int TL, int nkb,
     s.nib = o;  o += (uint32_t)QM_WARPS * S * TL * JB * 256;
     s.ds = o;   o += (uint32_t)QM_WARPS * S * TL * JB * 32;
     s.act = o;  o += (uint32_t)nkb * M * 64;
-    s.meta = o; o += (uint32_t)nkb * 64;
+    s.meta = o; o += (uint32_t)nkb * 96;
     s.out = o;  o += (uint32_t)out_units * TL * QM_VT * 4;
     s.tab = o;  o += TC_TAB_INTS * 4;
     s.bar = o;  o += (uint32_t)(QM_WARPS * S + 1) * 8;  // ring barriers, then the activation's
@@ -114,7 +115,8 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t a)
 // one 8-row tile), one (block b, row n) unit per thread and round.
 //   record (b, n, lane t): f16x2 (q[4t], q[4t+2]), (q[4t+1], q[4t+3]),
 //                          (q[16+4t], q[16+4t+2]) / 16, (q[16+4t+1], q[16+4t+3]) / 16
-//   meta (b, lane t): {d_a[2t], d_a[2t+1], C[2t], C[2t+1]}, zero for rows >= M.
+//   meta (b): [lane t] {C[2t], C[2t+1], C[2t], C[2t+1]} (64 B), then [lane t]
+//             {d_a[2t], d_a[2t+1]} (32 B); zero for rows >= M.
 // Units are numbered n fastest, so a warp's 16-byte stores land on 32
 // consecutive 64-byte records; unit u writes its four 16-byte pieces in the
 // order (k + u / 2) mod 4, which puts the eight stores of each quarter-warp
@@ -169,18 +171,21 @@ __device__ __forceinline__ void qm_stage_store(const uint32_t (&w)[QM_UNITS][9],
             sts_v4(rec + k * 16, v);
         }
         const float da = __half2float(__ushort_as_half((unsigned short)(w[u][0] & 0xFFFFu)));
-        const uint32_t mp = meta + (uint32_t)b * 64 + (n >> 1) * 16 + (n & 1) * 4;
-        sts_u32(mp, __float_as_uint(da));
-        sts_u32(mp + 8, __float_as_uint((float)(-1032 * s_lo - 72 * s_hi)));
+        const uint32_t mp = meta + (uint32_t)b * 96 + (n >> 1) * 16 + (n & 1) * 4;
+        const uint32_t cv = __float_as_uint((float)(-1032 * s_lo - 72 * s_hi));
+        sts_u32(mp, cv);
+        sts_u32(mp + 8, cv);
+        sts_u32(meta + (uint32_t)b * 96 + 64 + (n >> 1) * 8 + (n & 1) * 4, __float_as_uint(da));
     }
     if constexpr (M < 8) {
         // rows M .. 7 of every block: zero scale and start
         constexpr int PAD = 8 - M;
         for (int i = threadIdx.x; i < nkb * PAD; i += QM_THREADS) {
             const int b = i / PAD, n = M + (i - b * PAD);
-            const uint32_t mp = meta + (uint32_t)b * 64 + (n >> 1) * 16 + (n & 1) * 4;
+            const uint32_t mp = meta + (uint32_t)b * 96 + (n >> 1) * 16 + (n & 1) * 4;
             sts_u32(mp, 0u);
             sts_u32(mp + 8, 0u);
+            sts_u32(meta + (uint32_t)b * 96 + 64 + (n >> 1) * 8 + (n & 1) * 4, 0u);
         }
     }
 }
@@ -196,7 +201,8 @@ __device__ __forceinline__ void qm_stage_store(const uint32_t (&w)[QM_UNITS][9],
 //   sd: the lane's scale of row g for block 0 of tile 0: [4 TL groups][JB
 //       blocks][4 rows] fp16; row g + 8 two groups on, tile u 4u groups on;
 //   bA: the B fragment (lane t) of block 0 of the job, row min(g, M - 1);
-//   bM: the meta (lane t) of block 0 of the job.
+//   bM: the accumulator-start quad (lane t) of block 0 of the job; its d_a
+//       pair is 64 - 8t bytes on.
 // acc[u] (tile u: rows g, g, g + 8, g + 8; columns 2t, 2t + 1, 2t, 2t + 1)
 // += the job's sum.  The activation fragment and meta of a block are loaded
 // once for the TL tiles.
@@ -204,6 +210,7 @@ __device__ __forceinline__ void qm_stage_store(const uint32_t (&w)[QM_UNITS][9],
 template <int M, int JB, int TL>
 __device__ __forceinline__ void qm_job(uint32_t sn, uint32_t sd, uint32_t bA, uint32_t bM, float (&acc)[TL][4])
 {
+    const uint32_t bD = bM + 64 - (threadIdx.x & 3) * 8;  // the lane's d_a pairs
     float j[TL][4];
 #pragma unroll
     for (int u = 0; u < TL; ++u)
@@ -219,9 +226,10 @@ __device__ __forceinline__ void qm_job(uint32_t sn, uint32_t sd, uint32_t bA, ui
         for (int q = 0; q < 2; ++q) {
             const int pb = p + q;
             const uint4 B = lds_v4(bA + pb * M * 64);
-            const uint4 md = lds_v4(bM + pb * 64);
-            const float da0 = __uint_as_float(md.x), da1 = __uint_as_float(md.y);
-            const float c0 = __uint_as_float(md.z), c1 = __uint_as_float(md.w);
+            const uint4 cq = lds_v4(bM + pb * 96);
+            uint2 dd;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(dd.x), "=r"(dd.y) : "r"(bD + pb * 96));
+            const float da0 = __uint_as_float(dd.x), da1 = __uint_as_float(dd.y);
 #pragma unroll
             for (int u = 0; u < TL; ++u) {
                 const uint32_t wa = cw[u][2 * q], wb = cw[u][2 * q + 1];
@@ -233,7 +241,8 @@ __device__ __forceinline__ void qm_job(uint32_t sn, uint32_t sd, uint32_t bA, ui
                 const float dwa = lds_f16(sd + u * (4 * JB * 8) + pb * 8);
                 const float dwb = lds_f16(sd + u * (4 * JB * 8) + 2 * JB * 8 + pb * 8);
                 float d[4];
-                mma_f16_16816(d, A0, B.x, B.y, c0, c1, c0, c1);
+                mma_f16_16816(d, A0, B.x, B.y, __uint_as_float(cq.x), __uint_as_float(cq.y), __uint_as_float(cq.z),
+                              __uint_as_float(cq.w));
                 mma_f16_16816(d, A1, B.z, B.w, d[0], d[1], d[2], d[3]);
                 // j += (d_w d_a) I, the exact fp16 x fp16 product first
                 float sa0, sa1, sb0, sb1;
@@ -457,7 +466,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
         }
         ++consumed;
         qm_job<M, JB, TL>(wnib + (uint32_t)slot * NIB + ld_off, wds + (uint32_t)slot * DSB + sc_off,
-                          bA0 + (uint32_t)kj * (JB * M * 64), bM0 + (uint32_t)kj * (JB * 64), acc);
+                          bA0 + (uint32_t)kj * (JB * M * 64), bM0 + (uint32_t)kj * (JB * 96), acc);
         __syncwarp();
         if (issued < n_jobs) issue();  // into the stage just read
         if (++slot == S) {
