@@ -94,14 +94,22 @@ int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* str
  * x normalized by their RMS and scaled by gamma, written as Q8_1 without an
  * fp32 copy.  [closure] "Qwen3.6 27B Q4_0 DFlash/SYCL closure", What did not
  * clear the gate: the down-to-next-RMSNorm/Q8 boundary (RMSNorm fused with
- * the Q8 quantization).  Exact contract (all fp32, round to nearest, no
- * fused multiply-add), per row:
+ * the Q8 quantization).  What is computed, per row: RMSNorm(x) * gamma,
+ * xh_k = x_k * r * gamma_k with r = 1 / sqrt(sum_k x_k^2 / K + eps), then the
+ * Q8_1 quantizer of quantize_q8_1 applied to xh.  xh is computed in fp32 in
+ * a fixed order (all fp32, round to nearest, no fused multiply-add):
  *   s_t = sum over k = t, t + 512, ... < K, in increasing k, of x_k * x_k
  *         (t = 0..511, each added as s_t = s_t + (x_k * x_k));
  *   for h = 256, 128, ..., 1: s_t = s_t + s_{t+h} for t < h;   S = s_0;
  *   r = 1 / sqrt(S / K + eps);   xh_k = (x_k * r) * gamma_k;
- * then xq = quantize_q8_1(xh), bit for bit.  (The reduction order is part of
- * the definition so that the Q8_1 codes are reproducible.)
+ * so the output is deterministic (the same bytes on every call).  Against the
+ * exact RMSNorm rounded to fp32 and quantized, with e = (K / 512 + 16) 2^-24,
+ * the codes agree except where the exact xh_k / d lies within 508 e of a
+ * half-integer (there the code may differ by one), and the fp16 scale agrees
+ * except where d lies within a relative 4 e of a rounding midpoint between two
+ * fp16 values (there it may be the neighbouring one): the fp32 sum of squares
+ * is within a relative (K / 512 + 9) 2^-24 of the exact one, and a few more
+ * roundings follow.
  *   x      fp32 [M][ldx] device, ldx >= K      (read)
  *   gamma  fp32 [K] device                      (read)
  *   eps    finite, >= 0
@@ -261,7 +269,10 @@ int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, 
  *   QGEMV_UNSUPPORTED_SHAPE before anything is enqueued.
  *   The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.  Each call clears the scratch on `stream`
+ *   before any stream capture.  The address is kept for the life of the
+ *   process: after cudaDeviceReset (or any teardown of the device's primary
+ *   context) it is stale, so do not call this entry point on that device
+ *   again in the same process.  Each call clears the scratch on `stream`
  *   before its kernel.  All calls on a device share the one array: calls
  *   that overlap on the GPU (other streams, other host threads) race and may
  *   return wrong ids; serialize them. */
@@ -295,6 +306,14 @@ int qgemv_set_q4_0_tensor_cores(int enable);
  * size, ring stages per warp}, zeros for the SIMT kernels.  Enqueues
  * nothing; may query the current device.  (Not from the pages.) */
 int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info);
+
+/* lmhead_q6_k_top1_plan - the kernel lmhead_q6_k_top1 (and its candidate-max
+ * and no-allocation forms) would launch for this shape: info[4] = {1 for the
+ * ring kernel (the activation tile fits in shared memory), 0 for the
+ * lock-step kernel (K is staged in chunks), grid size, warps per CTA, ring
+ * stages per warp (0 for the lock-step kernel)}.  Enqueues nothing; may query
+ * the current device.  (Not from the pages.) */
+int lmhead_q6_k_top1_plan(int M, int K, int N, int* info);
 
 /* qgemv_set_q6_k_tensor_cores - the kernel family of qgemv_q6_k.  The
  * tensor-core kernel takes shapes with M >= 7, N a multiple of 16 and K a

@@ -53,7 +53,7 @@ def _load():
             lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_to_f64.restype = ctypes.c_double
             lib.oracle_quantize_q8_1.argtypes = [P, L, I, I, P]
-            lib.oracle_rmsnorm_quantize_q8_1.argtypes = [P, L, P, ctypes.c_float, I, I, P]
+            lib.oracle_rmsnorm_quantize_q8_1.argtypes = [P, L, P, ctypes.c_float, I, I, P, P]
             for name in ("oracle_dequant_q4_0", "oracle_dequant_q6_k", "oracle_dequant_q8_1", "oracle_dequant_q8_0",
                          "oracle_dequant_q4_k", "oracle_dequant_q5_k"):
                 getattr(lib, name).argtypes = [P, I, I, P]
@@ -111,18 +111,21 @@ def quantize_q8_1(x: np.ndarray, K: int | None = None) -> np.ndarray:
     return out
 
 
-def rmsnorm_quantize_q8_1(x: np.ndarray, gamma: np.ndarray, eps: float, K: int | None = None) -> np.ndarray:
-    """Q8_1 of RMSNorm(x) * gamma under the library's exact contract (fp32
-    sum of squares over 512 strided slices, pairwise slice tree, r = 1 /
-    sqrt(S / K + eps), xh = (x * r) * gamma): uint8 [M, K/32, 36]."""
+def rmsnorm_quantize_q8_1(x: np.ndarray, gamma: np.ndarray, eps: float, K: int | None = None,
+                          with_xh: bool = False):
+    """Q8_1 of RMSNorm(x) * gamma by the plain definition (fp64 sum of squares
+    in increasing k, r = 1 / sqrt(S / K + eps), xh = (x r) gamma in fp64, then
+    xh rounded to fp32 and quantized): uint8 [M, K/32, 36]; with_xh: also the
+    fp64 xh [M, K]."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     M, ldx = x.shape
     K = ldx if K is None else K
     g = np.ascontiguousarray(gamma, dtype=np.float32)
     assert K % 32 == 0 and K <= ldx and g.shape[0] >= K
     out = np.zeros((M, K // 32, 36), dtype=np.uint8)
-    _load().oracle_rmsnorm_quantize_q8_1(_ptr(x), ldx, _ptr(g), ctypes.c_float(eps), M, K, _ptr(out))
-    return out
+    xh = np.zeros((M, K), dtype=np.float64)
+    _load().oracle_rmsnorm_quantize_q8_1(_ptr(x), ldx, _ptr(g), ctypes.c_float(eps), M, K, _ptr(out), _ptr(xh))
+    return (out, xh) if with_xh else out
 
 
 def qgemv_q4_0(w: np.ndarray, xq: np.ndarray, nthreads: int | None = None):

@@ -32,6 +32,9 @@
  *     Q5_K = the same with 5-bit q.
  *   - Top-1 with the lowest-token-ID finite-tie rule: same page, "Exactness and
  *     safety contracts", item 3.
+ *   - RMSNorm fused with the Q8_1 quantizer ("Qwen3.6 27B Q4_0 DFlash/SYCL
+ *     closure", What did not clear the gate): the plain definition in fp64,
+ *     then the quantizer on the fp32 rounding of the normalized row.
  *
  * The dot products are the plain definition of the result: every Q8_1 block
  * dot is an exact integer sum, scaled by the two fp16 scales in fp64 and
@@ -158,37 +161,28 @@ void oracle_quantize_q8_1(const float* x, int64_t ldx, int M, int K, uint8_t* ou
     }
 }
 
-/* RMSNorm fused with the Q8_1 quantizer, the contract of the library's
- * rmsnorm_quantize_q8_1 ("Qwen3.6 27B Q4_0 DFlash/SYCL closure", What did not
- * clear the gate: the down-to-next-RMSNorm/Q8 boundary), step by step in fp32
- * (this file is compiled without contraction): the sum of squares over 512
- * strided slices in increasing k, the slices added pairwise (h = 256 .. 1),
- * r = 1 / sqrt(S / K + eps), xh_k = (x_k * r) * gamma_k, then the Q8_1
- * quantization of xh above. */
+/* RMSNorm fused with the Q8_1 quantizer ("Qwen3.6 27B Q4_0 DFlash/SYCL
+ * closure", What did not clear the gate: the down-to-next-RMSNorm/Q8
+ * boundary; the pages name the fusion, not its arithmetic).  The plain
+ * definition, per row, in fp64: S = sum_k x_k^2 (in increasing k),
+ * r = 1 / sqrt(S / K + eps), xh_k = (x_k r) gamma_k; then xh rounded to
+ * fp32 and quantized by oracle_quantize_q8_1 (the quantizer's fp32
+ * definition decides the codes).  xh_out (may be NULL) receives the fp64
+ * xh, [M][K], for the checks that need the exact value. */
 void oracle_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, int M, int K,
-                                  uint8_t* out)
+                                  uint8_t* out, double* xh_out)
 {
-    enum { T = 512 };
-    float part[T];
     float* xh = (float*)malloc(sizeof(float) * (size_t)K);
     if (!xh) return;
     for (int m = 0; m < M; ++m) {
         const float* xr = x + (int64_t)m * ldx;
-        for (int t = 0; t < T; ++t) {
-            float s = 0.0f;
-            for (int k = t; k < K; k += T) {
-                const float sq = xr[k] * xr[k];
-                s = s + sq;
-            }
-            part[t] = s;
-        }
-        for (int h = T / 2; h > 0; h >>= 1)
-            for (int t = 0; t < h; ++t) part[t] = part[t] + part[t + h];
-        const float mean = part[0] / (float)K;
-        const float r = 1.0f / sqrtf(mean + eps);
+        double S = 0.0;
+        for (int k = 0; k < K; ++k) S += (double)xr[k] * (double)xr[k];
+        const double r = 1.0 / sqrt(S / (double)K + (double)eps);
         for (int k = 0; k < K; ++k) {
-            const float a = xr[k] * r;
-            xh[k] = a * gamma[k];
+            const double v = ((double)xr[k] * r) * (double)gamma[k];
+            if (xh_out) xh_out[(int64_t)m * K + k] = v;
+            xh[k] = (float)v;
         }
         oracle_quantize_q8_1(xh, K, 1, K, out + (int64_t)m * (K / 32) * Q8_1_BYTES);
     }

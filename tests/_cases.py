@@ -278,3 +278,52 @@ def winner_q6_k_row(x_rows: np.ndarray) -> np.ndarray:
     sc = np.full((1, K // 16), 63, dtype=np.int8)
     d = np.array([[1e-3] * (K // 256)], dtype=np.float32).astype(np.float16).view(np.uint16)
     return q6_k_from_codes(codes, sc, d)[0]
+
+
+def rmsnorm_q8_1_bounds(K: int):
+    """The stated bounds of rmsnorm_quantize_q8_1 against the exact RMSNorm
+    (include/qgemv.h): a code may differ by one where the exact x / d lies
+    within `delta` of a half-integer, the fp16 scale may be the neighbouring
+    one where d lies within a relative `drel` of a rounding midpoint.  Both
+    follow from the fp32 sum of squares' relative error, (K / 512 + 9) 2^-24,
+    plus the few roundings after it, with a margin of four."""
+    e = (K / 512 + 16) * 2.0 ** -24
+    return 4 * 127 * e, 4 * e
+
+
+def check_q8_1_near(got: np.ndarray, ref: np.ndarray, xh: np.ndarray, K: int) -> dict:
+    """Compare Q8_1 bytes (uint8 [M, K/32, 36]) from the GPU against the
+    oracle's plain-definition bytes, allowing the near-boundary differences of
+    rmsnorm_q8_1_bounds; returns counts and 'ok'."""
+    delta, drel = rmsnorm_q8_1_bounds(K)
+    M, NB = ref.shape[0], ref.shape[1]
+    got = got.reshape(M, NB, 36)
+    dg = got[:, :, 0:2].copy().view(np.float16)[:, :, 0]
+    dr = ref[:, :, 0:2].copy().view(np.float16)[:, :, 0]
+    sg = got[:, :, 2:4].copy().view(np.float16)[:, :, 0].astype(np.float64)
+    qg = got[:, :, 4:].copy().view(np.int8).astype(np.int64)
+    qr = ref[:, :, 4:].copy().view(np.int8).astype(np.int64)
+    x32 = xh.astype(np.float32).reshape(M, NB, 32)
+    d32 = (np.max(np.abs(x32), axis=2) / np.float32(127.0)).astype(np.float32)
+    # codes: exact, or one apart where the exact xh / d is near a half-integer
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.abs(xh.reshape(M, NB, 32) / d32.astype(np.float64)[:, :, None])
+    frac = t - np.floor(t)
+    near_q = np.isfinite(t) & (np.abs(frac - 0.5) < delta)
+    dq = np.abs(qg - qr)
+    codes_ok = (dq == 0) | (near_q & (dq == 1))
+    # scales: exact, or the neighbouring fp16 value where d is near a midpoint
+    lo = dr.astype(np.float64) - np.spacing(dr).astype(np.float64) / 2
+    hi = dr.astype(np.float64) + np.spacing(dr).astype(np.float64) / 2
+    d64 = d32.astype(np.float64)
+    near_d = (np.abs(d64 - lo) <= drel * d64) | (np.abs(d64 - hi) <= drel * d64)
+    dd = np.abs(dg.view(np.int16).astype(np.int64) - dr.view(np.int16).astype(np.int64))
+    d_ok = (dd == 0) | (near_d & (dd == 1))
+    # s: the fp16 of d * sum(q) for the GPU's own codes, within one fp16 step
+    s_ref = (d32.astype(np.float64) * qg.sum(axis=2)).astype(np.float32).astype(np.float16).astype(np.float64)
+    s_ok = np.abs(sg - s_ref) <= np.spacing(np.abs(s_ref).astype(np.float16)).astype(np.float64) * 1.001
+    return {"ok": bool(codes_ok.all() and d_ok.all() and s_ok.all()), "codes_off_by_one": int((dq == 1).sum()),
+            "near_half_integer": int(near_q.sum()), "scales_off_by_one": int((dd == 1).sum()),
+            "near_fp16_midpoint": int(near_d.sum()), "bad_codes": int((~codes_ok).sum()),
+            "bad_scales": int((~d_ok).sum()), "bad_sums": int((~s_ok).sum()),
+            "blocks": int(M * NB), "values": int(M * NB * 32), "delta": delta, "drel": drel}

@@ -404,14 +404,22 @@ def test_qgemv_q4_0_residual_errors(ops):
 
 
 @pytest.mark.parametrize("M,K,ldx,eps", [(1, 32, 32, 1e-6), (6, 5120, 5120, 1e-5), (6, 17408, 17416, 1e-6),
-                                         (17, 1024, 1024, 0.0), (3, 96, 100, 1e-3)])
-def test_rmsnorm_quantize_q8_1_bit_exact(ops, M, K, ldx, eps):
+                                         (17, 1024, 1024, 0.0), (3, 96, 100, 1e-3), (17, 5120, 5120, 1e-6)])
+def test_rmsnorm_quantize_q8_1_matches_plain_definition(ops, M, K, ldx, eps):
+    """Against the oracle's plain definition (fp64 RMSNorm, then the fp32
+    quantizer): codes and scales equal except at the stated boundaries, where
+    they may be one apart; the counts are printed.  Two calls give the same
+    bytes (the kernel's fixed reduction order)."""
     g = np.random.default_rng(M * 7 + K)
     x = (g.standard_normal((M, ldx)) * g.uniform(0.1, 10.0, (M, 1))).astype(np.float32)
     gamma = g.uniform(-2.0, 2.0, K).astype(np.float32)
-    ref = oracle.rmsnorm_quantize_q8_1(x, gamma, eps, K=K)
+    ref, xh = oracle.rmsnorm_quantize_q8_1(x, gamma, eps, K=K, with_xh=True)
     got = _np(ops.rmsnorm_quantize_q8_1(_t(x), _t(gamma), eps, K=K)).reshape(M, K // 32, 36)
-    assert np.array_equal(got, ref)
+    again = _np(ops.rmsnorm_quantize_q8_1(_t(x), _t(gamma), eps, K=K)).reshape(M, K // 32, 36)
+    r = C.check_q8_1_near(got, ref, xh, K)
+    print("rmsnorm_quantize_q8_1", (M, K), r)
+    assert r["ok"], r
+    assert np.array_equal(got, again)
 
 
 def test_rmsnorm_quantize_q8_1_errors(ops):
