@@ -115,3 +115,12 @@ WORKLOADS = {
     "verifier_down": dict(fmt="q4_0", M=6, K=17408, N=5120, seed=2, outlier_frac=0.01),
     "lmhead_q6_k": dict(fmt="q6_k", M=5, K=5120, N=248320, seed=3, rows_from=1, x_rows=6),
 }
+
+
+def tiny_q4_0_inputs():
+    """The tiny Q4_0 workload exactly as configured: M = 1, K = 256, N = 512,
+    seed 0.  The one seed is split into independent child seeds, the first
+    for the weights, the second for the activation."""
+    c = WORKLOADS["tiny_q4_0"]
+    sw, sx = (int(ch.generate_state(1)[0]) for ch in np.random.SeedSequence(c["seed"]).spawn(2))
+    return q4_0_weights(c["N"], c["K"], seed=sw), activations(c["M"], c["K"], seed=sx)

@@ -1,6 +1,8 @@
 """Parity at the full workload sizes the benchmark times (same launch
 configuration: the library picks it from M, K, N), against the CPU oracle.
 
+  * tiny Q4_0 GEMV exactly as configured (M=1, K=256, N=512, seed 0): every
+    output, and the row argmax with lowest-index ties;
   * width-6 verifier MMVQ, Q4_0: gate/up M=6 K=5120 N=17408, down M=6 K=17408
     N=5120 (1% outlier channels x20) -- every output checked;
   * fused Q6_K LM-head top-1, K=5120 N=248320, rows 1..5 of a [6, 5120] block
@@ -44,6 +46,26 @@ def _t(a):
 def _np(t):
     torch.cuda.synchronize()
     return t.cpu().numpy()
+
+
+def test_tiny_q4_0_as_configured(ops):
+    c = synth.WORKLOADS["tiny_q4_0"]
+    M, K, N = c["M"], c["K"], c["N"]
+    w, x = synth.tiny_q4_0_inputs()
+    xq_ref = oracle.quantize_q8_1(x)
+    y_ref, S = oracle.qgemv_q4_0(w, xq_ref)
+    xq = ops.quantize_q8_1(_t(x))
+    assert np.array_equal(_np(xq).reshape(xq_ref.shape), xq_ref)
+    yd = ops.qgemv_q4_0(ops.qpack_q4_0(_t(w), N, K), xq, M, K, N)
+    y = _np(yd)
+    r = C.check_close(y, y_ref, S)
+    print("tiny_q4_0", r)
+    assert r["ok"], r
+    # the argmax: on the GPU's own fp32 output, the oracle's lowest-index
+    # rule bit for bit; against the fp64 oracle values, the gap rule
+    ids = _np(ops.argmax_f32_rows(yd))
+    assert np.array_equal(ids, oracle.top1(y.astype(np.float32)))
+    assert not C.check_top1(ids, y_ref)
 
 
 @pytest.mark.parametrize("name", ["verifier_gate_up", "verifier_down"])

@@ -225,6 +225,64 @@ def test_block_dots_sum_to_output():
     assert np.allclose(y, ref, rtol=1e-13, atol=0)
 
 
+def _q6_k_decode_numpy(w: np.ndarray):
+    """Codes, subscales and d of canonical Q6_K superblocks [N, ns, 210],
+    decoded in numpy from the documented byte layout (ql[128], qh[64], int8
+    sc[16], fp16 d; value i: low 4 bits = nibble (i & 1) of ql[i >> 1], high 2
+    bits = bits 2 (i & 3) of qh[i >> 2]; subscale i >> 4)."""
+    i = np.arange(256)
+    lo = (w[..., i >> 1] >> (4 * (i & 1))) & 0x0F
+    hi = (w[..., 128 + (i >> 2)] >> (2 * (i & 3))) & 0x03
+    q = (lo | (hi << 4)).astype(np.int64)
+    sc = w[..., 192:208].copy().view(np.int8).astype(np.int64)
+    d = w[..., 208:210].copy().view(np.float16)[..., 0].astype(np.float64)
+    return q, sc, d
+
+
+def test_q6_k_block_dots_match_per_block_dequant():
+    # random superblocks: each J[m, n, b], scaled by d6 of its superblock and
+    # d_a of its block, is the fp64 dot of block b's dequantized weights and
+    # activations; a slip in the (superblock, block) index or in the
+    # [m][n][b] layout breaks the match at once
+    M, K, N = 3, 1024, 7
+    w = synth.q6_k_weights(N, K, seed=21)
+    xq = oracle.quantize_q8_1(synth.activations(M, K, seed=22))
+    J = oracle.block_dots_q6_k(w, xq).astype(np.float64)
+    assert J.shape == (M, N, K // 32)
+    q, sc, d = _q6_k_decode_numpy(w)
+    wdq = (d[:, :, None] * sc[:, :, np.arange(256) >> 4] * (q - 32)).reshape(N, K)
+    da = xq[:, :, 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    qa = xq[:, :, 4:].copy().view(np.int8).astype(np.float64)
+    adq = (da[:, :, None] * qa).reshape(M, K)
+    per_block = np.einsum("mbi,nbi->mnb", adq.reshape(M, K // 32, 32), wdq.reshape(N, K // 32, 32))
+    d6 = np.repeat(d, 8, axis=1)  # the superblock scale of each block
+    got = J * d6[None, :, :] * da[:, None, :]
+    assert np.allclose(got, per_block, rtol=1e-13, atol=1e-300)
+    y, _ = oracle.qgemv_q6_k(w, xq)
+    assert np.allclose(got.sum(axis=2), y, rtol=1e-12, atol=0)
+
+
+def test_q6_k_block_dots_one_hot_per_half():
+    # a one-hot activation at value i of superblock s reads back, in block
+    # 8 s + (i mod 256) // 32 only, sc[(i mod 256) // 16] * (q_i - 32) * 127
+    # (the one-hot's code); every other block dot is 0
+    N, K = 2, 512
+    g = np.random.default_rng(23)
+    codes = g.integers(0, 64, (N, 2, 256))
+    sc = g.integers(-64, 64, (N, 2, 16))
+    w = np.stack([np.stack([_q6_k_superblock(2.0 ** -9, sc[n, s], codes[n, s]) for s in range(2)])
+                  for n in range(N)])
+    for i in (0, 15, 16, 31, 32, 47, 200, 255, 256, 271, 300, 511):
+        x = np.zeros((1, K), dtype=np.float32)
+        x[0, i] = 1.0
+        J = oracle.block_dots_q6_k(w, oracle.quantize_q8_1(x))
+        s, v = i // 256, i % 256
+        for n in range(N):
+            want = np.zeros(K // 32, dtype=np.int64)
+            want[8 * s + v // 32] = sc[n, s, v // 16] * (codes[n, s, v] - 32) * 127
+            assert np.array_equal(J[0, n], want), (i, n)
+
+
 def test_threads_do_not_change_results():
     w = synth.q6_k_weights(37, 512, seed=8)
     xq = oracle.quantize_q8_1(synth.activations(3, 512, seed=9))
