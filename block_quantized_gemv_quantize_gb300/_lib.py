@@ -60,6 +60,7 @@ SIGNATURES = {
     "qgemv_q4_0_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "qgemv_q8_0_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "qgemv_q6_k_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+    "lmhead_q6_k_top1_plan": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "lmhead_q6_k_top1_noalloc": (_I, [_P, _P, _L, _P, _I, _I, _I, _P]),
 }
 
@@ -384,6 +385,13 @@ def set_q6_k_tensor_cores(mode: int) -> int:
     faster (default), 2 = wherever the shape allows, 0 = never (dp4a);
     returns the previous mode."""
     return int(LIB.qgemv_set_q6_k_tensor_cores(int(mode)))
+
+
+def lmhead_q6_k_top1_plan(M: int, K: int, N: int) -> dict:
+    """The kernel the fused LM-head calls would launch for this shape."""
+    info = (ctypes.c_int * 4)()
+    _check("lmhead_q6_k_top1_plan", LIB.lmhead_q6_k_top1_plan(M, K, N, info))
+    return {"ring": bool(info[0]), "grid": info[1], "warps": info[2], "stages": info[3]}
 
 
 def qgemv_q4_0_plan(M: int, K: int, N: int, N_b: int = 0) -> dict:

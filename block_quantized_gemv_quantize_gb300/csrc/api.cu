@@ -380,6 +380,13 @@ int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info)
     return st == TC_NOT_TAKEN ? QGEMV_OK : st;
 }
 
+int lmhead_q6_k_top1_plan(int M, int K, int N, int* info)
+{
+    if (!info || M < 1 || K < QK_K || N < 1) return QGEMV_INVALID_ARG;
+    if (M > QGEMV_MAX_M || K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
+    return lmhead_q6_k_plan(M, K, N, info);
+}
+
 int qgemv_set_q6_k_tensor_cores(int mode) { return set_q6_k_tensor_cores(mode); }
 
 int qgemv_q6_k_plan(int M, int K, int N, int* info)

@@ -7,17 +7,16 @@ namespace qgemv {
 DeviceInfo device_info()
 {
     static DeviceInfo cache[64];
-    static bool have[64];
+    static std::once_flag once[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DeviceInfo{0, 0};
-    if (!have[dev]) {
+    std::call_once(once[dev], [&]() {
         DeviceInfo d{0, 0};
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DeviceInfo{0, 0};
-        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-            return DeviceInfo{0, 0};
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            d = DeviceInfo{0, 0};
         cache[dev] = d;
-        have[dev] = true;
-    }
+    });
     return cache[dev];
 }
 

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/qgemv.h"
 #include "mmvq.cuh"
 
@@ -144,27 +146,30 @@ int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
     a.KC = p.KC;
     a.stages = p.stages;
     a.parts = p.parts;
-    // Opt in to the device's full shared memory once per device and kernel.
-    static bool opted_ring[64], opted_lock[64];
+    // Opt in to the device's full shared memory once per device and kernel
+    // (call_once: concurrent first calls from several host threads are safe).
+    static std::once_flag once_ring[64], once_lock[64];
+    static bool ok_ring[64], ok_lock[64];
     static unsigned int* timeouts[64];
     if (p.ring) {
         auto kern = mmvq_ring_kernel<FMT, M, TOP1, PAIR, RES>;
-        if (!opted_ring[dev]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
-                return QGEMV_CUDA_ERROR;
-            if (cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) != cudaSuccess)
-                return QGEMV_CUDA_ERROR;
-            opted_ring[dev] = true;
-        }
+        std::call_once(once_ring[dev], [&]() {
+            ok_ring[dev] =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) == cudaSuccess &&
+                cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) == cudaSuccess;
+            if (!ok_ring[dev]) cudaGetLastError();
+        });
+        if (!ok_ring[dev]) return QGEMV_CUDA_ERROR;
         if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a, timeouts[dev]) != cudaSuccess)
             return QGEMV_CUDA_ERROR;
     } else {
         auto kern = mmvq_lockstep_kernel<FMT, M, TOP1, RES>;
-        if (!opted_lock[dev]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
-                return QGEMV_CUDA_ERROR;
-            opted_lock[dev] = true;
-        }
+        std::call_once(once_lock[dev], [&]() {
+            ok_lock[dev] =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) == cudaSuccess;
+            if (!ok_lock[dev]) cudaGetLastError();
+        });
+        if (!ok_lock[dev]) return QGEMV_CUDA_ERROR;
         if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a) != cudaSuccess) return QGEMV_CUDA_ERROR;
         if (PAIR) {  // the lock-step kernel takes the second weight in a launch of its own
             MmvqArgs b = a;
@@ -235,6 +240,9 @@ int launch_mmvq_q5_k(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullp
 unsigned int take_wait_timeouts_q5_k();
 int launch_qpack_q5_k(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
+// The launch plan of the fused LM-head kernel: {1 ring / 0 lock-step, grid,
+// warps, ring stages}.
+int lmhead_q6_k_plan(int M, int K, int N, int* info);
 unsigned int take_wait_timeouts_q4_0();
 unsigned int take_wait_timeouts_q4_0_pair();
 unsigned int take_wait_timeouts_q6_k();

@@ -544,8 +544,15 @@ __device__ __forceinline__ void top1_finish(const MmvqArgs& a, unsigned long lon
     }
 }
 
+// Keys a warp folds per row group in the lock-step top-1 kernel: R rows x M
+// activation rows, at most R_ROWS * MAX_M.
+constexpr int TOP1_GROUP_KEYS = R_ROWS * MAX_M;
+
 // Shared memory besides the activation tile and the rings, for TOP1.
-inline size_t top1_scratch_bytes(int nwarps) { return (size_t)nwarps * 64 * 8 + (size_t)nwarps * MAX_M * 8 + 16; }
+inline size_t top1_scratch_bytes(int nwarps)
+{
+    return (size_t)nwarps * TOP1_GROUP_KEYS * 8 + (size_t)nwarps * MAX_M * 8 + 16;
+}
 
 // ---------------------------------------------------------------------------
 // Ring kernel: the whole activation in shared memory, the weights streamed
@@ -1121,7 +1128,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lock
     t.am = reinterpret_cast<uint2*>(t.aq + 2 * M * KC);
     t.KC = KC;
     unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(t.am + M * KC);
-    unsigned long long* s_best = s_keys + W * 64;
+    unsigned long long* s_best = s_keys + W * TOP1_GROUP_KEYS;
     int* s_last = reinterpret_cast<int*>(s_best + W * MAX_M);
 
     const int64_t n_items = (L.n_groups + W - 1) / W;
@@ -1175,7 +1182,8 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lock
                 }
             }
         }
-        if (active) finish_rowgroup<M, R, TOP1, RES>(a, (int)(g * GROUP), acc, lane, s_keys + warp * 64, best);
+        if (active)
+            finish_rowgroup<M, R, TOP1, RES>(a, (int)(g * GROUP), acc, lane, s_keys + warp * TOP1_GROUP_KEYS, best);
     }
     if (TOP1) top1_finish<M>(a, s_best, s_last, best, lane, warp, W);
 }

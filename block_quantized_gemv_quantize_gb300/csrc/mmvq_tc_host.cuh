@@ -5,6 +5,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "launch.cuh"
 #include "mmvq_tc.cuh"
 
@@ -105,8 +107,8 @@ template <int FMT, int M, bool PAIR>
 int tc_max_clusters(int dev, int ci, size_t smem)
 {
     static int cache[64][4];
-    static bool have[64][4];
-    if (!have[dev][ci]) {
+    static std::once_flag once[64][4];
+    std::call_once(once[dev][ci], [&]() {
         const int C = TC_CLUSTERS[ci];
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C);
@@ -125,8 +127,7 @@ int tc_max_clusters(int dev, int ci, size_t smem)
             n = 0;
         }
         cache[dev][ci] = n;
-        have[dev][ci] = true;
-    }
+    });
     return cache[dev][ci];
 }
 
@@ -230,16 +231,16 @@ bool tc_plan(const DeviceInfo& di, int dev, int K, int N, int N2, TcPlan& best)
 template <int FMT, int M, bool PAIR>
 unsigned int* tc_prepare(const DeviceInfo& di, int dev)
 {
-    static bool opted[64];
+    static std::once_flag once[64];
     static unsigned int* timeouts[64];
-    if (!opted[dev]) {
+    std::call_once(once[dev], [&]() {
         if (cudaFuncSetAttribute(mmvq_tc_kernel<FMT, M, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 di.smem_optin) != cudaSuccess)
-            return nullptr;
-        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) != cudaSuccess)
-            return nullptr;
-        opted[dev] = true;
-    }
+                                 di.smem_optin) != cudaSuccess ||
+            cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) != cudaSuccess) {
+            timeouts[dev] = nullptr;
+            cudaGetLastError();
+        }
+    });
     return timeouts[dev];
 }
 

@@ -15,7 +15,10 @@
 // loads the library holds it until the process exits.  Host code cannot use
 // the array's name as a device address, so its device address is looked up
 // once per device with cudaGetSymbolAddress, with that device current, on the
-// first call made on the device.
+// first call made on the device.  The cached address does not survive a
+// reset of the device's primary context (cudaDeviceReset reloads the
+// library's module); the header tells callers not to use this entry point on
+// a device after resetting it.
 #include "../../include/qgemv.h"
 #include "launch.cuh"
 
