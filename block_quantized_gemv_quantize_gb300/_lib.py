@@ -42,6 +42,8 @@ SIGNATURES = {
     "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
+    "qgemv_debug_drop_next_copy": (_I, []),
+    "qgemv_debug_fail_fused": (_I, [_I]),
     "qgemv_set_q4_0_tensor_cores": (_I, [_I]),
     "qgemv_set_q6_k_tensor_cores": (_I, [_I]),
     "q8_0_pack_bytes": (_S, [_I, _I]),
@@ -309,6 +311,29 @@ def lmhead_q6_k_top1(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, ids:
     return ids
 
 
+def lmhead_top1_or_unfused(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, ids: torch.Tensor | None = None,
+                           ws: torch.Tensor | None = None):
+    """The greedy ids of the rows of x through the fused LM-head, falling back
+    to the ordinary path (quantize_q8_1, qgemv_q6_k with the logits written,
+    argmax_f32_rows) when the fused call does not go through ("Q6_K M=6 fused
+    DFlash top-1 production record", Exactness and safety contracts: the
+    ordinary argmax is skipped only once the fused enqueue has succeeded).
+    Returns (ids, "fused" or "ordinary"); a refused call enqueued nothing, so
+    the fallback starts from the same inputs."""
+    M = x.shape[0]
+    if ids is None:
+        ids = torch.empty(M, dtype=torch.int32, device=x.device)
+    try:
+        lmhead_q6_k_top1(w_pack, x, K, N, ids=ids, ws=ws)
+        return ids, "fused"
+    except QgemvError as e:
+        if e.status in (-1, -3, -6):  # bad arguments, misaligned, a pending timeout: the ordinary path fails too
+            raise
+    y = qgemv_q6_k(w_pack, quantize_q8_1(x, K=K), M, K, N)
+    argmax_f32_rows(y, ids=ids)
+    return ids, "ordinary"
+
+
 def lmhead_q6_k_candmax(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, cand: torch.Tensor,
                         ws: torch.Tensor | None = None):
     """(ids, top_vals, cand_vals): the greedy id of each row of fp32 x, its
@@ -434,7 +459,21 @@ def qgemv_q5_k_plan(M: int, K: int, N: int) -> dict:
 
 
 def qgemv_take_wait_timeouts() -> int:
-    """Warps that gave up waiting for a weight copy since the last call (synchronous)."""
+    """Warps that gave up waiting for their data since the last call; reads and
+    clears the count (synchronizes the device first), after which calls are
+    accepted again."""
+    torch.cuda.synchronize()
     c = ctypes.c_uint(0)
     _check("qgemv_take_wait_timeouts", LIB.qgemv_take_wait_timeouts(ctypes.byref(c)))
     return c.value
+
+
+def qgemv_debug_fail_fused(count: int) -> int:
+    """Test only: the next `count` fused LM-head calls fail before enqueueing."""
+    return int(LIB.qgemv_debug_fail_fused(int(count)))
+
+
+def qgemv_debug_drop_next_copy() -> int:
+    """Test only: the next small-M tensor-core Q4_0 launch skips one copy, so
+    one warp's bounded wait runs out (see include/qgemv.h)."""
+    return int(LIB.qgemv_debug_drop_next_copy())

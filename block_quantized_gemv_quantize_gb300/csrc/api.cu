@@ -6,9 +6,62 @@
 #include "../../include/qgemv.h"
 #include "launch.cuh"
 
+#include <atomic>
+#include <mutex>
+
 using namespace qgemv;
 
 namespace {
+
+// The wait-timeout counter.  A word of this library's own host memory,
+// registered (page-locked and mapped into the device address space) the first
+// time a kernel needs it: kernels add to it with system-scope atomics, the
+// host reads it without a copy, and every entry point can see, before it
+// enqueues anything, that an earlier call's kernel gave up waiting for its
+// data.  Where it cannot be registered, a device word stands in, which only
+// qgemv_take_wait_timeouts reads (with a copy).
+alignas(4096) unsigned int g_status_page[1024];
+__device__ unsigned int g_dev_counter;
+std::once_flag g_counter_once;
+unsigned int* g_counter_dev = nullptr;
+bool g_counter_mapped = false;
+std::atomic<int> g_drop_request{0};
+std::atomic<int> g_fail_fused{0};  // test only: fused LM-head calls to refuse
+
+// Takes one refusal request, if any is left.
+bool take_fused_failure()
+{
+    int v = g_fail_fused.load();
+    while (v > 0)
+        if (g_fail_fused.compare_exchange_weak(v, v - 1)) return true;
+    return false;
+}
+
+void counter_setup()
+{
+    void* p = nullptr;
+    if (cudaHostRegister(g_status_page, sizeof(g_status_page), cudaHostRegisterMapped | cudaHostRegisterPortable) ==
+            cudaSuccess &&
+        cudaHostGetDevicePointer(&p, g_status_page, 0) == cudaSuccess) {
+        g_counter_dev = static_cast<unsigned int*>(p);
+        g_counter_mapped = true;
+        return;
+    }
+    cudaGetLastError();
+    if (cudaGetSymbolAddress(&p, g_dev_counter) == cudaSuccess) g_counter_dev = static_cast<unsigned int*>(p);
+    else cudaGetLastError();
+}
+
+// An earlier call's kernel gave up waiting and the count was not taken yet.
+bool timeouts_pending()
+{
+    return g_counter_mapped && __atomic_load_n(&g_status_page[0], __ATOMIC_ACQUIRE) != 0;
+}
+
+#define QGEMV_FAIL_IF_TIMED_OUT() \
+    do {                          \
+        if (timeouts_pending()) return QGEMV_WAIT_TIMEOUT; \
+    } while (0)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -66,6 +119,9 @@ const char* qgemv_status_string(int status)
     case QGEMV_MISALIGNED: return "a device pointer is not 16-byte aligned";
     case QGEMV_WORKSPACE_TOO_SMALL: return "workspace too small";
     case QGEMV_CUDA_ERROR: return "CUDA error (launch or device query failed)";
+    case QGEMV_WAIT_TIMEOUT:
+        return "a kernel of an earlier call gave up waiting for its data, so that call's outputs are not valid "
+               "(qgemv_take_wait_timeouts reads and clears the count)";
     default: return "unknown status";
     }
 }
@@ -102,6 +158,7 @@ size_t argmax_f32_rows_workspace_bytes(int, int) { return top1_ws_bytes(); }
 
 int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!x || !xq) return QGEMV_INVALID_ARG;
     int st = check_mk(M, K, QK);
     if (st) return st;
@@ -113,6 +170,7 @@ int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* str
 int rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, void* xq, int M, int K,
                           void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!x || !gamma || !xq) return QGEMV_INVALID_ARG;
     int st = check_mk(M, K, QK);
     if (st) return st;
@@ -124,6 +182,7 @@ int rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float
 
 int qpack_q8_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!w_canon || !w_pack || N < 1 || K < 256) return QGEMV_INVALID_ARG;
     if (K % 256) return QGEMV_UNSUPPORTED_SHAPE;
     if (!aligned16(w_pack) || (reinterpret_cast<uintptr_t>(w_canon) & 1u)) return QGEMV_MISALIGNED;
@@ -132,6 +191,7 @@ int qpack_q8_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
 
 int qgemv_q8_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, y, ldy, M, K, N, 256);
     if (st) return st;
     MmvqArgs a{};
@@ -146,6 +206,7 @@ int qgemv_q8_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
 
 int qpack_q4_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!w_canon || !w_pack || N < 1 || K < QK_K) return QGEMV_INVALID_ARG;
     if (K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
     if (!aligned16(w_pack)) return QGEMV_MISALIGNED;
@@ -154,6 +215,7 @@ int qpack_q4_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
 
 int qgemv_q4_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK_K);
     if (st) return st;
     MmvqArgs a{};
@@ -168,6 +230,7 @@ int qgemv_q4_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
 
 int qpack_q5_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!w_canon || !w_pack || N < 1 || K < QK_K) return QGEMV_INVALID_ARG;
     if (K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
     if (!aligned16(w_pack)) return QGEMV_MISALIGNED;
@@ -176,6 +239,7 @@ int qpack_q5_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
 
 int qgemv_q5_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK_K);
     if (st) return st;
     MmvqArgs a{};
@@ -190,6 +254,7 @@ int qgemv_q5_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
 
 int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!w_canon || !w_pack || N < 1 || K < QK) return QGEMV_INVALID_ARG;
     if (K % QK) return QGEMV_UNSUPPORTED_SHAPE;
     if (!aligned16(w_canon) || !aligned16(w_pack)) return QGEMV_MISALIGNED;
@@ -198,6 +263,7 @@ int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream)
 
 int qpack_q6_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!w_canon || !w_pack || N < 1 || K < QK_K) return QGEMV_INVALID_ARG;
     if (K % QK_K) return QGEMV_UNSUPPORTED_SHAPE;
     if (!aligned16(w_canon) || !aligned16(w_pack)) return QGEMV_MISALIGNED;
@@ -206,6 +272,7 @@ int qpack_q6_k(const void* w_canon, void* w_pack, int N, int K, void* stream)
 
 int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK);
     if (st) return st;
     MmvqArgs a{};
@@ -223,6 +290,7 @@ int qgemv_q4_0(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
 int qgemv_q4_0_residual(const void* w_pack, const void* xq, const float* residual, int64_t ldr, float* y, int64_t ldy,
                         int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK);
     if (st) return st;
     if (!residual || ldr < N) return QGEMV_INVALID_ARG;
@@ -245,6 +313,7 @@ int qgemv_q4_0_residual(const void* w_pack, const void* xq, const float* residua
 int qgemv_q4_0_pair(const void* w_pack_a, const void* w_pack_b, const void* xq, float* y_a, float* y_b, int64_t ldy,
                     int M, int K, int N_a, int N_b, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack_a, xq, y_a, ldy, M, K, N_a, QK);
     if (st) return st;
     st = check_gemv(w_pack_b, xq, y_b, ldy, M, K, N_b, QK);
@@ -266,6 +335,7 @@ int qgemv_q4_0_pair(const void* w_pack_a, const void* w_pack_b, const void* xq, 
 
 int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, y, ldy, M, K, N, QK_K);
     if (st) return st;
     MmvqArgs a{};
@@ -283,12 +353,14 @@ int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
 int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* ids, void* workspace,
                      size_t ws_bytes, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!w_pack || !x || !ids || !workspace) return QGEMV_INVALID_ARG;
     int st = check_mk(M, K, QK_K);
     if (st) return st;
     if (N < 1 || ldx < K) return QGEMV_INVALID_ARG;
     if (ws_bytes < lmhead_ws_bytes(M, K)) return QGEMV_WORKSPACE_TOO_SMALL;
     if (!aligned16(w_pack) || !aligned16(x) || !aligned16(ids) || !aligned16(workspace)) return QGEMV_MISALIGNED;
+    if (take_fused_failure()) return QGEMV_CUDA_ERROR;  // test only: nothing enqueued
     // Pre-pass: x -> Q8_1 in the workspace (the same kernel as quantize_q8_1),
     // then the MMVQ kernel with the top-1 epilogue reads that copy.
     uint8_t* xq = static_cast<uint8_t*>(workspace) + LMHEAD_Q8_OFFSET;
@@ -311,6 +383,7 @@ int lmhead_q6_k_candmax(const void* w_pack, const float* x, int64_t ldx, const i
                         float* top_vals, float* cand_vals, void* workspace, size_t ws_bytes, int M, int K, int N,
                         void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!w_pack || !x || !cand || !ids || !top_vals || !cand_vals || !workspace) return QGEMV_INVALID_ARG;
     int st = check_mk(M, K, QK_K);
     if (st) return st;
@@ -343,6 +416,7 @@ int lmhead_q6_k_candmax(const void* w_pack, const float* x, int64_t ldx, const i
 int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, size_t ws_bytes, int M, int N,
                     void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     if (!y || !ids || !workspace) return QGEMV_INVALID_ARG;
     if (M < 1 || N < 1 || ldy < N) return QGEMV_INVALID_ARG;
     if (M > QGEMV_MAX_M) return QGEMV_UNSUPPORTED_SHAPE;
@@ -353,6 +427,7 @@ int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, 
 
 int qgemv_block_dots_q4_0(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, out, N, M, K, N, QK);
     if (st) return st;
     return launch_block_dots(FMT_Q4_0, w_pack, xq, out, M, K, N, as_stream(stream));
@@ -360,6 +435,7 @@ int qgemv_block_dots_q4_0(const void* w_pack, const void* xq, int32_t* out, int 
 
 int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream)
 {
+    QGEMV_FAIL_IF_TIMED_OUT();
     int st = check_gemv(w_pack, xq, out, N, M, K, N, QK_K);
     if (st) return st;
     return launch_block_dots(FMT_Q6_K, w_pack, xq, out, M, K, N, as_stream(stream));
@@ -437,11 +513,36 @@ int qgemv_q8_0_plan(int M, int K, int N, int* info)
 int qgemv_take_wait_timeouts(unsigned int* count)
 {
     if (!count) return QGEMV_INVALID_ARG;
-    *count = take_wait_timeouts_q4_0() + take_wait_timeouts_q4_0_pair() + take_wait_timeouts_q4_0_tc() + take_wait_timeouts_q4_0_mma() + take_wait_timeouts_q4_0_mma_pair() +
-             take_wait_timeouts_q4_0_residual() + take_wait_timeouts_q6_k() + take_wait_timeouts_q6_k_tc() +
-             take_wait_timeouts_lmhead() + take_wait_timeouts_q8_0() + take_wait_timeouts_q4_k() +
-             take_wait_timeouts_q5_k();
-    return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
+    *count = 0;
+    if (!wait_timeout_counter()) return QGEMV_CUDA_ERROR;
+    if (g_counter_mapped) {
+        *count = __atomic_exchange_n(&g_status_page[0], 0u, __ATOMIC_ACQ_REL);
+        return QGEMV_OK;
+    }
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dev_counter, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_dev_counter, &zero, sizeof(zero)) != cudaSuccess)
+        return QGEMV_CUDA_ERROR;
+    *count = v;
+    return QGEMV_OK;
 }
 
+int qgemv_debug_drop_next_copy(void) { return g_drop_request.exchange(1); }
+
+int qgemv_debug_fail_fused(int count) { return g_fail_fused.exchange(count > 0 ? count : 0); }
+
 }  // extern "C"
+
+namespace qgemv {
+
+unsigned int* wait_timeout_counter()
+{
+    std::call_once(g_counter_once, counter_setup);
+    return g_counter_dev;
+}
+
+bool wait_timeouts_pending() { return timeouts_pending(); }
+
+int take_drop_request() { return g_drop_request.exchange(0); }
+
+}  // namespace qgemv

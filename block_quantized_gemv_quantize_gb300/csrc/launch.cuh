@@ -38,9 +38,17 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// Counts warps that gave up waiting for a weight copy (one per translation
-// unit that instantiates the ring kernel).
-static __device__ unsigned int g_wait_timeouts;
+// The library-wide count of warps that gave up waiting for their data (a
+// bounded wait ran out): the device address kernels add to (system-scope
+// atomics), host memory mapped into the device address space when that could
+// be set up, a device word otherwise; null if neither could.
+unsigned int* wait_timeout_counter();
+// Whether a kernel gave up waiting since the count was last taken (false when
+// the counter is a device word, which the host cannot read without a copy).
+bool wait_timeouts_pending();
+// A test-only request (qgemv_debug_drop_next_copy) taken by the next launch of
+// the small-M Q4_0 kernel: 1 once, then 0.
+int take_drop_request();
 
 // Largest multiple-of-32 block chunk of activation that fits in shared memory
 // next to `extra` bytes (all of K when it fits).
@@ -154,9 +162,10 @@ int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
     if (p.ring) {
         auto kern = mmvq_ring_kernel<FMT, M, TOP1, PAIR, RES>;
         std::call_once(once_ring[dev], [&]() {
+            timeouts[dev] = wait_timeout_counter();
             ok_ring[dev] =
                 cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) == cudaSuccess &&
-                cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) == cudaSuccess;
+                timeouts[dev] != nullptr;
             if (!ok_ring[dev]) cudaGetLastError();
         });
         if (!ok_ring[dev]) return QGEMV_CUDA_ERROR;
@@ -196,15 +205,6 @@ int launch_mmvq_m(MmvqArgs a, cudaStream_t s)
     return launch_mmvq_pm<FMT, M, TOP1, false>(a, s);
 }
 
-// Reads and clears this translation unit's timeout counter (synchronous).
-inline unsigned int take_wait_timeouts_tu()
-{
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
-    cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
-    return v;
-}
-
 int launch_mmvq_q4_0(const MmvqArgs& a, int M, cudaStream_t s);
 // The tensor-core Q4_0 path (one weight or a pair); TC_NOT_TAKEN when it is
 // switched off or the shape is not one it takes (the caller then uses the
@@ -216,37 +216,25 @@ int set_q4_0_tensor_cores(int mode);
 // The small-M tensor-core Q4_0 path (M <= 8, N % 16 == 0, K % 1024 == 0,
 // checked by the caller); TC_NOT_TAKEN when no launch plan fits.
 int launch_mmvq_q4_0_mma(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int* info = nullptr);
-unsigned int take_wait_timeouts_q4_0_mma();
-unsigned int take_wait_timeouts_q4_0_mma_pair();
-unsigned int take_wait_timeouts_q4_0_tc();
 // The tensor-core Q6_K path (M >= TC_Q6_K_MIN_M, N % 16 == 0, K % 1024 == 0);
 // TC_NOT_TAKEN otherwise.
 int launch_mmvq_q6_k_tc(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
 int set_q6_k_tensor_cores(int mode);
-unsigned int take_wait_timeouts_q6_k_tc();
 int launch_mmvq_q4_0_pair(const MmvqArgs& a, int M, cudaStream_t s);
 // y = W x + residual on the SIMT kernels; the residual travels in a.x / a.ldx
 int launch_mmvq_q4_0_residual(const MmvqArgs& a, int M, cudaStream_t s);
-unsigned int take_wait_timeouts_q4_0_residual();
 int launch_mmvq_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 // Q8_0 (tensor cores, its own pack); QGEMV_UNSUPPORTED_SHAPE when no plan fits
 int launch_mmvq_q8_0(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
-unsigned int take_wait_timeouts_q8_0();
 int launch_qpack_q8_0(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_mmvq_q4_k(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
-unsigned int take_wait_timeouts_q4_k();
 int launch_qpack_q4_k(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_mmvq_q5_k(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
-unsigned int take_wait_timeouts_q5_k();
 int launch_qpack_q5_k(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
 // The launch plan of the fused LM-head kernel: {1 ring / 0 lock-step, grid,
 // warps, ring stages}.
 int lmhead_q6_k_plan(int M, int K, int N, int* info);
-unsigned int take_wait_timeouts_q4_0();
-unsigned int take_wait_timeouts_q4_0_pair();
-unsigned int take_wait_timeouts_q6_k();
-unsigned int take_wait_timeouts_lmhead();
 
 int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cudaStream_t s);
 int launch_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float eps, void* xq, int M, int K,

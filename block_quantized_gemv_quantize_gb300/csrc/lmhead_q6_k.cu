@@ -68,6 +68,5 @@ int lmhead_q6_k_plan(int M, int K, int N, int* info)
     }
 }
 
-unsigned int take_wait_timeouts_lmhead() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

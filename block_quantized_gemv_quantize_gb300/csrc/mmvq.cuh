@@ -983,7 +983,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             if (direct) issue_direct(it, c);
             else issue_next();
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wbar[slot], phase))) {
-                if (lane == 0) atomicAdd(timeouts, 1u);
+                if (lane == 0) atomicAdd_system(timeouts, 1u);
                 alive = false;
                 break;
             }

@@ -27,6 +27,5 @@ int launch_mmvq_q4_0(const MmvqArgs& a, int M, cudaStream_t s)
     }
 }
 
-unsigned int take_wait_timeouts_q4_0() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -11,6 +11,5 @@ int launch_mmvq_q4_0_mma(const MmvqArgs& a, int M, bool pair, cudaStream_t s, in
     return pair ? launch_mmvq_q4_0_mma_pair(a, M, s, info) : launch_qm<false>(a, M, s, info);
 }
 
-unsigned int take_wait_timeouts_q4_0_mma() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -356,9 +356,12 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     const uint64_t pol = __shfl_sync(FULL, l2_evict_first_policy(), 0);
 
     int issued = 0, iss_slot = 0;
+    // test only: the job whose copy is never issued, so that its wait runs out
+    // (job 0 of CTA 0, in the warp that holds it)
+    const int dropped = a.drop_copy && blockIdx.x == 0 && j0 == 0 && j1 > 0 ? 0 : -1;
     auto issue = [&]() {
         const int h = ikg & (JPC - 1), c = ikg >> JPC_LOG;  // which JB blocks of which 32-block chunk
-        if (lane == 0) {
+        if (lane == 0 && issued != dropped) {
             uint64_t* bar = &wbar[iss_slot];
             uint8_t* dst = wnib_p + (size_t)iss_slot * NIB;
             fence_proxy_async();
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     }
     bool alive = true;
     if (row_bytes > 0 && !__all_sync(FULL, mbar_wait_bounded(abar, 0))) {
-        if (lane == 0) atomicAdd(timeouts, 1u);
+        if (lane == 0) atomicAdd_system(timeouts, 1u);
         alive = false;
     }
     alive = __syncthreads_and(alive);
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     uint32_t phase = 0;
     for (int j = j0; alive && j < j1; ++j) {
         if (!__all_sync(FULL, mbar_wait_bounded(&wbar[slot], phase))) {
-            if (lane == 0) atomicAdd(timeouts, 1u);
+            if (lane == 0) atomicAdd_system(timeouts, 1u);
             alive = false;
             break;
         }
@@ -503,7 +506,8 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     // After a timeout, give the copies still in flight a bounded wait before
     // the shared memory is released.
     if (lane == 0) {
-        for (int jj = consumed; jj < issued; ++jj) mbar_wait_bounded(&wbar[jj % S], (uint32_t)((jj / S) & 1));
+        for (int jj = consumed; jj < issued; ++jj)
+            if (jj != dropped) mbar_wait_bounded(&wbar[jj % S], (uint32_t)((jj / S) & 1));
         if (!alive && warp == 0) mbar_wait_bounded(abar, 0);
     }
     alive = __syncthreads_and(alive);  // the ring area is free

@@ -97,7 +97,7 @@ const QmDevice& qm_device(const DeviceInfo& di, int dev)
         const int sm = di.smem_optin;
         q.ok = qm_opt_in<M, QM_JB[0], QM_TL[0], PAIR>(sm) && qm_opt_in<M, QM_JB[1], QM_TL[1], PAIR>(sm) &&
                qm_opt_in<M, QM_JB[2], QM_TL[2], PAIR>(sm) &&
-               cudaGetSymbolAddress(reinterpret_cast<void**>(&q.timeouts), g_wait_timeouts) == cudaSuccess;
+               (q.timeouts = wait_timeout_counter()) != nullptr;
         for (int ci = 0; ci < 4; ++ci) {
             const int C = TC_CLUSTERS[ci];
             int r[QM_SHAPES] = {0, 0, 0};
@@ -207,6 +207,7 @@ int launch_qm_m(const MmvqArgs& m, cudaStream_t s, int* info)
     a.jb = jb;
     a.nkb_max = p.nkb_max;
     a.out_tiles = p.out_units;
+    a.drop_copy = take_drop_request();
     cudaError_t e;
     switch (p.shape) {
     case 0: e = qm_launch<M, QM_JB[0], QM_TL[0], PAIR>(p, a, n0, d0, n1, d1, qd.timeouts, s); break;

@@ -9,6 +9,5 @@ int launch_mmvq_q4_0_mma_pair(const MmvqArgs& a, int M, cudaStream_t s, int* inf
     return launch_qm<true>(a, M, s, info);
 }
 
-unsigned int take_wait_timeouts_q4_0_mma_pair() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -28,6 +28,5 @@ int launch_mmvq_q4_0_residual(const MmvqArgs& a, int M, cudaStream_t s)
     }
 }
 
-unsigned int take_wait_timeouts_q4_0_residual() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -100,6 +100,5 @@ int launch_mmvq_q4_0_tc(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int
     return pair ? launch_tc<true>(a, M, s, info) : launch_tc<false>(a, M, s, info);
 }
 
-unsigned int take_wait_timeouts_q4_0_tc() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

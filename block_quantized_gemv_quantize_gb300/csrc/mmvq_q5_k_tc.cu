@@ -72,6 +72,5 @@ int launch_mmvq_q5_k(const MmvqArgs& a, int M, cudaStream_t s, int* info)
     }
 }
 
-unsigned int take_wait_timeouts_q5_k() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -27,6 +27,5 @@ int launch_mmvq_q6_k(const MmvqArgs& a, int M, cudaStream_t s)
     }
 }
 
-unsigned int take_wait_timeouts_q6_k() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -140,6 +140,5 @@ int launch_mmvq_q6_k_tc(const MmvqArgs& a, int M, cudaStream_t s, int* info)
     }
 }
 
-unsigned int take_wait_timeouts_q6_k_tc() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -72,6 +72,5 @@ int launch_mmvq_q8_0(const MmvqArgs& a, int M, cudaStream_t s, int* info)
     }
 }
 
-unsigned int take_wait_timeouts_q8_0() { return take_wait_timeouts_tu(); }
 
 }  // namespace qgemv

@@ -91,6 +91,7 @@ struct TcArgs {
     int jb;             // blocks per job (8 or 16)
     int nkb_max;        // activation blocks staged per CTA (the largest K part)
     int out_tiles;      // clusters: tiles per cluster the result buffer holds
+    int drop_copy;      // test only (small-M Q4_0 kernel): CTA 0's warp 0 issues no copy for its first job
 };
 
 // Shared-memory layout, identical on the host (sizing) and the device.
@@ -936,7 +937,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 
     if (row_bytes > 0 && !__all_sync(FULL, mbar_wait_bounded(abar, 0))) {
-        if (lane == 0) atomicAdd(timeouts, 1u);
+        if (lane == 0) atomicAdd_system(timeouts, 1u);
         alive = false;
     }
     alive = __syncthreads_and(alive);
@@ -965,7 +966,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int j = j0; alive && j < j1; ++j) {
         if (issued < n_jobs) issue();
         if (!__all_sync(FULL, mbar_wait_bounded(&wbar[slot], phase))) {
-            if (lane == 0) atomicAdd(timeouts, 1u);
+            if (lane == 0) atomicAdd_system(timeouts, 1u);
             break;
         }
         ++consumed;

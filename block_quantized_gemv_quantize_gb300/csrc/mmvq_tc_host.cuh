@@ -234,9 +234,9 @@ unsigned int* tc_prepare(const DeviceInfo& di, int dev)
     static std::once_flag once[64];
     static unsigned int* timeouts[64];
     std::call_once(once[dev], [&]() {
+        timeouts[dev] = wait_timeout_counter();
         if (cudaFuncSetAttribute(mmvq_tc_kernel<FMT, M, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 di.smem_optin) != cudaSuccess ||
-            cudaGetSymbolAddress(reinterpret_cast<void**>(&timeouts[dev]), g_wait_timeouts) != cudaSuccess) {
+                                 di.smem_optin) != cudaSuccess) {
             timeouts[dev] = nullptr;
             cudaGetLastError();
         }

@@ -61,6 +61,7 @@ using namespace qgemv;
 extern "C" int lmhead_q6_k_top1_noalloc(const void* w_pack, const float* x, int64_t ldx, int32_t* ids, int M, int K,
                                         int N, void* stream)
 {
+    if (wait_timeouts_pending()) return QGEMV_WAIT_TIMEOUT;
     if (!w_pack || !x || !ids) return QGEMV_INVALID_ARG;
     if (M < 1 || K < QK_K || N < 1 || ldx < K) return QGEMV_INVALID_ARG;
     if (M > QGEMV_NOALLOC_MAX_M) return QGEMV_UNSUPPORTED_SHAPE;  // beyond the fixed scratch

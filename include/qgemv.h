@@ -26,12 +26,21 @@
  * Conventions for every call:
  *   - Pointers named w_*, x, xq, y, ids, workspace are DEVICE pointers and
  *     must be 16-byte aligned; the caller allocates and owns all of them.
- *     The library allocates no memory and never synchronizes.
+ *     The library allocates no memory and never synchronizes (it registers
+ *     one page of its own host memory for the wait-timeout counter, below).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream); all work is enqueued on it, in order.
  *   - Arguments are validated on the host before anything is enqueued; on
  *     error nothing is enqueued and a negative status is returned.  Device
  *     faults surface at the caller's next synchronization.
+ *   - Every wait inside the kernels is bounded (about a second).  A kernel
+ *     whose wait runs out counts it and stops early, so that call's outputs
+ *     are not valid; from then on every call that enqueues work returns
+ *     QGEMV_WAIT_TIMEOUT before enqueueing anything, until
+ *     qgemv_take_wait_timeouts has read the count (fail closed).  This needs
+ *     the counter in mapped host memory (set up the first time a kernel needs
+ *     it); where that cannot be set up, the count is still kept and read by
+ *     qgemv_take_wait_timeouts, but calls are not refused.
  *   - Matrices are row-major: a weight is N rows of K values (K contiguous,
  *     the ggml [K, N] tensor); activations are M rows of K values with row
  *     stride ldx (in elements); outputs y are M rows of N values with row
@@ -54,6 +63,7 @@ extern "C" {
 #define QGEMV_MISALIGNED (-3)         /* a pointer is not 16-byte aligned      */
 #define QGEMV_WORKSPACE_TOO_SMALL (-4)
 #define QGEMV_CUDA_ERROR (-5)         /* a CUDA call or launch failed          */
+#define QGEMV_WAIT_TIMEOUT (-6)       /* an earlier call's kernel gave up      */
 
 #define QGEMV_MAX_M 17
 
@@ -414,11 +424,29 @@ int qgemv_q5_k_plan(int M, int K, int N, int* info);
 int qgemv_q8_0_plan(int M, int K, int N, int* info);
 
 /* qgemv_take_wait_timeouts - number of warps that, since the previous call,
- * waited about a second for a weight copy that never completed and gave up
- * (their outputs are then invalid); resets the count.  Synchronous: it reads
- * a device counter.  0 in normal operation.  (Not from the pages: a guard of
- * this implementation's bounded waits.) */
+ * waited about a second for their data (a weight copy, the activation) and
+ * gave up (their launch's outputs are then invalid); reads and clears the
+ * count, after which calls are accepted again.  Synchronize first, so that
+ * every kernel launched before has finished.  0 in normal operation.  (Not
+ * from the pages: a guard of this implementation's bounded waits.) */
 int qgemv_take_wait_timeouts(unsigned int* count);
+
+/* qgemv_debug_drop_next_copy - for tests of the timeout path only: the next
+ * launch of the small-M tensor-core Q4_0 kernel (qgemv_q4_0 or
+ * qgemv_q4_0_pair, 5 <= M <= 8, on its default path) issues no copy for the
+ * first job of CTA 0, so the warp holding that job finds its bounded wait
+ * running out (about a second); it counts the timeout and stops, with no copy
+ * in flight for it, and the rest of the launch completes.  Process-wide; returns the previous
+ * request (0 or 1).  (Not from the pages.) */
+int qgemv_debug_drop_next_copy(void);
+
+/* qgemv_debug_fail_fused - for tests of the fail-closed fallback only: the
+ * next `count` calls of lmhead_q6_k_top1 that pass validation return
+ * QGEMV_CUDA_ERROR without enqueueing anything, as a fused kernel that cannot
+ * be launched would.  [record] Exactness and safety contracts: a fused call
+ * that does not go through leaves the ordinary path to run.  Returns the
+ * previous count. */
+int qgemv_debug_fail_fused(int count);
 
 #ifdef __cplusplus
 }

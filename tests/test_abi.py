@@ -98,3 +98,21 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.quantize_q8_1(fake, 32, odd, 1, 32, None) == -3
     assert lib.lmhead_q6_k_top1(fake, fake, 512, fake, fake, 8, 5, 512, 100, None) == -4
     assert lib.lmhead_q6_k_top1(fake, fake, 512, fake, fake, 4096, 5, 320, 100, None) == -2
+
+
+def test_fused_failure_hook_refuses_before_any_cuda_call(lib):
+    # the test-only hook makes the next validated fused LM-head call return
+    # QGEMV_CUDA_ERROR before anything is enqueued: on a machine without a
+    # GPU the call returns at once, touching none of the (fake) buffers
+    lib.qgemv_debug_fail_fused.argtypes = [ctypes.c_int]
+    fn = lib.lmhead_q6_k_top1
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    fake = 0x10000  # 16-byte aligned, never dereferenced
+    assert lib.qgemv_debug_fail_fused(1) == 0
+    assert fn(fake, fake, 5120, fake, fake, 1 << 20, 5, 5120, 248320, None) == -5
+    assert lib.qgemv_debug_fail_fused(0) == 0  # the one request was taken
+    # validation still comes first: a bad argument is reported as such
+    assert lib.qgemv_debug_fail_fused(1) == 0
+    assert fn(None, fake, 5120, fake, fake, 1 << 20, 5, 5120, 248320, None) == -1
+    assert lib.qgemv_debug_fail_fused(0) == 1
