@@ -34,12 +34,14 @@ constexpr int MMVQ_MAX_THREADS = 512;
 constexpr int MMVQ_MAX_WARPS = MMVQ_MAX_THREADS / 32;
 
 // Threads per CTA of the ring and lock-step kernels: 16 warps while the
-// R x M partial sums and the unpacked weights fit in 128 registers; 12 warps
-// (168 registers) for the few (format, M) that would spill; 8 warps (255
-// registers) for M > 8.
+// R x M partial sums and the unpacked weights fit in 128 registers (the
+// top-1 forms at M = 4 and 6 included: 112 and 127 registers, and 16 warps
+// made the six-row fused head 6 us faster than the unfused path, where 12
+// had left it level); 12 warps (168 registers) for M = 7, 8, which would
+// spill; 8 warps (255 registers) for M > 8.
 template <int FMT, int M, bool TOP1>
 struct MmvqThreads {
-    static constexpr bool wide = FMT == FMT_Q4_0 ? (M == 7 || M == 8) : (M == 7 || M == 8 || (TOP1 && (M == 4 || M == 6)));
+    static constexpr bool wide = FMT == FMT_Q4_0 ? (M == 7 || M == 8) : (M == 7 || M == 8);
     static constexpr int value = M > 8 ? 256 : (wide ? 384 : 512);
 };
 
