@@ -65,6 +65,10 @@ def parse():
     p.add_argument("--sweep-m", default="1,2,4,6,9,12,17", help="sweep: comma-separated row counts M")
     p.add_argument("--sweep-n", default="5120,17408,248320", help="sweep: comma-separated output sizes N")
     p.add_argument("--sweep-k", type=int, default=5120, help="sweep: the reduction size K")
+    p.add_argument("--profile", choices=["mlp", "heads"], default=None,
+                   help="for a profiler: run only the verifier MLP projections (gate/up pair, down) or only the "
+                        "LM heads (target qgemv_q6_k M=6, fused top-1 M=5), --steps times each with an L2 flush "
+                        "between calls; prints per-call times, not a bench line")
     return p.parse_args()
 
 
@@ -738,6 +742,62 @@ def run_reference(args):
     }
 
 
+def run_profile(args):
+    """A few calls of one part of the step, each after an L2 flush, on the
+    step's own seeded inputs; a small device footprint for a profiler.  Prints
+    the median event time of each call."""
+    import torch
+
+    from block_quantized_gemv_quantize_gb300 import build, synth
+
+    build.build()
+    from block_quantized_gemv_quantize_gb300 import ops
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def pack(fmt, canon, n, k):
+        c = up(canon)
+        return (ops.qpack_q4_0 if fmt == "q4_0" else ops.qpack_q6_k)(c, n, k)
+
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    if args.profile == "mlp":
+        c1, c2 = synth.WORKLOADS["verifier_gate_up"], synth.WORKLOADS["verifier_down"]
+        wg = pack("q4_0", synth.q4_0_weights(N_FF, K_H, seed=c1["seed"]), N_FF, K_H)
+        wu = pack("q4_0", synth.q4_0_weights(N_FF, K_H, seed=c1["seed"] + 10), N_FF, K_H)
+        wd = pack("q4_0", synth.q4_0_weights(K_H, N_FF, seed=c2["seed"]), K_H, N_FF)
+        xq = ops.quantize_q8_1(up(synth.activations(M_T, K_H, seed=c1["seed"] + 100, outlier_frac=0.01)))
+        hq = ops.quantize_q8_1(up(synth.activations(M_T, N_FF, seed=c2["seed"] + 100, outlier_frac=0.01)))
+        yg, yu, yd = (torch.empty((M_T, n), device=dev) for n in (N_FF, N_FF, K_H))
+        calls = {"gate_up": lambda: ops.qgemv_q4_0_pair(wg, wu, xq, M_T, K_H, N_FF, N_FF, y_a=yg, y_b=yu),
+                 "down": lambda: ops.qgemv_q4_0(wd, hq, M_T, N_FF, K_H, y=yd)}
+    else:
+        c3 = synth.WORKLOADS["lmhead_q6_k"]
+        wv = pack("q6_k", synth.q6_k_weights(N_V, K_H, seed=c3["seed"]), N_V, K_H)
+        xd = up(synth.activations(6, K_H, seed=c3["seed"] + 100))
+        xq = ops.quantize_q8_1(up(synth.activations(M_T, K_H, seed=c3["seed"] + 200)))
+        logits = torch.empty((M_T, N_V), device=dev)
+        calls = {"target_head": lambda: ops.qgemv_q6_k(wv, xq, M_T, K_H, N_V, y=logits),
+                 "lmhead_top1": lambda: ops.lmhead_q6_k_top1(wv, xd[1:6], K_H, N_V)}
+    torch.cuda.synchronize()
+    times = {n: [] for n in calls}
+    for _ in range(max(1, args.steps)):
+        for n, f in calls.items():
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            torch.cuda.synchronize()
+            times[n].append(a.elapsed_time(b) * 1e3)
+    print(json.dumps({"profile": args.profile, "calls": args.steps,
+                      "median_us": {n: round(statistics.median(v), 2) for n, v in times.items()},
+                      "l2": "flushed before every call"}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -749,6 +809,10 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(args)
+        return
+    if args.profile:
+        if rank == 0:
+            run_profile(args)
         return
     if world > 1:
         import torch.distributed as dist
