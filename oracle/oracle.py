@@ -278,6 +278,36 @@ def lmhead_q6_k_top1(w: np.ndarray, x: np.ndarray, nthreads: int | None = None):
     return top1(y), y, S
 
 
+def topk(y: np.ndarray, k: int):
+    """The k largest values of each row with their indices, larger first,
+    exactly equal values by lower index (-0 == +0), NaN never ranked; a row
+    with fewer than k non-NaN values fills its last places with -1 / NaN.
+    The top-k form of the candidate-max precheck ("Qwen3.6 27B AutoRound
+    Handoff", Current next-execution plan: true top ids and values).  Plain
+    definition: a stable sort of (-value, index) over the non-NaN entries.
+    Returns (ids int32 [M, k], vals float64 [M, k])."""
+    y = np.asarray(y, dtype=np.float64)
+    M, N = y.shape
+    ids = np.full((M, k), -1, dtype=np.int32)
+    vals = np.full((M, k), np.nan)
+    for m in range(M):
+        idx = np.flatnonzero(~np.isnan(y[m]))
+        order = idx[np.lexsort((idx, -y[m, idx]))][:k]
+        ids[m, : order.size] = order
+        vals[m, : order.size] = y[m, order]
+    return ids, vals
+
+
+def lmhead_q6_k_topk(w: np.ndarray, x: np.ndarray, k: int, nthreads: int | None = None):
+    """Fused LM-head top-k, step by step: quantize the rows of x to Q8_1,
+    project them through the Q6_K weight, rank each row's logits (topk).
+    Returns (ids, vals, y, S) so that callers can decide near-ties."""
+    xq = quantize_q8_1(x)
+    y, S = qgemv_q6_k(w, xq, nthreads)
+    ids, vals = topk(y, k)
+    return ids, vals, y, S
+
+
 # --------------------------------------------------------------------------
 # independent numpy dequantization (the brute-force pin for the C decoder)
 # --------------------------------------------------------------------------

@@ -265,6 +265,43 @@ def check_top1(ids, y_ref: np.ndarray, tol: float = TOP1_TOL) -> list[str]:
     return errs
 
 
+def check_topk(ids, vals, y_ref: np.ndarray, S: np.ndarray, tol: float = TOP1_TOL, rel: float = REL_TOL) -> list[str]:
+    """Rule for a top-k [M][k] against the fp64 oracle logits y_ref [M][N]
+    (S: the per-output magnitude sums of the fp32 gate).  Per row: the id at
+    rank r has an oracle value within tol * |max| of the oracle's r-th largest
+    (so set and order are the oracle's wherever its gaps exceed that), ids are
+    distinct, each value is within the fp32 gate of its id's oracle logit,
+    values never increase and equal values come by increasing id; past the
+    row's non-NaN count, id -1 and NaN.  Returns a list of violations."""
+    ids, vals = np.asarray(ids), np.asarray(vals, dtype=np.float64)
+    errs = []
+    M, k = ids.shape
+    for m in range(M):
+        row = y_ref[m]
+        srt = np.sort(row[~np.isnan(row)])[::-1]
+        top = abs(srt[0]) if srt.size else 0.0
+        seen = set()
+        for r in range(k):
+            i, v = int(ids[m, r]), vals[m, r]
+            if r >= srt.size:
+                if i != -1 or not np.isnan(v):
+                    errs.append(f"row {m} rank {r}: ({i}, {v}) past the non-NaN logits")
+                continue
+            if not 0 <= i < row.size or i in seen:
+                errs.append(f"row {m} rank {r}: id {i} out of range or repeated")
+                continue
+            seen.add(i)
+            if abs(row[i] - srt[r]) > tol * top:
+                errs.append(f"row {m} rank {r}: id {i} has oracle value {row[i]:.6g}, rank value {srt[r]:.6g}")
+            if not abs(v - row[i]) <= rel * max(abs(row[i]), S[m, i]):
+                errs.append(f"row {m} rank {r}: value {v:.8g} vs oracle {row[i]:.8g}")
+            if r > 0 and 0 <= int(ids[m, r - 1]):
+                pv, pi = vals[m, r - 1], int(ids[m, r - 1])
+                if v > pv or (v == pv and i < pi):
+                    errs.append(f"row {m} rank {r}: ({i}, {v}) out of order after ({pi}, {pv})")
+    return errs
+
+
 # ---------------------------------------------------------------- adversarial top-1
 
 

@@ -356,6 +356,70 @@ def test_top1_matches_brute_force_argmax():
     assert ids.tolist() == np.argmax(ref, axis=1).tolist()
 
 
+def _topk_by_repeated_max(row, k):
+    """Brute force, a different procedure from the oracle's sort: k passes,
+    each taking the first (lowest-index) strict maximum among the unused
+    non-NaN entries."""
+    used, ids, vals = set(), [], []
+    for _ in range(k):
+        best = None
+        for n, v in enumerate(row):
+            if n in used or v != v:
+                continue
+            if best is None or v > row[best]:
+                best = n
+        if best is None:
+            ids.append(-1)
+            vals.append(float("nan"))
+        else:
+            used.add(best)
+            ids.append(best)
+            vals.append(float(row[best]))
+    return ids, vals
+
+
+def test_topk_hand_example():
+    y = np.array([[1.0, 5.0, 3.0, 5.0, np.nan, -2.0, 3.0],
+                  [np.nan, np.nan, 2.0, np.nan, np.nan, np.nan, np.nan],
+                  [-0.0, 0.0, -1.0, np.inf, -np.inf, 0.0, -0.0]])
+    ids, vals = oracle.topk(y, 4)
+    assert ids.tolist() == [[1, 3, 2, 6], [2, -1, -1, -1], [3, 0, 1, 5]]
+    assert vals[0].tolist() == [5.0, 5.0, 3.0, 3.0]
+    assert vals[1, 0] == 2.0 and np.isnan(vals[1, 1:]).all()
+    assert vals[2].tolist() == [np.inf, 0.0, 0.0, 0.0]
+
+
+def test_topk_matches_repeated_max_brute_force():
+    g = np.random.default_rng(5)
+    for trial in range(40):
+        N = int(g.integers(1, 40))
+        # few distinct values, so that ties are common; some NaN
+        y = g.integers(-3, 4, size=(3, N)).astype(np.float64)
+        y[g.random((3, N)) < 0.15] = np.nan
+        k = int(g.integers(1, 9))
+        ids, vals = oracle.topk(y, k)
+        for m in range(3):
+            bi, bv = _topk_by_repeated_max(y[m].tolist(), k)
+            assert ids[m].tolist() == bi, (trial, m)
+            np.testing.assert_array_equal(vals[m], np.array(bv))
+
+
+def test_topk_first_entry_is_top1():
+    y = synth.activations(6, 1000, seed=31).astype(np.float64)
+    y[2, 17] = y[2, 400] = y[2].max() + 1.0  # an exact tie for the maximum
+    ids, _ = oracle.topk(y, 5)
+    assert ids[:, 0].tolist() == oracle.top1(y).tolist()
+
+
+def test_lmhead_topk_matches_fp64_dequant_matmul():
+    w = synth.q6_k_weights(300, 512, seed=23)
+    x = synth.activations(4, 512, seed=24)
+    ids, vals, y, _ = oracle.lmhead_q6_k_topk(w, x, 8)
+    ref = oracle.dequant_q8_1_np(oracle.quantize_q8_1(x)) @ oracle.dequant_q6_k_np(w).T
+    assert ids.tolist() == np.argsort(-ref, axis=1, kind="stable")[:, :8].tolist()
+    np.testing.assert_allclose(vals, np.take_along_axis(ref, ids.astype(np.int64), axis=1), rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- pack layout model (test helpers)
 
 @pytest.mark.parametrize("N,K", [(3, 32), (2, 96), (5, 256), (4, 1056), (3, 5120), (8, 2048)])
