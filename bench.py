@@ -358,6 +358,16 @@ def run_native(args, rank, world):
     def candmax():
         ops.lmhead_q6_k_candmax(w["w_vocab"], xd_rows, K_H, N_V, cand, ws=ws1)
 
+    # the top-8 form of the candidate-max on the same rows and candidates
+    ws_k = torch.zeros(ops.lmhead_q6_k_topk_workspace_bytes(5, K_H, N_V, 8), dtype=torch.uint8, device=dev)
+    ids_k = torch.empty((5, 8), dtype=torch.int32, device=dev)
+    vals_k = torch.empty((5, 8), device=dev)
+    cv_k = torch.empty(5, device=dev)
+
+    def topk8():
+        ops.lmhead_q6_k_topk(w["w_vocab"], xd_rows, K_H, N_V, 8, cand=cand, ws=ws_k, ids=ids_k, vals=vals_k,
+                             cand_vals=cv_k)
+
     # the target side with all six rows fused (no logits) against the step's
     # unfused target head (quantize + qgemv_q6_k + argmax), same inputs
     ws6 = torch.zeros(ops.lmhead_q6_k_top1_workspace_bytes(M_T, K_H, N_V), dtype=torch.uint8, device=dev)
@@ -381,12 +391,13 @@ def run_native(args, rank, world):
     def q8_only():
         ops.quantize_q8_1(x, out=xq1)
 
-    ab = {"fused": [], "unfused": [], "candmax": [], "target_fused": [], "target_unfused": [], "rms_q8": [],
-          "q8_only": []}
+    ab = {"fused": [], "unfused": [], "candmax": [], "topk8": [], "target_fused": [], "target_unfused": [],
+          "rms_q8": [], "q8_only": []}
     ab_rounds = 20  # interleaved A/B rounds of 10 calls each
     for _ in range(ab_rounds):
-        for name, fn in (("fused", fused), ("unfused", unfused), ("candmax", candmax), ("target_fused", target_fused),
-                         ("target_unfused", target_unfused), ("rms_q8", rms_q8), ("q8_only", q8_only)):
+        for name, fn in (("fused", fused), ("unfused", unfused), ("candmax", candmax), ("topk8", topk8),
+                         ("target_fused", target_fused), ("target_unfused", target_unfused), ("rms_q8", rms_q8),
+                         ("q8_only", q8_only)):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for _ in range(10):
@@ -396,6 +407,7 @@ def run_native(args, rank, world):
             ab[name].append(a.elapsed_time(b) * 1e3 / 10)
     same_ids = ids_d.cpu().tolist() == ids_u.cpu().tolist()
     same_ids_t = ids_tf.cpu().tolist() == ids_t.cpu().tolist()
+    topk_first_is_top1 = ids_k[:, 0].cpu().tolist() == ids_d.cpu().tolist()
 
     # Fused against unfused LM-head over the M sweep (BASELINE config 3's
     # control): for each M, rows 0..M-1 of a [17, 5120] activation, the
@@ -519,6 +531,9 @@ def run_native(args, rank, world):
             "lmhead_top1_us": round(call_ms["lmhead_top1"] * 1e3, 2),
             "fused_vs_unfused_us": ab_pair("fused", "unfused", ("fused", "unfused"), {"same_ids": same_ids}),
             "candmax_us": round(statistics.median(ab["candmax"]), 2),
+            "topk8_vs_top1_us": ab_pair("fused", "topk8", ("top1", "topk8"),
+                                        {"rows": "1..5", "k": 8, "with_candidate_scores": True,
+                                         "rank0_equals_top1": topk_first_is_top1}),
             "rmsnorm_q8_1_vs_quantize_us": ab_pair("q8_only", "rms_q8", ("quantize_q8_1", "rmsnorm_q8_1"), {}),
             "target_m6_fused_vs_unfused_us": ab_pair("target_fused", "target_unfused", ("fused", "unfused"),
                                                      {"same_ids": same_ids_t}),

@@ -38,12 +38,17 @@ SIGNATURES = {
     "qgemv_q4_0_pair": (_I, [_P, _P, _P, _P, _P, _L, _I, _I, _I, _I, _P]),
     "lmhead_q6_k_top1": (_I, [_P, _P, _L, _P, _P, _S, _I, _I, _I, _P]),
     "lmhead_q6_k_candmax": (_I, [_P, _P, _L, _P, _P, _P, _P, _P, _S, _I, _I, _I, _P]),
+    "lmhead_q6_k_topk_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "lmhead_q6_k_topk": (_I, [_P, _P, _L, _I, _P, _P, _P, _P, _P, _S, _I, _I, _I, _P]),
     "argmax_f32_rows": (_I, [_P, _L, _P, _P, _S, _I, _I, _P]),
     "qgemv_block_dots_q4_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_block_dots_q6_k": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "qgemv_take_wait_timeouts": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "qgemv_debug_drop_next_copy": (_I, []),
     "qgemv_debug_fail_fused": (_I, [_I]),
+    "qgemv_bounds_check_build": (_I, []),
+    "qgemv_take_bounds_errors": (_I, [ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(ctypes.c_uint)]),
+    "qgemv_debug_plant_bad_store": (_I, []),
     "qgemv_set_q4_0_tensor_cores": (_I, [_I]),
     "qgemv_set_q6_k_tensor_cores": (_I, [_I]),
     "q8_0_pack_bytes": (_S, [_I, _I]),
@@ -73,11 +78,15 @@ class QgemvError(RuntimeError):
         self.status = status
 
 
+BOUNDS_CHECK = os.environ.get("QGEMV_BOUNDS_CHECK", "0") == "1"
+
+
 def _load() -> ctypes.CDLL:
-    path = _build.LIB
+    path = _build.LIB_DEBUG if BOUNDS_CHECK else _build.LIB
     if not os.path.exists(path):
         raise ImportError(f"{path} is missing: build the CUDA library first "
-                          f"(python -m block_quantized_gemv_quantize_gb300.build)")
+                          f"(python -m block_quantized_gemv_quantize_gb300.build"
+                          f"{' --debug' if BOUNDS_CHECK else ''})")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
@@ -87,7 +96,7 @@ def _load() -> ctypes.CDLL:
 
 
 LIB = _load()
-LIB_PATH = _build.LIB
+LIB_PATH = _build.LIB_DEBUG if BOUNDS_CHECK else _build.LIB
 
 
 def status_string(status: int) -> str:
@@ -129,6 +138,10 @@ def lmhead_q6_k_top1_workspace_bytes(M: int, K: int, N: int) -> int:
 
 def argmax_f32_rows_workspace_bytes(M: int, N: int) -> int:
     return LIB.argmax_f32_rows_workspace_bytes(M, N)
+
+
+def lmhead_q6_k_topk_workspace_bytes(M: int, K: int, N: int, k: int) -> int:
+    return LIB.lmhead_q6_k_topk_workspace_bytes(M, K, N, k)
 
 
 # ---------------------------------------------------------------- workspaces
@@ -354,6 +367,37 @@ def lmhead_q6_k_candmax(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, c
     return ids, top_vals, cand_vals
 
 
+def lmhead_q6_k_topk(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int, k: int,
+                     cand: torch.Tensor | None = None, ws: torch.Tensor | None = None, ids: torch.Tensor | None = None,
+                     vals: torch.Tensor | None = None, cand_vals: torch.Tensor | None = None):
+    """(ids [M][k], vals [M][k], cand_vals [M] or None): the k largest logits
+    of each row of fp32 x with their ids, larger first, exactly equal values
+    by lower id (id -1 / NaN where a row has fewer than k non-NaN logits),
+    and, given cand (int32 [M]), each row's candidate logit."""
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    if ids is None:
+        ids = torch.empty((M, k), dtype=torch.int32, device=x.device)
+    if vals is None:
+        vals = torch.empty((M, k), dtype=torch.float32, device=x.device)
+    assert ids.shape == (M, k) and ids.is_contiguous() and vals.shape == (M, k) and vals.is_contiguous()
+    if cand is None:
+        cand_vals = None
+    else:
+        assert cand.dtype == torch.int32 and cand.numel() == M
+        if cand_vals is None:
+            cand_vals = torch.empty(M, dtype=torch.float32, device=x.device)
+    nb = lmhead_q6_k_topk_workspace_bytes(M, K, N, k)
+    if ws is None:
+        ws = workspace(x.device, nb)
+    _check("lmhead_q6_k_topk", LIB.lmhead_q6_k_topk(_dev(w_pack, "w_pack"), _dev(x, "x"), x.stride(0), k,
+                                                    None if cand is None else _dev(cand, "cand"), _dev(ids, "ids"),
+                                                    _dev(vals, "vals"),
+                                                    None if cand_vals is None else _dev(cand_vals, "cand_vals"),
+                                                    _dev(ws, "workspace"), ws.numel(), M, K, N, _stream(x)))
+    return ids, vals, cand_vals
+
+
 def lmhead_q6_k_top1_noalloc(w_pack: torch.Tensor, x: torch.Tensor, K: int, N: int,
                              ids: torch.Tensor | None = None) -> torch.Tensor:
     """As lmhead_q6_k_top1, with the library's fixed device scratch instead of
@@ -471,6 +515,27 @@ def qgemv_take_wait_timeouts() -> int:
 def qgemv_debug_fail_fused(count: int) -> int:
     """Test only: the next `count` fused LM-head calls fail before enqueueing."""
     return int(LIB.qgemv_debug_fail_fused(int(count)))
+
+
+def qgemv_bounds_check_build() -> bool:
+    """Whether the loaded library is the bounds-checking build."""
+    return bool(LIB.qgemv_bounds_check_build())
+
+
+def qgemv_take_bounds_errors() -> tuple[int, int]:
+    """(failed checks, site number of the first) since the last call, after a
+    device synchronize; (0, 0) always in the release build."""
+    count, site = ctypes.c_uint(0), ctypes.c_uint(0)
+    _check("qgemv_take_bounds_errors", LIB.qgemv_take_bounds_errors(ctypes.byref(count), ctypes.byref(site)))
+    return count.value, site.value
+
+
+def qgemv_debug_plant_bad_store() -> int:
+    """Test hook of the bounds-checking build: the next ring-kernel MMVQ
+    launch moves its first stores out of their extent, which its checks skip
+    and record.  Returns the previous request (QGEMV_UNSUPPORTED_SHAPE in the
+    release build, where it does nothing)."""
+    return LIB.qgemv_debug_plant_bad_store()
 
 
 def qgemv_debug_drop_next_copy() -> int:

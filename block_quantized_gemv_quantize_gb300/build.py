@@ -2,6 +2,13 @@
 
 Each translation unit compiles in its own nvcc process, in parallel, then the
 objects are linked into one shared library under ``_build/``.
+
+``build(debug=True)`` (``python -m block_quantized_gemv_quantize_gb300.build
+--debug``) makes the bounds-checking library ``_build/debug/libqgemv.so``
+instead: the same sources with ``-DQGEMV_BOUNDS_CHECK``, whose kernels check
+the indexes of their computed accesses and record failures in the library's
+status page (read by ``qgemv_take_bounds_errors``) instead of faulting.  The
+binding loads it when the environment has ``QGEMV_BOUNDS_CHECK=1``.
 """
 from __future__ import annotations
 
@@ -14,6 +21,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libqgemv.so")
+BUILD_DEBUG = os.path.join(BUILD, "debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libqgemv.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,23 +47,26 @@ def _deps() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile every CUDA source and link libqgemv.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          debug: bool = False) -> str:
+    """Compile every CUDA source and link libqgemv.so (the bounds-checking
+    one under _build/debug with debug=True); returns its path."""
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
-    flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE] + (extra_flags or [])
+    flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE] + (["-DQGEMV_BOUNDS_CHECK"] if debug else []) + (extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -66,15 +78,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = sources()
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
 
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

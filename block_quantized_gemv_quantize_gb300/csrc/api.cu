@@ -21,11 +21,12 @@ namespace {
 // data.  Where it cannot be registered, a device word stands in, which only
 // qgemv_take_wait_timeouts reads (with a copy).
 alignas(4096) unsigned int g_status_page[1024];
-__device__ unsigned int g_dev_counter;
+__device__ unsigned int g_dev_counter[4];
 std::once_flag g_counter_once;
 unsigned int* g_counter_dev = nullptr;
 bool g_counter_mapped = false;
 std::atomic<int> g_drop_request{0};
+std::atomic<int> g_plant_request{0};
 std::atomic<int> g_fail_fused{0};  // test only: fused LM-head calls to refuse
 
 // Takes one refusal request, if any is left.
@@ -106,6 +107,18 @@ size_t lmhead_ws_bytes(int M, int K)
     return LMHEAD_Q8_OFFSET + (((size_t)(M > 0 ? M : 0) * (size_t)(K > 0 ? K / QK : 0) * Q8_1_BYTES + 15) & ~(size_t)15);
 }
 
+// Top-k workspace: the lmhead workspace, then (256-byte aligned) one list of
+// k keys per row for each CTA, at most TOPK_MAX_CTAS CTAs and never more than
+// the row groups of N.
+static_assert(QGEMV_TOPK_MAX == TOPK_MAX, "top-k bound");
+size_t topk_lists_offset(int M, int K) { return (lmhead_ws_bytes(M, K) + 255) & ~(size_t)255; }
+size_t topk_ws_bytes(int M, int K, int N, int k)
+{
+    const int64_t groups = N > 0 ? ((int64_t)N + GROUP - 1) / GROUP : 0;
+    const int64_t ctas = groups < TOPK_MAX_CTAS ? groups : TOPK_MAX_CTAS;
+    return topk_lists_offset(M, K) + (size_t)ctas * (size_t)(M > 0 ? M : 0) * (size_t)(k > 0 ? k : 0) * 8;
+}
+
 }  // namespace
 
 extern "C" {
@@ -155,6 +168,7 @@ size_t q6_k_pack_bytes(int N, int K)
 }
 size_t lmhead_q6_k_top1_workspace_bytes(int M, int K, int) { return lmhead_ws_bytes(M, K); }
 size_t argmax_f32_rows_workspace_bytes(int, int) { return top1_ws_bytes(); }
+size_t lmhead_q6_k_topk_workspace_bytes(int M, int K, int N, int k) { return topk_ws_bytes(M, K, N, k); }
 
 int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* stream)
 {
@@ -413,6 +427,42 @@ int lmhead_q6_k_candmax(const void* w_pack, const float* x, int64_t ldx, const i
     return launch_lmhead_q6_k(a, M, s);
 }
 
+int lmhead_q6_k_topk(const void* w_pack, const float* x, int64_t ldx, int k, const int32_t* cand, int32_t* ids,
+                     float* vals, float* cand_vals, void* workspace, size_t ws_bytes, int M, int K, int N,
+                     void* stream)
+{
+    QGEMV_FAIL_IF_TIMED_OUT();
+    if (!w_pack || !x || !ids || !workspace || (cand == nullptr) != (cand_vals == nullptr)) return QGEMV_INVALID_ARG;
+    int st = check_mk(M, K, QK_K);
+    if (st) return st;
+    if (N < 1 || ldx < K || k < 1 || k > QGEMV_TOPK_MAX || k > N) return QGEMV_INVALID_ARG;
+    if (ws_bytes < topk_ws_bytes(M, K, N, k)) return QGEMV_WORKSPACE_TOO_SMALL;
+    if (!aligned16(w_pack) || !aligned16(x) || !aligned16(ids) || !aligned16(workspace) || (vals && !aligned16(vals)) ||
+        (cand && (!aligned16(cand) || !aligned16(cand_vals))))
+        return QGEMV_MISALIGNED;
+    cudaStream_t s = as_stream(stream);
+    // a candidate outside 0 .. N-1 keeps this NaN (all-ones bits)
+    if (cand && cudaMemsetAsync(cand_vals, 0xFF, (size_t)M * sizeof(float), s) != cudaSuccess) return QGEMV_CUDA_ERROR;
+    uint8_t* xq = static_cast<uint8_t*>(workspace) + LMHEAD_Q8_OFFSET;
+    st = launch_quantize_q8_1(x, ldx, xq, M, K, s);
+    if (st != QGEMV_OK) return st;
+    MmvqArgs a{};
+    a.w_pack = w_pack;
+    a.x = x;
+    a.ldx = ldx;
+    a.xq = xq;
+    a.K = K;
+    a.N = N;
+    a.ws = static_cast<Top1Workspace*>(workspace);
+    a.ids = ids;
+    a.top_vals = vals;
+    a.cand = cand;
+    a.cand_vals = cand_vals;
+    a.topk = k;
+    a.topk_lists = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + topk_lists_offset(M, K));
+    return launch_lmhead_q6_k_topk(a, M, s);
+}
+
 int argmax_f32_rows(const float* y, int64_t ldy, int32_t* ids, void* workspace, size_t ws_bytes, int M, int N,
                     void* stream)
 {
@@ -529,6 +579,45 @@ int qgemv_take_wait_timeouts(unsigned int* count)
 
 int qgemv_debug_drop_next_copy(void) { return g_drop_request.exchange(1); }
 
+int qgemv_bounds_check_build(void)
+{
+#ifdef QGEMV_BOUNDS_CHECK
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int qgemv_take_bounds_errors(unsigned int* count, unsigned int* first_site)
+{
+    if (!count || !first_site) return QGEMV_INVALID_ARG;
+    *count = 0;
+    *first_site = 0;
+    if (!wait_timeout_counter()) return QGEMV_CUDA_ERROR;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QGEMV_CUDA_ERROR;
+    if (g_counter_mapped) {
+        *count = __atomic_exchange_n(&g_status_page[1], 0u, __ATOMIC_ACQ_REL);
+        *first_site = __atomic_exchange_n(&g_status_page[2], 0u, __ATOMIC_ACQ_REL);
+        return QGEMV_OK;
+    }
+    unsigned int v[3] = {0, 0, 0}, zero[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(v, g_dev_counter, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_dev_counter, zero, sizeof(zero), sizeof(unsigned int)) != cudaSuccess)
+        return QGEMV_CUDA_ERROR;
+    *count = v[1];
+    *first_site = v[2];
+    return QGEMV_OK;
+}
+
+int qgemv_debug_plant_bad_store(void)
+{
+#ifdef QGEMV_BOUNDS_CHECK
+    return g_plant_request.exchange(1);
+#else
+    return QGEMV_UNSUPPORTED_SHAPE;
+#endif
+}
+
 int qgemv_debug_fail_fused(int count) { return g_fail_fused.exchange(count > 0 ? count : 0); }
 
 }  // extern "C"
@@ -544,5 +633,7 @@ unsigned int* wait_timeout_counter()
 bool wait_timeouts_pending() { return timeouts_pending(); }
 
 int take_drop_request() { return g_drop_request.exchange(0); }
+
+int take_plant_request() { return g_plant_request.exchange(0); }
 
 }  // namespace qgemv

@@ -31,7 +31,8 @@ DeviceInfo device_info()
 constexpr int QUANT_THREADS = 128;
 
 __global__ void __launch_bounds__(QUANT_THREADS) quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
-                                                                      uint8_t* __restrict__ xq, int M, int NB)
+                                                                      uint8_t* __restrict__ xq, int M, int NB,
+                                                                      unsigned int* st)
 {
     pdl_launch_dependents();
     pdl_wait();
@@ -44,8 +45,11 @@ __global__ void __launch_bounds__(QUANT_THREADS) quantize_q8_1_kernel(const floa
         const int64_t mine = i0 + (lane >> 3);
         const int64_t i = mine < nblk ? mine : nblk - 1;  // spare lanes redo the last block, unwritten
         const int m = (int)(i / NB), b = (int)(i - (int64_t)m * NB);
-        const Q81Lanes o = q8_1_quantize_8lanes(load_4_values(x + (int64_t)m * ldx + (int64_t)b * QK + 4 * sub, vec4));
-        if (mine < nblk) {
+        const int64_t xo = (int64_t)m * ldx + (int64_t)b * QK + 4 * sub;
+        float4 xv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (QG_OK(qg_in(xo, 4, (int64_t)(M - 1) * ldx + (int64_t)NB * QK), st, 101)) xv = load_4_values(x + xo, vec4);
+        const Q81Lanes o = q8_1_quantize_8lanes(xv);
+        if (mine < nblk && QG_OK(qg_in(mine * Q8_1_BYTES, Q8_1_BYTES, nblk * Q8_1_BYTES), st, 102)) {
             uint32_t* blk = reinterpret_cast<uint32_t*>(xq + mine * Q8_1_BYTES);  // 4-byte aligned
             blk[1 + sub] = o.word;
             if (sub == 0) {
@@ -67,14 +71,14 @@ int launch_quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, cu
     int64_t grid = (nblk + per_cta - 1) / per_cta;
     if (grid > (int64_t)di.sms * 16) grid = (int64_t)di.sms * 16;
     if (launch_pdl(quantize_q8_1_kernel, dim3((unsigned)grid), dim3(QUANT_THREADS), 0, s, x, ldx,
-                   static_cast<uint8_t*>(xq), M, NB) != cudaSuccess)
+                   static_cast<uint8_t*>(xq), M, NB, wait_timeout_counter()) != cudaSuccess)
         return QGEMV_CUDA_ERROR;
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
 // ---------------------------------------------------------------------------
 // RMSNorm fused with the Q8_1 quantizer ("Qwen3.6 27B Q4_0 DFlash/SYCL
-// closure", What did not clear the gate: the down-to-next-RMSNorm/Q8
+// closure", Closed or negative paths: the down-to-next-RMSNorm/Q8
 // boundary): one CTA of RMS_THREADS threads per row,
 //   S = sum_k x_k^2 in fp32: thread t adds x_k * x_k for k = t, t + 512, ...
 //       in increasing k (separate multiply and add, no contraction), then the
@@ -87,7 +91,8 @@ constexpr int RMS_THREADS = 512;
 
 __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_quantize_q8_1_kernel(const float* __restrict__ x, int64_t ldx,
                                                                           const float* __restrict__ gamma, float eps,
-                                                                          uint8_t* __restrict__ xq, int K)
+                                                                          uint8_t* __restrict__ xq, int K,
+                                                                          unsigned int* st)
 {
     pdl_launch_dependents();
     pdl_wait();
@@ -96,7 +101,9 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_quantize_q8_1_kernel(cons
     const int m = blockIdx.x, t = threadIdx.x;
     const float* xr = x + (int64_t)m * ldx;
     float s = 0.0f;
-    for (int k = t; k < K; k += RMS_THREADS) s = __fadd_rn(s, __fmul_rn(xr[k], xr[k]));
+    for (int k = t; k < K; k += RMS_THREADS)
+        if (QG_OK(qg_in((int64_t)m * ldx + k, 1, (int64_t)(gridDim.x - 1) * ldx + K), st, 201))
+            s = __fadd_rn(s, __fmul_rn(xr[k], xr[k]));
     part[t] = s;
     for (int h = RMS_THREADS / 2; h > 0; h >>= 1) {
         __syncthreads();
@@ -110,12 +117,17 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_quantize_q8_1_kernel(cons
     for (int b0 = (t >> 5) * 4; b0 < NB; b0 += (RMS_THREADS / 32) * 4) {  // warp-uniform: 4 blocks per warp step
         const int mine = b0 + (lane >> 3);
         const int b = mine < NB ? mine : NB - 1;  // spare lanes redo the last block, unwritten
-        const float4 xv = load_4_values(xr + (int64_t)b * QK + 4 * sub, vec4);
-        const float4 gv = load_4_values(gamma + (int64_t)b * QK + 4 * sub, vec4);
+        float4 xv = make_float4(0.0f, 0.0f, 0.0f, 0.0f), gv = xv;
+        if (QG_OK(qg_in((int64_t)b * QK + 4 * sub, 4, K), st, 202)) {
+            xv = load_4_values(xr + (int64_t)b * QK + 4 * sub, vec4);
+            gv = load_4_values(gamma + (int64_t)b * QK + 4 * sub, vec4);
+        }
         const float4 v = make_float4(__fmul_rn(__fmul_rn(xv.x, r), gv.x), __fmul_rn(__fmul_rn(xv.y, r), gv.y),
                                      __fmul_rn(__fmul_rn(xv.z, r), gv.z), __fmul_rn(__fmul_rn(xv.w, r), gv.w));
         const Q81Lanes o = q8_1_quantize_8lanes(v);
-        if (mine < NB) {
+        if (mine < NB &&
+            QG_OK(qg_in(((int64_t)m * NB + mine) * Q8_1_BYTES, Q8_1_BYTES, (int64_t)gridDim.x * NB * Q8_1_BYTES), st,
+                  203)) {
             uint32_t* blk = reinterpret_cast<uint32_t*>(xq + ((int64_t)m * NB + mine) * Q8_1_BYTES);
             blk[1 + sub] = o.word;
             if (sub == 0) {
@@ -131,7 +143,7 @@ int launch_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma
                                  cudaStream_t s)
 {
     if (launch_pdl(rmsnorm_quantize_q8_1_kernel, dim3(M), dim3(RMS_THREADS), 0, s, x, ldx, gamma, eps,
-                   static_cast<uint8_t*>(xq), K) != cudaSuccess)
+                   static_cast<uint8_t*>(xq), K, wait_timeout_counter()) != cudaSuccess)
         return QGEMV_CUDA_ERROR;
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
@@ -149,10 +161,12 @@ int launch_rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma
 // 2t+8, 2t+9, 16+2t, 17+2t, 24+2t, 25+2t of row g, then of row g + 8, each
 // stored as q + 128 (q ^ 0x80).  Rows past N are zero codes and zero scales.
 // One thread per (tile, block, lane); scales are raw bit copies.
-__global__ void qpack_q8_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
+__global__ void qpack_q8_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K,
+                                  unsigned int* st)
 {
     const int NB = K / QK, NJ = NB / 8;
     const int64_t T = (N + 15) / 16;
+    const int64_t canon_bytes = (int64_t)N * NB * 34, pack_bytes = T * NJ * 4352;
     const int64_t total = T * NB * 32;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -165,21 +179,26 @@ __global__ void qpack_q8_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __
         uint32_t words[4];
         for (int h = 0; h < 2; ++h) {
             const int64_t n = tau * 16 + g + 8 * h;
+            const bool in = n < N && QG_OK(qg_in((n * NB + b) * 34, 34, canon_bytes), st, 301);
             const uint8_t* q = canon + (n * NB + b) * 34 + 2;
             const int e[8] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9, 16 + 2 * t, 17 + 2 * t, 24 + 2 * t, 25 + 2 * t};
             uint32_t w0 = 0, w1 = 0;
             for (int k = 0; k < 4; ++k) {
-                w0 |= (uint32_t)((n < N ? q[e[k]] : 0) ^ 0x80u) << (8 * k);
-                w1 |= (uint32_t)((n < N ? q[e[k + 4]] : 0) ^ 0x80u) << (8 * k);
+                w0 |= (uint32_t)((in ? q[e[k]] : 0) ^ 0x80u) << (8 * k);
+                w1 |= (uint32_t)((in ? q[e[k + 4]] : 0) ^ 0x80u) << (8 * k);
             }
             words[2 * h] = w0;
             words[2 * h + 1] = w1;
         }
-        *reinterpret_cast<uint4*>(region + (p * 32 + l) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+        const int64_t ro = (tau * NJ + j) * 4352;
+        if (QG_OK(qg_in(ro + (p * 32 + l) * 16, 16, pack_bytes), st, 302))
+            *reinterpret_cast<uint4*>(region + (p * 32 + l) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
         if (l < 16) {
             const int64_t n = tau * 16 + l;
-            const uint16_t d = n < N ? *reinterpret_cast<const uint16_t*>(canon + (n * NB + b) * 34) : (uint16_t)0;
-            *reinterpret_cast<uint16_t*>(region + 4096 + (p * 16 + l) * 2) = d;
+            const bool in = n < N && QG_OK(qg_in((n * NB + b) * 34, 2, canon_bytes), st, 303);
+            const uint16_t d = in ? *reinterpret_cast<const uint16_t*>(canon + (n * NB + b) * 34) : (uint16_t)0;
+            if (QG_OK(qg_in(ro + 4096 + (p * 16 + l) * 2, 2, pack_bytes), st, 304))
+                *reinterpret_cast<uint16_t*>(region + 4096 + (p * 16 + l) * 2) = d;
         }
     }
 }
@@ -189,7 +208,7 @@ int launch_qpack_q8_0(const void* canon, void* pack, int N, int K, cudaStream_t 
     const int64_t total = (int64_t)((N + 15) / 16) * (K / QK) * 32;
     const int64_t grid = total / 256 + 1 < 65535 ? total / 256 + 1 : 65535;
     qpack_q8_0_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon), static_cast<uint8_t*>(pack),
-                                                     N, K);
+                                                     N, K, wait_timeout_counter());
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -218,7 +237,8 @@ __device__ __forceinline__ void q4_k_unpack_scale_min(const uint8_t* s, int j, u
 // [p][row] word of fifth bits (byte k bit s = value k + 4 s of block p);
 // region 2880 B.
 template <bool FIVE>
-__global__ void qpack_q4_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
+__global__ void qpack_q4_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K,
+                                  unsigned int* st)
 {
     constexpr int CB = FIVE ? 176 : 144, RB = FIVE ? 2880 : 2368, SCM = FIVE ? 2560 : 2048;
     const int NS = K / QK_K;
@@ -233,6 +253,9 @@ __global__ void qpack_q4_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
         const int64_t n = tau * 16 + r;
         uint8_t* region = pack + (tau * NS + sbi) * RB;
         const int g = r & 7, half = r >> 3;
+        // every write below falls in this tile's region, every read in row n's superblock
+        if (!QG_OK(qg_in((tau * NS + sbi) * RB, RB, T * NS * RB), st, 311)) continue;
+        if (n < N && !QG_OK(qg_in((n * NS + sbi) * CB, CB, (int64_t)N * NS * CB), st, 312)) continue;
         if (n >= N) {
             for (int p = 0; p < 8; ++p) {
                 for (int t = 0; t < 4; ++t)
@@ -276,7 +299,7 @@ int launch_qpack_q4_k(const void* canon, void* pack, int N, int K, cudaStream_t 
     const int64_t total = (int64_t)((N + 15) / 16) * (K / QK_K) * 16;
     const int64_t grid = total / 256 + 1 < 65535 ? total / 256 + 1 : 65535;
     qpack_q4_k_kernel<false><<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon),
-                                                            static_cast<uint8_t*>(pack), N, K);
+                                                            static_cast<uint8_t*>(pack), N, K, wait_timeout_counter());
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -285,14 +308,16 @@ int launch_qpack_q5_k(const void* canon, void* pack, int N, int K, cudaStream_t 
     const int64_t total = (int64_t)((N + 15) / 16) * (K / QK_K) * 16;
     const int64_t grid = total / 256 + 1 < 65535 ? total / 256 + 1 : 65535;
     qpack_q4_k_kernel<true><<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(canon),
-                                                           static_cast<uint8_t*>(pack), N, K);
+                                                           static_cast<uint8_t*>(pack), N, K, wait_timeout_counter());
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
-__global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
+__global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K,
+                                  unsigned int* st)
 {
     const Layout L = make_layout(FMT_Q4_0, N, K);
     const int64_t nblocks = (int64_t)N * L.NB;
+    const int64_t total = L.total_bytes();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = i / L.NB;
@@ -302,20 +327,24 @@ __global__ void qpack_q4_0_kernel(const uint8_t* __restrict__ canon, uint8_t* __
 #pragma unroll
         for (int k = 0; k < 4; ++k) q[k] = (uint32_t)src[1 + 2 * k] | ((uint32_t)src[2 + 2 * k] << 16);
         const BlockAddr ad = block_addr(pack, L, n, b);
-        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(ad.q)) = make_uint4(q[0], q[1], q[2], q[3]);
-        *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.d)) = src[0];
+        if (QG_OK(qg_in(ad.q - pack, 16, total), st, 321))
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(ad.q)) = make_uint4(q[0], q[1], q[2], q[3]);
+        if (QG_OK(qg_in(ad.d - pack, 2, total), st, 322)) *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.d)) = src[0];
         const int rows = L.rows_in(n / GROUP), c = b / CHUNK, nb = L.nb(c);
         if ((n % GROUP) == 0 && b % CHUNK == 0) {  // zero the group-chunk's pad bytes
             uint8_t* gc = pack + L.chunk_offset(n / GROUP, c);
-            for (int p = nb * rows * 18; p < L.chunk_bytes(rows, c); ++p) gc[p] = 0;
+            for (int p = nb * rows * 18; p < L.chunk_bytes(rows, c); ++p)
+                if (QG_OK(qg_in(gc + p - pack, 1, total), st, 323)) gc[p] = 0;
         }
     }
 }
 
-__global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K)
+__global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __restrict__ pack, int N, int K,
+                                  unsigned int* st)
 {
     const Layout L = make_layout(FMT_Q6_K, N, K);
     const int64_t nblocks = (int64_t)N * L.NB;
+    const int64_t total = L.total_bytes();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = i / L.NB;
@@ -349,15 +378,21 @@ __global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
             wh[t >> 2] |= byte << (8 * (t & 3));
         }
         const BlockAddr ad = block_addr(pack, L, n, b);
-        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(ad.q)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        *reinterpret_cast<uint2*>(const_cast<uint8_t*>(ad.qh)) = make_uint2(wh[0], wh[1]);
-        *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.sc)) =
-            (uint16_t)sb[192 + 2 * bb] | ((uint16_t)sb[192 + 2 * bb + 1] << 8);
-        if (bb == 0) *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.d)) = (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
+        if (QG_OK(qg_in(ad.q - pack, 16, total) && qg_in(ad.qh - pack, 8, total) && qg_in(ad.sc - pack, 2, total) &&
+                      qg_in(ad.d - pack, 2, total),
+                  st, 331)) {
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(ad.q)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            *reinterpret_cast<uint2*>(const_cast<uint8_t*>(ad.qh)) = make_uint2(wh[0], wh[1]);
+            *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.sc)) =
+                (uint16_t)sb[192 + 2 * bb] | ((uint16_t)sb[192 + 2 * bb + 1] << 8);
+            if (bb == 0)
+                *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(ad.d)) = (uint16_t)sb[208] | ((uint16_t)sb[209] << 8);
+        }
         const int rows = L.rows_in(n / GROUP), c = b / CHUNK, nb = L.nb(c);
         if ((n % GROUP) == 0 && b % CHUNK == 0) {  // zero the scale part's pad bytes
             uint8_t* dq = pack + L.chunk_offset(n / GROUP, c) + rows * nb * 26;
-            for (int p = rows * (nb / 8) * 2; p < pad16(rows * (nb / 8) * 2); ++p) dq[p] = 0;
+            for (int p = rows * (nb / 8) * 2; p < pad16(rows * (nb / 8) * 2); ++p)
+                if (QG_OK(qg_in(dq + p - pack, 1, total), st, 332)) dq[p] = 0;
         }
     }
 }
@@ -375,7 +410,8 @@ int launch_qpack_q4_0(const void* canon, void* pack, int N, int K, cudaStream_t 
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     const int64_t nblocks = (int64_t)N * (K / QK);
     qpack_q4_0_kernel<<<grid_for(nblocks, 256, di.sms), 256, 0, s>>>(static_cast<const uint8_t*>(canon),
-                                                                     static_cast<uint8_t*>(pack), N, K);
+                                                                     static_cast<uint8_t*>(pack), N, K,
+                                                                     wait_timeout_counter());
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -385,7 +421,8 @@ int launch_qpack_q6_k(const void* canon, void* pack, int N, int K, cudaStream_t 
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     const int64_t nblocks = (int64_t)N * (K / QK);
     qpack_q6_k_kernel<<<grid_for(nblocks, 256, di.sms), 256, 0, s>>>(static_cast<const uint8_t*>(canon),
-                                                                     static_cast<uint8_t*>(pack), N, K);
+                                                                     static_cast<uint8_t*>(pack), N, K,
+                                                                     wait_timeout_counter());
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 
@@ -403,7 +440,7 @@ constexpr int ARGMAX_THREADS = 256;
 template <int M>
 __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float* __restrict__ y, int64_t ldy,
                                                                      int32_t* __restrict__ ids, Top1Workspace* ws,
-                                                                     int N)
+                                                                     int N, unsigned int* st)
 {
     __shared__ unsigned long long s_red[ARGMAX_THREADS / 32][M];
     __shared__ int s_last;
@@ -416,12 +453,16 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float
     const bool vec4 = ((reinterpret_cast<uintptr_t>(y) | ((uintptr_t)ldy * 4)) & 15u) == 0;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t extent = (int64_t)(M - 1) * ldy + N;  // elements of y read
     if (vec4) {
         const int64_t n4 = N / 4;
         for (int64_t q = tid; q < n4; q += nthreads) {
             float4 v[M];
 #pragma unroll
-            for (int m = 0; m < M; ++m) v[m] = __ldg(reinterpret_cast<const float4*>(y + (int64_t)m * ldy) + q);
+            for (int m = 0; m < M; ++m)
+                v[m] = QG_OK(qg_in((int64_t)m * ldy + 4 * q, 4, extent), st, 401)
+                           ? __ldg(reinterpret_cast<const float4*>(y + (int64_t)m * ldy) + q)
+                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const int n = (int)(4 * q);
@@ -439,6 +480,7 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float
         for (int64_t n = 4 * n4 + tid; n < N; n += nthreads) {
 #pragma unroll
             for (int m = 0; m < M; ++m) {
+                if (!QG_OK(qg_in((int64_t)m * ldy + n, 1, extent), st, 402)) continue;
                 const unsigned long long c = top1_key(__ldg(y + (int64_t)m * ldy + n), (int)n);
                 k[m] = c > k[m] ? c : k[m];
             }
@@ -447,6 +489,7 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_rows_kernel(const float
         for (int64_t n = tid; n < N; n += nthreads) {
 #pragma unroll
             for (int m = 0; m < M; ++m) {
+                if (!QG_OK(qg_in((int64_t)m * ldy + n, 1, extent), st, 402)) continue;
                 const unsigned long long c = top1_key(__ldg(y + (int64_t)m * ldy + n), (int)n);
                 k[m] = c > k[m] ? c : k[m];
             }
@@ -480,7 +523,8 @@ template <int M>
 static cudaError_t launch_argmax_m(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int N, int grid,
                                    cudaStream_t s)
 {
-    return launch_pdl(argmax_rows_kernel<M>, dim3(grid), dim3(ARGMAX_THREADS), 0, s, y, ldy, ids, ws, N);
+    return launch_pdl(argmax_rows_kernel<M>, dim3(grid), dim3(ARGMAX_THREADS), 0, s, y, ldy, ids, ws, N,
+                      wait_timeout_counter());
 }
 
 int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace* ws, int M, int N, cudaStream_t s)
@@ -512,9 +556,11 @@ int launch_argmax_rows(const float* y, int64_t ldy, int32_t* ids, Top1Workspace*
 
 template <int FMT>
 __global__ void block_dots_kernel(const void* __restrict__ w_pack, const uint8_t* __restrict__ xq,
-                                  int32_t* __restrict__ out, int M, int NB, int N)
+                                  int32_t* __restrict__ out, int M, int NB, int N, unsigned int* st)
 {
     const int64_t total = (int64_t)M * N * NB;
+    const Layout L = make_layout(FMT, N, NB * QK);
+    const int64_t wbytes = L.total_bytes();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int b = (int)(i % NB);
@@ -522,9 +568,16 @@ __global__ void block_dots_kernel(const void* __restrict__ w_pack, const uint8_t
         const int n = (int)(mn % N), m = (int)(mn / N);
         uint4 lo, hi;
         uint2 meta;
+        if (!QG_OK(qg_in(((int64_t)m * NB + b) * Q8_1_BYTES, Q8_1_BYTES, (int64_t)M * NB * Q8_1_BYTES), st, 501))
+            continue;
         act_from_q8_1<FMT>(xq + ((int64_t)m * NB + b) * Q8_1_BYTES, lo, hi, meta);
         uint32_t w[8];
-        const BlockAddr ad = block_addr(w_pack, make_layout(FMT, N, NB * QK), n, b);
+        const BlockAddr ad = block_addr(w_pack, L, n, b);
+        const uint8_t* w0 = static_cast<const uint8_t*>(w_pack);
+        if (!QG_OK(qg_in(ad.q - w0, 16, wbytes) && (FMT == FMT_Q4_0 || (qg_in(ad.qh - w0, 8, wbytes) &&
+                                                                      qg_in(ad.sc - w0, 2, wbytes))),
+                   st, 502))
+            continue;
         if (FMT == FMT_Q4_0) {
             q4_0_unpack(*reinterpret_cast<const uint4*>(ad.q), w);
             out[i] = q4_0_dot(w, lo, hi, (int)meta.y);
@@ -543,9 +596,11 @@ int launch_block_dots(int fmt, const void* w_pack, const void* xq, int32_t* out,
     const int64_t total = (int64_t)M * N * NB;
     const int grid = grid_for(total, 256, di.sms);
     if (fmt == FMT_Q4_0)
-        block_dots_kernel<FMT_Q4_0><<<grid, 256, 0, s>>>(w_pack, static_cast<const uint8_t*>(xq), out, M, NB, N);
+        block_dots_kernel<FMT_Q4_0><<<grid, 256, 0, s>>>(w_pack, static_cast<const uint8_t*>(xq), out, M, NB, N,
+                                                         wait_timeout_counter());
     else
-        block_dots_kernel<FMT_Q6_K><<<grid, 256, 0, s>>>(w_pack, static_cast<const uint8_t*>(xq), out, M, NB, N);
+        block_dots_kernel<FMT_Q6_K><<<grid, 256, 0, s>>>(w_pack, static_cast<const uint8_t*>(xq), out, M, NB, N,
+                                                         wait_timeout_counter());
     return cudaGetLastError() == cudaSuccess ? QGEMV_OK : QGEMV_CUDA_ERROR;
 }
 

@@ -49,6 +49,9 @@ bool wait_timeouts_pending();
 // A test-only request (qgemv_debug_drop_next_copy) taken by the next launch of
 // the small-M Q4_0 kernel: 1 once, then 0.
 int take_drop_request();
+// Debug build only (test hook): whether the next ring-kernel launch should
+// move one output store out of its extent, for its bounds check to catch.
+int take_plant_request();
 
 // Largest multiple-of-32 block chunk of activation that fits in shared memory
 // next to `extra` bytes (all of K when it fits).
@@ -97,11 +100,11 @@ inline int ring_parts(int64_t groups_per_cta, int nch, int max_warps, bool top1)
 
 // N2 > 0: a second weight of N2 rows and the same K, whose row groups the
 // ring kernel takes after the first's.
-template <int FMT, int M, bool TOP1, bool PAIR = false>
+template <int FMT, int M, bool TOP1, bool PAIR = false, bool TOPK = false>
 MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N, int N2 = 0)
 {
     const Layout L = make_layout(FMT, N, K);
-    const int max_warps = MmvqThreads<FMT, M, TOP1>::value / 32;
+    const int max_warps = MmvqThreads<FMT, M, TOP1, TOPK>::value / 32;
     MmvqPlan p{};
     const int64_t n_groups = L.n_groups + (N2 > 0 ? ((int64_t)N2 + GROUP - 1) / GROUP : 0);
     p.grid = n_groups < di.sms ? (int)n_groups : di.sms;
@@ -110,7 +113,7 @@ MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N, int N2 = 0)
     const int64_t items = per_cta * p.parts;
     p.warps = items < max_warps ? (int)items : max_warps;
     const size_t act = RingAct<FMT, M>::bytes(L.NB);
-    const size_t extra = ring_extra_bytes<M, TOP1, PAIR>((int)per_cta, p.parts, max_warps);
+    const size_t extra = ring_extra_bytes<M, TOP1, PAIR, TOPK>((int)per_cta, p.parts, max_warps);
     const size_t stage = (size_t)L.chunk_bytes(GROUP, 0) + 8;  // a group-chunk and its mbarrier
     const size_t fixed = act + extra + 128;
     long long s = fixed < (size_t)di.smem_optin ? (long long)(((size_t)di.smem_optin - fixed) / (p.warps * stage)) : 0;
@@ -142,25 +145,33 @@ MmvqPlan mmvq_plan(const DeviceInfo& di, int K, int N, int N2 = 0)
     return p;
 }
 
-template <int FMT, int M, bool TOP1, bool PAIR, bool RES = false>
+// The most CTAs a top-k launch may have: its workspace holds one list per CTA.
+constexpr int TOPK_MAX_CTAS = 256;
+
+template <int FMT, int M, bool TOP1, bool PAIR, bool RES = false, bool TOPK = false>
 int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
 {
     const DeviceInfo di = device_info();
     if (di.sms <= 0) return QGEMV_CUDA_ERROR;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QGEMV_CUDA_ERROR;
-    const MmvqPlan p = mmvq_plan<FMT, M, TOP1, PAIR>(di, a.K, a.N, PAIR ? a.N2 : 0);
+    const MmvqPlan p = mmvq_plan<FMT, M, TOP1, PAIR, TOPK>(di, a.K, a.N, PAIR ? a.N2 : 0);
     if (p.smem > (size_t)di.smem_optin) return QGEMV_UNSUPPORTED_SHAPE;
+    // top-k runs on the ring kernel only, with one list per CTA in the workspace
+    if (TOPK && (!p.ring || p.grid > TOPK_MAX_CTAS)) return QGEMV_UNSUPPORTED_SHAPE;
     a.KC = p.KC;
     a.stages = p.stages;
     a.parts = p.parts;
+#ifdef QGEMV_BOUNDS_CHECK
+    a.plant_bad_store = p.ring && !TOP1 ? take_plant_request() : 0;
+#endif
     // Opt in to the device's full shared memory once per device and kernel
     // (call_once: concurrent first calls from several host threads are safe).
     static std::once_flag once_ring[64], once_lock[64];
     static bool ok_ring[64], ok_lock[64];
     static unsigned int* timeouts[64];
     if (p.ring) {
-        auto kern = mmvq_ring_kernel<FMT, M, TOP1, PAIR, RES>;
+        auto kern = mmvq_ring_kernel<FMT, M, TOP1, PAIR, RES, TOPK>;
         std::call_once(once_ring[dev], [&]() {
             timeouts[dev] = wait_timeout_counter();
             ok_ring[dev] =
@@ -171,7 +182,7 @@ int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
         if (!ok_ring[dev]) return QGEMV_CUDA_ERROR;
         if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a, timeouts[dev]) != cudaSuccess)
             return QGEMV_CUDA_ERROR;
-    } else {
+    } else if constexpr (!TOPK) {
         auto kern = mmvq_lockstep_kernel<FMT, M, TOP1, RES>;
         std::call_once(once_lock[dev], [&]() {
             ok_lock[dev] =
@@ -179,7 +190,9 @@ int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
             if (!ok_lock[dev]) cudaGetLastError();
         });
         if (!ok_lock[dev]) return QGEMV_CUDA_ERROR;
-        if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a) != cudaSuccess) return QGEMV_CUDA_ERROR;
+        unsigned int* status = wait_timeout_counter();
+        if (launch_pdl(kern, dim3(p.grid), dim3(p.warps * 32), p.smem, s, a, status) != cudaSuccess)
+            return QGEMV_CUDA_ERROR;
         if (PAIR) {  // the lock-step kernel takes the second weight in a launch of its own
             MmvqArgs b = a;
             b.w_pack = a.w_pack2;
@@ -190,7 +203,7 @@ int launch_mmvq_pm(MmvqArgs a, cudaStream_t s)
             b.N2 = 0;
             const MmvqPlan p2 = mmvq_plan<FMT, M, TOP1>(di, b.K, b.N);
             b.KC = p2.KC;
-            if (launch_pdl(kern, dim3(p2.grid), dim3(p2.warps * 32), p2.smem, s, b) != cudaSuccess)
+            if (launch_pdl(kern, dim3(p2.grid), dim3(p2.warps * 32), p2.smem, s, b, status) != cudaSuccess)
                 return QGEMV_CUDA_ERROR;
         }
     }
@@ -232,6 +245,10 @@ int launch_qpack_q4_k(const void* canon, void* pack, int N, int K, cudaStream_t 
 int launch_mmvq_q5_k(const MmvqArgs& a, int M, cudaStream_t s, int* info = nullptr);
 int launch_qpack_q5_k(const void* canon, void* pack, int N, int K, cudaStream_t s);
 int launch_lmhead_q6_k(const MmvqArgs& a, int M, cudaStream_t s);
+// The top-k form (a.topk in 1..TOPK_MAX, a.topk_lists sized for TOPK_MAX_CTAS
+// lists); QGEMV_UNSUPPORTED_SHAPE where the activation does not fit the ring
+// kernel's shared memory.
+int launch_lmhead_q6_k_topk(const MmvqArgs& a, int M, cudaStream_t s);
 // The launch plan of the fused LM-head kernel: {1 ring / 0 lock-step, grid,
 // warps, ring stages}.
 int lmhead_q6_k_plan(int M, int K, int N, int* info);

@@ -37,11 +37,11 @@ constexpr int MMVQ_MAX_WARPS = MMVQ_MAX_THREADS / 32;
 // R x M partial sums and the unpacked weights fit in 128 registers (the
 // top-1 forms at M = 4 and 6 included: 112 and 127 registers, and 16 warps
 // made the six-row fused head 6 us faster than the unfused path, where 12
-// had left it level); 12 warps (168 registers) for M = 7, 8, which would
-// spill; 8 warps (255 registers) for M > 8.
-template <int FMT, int M, bool TOP1>
+// had left it level); 12 warps (168 registers) for M = 7, 8, and for the
+// top-k form from M = 3, which would spill; 8 warps (255 registers) for M > 8.
+template <int FMT, int M, bool TOP1, bool TOPK = false>
 struct MmvqThreads {
-    static constexpr bool wide = FMT == FMT_Q4_0 ? (M == 7 || M == 8) : (M == 7 || M == 8);
+    static constexpr bool wide = M == 7 || M == 8 || (TOPK && M >= 3);
     static constexpr int value = M > 8 ? 256 : (wide ? 384 : 512);
 };
 
@@ -433,8 +433,18 @@ struct MmvqArgs {
     const uint8_t* xq;  // Q8_1 [M][NB]; null (top-1 kernels only): quantize x in the kernel
     const float* x;     // fp32 [M][ldx] (when xq is null); the residual of a RES kernel
     int64_t ldx;
-    float* y;
-    int64_t ldy;
+    union {
+        struct {
+            float* y;  // the output [M][ldy] (kernels that write one)
+            int64_t ldy;
+        };
+        struct {
+            // top-k kernels (which write no output): each CTA's k best keys
+            // per row, [grid][M][k], merged by the last CTA; and k
+            unsigned long long* topk_lists;
+            int64_t topk;
+        };
+    };
     int K, N;
     // optional second weight of the same K against the same activation (a
     // pair such as gate and up): its row groups follow the first's
@@ -448,10 +458,41 @@ struct MmvqArgs {
     int32_t* ids;
     // candidate-max (top-1 kernels, all optional): the top value of each row,
     // and the logit of a given candidate id per row
-    float* top_vals;
+    float* top_vals;  // (top-k kernels: [M][k], as ids)
     const int32_t* cand;
     float* cand_vals;
+#ifdef QGEMV_BOUNDS_CHECK
+    // test hook: move the first stores of CTA 0, warp 0 out of their extent,
+    // for the bounds check to catch
+    int plant_bad_store;
+#endif
 };
+
+// Debug-build checks of the ring and lock-step kernels' computed accesses.
+// A weight copy must lie in the pack of the first weight or, for a pair, of
+// the second; an output (m, n) in the [M][ldy] output of its weight.
+__device__ __forceinline__ bool pack_range_ok(const MmvqArgs& a, int fmt, const uint8_t* src, uint32_t bytes)
+{
+    const int64_t o0 = (int64_t)(reinterpret_cast<uintptr_t>(src) - reinterpret_cast<uintptr_t>(a.w_pack));
+    if (qg_in(o0, bytes, make_layout(fmt, a.N, a.K).total_bytes())) return true;
+    if (!a.w_pack2) return false;
+    const int64_t o1 = (int64_t)(reinterpret_cast<uintptr_t>(src) - reinterpret_cast<uintptr_t>(a.w_pack2));
+    return qg_in(o1, bytes, make_layout(fmt, a.N2, a.K).total_bytes());
+}
+
+__device__ __forceinline__ bool store_ok(const MmvqArgs& a, const float* y, int m, int M, int64_t n)
+{
+    const int Ny = (a.y2 && y == a.y2) ? a.N2 : a.N;
+    return m >= 0 && m < M && n >= 0 && n < Ny;
+}
+
+// Bytes of dynamic shared memory the kernel was launched with.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes()
+{
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
 
 // Output store of a plain MMVQ; the residual instantiation (RES) adds the
 // residual, which such calls pass in the fp32-activation field x (row stride
@@ -467,7 +508,7 @@ __device__ __forceinline__ void mmvq_store(const MmvqArgs& a, float* y, int m, i
 // false) or fold their keys into the warp's running best per row (TOP1).
 template <int M, int R, bool TOP1, bool RES = false>
 __device__ __forceinline__ void finish_rowgroup(const MmvqArgs& a, int n0, float (&acc)[R][M], int lane,
-                                                unsigned long long* wk, unsigned long long& best)
+                                                unsigned long long* wk, unsigned long long& best, unsigned int* status)
 {
     constexpr int V = R * M;
     constexpr int P = next_pow2(V);
@@ -484,7 +525,8 @@ __device__ __forceinline__ void finish_rowgroup(const MmvqArgs& a, int n0, float
                 if (vi < V) {
                     const int r = vi / M, m = vi - (vi / M) * M;
                     const int n = n0 + r;
-                    if (n < a.N) mmvq_store<RES>(a, a.y, m, n, v[j]);
+                    if (n < a.N && QG_OK(store_ok(a, a.y, m, M, n), status, 720))
+                        mmvq_store<RES>(a, a.y, m, n, v[j]);
                 }
             }
         }
@@ -543,6 +585,64 @@ __device__ __forceinline__ void top1_finish(const MmvqArgs& a, unsigned long lon
             if (a.top_vals) a.top_vals[threadIdx.x] = top1_key_to_value(k);
         }
         if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Top-k on the same ordered keys.  Keys are unique (the id is part of the
+// key), so the k largest keys of a row form one set whatever the order in
+// which they are kept, merged or selected: the result is deterministic.
+// 0 is "no key" (a NaN, or no entry), below every real key.  Each warp keeps
+// one list per row, each CTA merges its warps' lists, and the last CTA
+// merges the CTAs' lists.
+// ---------------------------------------------------------------------------
+
+constexpr int TOPK_MAX = 8;
+
+// Whole warp.  Each lane offers NR keys (0: none), key j for row row[j], to
+// the warp's lists wl[row * TOPK_MAX + i], i < k, kept in descending order
+// (0-filled).  A key enters only if it beats the row's k-th key; such keys
+// are taken one at a time, the k lanes of the list shifting it down by one.
+template <int NR>
+__device__ __forceinline__ void topk_offer(unsigned long long* wl, int k, const unsigned long long (&key)[NR],
+                                           const int (&row)[NR], int lane)
+{
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        unsigned int mask = __ballot_sync(0xffffffffu, key[j] > wl[row[j] * TOPK_MAX + k - 1]);
+        while (mask) {
+            const int src = __ffs(mask) - 1;
+            mask &= mask - 1;
+            const unsigned long long kk = __shfl_sync(0xffffffffu, key[j], src);
+            unsigned long long* list = wl + __shfl_sync(0xffffffffu, row[j], src) * TOPK_MAX;
+            const unsigned long long cur = lane < k ? list[lane] : 0ull;
+            // entries that stay above it (the threshold may have risen since
+            // the ballot: then pos == k and nothing moves)
+            const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && cur > kk));
+            const unsigned long long up = __shfl_up_sync(0xffffffffu, cur, 1);
+            if (lane < k && lane >= pos) list[lane] = lane == pos ? kk : up;
+            __syncwarp();
+        }
+    }
+}
+
+// Whole warp: the k largest of `count` keys load(e), e < count, handed to
+// out(r, key) by lane 0 in descending order (r = 0..k-1); when fewer than k
+// keys are nonzero the remaining picks are 0.  k rounds, each a strided scan
+// for the largest key below the previous pick and a warp maximum.
+template <class Load, class Out>
+__device__ __forceinline__ void topk_select(int count, int k, int lane, Load load, Out out)
+{
+    unsigned long long prev = ~0ull;
+    for (int r = 0; r < k; ++r) {
+        unsigned long long best = 0ull;
+        for (int e = lane; e < count; e += 32) {
+            const unsigned long long x = load(e);
+            if (x < prev && x > best) best = x;
+        }
+        best = warp_max_u64(best);
+        if (lane == 0) out(r, best);
+        prev = best;
     }
 }
 
@@ -795,9 +895,11 @@ __device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q6_K>& H, const ui
     }
 }
 
-template <int FMT, int M, bool TOP1, bool PAIR, bool RES = false>
-__global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
+template <int FMT, int M, bool TOP1, bool PAIR, bool RES = false, bool TOPK = false>
+__global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1, TOPK>::value, 1)
+    mmvq_ring_kernel(const MmvqArgs a, unsigned int* timeouts)
 {
+    static_assert(!TOPK || (TOP1 && !PAIR && !RES), "top-k is a top-1 kernel of one weight");
     constexpr int R = R_ROWS;
     constexpr int V = R * M;              // sums per row group
     constexpr int NRED = (V + 31) / 32;   // reduced sums per lane
@@ -843,16 +945,30 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
     int* s_last = reinterpret_cast<int*>(s_best + MAX_M);
     // top-1: running key of each reduced sum a lane holds, [NRED][W * 32]
     unsigned long long* s_lane_best = reinterpret_cast<unsigned long long*>(s_best + MAX_M + 2);
+    // top-k: the warps' lists, [W][M][TOPK_MAX]
+    unsigned long long* s_topk = s_lane_best + (size_t)NRED * W * 32;
+    const int KT = TOPK ? (int)a.topk : 0;  // k of the top-k
     static_assert(Act::META % 8 == 0 && (V * sizeof(float)) % 8 == 0, "ring shared-memory alignment");
 
     uint64_t* wbar = bars + warp * S;
     uint8_t* wring = rings + (size_t)warp * S * CB;
     const uint64_t pol = l2_evict_first_policy();
+#ifdef QGEMV_BOUNDS_CHECK
+    {
+        // (debug build: the layout above must end within the launch's shared memory)
+        const uint8_t* end = TOP1 ? reinterpret_cast<const uint8_t*>(s_topk + (TOPK ? (size_t)W * M * TOPK_MAX : 0))
+                                  : reinterpret_cast<const uint8_t*>(part + (P > 1 ? (size_t)ng * P * V : 0));
+        if (!QG_OK(end - smem <= (ptrdiff_t)dynamic_smem_bytes() && warp < W, timeouts, 610)) return;
+    }
+#endif
 
     if (TOP1) {
         if (threadIdx.x < MAX_M) s_best[threadIdx.x] = 0ull;
 #pragma unroll
         for (int j = 0; j < NRED; ++j) s_lane_best[j * blockDim.x + threadIdx.x] = 0ull;
+    }
+    if (TOPK) {
+        for (int i = lane; i < M * TOPK_MAX; i += 32) s_topk[(size_t)warp * M * TOPK_MAX + i] = 0ull;
     }
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&wbar[s], 1);
@@ -907,8 +1023,10 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
         uint64_t* bar = wbar + iss_slot;
         if (lane == 0) {
             fence_proxy_async();
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(wring + (size_t)iss_slot * CB, src, bytes, bar, pol_u);
+            // (debug build: a copy outside the packs is skipped, its stage completing empty)
+            const bool ok = QG_OK(pack_range_ok(a, FMT, src, bytes) && bytes <= CB, timeouts, 601);
+            mbar_arrive_expect_tx(bar, ok ? bytes : 0u);
+            if (ok) bulk_g2s(wring + (size_t)iss_slot * CB, src, bytes, bar, pol_u);
         }
         ++issued;
         if (++iss_slot == S) iss_slot = 0;
@@ -929,8 +1047,9 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
         uint64_t* bar = wbar + iss_slot;
         if (lane == 0) {
             fence_proxy_async();
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(wring + (size_t)iss_slot * CB, src, bytes, bar, pol_u);
+            const bool ok = QG_OK(pack_range_ok(a, FMT, src, bytes) && bytes <= CB, timeouts, 602);
+            mbar_arrive_expect_tx(bar, ok ? bytes : 0u);
+            if (ok) bulk_g2s(wring + (size_t)iss_slot * CB, src, bytes, bar, pol_u);
         }
         ++issued;
         if (++iss_slot == S) iss_slot = 0;
@@ -941,7 +1060,7 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
         RingStream pf = k;
         for (int j = 0; j < S - 1 + RING_PREFETCH_JOBS && pf.it < n_items; ++j) {
             const uint32_t bytes = pf.c == nch - 1 ? pf.cbl : pf.cbr;
-            bulk_prefetch_l2(pf.src, bytes);
+            if (QG_OK(pack_range_ok(a, FMT, pf.src, bytes), timeouts, 603)) bulk_prefetch_l2(pf.src, bytes);
             pf.src += bytes;
             if (++pf.c == pf.c1) ring_stream_at<PAIR>(pf, sp, wbase, L, g0, n_items, P, CB, CBL, GB, pf.it + W);
         }
@@ -970,7 +1089,8 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             if (PAIR ? sp->rows(ga) == GROUP : ga <= last_whole) {
                 const int ca = P == 1 ? 0 : pa * nch / P, cb = P == 1 ? nch : (pa + 1) * nch / P;
                 const uint32_t span = (uint32_t)(cb - ca) * CB - (cb == nch ? CB - CBL : 0u);
-                bulk_prefetch_l2((PAIR ? sp->group_src(ga, GB) : wbase + ga * GB) + (int64_t)ca * CB, span);
+                const uint8_t* ps = (PAIR ? sp->group_src(ga, GB) : wbase + ga * GB) + (int64_t)ca * CB;
+                if (QG_OK(pack_range_ok(a, FMT, ps, span), timeouts, 604)) bulk_prefetch_l2(ps, span);
             }
         }
         const int64_t g = g0 + gl;
@@ -1015,8 +1135,25 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
 
         float v[NRED];
         ring_reduce<M, R>(acc, v, lane);
+        if (TOPK) {
+            // (P == 1 and one weight here)
+            unsigned long long key[NRED];
+            int row[NRED];
+#pragma unroll
+            for (int j = 0; j < NRED; ++j) {
+                const int vi = ring_value_index<V>(j, lane);
+                const int rr = vi / M, m = vi - rr * M;
+                const bool own = ring_value_owner<V>(j, lane) && rr < rows;
+                const int n = (int)(g * GROUP) + rr;
+                key[j] = own ? top1_key(v[j], n) : 0ull;
+                row[j] = own ? m : 0;
+                if (own && a.cand_vals && n == a.cand[m]) a.cand_vals[m] = v[j];
+            }
+            topk_offer<NRED>(s_topk + (size_t)warp * M * TOPK_MAX, KT, key, row, lane);
+        }
 #pragma unroll
         for (int j = 0; j < NRED; ++j) {
+            if (TOPK) break;
             const int vi = ring_value_index<V>(j, lane);
             if (!ring_value_owner<V>(j, lane)) continue;
             if (P > 1) {
@@ -1033,7 +1170,12 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
                     if (key > b) b = key;
                     if (a.cand_vals && n == a.cand[m]) a.cand_vals[m] = v[j];
                 } else {
-                    mmvq_store<RES>(a, PAIR ? sp->y_of(g) : a.y, m, n, v[j]);
+                    float* y = PAIR ? sp->y_of(g) : a.y;
+                    int64_t ns = n;
+#ifdef QGEMV_BOUNDS_CHECK
+                    if (a.plant_bad_store && blockIdx.x == 0 && warp == 0 && it == 0) ns += a.N;
+#endif
+                    if (QG_OK(store_ok(a, y, m, M, ns), timeouts, 620)) mmvq_store<RES>(a, y, m, ns, v[j]);
                 }
             }
         }
@@ -1064,11 +1206,94 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
             if (rr < (PAIR ? sp->rows(g) : L.rows_in(g))) {
                 const int64_t n = (PAIR ? sp->local(g) : g) * GROUP + rr;
                 if (TOP1) atomicMax(&s_best[m], top1_key(sum, (int)n));
-                else mmvq_store<RES>(a, PAIR ? sp->y_of(g) : a.y, m, n, sum);
+                else if (QG_OK(store_ok(a, PAIR ? sp->y_of(g) : a.y, m, M, n), timeouts, 621))
+                    mmvq_store<RES>(a, PAIR ? sp->y_of(g) : a.y, m, n, sum);
             }
         }
     }
-    if (TOP1) {
+    if (TOPK) {
+        __syncthreads();  // every warp's lists are final
+        // this CTA's k best keys per row, from the warps' lists
+        for (int m = warp; m < M; m += W) {
+            unsigned long long* dst = a.topk_lists + ((size_t)blockIdx.x * M + m) * KT;
+            topk_select(
+                W * KT, KT, lane,
+                [&](int e) {
+                    const int w = e / KT;
+                    return s_topk[((size_t)w * M + m) * TOPK_MAX + (e - w * KT)];
+                },
+                [&](int r, unsigned long long key) { dst[r] = key; });
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const unsigned prev = atomicAdd(&a.ws->done, 1u);
+            *s_last = prev == gridDim.x - 1;
+        }
+        __syncthreads();
+        if (*s_last) {
+            __threadfence();
+            // Merge the CTAs' lists.  Each row's G k keys are copied (all the
+            // loads in flight at once) into its slice of the rings and the
+            // activation tile, both free now.  A key of the row's top k is in
+            // its CTA's list and is at least t0 = the largest k-th key of any
+            // list (that list alone holds k keys >= t0): those keys are
+            // compacted in place and the k largest picked from them.  Should
+            // the slices not fit, the k largest are picked from the lists in
+            // global memory directly.
+            const int G = gridDim.x;
+            const unsigned long long* lists = a.topk_lists;
+            const int total = G * KT;
+            unsigned long long* region = reinterpret_cast<unsigned long long*>(rings);
+            const bool fits = (size_t)M * total * 8 <= (size_t)(t.meta - rings);
+            for (int m = warp; m < M; m += W) {
+                auto emit = [&](int r, unsigned long long key) {
+                    a.ids[m * KT + r] = key ? top1_key_to_id(key) : -1;
+                    if (a.top_vals) a.top_vals[m * KT + r] = key ? top1_key_to_value(key) : __int_as_float(0x7fffffff);
+                };
+                if (!fits) {
+                    topk_select(
+                        total, KT, lane,
+                        [&](int e) {
+                            const int c = e / KT;
+                            return __ldcg(lists + ((size_t)c * M + m) * KT + (e - c * KT));
+                        },
+                        emit);
+                    continue;
+                }
+                unsigned long long* buf = region + (size_t)m * total;
+#pragma unroll 4
+                for (int e = lane; e < total; e += 32) {
+                    const int c = e / KT;
+                    buf[e] = __ldcg(lists + ((size_t)c * M + m) * KT + (e - c * KT));
+                }
+                __syncwarp();
+                unsigned long long t0 = 0ull;
+                for (int c = lane; c < G; c += 32) {
+                    const unsigned long long x = buf[c * KT + KT - 1];
+                    t0 = x > t0 ? x : t0;
+                }
+                t0 = warp_max_u64(t0);
+                int cnt = 0;
+                for (int e0 = 0; e0 < total; e0 += 32) {
+                    // in place: a key moves only down to an index already read
+                    const int e = e0 + lane;
+                    const unsigned long long x = e < total ? buf[e] : 0ull;
+                    const bool take = x != 0ull && x >= t0;
+                    const unsigned int bal = __ballot_sync(0xffffffffu, take);
+                    __syncwarp();
+                    if (take) buf[cnt + __popc(bal & ((1u << lane) - 1u))] = x;
+                    cnt += __popc(bal);
+                    __syncwarp();
+                }
+                topk_select(cnt, KT, lane, [&](int e) { return buf[e]; }, emit);
+                __syncwarp();
+            }
+            if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
+        }
+    }
+    if (TOP1 && !TOPK) {
         if (P == 1) {
 #pragma unroll
             for (int j = 0; j < NRED; ++j) {
@@ -1099,13 +1324,14 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_ring
 
 // Shared memory of the ring kernel besides the rings, their mbarriers and
 // the tile.
-template <int M, bool TOP1, bool PAIR>
+template <int M, bool TOP1, bool PAIR, bool TOPK = false>
 inline size_t ring_extra_bytes(int max_groups_per_cta, int P, int warps)
 {
     const size_t streams = (PAIR ? sizeof(RowSpace) : 0) + (size_t)warps * sizeof(RingStream);
     const size_t part = P > 1 ? (size_t)max_groups_per_cta * P * R_ROWS * M * sizeof(float) : 0;
     const size_t nred = (R_ROWS * M + 31) / 32;
-    return streams + part + (TOP1 ? (size_t)(MAX_M + 2) * 8 + nred * warps * 32 * 8 : 0);
+    return streams + part + (TOP1 ? (size_t)(MAX_M + 2) * 8 + nred * warps * 32 * 8 : 0) +
+           (TOPK ? (size_t)warps * M * TOPK_MAX * 8 : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1116,7 +1342,8 @@ inline size_t ring_extra_bytes(int max_groups_per_cta, int P, int warps)
 // ---------------------------------------------------------------------------
 
 template <int FMT, int M, bool TOP1, bool RES = false>
-__global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lockstep_kernel(const MmvqArgs a)
+__global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1)
+    mmvq_lockstep_kernel(const MmvqArgs a, unsigned int* status)
 {
     pdl_launch_dependents();
     pdl_wait();
@@ -1163,6 +1390,11 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lock
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const BlockAddr ad = block_addr(a.w_pack, L, rows[r], b);
+                        if (!QG_OK(pack_range_ok(a, FMT, ad.q, 16) && pack_range_ok(a, FMT, ad.d, 2), status, 701)) {
+                            w16[r] = make_uint4(0u, 0u, 0u, 0u);
+                            dw[r] = 0.0f;
+                            continue;
+                        }
                         w16[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.q));
                         dw[r] = __half2float(__ushort_as_half(ld_stream_u16(ad.d)));
                     }
@@ -1175,6 +1407,15 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lock
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const BlockAddr ad = block_addr(a.w_pack, L, rows[r], b);
+                        if (!QG_OK(pack_range_ok(a, FMT, ad.q, 16) && pack_range_ok(a, FMT, ad.qh, 8) &&
+                                       pack_range_ok(a, FMT, ad.sc, 2) && pack_range_ok(a, FMT, ad.d, 2),
+                                   status, 702)) {
+                            ql[r] = make_uint4(0u, 0u, 0u, 0u);
+                            qh[r] = make_uint2(0u, 0u);
+                            sc[r] = 0u;
+                            dw[r] = 0.0f;
+                            continue;
+                        }
                         ql[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.q));
                         qh[r] = ld_stream_v2(reinterpret_cast<const uint2*>(ad.qh));
                         sc[r] = ld_stream_u16(ad.sc);
@@ -1185,7 +1426,8 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1) mmvq_lock
             }
         }
         if (active)
-            finish_rowgroup<M, R, TOP1, RES>(a, (int)(g * GROUP), acc, lane, s_keys + warp * TOP1_GROUP_KEYS, best);
+            finish_rowgroup<M, R, TOP1, RES>(a, (int)(g * GROUP), acc, lane, s_keys + warp * TOP1_GROUP_KEYS, best,
+                                             status);
     }
     if (TOP1) top1_finish<M>(a, s_best, s_last, best, lane, warp, W);
 }

@@ -318,6 +318,9 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
     const int n_jobs = j1 - j0;
     const QmSmem sl = qm_smem(M, S, JB, TL, a.nkb_max, C > 1 ? a.out_tiles : 0);
+    // (debug build: the layout must fit the launch's shared memory; every CTA
+    // of a cluster decides alike)
+    if (!QG_OK(sl.bytes <= dynamic_smem_bytes(), timeouts, 910)) return;
     float* outb = reinterpret_cast<float*>(smem + sl.out);
     int* tab = reinterpret_cast<int*>(smem + sl.tab);
     uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + sl.bar) + warp * S;
@@ -361,15 +364,20 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     const int dropped = a.drop_copy && blockIdx.x == 0 && j0 == 0 && j1 > 0 ? 0 : -1;
     auto issue = [&]() {
         const int h = ikg & (JPC - 1), c = ikg >> JPC_LOG;  // which JB blocks of which 32-block chunk
+        // (debug build: a job outside its weight completes its stage empty)
+        const bool ok =
+            QG_OK(igrp >= 0 && igrp < (isec ? a.N2 : a.N) / GROUP && c < (NB + CHUNK - 1) / CHUNK, timeouts, 901);
         if (lane == 0 && issued != dropped) {
             uint64_t* bar = &wbar[iss_slot];
             uint8_t* dst = wnib_p + (size_t)iss_slot * NIB;
             fence_proxy_async();
-            mbar_arrive_expect_tx(bar, NIB + DSB);
+            mbar_arrive_expect_tx(bar, ok ? NIB + DSB : 0u);
             const CUtensorMap* map = isec ? &tn1 : &tn0;
-            tma_load_4d(dst, map, h * JB * 16, 0, c, igrp, bar, pol);
-            if (JB > TC_LINE_JB) tma_load_4d(dst + TC_BOX, map, h * JB * 16 + 128, 0, c, igrp, bar, pol);
-            tma_load_3d(wds_p + (size_t)iss_slot * DSB, isec ? &td1 : &td0, h * JB * 8, c, igrp, bar, pol);
+            if (ok) {
+                tma_load_4d(dst, map, h * JB * 16, 0, c, igrp, bar, pol);
+                if (JB > TC_LINE_JB) tma_load_4d(dst + TC_BOX, map, h * JB * 16 + 128, 0, c, igrp, bar, pol);
+                tma_load_3d(wds_p + (size_t)iss_slot * DSB, isec ? &td1 : &td0, h * JB * 8, c, igrp, bar, pol);
+            }
         }
         ++ikg;
         if (++ikj == jpt) {  // next unit
@@ -393,8 +401,11 @@ __global__ void __launch_bounds__(QM_THREADS, 1)
     const uint32_t row_bytes = (uint32_t)nkb * Q8_1_BYTES, rstride = row_bytes + 16;
     const uint32_t raw_off = sl.act + (uint32_t)a.nkb_max * M * 64 - (uint32_t)M * rstride;
     if (threadIdx.x == 0 && row_bytes > 0) {
-        mbar_arrive_expect_tx(abar, (uint32_t)M * row_bytes);
-        for (int n = 0; n < M; ++n)
+        const bool ok = QG_OK(qg_in(((int64_t)(M - 1) * NB + (int64_t)jb0 * JB) * Q8_1_BYTES, row_bytes,
+                                    (int64_t)M * NB * Q8_1_BYTES),
+                              timeouts, 902);
+        mbar_arrive_expect_tx(abar, ok ? (uint32_t)M * row_bytes : 0u);
+        for (int n = 0; ok && n < M; ++n)
             bulk_g2s_plain(smem + raw_off + (size_t)n * rstride,
                            a.xq + ((int64_t)n * NB + (int64_t)jb0 * JB) * Q8_1_BYTES, row_bytes, abar);
     }

@@ -331,27 +331,6 @@ __device__ __forceinline__ void tc_stage_act(uint8_t* act, float* meta, const ui
     }
 }
 
-// Packed fp32 pairs (sm_100 and later): (ax, ay) = (bx, by) * (cx, cy) + (ax, ay)
-// and (dx, dy) = (bx, by) * (cx, cy), each lane one IEEE fma / mul, so the
-// results equal the scalar ones bit for bit with half the instructions.
-__device__ __forceinline__ void fma_f32x2(float& ax, float& ay, float bx, float by, float cx, float cy)
-{
-    asm("{\n\t.reg .b64 a, b, c;\n\t"
-        "mov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
-        "fma.rn.f32x2 a, b, c, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
-        : "+f"(ax), "+f"(ay)
-        : "f"(bx), "f"(by), "f"(cx), "f"(cy));
-}
-
-__device__ __forceinline__ void mul_f32x2(float& dx, float& dy, float bx, float by, float cx, float cy)
-{
-    asm("{\n\t.reg .b64 d, b, c;\n\t"
-        "mov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
-        "mul.rn.f32x2 d, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(dx), "=f"(dy)
-        : "f"(bx), "f"(by), "f"(cx), "f"(cy));
-}
-
 // One job: 16 blocks of the tile in ring stage (sn codes, sd scales) against
 // staged blocks kb .. kb + 7.  acc[nt][i]: rows g, g, g+8, g+8 and columns
 // 8 nt + 2t, +1, +0, +1 (the mma accumulator layout).
@@ -790,6 +769,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int j0 = warp * J / W, j1 = (warp + 1) * J / W;
     const TcSmem sl = tc_smem(M, W, S, a.nkb_max, C > 1 ? a.out_tiles : 0, NIB, DSB,
                               tc_meta_bytes(FMT));
+    // (debug build: the layout must fit the launch's shared memory; every CTA
+    // of a cluster decides alike, so none waits on a CTA that left)
+    if (!QG_OK(sl.bytes <= dynamic_smem_bytes(), timeouts, 810)) return;
     uint8_t* nib = smem + sl.nib;
     uint8_t* ds = smem + sl.ds;
     uint8_t* act = smem + sl.act;
@@ -842,12 +824,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     auto issue = [&]() {
         const int h = ikg & (JPC - 1), c = ikg >> JPC_LOG;  // which JB blocks of which 32-block chunk
+        // (debug build: a job outside its weight completes its stage empty)
+        const int Nw = isec ? a.N2 : a.N;
+        const int64_t T16 = (Nw + TC_ROWS - 1) / TC_ROWS;
+        const int PER = JB < TC_Q8_0_JOB_BLOCKS ? TC_Q8_0_JOB_BLOCKS / JB : 1;  // Q8_0 jobs per region
+        const bool ok = QG_OK(FMT == TCF_Q8_0   ? qg_in(((int64_t)(igrp >> 2) * (njb / PER) + ikg / PER) * TC_Q8_0_JOB,
+                                                       TC_Q8_0_JOB, T16 * (njb / PER) * TC_Q8_0_JOB)
+                              : (FMT == TCF_Q4_K || FMT == TCF_Q5_K)
+                                  ? qg_in(((int64_t)(igrp >> 2) * njb + ikg) * NIB, NIB, T16 * njb * NIB)
+                                  : igrp >= 0 && igrp < Nw / GROUP && c < (NB + CHUNK - 1) / CHUNK,
+                              timeouts, 801);
         if (lane == 0) {
             uint64_t* bar = &wbar[iss_slot];
             uint8_t* dst = wnib + (size_t)iss_slot * NIB;
             fence_proxy_async();
-            mbar_arrive_expect_tx(bar, NIB + DSB);
-            if constexpr (FMT == TCF_Q8_0) {
+            mbar_arrive_expect_tx(bar, ok ? NIB + DSB : 0u);
+            if (!ok) {
+            } else if constexpr (FMT == TCF_Q8_0) {
                 // the job's part of the Q8_0 pack: tile igrp / 4, region (8
                 // blocks) ikg * JB / 8, all of it or the half h of its codes
                 // and of its scales
@@ -901,8 +894,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t row_bytes = (uint32_t)jpt * JB * Q8_1_BYTES, rstride = row_bytes + 16;
     uint8_t* raw = act + (size_t)a.nkb_max * M * 64 - (size_t)M * rstride;
     if (threadIdx.x == 0 && row_bytes > 0) {
-        mbar_arrive_expect_tx(abar, (uint32_t)M * row_bytes);
-        for (int n = 0; n < M; ++n)
+        const bool ok = QG_OK(qg_in(((int64_t)(M - 1) * NB + (int64_t)jb0 * JB) * Q8_1_BYTES, row_bytes,
+                                    (int64_t)M * NB * Q8_1_BYTES),
+                              timeouts, 802);
+        mbar_arrive_expect_tx(abar, ok ? (uint32_t)M * row_bytes : 0u);
+        for (int n = 0; ok && n < M; ++n)
             bulk_g2s_plain(raw + (size_t)n * rstride, a.xq + ((int64_t)n * NB + (int64_t)jb0 * JB) * Q8_1_BYTES,
                            row_bytes, abar);
     }

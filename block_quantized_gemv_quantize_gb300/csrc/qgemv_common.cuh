@@ -26,6 +26,37 @@ constexpr int Q6_K_BYTES = 210;
 constexpr int MAX_M = 17;
 
 // ---------------------------------------------------------------------------
+// Debug build (compiled with -DQGEMV_BOUNDS_CHECK): explicit checks of the
+// indexes the kernels compute for their global and shared-memory accesses,
+// against the extents their arguments imply.  A failing check skips the
+// access (a skipped copy still completes its mbarrier stage, with no bytes)
+// and records itself in the library's status page: word 1 counts failures,
+// word 2 keeps the site number of the first.  `status` is that page (word 0
+// is the wait-timeout count).  No assert, no trap: the kernel runs on.  In
+// the release build QG_OK is the constant true and every check compiles away.
+// ---------------------------------------------------------------------------
+#ifdef QGEMV_BOUNDS_CHECK
+static __device__ __noinline__ void qg_bounds_fail(unsigned int* status, unsigned int site)
+{
+    if (atomicAdd_system(status + 1, 1u) == 0u) atomicExch_system(status + 2, site);
+}
+__device__ __forceinline__ bool qg_ok(bool ok, unsigned int* status, unsigned int site)
+{
+    if (!ok && status) qg_bounds_fail(status, site);
+    return ok;
+}
+#define QG_OK(cond, status, site) ::qgemv::qg_ok((cond), (status), (site))
+#else
+#define QG_OK(cond, status, site) true
+#endif
+
+// [lo, lo + n) lies within [0, extent) (64-bit byte or element offsets).
+__host__ __device__ __forceinline__ bool qg_in(int64_t lo, int64_t n, int64_t extent)
+{
+    return lo >= 0 && n >= 0 && lo + n <= extent;
+}
+
+// ---------------------------------------------------------------------------
 // Packed weight layouts.  Rows are taken in groups of 4 (the last group may
 // hold fewer) and each row of NB = K/32 blocks is cut into chunks of 32
 // blocks (the last chunk may be shorter, nb_tail blocks).  One (group, chunk)
@@ -381,8 +412,9 @@ __device__ __forceinline__ void q6_k_unpack(const uint4 ql, const uint2 qh, uint
 // J = sc0 * sum_{i<16} (q - 32) q_a + sc1 * sum_{i>=16} (q - 32) q_a, with the
 // offsets folded into the chain starts: g0 = -32 * sum(q_a[0..15]),
 // g1 = -32 * sum(q_a[16..31]); sc0, sc1 = the block's two int8 subscales.
-__device__ __forceinline__ int q6_k_dot_init(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, int g0, int g1,
-                                             int sc0, int sc1)
+// The two 16-value half-block dp4a chains of a Q6_K block, continued from
+// the starts g0 and g1.
+__device__ __forceinline__ void q6_k_half_dots(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, int& g0, int& g1)
 {
     g0 = __dp4a((int)w[0], (int)lo.x, g0);
     g0 = __dp4a((int)w[1], (int)lo.y, g0);
@@ -392,6 +424,12 @@ __device__ __forceinline__ int q6_k_dot_init(const uint32_t (&w)[8], const uint4
     g1 = __dp4a((int)w[5], (int)hi.y, g1);
     g1 = __dp4a((int)w[6], (int)hi.z, g1);
     g1 = __dp4a((int)w[7], (int)hi.w, g1);
+}
+
+__device__ __forceinline__ int q6_k_dot_init(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, int g0, int g1,
+                                             int sc0, int sc1)
+{
+    q6_k_half_dots(w, lo, hi, g0, g1);
     return sc0 * g0 + sc1 * g1;
 }
 
@@ -402,6 +440,37 @@ __device__ __forceinline__ int q6_k_dot(const uint32_t (&w)[8], const uint4 lo, 
 {
     return q6_k_dot_init(w, lo, hi, -32 * (int)(int16_t)(sums & 0xFFFFu), -32 * (int)(int16_t)(sums >> 16),
                          (int)(int8_t)(sc2 & 0xFFu), (int)(int8_t)((sc2 >> 8) & 0xFFu));
+}
+
+// Packed fp32 pairs (sm_100 and later): (ax, ay) = (bx, by) * (cx, cy) + (ax, ay),
+// (dx, dy) = (bx, by) * (cx, cy) and (dx, dy) = (bx, by) + (cx, cy), each
+// lane one IEEE fma / mul / add, so the results equal the scalar ones bit for
+// bit with half the instructions.
+__device__ __forceinline__ void fma_f32x2(float& ax, float& ay, float bx, float by, float cx, float cy)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\t"
+        "mov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
+        "fma.rn.f32x2 a, b, c, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(ax), "+f"(ay)
+        : "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+
+__device__ __forceinline__ void mul_f32x2(float& dx, float& dy, float bx, float by, float cx, float cy)
+{
+    asm("{\n\t.reg .b64 d, b, c;\n\t"
+        "mov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(dx), "=f"(dy)
+        : "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+
+__device__ __forceinline__ void add_f32x2(float& dx, float& dy, float bx, float by, float cx, float cy)
+{
+    asm("{\n\t.reg .b64 d, b, c;\n\t"
+        "mov.b64 b, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\t"
+        "add.rn.f32x2 d, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(dx), "=f"(dy)
+        : "f"(bx), "f"(by), "f"(cx), "f"(cy));
 }
 
 // Exact int -> float for |i| < 2^22 without a conversion instruction: the

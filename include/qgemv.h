@@ -66,6 +66,7 @@ extern "C" {
 #define QGEMV_WAIT_TIMEOUT (-6)       /* an earlier call's kernel gave up      */
 
 #define QGEMV_MAX_M 17
+#define QGEMV_TOPK_MAX 8
 
 /* Human-readable text for a status code (static storage). */
 const char* qgemv_status_string(int status);
@@ -102,8 +103,8 @@ int quantize_q8_1(const float* x, int64_t ldx, void* xq, int M, int K, void* str
 
 /* rmsnorm_quantize_q8_1 - RMSNorm fused with the Q8_1 quantizer: the rows of
  * x normalized by their RMS and scaled by gamma, written as Q8_1 without an
- * fp32 copy.  [closure] "Qwen3.6 27B Q4_0 DFlash/SYCL closure", What did not
- * clear the gate: the down-to-next-RMSNorm/Q8 boundary (RMSNorm fused with
+ * fp32 copy.  [closure] "Qwen3.6 27B Q4_0 DFlash/SYCL closure", Closed or negative
+ * paths: the down-to-next-RMSNorm/Q8 boundary (RMSNorm fused with
  * the Q8 quantization).  What is computed, per row: RMSNorm(x) * gamma,
  * xh_k = x_k * r * gamma_k with r = 1 / sqrt(sum_k x_k^2 / K + eps), then the
  * Q8_1 quantizer of quantize_q8_1 applied to xh.  xh is computed in fp32 in
@@ -177,7 +178,7 @@ int qgemv_q6_k(const void* w_pack, const void* xq, float* y, int64_t ldy, int M,
  *   y[m][n] = (W x)[m][n] + residual[m * ldr + n],
  * the sum taken in fp32 when the output is stored (the MMVQ part exactly as
  * qgemv_q4_0 computes it, then one fp32 addition).  [closure] "Qwen3.6 27B
- * Q4_0 DFlash/SYCL closure", What did not clear the gate: an MMVQ with a
+ * Q4_0 DFlash/SYCL closure", Closed or negative paths: an MMVQ with a
  * residual epilogue (the down projection writing its output plus the
  * residual stream in one pass).
  *   residual  DEVICE fp32, M rows of N values, row stride ldr >= N; it may be
@@ -247,6 +248,42 @@ int lmhead_q6_k_top1(const void* w_pack, const float* x, int64_t ldx, int32_t* i
 int lmhead_q6_k_candmax(const void* w_pack, const float* x, int64_t ldx, const int32_t* cand, int32_t* ids,
                         float* top_vals, float* cand_vals, void* workspace, size_t ws_bytes, int M, int K, int N,
                         void* stream);
+
+/* lmhead_q6_k_topk_workspace_bytes - workspace bytes for lmhead_q6_k_topk:
+ * the lmhead_q6_k_top1 workspace (its first 256 bytes under the same
+ * zero-fill contract, then the Q8_1 copy of x), then, 256-byte aligned, one
+ * list of k 64-bit keys per row for each CTA of the launch, at most
+ * min(ceil(N / 4), 256) CTAs.  Host-only. */
+size_t lmhead_q6_k_topk_workspace_bytes(int M, int K, int N, int k);
+
+/* lmhead_q6_k_topk - the candidate-max's top-k form over the same fused
+ * LM-head: for each row m, the k largest logits with their ids, in
+ * descending order, plus (optionally) the logit of a given candidate id.
+ * No logits are written.  [handoff] "Current next-execution plan", the
+ * candidate-max precheck (the true top ids and values plus per-row candidate
+ * scores).  Order: by value, larger first; exactly equal values by lower id
+ * first; -0 == +0; NaN logits are never ranked; a row with fewer than k
+ * non-NaN logits fills its last places with id -1 and value NaN.  Entry 0 is
+ * lmhead_q6_k_top1's id except for a row of only NaN (there -1, not 0).
+ * The result is deterministic: the logits are the fused kernel's fp32 sums
+ * (each independent of where its row falls in the launch) and the ranking of
+ * the (value, id) keys is a total order.
+ *   w_pack, x, ldx, M, K, N  as lmhead_q6_k_top1
+ *   k          1 <= k <= QGEMV_TOPK_MAX (8), k <= N
+ *   cand       int32 [M] (read) or NULL: the candidate id of each row; one
+ *              outside 0 .. N-1 gives cand_vals[m] = NaN
+ *   ids        int32 [M][k] (written)
+ *   vals       fp32 [M][k] (written) or NULL: the logits of ids
+ *   cand_vals  fp32 [M] (written), NULL exactly when cand is NULL
+ *   workspace  lmhead_q6_k_topk_workspace_bytes(M, K, N, k) bytes, first 256
+ *              bytes zero-filled before the first use (every call leaves them
+ *              so); calls that share a workspace must not overlap in time.
+ *   Returns QGEMV_UNSUPPORTED_SHAPE where the activation does not fit next
+ *   to the weight rings in shared memory (M * K beyond what the top-1 call
+ *   serves with its ring kernel, e.g. M = 17 at K = 17408). */
+int lmhead_q6_k_topk(const void* w_pack, const float* x, int64_t ldx, int k, const int32_t* cand, int32_t* ids,
+                     float* vals, float* cand_vals, void* workspace, size_t ws_bytes, int M, int K, int N,
+                     void* stream);
 
 /* ---- A6: row argmax (the unfused control) -------------------------------- */
 
@@ -447,6 +484,34 @@ int qgemv_debug_drop_next_copy(void);
  * that does not go through leaves the ordinary path to run.  Returns the
  * previous count. */
 int qgemv_debug_fail_fused(int count);
+
+/* ---- the bounds-checking build ------------------------------------------ */
+
+/* The library also builds with -DQGEMV_BOUNDS_CHECK (build.py --debug):
+ * every kernel then checks the indexes it computes for its global and
+ * shared-memory accesses (weight copies and tensor-map coordinates inside the
+ * pack, activation and output offsets inside their [M][ld] extents, the
+ * shared-memory layout inside the launch's size).  A failing check skips the
+ * access (a skipped copy completes its pipeline stage with no bytes, so no
+ * wait hangs) and is recorded; results are then wrong but the context stays
+ * usable.  There is no counterpart on the pages: it stands in for a memory
+ * checker where none can run.  The release build compiles every check away.
+ *
+ * qgemv_bounds_check_build - 1 for the bounds-checking build, 0 otherwise. */
+int qgemv_bounds_check_build(void);
+
+/* qgemv_take_bounds_errors - after a device synchronize, the number of failed
+ * checks since the previous call and the site number of the first (0, 0 in
+ * the release build), then clears both.  Returns QGEMV_INVALID_ARG for a null
+ * pointer, QGEMV_CUDA_ERROR when the status page cannot be read. */
+int qgemv_take_bounds_errors(unsigned int* count, unsigned int* first_site);
+
+/* qgemv_debug_plant_bad_store - for tests of the bounds-checking build only:
+ * the next MMVQ launch on the ring kernel (no top-1) moves the first stores
+ * of its CTA 0, warp 0 one output row-length past their extent; its checks
+ * skip them and record them.  Returns the previous request, or
+ * QGEMV_UNSUPPORTED_SHAPE in the release build (where it does nothing). */
+int qgemv_debug_plant_bad_store(void);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,7 @@
  *   - Top-1 with the lowest-token-ID finite-tie rule: same page, "Exactness and
  *     safety contracts", item 3.
  *   - RMSNorm fused with the Q8_1 quantizer ("Qwen3.6 27B Q4_0 DFlash/SYCL
- *     closure", What did not clear the gate): the plain definition in fp64,
+ *     closure", Closed or negative paths): the plain definition in fp64,
  *     then the quantizer on the fp32 rounding of the normalized row.
  *
  * The dot products are the plain definition of the result: every Q8_1 block
@@ -162,7 +162,7 @@ void oracle_quantize_q8_1(const float* x, int64_t ldx, int M, int K, uint8_t* ou
 }
 
 /* RMSNorm fused with the Q8_1 quantizer ("Qwen3.6 27B Q4_0 DFlash/SYCL
- * closure", What did not clear the gate: the down-to-next-RMSNorm/Q8
+ * closure", Closed or negative paths: the down-to-next-RMSNorm/Q8
  * boundary; the pages name the fusion, not its arithmetic).  The plain
  * definition, per row, in fp64: S = sum_k x_k^2 (in increasing k),
  * r = 1 / sqrt(S / K + eps), xh_k = (x_k r) gamma_k; then xh rounded to

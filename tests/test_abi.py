@@ -71,6 +71,12 @@ def test_sizes(lib):
     lib.q5_k_pack_bytes.restype = ctypes.c_size_t
     assert lib.q5_k_pack_bytes(16, 5120) == 20 * 2880  # 180 B per row and superblock
     assert lib.q5_k_pack_bytes(16, 384) == 0  # K % 256
+    # top-k: the top-1 workspace rounded to 256 bytes, then k 8-byte keys per
+    # row for each CTA, at most min(ceil(N / 4), 256) CTAs
+    lib.lmhead_q6_k_topk_workspace_bytes.restype = ctypes.c_size_t
+    lib.lmhead_q6_k_topk_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    assert lib.lmhead_q6_k_topk_workspace_bytes(5, 5120, 248320, 8) == 29184 + 256 * 5 * 8 * 8
+    assert lib.lmhead_q6_k_topk_workspace_bytes(1, 256, 7, 7) == 768 + 2 * 1 * 7 * 8
 
 
 def test_status_strings(lib):
@@ -98,6 +104,16 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.quantize_q8_1(fake, 32, odd, 1, 32, None) == -3
     assert lib.lmhead_q6_k_top1(fake, fake, 512, fake, fake, 8, 5, 512, 100, None) == -4
     assert lib.lmhead_q6_k_top1(fake, fake, 512, fake, fake, 4096, 5, 320, 100, None) == -2
+    topk = lib.lmhead_q6_k_topk
+    topk.argtypes = [P, P, L, I, P, P, P, P, P, ctypes.c_size_t, I, I, I, P]
+    big = 1 << 20
+    assert topk(fake, fake, 512, 0, None, fake, fake, None, fake, big, 5, 512, 100, None) == -1  # k = 0
+    assert topk(fake, fake, 512, 9, None, fake, fake, None, fake, big, 5, 512, 100, None) == -1  # k > 8
+    assert topk(fake, fake, 512, 8, None, fake, fake, None, fake, big, 5, 512, 7, None) == -1  # k > N
+    assert topk(fake, fake, 512, 8, fake, fake, fake, None, fake, big, 5, 512, 100, None) == -1  # cand alone
+    assert topk(fake, fake, 512, 8, None, fake, fake, None, fake, 4096, 5, 512, 100, None) == -4
+    assert topk(fake, fake, 512, 8, None, fake, odd, None, fake, big, 5, 512, 100, None) == -3
+    assert topk(fake, fake, 512, 8, None, fake, None, None, fake, big, 18, 512, 100, None) == -2
 
 
 def test_fused_failure_hook_refuses_before_any_cuda_call(lib):

@@ -145,6 +145,38 @@ def test_lmhead_candmax_full(ops, vocab):
     assert cand_vals[0] == top_vals[0] and cand_vals[4] == top_vals[4]
 
 
+def test_lmhead_topk_full(ops, vocab):
+    # rows 1..5 at the full vocabulary, k = 8: the oracle's ranking within the
+    # top-k gate, and exactly the ranking of the unfused fp32 logits (both
+    # kernels take K whole here, so the values are equal bit for bit)
+    x6d = _t(vocab["x6"])
+    y_ref, S = vocab["y_ref"], vocab["S"]
+    ids_ref = y_ref.argmax(axis=1)
+    cand = np.array([ids_ref[0], 0, N_V - 1, 123456, ids_ref[4]], dtype=np.int32)
+    ids, vals, cv = ops.lmhead_q6_k_topk(vocab["wp"], x6d[1:6], K_H, N_V, 8, cand=_t(cand))
+    ids, vals, cv = _np(ids), _np(vals), _np(cv)
+    errs = C.check_topk(ids, vals, y_ref, S)
+    assert errs == [], errs[:5]
+    print("top-8 ranks equal to the oracle's:", int((ids == oracle.topk(y_ref, 8)[0]).sum()), "of", ids.size)
+    y = _np(ops.qgemv_q6_k(vocab["wp"], ops.quantize_q8_1(x6d[1:6]), 5, K_H, N_V))
+    assert np.array_equal(vals, np.take_along_axis(y, ids.astype(np.int64), axis=1))
+    assert ids.tolist() == np.argsort(-y, axis=1, kind="stable")[:, :8].tolist()
+    assert ids[:, 0].tolist() == _np(ops.lmhead_q6_k_top1(vocab["wp"], x6d[1:6], K_H, N_V)).tolist()
+    for m in range(5):
+        assert cv[m] == y[m, cand[m]]
+    assert np.array_equal(_np(ops.lmhead_q6_k_topk(vocab["wp"], x6d[1:6], K_H, N_V, 8)[0]), ids)
+
+
+def test_lmhead_topk_target_six_rows_full(ops, vocab):
+    # the target side's six rows: the ranking of the unfused fp32 logits
+    x6d = _t(vocab["x6"])
+    ids, vals, _ = ops.lmhead_q6_k_topk(vocab["wp"], x6d, K_H, N_V, 8)
+    ids, vals = _np(ids), _np(vals)
+    y = _np(ops.qgemv_q6_k(vocab["wp"], ops.quantize_q8_1(x6d), 6, K_H, N_V))
+    assert ids.tolist() == np.argsort(-y, axis=1, kind="stable")[:, :8].tolist()
+    assert np.array_equal(vals, np.take_along_axis(y, ids.astype(np.int64), axis=1))
+
+
 def _sample_rows(N, seed=0):
     g = np.random.default_rng(seed)
     return np.unique(np.concatenate([np.arange(min(64, N)), np.arange(max(0, N - 64), N),
