@@ -67,8 +67,8 @@ def parse():
     p.add_argument("--sweep-k", type=int, default=5120, help="sweep: the reduction size K")
     p.add_argument("--profile", choices=["mlp", "heads"], default=None,
                    help="for a profiler: run only the verifier MLP projections (gate/up pair, down) or only the "
-                        "LM heads (target qgemv_q6_k M=6, fused top-1 M=5), --steps times each with an L2 flush "
-                        "between calls; prints per-call times, not a bench line")
+                        "LM heads (target qgemv_q6_k M=6, fused top-1 M=5, and the tensor-core qgemv_q6_k at M=8), "
+                        "--steps times each with an L2 flush between calls; prints per-call times, not a bench line")
     return p.parse_args()
 
 
@@ -795,8 +795,19 @@ def run_profile(args):
         xd = up(synth.activations(6, K_H, seed=c3["seed"] + 100))
         xq = ops.quantize_q8_1(up(synth.activations(M_T, K_H, seed=c3["seed"] + 200)))
         logits = torch.empty((M_T, N_V), device=dev)
+        x8 = up(synth.activations(8, K_H, seed=c3["seed"] + 300))
+        xq8 = ops.quantize_q8_1(x8)
+        logits8 = torch.empty((8, N_V), device=dev)
+
+        def tc_m8():
+            # the tensor-core Q6_K kernel at M = 8, for comparison with the dp4a heads
+            prev = ops.set_q6_k_tensor_cores(2)
+            ops.qgemv_q6_k(wv, xq8, 8, K_H, N_V, y=logits8)
+            ops.set_q6_k_tensor_cores(prev)
+
         calls = {"target_head": lambda: ops.qgemv_q6_k(wv, xq, M_T, K_H, N_V, y=logits),
-                 "lmhead_top1": lambda: ops.lmhead_q6_k_top1(wv, xd[1:6], K_H, N_V)}
+                 "lmhead_top1": lambda: ops.lmhead_q6_k_top1(wv, xd[1:6], K_H, N_V),
+                 "q6_k_tc_m8": tc_m8}
     torch.cuda.synchronize()
     times = {n: [] for n in calls}
     for _ in range(max(1, args.steps)):
