@@ -409,10 +409,11 @@ def run_native(args, rank, world):
     same_ids_t = ids_tf.cpu().tolist() == ids_t.cpu().tolist()
     topk_first_is_top1 = ids_k[:, 0].cpu().tolist() == ids_d.cpu().tolist()
 
-    # Fused against unfused LM-head over the M sweep (BASELINE config 3's
-    # control): for each M, rows 0..M-1 of a [17, 5120] activation, the
-    # fused top-1 against quantize + qgemv_q6_k + argmax_f32_rows on the same
-    # inputs, interleaved rounds of 10 calls each.
+    # Fused against unfused LM-head over the M sweep (the unfused control
+    # writes the full fp32 logits and runs a separate argmax): for each M,
+    # rows 0..M-1 of a [17, 5120] activation, the fused top-1 against
+    # quantize + qgemv_q6_k + argmax_f32_rows on the same inputs, interleaved
+    # rounds of 10 calls each.
     xs = up(synth.activations(17, K_H, seed=c_sweep_seed))
     ys = torch.empty((17, N_V), device=dev)
     xqs = torch.empty(ops.q8_1_bytes(17, K_H), dtype=torch.uint8, device=dev)
