@@ -148,18 +148,22 @@ def test_qgemv_q4_0_pair_matches_oracle(ops, M, K, Na, Nb):
 # Tensor-core Q4_0 path: shapes it takes (N, N_b multiples of 16, K of 1024),
 # over several tiles per CTA, warp ranges that cut tiles, clusters that split
 # K (large K or few tiles), and M across the 8-row MMA tiles; each against the
-# oracle with the tensor cores on and off.
+# oracle in the three kernel modes: 1 = the small-M kernel up to M = 16 (the
+# general one above), 2 = the general tensor-core kernel, 0 = SIMT only.
 TC_SHAPES = [(5, 1024, 16), (6, 1024, 48), (7, 2048, 160), (6, 5120, 2448), (8, 3072, 512), (9, 1024, 4096),
              (12, 5120, 336), (16, 2048, 1040), (17, 5120, 272), (6, 17408, 320), (5, 17408, 64), (5, 9216, 784),
              (7, 1024, 9728)]
 
 
-@pytest.mark.parametrize("tc", [True, False])
+@pytest.mark.parametrize("tc", [1, 2, 0])
 @pytest.mark.parametrize("M,K,N", TC_SHAPES)
 def test_qgemv_q4_0_tensor_core_shapes(ops, M, K, N, tc):
     prev = ops.set_q4_0_tensor_cores(tc)
     try:
-        assert ops.qgemv_q4_0_plan(M, K, N)["tensor_cores"] == tc
+        plan = ops.qgemv_q4_0_plan(M, K, N)
+        assert plan["tensor_cores"] == bool(tc)
+        if tc == 2 or (tc == 1 and M > 16):
+            assert plan["kernel"] == "tc"
         y, y_ref, S = _gemv_case(ops, "q4_0", M, K, N, seed=3 * M + K + N)
     finally:
         ops.set_q4_0_tensor_cores(prev)
@@ -182,7 +186,8 @@ def test_qgemv_q4_0_tensor_core_plans(ops):
 
 
 @pytest.mark.parametrize("M,K,Na,Nb", [(5, 1024, 16, 32), (6, 5120, 1536, 1552), (6, 17408, 64, 128),
-                                       (17, 2048, 256, 80), (8, 3072, 4096, 16)])
+                                       (17, 2048, 256, 80), (8, 3072, 4096, 16), (12, 5120, 256, 128),
+                                       (16, 1024, 48, 32)])
 def test_qgemv_q4_0_pair_tensor_cores(ops, M, K, Na, Nb):
     assert ops.qgemv_q4_0_plan(M, K, Na, Nb)["tensor_cores"]
     x = synth.activations(M, K, seed=M + K + 1, outlier_frac=0.01)
@@ -208,8 +213,9 @@ def _unit_scale_case(M, K, N, seed):
     return w, x
 
 
-@pytest.mark.parametrize("tc", [True, False])
-@pytest.mark.parametrize("M,K,N", [(6, 5120, 64), (5, 1024, 4096), (9, 2048, 48), (17, 1024, 32), (6, 8192, 64)])
+@pytest.mark.parametrize("tc", [1, 2, 0])
+@pytest.mark.parametrize("M,K,N", [(6, 5120, 64), (5, 1024, 4096), (9, 2048, 48), (17, 1024, 32), (6, 8192, 64),
+                                   (12, 5120, 64), (16, 2048, 96)])
 def test_qgemv_q4_0_unit_scales_exact(ops, M, K, N, tc):
     # pins the exactness of the block dots on both paths: with unit scales the
     # output is the integer sum of the exact block dots (|y| <= K * 8 * 127 < 2^24)
@@ -220,15 +226,16 @@ def test_qgemv_q4_0_unit_scales_exact(ops, M, K, N, tc):
     assert np.all(y_ref == np.round(y_ref))
     prev = ops.set_q4_0_tensor_cores(tc)
     try:
-        assert ops.qgemv_q4_0_plan(M, K, N)["tensor_cores"] == (tc and M >= 5)
+        assert ops.qgemv_q4_0_plan(M, K, N)["tensor_cores"] == (tc > 0 and M >= 5)
         y = _np(ops.qgemv_q4_0(ops.qpack_q4_0(_t(w), N, K), ops.quantize_q8_1(_t(x)), M, K, N))
     finally:
         ops.set_q4_0_tensor_cores(prev)
     assert np.array_equal(y.astype(np.float64), y_ref)
 
 
-def test_qgemv_q4_0_pair_unit_scales_exact(ops):
-    M, K, Na, Nb = 6, 4096, 48, 80
+@pytest.mark.parametrize("M", [6, 12])
+def test_qgemv_q4_0_pair_unit_scales_exact(ops, M):
+    K, Na, Nb = 4096, 48, 80
     wa, x = _unit_scale_case(M, K, Na, seed=5)
     wb, _ = _unit_scale_case(M, K, Nb, seed=6)
     xq_ref = oracle.quantize_q8_1(x)
