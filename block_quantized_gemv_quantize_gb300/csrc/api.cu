@@ -7,6 +7,7 @@
 #include "launch.cuh"
 
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 using namespace qgemv;
@@ -29,9 +30,18 @@ std::atomic<int> g_drop_request{0};
 std::atomic<int> g_plant_request{0};
 std::atomic<int> g_fail_fused{0};  // test only: fused LM-head calls to refuse
 
-// Takes one refusal request, if any is left.
+// Takes one refusal request, if any is left.  The environment variable
+// QGEMV_FAIL_FUSED=n (test only) adds n requests when the library first
+// looks, so that a process can be started with failing fused calls.
+std::once_flag g_fail_env_once;
+
 bool take_fused_failure()
 {
+    std::call_once(g_fail_env_once, []() {
+        const char* e = std::getenv("QGEMV_FAIL_FUSED");
+        const int n = e ? std::atoi(e) : 0;
+        if (n > 0) g_fail_fused.fetch_add(n);
+    });
     int v = g_fail_fused.load();
     while (v > 0)
         if (g_fail_fused.compare_exchange_weak(v, v - 1)) return true;

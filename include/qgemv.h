@@ -482,7 +482,9 @@ int qgemv_debug_drop_next_copy(void);
  * QGEMV_CUDA_ERROR without enqueueing anything, as a fused kernel that cannot
  * be launched would.  [record] Exactness and safety contracts: a fused call
  * that does not go through leaves the ordinary path to run.  Returns the
- * previous count. */
+ * previous count.  The environment variable QGEMV_FAIL_FUSED=n adds n such
+ * requests when the library first checks for one (a process started with
+ * failing fused calls). */
 int qgemv_debug_fail_fused(int count);
 
 /* ---- the bounds-checking build ------------------------------------------ */

@@ -132,3 +132,30 @@ def test_fused_failure_hook_refuses_before_any_cuda_call(lib):
     assert lib.qgemv_debug_fail_fused(1) == 0
     assert fn(None, fake, 5120, fake, fake, 1 << 20, 5, 5120, 248320, None) == -1
     assert lib.qgemv_debug_fail_fused(0) == 1
+
+
+def test_fused_failure_hook_from_the_environment():
+    # QGEMV_FAIL_FUSED=2 in a fresh process: its first two validated fused
+    # calls are refused before any CUDA call, the third is not refused by the
+    # hook (without a GPU it then fails later, with another status)
+    code = (
+        "import ctypes, sys\n"
+        "lib = ctypes.CDLL(sys.argv[1])\n"
+        "fn = lib.lmhead_q6_k_top1\n"
+        "fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,\n"
+        "               ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]\n"
+        "fake = 0x10000\n"
+        "print(fn(fake, fake, 5120, fake, fake, 1 << 20, 5, 5120, 248320, None),\n"
+        "      fn(fake, fake, 5120, fake, fake, 1 << 20, 5, 5120, 248320, None),\n"
+        "      lib.qgemv_debug_fail_fused(0))\n"
+    )
+    import subprocess
+    import sys
+
+    from block_quantized_gemv_quantize_gb300 import build
+
+    env = dict(os.environ, QGEMV_FAIL_FUSED="2")
+    out = subprocess.run([sys.executable, "-c", code, build.LIB], env=env, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["-5", "-5", "0"]
