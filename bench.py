@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--eager", action="store_true",
+                   help="launch the step's calls one by one in the timed regions instead of replaying a CUDA graph "
+                        "captured from them")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded oracle sample length")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: time qgemv_<format> over M in {1,2,4,6,9,12,17}, K=5120, "
@@ -275,13 +278,32 @@ def run_native(args, rank, world):
         step()
     torch.cuda.synchronize()
 
+    # The timed regions replay CUDA graphs captured from the library calls
+    # (the same kernels, arguments and buffers, without the per-call host
+    # work); --eager launches the calls one by one instead.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    g_step = None if args.eager else capture(step)
+    if g_step is not None:
+        for _ in range(3):
+            g_step.replay()
+        torch.cuda.synchronize()
+
     # timed region: K steps bracketed by two events
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     t0.record(stream)
     for _ in range(args.steps):
-        step()
+        if g_step is not None:
+            g_step.replay()
+        else:
+            step()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -330,11 +352,19 @@ def run_native(args, rank, world):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
+    g_e2e = None if args.eager else capture(e2e_step)
+    if g_e2e is not None:
+        for _ in range(3):
+            g_e2e.replay()
+        torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        e2e_step()
+        if g_e2e is not None:
+            g_e2e.replay()
+        else:
+            e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
@@ -548,6 +578,7 @@ def run_native(args, rank, world):
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": sum(kernels_per_call.get(n, 1) for n in names) * args.steps,
+            "launch": "eager" if args.eager else "cuda_graph (captured from the library calls, replayed per step)",
             "breakdown_steps": n_break,
             "clocks": clocks,
         }
