@@ -37,12 +37,14 @@ constexpr int MMVQ_MAX_WARPS = MMVQ_MAX_THREADS / 32;
 // R x M partial sums and the unpacked weights fit in 128 registers (the
 // top-1 forms at M = 4 and 6 included: 112 and 127 registers, and 16 warps
 // made the six-row fused head 6 us faster than the unfused path, where 12
-// had left it level); 12 warps (168 registers) for M = 7, 8, and for the
-// top-k form from M = 3, which would spill; 8 warps (255 registers) for M > 8.
+// had left it level); 12 warps (168 registers) for M = 7 .. 16, and for the
+// top-k form from M = 3, which would spill with 16 (12 warps took the Q6_K
+// heads at M = 9, 12 and 16 from 294 / 356 / 446 to 280 / 351 / 441 us
+// against 8); 8 warps (255 registers) for M = 17.
 template <int FMT, int M, bool TOP1, bool TOPK = false>
 struct MmvqThreads {
     static constexpr bool wide = M == 7 || M == 8 || (TOPK && M >= 3);
-    static constexpr int value = M > 8 ? 256 : (wide ? 384 : 512);
+    static constexpr int value = M > 16 ? 256 : (M > 8 || wide ? 384 : 512);
 };
 
 // Rows per warp: one 4-row group of the packed layout.
