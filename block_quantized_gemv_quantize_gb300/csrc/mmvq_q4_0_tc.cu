@@ -89,10 +89,17 @@ int launch_mmvq_q4_0_tc(const MmvqArgs& a, int M, bool pair, cudaStream_t s, int
 {
     const int mode = g_tc_enabled.load();
     if (!mode) return TC_NOT_TAKEN;
-    // Below 5 rows the SIMT kernels are as fast or faster (measured on GB300:
-    // M <= 4 loses up to 12% on the tensor cores, M >= 5 gains up to 34%).
-    if (M < TC_MIN_M) return TC_NOT_TAKEN;
     if (a.N % TC_ROWS || (pair && a.N2 % TC_ROWS) || a.K % (CHUNK * QK)) return TC_NOT_TAKEN;
+    // Below 5 rows the SIMT kernels are as fast or faster on the verifier's
+    // weights (their fixed cost per call is lower: 1-2 us better at N = 5120
+    // and 17408, K = 5120), but on large weights the small-M kernel streams
+    // faster at any M (N = 248320, K = 5120, M = 1..4: 109-113 us against
+    // 115-120 us on dp4a, back to back).
+    if (M < TC_MIN_M) {
+        const int64_t elems = (int64_t)(a.N + (pair ? a.N2 : 0)) * a.K;
+        if (mode != 1 || elems < TC_SMALL_M_MIN_ELEMS) return TC_NOT_TAKEN;
+        return launch_mmvq_q4_0_mma(a, M, pair, s, info);  // TC_NOT_TAKEN without a plan
+    }
     if (mode == 1 && M <= 8) {  // one 8-column MMA tile: the small-M kernel, where it has a plan
         const int st = launch_mmvq_q4_0_mma(a, M, pair, s, info);
         if (st != TC_NOT_TAKEN) return st;

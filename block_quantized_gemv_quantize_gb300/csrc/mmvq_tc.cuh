@@ -74,6 +74,9 @@ constexpr int TC_Q8_0_JOB_BLOCKS = 8;                          // blocks of a pa
 // its codes and half of its scales)
 __host__ __device__ inline int tc_q8_0_job_bytes(int jb) { return jb * (512 + 32); }
 constexpr int TC_MIN_M = 5;  // activation rows from which the tensor-core path is taken (Q4_0)
+// below TC_MIN_M rows, the weight elements (N K, both weights of a pair) from
+// which the small-M kernel is taken all the same (2^28: a 151 MB Q4_0 pack)
+constexpr int64_t TC_SMALL_M_MIN_ELEMS = (int64_t)1 << 28;
 constexpr int TC_Q6_K_MIN_M = 7;  // the same for Q6_K
 constexpr int TC_MAX_STAGES = 6;
 

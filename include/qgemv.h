@@ -338,19 +338,25 @@ int qgemv_block_dots_q4_0(const void* w_pack, const void* xq, int32_t* out, int 
 int qgemv_block_dots_q6_k(const void* w_pack, const void* xq, int32_t* out, int M, int K, int N, void* stream);
 
 /* qgemv_set_q4_0_tensor_cores - choose the kernel family of qgemv_q4_0 and
- * qgemv_q4_0_pair: 1 (the default) runs shapes with M >= 5, N (and N_b) a
- * multiple of 16 and K a multiple of 1024 on the tensor cores (f16 mma.sync with exact
- * integer block dots, the scales applied per block in fp32); 0 runs every
- * shape on the SIMT dp4a kernels.  Both compute the formula of qgemv_q4_0
- * within its fp32 rounding; the fp32 summation order differs, so the two may
- * differ in the last bits.  Process-wide; returns the previous setting.
- * (Not from the pages: a choice of this implementation.) */
+ * qgemv_q4_0_pair, for shapes with N (and N_b) a multiple of 16 and K a
+ * multiple of 1024 (other shapes always run on the SIMT dp4a kernels):
+ *   1 (the default): the tensor cores (f16 mma.sync with exact integer block
+ *     dots, the scales applied per block in fp32) from M = 5, and below 5
+ *     rows on weights of at least 2^28 elements (N K, both weights of a
+ *     pair); the small-M kernel up to M = 8, the general one above;
+ *   2: the general tensor-core kernel for every M from 5;
+ *   0: the SIMT dp4a kernels for every shape.
+ * All compute the formula of qgemv_q4_0 within its fp32 rounding; the fp32
+ * summation order differs, so they may differ in the last bits.
+ * Process-wide; returns the previous setting.  (Not from the pages: a choice
+ * of this implementation.) */
 int qgemv_set_q4_0_tensor_cores(int enable);
 
 /* qgemv_q4_0_plan - which kernel qgemv_q4_0 (N_b = 0) or qgemv_q4_0_pair
  * (N_b > 0) would launch for this shape under the current setting; writes
- * info[4] = {1 if tensor cores else 0, CTAs per cluster (the K parts), grid
- * size, ring stages per warp}, zeros for the SIMT kernels.  Enqueues
+ * info[4] = {0 for the SIMT kernels, 1 for the general tensor-core kernel, 2
+ * for the small-M one; CTAs per cluster (the K parts), grid size, ring
+ * stages per warp}, zeros after the first for the SIMT kernels.  Enqueues
  * nothing; may query the current device.  (Not from the pages.) */
 int qgemv_q4_0_plan(int M, int K, int N, int N_b, int* info);
 

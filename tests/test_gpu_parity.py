@@ -178,6 +178,9 @@ def test_qgemv_q4_0_tensor_core_plans(ops):
     assert ops.qgemv_q4_0_plan(6, 17408, 5120)["cluster"] > 1
     assert ops.qgemv_q4_0_plan(5, 17408, 64)["cluster"] >= 4
     assert not ops.qgemv_q4_0_plan(4, 5120, 17408)["tensor_cores"]  # M < 5: the SIMT kernels
+    # ... except on large weights, where the small-M kernel streams faster
+    assert ops.qgemv_q4_0_plan(2, 5120, 248320)["kernel"] == "tc_small_m"
+    assert ops.qgemv_q4_0_plan(4, 5120, 32768)["kernel"] == "simt"
     assert not ops.qgemv_q4_0_plan(6, 5120, 17400)["tensor_cores"]  # N % 16
     assert not ops.qgemv_q4_0_plan(6, 5056, 17408)["tensor_cores"]  # K % 1024
     for M, K, N in TC_SHAPES:
