@@ -68,10 +68,11 @@ def parse():
     p.add_argument("--sweep-m", default="1,2,4,6,9,12,17", help="sweep: comma-separated row counts M")
     p.add_argument("--sweep-n", default="5120,17408,248320", help="sweep: comma-separated output sizes N")
     p.add_argument("--sweep-k", type=int, default=5120, help="sweep: the reduction size K")
-    p.add_argument("--profile", choices=["mlp", "heads"], default=None,
-                   help="for a profiler: run only the verifier MLP projections (gate/up pair, down) or only the "
+    p.add_argument("--profile", choices=["mlp", "heads", "topk"], default=None,
+                   help="for a profiler: run only the verifier MLP projections (gate/up pair, down), only the "
                         "LM heads (target qgemv_q6_k M=6, fused top-1 M=5, and the tensor-core qgemv_q6_k at M=8), "
-                        "--steps times each with an L2 flush between calls; prints per-call times, not a bench line")
+                        "or the fused top-1 and top-8 of rows 1..5, --steps times each with an L2 flush between "
+                        "calls; prints per-call times, not a bench line")
     return p.parse_args()
 
 
@@ -825,6 +826,15 @@ def run_profile(args):
         yg, yu, yd = (torch.empty((M_T, n), device=dev) for n in (N_FF, N_FF, K_H))
         calls = {"gate_up": lambda: ops.qgemv_q4_0_pair(wg, wu, xq, M_T, K_H, N_FF, N_FF, y_a=yg, y_b=yu),
                  "down": lambda: ops.qgemv_q4_0(wd, hq, M_T, N_FF, K_H, y=yd)}
+    elif args.profile == "topk":
+        c3 = synth.WORKLOADS["lmhead_q6_k"]
+        wv = pack("q6_k", synth.q6_k_weights(N_V, K_H, seed=c3["seed"]), N_V, K_H)
+        xd = up(synth.activations(6, K_H, seed=c3["seed"] + 100))
+        ids5 = torch.empty(5, dtype=torch.int32, device=dev)
+        idk = torch.empty((5, 8), dtype=torch.int32, device=dev)
+        vk = torch.empty((5, 8), dtype=torch.float32, device=dev)
+        calls = {"lmhead_top1": lambda: ops.lmhead_q6_k_top1(wv, xd[1:6], K_H, N_V, ids=ids5),
+                 "lmhead_top8": lambda: ops.lmhead_q6_k_topk(wv, xd[1:6], K_H, N_V, 8, ids=idk, vals=vk)}
     else:
         c3 = synth.WORKLOADS["lmhead_q6_k"]
         wv = pack("q6_k", synth.q6_k_weights(N_V, K_H, seed=c3["seed"]), N_V, K_H)

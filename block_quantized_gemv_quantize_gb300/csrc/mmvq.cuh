@@ -38,12 +38,13 @@ constexpr int MMVQ_MAX_WARPS = MMVQ_MAX_THREADS / 32;
 // top-1 forms at M = 4 and 6 included: 112 and 127 registers, and 16 warps
 // made the six-row fused head 6 us faster than the unfused path, where 12
 // had left it level); 12 warps (168 registers) for M = 7 .. 16, and for the
-// top-k form from M = 3, which would spill with 16 (12 warps took the Q6_K
-// heads at M = 9, 12 and 16 from 294 / 356 / 446 to 280 / 351 / 441 us
-// against 8); 8 warps (255 registers) for M = 17.
+// top-k form at M = 3 and 4, which would spill with 16 (12 warps took the
+// Q6_K heads at M = 9, 12 and 16 from 294 / 356 / 446 to 280 / 351 / 441 us
+// against 8; 16 instead of 12 took the top-8 at M = 5 from 225 to 214 us);
+// 8 warps (255 registers) for M = 17.
 template <int FMT, int M, bool TOP1, bool TOPK = false>
 struct MmvqThreads {
-    static constexpr bool wide = M == 7 || M == 8 || (TOPK && M >= 3);
+    static constexpr bool wide = M == 7 || M == 8 || (TOPK && (M == 3 || M == 4));
     static constexpr int value = M > 16 ? 256 : (M > 8 || wide ? 384 : 512);
 };
 
@@ -648,6 +649,41 @@ __device__ __forceinline__ void topk_select(int count, int k, int lane, Load loa
     }
 }
 
+// Whole warp: the k largest keys of `n` lists, each sorted larger first and
+// 0-filled, list j at lists[j * stride .. + k - 1], handed to out(r, key) by
+// lane 0 in descending order (0 once the lists hold no more keys).  Lane l
+// holds the heads of lists l, l + 32, ... (n <= 32 * TOPK_HEADS); each round
+// is a warp maximum over the heads, and the list holding the winner (keys are
+// unique) moves its head on.
+constexpr int TOPK_HEADS = 8;
+template <class Out>
+__device__ __forceinline__ void topk_merge_sorted(const unsigned long long* lists, int n, int stride, int k, int lane,
+                                                  Out out)
+{
+    int head[TOPK_HEADS];
+#pragma unroll
+    for (int j = 0; j < TOPK_HEADS; ++j) head[j] = 0;
+    for (int r = 0; r < k; ++r) {
+        unsigned long long best = 0ull;
+#pragma unroll
+        for (int j = 0; j < TOPK_HEADS; ++j) {
+            const int c = lane + 32 * j;
+            if (c < n && head[j] < k) {
+                const unsigned long long x = lists[(size_t)c * stride + head[j]];
+                best = x > best ? x : best;
+            }
+        }
+        best = warp_max_u64(best);
+        if (lane == 0) out(r, best);
+        if (best == 0ull) continue;
+#pragma unroll
+        for (int j = 0; j < TOPK_HEADS; ++j) {
+            const int c = lane + 32 * j;
+            if (c < n && head[j] < k && lists[(size_t)c * stride + head[j]] == best) ++head[j];
+        }
+    }
+}
+
 // Keys a warp folds per row group in the lock-step top-1 kernel: R rows x M
 // activation rows, at most R_ROWS * MAX_M.
 constexpr int TOP1_GROUP_KEYS = R_ROWS * MAX_M;
@@ -1236,19 +1272,17 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1, TOPK>::value, 1)
         __syncthreads();
         if (*s_last) {
             __threadfence();
-            // Merge the CTAs' lists.  Each row's G k keys are copied (all the
-            // loads in flight at once) into its slice of the rings and the
-            // activation tile, both free now.  A key of the row's top k is in
-            // its CTA's list and is at least t0 = the largest k-th key of any
-            // list (that list alone holds k keys >= t0): those keys are
-            // compacted in place and the k largest picked from them.  Should
-            // the slices not fit, the k largest are picked from the lists in
+            // Merge the CTAs' lists ([CTA][row][k], each sorted larger
+            // first): the row's warp copies its G lists (eight loads a lane
+            // in flight) into the row's slice of the rings and the activation
+            // tile, both free now, and merges them there (topk_merge_sorted).
+            // Should they not fit, the k largest are picked from the lists in
             // global memory directly.
             const int G = gridDim.x;
             const unsigned long long* lists = a.topk_lists;
-            const int total = G * KT;
             unsigned long long* region = reinterpret_cast<unsigned long long*>(rings);
-            const bool fits = (size_t)M * total * 8 <= (size_t)(t.meta - rings);
+            const int total = G * KT;
+            const bool fits = (size_t)M * total * 8 <= (size_t)(t.meta - rings) && G <= 32 * TOPK_HEADS;
             for (int m = warp; m < M; m += W) {
                 auto emit = [&](int r, unsigned long long key) {
                     a.ids[m * KT + r] = key ? top1_key_to_id(key) : -1;
@@ -1265,31 +1299,13 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1, TOPK>::value, 1)
                     continue;
                 }
                 unsigned long long* buf = region + (size_t)m * total;
-#pragma unroll 4
+#pragma unroll 8
                 for (int e = lane; e < total; e += 32) {
                     const int c = e / KT;
                     buf[e] = __ldcg(lists + ((size_t)c * M + m) * KT + (e - c * KT));
                 }
                 __syncwarp();
-                unsigned long long t0 = 0ull;
-                for (int c = lane; c < G; c += 32) {
-                    const unsigned long long x = buf[c * KT + KT - 1];
-                    t0 = x > t0 ? x : t0;
-                }
-                t0 = warp_max_u64(t0);
-                int cnt = 0;
-                for (int e0 = 0; e0 < total; e0 += 32) {
-                    // in place: a key moves only down to an index already read
-                    const int e = e0 + lane;
-                    const unsigned long long x = e < total ? buf[e] : 0ull;
-                    const bool take = x != 0ull && x >= t0;
-                    const unsigned int bal = __ballot_sync(0xffffffffu, take);
-                    __syncwarp();
-                    if (take) buf[cnt + __popc(bal & ((1u << lane) - 1u))] = x;
-                    cnt += __popc(bal);
-                    __syncwarp();
-                }
-                topk_select(cnt, KT, lane, [&](int e) { return buf[e]; }, emit);
+                topk_merge_sorted(buf, G, KT, KT, lane, emit);
                 __syncwarp();
             }
             if (threadIdx.x == 0) atomicExch(&a.ws->done, 0u);
