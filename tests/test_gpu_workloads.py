@@ -8,7 +8,9 @@ configuration: the library picks it from M, K, N), against the CPU oracle.
   * fused Q6_K LM-head top-1, K=5120 N=248320, rows 1..5 of a [6, 5120] block
     -- ids against the full oracle, and against the unfused path;
   * M sweep {1,2,4,6,9,12,17} for Q4_0 and Q6_K at K=5120, N in {5120, 17408,
-    248320} -- sampled rows (first 64, last 64 and 1024 random rows);
+    248320} -- sampled rows (first 64, last 64 and 1024 random rows); the
+    further formats Q8_0, Q4_K, Q5_K at M in {1, 6, 9, 17}, N in {17408,
+    248320}, the same way;
   * adversarial top-1 at K=5120 N=248320 M=5: all-zero weights, planted exact
     ties at (1,256), (255,256), (0,248319), a planted near tie.
 """
@@ -197,6 +199,27 @@ def test_m_sweep_sampled(ops, fmt, N):
         y = _np((ops.qgemv_q4_0 if fmt == "q4_0" else ops.qgemv_q6_k)(wp, xq, M, K, N))
         f = oracle.qgemv_q4_0 if fmt == "q4_0" else oracle.qgemv_q6_k
         y_ref, S = f(w[rows], xq_ref)
+        r = C.check_close(y[:, rows], y_ref, S)
+        assert r["ok"], (M, r)
+    del wp
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q5_k"])
+@pytest.mark.parametrize("N", [17408, 248320])
+def test_further_formats_sweep_sampled(ops, fmt, N):
+    # the M sweep's shapes for the further formats (their tensor-core kernel,
+    # the launch configuration the sweep times), on sampled rows
+    K = K_H
+    w = getattr(synth, fmt + "_weights")(N, K, seed=N + 3)
+    wp = getattr(ops, "qpack_" + fmt)(_t(w), N, K)
+    rows = _sample_rows(N)
+    for M in (1, 6, 9, 17):
+        x = synth.activations(M, K, seed=2000 + M, outlier_frac=0.01)
+        xq_ref = oracle.quantize_q8_1(x)
+        xq = ops.quantize_q8_1(_t(x))
+        y = _np(getattr(ops, "qgemv_" + fmt)(wp, xq, M, K, N))
+        y_ref, S = getattr(oracle, "qgemv_" + fmt)(w[rows], xq_ref)
         r = C.check_close(y[:, rows], y_ref, S)
         assert r["ok"], (M, r)
     del wp
