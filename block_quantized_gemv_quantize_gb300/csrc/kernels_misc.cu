@@ -363,19 +363,19 @@ __global__ void qpack_q6_k_kernel(const uint8_t* __restrict__ canon, uint8_t* __
             const int hi = (sb[128 + (gv >> 2)] >> (2 * (gv & 3))) & 0x03;
             q[v] = (uint8_t)(lo | (hi << 4));
         }
+        // P[16]: byte t = q_t | high2(q_{16+t}) << 6; Q[8]: byte u =
+        // low4(q_{16+u}) | low4(q_{24+u}) << 4 (q6_k_unpack reads them back)
         uint32_t wl[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-            const uint32_t byte = (uint32_t)(q[t] & 0x0F) | ((uint32_t)(q[t + 16] & 0x0F) << 4);
+            const uint32_t byte = (uint32_t)q[t] | ((uint32_t)(q[t + 16] >> 4) << 6);
             wl[t >> 2] |= byte << (8 * (t & 3));
         }
         uint32_t wh[2] = {0, 0};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            uint32_t byte = 0;
-#pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) byte |= (uint32_t)(q[t + 8 * s2] >> 4) << (2 * s2);
-            wh[t >> 2] |= byte << (8 * (t & 3));
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t byte = (uint32_t)(q[16 + u] & 0x0F) | ((uint32_t)(q[24 + u] & 0x0F) << 4);
+            wh[u >> 2] |= byte << (8 * (u & 3));
         }
         const BlockAddr ad = block_addr(pack, L, n, b);
         if (QG_OK(qg_in(ad.q - pack, 16, total) && qg_in(ad.qh - pack, 8, total) && qg_in(ad.sc - pack, 2, total) &&
@@ -583,7 +583,7 @@ __global__ void block_dots_kernel(const void* __restrict__ w_pack, const uint8_t
             out[i] = q4_0_dot(w, lo, hi, (int)meta.y);
         } else {
             q6_k_unpack(*reinterpret_cast<const uint4*>(ad.q), *reinterpret_cast<const uint2*>(ad.qh), w);
-            out[i] = q6_k_dot(w, lo, hi, meta.y, *reinterpret_cast<const uint16_t*>(ad.sc));
+            out[i] = q6_k_dot(w, lo, hi, meta.y, *reinterpret_cast<const uint16_t*>(ad.sc)) >> 2;  // 4 J -> J, exact
         }
     }
 }

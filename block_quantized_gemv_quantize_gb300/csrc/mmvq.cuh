@@ -257,8 +257,12 @@ __device__ __forceinline__ void accumulate_q6_k(const uint4 (&ql)[R], const uint
                                                 const float (&dw)[R], const ActTile& t, int ti, float (&acc)[R][M])
 {
     uint32_t w[R][8];
+    float dq[R];  // the superblock scale over four (q6_k_dot returns 4 J)
 #pragma unroll
-    for (int r = 0; r < R; ++r) q6_k_unpack(ql[r], qh[r], w[r]);
+    for (int r = 0; r < R; ++r) {
+        q6_k_unpack(ql[r], qh[r], w[r]);
+        dq[r] = dw[r] * 0.25f;
+    }
 #pragma unroll
     for (int m = 0; m < M; ++m) {
         const uint4 lo = t.aq[(m * 2 + 0) * t.KC + ti];
@@ -267,8 +271,8 @@ __device__ __forceinline__ void accumulate_q6_k(const uint4 (&ql)[R], const uint
         const float da = __uint_as_float(mt.x);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int J = q6_k_dot(w[r], lo, hi, mt.y, sc[r]);
-            acc[r][m] = fmaf(dw[r] * da, (float)J, acc[r][m]);
+            const int J4 = q6_k_dot(w[r], lo, hi, mt.y, sc[r]);
+            acc[r][m] = fmaf(dq[r] * da, (float)J4, acc[r][m]);
         }
     }
 }
@@ -307,7 +311,8 @@ __device__ __forceinline__ void ring_meta_store(uint8_t* p, float da, int s_lo, 
         *reinterpret_cast<uint2*>(p) =
             make_uint2(__float_as_uint(da), (uint32_t)(-8 * (s_lo + s_hi) + MAGIC_I2F_BITS));
     } else {
-        *reinterpret_cast<uint4*>(p) = make_uint4(__float_as_uint(da), (uint32_t)(-32 * s_lo), (uint32_t)(-32 * s_hi), 0u);
+        // the second half's codes come four times over (q6_k_unpack)
+        *reinterpret_cast<uint4*>(p) = make_uint4(__float_as_uint(da), (uint32_t)(-32 * s_lo), (uint32_t)(-128 * s_hi), 0u);
     }
 }
 
@@ -371,58 +376,6 @@ __device__ __forceinline__ void ring_act_from_f32(const RingAct<FMT, M>& t, cons
             if (sub == 0)
                 ring_meta_store<FMT>(t.meta + (b * A::MROWS + m) * A::META, __half2float(__float2half_rn(o.d)),
                                      o.s_half, o.s_all - o.s_half);
-        }
-    }
-}
-
-// Q4_0 block (one per lane) of R rows against the tile.  ab, am: the block's
-// codes and meta words in the tile.
-template <int M, int R>
-__device__ __forceinline__ void ring_dot_q4_0(const uint4 (&w16)[R], const float (&dw)[R], const uint8_t* ab,
-                                              const uint8_t* am, float (&acc)[R][M])
-{
-    uint32_t w[R][8];
-#pragma unroll
-    for (int r = 0; r < R; ++r) q4_0_unpack(w16[r], w[r]);
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-        const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
-        const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
-        const uint2 mt = *reinterpret_cast<const uint2*>(am + 8 * m);
-        const float da = __uint_as_float(mt.x);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int sI = q4_0_dot(w[r], lo, hi, (int)mt.y);
-            const float f = __int_as_float(sI) - MAGIC_I2F;  // exact I
-            acc[r][m] = fmaf(dw[r] * da, f, acc[r][m]);
-        }
-    }
-}
-
-// Q6_K block (one per lane) of R rows against the tile.
-template <int M, int R>
-__device__ __forceinline__ void ring_dot_q6_k(const uint4 (&ql)[R], const uint2 (&qh)[R], const uint32_t (&sc2)[R],
-                                              const float (&dw)[R], const uint8_t* ab, const uint8_t* am,
-                                              float (&acc)[R][M])
-{
-    uint32_t w[R][8];
-    int sc0[R], sc1[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        q6_k_unpack(ql[r], qh[r], w[r]);
-        sc0[r] = (int)(int8_t)(sc2[r] & 0xFFu);
-        sc1[r] = (int)(int8_t)((sc2[r] >> 8) & 0xFFu);
-    }
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-        const uint4 lo = *reinterpret_cast<const uint4*>(ab + 32 * m);
-        const uint4 hi = *reinterpret_cast<const uint4*>(ab + 32 * m + 16);
-        const uint4 mt = *reinterpret_cast<const uint4*>(am + 16 * m);
-        const float da = __uint_as_float(mt.x);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int J = q6_k_dot_init(w[r], lo, hi, (int)mt.y, (int)mt.z, sc0[r], sc1[r]);
-            acc[r][m] = fmaf(dw[r] * da, (float)J, acc[r][m]);
         }
     }
 }
@@ -912,12 +865,14 @@ __device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q6_K>& H, const ui
                                           float (&acc)[R_ROWS][M])
 {
     uint32_t w[R_ROWS][8];
-    int sc0[R_ROWS], sc1[R_ROWS];
+    int sc0x4[R_ROWS], sc1[R_ROWS];
+    float dq[R_ROWS];  // the superblock scale over four (q6_k_dot_init returns 4 J)
 #pragma unroll
     for (int q = 0; q < R_ROWS; ++q) {
         q6_k_unpack(H.ql[q], H.qh[q], w[q]);
-        sc0[q] = (int)(int8_t)(H.sc[q] & 0xFFu);
+        sc0x4[q] = 4 * (int)(int8_t)(H.sc[q] & 0xFFu);
         sc1[q] = (int)(int8_t)((H.sc[q] >> 8) & 0xFFu);
+        dq[q] = H.dw[q] * 0.25f;
     }
 #pragma unroll
     for (int m = 0; m < M; ++m) {
@@ -927,8 +882,8 @@ __device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q6_K>& H, const ui
         const float da = __uint_as_float(mt.x);
 #pragma unroll
         for (int q = 0; q < R_ROWS; ++q) {
-            const int J = q6_k_dot_init(w[q], lo, hi, (int)mt.y, (int)mt.z, sc0[q], sc1[q]);
-            acc[q][m] = fmaf(H.dw[q] * da, (float)J, acc[q][m]);
+            const int J4 = q6_k_dot_init(w[q], lo, hi, (int)mt.y, (int)mt.z, sc0x4[q], sc1[q]);
+            acc[q][m] = fmaf(dq[q] * da, (float)J4, acc[q][m]);
         }
     }
 }

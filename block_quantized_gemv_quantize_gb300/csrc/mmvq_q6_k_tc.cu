@@ -13,11 +13,11 @@ std::atomic<int> g_q6_k_tc_enabled{1};
 
 // Tensor maps of a packed Q6_K weight whose groups and chunks are all whole
 // (N % 16 == 0, K % 1024 == 0): every group-chunk is 3360 B = four 832-byte
-// row tiles (ql[32][16 B], qh[32][8 B], sc[32][2 B]) then d[4 rows][4
-// superblocks] fp16.  The first three maps view the row tiles as bytes (832) x
+// row tiles (the code bytes P[32][16 B] and Q[32][8 B], sc[32][2 B]) then
+// d[4 rows][4 superblocks] fp16.  The first three maps view the row tiles as bytes (832) x
 // row (4) x chunk x group and differ in box and swizzle:
-//   ql: box 128 B x 4 x 1 x 4 groups (16 rows x 8 blocks), 128-byte swizzle;
-//   qh: box  64 B x 4 x 1 x 4, 64-byte swizzle;
+//   P:  box 128 B x 4 x 1 x 4 groups (16 rows x 8 blocks), 128-byte swizzle;
+//   Q:  box  64 B x 4 x 1 x 4, 64-byte swizzle;
 //   sc: box  16 B x 4 x 1 x 4;
 // the fourth views the scale tails as bytes (32) x chunk x group, box 32 B x
 // 1 x 4 groups.

@@ -391,24 +391,38 @@ __device__ __forceinline__ void tc_job(const uint8_t* sn, const uint8_t* sd, con
 }
 
 // ---------------------------------------------------------------------------
-// Q6_K over the existing pack (a row's chunk tile: ql[32 blocks][16 B], then
-// qh[32][8 B], then sc[32][2 B]; the chunk's superblock scales d[4 rows][4]
-// after the four tiles).  Block value v < 16 is the low nibble of ql byte v
-// and v >= 16 the high nibble of byte v - 16; its two high bits are bits
-// 2 (v / 8) of qh byte v % 8.  Lane t takes values 4t .. 4t+3 and 16 + 4t ..
-// 16 + 4t + 3 (the K order the activation is staged in): one ql word and one
-// qh word per row and block, the qh word shifted right by 2 (t / 2) so that
-// byte j holds value 4t + j's high bits at bits 0-1 and value 16 + 4t + j's
-// at bits 4-5.
+// Q6_K over the existing pack (a row's chunk tile: P[32 blocks][16 B], then
+// Q[32][8 B], then sc[32][2 B]; the chunk's superblock scales d[4 rows][4]
+// after the four tiles).  Block value v < 16 is bits 0-5 of P byte v; value
+// 16 + u has its high two bits at bits 6-7 of P byte u and its low four bits
+// in Q byte u % 8 (bits 0-3 for u < 8, bits 4-7 for u >= 8).  Lane t takes
+// values 4t .. 4t+3 and 16 + 4t .. 16 + 4t + 3 (the K order the activation
+// is staged in): one P word and one Q word per row and block, the Q word
+// shifted left by 4 for t < 2 so that the low four bits of value 16 + 4t + j
+// sit at bits 4-7 of byte j.
 // ---------------------------------------------------------------------------
 
-// Four codes of a row as two f16x2 A registers per MMA: (ql & LO) | (hi & HM)
-// | 0x6400 per half = 1024 + q (LO = 0x000F000F, HM = 0x00300030) or
-// 1024 + 16 q (LO = 0x00F000F0, HM = 0x03000300), exactly.
-template <uint32_t LO, uint32_t HM>
-__device__ __forceinline__ uint32_t q6_f16x2(uint32_t ql, uint32_t hi)
+// Two codes of the first half-block as an f16x2 A register: 1024 + q per
+// half (the code's six bits under 0x6400), exactly.
+__device__ __forceinline__ uint32_t q6_lo_f16x2(uint32_t p)
 {
-    return (ql & LO) | (hi & HM) | 0x64006400u;
+    return (p & 0x003F003Fu) | 0x64006400u;
+}
+
+// Two codes of the second half-block: 1024 + 16 q per half, the high two bits
+// (h, already at bits 8-9) and the low four (l, at bits 4-7) under 0x6400.
+__device__ __forceinline__ uint32_t q6_hi_f16x2(uint32_t h, uint32_t l)
+{
+    return (h & 0x03000300u) | (l & 0x00F000F0u) | 0x64006400u;
+}
+
+// Four-bit codes with a fifth bit as two f16x2 A registers per MMA (Q5_K):
+// (lo & LO) | (hi & HM) | 0x6400 per half = 1024 + q (LO = 0x000F000F, HM =
+// 0x00100010) or 1024 + 16 q (LO = 0x00F000F0, HM = 0x01000100), exactly.
+template <uint32_t LO, uint32_t HM>
+__device__ __forceinline__ uint32_t q5_f16x2(uint32_t lo, uint32_t hi)
+{
+    return (lo & LO) | (hi & HM) | 0x64006400u;
 }
 
 // int8 byte k of w (stored biased: byte ^ 0x80) as a float, exactly:
@@ -439,7 +453,7 @@ __device__ __forceinline__ void tc_job_q6_k(const uint8_t* sq, const uint8_t* ss
     // c ^ ((g / 2) & 3)), row g + 8 512 B on
     const uint8_t* qlg = sq + g * 128 + 4 * t;
     const uint8_t* qhg = sq + 2048 + g * 64 + 4 * (t & 1);
-    const int hsw = (g >> 1) & 3, sh = 2 * (t >> 1);
+    const int hsw = (g >> 1) & 3, sh = 4 - 4 * (t >> 1);
     const uint4 sva = *reinterpret_cast<const uint4*>(ss + g * 16);  // rows g, g + 8: sc of the 8 blocks
     const uint4 svb = *reinterpret_cast<const uint4*>(ss + (g + 8) * 16);
     const uint32_t sca[4] = {sva.x ^ 0x80808080u, sva.y ^ 0x80808080u, sva.z ^ 0x80808080u, sva.w ^ 0x80808080u};
@@ -450,16 +464,13 @@ __device__ __forceinline__ void tc_job_q6_k(const uint8_t* sq, const uint8_t* ss
         const int hoff = (((p >> 1) ^ hsw) << 4) + (p & 1) * 8;
         const uint32_t wa = *reinterpret_cast<const uint32_t*>(qlg + swq);
         const uint32_t wb = *reinterpret_cast<const uint32_t*>(qlg + 1024 + swq);
-        const uint32_t ha = *reinterpret_cast<const uint32_t*>(qhg + hoff) >> sh;
-        const uint32_t hb = *reinterpret_cast<const uint32_t*>(qhg + 512 + hoff) >> sh;
-        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-        const uint32_t ha4 = ha << 4, hb4 = hb << 4, ha_4 = ha >> 4, hb_4 = hb >> 4;
-        const uint32_t A0[4] = {q6_f16x2<0x000F000Fu, 0x00300030u>(wa, ha4), q6_f16x2<0x000F000Fu, 0x00300030u>(wb, hb4),
-                                q6_f16x2<0x000F000Fu, 0x00300030u>(wa8, ha_4),
-                                q6_f16x2<0x000F000Fu, 0x00300030u>(wb8, hb_4)};
-        const uint32_t A1[4] = {q6_f16x2<0x00F000F0u, 0x03000300u>(wa, ha4), q6_f16x2<0x00F000F0u, 0x03000300u>(wb, hb4),
-                                q6_f16x2<0x00F000F0u, 0x03000300u>(wa8, ha_4),
-                                q6_f16x2<0x00F000F0u, 0x03000300u>(wb8, hb_4)};
+        const uint32_t la = *reinterpret_cast<const uint32_t*>(qhg + hoff) << sh;
+        const uint32_t lb = *reinterpret_cast<const uint32_t*>(qhg + 512 + hoff) << sh;
+        // values (4t, 4t + 2) of rows g, g + 8, then (4t + 1, 4t + 3); the
+        // same for the second half
+        const uint32_t A0[4] = {q6_lo_f16x2(wa), q6_lo_f16x2(wb), q6_lo_f16x2(wa >> 8), q6_lo_f16x2(wb >> 8)};
+        const uint32_t A1[4] = {q6_hi_f16x2(wa << 2, la), q6_hi_f16x2(wb << 2, lb), q6_hi_f16x2(wa >> 6, la >> 8),
+                                q6_hi_f16x2(wb >> 6, lb >> 8)};
         // subscales of halves 0 and 1 of block p: bytes 2p, 2p + 1 of the row's 16
         const float s0a = sc_f32(sca[p >> 1], 2 * (p & 1)), s1a = sc_f32(sca[p >> 1], 2 * (p & 1) + 1);
         const float s0b = sc_f32(scb[p >> 1], 2 * (p & 1)), s1b = sc_f32(scb[p >> 1], 2 * (p & 1) + 1);
@@ -543,14 +554,14 @@ __device__ __forceinline__ void tc_job_q4_k(const uint8_t* sn, const uint8_t* ac
             const uint32_t ha = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + (p * TC_ROWS + g) * 4) >> t;
             const uint32_t hb = *reinterpret_cast<const uint32_t*>(sn + 8 * 256 + (p * TC_ROWS + g + 8) * 4) >> t;
             const uint32_t ha4 = ha << 4, hb4 = hb << 4, ha_4 = ha >> 4, hb_4 = hb >> 4;
-            A0[0] = q6_f16x2<0x000F000Fu, 0x00100010u>(w.x, ha4);
-            A0[1] = q6_f16x2<0x000F000Fu, 0x00100010u>(w.y, hb4);
-            A0[2] = q6_f16x2<0x000F000Fu, 0x00100010u>(wa8, ha_4);
-            A0[3] = q6_f16x2<0x000F000Fu, 0x00100010u>(wb8, hb_4);
-            A1[0] = q6_f16x2<0x00F000F0u, 0x01000100u>(w.x, ha4);
-            A1[1] = q6_f16x2<0x00F000F0u, 0x01000100u>(w.y, hb4);
-            A1[2] = q6_f16x2<0x00F000F0u, 0x01000100u>(wa8, ha_4);
-            A1[3] = q6_f16x2<0x00F000F0u, 0x01000100u>(wb8, hb_4);
+            A0[0] = q5_f16x2<0x000F000Fu, 0x00100010u>(w.x, ha4);
+            A0[1] = q5_f16x2<0x000F000Fu, 0x00100010u>(w.y, hb4);
+            A0[2] = q5_f16x2<0x000F000Fu, 0x00100010u>(wa8, ha_4);
+            A0[3] = q5_f16x2<0x000F000Fu, 0x00100010u>(wb8, hb_4);
+            A1[0] = q5_f16x2<0x00F000F0u, 0x01000100u>(w.x, ha4);
+            A1[1] = q5_f16x2<0x00F000F0u, 0x01000100u>(w.y, hb4);
+            A1[2] = q5_f16x2<0x00F000F0u, 0x01000100u>(wa8, ha_4);
+            A1[3] = q5_f16x2<0x00F000F0u, 0x01000100u>(wb8, hb_4);
         } else {
             A0[0] = nib_f16x2<0x000F000Fu>(w.x);
             A0[1] = nib_f16x2<0x000F000Fu>(w.y);

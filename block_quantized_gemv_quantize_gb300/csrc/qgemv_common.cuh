@@ -133,8 +133,8 @@ __host__ __device__ inline Layout make_layout(int fmt, int N, int K)
 
 // Where the pieces of block b of row n live.
 struct BlockAddr {
-    const uint8_t* q;   // Q4_0: the 16 code bytes;  Q6_K: ql (16 B)
-    const uint8_t* qh;  // Q6_K: qh (8 B)
+    const uint8_t* q;   // Q4_0: the 16 code bytes;  Q6_K: the code bytes P (16 B)
+    const uint8_t* qh;  // Q6_K: the code bytes Q (8 B)
     const uint8_t* sc;  // Q6_K: the two subscales
     const uint8_t* d;   // fp16 scale (Q4_0: the block's; Q6_K: the superblock's)
 };
@@ -394,52 +394,67 @@ __device__ __forceinline__ int q4_0_dot(const uint32_t (&w)[8], const uint4 lo, 
     return s;
 }
 
-// Q6_K: the 8 words of 6-bit codes of one packed 32-value block, value order
-// 4i .. 4i+3 in word i.
-__device__ __forceinline__ void q6_k_unpack(const uint4 ql, const uint2 qh, uint32_t (&w)[8])
+// Q6_K: the 8 words of one packed 32-value block (the pack's per-row,
+// per-block 24 code bytes: P[16], byte t = q_t | high2(q_{16+t}) << 6, and
+// Q[8], byte u = low4(q_{16+u}) | low4(q_{24+u}) << 4).  Words 0..3 hold the
+// codes q_0 .. q_15 (values 4i .. 4i+3 in word i); words 4..7 hold 4 q_16 ..
+// 4 q_31, each code times four, which puts its low four bits next to its high
+// two without a shift of P.  The factor four is taken out of the second
+// half's dot product by the caller (q6_k_dot_init).
+__device__ __forceinline__ void q6_k_unpack(const uint4 P, const uint2 Q, uint32_t (&w)[8])
 {
-    const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x30303030u;
-    w[0] = (ql.x & m4) | ((qh.x << 4) & m2);
-    w[1] = (ql.y & m4) | ((qh.y << 4) & m2);
-    w[2] = (ql.z & m4) | ((qh.x << 2) & m2);
-    w[3] = (ql.w & m4) | ((qh.y << 2) & m2);
-    w[4] = ((ql.x >> 4) & m4) | (qh.x & m2);
-    w[5] = ((ql.y >> 4) & m4) | (qh.y & m2);
-    w[6] = ((ql.z >> 4) & m4) | ((qh.x >> 2) & m2);
-    w[7] = ((ql.w >> 4) & m4) | ((qh.y >> 2) & m2);
+    const uint32_t m6 = 0x3F3F3F3Fu, mh = 0xC0C0C0C0u, ml = 0x3C3C3C3Cu;
+    w[0] = P.x & m6;
+    w[1] = P.y & m6;
+    w[2] = P.z & m6;
+    w[3] = P.w & m6;
+    w[4] = (P.x & mh) | ((Q.x << 2) & ml);
+    w[5] = (P.y & mh) | ((Q.y << 2) & ml);
+    w[6] = (P.z & mh) | ((Q.x >> 2) & ml);
+    w[7] = (P.w & mh) | ((Q.y >> 2) & ml);
 }
 
-// J = sc0 * sum_{i<16} (q - 32) q_a + sc1 * sum_{i>=16} (q - 32) q_a, with the
-// offsets folded into the chain starts: g0 = -32 * sum(q_a[0..15]),
-// g1 = -32 * sum(q_a[16..31]); sc0, sc1 = the block's two int8 subscales.
+// d = dot of the four unsigned bytes of a with the four signed bytes of b, plus c.
+__device__ __forceinline__ int dp4a_u8s8(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // The two 16-value half-block dp4a chains of a Q6_K block, continued from
-// the starts g0 and g1.
+// the starts g0 and g1: g0 += sum_{i<16} q_i q_a[i], g1 += sum_{i>=16} 4 q_i q_a[i].
 __device__ __forceinline__ void q6_k_half_dots(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, int& g0, int& g1)
 {
     g0 = __dp4a((int)w[0], (int)lo.x, g0);
     g0 = __dp4a((int)w[1], (int)lo.y, g0);
     g0 = __dp4a((int)w[2], (int)lo.z, g0);
     g0 = __dp4a((int)w[3], (int)lo.w, g0);
-    g1 = __dp4a((int)w[4], (int)hi.x, g1);
-    g1 = __dp4a((int)w[5], (int)hi.y, g1);
-    g1 = __dp4a((int)w[6], (int)hi.z, g1);
-    g1 = __dp4a((int)w[7], (int)hi.w, g1);
+    g1 = dp4a_u8s8(w[4], hi.x, g1);
+    g1 = dp4a_u8s8(w[5], hi.y, g1);
+    g1 = dp4a_u8s8(w[6], hi.z, g1);
+    g1 = dp4a_u8s8(w[7], hi.w, g1);
 }
 
+// 4 J, J = sc0 * sum_{i<16} (q_i - 32) q_a[i] + sc1 * sum_{i>=16} (q_i - 32) q_a[i]
+// exactly (|4 J| < 2^27), with the offsets folded into the chain starts:
+// g0 = -32 * sum(q_a[0..15]), g1 = -128 * sum(q_a[16..31]) (the second half's
+// codes come four times over); sc0x4 = 4 * sc0, sc1 = the block's two int8
+// subscales.
 __device__ __forceinline__ int q6_k_dot_init(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, int g0, int g1,
-                                             int sc0, int sc1)
+                                             int sc0x4, int sc1)
 {
     q6_k_half_dots(w, lo, hi, g0, g1);
-    return sc0 * g0 + sc1 * g1;
+    return sc0x4 * g0 + sc1 * g1;
 }
 
-// Same, from the packed activation sums (sum(q_a[0..15]) | sum(q_a[16..31])
-// << 16, int16 pair) and the two subscale bytes sc2.
+// The same 4 J, from the packed activation sums (sum(q_a[0..15]) |
+// sum(q_a[16..31]) << 16, int16 pair) and the two subscale bytes sc2.
 __device__ __forceinline__ int q6_k_dot(const uint32_t (&w)[8], const uint4 lo, const uint4 hi, uint32_t sums,
                                         uint32_t sc2)
 {
-    return q6_k_dot_init(w, lo, hi, -32 * (int)(int16_t)(sums & 0xFFFFu), -32 * (int)(int16_t)(sums >> 16),
-                         (int)(int8_t)(sc2 & 0xFFu), (int)(int8_t)((sc2 >> 8) & 0xFFu));
+    return q6_k_dot_init(w, lo, hi, -32 * (int)(int16_t)(sums & 0xFFFFu), -128 * (int)(int16_t)(sums >> 16),
+                         4 * (int)(int8_t)(sc2 & 0xFFu), (int)(int8_t)((sc2 >> 8) & 0xFFu));
 }
 
 // Packed fp32 pairs (sm_100 and later): (ax, ay) = (bx, by) * (cx, cy) + (ax, ay),

@@ -152,19 +152,15 @@ def _q6_k_codes(w: np.ndarray) -> np.ndarray:
 
 def pack_q6_k(w: np.ndarray) -> np.ndarray:
     """Canonical Q6_K -> the documented layout: groups of 4 rows; per
-    (group, 32-block chunk) each row's tile = ql (byte t = low4(q_t) |
-    low4(q_t+16) << 4), qh (byte t, bits 2s = high2(q_t+8s)), sc (the block's
-    two subscales); then the chunk's fp16 scales d[rows][blocks / 8], zero
-    padded to 16 bytes."""
+    (group, 32-block chunk) each row's tile = P (16 bytes, byte t = q_t |
+    high2(q_16+t) << 6), Q (8 bytes, byte u = low4(q_16+u) | low4(q_24+u) <<
+    4), sc (the block's two subscales); then the chunk's fp16 scales
+    d[rows][blocks / 8], zero padded to 16 bytes."""
     N, ns, _ = w.shape
     nb = ns * 8
     q = _q6_k_codes(w).reshape(N, nb, 32)
-    ql = ((q[:, :, 0:16] & 0x0F) | ((q[:, :, 16:32] & 0x0F) << 4)).astype(np.uint8)
-    hi = q >> 4
-    qh = np.zeros((N, nb, 8), dtype=np.int64)
-    for s in range(4):
-        qh |= hi[:, :, 8 * s: 8 * s + 8] << (2 * s)
-    qh = qh.astype(np.uint8)
+    ql = (q[:, :, 0:16] | ((q[:, :, 16:32] >> 4) << 6)).astype(np.uint8)
+    qh = ((q[:, :, 16:24] & 0x0F) | ((q[:, :, 24:32] & 0x0F) << 4)).astype(np.uint8)
     sc = w[:, :, 192:208].reshape(N, nb, 2)
     d = w[:, :, 208:210]  # [N, ns, 2]
     out = []
@@ -198,10 +194,9 @@ def unpack_q6_k(pack: np.ndarray, N: int, K: int) -> np.ndarray:
             off += _pad16(dn)
     assert off == pack.size
     q = np.zeros((N, nb, 32), dtype=np.int64)
-    q[:, :, 0:16] = ql & 0x0F
-    q[:, :, 16:32] = ql >> 4
-    for s in range(4):
-        q[:, :, 8 * s: 8 * s + 8] |= ((qh >> (2 * s)) & 3) << 4
+    q[:, :, 0:16] = ql & 0x3F
+    q[:, :, 16:24] = (qh & 0x0F) | ((ql[:, :, 0:8] >> 6) << 4)
+    q[:, :, 24:32] = (qh >> 4) | ((ql[:, :, 8:16] >> 6) << 4)
     return q6_k_from_codes(q.reshape(N, K), sc.reshape(N, K // 16).view(np.int8),
                            d.copy().view(np.uint16).reshape(N, ns))
 
