@@ -145,9 +145,11 @@ int rmsnorm_quantize_q8_1(const float* x, int64_t ldx, const float* gamma, float
 int qpack_q4_0(const void* w_canon, void* w_pack, int N, int K, void* stream);
 
 /* qpack_q6_k - reorder canonical Q6_K superblocks into the kernel's tiles:
- * per (row, 32-block chunk) the low nibbles (16 B per block), the high bit
- * pairs (8 B per block) and the subscales (2 B per block), all rows' tiles
- * back to back, then the fp16 superblock scales (raw bits); same size.
+ * per (row, 32-block chunk) 16 code bytes per block (the first 16 values'
+ * six-bit codes, with the high two bits of the other 16 on top), 8 more per
+ * block (the low four bits of those 16) and the subscales (2 B per block),
+ * all rows' tiles back to back, then the fp16 superblock scales (raw bits);
+ * same size.
  * [record] "Why this was slow" (the Q6_K output tensor is packed once).
  *   w_canon  uint8 [N][K/256][210] device (read)
  *   w_pack   q6_k_pack_bytes(N, K) device (written; must not alias w_canon)
