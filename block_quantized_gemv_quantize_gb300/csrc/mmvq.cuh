@@ -251,16 +251,17 @@ __device__ __forceinline__ void accumulate_q4_0(const uint4 (&w16)[R], const flo
     }
 }
 
-// Q6_K: ql/qh/sc of the block for row r, dw[r] = its superblock scale.
+// Q6_K: the code bytes P and Q, the subscales of the block for row r, dw[r] =
+// its superblock scale.
 template <int M, int R>
-__device__ __forceinline__ void accumulate_q6_k(const uint4 (&ql)[R], const uint2 (&qh)[R], const uint32_t (&sc)[R],
+__device__ __forceinline__ void accumulate_q6_k(const uint4 (&cp)[R], const uint2 (&cq)[R], const uint32_t (&sc)[R],
                                                 const float (&dw)[R], const ActTile& t, int ti, float (&acc)[R][M])
 {
     uint32_t w[R][8];
     float dq[R];  // the superblock scale over four (q6_k_dot returns 4 J)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        q6_k_unpack(ql[r], qh[r], w[r]);
+        q6_k_unpack(cp[r], cq[r], w[r]);
         dq[r] = dw[r] * 0.25f;
     }
 #pragma unroll
@@ -285,9 +286,10 @@ __device__ __forceinline__ void accumulate_q6_k(const uint4 (&ql)[R], const uint
 // no conflict).  Block b's per-row words lie at meta + (b * MROWS + m) * META
 // with MROWS = M rounded up to odd, for the same reason:
 //   Q4_0 (8 B):  fp32 bits of the fp16 scale d_a;  -8 * sum(q) + 0x4B400000
-//   Q6_K (16 B): fp32 bits of d_a; -32 * sum(q[0..15]); -32 * sum(q[16..31]); 0
+//   Q6_K (16 B): fp32 bits of d_a; -32 * sum(q[0..15]); -128 * sum(q[16..31]); 0
 // The integer words start the dp4a chains, folding the weight offsets
-// (q_w - 8, q_w - 32) in exactly; the Q4_0 one also carries the bias of the
+// (q_w - 8, q_w - 32) in exactly (the Q6_K second half's codes come four
+// times over, q6_k_unpack); the Q4_0 one also carries the bias of the
 // int -> float conversion below.
 // ---------------------------------------------------------------------------
 
@@ -808,8 +810,8 @@ struct HalfLoads<FMT_Q4_0> {
 
 template <>
 struct HalfLoads<FMT_Q6_K> {
-    uint4 ql[R_ROWS];
-    uint2 qh[R_ROWS];
+    uint4 cp[R_ROWS];
+    uint2 cq[R_ROWS];
     uint32_t sc[R_ROWS];
     float dw[R_ROWS];
     __device__ __forceinline__ void whole(const uint8_t* st, int lane)
@@ -817,8 +819,8 @@ struct HalfLoads<FMT_Q6_K> {
         constexpr int TB = CHUNK * 26;
 #pragma unroll
         for (int q = 0; q < R_ROWS; ++q) {
-            ql[q] = *reinterpret_cast<const uint4*>(st + q * TB + lane * 16);
-            qh[q] = *reinterpret_cast<const uint2*>(st + q * TB + CHUNK * 16 + lane * 8);
+            cp[q] = *reinterpret_cast<const uint4*>(st + q * TB + lane * 16);
+            cq[q] = *reinterpret_cast<const uint2*>(st + q * TB + CHUNK * 16 + lane * 8);
             sc[q] = *reinterpret_cast<const uint16_t*>(st + q * TB + CHUNK * 24 + lane * 2);
             dw[q] = __half2float(__ushort_as_half(
                 *reinterpret_cast<const uint16_t*>(st + R_ROWS * TB + (q * (CHUNK / 8) + (lane >> 3)) * 2)));
@@ -830,8 +832,8 @@ struct HalfLoads<FMT_Q6_K> {
         const uint16_t* dq = reinterpret_cast<const uint16_t*>(st + rows * tb);
 #pragma unroll
         for (int q = 0; q < R_ROWS; ++q) {
-            ql[q] = *reinterpret_cast<const uint4*>(st + q * tb + lane * 16);
-            qh[q] = *reinterpret_cast<const uint2*>(st + q * tb + nb * 16 + lane * 8);
+            cp[q] = *reinterpret_cast<const uint4*>(st + q * tb + lane * 16);
+            cq[q] = *reinterpret_cast<const uint2*>(st + q * tb + nb * 16 + lane * 8);
             sc[q] = *reinterpret_cast<const uint16_t*>(st + q * tb + nb * 24 + lane * 2);
             dw[q] = __half2float(__ushort_as_half(dq[min(q, rows - 1) * (nb >> 3) + (lane >> 3)]));
         }
@@ -869,7 +871,7 @@ __device__ __forceinline__ void ring_dot4(const HalfLoads<FMT_Q6_K>& H, const ui
     float dq[R_ROWS];  // the superblock scale over four (q6_k_dot_init returns 4 J)
 #pragma unroll
     for (int q = 0; q < R_ROWS; ++q) {
-        q6_k_unpack(H.ql[q], H.qh[q], w[q]);
+        q6_k_unpack(H.cp[q], H.cq[q], w[q]);
         sc0x4[q] = 4 * (int)(int8_t)(H.sc[q] & 0xFFu);
         sc1[q] = (int)(int8_t)((H.sc[q] >> 8) & 0xFFu);
         dq[q] = H.dw[q] * 0.25f;
@@ -1373,8 +1375,8 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1)
                     }
                     accumulate_q4_0<M, R>(w16, dw, t, ti, acc);
                 } else {
-                    uint4 ql[R];
-                    uint2 qh[R];
+                    uint4 cp[R];
+                    uint2 cq[R];
                     uint32_t sc[R];
                     float dw[R];
 #pragma unroll
@@ -1383,18 +1385,18 @@ __global__ void __launch_bounds__(MmvqThreads<FMT, M, TOP1>::value, 1)
                         if (!QG_OK(pack_range_ok(a, FMT, ad.q, 16) && pack_range_ok(a, FMT, ad.qh, 8) &&
                                        pack_range_ok(a, FMT, ad.sc, 2) && pack_range_ok(a, FMT, ad.d, 2),
                                    status, 702)) {
-                            ql[r] = make_uint4(0u, 0u, 0u, 0u);
-                            qh[r] = make_uint2(0u, 0u);
+                            cp[r] = make_uint4(0u, 0u, 0u, 0u);
+                            cq[r] = make_uint2(0u, 0u);
                             sc[r] = 0u;
                             dw[r] = 0.0f;
                             continue;
                         }
-                        ql[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.q));
-                        qh[r] = ld_stream_v2(reinterpret_cast<const uint2*>(ad.qh));
+                        cp[r] = ld_stream_v4(reinterpret_cast<const uint4*>(ad.q));
+                        cq[r] = ld_stream_v2(reinterpret_cast<const uint2*>(ad.qh));
                         sc[r] = ld_stream_u16(ad.sc);
                         dw[r] = __half2float(__ushort_as_half(ld_stream_u16(ad.d)));
                     }
-                    accumulate_q6_k<M, R>(ql, qh, sc, dw, t, ti, acc);
+                    accumulate_q6_k<M, R>(cp, cq, sc, dw, t, ti, acc);
                 }
             }
         }
